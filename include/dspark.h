@@ -1,0 +1,187 @@
+/*
+ * dspark.h -- C ABI of the DSpark draft + verify step on one GB300 (sm_103a).
+ *
+ * Sources cited below (page title, then section):
+ *   [P2] "DSpark：半自回归生成与置信度调度的投机解码" (pinghaoyang.com.cn/aigc/posts/dspark/)
+ *   [P3] "拒绝盲猜与算力空转：深度拆解 DeepSeek 开源投机采样方案 DeepSpec & DSpark"
+ *        (val213.github.io/2026/06/28/DSpark&DSpec/)
+ *   [P4] "DeepSeek-AI与北京大学联手破局：AI聊天机器人"慢速打字"的终极解决方案"
+ *        (techwalker.com/2026/0716/3193540.shtml)
+ *
+ * Conventions for every call:
+ *   - Tensor pointers are CUDA device pointers owned by the caller, row-major and
+ *     contiguous, with the shapes given in brackets.  Nothing here allocates
+ *     device memory; calls that need scratch take a workspace (ws, ws_bytes)
+ *     sized by dspark_workspace_bytes() and cleared once by
+ *     dspark_workspace_init().  A workspace must not be shared by calls that
+ *     may run concurrently.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and return after enqueueing work.  Host-side argument
+ *     errors return DSPARK_ERR_INVALID / DSPARK_ERR_UNSUPPORTED before any
+ *     work is enqueued; a launch failure returns DSPARK_ERR_CUDA.
+ *   - Device-side checks (token ids out of range, verify lengths out of
+ *     [0, gamma]) never trap: the offending element is skipped, a bit is set
+ *     in the workspace status word, and dspark_sync_status() reports it.
+ *   - Results depend only on the inputs, seed, step and request ids: the
+ *     random numbers are Philox4x32-10 (Salmon et al., SC'11) with
+ *       key = (seed mod 2^32, seed div 2^32),
+ *       counter = (col div 4, req*(gamma+1) + row, step mod 2^32,
+ *                  domain + 4*(step div 2^32)), word = col mod 4,
+ *     u = (2*(x div 2^9) + 1) * 2^-24, Gumbel G = -log(-log u).
+ *     Domains: 0 draft, 1 acceptance uniform, 2 residual, 3 bonus.
+ *     req = req_base + b.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID = -1,      /* bad argument (null pointer, size, alignment) */
+    DSPARK_ERR_CUDA = -2,         /* a CUDA runtime call or launch failed */
+    DSPARK_ERR_TIMEOUT = -3,      /* a bounded device wait expired */
+    DSPARK_ERR_UNSUPPORTED = -4,  /* valid but not implemented (dtype / shape combination) */
+    DSPARK_ERR_DEVICE = -5        /* a device-side range check fired (see dspark_sync_status) */
+} dspark_status;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+typedef enum {
+    DSPARK_SCHED_OFF = 0,    /* every request verifies its whole block: K_b = gamma */
+    DSPARK_SCHED_SYNC = 1,   /* greedy admission with early stop [P4 §四] */
+    DSPARK_SCHED_ASYNC = 2   /* capacity from survivals two steps old, no early stop [P4 §五] */
+} dspark_sched_mode;
+
+/* Limits of this build. */
+#define DSPARK_MAX_GAMMA 16
+#define DSPARK_MAX_SCHED_ITEMS 4096   /* B * gamma for dspark_schedule */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int dspark_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* dspark_status_string(dspark_status s);
+
+/* Workspace bytes for a step of B requests, block length gamma, vocabulary V,
+ * Markov rank r.  Returns 0 if the sizes are out of range. */
+size_t dspark_workspace_bytes(int B, int gamma, int V, int r);
+
+/* Zero a workspace (its status word and the arrival counters the kernels
+ * use).  Call once after allocating it; the kernels leave it reusable. */
+dspark_status dspark_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the workspace status word.
+ * Returns DSPARK_OK, DSPARK_ERR_DEVICE (range check fired), DSPARK_ERR_TIMEOUT,
+ * or DSPARK_ERR_CUDA (the stream reported an error).  If bits is non-NULL the
+ * raw status bits are stored there. */
+dspark_status dspark_sync_status(void* ws, void* stream, uint32_t* bits);
+
+/*
+ * Steps a1-a3: the Markov-head draft loop [P2 §整体架构, §Markov Head：一阶转移偏置],
+ * [P3 §DSpark 的解法：半自回归架构与低秩马尔可夫头].  For k = 1..gamma, request b:
+ *     h      = W1[x~_{k-1}]                      (x~_0 = anchor[b])
+ *     z_k    = (U[b,k-1,:] + h . W2) / tau        (draft logits over V)
+ *     lse_q  = log sum_v exp(z_k[v])
+ *     x~_k   = argmax_v z_k[v] + G(domain 0, row k-1, col v)   (lowest v on ties)
+ * Inputs : U [B,gamma,V] (U_t), W1 [V,r], W2 [r,V] (W_t), anchor [B] in [0,V).
+ *          bf16 weights run the W2 contraction on the tensor cores (fp32
+ *          accumulation); fp32 weights run it on CUDA cores.
+ * Outputs: draft_tok [B,gamma] int32, lse_q [B,gamma], z_tok [B,gamma] = z_k[x~_k].
+ *          logits_out, if non-NULL, receives z [B,gamma,V] fp32 (parity checks;
+ *          pass NULL on the hot path).
+ * Limits : 1 <= gamma <= DSPARK_MAX_GAMMA, V % 8 == 0, 1 <= r <= 1024,
+ *          B*(gamma+1) + req_base < 2^32, tau > 0.
+ */
+dspark_status dspark_draft_markov(
+    const void* U, dspark_dtype U_t,
+    const void* W1, const void* W2, dspark_dtype W_t,
+    const int32_t* anchor,
+    int B, int gamma, int V, int r, int req_base, float tau,
+    uint64_t seed, uint64_t step,
+    int32_t* draft_tok, float* lse_q, float* z_tok, float* logits_out,
+    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Step a4: confidence head, sequential temperature scaling and prefix survival
+ * [P2 §置信度头：预测自己的命运, §校准问题：原始置信度不可靠], [P4 §四].
+ *     s_k        = w_c . [h[b,k-1,:] ; emb[x~_{k-1},:]] + b_c
+ *     conf_cal   = sigmoid(s_k / T[k-1])            (= sigmoid(logit(c_k)/T_k))
+ *     log_surv   = sum_{i<=k} log conf_cal_i         (log of the survival a_{b,k})
+ * Inputs : h [B,gamma,d] fp32, emb [V,e] (emb_t), anchor [B], draft_tok [B,gamma],
+ *          w_c [d+e] fp32, T [gamma] fp32 (> 0).  e = d follows the workload
+ *          definition (an embedding table); passing W1 with e = r follows
+ *          [P2], which reuses the Markov head's W1 rows.
+ * Outputs: conf_cal [B,gamma], log_surv [B,gamma] (non-increasing in k).
+ */
+dspark_status dspark_confidence_sts(
+    const float* h, int d,
+    const void* emb, dspark_dtype emb_t, int e,
+    const int32_t* anchor, const int32_t* draft_tok,
+    const float* w_c, float b_c, const float* T,
+    int B, int gamma, int V,
+    float* conf_cal, float* log_surv,
+    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Step a5: hardware-aware greedy prefix scheduler [P2 §硬件感知前缀调度器],
+ * [P4 §四, §五].  Candidates (b, j) sorted by survival descending (ties: b,
+ * then j); R = B;  Theta(n) = (R + sum of the first n survivals) * sps[R+n-1].
+ *   SYNC : admit in order while Theta strictly rises; stop at the first non-rise.
+ *   ASYNC: n* = first argmax_n Theta_hist(n) over the list of log_surv_hist
+ *          (survivals two steps old; NULL = use log_surv), then admit the n*
+ *          best current candidates.
+ *   OFF  : K_b = gamma.
+ * Inputs : log_surv [B,gamma] fp32 (non-increasing in j), log_surv_hist or
+ *          NULL, sps [sps_len] fp32 with sps_len >= B + B*gamma.
+ * Outputs: K [B] verify lengths, n_total [1] admitted drafts, theta [1] =
+ *          Theta at the admitted count (fp32).
+ * Limits : B*gamma <= DSPARK_MAX_SCHED_ITEMS.
+ */
+dspark_status dspark_schedule(
+    const float* log_surv, const float* log_surv_hist,
+    const float* sps, int sps_len, int B, int gamma, dspark_sched_mode mode,
+    int32_t* K, int32_t* n_total, float* theta,
+    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Steps a6-a8: lossless verification and ragged compaction
+ * [P2 §形式化定义], [P4 §四, §五].  For request b, with p_i = softmax(target[b,i,:]/tau):
+ *   walk k = 1..K_b: accept x~_k iff u(domain 1, row k-1) < min(1, p_k(x~_k)/q_k(x~_k)),
+ *     q_k(x~_k) = exp(z_tok - lse_q);
+ *   first rejection j: emit argmax_v log(max(0, p_j - q_j)[v]) + G(domain 2, row j-1, v)
+ *     (q_j recomputed over V from U, W1, W2; if p_j <= q_j everywhere, from p_j);
+ *   all K_b accepted: emit the bonus argmax_v target[b,K_b,v]/tau + G(domain 3, row K_b, v).
+ * Output layout: out_off = exclusive scan of (A_b + 1) over b ([B+1]);
+ *   out_tok/out_req/out_pos [B*(gamma+1)] hold the accepted drafts then the
+ *   final token of each request at out_off[b]..out_off[b+1]-1; next_anchor [B]
+ *   is the last emitted token; accepted [B] = A_b.
+ * Inputs : target [B,gamma+1,V] (target_t), U, W1, W2 as for the draft, anchor,
+ *          draft_tok, lse_q, z_tok from dspark_draft_markov, K [B] in [0,gamma].
+ * Optional: p_tok [B,gamma] receives p_k(x~_k) for walked rows (others untouched);
+ *          near_ties [4] (zeroed by the caller) counts: [0] acceptance
+ *          uniforms within 1e-5 of their threshold, [1] residual draws that
+ *          fell back to p, [2] final draws, [3] reserved.
+ */
+dspark_status dspark_verify(
+    const void* target, dspark_dtype target_t,
+    const void* U, dspark_dtype U_t,
+    const void* W1, const void* W2, dspark_dtype W_t,
+    const int32_t* anchor, const int32_t* draft_tok,
+    const float* lse_q, const float* z_tok, const int32_t* K,
+    int B, int gamma, int V, int r, int req_base, float tau,
+    uint64_t seed, uint64_t step,
+    int32_t* accepted, int32_t* out_tok, int32_t* out_req, int32_t* out_pos,
+    int32_t* out_off, int32_t* next_anchor,
+    float* p_tok, uint32_t* near_ties,
+    void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_H */

@@ -1,0 +1,76 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/dspark.h declares, sizes its workspace, and rejects
+bad arguments before touching the device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from verify_markov_head_gb300 import build as b
+    return C.CDLL(b.build())
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(dspark_[a-z_0-9]+)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"dspark_draft_markov", "dspark_confidence_sts", "dspark_schedule", "dspark_verify"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    lib.dspark_status_string.restype = C.c_char_p
+    assert lib.dspark_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.dspark_status_string(code)
+
+
+def test_workspace_sizes(lib):
+    lib.dspark_workspace_bytes.restype = C.c_size_t
+    assert lib.dspark_workspace_bytes(64, 7, 151936, 256) > 0
+    assert lib.dspark_workspace_bytes(4, 7, 1024, 32) > 0
+    assert lib.dspark_workspace_bytes(0, 7, 1024, 32) == 0        # B < 1
+    assert lib.dspark_workspace_bytes(4, 17, 1024, 32) == 0       # gamma above the limit
+    assert lib.dspark_workspace_bytes(4, 7, 1020, 32) == 0        # V not a multiple of 8
+
+
+def test_null_pointers_are_rejected_without_a_device(lib):
+    vp = C.c_void_p
+    lib.dspark_draft_markov.argtypes = [vp, C.c_int, vp, vp, C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_int,
+                                        C.c_int, C.c_float, C.c_uint64, C.c_uint64, vp, vp, vp, vp, vp,
+                                        C.c_size_t, vp]
+    st = lib.dspark_draft_markov(None, 0, None, None, 0, None, 4, 7, 1024, 32, 0, 1.0, 0, 0,
+                                 None, None, None, None, None, 0, None)
+    assert st == -1
+    st = lib.dspark_draft_markov(None, 0, None, None, 0, None, 4, 7, 1024, 32, 0, -1.0, 0, 0,
+                                 None, None, None, None, None, 0, None)
+    assert st == -1
+    lib.dspark_schedule.argtypes = [vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, vp, vp,
+                                    C.c_size_t, vp]
+    assert lib.dspark_schedule(None, None, None, 32, 4, 7, 1, None, None, None, None, 0, None) == -1
+    assert lib.dspark_schedule(None, None, None, 32, 1000, 7, 1, None, None, None, None, 0, None) == -1
+    assert lib.dspark_schedule(None, None, None, 32, 4, 7, 9, None, None, None, None, 0, None) == -1
+
+
+def test_package_imports_and_fails_loudly_without_library(tmp_path):
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r); import verify_markov_head_gb300 as vm; "
+            "print(vm.dspark_version())" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert r.returncode == 0 and int(r.stdout.strip()) >= 100

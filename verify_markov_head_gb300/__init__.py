@@ -1,0 +1,245 @@
+"""Python binding of libdspark (the C ABI in include/dspark.h).
+
+Argument marshalling only: every function below checks tensor shapes, passes
+``data_ptr()`` values and sizes to the C function of the same name, and
+raises ``DsparkError`` on a non-OK status.  All arithmetic runs in the CUDA
+kernels of the library.  PyTorch provides device memory and streams.
+
+The library must be built (``verify_markov_head_gb300.build.build()``);
+importing this package without it raises ImportError: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
+    "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
+    "dspark_schedule", "dspark_verify", "Workspace", "StepBuffers", "run_step", "run_step_host",
+    "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
+]
+
+SCHED_OFF, SCHED_SYNC, SCHED_ASYNC = 0, 1, 2
+_F32, _BF16 = 0, 1
+
+lib_path = _build.LIB
+if not os.path.exists(lib_path):
+    raise ImportError(f"libdspark.so is not built ({lib_path}); run verify_markov_head_gb300.build.build()")
+_lib = C.CDLL(lib_path)
+
+_vp, _i, _f, _u64, _sz = C.c_void_p, C.c_int, C.c_float, C.c_uint64, C.c_size_t
+_lib.dspark_version.restype = _i
+_lib.dspark_status_string.argtypes = [_i]
+_lib.dspark_status_string.restype = C.c_char_p
+_lib.dspark_workspace_bytes.argtypes = [_i, _i, _i, _i]
+_lib.dspark_workspace_bytes.restype = _sz
+_lib.dspark_workspace_init.argtypes = [_vp, _sz, _vp]
+_lib.dspark_workspace_init.restype = _i
+_lib.dspark_sync_status.argtypes = [_vp, _vp, C.POINTER(C.c_uint32)]
+_lib.dspark_sync_status.restype = _i
+_lib.dspark_draft_markov.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
+                                     _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_draft_markov.restype = _i
+_lib.dspark_confidence_sts.argtypes = [_vp, _i, _vp, _i, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i,
+                                       _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_confidence_sts.restype = _i
+_lib.dspark_schedule.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_schedule.restype = _i
+_lib.dspark_verify.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
+                               _i, _i, _i, _i, _i, _f, _u64, _u64,
+                               _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_verify.restype = _i
+
+
+class DsparkError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {dspark_status_string(status)} ({status})")
+
+
+def _check(fn, st):
+    if st != 0:
+        raise DsparkError(fn, st)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return _F32
+    if t.dtype == torch.bfloat16:
+        return _BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def dspark_version() -> int:
+    return int(_lib.dspark_version())
+
+
+def dspark_status_string(status: int) -> str:
+    return _lib.dspark_status_string(int(status)).decode()
+
+
+def dspark_workspace_bytes(B, gamma, V, r) -> int:
+    return int(_lib.dspark_workspace_bytes(B, gamma, V, r))
+
+
+def dspark_workspace_init(ws: torch.Tensor, stream=None):
+    _check("dspark_workspace_init", _lib.dspark_workspace_init(_p(ws), ws.numel(), _stream(stream)))
+
+
+def dspark_sync_status(ws: torch.Tensor, stream=None):
+    """Synchronise the stream; return (status, bits) of the workspace status word."""
+    bits = C.c_uint32(0)
+    st = _lib.dspark_sync_status(_p(ws), _stream(stream), C.byref(bits))
+    return int(st), int(bits.value)
+
+
+class Workspace:
+    """Device scratch for a step of (B, gamma, V, r), cleared once."""
+
+    def __init__(self, B, gamma, V, r, device="cuda", stream=None):
+        n = dspark_workspace_bytes(B, gamma, V, r)
+        if n == 0:
+            raise ValueError("sizes out of range")
+        self.tensor = torch.empty(n + 256, dtype=torch.uint8, device=device)
+        off = (-self.tensor.data_ptr()) % 256
+        self.buf = self.tensor[off:off + n]
+        dspark_workspace_init(self.buf, stream)
+
+    def ptr(self):
+        return self.buf.data_ptr()
+
+    def nbytes(self):
+        return self.buf.numel()
+
+
+def dspark_draft_markov(U, W1, W2, anchor, draft_tok, lse_q, z_tok, ws: Workspace, *,
+                        tau=1.0, seed=0, step=0, req_base=0, logits_out=None, stream=None):
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if W1.shape != (V, r) or W2.shape != (r, V) or W1.dtype != W2.dtype:
+        raise ValueError("W1 [V,r] and W2 [r,V] must share a dtype")
+    for t, shp in ((anchor, (B,)), (draft_tok, (B, gamma)), (lse_q, (B, gamma)), (z_tok, (B, gamma))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"shape {tuple(t.shape)} != {shp}")
+    _check("dspark_draft_markov", _lib.dspark_draft_markov(
+        _p(U), _dt(U), _p(W1), _p(W2), _dt(W1), _p(anchor), B, gamma, V, r, req_base, float(tau),
+        int(seed), int(step), _p(draft_tok), _p(lse_q), _p(z_tok), _p(logits_out),
+        ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def dspark_confidence_sts(h, emb, anchor, draft_tok, w_c, b_c, T, conf_cal, log_surv, ws: Workspace,
+                          *, stream=None):
+    B, gamma, d = h.shape
+    V, e = emb.shape
+    if w_c.numel() != d + e or T.numel() != gamma:
+        raise ValueError("w_c must hold d+e weights and T gamma temperatures")
+    _check("dspark_confidence_sts", _lib.dspark_confidence_sts(
+        _p(h), d, _p(emb), _dt(emb), e, _p(anchor), _p(draft_tok), _p(w_c), float(b_c), _p(T),
+        B, gamma, V, _p(conf_cal), _p(log_surv), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def dspark_schedule(log_surv, sps, mode, K, n_total, theta, ws: Workspace, *, log_surv_hist=None,
+                    stream=None):
+    B, gamma = log_surv.shape
+    _check("dspark_schedule", _lib.dspark_schedule(
+        _p(log_surv), _p(log_surv_hist), _p(sps), sps.numel(), B, gamma, int(mode), _p(K), _p(n_total),
+        _p(theta), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def dspark_verify(target, U, W1, W2, anchor, draft_tok, lse_q, z_tok, K, accepted, out_tok, out_req,
+                  out_pos, out_off, next_anchor, ws: Workspace, *, tau=1.0, seed=0, step=0, req_base=0,
+                  p_tok=None, near_ties=None, stream=None):
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if tuple(target.shape) != (B, gamma + 1, V):
+        raise ValueError("target must be [B, gamma+1, V]")
+    if out_tok.numel() < B * (gamma + 1) or out_off.numel() != B + 1:
+        raise ValueError("output buffers too small")
+    _check("dspark_verify", _lib.dspark_verify(
+        _p(target), _dt(target), _p(U), _dt(U), _p(W1), _p(W2), _dt(W1), _p(anchor), _p(draft_tok),
+        _p(lse_q), _p(z_tok), _p(K), B, gamma, V, r, req_base, float(tau), int(seed), int(step),
+        _p(accepted), _p(out_tok), _p(out_req), _p(out_pos), _p(out_off), _p(next_anchor),
+        _p(p_tok), _p(near_ties), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+class StepBuffers:
+    """Device outputs of one step for B requests of block length gamma."""
+
+    def __init__(self, B, gamma, V, r, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.B, self.gamma = B, gamma
+        self.draft_tok = torch.empty((B, gamma), **i32)
+        self.lse_q = torch.empty((B, gamma), **f32)
+        self.z_tok = torch.empty((B, gamma), **f32)
+        self.conf_cal = torch.empty((B, gamma), **f32)
+        self.log_surv = torch.empty((B, gamma), **f32)
+        self.K = torch.empty((B,), **i32)
+        self.n_total = torch.empty((1,), **i32)
+        self.theta = torch.empty((1,), **f32)
+        self.accepted = torch.empty((B,), **i32)
+        self.out_tok = torch.empty((B * (gamma + 1),), **i32)
+        self.out_req = torch.empty((B * (gamma + 1),), **i32)
+        self.out_pos = torch.empty((B * (gamma + 1),), **i32)
+        self.out_off = torch.empty((B + 1,), **i32)
+        self.next_anchor = torch.empty((B,), **i32)
+        self.p_tok = torch.empty((B, gamma), **f32)
+        self.near_ties = torch.zeros((4,), dtype=torch.int32, device=device)
+        self.ws = Workspace(B, gamma, V, r, device)
+
+
+def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_base=0, log_surv_hist=None,
+         stream=None, p_tok=False):
+    """One whole draft + verify step (a1-a8) on device-resident inputs: the
+    four ABI calls in order, all on `stream`."""
+    dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
+                        buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, stream=stream)
+    dspark_confidence_sts(inp["h"], inp["emb"], inp["anchor"], buf.draft_tok, inp["w_c"], inp["b_c"], inp["T"],
+                          buf.conf_cal, buf.log_surv, buf.ws, stream=stream)
+    dspark_schedule(buf.log_surv, inp["sps"], mode, buf.K, buf.n_total, buf.theta, buf.ws,
+                    log_surv_hist=log_surv_hist, stream=stream)
+    dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
+                  buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
+                  buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
+                  p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
+
+
+_PER_STEP = ("U", "target", "h", "anchor")
+
+
+def run_step_host(host_inp: dict, dev_inp: dict, buf: StepBuffers, host_out: dict, *, mode, seed, step=0,
+              tau=1.0, stream=None):
+    """End-to-end step from host memory: copies the step's activations
+    (U, target logits, hidden states, anchors) from pinned host tensors into
+    the device inputs, runs the step, and copies the emitted tokens, offsets
+    and next anchors back.  Returns (h2d_bytes, d2h_bytes)."""
+    h2d = 0
+    for k in _PER_STEP:
+        dev_inp[k].copy_(host_inp[k], non_blocking=True)
+        h2d += host_inp[k].numel() * host_inp[k].element_size()
+    run_step(dev_inp, buf, mode=mode, seed=seed, step=step, tau=tau, stream=stream)
+    d2h = 0
+    for name in ("out_tok", "out_off", "next_anchor"):
+        src = getattr(buf, name)
+        host_out[name].copy_(src, non_blocking=True)
+        d2h += src.numel() * src.element_size()
+    return h2d, d2h

@@ -1,0 +1,245 @@
+// api.cu -- the C ABI declared in include/dspark.h: host-side argument
+// checks, workspace layout and the launch sequence of each call.
+#include <cuda_runtime.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(int B, int gamma, int V) {
+    WsLayout L;
+    L.nseg = (V + kVerifySeg - 1) / kVerifySeg;
+    const int ntiles = (V + kPartTile - 1) / kPartTile;
+    L.parts = ntiles < kMaxParts ? ntiles : kMaxParts;
+    size_t o = 0;
+    const size_t nchunks = ((size_t)B + kChunk - 1) / kChunk;
+    L.status = o;      o = align256(o + 16);
+    L.tickets = o;     o = align256(o + sizeof(uint32_t) * 2 * nchunks);
+    L.draft_part = o;  o = align256(o + sizeof(DrawLse) * (size_t)B * L.parts);
+    L.verify_part = o; o = align256(o + sizeof(LseDraw) * (size_t)B * (gamma + 1) * L.nseg);
+    L.rej = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
+    L.acc = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
+    L.fin = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
+    L.lse_rej = o;     o = align256(o + sizeof(float2) * (size_t)B);
+    L.resid_part = o;  o = align256(o + sizeof(Draw2) * (size_t)B * L.parts);
+    L.total = o;
+    return L;
+}
+
+WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
+    const WsLayout L = ws_layout(B, gamma, V);
+    char* base = static_cast<char*>(ws);
+    WsPtrs P;
+    P.status = reinterpret_cast<uint32_t*>(base + L.status);
+    P.tickets_draft = reinterpret_cast<uint32_t*>(base + L.tickets);
+    P.tickets_resid = P.tickets_draft + ((size_t)B + kChunk - 1) / kChunk;
+    P.draft_part = reinterpret_cast<DrawLse*>(base + L.draft_part);
+    P.verify_part = reinterpret_cast<LseDraw*>(base + L.verify_part);
+    P.rej = reinterpret_cast<int32_t*>(base + L.rej);
+    P.acc = reinterpret_cast<int32_t*>(base + L.acc);
+    P.fin = reinterpret_cast<int32_t*>(base + L.fin);
+    P.lse_rej = reinterpret_cast<float2*>(base + L.lse_rej);
+    P.resid_part = reinterpret_cast<Draw2*>(base + L.resid_part);
+    P.nseg = L.nseg;
+    P.parts = L.parts;
+    return P;
+}
+
+// A pointer the device can dereference: device memory or managed memory.
+static bool is_device_ptr(const void* p) {
+    if (!p) return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) { cudaGetLastError(); return false; }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static dspark_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return DSPARK_OK;
+    fprintf(stderr, "dspark: launch failed: %s\n", cudaGetErrorString(e));
+    return DSPARK_ERR_CUDA;
+}
+
+static bool sizes_ok(int B, int gamma, int V, int r) {
+    if (B < 1 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 8 || (V % 8) != 0 || r < 1 || r > 1024)
+        return false;
+    if ((double)B * (gamma + 1) >= 4294967295.0) return false;
+    if (B > 1000000) return false;
+    return true;
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" {
+
+int dspark_version(void) { return 100; }
+
+const char* dspark_status_string(dspark_status s) {
+    switch (s) {
+        case DSPARK_OK: return "ok";
+        case DSPARK_ERR_INVALID: return "invalid argument";
+        case DSPARK_ERR_CUDA: return "CUDA error";
+        case DSPARK_ERR_TIMEOUT: return "device wait timed out";
+        case DSPARK_ERR_UNSUPPORTED: return "unsupported configuration";
+        case DSPARK_ERR_DEVICE: return "device-side range check fired";
+    }
+    return "unknown status";
+}
+
+size_t dspark_workspace_bytes(int B, int gamma, int V, int r) {
+    if (!sizes_ok(B, gamma, V, r)) return 0;
+    return ws_layout(B, gamma, V).total;
+}
+
+dspark_status dspark_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!is_device_ptr(ws) || ws_bytes < 256) return DSPARK_ERR_INVALID;
+    return launch_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+dspark_status dspark_sync_status(void* ws, void* stream, uint32_t* bits) {
+    if (!is_device_ptr(ws)) return DSPARK_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "dspark: %s\n", cudaGetErrorString(e));
+        return DSPARK_ERR_CUDA;
+    }
+    if (host) {
+        e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    if (bits) *bits = host;
+    if (host & kTimeout) return DSPARK_ERR_TIMEOUT;
+    if (host) return DSPARK_ERR_DEVICE;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_draft_markov(const void* U, dspark_dtype U_t, const void* W1, const void* W2,
+                                  dspark_dtype W_t, const int32_t* anchor, int B, int gamma, int V,
+                                  int r, int req_base, float tau, uint64_t seed, uint64_t step,
+                                  int32_t* draft_tok, float* lse_q, float* z_tok, float* logits_out,
+                                  void* ws, size_t ws_bytes, void* stream) {
+    if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
+    if ((U_t != DSPARK_F32 && U_t != DSPARK_BF16) || (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
+        return DSPARK_ERR_UNSUPPORTED;
+    if (!is_device_ptr(U) || !is_device_ptr(W1) || !is_device_ptr(W2) || !is_device_ptr(anchor) ||
+        !is_device_ptr(draft_tok) || !is_device_ptr(lse_q) || !is_device_ptr(z_tok) || !is_device_ptr(ws))
+        return DSPARK_ERR_INVALID;
+    if (logits_out && !is_device_ptr(logits_out)) return DSPARK_ERR_INVALID;
+    if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(ws, 256)) return DSPARK_ERR_INVALID;
+    if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;
+    if ((double)(req_base + (double)B) * (gamma + 1) >= 4294967295.0) return DSPARK_ERR_INVALID;
+
+    DraftParams p;
+    p.U = U; p.U_bf16 = (U_t == DSPARK_BF16);
+    p.W1 = W1; p.W2 = W2; p.W_bf16 = (W_t == DSPARK_BF16);
+    p.anchor = anchor;
+    p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.req_base = req_base;
+    p.inv_tau = 1.f / tau;
+    p.seed = seed; p.step = step;
+    p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.logits_out = logits_out;
+    p.ws = ws_ptrs(ws, B, gamma, V);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool tc = draft_tc_supported(p);
+    for (int k = 1; k <= gamma; ++k) {
+        const cudaError_t e = tc ? launch_draft_tc(p, k, s) : launch_draft_simt(p, k, s);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return DSPARK_OK;
+}
+
+dspark_status dspark_confidence_sts(const float* h, int d, const void* emb, dspark_dtype emb_t, int e,
+                                    const int32_t* anchor, const int32_t* draft_tok, const float* w_c,
+                                    float b_c, const float* T, int B, int gamma, int V, float* conf_cal,
+                                    float* log_surv, void* ws, size_t ws_bytes, void* stream) {
+    if (B < 1 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || d < 1 || e < 1 || V < 1) return DSPARK_ERR_INVALID;
+    if (emb_t != DSPARK_F32 && emb_t != DSPARK_BF16) return DSPARK_ERR_UNSUPPORTED;
+    if (!is_device_ptr(h) || !is_device_ptr(emb) || !is_device_ptr(anchor) || !is_device_ptr(draft_tok) ||
+        !is_device_ptr(w_c) || !is_device_ptr(T) || !is_device_ptr(conf_cal) || !is_device_ptr(log_surv) ||
+        !is_device_ptr(ws))
+        return DSPARK_ERR_INVALID;
+    if (!aligned(h, 16) || !aligned(emb, 16) || !aligned(w_c, 16) || ws_bytes < 256) return DSPARK_ERR_INVALID;
+    ConfParams p;
+    p.h = h; p.d = d; p.emb = emb; p.emb_bf16 = (emb_t == DSPARK_BF16); p.e = e;
+    p.anchor = anchor; p.draft_tok = draft_tok; p.w_c = w_c; p.b_c = b_c; p.T = T;
+    p.B = B; p.gamma = gamma; p.V = V; p.conf_cal = conf_cal; p.log_surv = log_surv;
+    p.status = static_cast<uint32_t*>(ws);
+    return launch_status(launch_confidence(p, static_cast<cudaStream_t>(stream)));
+}
+
+dspark_status dspark_schedule(const float* log_surv, const float* log_surv_hist, const float* sps,
+                              int sps_len, int B, int gamma, dspark_sched_mode mode, int32_t* K,
+                              int32_t* n_total, float* theta, void* ws, size_t ws_bytes, void* stream) {
+    (void)ws; (void)ws_bytes;
+    if (B < 1 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || B * gamma > DSPARK_MAX_SCHED_ITEMS)
+        return DSPARK_ERR_INVALID;
+    if (mode != DSPARK_SCHED_OFF && mode != DSPARK_SCHED_SYNC && mode != DSPARK_SCHED_ASYNC)
+        return DSPARK_ERR_INVALID;
+    if (sps_len < B + B * gamma) return DSPARK_ERR_INVALID;
+    if (!is_device_ptr(log_surv) || !is_device_ptr(sps) || !is_device_ptr(K) || !is_device_ptr(n_total) ||
+        !is_device_ptr(theta))
+        return DSPARK_ERR_INVALID;
+    if (log_surv_hist && !is_device_ptr(log_surv_hist)) return DSPARK_ERR_INVALID;
+    SchedParams p;
+    p.log_surv = log_surv; p.log_surv_hist = log_surv_hist; p.sps = sps; p.sps_len = sps_len;
+    p.B = B; p.gamma = gamma; p.mode = (int)mode; p.K = K; p.n_total = n_total; p.theta = theta;
+    return launch_status(launch_schedule(p, static_cast<cudaStream_t>(stream)));
+}
+
+dspark_status dspark_verify(const void* target, dspark_dtype target_t, const void* U, dspark_dtype U_t,
+                            const void* W1, const void* W2, dspark_dtype W_t, const int32_t* anchor,
+                            const int32_t* draft_tok, const float* lse_q, const float* z_tok,
+                            const int32_t* K, int B, int gamma, int V, int r, int req_base, float tau,
+                            uint64_t seed, uint64_t step, int32_t* accepted, int32_t* out_tok,
+                            int32_t* out_req, int32_t* out_pos, int32_t* out_off, int32_t* next_anchor,
+                            float* p_tok, uint32_t* near_ties, void* ws, size_t ws_bytes, void* stream) {
+    if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
+    if ((target_t != DSPARK_F32 && target_t != DSPARK_BF16) || (U_t != DSPARK_F32 && U_t != DSPARK_BF16) ||
+        (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
+        return DSPARK_ERR_UNSUPPORTED;
+    const void* need[] = {target, U, W1, W2, anchor, draft_tok, lse_q, z_tok, K, accepted,
+                          out_tok, out_req, out_pos, out_off, next_anchor, ws};
+    for (const void* q : need)
+        if (!is_device_ptr(q)) return DSPARK_ERR_INVALID;
+    if ((p_tok && !is_device_ptr(p_tok)) || (near_ties && !is_device_ptr(near_ties))) return DSPARK_ERR_INVALID;
+    if (!aligned(target, 16) || !aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(ws, 256))
+        return DSPARK_ERR_INVALID;
+    if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;
+    if ((double)(req_base + (double)B) * (gamma + 1) >= 4294967295.0) return DSPARK_ERR_INVALID;
+    VerifyParams p;
+    p.target = target; p.target_bf16 = (target_t == DSPARK_BF16);
+    p.U = U; p.U_bf16 = (U_t == DSPARK_BF16);
+    p.W1 = W1; p.W2 = W2; p.W_bf16 = (W_t == DSPARK_BF16);
+    p.anchor = anchor; p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.K = K;
+    p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.req_base = req_base;
+    p.inv_tau = 1.f / tau; p.seed = seed; p.step = step;
+    p.accepted = accepted; p.out_tok = out_tok; p.out_req = out_req; p.out_pos = out_pos;
+    p.out_off = out_off; p.next_anchor = next_anchor; p.p_tok = p_tok; p.near_ties = near_ties;
+    p.ws = ws_ptrs(ws, B, gamma, V);
+    return launch_status(launch_verify(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,195 @@
+// common.cuh -- device helpers shared by the DSpark kernels: the counter-based
+// generator, the Gumbel transform, the mergeable sampling / log-sum-exp state,
+// and the workspace layout.
+//
+// Random numbers follow the stream definition stated in include/dspark.h:
+// Philox4x32-10 as specified by Salmon, Moraes, Dror and Shaw ("Parallel
+// Random Numbers: As Easy as 1, 2, 3", SC'11, section 3), written here from
+// that specification.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------- Philox4x32-10
+struct Philox {
+    static constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;   // round multipliers
+    static constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;   // key increments
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        if (i) { k0 += Philox::kW0; k1 += Philox::kW1; }
+        const uint32_t hi0 = __umulhi(Philox::kM0, c.x), lo0 = Philox::kM0 * c.x;
+        const uint32_t hi1 = __umulhi(Philox::kM1, c.z), lo1 = Philox::kM1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// The four words for columns 4*quad .. 4*quad+3 of one (row, domain) stream.
+struct Stream {
+    uint32_t k0, k1, row, step_lo, dom_hi;
+    __device__ __forceinline__ Stream(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row_)
+        : k0((uint32_t)seed), k1((uint32_t)(seed >> 32)), row(row_), step_lo((uint32_t)step),
+          dom_hi(domain + 4u * (uint32_t)(step >> 32)) {}
+    __device__ __forceinline__ uint4 quad(uint32_t q) const {
+        return philox4x32_10(make_uint4(q, row, step_lo, dom_hi), k0, k1);
+    }
+    __device__ __forceinline__ uint32_t word(uint32_t col) const {
+        const uint4 w = quad(col >> 2);
+        const uint32_t s = col & 3u;
+        return s == 0 ? w.x : s == 1 ? w.y : s == 2 ? w.z : w.w;
+    }
+};
+
+// u = (2*(x >> 9) + 1) * 2^-24: exact in binary32, strictly inside (0, 1).
+__device__ __forceinline__ float uniform_of(uint32_t x) {
+    return (float)(2u * (x >> 9) + 1u) * 5.9604644775390625e-8f;
+}
+
+// Standard Gumbel variate -log(-log u), with CUDA's full-accuracy logf (the
+// inner log near u = 1 keeps its relative accuracy, which the outer log needs).
+__device__ __forceinline__ float gumbel_of(uint32_t x) {
+    return -logf(-logf(uniform_of(x)));
+}
+
+// ---------------------------------------------------------------- merge states
+// Gumbel-max draw fused with a log-sum-exp: over a set of entries,
+//   best  = max (z_v + G_v), idx = its v (lowest v on ties), zb = z_idx,
+//   s     = sum exp(z_v - best).
+// best is a safe log-sum-exp reference: G lies in [-2.82, 16.64] for the
+// uniforms above, so z_v - best <= 2.82 and exp never overflows.
+struct DrawLse {
+    float best;
+    int idx;
+    float zb;
+    float s;
+};
+
+__device__ __forceinline__ DrawLse drawlse_empty() { return DrawLse{-INFINITY, 0x7fffffff, 0.f, 0.f}; }
+
+__device__ __forceinline__ bool wins(float sa, int ia, float sb, int ib) {
+    return sa > sb || (sa == sb && ia < ib);
+}
+
+__device__ __forceinline__ DrawLse drawlse_merge(const DrawLse& a, const DrawLse& b) {
+    if (b.best == -INFINITY) return a;
+    if (a.best == -INFINITY) return b;
+    DrawLse o;
+    if (wins(b.best, b.idx, a.best, a.idx)) {
+        o.best = b.best; o.idx = b.idx; o.zb = b.zb;
+        o.s = b.s + a.s * __expf(a.best - b.best);
+    } else {
+        o.best = a.best; o.idx = a.idx; o.zb = a.zb;
+        o.s = a.s + b.s * __expf(b.best - a.best);
+    }
+    return o;
+}
+
+__device__ __forceinline__ DrawLse shfl_xor(const DrawLse& a, int m) {
+    DrawLse o;
+    o.best = __shfl_xor_sync(0xffffffffu, a.best, m);
+    o.idx = __shfl_xor_sync(0xffffffffu, a.idx, m);
+    o.zb = __shfl_xor_sync(0xffffffffu, a.zb, m);
+    o.s = __shfl_xor_sync(0xffffffffu, a.s, m);
+    return o;
+}
+
+// Online log-sum-exp (running max reference) plus an optional Gumbel-max draw.
+struct LseDraw {
+    float m;     // running max of x
+    float s;     // sum exp(x - m)
+    float best;  // max (x + G) or -inf when no draw is taken
+    int idx;
+};
+
+__device__ __forceinline__ LseDraw lsedraw_empty() { return LseDraw{-INFINITY, 0.f, -INFINITY, 0x7fffffff}; }
+
+__device__ __forceinline__ LseDraw lsedraw_merge(const LseDraw& a, const LseDraw& b) {
+    LseDraw o;
+    if (b.m == -INFINITY) { o.m = a.m; o.s = a.s; }
+    else if (a.m == -INFINITY) { o.m = b.m; o.s = b.s; }
+    else if (a.m >= b.m) { o.m = a.m; o.s = a.s + b.s * __expf(b.m - a.m); }
+    else { o.m = b.m; o.s = b.s + a.s * __expf(a.m - b.m); }
+    if (wins(b.best, b.idx, a.best, a.idx)) { o.best = b.best; o.idx = b.idx; }
+    else { o.best = a.best; o.idx = a.idx; }
+    return o;
+}
+
+__device__ __forceinline__ LseDraw shfl_xor(const LseDraw& a, int m) {
+    LseDraw o;
+    o.m = __shfl_xor_sync(0xffffffffu, a.m, m);
+    o.s = __shfl_xor_sync(0xffffffffu, a.s, m);
+    o.best = __shfl_xor_sync(0xffffffffu, a.best, m);
+    o.idx = __shfl_xor_sync(0xffffffffu, a.idx, m);
+    return o;
+}
+
+// Two Gumbel-max draws over the same set (residual law and its fallback p).
+struct Draw2 {
+    float best_r; int idx_r;   // argmax log(max(0, p - q)) + G   (only where p > q)
+    float best_p; int idx_p;   // argmax x_p + G                  (fallback law p)
+};
+
+__device__ __forceinline__ Draw2 draw2_empty() { return Draw2{-INFINITY, 0x7fffffff, -INFINITY, 0x7fffffff}; }
+
+__device__ __forceinline__ Draw2 draw2_merge(const Draw2& a, const Draw2& b) {
+    Draw2 o;
+    if (wins(b.best_r, b.idx_r, a.best_r, a.idx_r)) { o.best_r = b.best_r; o.idx_r = b.idx_r; }
+    else { o.best_r = a.best_r; o.idx_r = a.idx_r; }
+    if (wins(b.best_p, b.idx_p, a.best_p, a.idx_p)) { o.best_p = b.best_p; o.idx_p = b.idx_p; }
+    else { o.best_p = a.best_p; o.idx_p = a.idx_p; }
+    return o;
+}
+
+__device__ __forceinline__ Draw2 shfl_xor(const Draw2& a, int m) {
+    Draw2 o;
+    o.best_r = __shfl_xor_sync(0xffffffffu, a.best_r, m);
+    o.idx_r = __shfl_xor_sync(0xffffffffu, a.idx_r, m);
+    o.best_p = __shfl_xor_sync(0xffffffffu, a.best_p, m);
+    o.idx_p = __shfl_xor_sync(0xffffffffu, a.idx_p, m);
+    return o;
+}
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(uint16_t x) { return __uint_as_float(((uint32_t)x) << 16); }
+
+template <typename T> struct Vec4;
+template <> struct Vec4<float> {
+    __device__ __forceinline__ static float4 load(const float* p) { return *reinterpret_cast<const float4*>(p); }
+    __device__ __forceinline__ static float4 load_stream(const float* p) {
+        return __ldcs(reinterpret_cast<const float4*>(p));
+    }
+};
+template <> struct Vec4<uint16_t> {
+    __device__ __forceinline__ static float4 cvt(uint2 v) {
+        return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    }
+    __device__ __forceinline__ static float4 load(const uint16_t* p) {
+        return cvt(*reinterpret_cast<const uint2*>(p));
+    }
+    __device__ __forceinline__ static float4 load_stream(const uint16_t* p) {
+        return cvt(__ldcs(reinterpret_cast<const uint2*>(p)));
+    }
+};
+
+// ---------------------------------------------------------------- status word
+enum StatusBits : uint32_t {
+    kBadToken = 1u << 0,     // a token id outside [0, V)
+    kBadLength = 1u << 1,    // a verify length outside [0, gamma]
+    kTimeout = 1u << 2,      // a bounded wait expired
+};
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+}  // namespace dspark

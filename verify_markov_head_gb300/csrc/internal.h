@@ -1,0 +1,99 @@
+// internal.h -- parameter blocks, workspace layout and launcher declarations
+// shared between the ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+struct DrawLse;
+struct LseDraw;
+struct Draw2;
+
+constexpr int kMaxParts = 1024;        // cap on partial states per request per launch
+constexpr int kPartTile = 128;         // vocabulary entries per tile of the partial-producing kernels
+constexpr int kVerifySeg = 4096;       // vocabulary entries per verify-stream CTA
+constexpr int kChunk = 16;             // requests per chunk of the partial-producing kernels
+
+// Byte offsets of the workspace regions (all 256-byte aligned).
+struct WsLayout {
+    size_t status, tickets, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, total;
+    int nseg;    // verify-stream segments per row
+    int parts;   // partial-state slots per request (>= CTAs along V of any launch)
+};
+WsLayout ws_layout(int B, int gamma, int V);
+
+struct WsPtrs {
+    uint32_t* status;
+    uint32_t* tickets_draft;   // [ceil(B/kChunk)] arrival counters, zero between launches
+    uint32_t* tickets_resid;   // [ceil(B/kChunk)]
+    DrawLse* draft_part;
+    LseDraw* verify_part;
+    int32_t* rej;        // [B] 0-based rejected row, -1 if every walked draft was accepted
+    int32_t* acc;        // [B] accepted count
+    int32_t* fin;        // [B] final token
+    float2* lse_rej;     // [B] (lse_p, lse_q) of the rejected row
+    Draw2* resid_part;   // [B][parts]
+    int nseg;
+    int parts;
+};
+WsPtrs ws_ptrs(void* ws, int B, int gamma, int V);
+
+struct DraftParams {
+    const void* U; int U_bf16;
+    const void* W1; const void* W2; int W_bf16;
+    const int32_t* anchor;
+    int B, gamma, V, r, req_base;
+    float inv_tau;
+    uint64_t seed, step;
+    int32_t* draft_tok; float* lse_q; float* z_tok; float* logits_out;
+    WsPtrs ws;
+};
+
+struct ConfParams {
+    const float* h; int d;
+    const void* emb; int emb_bf16; int e;
+    const int32_t* anchor; const int32_t* draft_tok;
+    const float* w_c; float b_c; const float* T;
+    int B, gamma, V;
+    float* conf_cal; float* log_surv;
+    uint32_t* status;
+};
+
+struct SchedParams {
+    const float* log_surv; const float* log_surv_hist;
+    const float* sps; int sps_len;
+    int B, gamma, mode;
+    int32_t* K; int32_t* n_total; float* theta;
+};
+
+struct VerifyParams {
+    const void* target; int target_bf16;
+    const void* U; int U_bf16;
+    const void* W1; const void* W2; int W_bf16;
+    const int32_t* anchor; const int32_t* draft_tok;
+    const float* lse_q; const float* z_tok; const int32_t* K;
+    int B, gamma, V, r, req_base;
+    float inv_tau;
+    uint64_t seed, step;
+    int32_t* accepted; int32_t* out_tok; int32_t* out_req; int32_t* out_pos;
+    int32_t* out_off; int32_t* next_anchor;
+    float* p_tok; uint32_t* near_ties;
+    WsPtrs ws;
+};
+
+int num_sms();
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_draft_simt(const DraftParams& p, int k, cudaStream_t s);
+bool draft_tc_supported(const DraftParams& p);
+cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s);
+cudaError_t launch_confidence(const ConfParams& p, cudaStream_t s);
+cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+
+}  // namespace dspark

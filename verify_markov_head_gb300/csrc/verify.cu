@@ -1,0 +1,365 @@
+// verify.cu -- lossless verification and ragged compaction
+// ("DSpark：半自回归生成与置信度调度的投机解码" section 形式化定义;
+//  "DeepSeek-AI与北京大学联手破局" sections 四 and 五).
+//
+// Four launches, all stream-ordered and free of waits:
+//   verify_stream   rows i = 0..K_b of the target logits, split in 4096-entry
+//                   segments: online log-sum-exp of t/tau and, on the bonus
+//                   row i = K_b, a Gumbel-max draw (domain 3).  128-bit
+//                   streaming loads (evict-first), warp-shuffle reductions.
+//   verify_accept   one warp per request: merges the segment partials into
+//                   lse_p per row, walks k = 1..K_b with the acceptance
+//                   uniforms (domain 1), records the first rejection.
+//   verify_residual rejected requests only: recomputes the draft logits of
+//                   the rejected row (bias h . W2 plus U), forms
+//                   max(0, p - q) and draws from it by Gumbel-max (domain 2),
+//                   with the draw from p kept as the fallback.
+//   verify_compact  one CTA: exclusive scan of A_b + 1, scatter of the
+//                   accepted drafts and the final token of every request.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kStreamThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float load_scalar(const T* p, size_t i) { return to_f32(p[i]); }
+
+template <typename TT>
+__global__ void __launch_bounds__(kStreamThreads)
+verify_stream_kernel(const VerifyParams p) {
+    const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
+    const int seg = blockIdx.x % nseg;
+    const int i = (blockIdx.x / nseg) % (gamma + 1);
+    const int b = blockIdx.x / (nseg * (gamma + 1));
+    int Kb = p.K[b];
+    if (Kb < 0 || Kb > gamma) {
+        if (seg == 0 && i == 0 && threadIdx.x == 0) raise_status(p.ws.status, kBadLength);
+        Kb = Kb < 0 ? 0 : gamma;
+    }
+    if (i > Kb) return;
+    const bool bonus = (i == Kb);
+    const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
+    const int v_beg = seg * kVerifySeg;
+    const int v_end = min(V, v_beg + kVerifySeg);
+    const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
+
+    LseDraw st = lsedraw_empty();
+    for (int v = v_beg + 4 * threadIdx.x; v < v_end; v += 4 * kStreamThreads) {
+        const float4 x4 = Vec4<TT>::load_stream(row + v);
+        const float xs[4] = {x4.x * p.inv_tau, x4.y * p.inv_tau, x4.z * p.inv_tau, x4.w * p.inv_tau};
+        const float mx = fmaxf(fmaxf(xs[0], xs[1]), fmaxf(xs[2], xs[3]));
+        if (mx > st.m) { st.s = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mx); st.m = mx; }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.s += __expf(xs[e] - st.m);
+        if (bonus) {
+            const uint4 w = rng.quad((uint32_t)v >> 2);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float sc = xs[e] + gumbel_of(ws[e]);
+                if (wins(sc, v + e, st.best, st.idx)) { st.best = sc; st.idx = v + e; }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
+    __shared__ LseDraw s_part[kStreamThreads / 32];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (lane == 0) s_part[warp] = st;
+    __syncthreads();
+    if (warp == 0) {
+        st = lane < kStreamThreads / 32 ? s_part[lane] : lsedraw_empty();
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
+        if (lane == 0) p.ws.verify_part[((size_t)b * (gamma + 1) + i) * p.ws.nseg + seg] = st;
+    }
+}
+
+template <typename TT>
+__global__ void __launch_bounds__(32)
+verify_accept_kernel(const VerifyParams p) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
+    int Kb = p.K[b];
+    Kb = Kb < 0 ? 0 : (Kb > gamma ? gamma : Kb);
+    __shared__ float s_lse[DSPARK_MAX_GAMMA + 1];
+    int bonus_idx = 0;
+    for (int i = 0; i <= Kb; ++i) {
+        const LseDraw* part = p.ws.verify_part + ((size_t)b * (gamma + 1) + i) * nseg;
+        LseDraw a = lsedraw_empty();
+        for (int s = lane; s < nseg; s += 32) a = lsedraw_merge(a, part[s]);
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
+        if (lane == 0) s_lse[i] = a.m + logf(a.s);
+        if (i == Kb) bonus_idx = a.idx;
+    }
+    __syncwarp();
+    if (lane != 0) return;
+    const TT* target = static_cast<const TT*>(p.target);
+    const uint32_t row0 = (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1);
+    int A = Kb, rej = -1;
+    for (int k = 1; k <= Kb; ++k) {
+        const size_t o = (size_t)b * gamma + (k - 1);
+        int x = p.draft_tok[o];
+        if (x < 0 || x >= V) { raise_status(p.ws.status, kBadToken); x = 0; }
+        const float t = load_scalar(target, ((size_t)b * (gamma + 1) + (k - 1)) * V + x) * p.inv_tau;
+        const float lp = t - s_lse[k - 1];
+        const float lq = p.z_tok[o] - p.lse_q[o];
+        if (p.p_tok) p.p_tok[o] = expf(lp);
+        const float thr = fminf(1.f, expf(lp - lq));
+        const float u = uniform_of(Stream(p.seed, p.step, 1u, row0 + (uint32_t)(k - 1)).word(0));
+        if (p.near_ties && fabsf(u - thr) < 1e-5f) atomicAdd(&p.near_ties[0], 1u);
+        if (!(u < thr)) { A = k - 1; rej = k - 1; break; }
+    }
+    p.ws.acc[b] = A;
+    p.ws.rej[b] = rej;
+    p.ws.fin[b] = bonus_idx;
+    if (rej >= 0) {
+        const size_t o = (size_t)b * gamma + rej;
+        p.ws.lse_rej[b] = make_float2(s_lse[rej], p.lse_q[o]);
+    }
+    p.accepted[b] = A;
+}
+
+// ----------------------------------------------------------------- residual
+constexpr int kTV = 128;
+constexpr int kBC = kChunk;
+constexpr int kResThreads = 256;
+
+template <typename WT, typename UT, typename TT>
+__global__ void __launch_bounds__(kResThreads)
+verify_residual_simt_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) float smem[];
+    const int r = p.r, V = p.V, gamma = p.gamma;
+    float* sh = smem;                         // [kBC][r]
+    float* tile = smem + kBC * r;             // [kBC][kTV + 4] draft logits z
+    constexpr int kLd = kTV + 4;
+    __shared__ int s_row[kBC];
+    __shared__ int s_any;
+
+    const int tid = threadIdx.x, chunk = blockIdx.y, b0 = chunk * kBC;
+    const int nb = min(kBC, p.B - b0);
+    if (tid == 0) s_any = 0;
+    __syncthreads();
+    if (tid < kBC) {
+        const int row = (tid < nb) ? __ldcg(&p.ws.rej[b0 + tid]) : -1;
+        s_row[tid] = row;
+        if (row >= 0) atomicOr(&s_any, 1);
+    }
+    __syncthreads();
+    const WT* W1 = static_cast<const WT*>(p.W1);
+    const WT* W2 = static_cast<const WT*>(p.W2);
+    const UT* U = static_cast<const UT*>(p.U);
+    const TT* target = static_cast<const TT*>(p.target);
+
+    const int warp = tid / 32, lane = tid % 32;
+    const int bl_e = tid / 16, seg = tid % 16;
+    Draw2 st = draw2_empty();
+    if (s_any) {
+        for (int i = tid; i < kBC * r; i += kResThreads) {
+            const int bl = i / r, rho = i - bl * r;
+            float v = 0.f;
+            const int row = s_row[bl];
+            if (row >= 0) {
+                const int b = b0 + bl;
+                int x = (row == 0) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + row - 1];
+                if (x >= 0 && x < V) v = to_f32(W1[(size_t)x * r + rho]);
+            }
+            sh[i] = v;
+        }
+        __syncthreads();
+        const int v_local = tid % kTV, bh = tid / kTV;
+        const int ntiles = (V + kTV - 1) / kTV;
+        const int my_row = (bl_e < nb) ? s_row[bl_e] : -1;
+        const float2 lse = (my_row >= 0) ? p.ws.lse_rej[b0 + bl_e] : make_float2(0.f, 0.f);
+        const Stream rng(p.seed, p.step, 2u,
+                         (uint32_t)(p.req_base + b0 + bl_e) * (uint32_t)(gamma + 1) + (uint32_t)(my_row < 0 ? 0 : my_row));
+        const TT* trow = target + ((size_t)(b0 + bl_e) * (gamma + 1) + (my_row < 0 ? 0 : my_row)) * V;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const int v0 = t * kTV;
+            const int v = v0 + v_local;
+            float acc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+            if (v < V) {
+                const float* hb = sh + (bh * 8) * r;
+                for (int rho = 0; rho < r; ++rho) {
+                    const float w = to_f32(W2[(size_t)rho * V + v]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = fmaf(hb[j * r + rho], w, acc[j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int bl = bh * 8 + j;
+                const int row = s_row[bl];
+                float z = 0.f;
+                if (row >= 0 && v < V)
+                    z = (to_f32(U[((size_t)(b0 + bl) * gamma + row) * V + v]) + acc[j]) * p.inv_tau;
+                tile[bl * kLd + v_local] = z;
+            }
+            __syncthreads();
+            if (my_row >= 0) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int vl = seg * 8 + q * 4;
+                    const int vq = v0 + vl;
+                    if (vq < V) {
+                        const uint4 w = rng.quad((uint32_t)vq >> 2);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                        const float4 t4 = Vec4<TT>::load(trow + vq);
+                        const float ts[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float z = tile[bl_e * kLd + vl + e];
+                            const float tv = ts[e] * p.inv_tau;
+                            const float g = gumbel_of(ws[e]);
+                            const float pr = expf(tv - lse.x) - expf(z - lse.y);
+                            const int idx = vq + e;
+                            if (pr > 0.f) {
+                                const float sc = logf(pr) + g;
+                                if (wins(sc, idx, st.best_r, st.idx_r)) { st.best_r = sc; st.idx_r = idx; }
+                            }
+                            const float sp = tv + g;
+                            if (wins(sp, idx, st.best_p, st.idx_p)) { st.best_p = sp; st.idx_p = idx; }
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int m = 1; m < 16; m <<= 1) st = draw2_merge(st, shfl_xor(st, m));
+        if (seg == 0 && my_row >= 0) p.ws.resid_part[(size_t)(b0 + bl_e) * p.ws.parts + blockIdx.x] = st;
+    }
+
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&p.ws.tickets_resid[chunk], 1u);
+        s_last = (prev == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int bl = warp; bl < nb; bl += kResThreads / 32) {
+        if (s_row[bl] < 0) continue;
+        const int b = b0 + bl;
+        const Draw2* part = p.ws.resid_part + (size_t)b * p.ws.parts;
+        Draw2 a = draw2_empty();
+        for (int i = lane; i < (int)gridDim.x; i += 32) {
+            Draw2 c;
+            c.best_r = __ldcg(&part[i].best_r); c.idx_r = __ldcg(&part[i].idx_r);
+            c.best_p = __ldcg(&part[i].best_p); c.idx_p = __ldcg(&part[i].idx_p);
+            a = draw2_merge(a, c);
+        }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) a = draw2_merge(a, shfl_xor(a, m));
+        if (lane == 0) {
+            if (a.best_r > -INFINITY) {
+                p.ws.fin[b] = a.idx_r;
+            } else {
+                p.ws.fin[b] = a.idx_p;
+                if (p.near_ties) atomicAdd(&p.near_ties[1], 1u);
+            }
+        }
+    }
+    if (tid == 0) p.ws.tickets_resid[chunk] = 0u;
+}
+
+// ----------------------------------------------------------------- compaction
+constexpr int kCompactThreads = 1024;
+
+__global__ void __launch_bounds__(kCompactThreads)
+verify_compact_kernel(const VerifyParams p) {
+    __shared__ int s_warp[kCompactThreads / 32];
+    __shared__ int s_carry;
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    const int gamma = p.gamma;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < p.B; base += kCompactThreads) {
+        const int b = base + tid;
+        const int A = (b < p.B) ? p.ws.acc[b] : 0;
+        const int len = (b < p.B) ? A + 1 : 0;
+        int incl = len;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, m);
+            if (lane >= m) incl += y;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = s_warp[lane];
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, m);
+                if (lane >= m) w += y;
+            }
+            s_warp[lane] = w;
+        }
+        __syncthreads();
+        const int off = s_carry + (warp ? s_warp[warp - 1] : 0) + incl - len;
+        if (b < p.B) {
+            const int fin = p.ws.fin[b];
+            for (int i = 0; i < A; ++i) {
+                p.out_tok[off + i] = p.draft_tok[(size_t)b * gamma + i];
+                p.out_req[off + i] = b;
+                p.out_pos[off + i] = i;
+            }
+            p.out_tok[off + A] = fin;
+            p.out_req[off + A] = b;
+            p.out_pos[off + A] = A;
+            p.out_off[b] = off;
+            p.next_anchor[b] = fin;
+        }
+        __syncthreads();
+        if (tid == 0) s_carry += s_warp[kCompactThreads / 32 - 1];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        p.out_off[p.B] = s_carry;
+        if (p.near_ties) atomicAdd(&p.near_ties[2], (unsigned)p.B);
+    }
+}
+
+template <typename TT>
+cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
+    const unsigned g1 = (unsigned)p.B * (unsigned)(p.gamma + 1) * (unsigned)p.ws.nseg;
+    verify_stream_kernel<TT><<<g1, kStreamThreads, 0, s>>>(p);
+    verify_accept_kernel<TT><<<p.B, 32, 0, s>>>(p);
+    const int nchunks = (p.B + kBC - 1) / kBC;
+    const int ntiles = (p.V + kTV - 1) / kTV;
+    int gx = (4 * num_sms()) / nchunks;
+    gx = gx < 1 ? 1 : (gx > ntiles ? ntiles : gx);
+    gx = gx > p.ws.parts ? p.ws.parts : gx;
+    const size_t smem = sizeof(float) * ((size_t)kBC * p.r + (size_t)kBC * (kTV + 4));
+    const dim3 g2(gx, nchunks);
+#define DSPARK_RES_LAUNCH(WT, UT)                                                                    \
+    do {                                                                                             \
+        auto kern = verify_residual_simt_kernel<WT, UT, TT>;                                         \
+        if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        kern<<<g2, kResThreads, smem, s>>>(p);                                                       \
+    } while (0)
+    if (p.W_bf16) {
+        if (p.U_bf16) DSPARK_RES_LAUNCH(uint16_t, uint16_t); else DSPARK_RES_LAUNCH(uint16_t, float);
+    } else {
+        if (p.U_bf16) DSPARK_RES_LAUNCH(float, uint16_t); else DSPARK_RES_LAUNCH(float, float);
+    }
+#undef DSPARK_RES_LAUNCH
+    verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
+    return p.target_bf16 ? launch_verify_t<uint16_t>(p, s) : launch_verify_t<float>(p, s);
+}
+
+}  // namespace dspark
