@@ -12,7 +12,11 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from verify_markov_head_gb300 import build as b
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "dspark_build", os.path.join(ROOT, "verify_markov_head_gb300", "build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
     return C.CDLL(b.build())
 
 

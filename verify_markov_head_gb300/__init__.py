@@ -5,8 +5,9 @@ Argument marshalling only: every function below checks tensor shapes, passes
 raises ``DsparkError`` on a non-OK status.  All arithmetic runs in the CUDA
 kernels of the library.  PyTorch provides device memory and streams.
 
-The library must be built (``verify_markov_head_gb300.build.build()``);
-importing this package without it raises ImportError: there is no fallback.
+The library must be built first (``python verify_markov_head_gb300/build.py``
+or ``__graft_entry__.build()``); importing this package without it raises
+ImportError: there is no fallback.
 """
 from __future__ import annotations
 
@@ -15,7 +16,6 @@ import os
 
 import torch
 
-from . import build as _build
 
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
@@ -27,9 +27,9 @@ __all__ = [
 SCHED_OFF, SCHED_SYNC, SCHED_ASYNC = 0, 1, 2
 _F32, _BF16 = 0, 1
 
-lib_path = _build.LIB
+lib_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libdspark.so")
 if not os.path.exists(lib_path):
-    raise ImportError(f"libdspark.so is not built ({lib_path}); run verify_markov_head_gb300.build.build()")
+    raise ImportError(f"libdspark.so is not built ({lib_path}); run verify_markov_head_gb300/build.py")
 _lib = C.CDLL(lib_path)
 
 _vp, _i, _f, _u64, _sz = C.c_void_p, C.c_int, C.c_float, C.c_uint64, C.c_size_t
