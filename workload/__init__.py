@@ -100,6 +100,8 @@ def custom(base: str = "tiny", **kw) -> Workload:
     d.update(kw)
     if "gamma" in kw and "boost" not in kw:
         d["boost"] = (w.boost + (w.boost[-1],) * kw["gamma"])[: kw["gamma"]]
+    if "sps_len" not in kw:       # the capacity table must cover R + B*gamma tokens
+        d["sps_len"] = max(w.sps_len, d["B"] * (d["gamma"] + 1))
     return Workload(**d)
 
 
