@@ -416,11 +416,9 @@ cudaError_t launch_nc(const DraftParams& p, int k, cudaStream_t s) {
     }
     const Layout L = tc_layout(NC, C::SC, p.r);
     const size_t smem = L.total + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(draft_tc_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        attr_set = true;
-    }
+    // the opt-in limit covers static + dynamic shared memory, so request exactly what this launch needs
+    cudaError_t e = cudaFuncSetAttribute(draft_tc_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     const int nchunks = (p.B + NC - 1) / NC;
     const int ntiles = (p.V + 127) / 128;
     int gx = num_sms() / nchunks;
