@@ -354,3 +354,15 @@ def test_host_pointers_are_rejected():
     with pytest.raises(vm.DsparkError):
         vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
                                buf.z_tok, buf.ws, seed=0)
+
+
+@pytest.mark.parametrize("vocab_lanes", [False, True])
+def test_draft_both_tensor_core_layouts(vocab_lanes, monkeypatch):
+    """Requests-on-lanes (B >= 32) and vocabulary-on-lanes tensor-core kernels
+    against the oracle on the same ragged case."""
+    if vocab_lanes:
+        monkeypatch.setenv("DSPARK_DRAFT_VOCAB_LANES", "1")
+    w = workload.custom("tiny", B=70, V=2056, r=256, w_dtype=torch.bfloat16, w_std=0.1, seed=5)
+    inp = workload.inputs(w, device=DEV)
+    compared, flagged = _check_draft(inp, w, seed=7, step=1)
+    assert flagged <= max(1, compared // 100)

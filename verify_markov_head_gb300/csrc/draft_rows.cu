@@ -1,0 +1,384 @@
+// draft_rows.cu -- Markov-head draft position on the tcgen05 tensor cores,
+// requests on the TMEM lanes (batches of 32 requests and more).
+//
+// Per position k ("DSpark：半自回归生成与置信度调度的投机解码" sections 整体架构 and
+// Markov Head; "拒绝盲猜与算力空转" section on the low-rank Markov head):
+//   bias[b, v] = W1[x~_{k-1}(b)] . W2[:, v]      (rank r, bf16 in, fp32 accumulate)
+//   z[b, v]    = (U[b, k-1, v] + bias[b, v]) / tau
+//   x~_k       = argmax_v z + G,  lse_q = log sum exp z,  z_tok = z[x~_k]
+//
+// D[M = 128 request rows, N = 128 vocabulary entries] = h[M, K = r] * W2tile[K, N]:
+//   A = the gathered rows h = W1[x~_{k-1}] (K-major, 128-byte swizzle, staged
+//       once per CTA; rows past the batch are zero),
+//   B = a 128-entry slice of W2 read by TMA straight from the [r, V] row-major
+//       tensor (MN-major, 128-byte swizzle), in 64-rank K-chunks,
+//   D = fp32 in TMEM, two buffers so the MMA of tile t+1 overlaps the
+//       epilogue of tile t.
+// With the request on the TMEM lane, every epilogue thread owns one request
+// row and reads 32 consecutive vocabulary entries of it in one tcgen05.ld; the
+// matching U slice arrives by TMA (128-byte swizzle, so the 32 lanes of a warp
+// read 32 rows without bank conflicts).  Each thread folds z + Gumbel into its
+// own running Gumbel-max + log-sum-exp state: no transposition, no per-tile
+// cross-thread reduction.
+//
+// CTA = 18 warps: warps 0-15 epilogue (warp w reads TMEM lane quarter w % 4
+// and the 32-column block w / 4 of each tile), warp 16 TMA producer, warp 17
+// TMEM owner and single-thread MMA issuer.  Every mbarrier wait is bounded;
+// on expiry the kernel raises the timeout bit, lets its copies land, frees
+// TMEM and returns.  Partial states go to the workspace and the last CTA of a
+// request chunk to arrive merges them (atomic ticket, no waiting).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = (kEpiWarps + 2) * 32;   // 576
+constexpr int kProducerWarp = 16, kMmaWarp = 17;
+constexpr int kTN = 128;                          // vocabulary entries per tile
+constexpr int kStages = 4;                        // W2 K-chunk ring
+constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile (bf16), 16 KB
+constexpr int kURingBytes = 64 * 1024;
+constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
+
+struct Layout {
+    uint32_t b, a, u, merge, bar, misc, total;
+    int uslots;
+};
+
+__host__ __device__ inline Layout rows_layout(int NC, int r) {
+    Layout L;
+    L.b = 0;
+    L.a = L.b + kStages * kBBytes;
+    L.u = L.a + (uint32_t)(r / 64) * 128u * 128u;            // 128 rows x 128 B per K-chunk
+    const int slot = NC * 128;                                // one [NC rows][32 fp32] U slice
+    L.uslots = kURingBytes / slot;
+    if (L.uslots > 16) L.uslots = 16;
+    L.merge = L.u + (uint32_t)(L.uslots * slot);
+    L.bar = L.merge + 4u * 128u * 16u;
+    L.misc = L.bar + 8u * (2 * kStages + 2 * L.uslots + 5);
+    L.misc = (L.misc + 15u) & ~15u;
+    L.total = L.misc + 16u + 4u * 128u;
+    return L;
+}
+
+struct RowsArgs {
+    CUtensorMap w2map;   // bf16 [r][V], box {64 vocab, 64 rank}, 128-byte swizzle
+    CUtensorMap umap;    // fp32 [B][gamma][V], box {32 vocab, 1, NC requests}, 128-byte swizzle
+    DraftParams p;
+    int NC;              // request rows per CTA (32, 64 or 128)
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+draft_rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
+    const DraftParams& p = a.p;
+    const int NC = a.NC;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const Layout L = rows_layout(NC, p.r);
+    const int KCH = p.r / 64;
+    const int US = L.uslots;
+    const uint32_t slot_bytes = (uint32_t)NC * 128u;
+
+    const uint32_t bar0 = base + L.bar;
+    auto full = [&](int i) { return bar0 + 8u * i; };
+    auto empty = [&](int i) { return bar0 + 8u * (kStages + i); };
+    auto ufull = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
+    auto uempty = [&](int i) { return bar0 + 8u * (2 * kStages + US + i); };
+    auto tfull = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + i); };
+    auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + 2 + i); };
+    const uint32_t drain = bar0 + 8u * (2 * kStages + 2 * US + 4);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L.misc);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 4);
+    volatile uint32_t* never = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 8);
+    int* s_tok = reinterpret_cast<int*>(gbase + L.misc + 16);
+    DrawLse* s_merge = reinterpret_cast<DrawLse*>(gbase + L.merge);   // [4 column blocks][128 rows]
+
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int chunk = blockIdx.y, b_base = chunk * NC;
+    const int nb = min(NC, p.B - b_base);
+    const int nq = (nb + 31) / 32;                 // TMEM lane quarters holding requests
+    const int V = p.V, gamma = p.gamma, r = p.r;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), 1); }
+        for (int i = 0; i < US; ++i) { ptx::mbar_init(ufull(i), 1); ptx::mbar_init(uempty(i), (uint32_t)nq); }
+        for (int i = 0; i < 2; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        *never = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (tid == kProducerWarp * 32) { ptx::prefetch_tmap(&a.w2map); ptx::prefetch_tmap(&a.umap); }
+    if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 256u); ptx::tmem_relinquish(); }
+    for (int n = tid; n < 128; n += kThreads) {
+        int x = -1;
+        if (n < nb) {
+            const int b = b_base + n;
+            x = (k == 1) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (k - 2)];
+            if (x < 0 || x >= V) { raise_status(p.ws.status, kBadToken); x = -1; }
+        }
+        s_tok[n] = x;
+    }
+    __syncthreads();
+    // A operand: h rows, K-major with 128-byte swizzle.  K-chunk j (64 ranks) is a
+    // [128 rows][128 B] block; 16-byte unit u of row n sits at unit u ^ (n mod 8).
+    {
+        const uint16_t* W1 = static_cast<const uint16_t*>(p.W1);
+        const int units = r / 8;
+        for (int idx = tid; idx < 128 * units; idx += kThreads) {
+            const int n = idx / units, u16 = idx - n * units;
+            const int j = u16 >> 3, u = u16 & 7;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            const int x = s_tok[n];
+            if (x >= 0) val = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)u16 * 8);
+            *reinterpret_cast<uint4*>(gbase + L.a + (size_t)j * 16384 + (size_t)n * 128 + ((u ^ (n & 7)) << 4)) = val;
+        }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int ntiles = (V + kTN - 1) / kTN;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = ptx::policy_evict_last(), pol_u = ptx::policy_evict_first();
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            int lt = 0;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+                const int v0 = t * kTN;
+                for (int j = 0; j < KCH; ++j) {
+                    if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kWaitCycles))) break;
+                    ptx::mbar_arrive_expect_tx(full(stage), kBBytes);
+                    const uint32_t dst = base + L.b + (uint32_t)stage * kBBytes;
+                    ptx::tma_load_2d(dst, &a.w2map, v0, j * 64, full(stage), pol_w);
+                    ptx::tma_load_2d(dst + kBBytes / 2, &a.w2map, v0 + 64, j * 64, full(stage), pol_w);
+                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                }
+                for (int c = 0; c < 4 && ok; ++c) {
+                    const int n = lt * 4 + c, s = n % US;
+                    const uint32_t par = (uint32_t)((n / US) & 1);
+                    if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) break;
+                    ptx::mbar_arrive_expect_tx(ufull(s), slot_bytes);
+                    ptx::tma_load_3d(base + L.u + (uint32_t)s * slot_bytes, &a.umap, v0 + 32 * c, k - 1, b_base,
+                                     ufull(s), pol_u);
+                }
+            }
+            if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTN, /*A K-major*/ false, /*B MN-major*/ true);
+            int stage = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTN);
+                for (int j = 0; j < KCH; ++j) {
+                    if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) break;
+                    ptx::tc_fence_after();
+                    const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
+                    const uint32_t a_addr = base + L.a + (uint32_t)j * 16384u;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // A: K-major rows of 128 B, 8-row groups 1 KB apart (SBO); 16 ranks = 32 B.
+                        const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                        // B: MN-major, 64-entry swizzle atoms 8 KB apart along N (LBO),
+                        //    8-rank groups 1 KB apart along K (SBO); 16 ranks = 2 KB.
+                        const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
+                        ptx::mma_f16(d_tmem, ad, bd, idesc, (j | kk) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty(stage));
+                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull(acc));
+                if (++acc == 2) { acc = 0; aph ^= 1u; }
+            }
+            if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
+            ptx::mma_commit(drain);                 // every MMA above completes before TMEM is freed
+            ptx::mbar_wait(drain, 0u, never, kWaitCycles);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3, cb = warp >> 2;     // lane quarter, 32-column block of the tile
+        const int row = 32 * q + lane;              // request row within the chunk (TMEM lane)
+        const bool active = q < nq;
+        const int b = b_base + row;
+        const bool real = active && row < nb;
+        const Stream rng(p.seed, p.step, 0u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)(k - 1));
+        const size_t out_row = ((size_t)b * gamma + (k - 1)) * V;
+        DrawLse st = drawlse_empty();
+        int acc = 0;
+        uint32_t aph = 0;
+        int lt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+            bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            float bias[32];
+            if (active) {
+                ptx::tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kTN + 32 * cb), bias);
+                ptx::tmem_wait_ld();
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty(acc));
+            if (++acc == 2) { acc = 0; aph ^= 1u; }
+            if (!active) continue;
+            const int n = lt * 4 + cb, s = n % US;
+            ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const int v0 = t * kTN + 32 * cb;
+            if (real) {
+                const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int vq = v0 + 4 * c;
+                    if (vq < V) {
+                        const float4 u4 = *reinterpret_cast<const float4*>(srow + ((c ^ (row & 7)) << 4));
+                        const float zs[4] = {(u4.x + bias[4 * c]) * p.inv_tau, (u4.y + bias[4 * c + 1]) * p.inv_tau,
+                                             (u4.z + bias[4 * c + 2]) * p.inv_tau, (u4.w + bias[4 * c + 3]) * p.inv_tau};
+                        if (p.logits_out)
+                            *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(zs[0], zs[1], zs[2], zs[3]);
+                        const uint4 w = rng.quad((uint32_t)vq >> 2);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float sc = zs[e] + gumbel_of(ws[e]);
+                            const int idx = vq + e;
+                            if (st.best == -INFINITY) {
+                                st.best = sc; st.idx = idx; st.zb = zs[e]; st.s = __expf(zs[e] - sc);
+                            } else if (wins(sc, idx, st.best, st.idx)) {
+                                st.s = st.s * __expf(st.best - sc) + __expf(zs[e] - sc);
+                                st.best = sc; st.idx = idx; st.zb = zs[e];
+                            } else {
+                                st.s += __expf(zs[e] - st.best);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(uempty(s));
+        }
+        s_merge[cb * 128 + row] = st;
+    }
+
+    if (*abort_flag) {
+        for (int i = 0; i < 64; ++i) __nanosleep(1000);    // let copies in flight land
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, 256u);
+    }
+    // fold the four column blocks of each request row
+    if (tid < nb) {
+        DrawLse s = s_merge[tid];
+#pragma unroll
+        for (int cb = 1; cb < 4; ++cb) s = drawlse_merge(s, s_merge[cb * 128 + tid]);
+        p.ws.draft_part[(size_t)(b_base + tid) * p.ws.parts + blockIdx.x] = s;
+    }
+
+    // last-arriving CTA of this request chunk merges the partial states
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&p.ws.tickets_draft[chunk], 1u);
+        s_last = (prev == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int n = warp; n < nb; n += kThreads / 32) {
+        const int bb = b_base + n;
+        const DrawLse* part = p.ws.draft_part + (size_t)bb * p.ws.parts;
+        DrawLse m = drawlse_empty();
+        for (int i = lane; i < (int)gridDim.x; i += 32) {
+            DrawLse c;
+            c.best = __ldcg(&part[i].best); c.idx = __ldcg(&part[i].idx);
+            c.zb = __ldcg(&part[i].zb); c.s = __ldcg(&part[i].s);
+            m = drawlse_merge(m, c);
+        }
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) m = drawlse_merge(m, shfl_xor(m, sh));
+        if (lane == 0) {
+            const size_t o = (size_t)bb * gamma + (k - 1);
+            p.draft_tok[o] = m.idx;
+            p.lse_q[o] = m.best + logf(m.s);
+            p.z_tok[o] = m.zb;
+        }
+    }
+    if (tid == 0) p.ws.tickets_draft[chunk] = 0u;
+}
+
+}  // namespace
+
+bool draft_rows_supported(const DraftParams& p) {
+    return p.W_bf16 && !p.U_bf16 && p.B >= 32 && p.r % 64 == 0 && p.r <= 256 && p.V % 8 == 0 &&
+           tma_encoder() != nullptr;
+}
+
+cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s) {
+    auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
+    if (!enc) return cudaErrorNotSupported;
+    RowsArgs a;
+    a.p = p;
+    a.NC = p.B <= 32 ? 32 : (p.B <= 64 ? 64 : 128);
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.r};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.V * 2};
+        const cuuint32_t box[2] = {64, 64};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&a.w2map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.W2), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)p.gamma, (cuuint64_t)p.B};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.V * 4, (cuuint64_t)p.gamma * p.V * 4};
+        const cuuint32_t box[3] = {32, 1, (cuuint32_t)a.NC};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&a.umap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(p.U), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const Layout L = rows_layout(a.NC, p.r);
+    const size_t smem = L.total + 1024;
+    cudaError_t e = cudaFuncSetAttribute(draft_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int nchunks = (p.B + a.NC - 1) / a.NC;
+    const int ntiles = (p.V + kTN - 1) / kTN;
+    int gx = num_sms() / nchunks;
+    gx = gx < 1 ? 1 : gx;
+    gx = gx > ntiles ? ntiles : gx;
+    gx = gx > p.ws.parts ? p.ws.parts : gx;
+    draft_rows_kernel<<<dim3(gx, nchunks), kThreads, smem, s>>>(a, k);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -368,18 +368,6 @@ draft_tc_kernel(const __grid_constant__ TcArgs a, const int k) {
     if (tid == 0) p.ws.tickets_draft[chunk] = 0u;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    return fn;
-}
-
 int pick_nc(int B, int r) {
     int nc = 16;
     while (nc < B && nc < 256) nc *= 2;
@@ -390,7 +378,7 @@ int pick_nc(int B, int r) {
 template <int NC>
 cudaError_t launch_nc(const DraftParams& p, int k, cudaStream_t s) {
     using C = Cfg<NC>;
-    auto enc = encode_fn();
+    auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
     if (!enc) return cudaErrorNotSupported;
     TcArgs a;
     a.p = p;
@@ -431,16 +419,31 @@ cudaError_t launch_nc(const DraftParams& p, int k, cudaStream_t s) {
 
 }  // namespace
 
+void* tma_encoder() {
+    static void* fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = f;
+    }
+    return fn;
+}
+
 bool draft_tc_supported(const DraftParams& p) {
     if (!p.W_bf16 || p.U_bf16) return false;
     if (p.r % 64 != 0 || p.r > 512 || p.V % 8 != 0) return false;
     if ((reinterpret_cast<uintptr_t>(p.W2) & 15) || (reinterpret_cast<uintptr_t>(p.U) & 15)) return false;
-    if (encode_fn() == nullptr) return false;
+    if (tma_encoder() == nullptr) return false;
     if (getenv("DSPARK_DRAFT_SIMT")) return false;
     return true;
 }
 
 cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s) {
+    if (draft_rows_supported(p) && !getenv("DSPARK_DRAFT_VOCAB_LANES")) return launch_draft_rows(p, k, s);
     switch (pick_nc(p.B, p.r)) {
         case 16: return launch_nc<16>(p, k, s);
         case 32: return launch_nc<32>(p, k, s);

@@ -92,6 +92,9 @@ int num_sms();
 cudaError_t launch_draft_simt(const DraftParams& p, int k, cudaStream_t s);
 bool draft_tc_supported(const DraftParams& p);
 cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s);
+bool draft_rows_supported(const DraftParams& p);
+cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s);
+void* tma_encoder();   // cuTensorMapEncodeTiled from the driver, or NULL
 cudaError_t launch_confidence(const ConfParams& p, cudaStream_t s);
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
