@@ -181,6 +181,18 @@ dspark_status dspark_verify(
     float* p_tok, uint32_t* near_ties,
     void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Diagnostics: the random stream as the kernels draw it.  For columns
+ * v = 0..n-1 of stream (seed, step, domain, row) writes the uniform
+ * u = (2*(x div 2^9) + 1) * 2^-24 and the Gumbel variate G = -log(-log u) the
+ * kernels use (either output may be NULL, not both).  G is formed in binary32
+ * with the hardware log2 and, for 1 - u < 1/8, a series for -log(1 - w);
+ * it stays within ~2e-6 of the exact value.  No counterpart on the pages: it
+ * exists so tests can check the device generator against the definition.
+ */
+dspark_status dspark_gumbel_stream(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row, int n,
+                                   float* gumbel_out, float* uniform_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

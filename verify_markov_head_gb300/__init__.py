@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "Workspace", "StepBuffers", "run_step", "run_step_host",
+    "dspark_schedule", "dspark_verify", "dspark_gumbel_stream", "Workspace", "StepBuffers", "run_step", "run_step_host",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
@@ -54,6 +54,8 @@ _lib.dspark_verify.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _v
                                _i, _i, _i, _i, _i, _f, _u64, _u64,
                                _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.dspark_verify.restype = _i
+_lib.dspark_gumbel_stream.argtypes = [_u64, _u64, C.c_uint32, C.c_uint32, _i, _vp, _vp, _vp]
+_lib.dspark_gumbel_stream.restype = _i
 
 
 class DsparkError(RuntimeError):
@@ -179,6 +181,11 @@ def dspark_verify(target, U, W1, W2, anchor, draft_tok, lse_q, z_tok, K, accepte
         _p(lse_q), _p(z_tok), _p(K), B, gamma, V, r, req_base, float(tau), int(seed), int(step),
         _p(accepted), _p(out_tok), _p(out_req), _p(out_pos), _p(out_off), _p(next_anchor),
         _p(p_tok), _p(near_ties), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def dspark_gumbel_stream(seed, step, domain, row, n, gumbel_out=None, uniform_out=None, stream=None):
+    _check("dspark_gumbel_stream", _lib.dspark_gumbel_stream(
+        int(seed), int(step), int(domain), int(row), int(n), _p(gumbel_out), _p(uniform_out), _stream(stream)))
 
 
 class StepBuffers:

@@ -242,4 +242,14 @@ dspark_status dspark_verify(const void* target, dspark_dtype target_t, const voi
     return launch_status(launch_verify(p, static_cast<cudaStream_t>(stream)));
 }
 
+dspark_status dspark_gumbel_stream(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row, int n,
+                                   float* gumbel_out, float* uniform_out, void* stream) {
+    if (n < 0 || domain > 3 || (!gumbel_out && !uniform_out)) return DSPARK_ERR_INVALID;
+    if ((gumbel_out && !is_device_ptr(gumbel_out)) || (uniform_out && !is_device_ptr(uniform_out)))
+        return DSPARK_ERR_INVALID;
+    if (n == 0) return DSPARK_OK;
+    return launch_status(launch_gumbel_stream(seed, step, domain, row, n, gumbel_out, uniform_out,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

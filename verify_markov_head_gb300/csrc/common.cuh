@@ -48,15 +48,41 @@ struct Stream {
     }
 };
 
-// u = (2*(x >> 9) + 1) * 2^-24: exact in binary32, strictly inside (0, 1).
+// u = (2*(x >> 9) + 1) * 2^-24, exact in binary32, strictly inside (0, 1):
+// with j = x >> 9, the float 1 + j*2^-23 (exponent 127, mantissa j) minus
+// 1 - 2^-24 is exactly (2j + 1) * 2^-24.
+constexpr float kOneMinusHalfUlp = 0.99999994039535522f;   // 1 - 2^-24
 __device__ __forceinline__ float uniform_of(uint32_t x) {
-    return (float)(2u * (x >> 9) + 1u) * 5.9604644775390625e-8f;
+    return __uint_as_float((x >> 9) | 0x3f800000u) - kOneMinusHalfUlp;
+}
+// 1 - u, exactly: the same construction on the complemented top 23 bits.
+__device__ __forceinline__ float one_minus_uniform_of(uint32_t x) {
+    return __uint_as_float((~x >> 9) | 0x3f800000u) - kOneMinusHalfUlp;
 }
 
-// Standard Gumbel variate -log(-log u), with CUDA's full-accuracy logf (the
-// inner log near u = 1 keeps its relative accuracy, which the outer log needs).
+// Standard Gumbel variate G = -ln(E), E = -ln(u).
+//   E: for u <= 7/8, -ln2 * log2(u) with the hardware log2 (absolute error
+//      <= 2^-22 on [1/2, 2], 2 ulp elsewhere, so E keeps ~1e-6 relative
+//      accuracy where |log2 u| >= 0.19); for w = 1 - u < 1/8, the Taylor
+//      series -ln(1 - w) = sum_{n>=1} w^n / n to n = 8 (next term below
+//      7e-9 relative).  w is exact, so E stays accurate as u -> 1, where
+//      the largest variates (the likely winners) come from.
+//   G: -ln2 * log2(E), absolute error <= 2e-7.
+// Overall |G - exact| stays near 1e-6; the oracle computes G in binary64.
+constexpr float kLn2 = 0.69314718055994531f;
 __device__ __forceinline__ float gumbel_of(uint32_t x) {
-    return -logf(-logf(uniform_of(x)));
+    const float u = uniform_of(x);
+    const float w = one_minus_uniform_of(x);
+    const float e_log = -kLn2 * __log2f(u);
+    float poly = fmaf(w, 0.125f, 0.142857143f);
+    poly = fmaf(w, poly, 0.166666667f);
+    poly = fmaf(w, poly, 0.2f);
+    poly = fmaf(w, poly, 0.25f);
+    poly = fmaf(w, poly, 0.333333333f);
+    poly = fmaf(w, poly, 0.5f);
+    poly = fmaf(w, poly, 1.0f);
+    const float E = (w < 0.125f) ? w * poly : e_log;
+    return -kLn2 * __log2f(E);
 }
 
 // ---------------------------------------------------------------- merge states

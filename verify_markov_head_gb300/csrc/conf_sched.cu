@@ -22,49 +22,57 @@
 namespace dspark {
 namespace {
 
+constexpr int kConfThreads = 512;
+
+// One CTA per request; position k's dot product over [h_k ; emb(x~_{k-1})]
+// is a block reduction, all positions handled in one pass over the inputs.
 template <typename ET>
-__global__ void confidence_kernel(const ConfParams p) {
+__global__ void __launch_bounds__(kConfThreads) confidence_kernel(const ConfParams p) {
     const int b = blockIdx.x;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int gamma = p.gamma, d = p.d, e = p.e;
-    __shared__ float s_s[DSPARK_MAX_GAMMA];
-    if (warp < gamma) {
-        const int k = warp + 1;
-        int x = (k == 1) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (k - 2)];
-        const bool ok = (x >= 0 && x < p.V);
-        if (!ok) { if (lane == 0) raise_status(p.status, kBadToken); x = 0; }
-        const float* hk = p.h + ((size_t)b * gamma + (k - 1)) * d;
-        const ET* ek = static_cast<const ET*>(p.emb) + (size_t)x * e;
+    __shared__ float s_part[kConfThreads / 32][DSPARK_MAX_GAMMA];
+    __shared__ int s_x[DSPARK_MAX_GAMMA];
+    if (tid < gamma) {
+        int x = (tid == 0) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (tid - 1)];
+        if (x < 0 || x >= p.V) { raise_status(p.status, kBadToken); x = -1; }
+        s_x[tid] = x;
+    }
+    __syncthreads();
+    const bool vec = (d % 4) == 0 && (e % 4) == 0;
+    for (int k = 0; k < gamma; ++k) {
+        const float* hk = p.h + ((size_t)b * gamma + k) * d;
+        const int x = s_x[k];
+        const ET* ek = static_cast<const ET*>(p.emb) + (size_t)(x < 0 ? 0 : x) * e;
         float acc = 0.f;
-        if ((d % 4) == 0) {
-            for (int i = 4 * lane; i < d; i += 128) {
-                const float4 w = *reinterpret_cast<const float4*>(p.w_c + i);
-                const float4 hv = *reinterpret_cast<const float4*>(hk + i);
+        if (vec) {
+            for (int i = 4 * tid; i < d; i += 4 * kConfThreads) {
+                const float4 w = __ldg(reinterpret_cast<const float4*>(p.w_c + i));
+                const float4 hv = __ldcs(reinterpret_cast<const float4*>(hk + i));
                 acc = fmaf(w.x, hv.x, fmaf(w.y, hv.y, fmaf(w.z, hv.z, fmaf(w.w, hv.w, acc))));
             }
-        } else {
-            for (int i = lane; i < d; i += 32) acc = fmaf(p.w_c[i], hk[i], acc);
-        }
-        if (ok) {
-            if ((e % 4) == 0 && (d % 4) == 0) {
-                for (int i = 4 * lane; i < e; i += 128) {
-                    const float4 w = *reinterpret_cast<const float4*>(p.w_c + d + i);
+            if (x >= 0)
+                for (int i = 4 * tid; i < e; i += 4 * kConfThreads) {
+                    const float4 w = __ldg(reinterpret_cast<const float4*>(p.w_c + d + i));
                     const float4 ev = Vec4<ET>::load(ek + i);
                     acc = fmaf(w.x, ev.x, fmaf(w.y, ev.y, fmaf(w.z, ev.z, fmaf(w.w, ev.w, acc))));
                 }
-            } else {
-                for (int i = lane; i < e; i += 32) acc = fmaf(p.w_c[d + i], to_f32(ek[i]), acc);
-            }
+        } else {
+            for (int i = tid; i < d; i += kConfThreads) acc = fmaf(p.w_c[i], hk[i], acc);
+            if (x >= 0)
+                for (int i = tid; i < e; i += kConfThreads) acc = fmaf(p.w_c[d + i], to_f32(ek[i]), acc);
         }
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (lane == 0) s_s[warp] = acc + p.b_c;
+        if (lane == 0) s_part[warp][k] = acc;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         float run = 0.f;
         for (int k = 1; k <= gamma; ++k) {
-            const float x = s_s[k - 1] / p.T[k - 1];
+            float sk = 0.f;
+            for (int w = 0; w < kConfThreads / 32; ++w) sk += s_part[w][k - 1];
+            const float x = (sk + p.b_c) / p.T[k - 1];
             // sigmoid and its log, stable for either sign of x
             const float en = expf(-fabsf(x));
             const float c = (x >= 0.f) ? 1.f / (1.f + en) : en / (1.f + en);
@@ -209,7 +217,7 @@ __device__ void theta_items(SchedSmem& S, const float* ls, const float* sps, int
     double sum = 0.0;
 #pragma unroll
     for (int j = 0; j < kIPT; ++j) {
-        a[j] = (i0 + j < n) ? exp((double)ls[S.val[0][i0 + j]]) : 0.0;
+        a[j] = (i0 + j < n) ? (double)expf(ls[S.val[0][i0 + j]]) : 0.0;
         sum += a[j];
     }
     double total;
@@ -228,6 +236,11 @@ __global__ void __launch_bounds__(kST) schedule_kernel(const SchedParams p) {
     const int B = p.B, gamma = p.gamma, n = B * gamma;
     const double theta0 = (double)B * (double)p.sps[B - 1];
 
+    if (p.mode == DSPARK_SCHED_OFF) {       // every request verifies its whole block
+        for (int b = tid; b < B; b += kST) p.K[b] = gamma;
+        if (tid == 0) { *p.n_total = n; *p.theta = 0.f; }
+        return;
+    }
     int admit = 0;
     if (p.mode == DSPARK_SCHED_ASYNC) {
         const float* src = p.log_surv_hist ? p.log_surv_hist : p.log_surv;
@@ -324,9 +337,8 @@ __global__ void __launch_bounds__(kST) schedule_kernel(const SchedParams p) {
 }  // namespace
 
 cudaError_t launch_confidence(const ConfParams& p, cudaStream_t s) {
-    const int threads = 32 * p.gamma;
-    if (p.emb_bf16) confidence_kernel<uint16_t><<<p.B, threads, 0, s>>>(p);
-    else confidence_kernel<float><<<p.B, threads, 0, s>>>(p);
+    if (p.emb_bf16) confidence_kernel<uint16_t><<<p.B, kConfThreads, 0, s>>>(p);
+    else confidence_kernel<float><<<p.B, kConfThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

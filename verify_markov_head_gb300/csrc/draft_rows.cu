@@ -27,6 +27,15 @@
 // on expiry the kernel raises the timeout bit, lets its copies land, frees
 // TMEM and returns.  Partial states go to the workspace and the last CTA of a
 // request chunk to arrive merges them (atomic ticket, no waiting).
+//
+// The same pipeline serves the residual draw of verification
+// ("DSpark：半自回归生成与置信度调度的投机解码" section 形式化定义): for every
+// request whose walk rejected draft j, h = W1[x~_{j-1}] and the epilogue forms
+// q = softmax(z_j) and p = softmax(t_j / tau) from the passed log-normalisers,
+// then draws argmax_v log(max(0, p - q)) + G (domain 2), with the draw from p
+// kept for the case p <= q everywhere.  Each thread reads its own row of U and
+// of the target logits (the rejected rows differ per request, so no common
+// TMA box exists); no U slice ring is used.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -63,7 +72,7 @@ __host__ __device__ inline Layout rows_layout(int NC, int r) {
     L.bar = L.merge + 4u * 128u * 16u;
     L.misc = L.bar + 8u * (2 * kStages + 2 * L.uslots + 5);
     L.misc = (L.misc + 15u) & ~15u;
-    L.total = L.misc + 16u + 4u * 128u;
+    L.total = L.misc + 16u + 8u * 128u;
     return L;
 }
 
@@ -72,10 +81,14 @@ struct RowsArgs {
     CUtensorMap umap;    // fp32 [B][gamma][V], box {32 vocab, 1, NC requests}, 128-byte swizzle
     DraftParams p;
     int NC;              // request rows per CTA (32, 64 or 128)
+    // residual mode only
+    const void* target;  // [B][gamma+1][V]
+    uint32_t* near_ties;
 };
 
+template <bool kResid, typename TT>
 __global__ void __launch_bounds__(kThreads, 1)
-draft_rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
+rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     const DraftParams& p = a.p;
     const int NC = a.NC;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -118,14 +131,21 @@ draft_rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     }
     if (tid == kProducerWarp * 32) { ptx::prefetch_tmap(&a.w2map); ptx::prefetch_tmap(&a.umap); }
     if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 256u); ptx::tmem_relinquish(); }
+    int* s_row = s_tok + 128;                       // residual mode: rejected row per request, or -1
     for (int n = tid; n < 128; n += kThreads) {
-        int x = -1;
+        int x = -1, prow = -1;
         if (n < nb) {
             const int b = b_base + n;
-            x = (k == 1) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (k - 2)];
-            if (x < 0 || x >= V) { raise_status(p.ws.status, kBadToken); x = -1; }
+            if constexpr (kResid) {
+                prow = __ldcg(&p.ws.rej[b]);
+                if (prow >= 0) x = (prow == 0) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (prow - 1)];
+            } else {
+                x = (k == 1) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (k - 2)];
+            }
+            if (x >= V || (x < 0 && !kResid)) { raise_status(p.ws.status, kBadToken); x = -1; }
         }
         s_tok[n] = x;
+        s_row[n] = prow;
     }
     __syncthreads();
     // A operand: h rows, K-major with 128-byte swizzle.  K-chunk j (64 ranks) is a
@@ -167,7 +187,7 @@ draft_rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                     ptx::tma_load_2d(dst + kBBytes / 2, &a.w2map, v0 + 64, j * 64, full(stage), pol_w);
                     if (++stage == kStages) { stage = 0; ph ^= 1u; }
                 }
-                for (int c = 0; c < 4 && ok; ++c) {
+                for (int c = 0; c < 4 && ok && !kResid; ++c) {
                     const int n = lt * 4 + c, s = n % US;
                     const uint32_t par = (uint32_t)((n / US) & 1);
                     if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) break;
@@ -222,10 +242,17 @@ draft_rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
         const int row = 32 * q + lane;              // request row within the chunk (TMEM lane)
         const bool active = q < nq;
         const int b = b_base + row;
-        const bool real = active && row < nb;
-        const Stream rng(p.seed, p.step, 0u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)(k - 1));
+        const bool real = active && row < nb && (!kResid || s_row[row] >= 0);
+        const int urow = kResid ? (real ? s_row[row] : 0) : (k - 1);      // row of U (and of the target)
+        const Stream rng(p.seed, p.step, kResid ? 2u : 0u,
+                         (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)urow);
         const size_t out_row = ((size_t)b * gamma + (k - 1)) * V;
+        const float* Urow = static_cast<const float*>(p.U) + ((size_t)b * gamma + urow) * V;
+        const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + urow) * V;
+        float2 lse = make_float2(0.f, 0.f);
+        if (kResid && real) lse = p.ws.lse_rej[b];
         DrawLse st = drawlse_empty();
+        Draw2 st2 = draw2_empty();
         int acc = 0;
         uint32_t aph = 0;
         int lt = 0;
@@ -244,44 +271,84 @@ draft_rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
             if (lane == 0) ptx::mbar_arrive(tempty(acc));
             if (++acc == 2) { acc = 0; aph ^= 1u; }
             if (!active) continue;
-            const int n = lt * 4 + cb, s = n % US;
-            ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
             const int v0 = t * kTN + 32 * cb;
-            if (real) {
-                const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
+            if constexpr (kResid) {
+                if (real) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int vq = v0 + 4 * c;
-                    if (vq < V) {
-                        const float4 u4 = *reinterpret_cast<const float4*>(srow + ((c ^ (row & 7)) << 4));
-                        const float zs[4] = {(u4.x + bias[4 * c]) * p.inv_tau, (u4.y + bias[4 * c + 1]) * p.inv_tau,
-                                             (u4.z + bias[4 * c + 2]) * p.inv_tau, (u4.w + bias[4 * c + 3]) * p.inv_tau};
-                        if (p.logits_out)
-                            *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(zs[0], zs[1], zs[2], zs[3]);
-                        const uint4 w = rng.quad((uint32_t)vq >> 2);
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                  for (int half = 0; half < 2; ++half) {
+                    float4 u4[8], t4[8];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float sc = zs[e] + gumbel_of(ws[e]);
-                            const int idx = vq + e;
-                            if (st.best == -INFINITY) {
-                                st.best = sc; st.idx = idx; st.zb = zs[e]; st.s = __expf(zs[e] - sc);
-                            } else if (wins(sc, idx, st.best, st.idx)) {
-                                st.s = st.s * __expf(st.best - sc) + __expf(zs[e] - sc);
-                                st.best = sc; st.idx = idx; st.zb = zs[e];
-                            } else {
-                                st.s += __expf(zs[e] - st.best);
+                    for (int c = 4 * half; c < 4 * half + 4; ++c) {
+                        const int vq = v0 + 4 * c;
+                        u4[c] = (vq < V) ? __ldcs(reinterpret_cast<const float4*>(Urow + vq)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        t4[c] = (vq < V) ? Vec4<TT>::load_stream(Trow + vq) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int c = 4 * half; c < 4 * half + 4; ++c) {
+                        const int vq = v0 + 4 * c;
+                        if (vq < V) {
+                            const float us[4] = {u4[c].x, u4[c].y, u4[c].z, u4[c].w};
+                            const float ts[4] = {t4[c].x, t4[c].y, t4[c].z, t4[c].w};
+                            const uint4 w = rng.quad((uint32_t)vq >> 2);
+                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float z = (us[e] + bias[4 * c + e]) * p.inv_tau;
+                                const float tv = ts[e] * p.inv_tau;
+                                const float g = gumbel_of(ws[e]);
+                                const float pr = expf(tv - lse.x) - expf(z - lse.y);
+                                const int idx = vq + e;
+                                if (pr > 0.f) {
+                                    const float sc = logf(pr) + g;
+                                    if (wins(sc, idx, st2.best_r, st2.idx_r)) { st2.best_r = sc; st2.idx_r = idx; }
+                                }
+                                const float sp = tv + g;
+                                if (wins(sp, idx, st2.best_p, st2.idx_p)) { st2.best_p = sp; st2.idx_p = idx; }
+                            }
+                        }
+                    }
+                  }
+                }
+            } else {
+                const int n = lt * 4 + cb, s = n % US;
+                ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if (real) {
+                    const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int vq = v0 + 4 * c;
+                        if (vq < V) {
+                            const float4 u4 = *reinterpret_cast<const float4*>(srow + ((c ^ (row & 7)) << 4));
+                            const float zs[4] = {(u4.x + bias[4 * c]) * p.inv_tau, (u4.y + bias[4 * c + 1]) * p.inv_tau,
+                                                 (u4.z + bias[4 * c + 2]) * p.inv_tau, (u4.w + bias[4 * c + 3]) * p.inv_tau};
+                            if (p.logits_out)
+                                *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(zs[0], zs[1], zs[2], zs[3]);
+                            const uint4 w = rng.quad((uint32_t)vq >> 2);
+                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float sc = zs[e] + gumbel_of(ws[e]);
+                                const int idx = vq + e;
+                                // an empty state has best = -inf and s = 0, so the first
+                                // entry takes the first branch with exp(-inf) = 0
+                                if (wins(sc, idx, st.best, st.idx)) {
+                                    st.s = st.s * __expf(st.best - sc) + __expf(zs[e] - sc);
+                                    st.best = sc; st.idx = idx; st.zb = zs[e];
+                                } else {
+                                    st.s += __expf(zs[e] - st.best);
+                                }
                             }
                         }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(uempty(s));
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(uempty(s));
         }
-        s_merge[cb * 128 + row] = st;
+        if constexpr (kResid) reinterpret_cast<Draw2*>(s_merge)[cb * 128 + row] = st2;
+        else s_merge[cb * 128 + row] = st;
     }
 
     if (*abort_flag) {
@@ -295,18 +362,27 @@ draft_rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     }
     // fold the four column blocks of each request row
     if (tid < nb) {
-        DrawLse s = s_merge[tid];
+        if constexpr (kResid) {
+            const Draw2* m2 = reinterpret_cast<const Draw2*>(s_merge);
+            Draw2 s2 = m2[tid];
 #pragma unroll
-        for (int cb = 1; cb < 4; ++cb) s = drawlse_merge(s, s_merge[cb * 128 + tid]);
-        p.ws.draft_part[(size_t)(b_base + tid) * p.ws.parts + blockIdx.x] = s;
+            for (int cb = 1; cb < 4; ++cb) s2 = draw2_merge(s2, m2[cb * 128 + tid]);
+            if (s_row[tid] >= 0) p.ws.resid_part[(size_t)(b_base + tid) * p.ws.parts + blockIdx.x] = s2;
+        } else {
+            DrawLse s1 = s_merge[tid];
+#pragma unroll
+            for (int cb = 1; cb < 4; ++cb) s1 = drawlse_merge(s1, s_merge[cb * 128 + tid]);
+            p.ws.draft_part[(size_t)(b_base + tid) * p.ws.parts + blockIdx.x] = s1;
+        }
     }
 
     // last-arriving CTA of this request chunk merges the partial states
+    uint32_t* ticket = kResid ? &p.ws.tickets_resid[chunk] : &p.ws.tickets_draft[chunk];
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        const unsigned prev = atomicAdd(&p.ws.tickets_draft[chunk], 1u);
+        const unsigned prev = atomicAdd(ticket, 1u);
         s_last = (prev == gridDim.x - 1);
     }
     __syncthreads();
@@ -314,39 +390,66 @@ draft_rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     __threadfence();
     for (int n = warp; n < nb; n += kThreads / 32) {
         const int bb = b_base + n;
-        const DrawLse* part = p.ws.draft_part + (size_t)bb * p.ws.parts;
-        DrawLse m = drawlse_empty();
-        for (int i = lane; i < (int)gridDim.x; i += 32) {
-            DrawLse c;
-            c.best = __ldcg(&part[i].best); c.idx = __ldcg(&part[i].idx);
-            c.zb = __ldcg(&part[i].zb); c.s = __ldcg(&part[i].s);
-            m = drawlse_merge(m, c);
-        }
+        if constexpr (kResid) {
+            if (s_row[n] < 0) continue;
+            const Draw2* part = p.ws.resid_part + (size_t)bb * p.ws.parts;
+            Draw2 m = draw2_empty();
+            for (int i = lane; i < (int)gridDim.x; i += 32) {
+                Draw2 c;
+                c.best_r = __ldcg(&part[i].best_r); c.idx_r = __ldcg(&part[i].idx_r);
+                c.best_p = __ldcg(&part[i].best_p); c.idx_p = __ldcg(&part[i].idx_p);
+                m = draw2_merge(m, c);
+            }
 #pragma unroll
-        for (int sh = 1; sh < 32; sh <<= 1) m = drawlse_merge(m, shfl_xor(m, sh));
-        if (lane == 0) {
-            const size_t o = (size_t)bb * gamma + (k - 1);
-            p.draft_tok[o] = m.idx;
-            p.lse_q[o] = m.best + logf(m.s);
-            p.z_tok[o] = m.zb;
+            for (int sh = 1; sh < 32; sh <<= 1) m = draw2_merge(m, shfl_xor(m, sh));
+            if (lane == 0) {
+                if (m.best_r > -INFINITY) {
+                    p.ws.fin[bb] = m.idx_r;
+                } else {
+                    p.ws.fin[bb] = m.idx_p;
+                    if (a.near_ties) atomicAdd(&a.near_ties[1], 1u);
+                }
+            }
+        } else {
+            const DrawLse* part = p.ws.draft_part + (size_t)bb * p.ws.parts;
+            DrawLse m = drawlse_empty();
+            for (int i = lane; i < (int)gridDim.x; i += 32) {
+                DrawLse c;
+                c.best = __ldcg(&part[i].best); c.idx = __ldcg(&part[i].idx);
+                c.zb = __ldcg(&part[i].zb); c.s = __ldcg(&part[i].s);
+                m = drawlse_merge(m, c);
+            }
+#pragma unroll
+            for (int sh = 1; sh < 32; sh <<= 1) m = drawlse_merge(m, shfl_xor(m, sh));
+            if (lane == 0) {
+                const size_t o = (size_t)bb * gamma + (k - 1);
+                p.draft_tok[o] = m.idx;
+                p.lse_q[o] = m.best + logf(m.s);
+                p.z_tok[o] = m.zb;
+            }
         }
     }
-    if (tid == 0) p.ws.tickets_draft[chunk] = 0u;
+    if (tid == 0) *ticket = 0u;
 }
 
 }  // namespace
 
-bool draft_rows_supported(const DraftParams& p) {
+bool rows_supported(const DraftParams& p) {
     return p.W_bf16 && !p.U_bf16 && p.B >= 32 && p.r % 64 == 0 && p.r <= 256 && p.V % 8 == 0 &&
            tma_encoder() != nullptr;
 }
 
-cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s) {
+bool draft_rows_supported(const DraftParams& p) { return rows_supported(p); }
+
+static cudaError_t launch_rows(const DraftParams& p, int k, bool resid, const void* target, bool target_bf16,
+                               uint32_t* near_ties, cudaStream_t s) {
     auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
     if (!enc) return cudaErrorNotSupported;
     RowsArgs a;
     a.p = p;
     a.NC = p.B <= 32 ? 32 : (p.B <= 64 ? 64 : 128);
+    a.target = target;
+    a.near_ties = near_ties;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.r};
         const cuuint64_t strides[1] = {(cuuint64_t)p.V * 2};
@@ -369,7 +472,8 @@ cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s) {
     }
     const Layout L = rows_layout(a.NC, p.r);
     const size_t smem = L.total + 1024;
-    cudaError_t e = cudaFuncSetAttribute(draft_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = !resid ? rows_kernel<false, float> : (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nchunks = (p.B + a.NC - 1) / a.NC;
     const int ntiles = (p.V + kTN - 1) / kTN;
@@ -377,8 +481,21 @@ cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s) {
     gx = gx < 1 ? 1 : gx;
     gx = gx > ntiles ? ntiles : gx;
     gx = gx > p.ws.parts ? p.ws.parts : gx;
-    draft_rows_kernel<<<dim3(gx, nchunks), kThreads, smem, s>>>(a, k);
+    kern<<<dim3(gx, nchunks), kThreads, smem, s>>>(a, k);
     return cudaGetLastError();
+}
+
+cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s) {
+    return launch_rows(p, k, false, nullptr, false, nullptr, s);
+}
+
+bool resid_rows_supported(const VerifyParams& v) {
+    DraftParams p = draft_view(v);
+    return rows_supported(p);
+}
+
+cudaError_t launch_resid_rows(const VerifyParams& v, cudaStream_t s) {
+    return launch_rows(draft_view(v), 1, true, v.target, v.target_bf16 != 0, v.near_ties, s);
 }
 
 }  // namespace dspark

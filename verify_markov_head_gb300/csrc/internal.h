@@ -16,7 +16,7 @@ struct Draw2;
 
 constexpr int kMaxParts = 1024;        // cap on partial states per request per launch
 constexpr int kPartTile = 128;         // vocabulary entries per tile of the partial-producing kernels
-constexpr int kVerifySeg = 4096;       // vocabulary entries per verify-stream CTA
+constexpr int kVerifySeg = 8192;       // vocabulary entries per verify-stream work item
 constexpr int kChunk = 16;             // requests per chunk of the partial-producing kernels
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
@@ -95,6 +95,21 @@ cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s);
 bool draft_rows_supported(const DraftParams& p);
 cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s);
 void* tma_encoder();   // cuTensorMapEncodeTiled from the driver, or NULL
+bool resid_rows_supported(const VerifyParams& v);
+cudaError_t launch_resid_rows(const VerifyParams& v, cudaStream_t s);
+
+// The draft-side view of a verify call (same U, W1, W2, tokens and workspace).
+inline DraftParams draft_view(const VerifyParams& v) {
+    DraftParams p;
+    p.U = v.U; p.U_bf16 = v.U_bf16; p.W1 = v.W1; p.W2 = v.W2; p.W_bf16 = v.W_bf16;
+    p.anchor = v.anchor; p.B = v.B; p.gamma = v.gamma; p.V = v.V; p.r = v.r; p.req_base = v.req_base;
+    p.inv_tau = v.inv_tau; p.seed = v.seed; p.step = v.step;
+    p.draft_tok = const_cast<int32_t*>(v.draft_tok); p.lse_q = nullptr; p.z_tok = nullptr; p.logits_out = nullptr;
+    p.ws = v.ws;
+    return p;
+}
+cudaError_t launch_gumbel_stream(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row, int n, float* g,
+                                 float* u, cudaStream_t s);
 cudaError_t launch_confidence(const ConfParams& p, cudaStream_t s);
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);

@@ -16,68 +16,93 @@
 //                   with the draw from p kept as the fallback.
 //   verify_compact  one CTA: exclusive scan of A_b + 1, scatter of the
 //                   accepted drafts and the final token of every request.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace dspark {
 namespace {
 
-constexpr int kStreamThreads = 256;
+constexpr int kStreamThreads = 512;
+constexpr int kStreamVec = kVerifySeg / (4 * kStreamThreads);   // float4 loads per thread per item (4)
 
 template <typename T>
 __device__ __forceinline__ float load_scalar(const T* p, size_t i) { return to_f32(p[i]); }
 
+// Work item w = (b, i, seg) with seg fastest; rows i > K_b are skipped.  All
+// kStreamVec loads of an item are issued before any is used.
 template <typename TT>
 __global__ void __launch_bounds__(kStreamThreads)
 verify_stream_kernel(const VerifyParams p) {
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
-    const int seg = blockIdx.x % nseg;
-    const int i = (blockIdx.x / nseg) % (gamma + 1);
-    const int b = blockIdx.x / (nseg * (gamma + 1));
-    int Kb = p.K[b];
-    if (Kb < 0 || Kb > gamma) {
-        if (seg == 0 && i == 0 && threadIdx.x == 0) raise_status(p.ws.status, kBadLength);
-        Kb = Kb < 0 ? 0 : gamma;
-    }
-    if (i > Kb) return;
-    const bool bonus = (i == Kb);
-    const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
-    const int v_beg = seg * kVerifySeg;
-    const int v_end = min(V, v_beg + kVerifySeg);
-    const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
-
-    LseDraw st = lsedraw_empty();
-    for (int v = v_beg + 4 * threadIdx.x; v < v_end; v += 4 * kStreamThreads) {
-        const float4 x4 = Vec4<TT>::load_stream(row + v);
-        const float xs[4] = {x4.x * p.inv_tau, x4.y * p.inv_tau, x4.z * p.inv_tau, x4.w * p.inv_tau};
-        const float mx = fmaxf(fmaxf(xs[0], xs[1]), fmaxf(xs[2], xs[3]));
-        if (mx > st.m) { st.s = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mx); st.m = mx; }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) st.s += __expf(xs[e] - st.m);
-        if (bonus) {
-            const uint4 w = rng.quad((uint32_t)v >> 2);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float sc = xs[e] + gumbel_of(ws[e]);
-                if (wins(sc, v + e, st.best, st.idx)) { st.best = sc; st.idx = v + e; }
-            }
-        }
-    }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
+    const int items = p.B * (gamma + 1) * nseg;
     __shared__ LseDraw s_part[kStreamThreads / 32];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (lane == 0) s_part[warp] = st;
-    __syncthreads();
-    if (warp == 0) {
-        st = lane < kStreamThreads / 32 ? s_part[lane] : lsedraw_empty();
+    for (int w = blockIdx.x; w < items; w += gridDim.x) {
+        const int seg = w % nseg;
+        const int i = (w / nseg) % (gamma + 1);
+        const int b = w / (nseg * (gamma + 1));
+        int Kb = p.K[b];
+        if (Kb < 0 || Kb > gamma) {
+            if (seg == 0 && i == 0 && threadIdx.x == 0) raise_status(p.ws.status, kBadLength);
+            Kb = Kb < 0 ? 0 : gamma;
+        }
+        if (i > Kb) continue;                      // uniform over the CTA
+        const bool bonus = (i == Kb);
+        const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
+        const int v_beg = seg * kVerifySeg;
+        float4 x4[kStreamVec];
+#pragma unroll
+        for (int j = 0; j < kStreamVec; ++j) {
+            const int v = v_beg + 4 * (threadIdx.x + j * kStreamThreads);
+            x4[j] = (v < V) ? Vec4<TT>::load_stream(row + v) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        LseDraw st = lsedraw_empty();
+#pragma unroll
+        for (int j = 0; j < kStreamVec; ++j) {
+            const float xs[4] = {x4[j].x * p.inv_tau, x4[j].y * p.inv_tau, x4[j].z * p.inv_tau, x4[j].w * p.inv_tau};
+            const float mx = fmaxf(fmaxf(xs[0], xs[1]), fmaxf(xs[2], xs[3]));
+            if (mx > st.m) { st.s = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mx); st.m = mx; }
+            if (mx > -INFINITY) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) st.s += __expf(xs[e] - st.m);
+            }
+        }
+        if (bonus) {
+            const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
+#pragma unroll
+            for (int j = 0; j < kStreamVec; ++j) {
+                const int v = v_beg + 4 * (threadIdx.x + j * kStreamThreads);
+                if (v < V) {
+                    const uint4 wq = rng.quad((uint32_t)v >> 2);
+                    const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
+                    const float xs[4] = {x4[j].x * p.inv_tau, x4[j].y * p.inv_tau, x4[j].z * p.inv_tau, x4[j].w * p.inv_tau};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float sc = xs[e] + gumbel_of(ws[e]);
+                        if (wins(sc, v + e, st.best, st.idx)) { st.best = sc; st.idx = v + e; }
+                    }
+                }
+            }
+        }
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
-        if (lane == 0) p.ws.verify_part[((size_t)b * (gamma + 1) + i) * p.ws.nseg + seg] = st;
+        if (lane == 0) s_part[warp] = st;
+        __syncthreads();
+        if (warp == 0) {
+            st = lane < kStreamThreads / 32 ? s_part[lane] : lsedraw_empty();
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
+            if (lane == 0) p.ws.verify_part[((size_t)b * (gamma + 1) + i) * nseg + seg] = st;
+        }
+        __syncthreads();
     }
 }
 
+// One warp per request: lse_p of rows 0..K_b from the segment partials, then
+// the accept test of every walked position at once (lane k-1 tests draft k),
+// the first rejection found by a ballot.
 template <typename TT>
 __global__ void __launch_bounds__(32)
 verify_accept_kernel(const VerifyParams p) {
@@ -85,7 +110,21 @@ verify_accept_kernel(const VerifyParams p) {
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
     int Kb = p.K[b];
     Kb = Kb < 0 ? 0 : (Kb > gamma ? gamma : Kb);
-    __shared__ float s_lse[DSPARK_MAX_GAMMA + 1];
+    const TT* target = static_cast<const TT*>(p.target);
+    const uint32_t row0 = (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1);
+    // per-lane draft data for position k = lane + 1 (issued before the merges)
+    int x = 0;
+    float t = 0.f, lq = 0.f, u = 1.f;
+    const bool walk = lane < Kb;
+    if (walk) {
+        const size_t o = (size_t)b * gamma + lane;
+        x = p.draft_tok[o];
+        if (x < 0 || x >= V) { raise_status(p.ws.status, kBadToken); x = 0; }
+        t = load_scalar(target, ((size_t)b * (gamma + 1) + lane) * V + x) * p.inv_tau;
+        lq = p.z_tok[o] - p.lse_q[o];
+        u = uniform_of(Stream(p.seed, p.step, 1u, row0 + (uint32_t)lane).word(0));
+    }
+    float lse_mine = 0.f;        // lse_p of row `lane`
     int bonus_idx = 0;
     for (int i = 0; i <= Kb; ++i) {
         const LseDraw* part = p.ws.verify_part + ((size_t)b * (gamma + 1) + i) * nseg;
@@ -93,35 +132,29 @@ verify_accept_kernel(const VerifyParams p) {
         for (int s = lane; s < nseg; s += 32) a = lsedraw_merge(a, part[s]);
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
-        if (lane == 0) s_lse[i] = a.m + logf(a.s);
+        if (lane == i) lse_mine = a.m + logf(a.s);
         if (i == Kb) bonus_idx = a.idx;
     }
-    __syncwarp();
-    if (lane != 0) return;
-    const TT* target = static_cast<const TT*>(p.target);
-    const uint32_t row0 = (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1);
-    int A = Kb, rej = -1;
-    for (int k = 1; k <= Kb; ++k) {
-        const size_t o = (size_t)b * gamma + (k - 1);
-        int x = p.draft_tok[o];
-        if (x < 0 || x >= V) { raise_status(p.ws.status, kBadToken); x = 0; }
-        const float t = load_scalar(target, ((size_t)b * (gamma + 1) + (k - 1)) * V + x) * p.inv_tau;
-        const float lp = t - s_lse[k - 1];
-        const float lq = p.z_tok[o] - p.lse_q[o];
-        if (p.p_tok) p.p_tok[o] = expf(lp);
+    bool reject = false, near = false;
+    if (walk) {
+        const float lp = t - lse_mine;
+        if (p.p_tok) p.p_tok[(size_t)b * gamma + lane] = expf(lp);
         const float thr = fminf(1.f, expf(lp - lq));
-        const float u = uniform_of(Stream(p.seed, p.step, 1u, row0 + (uint32_t)(k - 1)).word(0));
-        if (p.near_ties && fabsf(u - thr) < 1e-5f) atomicAdd(&p.near_ties[0], 1u);
-        if (!(u < thr)) { A = k - 1; rej = k - 1; break; }
+        reject = !(u < thr);
+        near = fabsf(u - thr) < 1e-5f;
     }
-    p.ws.acc[b] = A;
-    p.ws.rej[b] = rej;
-    p.ws.fin[b] = bonus_idx;
-    if (rej >= 0) {
-        const size_t o = (size_t)b * gamma + rej;
-        p.ws.lse_rej[b] = make_float2(s_lse[rej], p.lse_q[o]);
+    const unsigned rej_mask = __ballot_sync(0xffffffffu, reject);
+    const int rej = rej_mask ? __ffs(rej_mask) - 1 : -1;     // 0-based row of the first rejection
+    if (p.near_ties && near && (rej < 0 || lane <= rej)) atomicAdd(&p.near_ties[0], 1u);   // decisions taken
+    const float lse_rej = __shfl_sync(0xffffffffu, lse_mine, rej < 0 ? 0 : rej);
+    if (lane == 0) {
+        const int A = rej < 0 ? Kb : rej;
+        p.ws.acc[b] = A;
+        p.ws.rej[b] = rej;
+        p.ws.fin[b] = bonus_idx;
+        if (rej >= 0) p.ws.lse_rej[b] = make_float2(lse_rej, p.lse_q[(size_t)b * gamma + rej]);
+        p.accepted[b] = A;
     }
-    p.accepted[b] = A;
 }
 
 // ----------------------------------------------------------------- residual
@@ -330,7 +363,8 @@ verify_compact_kernel(const VerifyParams p) {
 
 template <typename TT>
 cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
-    const unsigned g1 = (unsigned)p.B * (unsigned)(p.gamma + 1) * (unsigned)p.ws.nseg;
+    const long long items = (long long)p.B * (p.gamma + 1) * p.ws.nseg;
+    const int g1 = (int)(items < 8LL * num_sms() ? items : 8LL * num_sms());
     verify_stream_kernel<TT><<<g1, kStreamThreads, 0, s>>>(p);
     verify_accept_kernel<TT><<<p.B, 32, 0, s>>>(p);
     const int nchunks = (p.B + kBC - 1) / kBC;
@@ -340,6 +374,12 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     gx = gx > p.ws.parts ? p.ws.parts : gx;
     const size_t smem = sizeof(float) * ((size_t)kBC * p.r + (size_t)kBC * (kTV + 4));
     const dim3 g2(gx, nchunks);
+    if (resid_rows_supported(p) && !getenv("DSPARK_RESID_SIMT")) {
+        const cudaError_t e = launch_resid_rows(p, s);
+        if (e != cudaSuccess) return e;
+        verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
 #define DSPARK_RES_LAUNCH(WT, UT)                                                                    \
     do {                                                                                             \
         auto kern = verify_residual_simt_kernel<WT, UT, TT>;                                         \
