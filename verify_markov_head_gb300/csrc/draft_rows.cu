@@ -273,30 +273,68 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
             if (!active) continue;
             const int v0 = t * kTN + 32 * cb;
             if constexpr (kResid) {
+                // The rejected rows differ per request, so the warp stages its 32
+                // rows of U and then of the target through a 4 KB shared buffer:
+                // coalesced loads (8 lanes per 128-byte row segment), 128-byte
+                // swizzle on the chunk index, then each lane reads its own row.
+                uint8_t* wbuf = gbase + L.u + (size_t)warp * 4096;
+                const unsigned real_mask = __ballot_sync(0xffffffffu, real);
+                float* z = bias;                           // z overwrites the bias in place
+                {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int rr = 4 * j + (lane >> 3), c = lane & 7;
+                        const float* src = reinterpret_cast<const float*>(
+                            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(Urow), rr));
+                        if ((real_mask >> rr) & 1u) {
+                            const int vq = v0 + 4 * c;
+                            const float4 x = (vq < V) ? __ldcs(reinterpret_cast<const float4*>(src + vq))
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                            *reinterpret_cast<float4*>(wbuf + rr * 128 + ((c ^ (rr & 7)) << 4)) = x;
+                        }
+                    }
+                    __syncwarp();
+                    if (real) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float4 u4 = *reinterpret_cast<const float4*>(wbuf + lane * 128 + ((c ^ (lane & 7)) << 4));
+                            z[4 * c] = (u4.x + bias[4 * c]) * p.inv_tau;
+                            z[4 * c + 1] = (u4.y + bias[4 * c + 1]) * p.inv_tau;
+                            z[4 * c + 2] = (u4.z + bias[4 * c + 2]) * p.inv_tau;
+                            z[4 * c + 3] = (u4.w + bias[4 * c + 3]) * p.inv_tau;
+                        }
+                    }
+                    __syncwarp();
+                }
+                {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int rr = 4 * j + (lane >> 3), c = lane & 7;
+                        const TT* src = reinterpret_cast<const TT*>(
+                            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(Trow), rr));
+                        if ((real_mask >> rr) & 1u) {
+                            const int vq = v0 + 4 * c;
+                            const float4 x = (vq < V) ? Vec4<TT>::load_stream(src + vq) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            *reinterpret_cast<float4*>(wbuf + rr * 128 + ((c ^ (rr & 7)) << 4)) = x;
+                        }
+                    }
+                    __syncwarp();
+                }
                 if (real) {
 #pragma unroll
-                  for (int half = 0; half < 2; ++half) {
-                    float4 u4[8], t4[8];
-#pragma unroll
-                    for (int c = 4 * half; c < 4 * half + 4; ++c) {
-                        const int vq = v0 + 4 * c;
-                        u4[c] = (vq < V) ? __ldcs(reinterpret_cast<const float4*>(Urow + vq)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        t4[c] = (vq < V) ? Vec4<TT>::load_stream(Trow + vq) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int c = 4 * half; c < 4 * half + 4; ++c) {
+                    for (int c = 0; c < 8; ++c) {
                         const int vq = v0 + 4 * c;
                         if (vq < V) {
-                            const float us[4] = {u4[c].x, u4[c].y, u4[c].z, u4[c].w};
-                            const float ts[4] = {t4[c].x, t4[c].y, t4[c].z, t4[c].w};
+                            const float4 t4 = *reinterpret_cast<const float4*>(wbuf + lane * 128 + ((c ^ (lane & 7)) << 4));
+                            const float ts[4] = {t4.x, t4.y, t4.z, t4.w};
                             const uint4 w = rng.quad((uint32_t)vq >> 2);
                             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float z = (us[e] + bias[4 * c + e]) * p.inv_tau;
+                                const float zz = z[4 * c + e];
                                 const float tv = ts[e] * p.inv_tau;
                                 const float g = gumbel_of(ws[e]);
-                                const float pr = expf(tv - lse.x) - expf(z - lse.y);
+                                const float pr = expf(tv - lse.x) - expf(zz - lse.y);
                                 const int idx = vq + e;
                                 if (pr > 0.f) {
                                     const float sc = logf(pr) + g;
@@ -307,8 +345,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                             }
                         }
                     }
-                  }
                 }
+                __syncwarp();
             } else {
                 const int n = lt * 4 + cb, s = n % US;
                 ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles);

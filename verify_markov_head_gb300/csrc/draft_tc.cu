@@ -80,15 +80,6 @@ struct TcArgs {
     DraftParams p;
 };
 
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(out) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
-    return out != 0;
-}
-
 template <int NC>
 __global__ void __launch_bounds__(kThreads, 1)
 draft_tc_kernel(const __grid_constant__ TcArgs a, const int k) {
@@ -272,7 +263,7 @@ draft_tc_kernel(const __grid_constant__ TcArgs a, const int k) {
                             p.logits_out[((size_t)b * gamma + (k - 1)) * V + v] = z;
                     }
                 }
-                if (bar_red_or(1, 128, !uok)) { failed = true; break; }
+                if (ptx::bar_red_or(1, 128, !uok)) { failed = true; break; }
                 // transposed pass: request row b_loc, entries seg*VPT .. +VPT
                 const int b = b_base + c * C::SC + b_loc;
                 if (b < p.B) {

@@ -20,84 +20,148 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace dspark {
 namespace {
 
-constexpr int kStreamThreads = 512;
-constexpr int kStreamVec = kVerifySeg / (4 * kStreamThreads);   // float4 loads per thread per item (4)
+constexpr int kStreamConsumers = 8;                        // consumer warps
+constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;  // + one producer warp
+constexpr int kStreamStages = 6;
+constexpr int kStreamStageBytes = kVerifySeg * 4;            // one fp32 segment (bf16 uses half)
+constexpr long long kStreamWaitCycles = 4000000000LL;        // ~2 s at 2 GHz
 
 template <typename T>
 __device__ __forceinline__ float load_scalar(const T* p, size_t i) { return to_f32(p[i]); }
 
-// Work item w = (b, i, seg) with seg fastest; rows i > K_b are skipped.  All
-// kStreamVec loads of an item are issued before any is used.
+// Persistent streaming pass over the target rows 0..K_b of every request.
+// Work item w = (b, i, seg), seg fastest; CTA c takes items c, c + grid, ...
+// and skips rows i > K_b (producer and consumers apply the same rule).  A
+// producer thread moves each 8192-entry segment into a 6-stage shared-memory
+// ring with one bulk copy (evict-first); 8 consumer warps fold it into an
+// online log-sum-exp (plus the bonus Gumbel-max draw on row K_b) and write
+// one partial per item.  All waits are bounded.
 template <typename TT>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, 1)
 verify_stream_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 127u) & ~127u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + kStreamStages * kStreamStageBytes;
+    auto full = [&](int i) { return bar0 + 8u * i; };
+    auto empty = [&](int i) { return bar0 + 8u * (kStreamStages + i); };
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages);
+    LseDraw* s_part = reinterpret_cast<LseDraw*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16);
+
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
     const int items = p.B * (gamma + 1) * nseg;
-    __shared__ LseDraw s_part[kStreamThreads / 32];
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    for (int w = blockIdx.x; w < items; w += gridDim.x) {
-        const int seg = w % nseg;
-        const int i = (w / nseg) % (gamma + 1);
-        const int b = w / (nseg * (gamma + 1));
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    if (tid == 0) {
+        for (int i = 0; i < kStreamStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), kStreamConsumers); }
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto decode = [&](int w, int& b, int& i, int& seg, bool& skip) {
+        seg = w % nseg;
+        i = (w / nseg) % (gamma + 1);
+        b = w / (nseg * (gamma + 1));
         int Kb = p.K[b];
-        if (Kb < 0 || Kb > gamma) {
-            if (seg == 0 && i == 0 && threadIdx.x == 0) raise_status(p.ws.status, kBadLength);
-            Kb = Kb < 0 ? 0 : gamma;
-        }
-        if (i > Kb) continue;                      // uniform over the CTA
-        const bool bonus = (i == Kb);
-        const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
-        const int v_beg = seg * kVerifySeg;
-        float4 x4[kStreamVec];
-#pragma unroll
-        for (int j = 0; j < kStreamVec; ++j) {
-            const int v = v_beg + 4 * (threadIdx.x + j * kStreamThreads);
-            x4[j] = (v < V) ? Vec4<TT>::load_stream(row + v) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
-        LseDraw st = lsedraw_empty();
-#pragma unroll
-        for (int j = 0; j < kStreamVec; ++j) {
-            const float xs[4] = {x4[j].x * p.inv_tau, x4[j].y * p.inv_tau, x4[j].z * p.inv_tau, x4[j].w * p.inv_tau};
-            const float mx = fmaxf(fmaxf(xs[0], xs[1]), fmaxf(xs[2], xs[3]));
-            if (mx > st.m) { st.s = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mx); st.m = mx; }
-            if (mx > -INFINITY) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) st.s += __expf(xs[e] - st.m);
+        if (Kb < 0 || Kb > gamma) Kb = Kb < 0 ? 0 : gamma;
+        skip = i > Kb;
+        return Kb;
+    };
+
+    if (warp == kStreamConsumers) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = ptx::policy_evict_first();
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x) {
+                int b, i, seg; bool skip;
+                decode(w, b, i, seg, skip);
+                if (skip) continue;
+                if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kStreamWaitCycles))) break;
+                const int v_beg = seg * kVerifySeg;
+                const int n = min(kVerifySeg, V - v_beg);
+                const uint32_t bytes = (uint32_t)(n * (int)sizeof(TT));
+                const TT* src = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V + v_beg;
+                ptx::mbar_arrive_expect_tx(full(stage), bytes);
+                ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes, src, bytes, full(stage), pol);
+                if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
             }
+            if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
         }
-        if (bonus) {
-            const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int ctid = tid;                            // 0 .. 255
+        int stage = 0;
+        uint32_t ph = 0;
+        for (int w = blockIdx.x; w < items; w += gridDim.x) {
+            int b, i, seg; bool skip;
+            const int Kb = decode(w, b, i, seg, skip);
+            if (p.K[b] < 0 || p.K[b] > gamma) {
+                if (seg == 0 && i == 0 && ctid == 0) raise_status(p.ws.status, kBadLength);
+            }
+            if (skip) continue;
+            bool ok = ptx::mbar_wait(full(stage), ph, abort_flag, kStreamWaitCycles);
+            ok = __all_sync(0xffffffffu, ok);
+            LseDraw st = lsedraw_empty();
+            if (ok) {
+                const bool bonus = (i == Kb);
+                const int v_beg = seg * kVerifySeg;
+                const int n = min(kVerifySeg, V - v_beg);
+                const TT* sbuf = reinterpret_cast<const TT*>(gbase + (size_t)stage * kStreamStageBytes);
+                const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
+#pragma unroll 4
+                for (int j = 0; j < kVerifySeg / (4 * 32 * kStreamConsumers); ++j) {
+                    const int e0 = 4 * (ctid + j * 32 * kStreamConsumers);
+                    if (e0 < n) {
+                        const float4 x4 = Vec4<TT>::load(sbuf + e0);
+                        const float xs[4] = {x4.x * p.inv_tau, x4.y * p.inv_tau, x4.z * p.inv_tau, x4.w * p.inv_tau};
+                        const float mx = fmaxf(fmaxf(xs[0], xs[1]), fmaxf(xs[2], xs[3]));
+                        if (mx > st.m) { st.s = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mx); st.m = mx; }
 #pragma unroll
-            for (int j = 0; j < kStreamVec; ++j) {
-                const int v = v_beg + 4 * (threadIdx.x + j * kStreamThreads);
-                if (v < V) {
-                    const uint4 wq = rng.quad((uint32_t)v >> 2);
-                    const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
-                    const float xs[4] = {x4[j].x * p.inv_tau, x4[j].y * p.inv_tau, x4[j].z * p.inv_tau, x4[j].w * p.inv_tau};
+                        for (int e = 0; e < 4; ++e) st.s += __expf(xs[e] - st.m);
+                        if (bonus) {
+                            const int v = v_beg + e0;
+                            const uint4 wq = rng.quad((uint32_t)v >> 2);
+                            const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float sc = xs[e] + gumbel_of(ws[e]);
-                        if (wins(sc, v + e, st.best, st.idx)) { st.best = sc; st.idx = v + e; }
+                            for (int e = 0; e < 4; ++e) {
+                                const float sc = xs[e] + gumbel_of(ws[e]);
+                                if (wins(sc, v + e, st.best, st.idx)) { st.best = sc; st.idx = v + e; }
+                            }
+                        }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(empty(stage));      // this warp is done with the stage
+#pragma unroll
+                for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
             }
-        }
+            if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
+            if (lane == 0) s_part[warp] = st;
+            // one barrier publishes s_part and makes a failed wait a group decision
+            if (ptx::bar_red_or(1, 32 * kStreamConsumers, !ok)) { *abort_flag = 1u; break; }
+            if (warp == 0) {
+                st = lane < kStreamConsumers ? s_part[lane] : lsedraw_empty();
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
-        if (lane == 0) s_part[warp] = st;
-        __syncthreads();
-        if (warp == 0) {
-            st = lane < kStreamThreads / 32 ? s_part[lane] : lsedraw_empty();
-#pragma unroll
-            for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
-            if (lane == 0) p.ws.verify_part[((size_t)b * (gamma + 1) + i) * nseg + seg] = st;
+                for (int m = 1; m < kStreamConsumers; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
+                if (lane == 0) p.ws.verify_part[((size_t)b * (gamma + 1) + i) * nseg + seg] = st;
+            }
+            ptx::named_barrier(1, 32 * kStreamConsumers);
         }
-        __syncthreads();
     }
+    if (*abort_flag) {
+        for (int i = 0; i < 64; ++i) __nanosleep(1000);   // let copies in flight land
+    }
+    __syncthreads();
 }
 
 // One warp per request: lse_p of rows 0..K_b from the segment partials, then
@@ -364,8 +428,12 @@ verify_compact_kernel(const VerifyParams p) {
 template <typename TT>
 cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     const long long items = (long long)p.B * (p.gamma + 1) * p.ws.nseg;
-    const int g1 = (int)(items < 8LL * num_sms() ? items : 8LL * num_sms());
-    verify_stream_kernel<TT><<<g1, kStreamThreads, 0, s>>>(p);
+    const int g1 = (int)(items < (long long)num_sms() ? items : (long long)num_sms());
+    const size_t smem1 = 128 + (size_t)kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16 +
+                         sizeof(LseDraw) * kStreamConsumers;
+    cudaError_t e1 = cudaFuncSetAttribute(verify_stream_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+    if (e1 != cudaSuccess) return e1;
+    verify_stream_kernel<TT><<<g1, kStreamThreads, smem1, s>>>(p);
     verify_accept_kernel<TT><<<p.B, 32, 0, s>>>(p);
     const int nchunks = (p.B + kBC - 1) / kBC;
     const int ntiles = (p.V + kTV - 1) / kTV;
