@@ -106,6 +106,8 @@ def test_tiny_workload_all_scheduler_modes(mode):
     (17, 1032, 128, torch.bfloat16),     # ragged request chunk
     (64, 4096, 256, torch.bfloat16),
     (130, 1024, 64, torch.bfloat16),
+    (32, 2056, 128, torch.bfloat16),     # 4 vocabulary tiles per accumulator, ragged tail
+    (40, 1032, 256, torch.bfloat16),     # 2 tiles per accumulator, partly filled rows
 ])
 def test_draft_parity(B, V, r, wdt):
     w = workload.custom("tiny", B=B, V=V, r=r, w_dtype=wdt, w_std=0.1, seed=B + V + r)
@@ -243,6 +245,8 @@ def _verify_case(w, seed, K=None, req_base=0):
     (7, 4104, 64, torch.bfloat16, torch.float32),
     (33, 2056, 128, torch.bfloat16, torch.bfloat16),
     (64, 1024, 256, torch.bfloat16, torch.float32),
+    (32, 1032, 128, torch.bfloat16, torch.bfloat16),
+    (130, 2048, 64, torch.bfloat16, torch.float32),
 ])
 def test_verify_parity(B, V, r, wdt, tdt):
     w = workload.custom("tiny", B=B, V=V, r=r, w_dtype=wdt, target_dtype=tdt, w_std=0.1, seed=B * 3 + r)

@@ -85,6 +85,14 @@ __device__ __forceinline__ float gumbel_of(uint32_t x) {
     return -kLn2 * __log2f(E);
 }
 
+// 2^x on the special-function unit (relative error about 2^-22, subnormal
+// results flushed to zero).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- merge states
 // Gumbel-max draw fused with a log-sum-exp: over a set of entries,
 //   best  = max (z_v + G_v), idx = its v (lowest v on ties), zb = z_idx,

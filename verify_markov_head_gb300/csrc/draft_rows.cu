@@ -7,13 +7,20 @@
 //   z[b, v]    = (U[b, k-1, v] + bias[b, v]) / tau
 //   x~_k       = argmax_v z + G,  lse_q = log sum exp z,  z_tok = z[x~_k]
 //
-// D[M = 128 request rows, N = 128 vocabulary entries] = h[M, K = r] * W2tile[K, N]:
+// D[M = 128 rows, N = 128 vocabulary entries] accumulates h * W2tile over K = r:
 //   A = the gathered rows h = W1[x~_{k-1}] (K-major, 128-byte swizzle, staged
 //       once per CTA; rows past the batch are zero),
 //   B = a 128-entry slice of W2 read by TMA straight from the [r, V] row-major
 //       tensor (MN-major, 128-byte swizzle), in 64-rank K-chunks,
 //   D = fp32 in TMEM, two buffers so the MMA of tile t+1 overlaps the
 //       epilogue of tile t.
+// A chunk of NC < 128 requests would leave TMEM lanes NC..127 (and the warps
+// that read them) idle, so the 128 lanes hold RF = 128 / NC vocabulary tiles
+// at once: the A operand is block diagonal, rows [i*NC, (i+1)*NC) carry h
+// against tile i and zeros elsewhere, so one accumulator takes RF tiles
+// through RF * r/64 K-chunk MMAs.  The zero blocks are shared: shared memory
+// holds Z^(RF-1) H_0 Z^(RF-1) H_1 ... H_last Z^(RF-1) and the window for
+// (tile i, K-chunk j) starts i blocks before H_j.
 // With the request on the TMEM lane, every epilogue thread owns one request
 // row and reads 32 consecutive vocabulary entries of it in one tcgen05.ld; the
 // matching U slice arrives by TMA (128-byte swizzle, so the 32 lanes of a warp
@@ -60,15 +67,18 @@ struct Layout {
     int uslots;
 };
 
+constexpr int kSlotBytes = 128 * 128;             // one U slice: 128 rows x 32 fp32
+
+// RF = 128 / NC vocabulary tiles per accumulator; the A region holds
+// (RF - 1) + RF * (r / 64) blocks of NC rows x 128 B.
 __host__ __device__ inline Layout rows_layout(int NC, int r) {
     Layout L;
+    const int RF = 128 / NC;
     L.b = 0;
     L.a = L.b + kStages * kBBytes;
-    L.u = L.a + (uint32_t)(r / 64) * 128u * 128u;            // 128 rows x 128 B per K-chunk
-    const int slot = NC * 128;                                // one [NC rows][32 fp32] U slice
-    L.uslots = kURingBytes / slot;
-    if (L.uslots > 16) L.uslots = 16;
-    L.merge = L.u + (uint32_t)(L.uslots * slot);
+    L.u = L.a + (uint32_t)((RF - 1) + RF * (r / 64)) * (uint32_t)NC * 128u;
+    L.uslots = kURingBytes / kSlotBytes;
+    L.merge = L.u + (uint32_t)(L.uslots * kSlotBytes);
     L.bar = L.merge + 4u * 128u * 16u;
     L.misc = L.bar + 8u * (2 * kStages + 2 * L.uslots + 5);
     L.misc = (L.misc + 15u) & ~15u;
@@ -97,8 +107,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     uint8_t* gbase = smem_raw + (base - raw);
     const Layout L = rows_layout(NC, p.r);
     const int KCH = p.r / 64;
+    const int RF = 128 / NC;                      // vocabulary tiles per accumulator
     const int US = L.uslots;
-    const uint32_t slot_bytes = (uint32_t)NC * 128u;
+    const uint32_t slot_bytes = (uint32_t)kSlotBytes;
+    const uint32_t blk = (uint32_t)NC * 128u;     // bytes of one A block
 
     const uint32_t bar0 = base + L.bar;
     auto full = [&](int i) { return bar0 + 8u * i; };
@@ -117,12 +129,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int chunk = blockIdx.y, b_base = chunk * NC;
     const int nb = min(NC, p.B - b_base);
-    const int nq = (nb + 31) / 32;                 // TMEM lane quarters holding requests
     const int V = p.V, gamma = p.gamma, r = p.r;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), 1); }
-        for (int i = 0; i < US; ++i) { ptx::mbar_init(ufull(i), 1); ptx::mbar_init(uempty(i), (uint32_t)nq); }
+        for (int i = 0; i < US; ++i) { ptx::mbar_init(ufull(i), 1); ptx::mbar_init(uempty(i), 4u); }
         for (int i = 0; i < 2; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0u;
@@ -148,18 +159,25 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
         s_row[n] = prow;
     }
     __syncthreads();
-    // A operand: h rows, K-major with 128-byte swizzle.  K-chunk j (64 ranks) is a
-    // [128 rows][128 B] block; 16-byte unit u of row n sits at unit u ^ (n mod 8).
+    // A operand: h rows, K-major with 128-byte swizzle.  Block H_j (K-chunk j,
+    // 64 ranks) is [NC rows][128 B] at block index (RF - 1) + j * RF; the other
+    // blocks are zero.  16-byte unit u of row n sits at unit u ^ (n mod 8).
     {
         const uint16_t* W1 = static_cast<const uint16_t*>(p.W1);
-        const int units = r / 8;
-        for (int idx = tid; idx < 128 * units; idx += kThreads) {
-            const int n = idx / units, u16 = idx - n * units;
-            const int j = u16 >> 3, u = u16 & 7;
+        const int nblocks = (RF - 1) + RF * KCH;
+        const int units = nblocks * NC * 8;
+        for (int idx = tid; idx < units; idx += kThreads) {
+            const int bi = idx / (NC * 8), rem = idx - bi * (NC * 8);
+            const int n = rem >> 3, uu = rem & 7;     // row in block, physical 16-byte unit
             uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            const int x = s_tok[n];
-            if (x >= 0) val = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)u16 * 8);
-            *reinterpret_cast<uint4*>(gbase + L.a + (size_t)j * 16384 + (size_t)n * 128 + ((u ^ (n & 7)) << 4)) = val;
+            const int rel = bi - (RF - 1);
+            if (rel >= 0 && rel % RF == 0) {
+                const int j = rel / RF;
+                const int u = uu ^ (n & 7);            // logical unit stored at this position
+                const int x = s_tok[n];
+                if (x >= 0) val = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)(j * 64 + u * 8));
+            }
+            *reinterpret_cast<uint4*>(gbase + L.a + (size_t)bi * blk + (size_t)n * 128 + (uu << 4)) = val;
         }
     }
     ptx::fence_proxy_async_smem();
@@ -167,7 +185,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int ntiles = (V + kTN - 1) / kTN;
+    const int ntiles = (V + kTN * RF - 1) / (kTN * RF);   // super-tiles of RF vocabulary tiles
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
@@ -178,22 +196,26 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
             bool ok = true;
             int lt = 0;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
-                const int v0 = t * kTN;
-                for (int j = 0; j < KCH; ++j) {
-                    if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kWaitCycles))) break;
-                    ptx::mbar_arrive_expect_tx(full(stage), kBBytes);
-                    const uint32_t dst = base + L.b + (uint32_t)stage * kBBytes;
-                    ptx::tma_load_2d(dst, &a.w2map, v0, j * 64, full(stage), pol_w);
-                    ptx::tma_load_2d(dst + kBBytes / 2, &a.w2map, v0 + 64, j * 64, full(stage), pol_w);
-                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                const int vs = t * kTN * RF;
+                for (int i = 0; i < RF && ok; ++i) {
+                    for (int j = 0; j < KCH; ++j) {
+                        if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kWaitCycles))) break;
+                        ptx::mbar_arrive_expect_tx(full(stage), kBBytes);
+                        const uint32_t dst = base + L.b + (uint32_t)stage * kBBytes;
+                        const int v0 = vs + i * kTN;
+                        ptx::tma_load_2d(dst, &a.w2map, v0, j * 64, full(stage), pol_w);
+                        ptx::tma_load_2d(dst + kBBytes / 2, &a.w2map, v0 + 64, j * 64, full(stage), pol_w);
+                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                    }
                 }
                 for (int c = 0; c < 4 && ok && !kResid; ++c) {
                     const int n = lt * 4 + c, s = n % US;
                     const uint32_t par = (uint32_t)((n / US) & 1);
                     if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) break;
                     ptx::mbar_arrive_expect_tx(ufull(s), slot_bytes);
-                    ptx::tma_load_3d(base + L.u + (uint32_t)s * slot_bytes, &a.umap, v0 + 32 * c, k - 1, b_base,
-                                     ufull(s), pol_u);
+                    for (int i = 0; i < RF; ++i)      // rows [i*NC, (i+1)*NC) hold tile i's U slice
+                        ptx::tma_load_3d(base + L.u + (uint32_t)s * slot_bytes + (uint32_t)i * blk, &a.umap,
+                                         vs + i * kTN + 32 * c, k - 1, b_base, ufull(s), pol_u);
                 }
             }
             if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
@@ -210,22 +232,25 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                 if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTN);
-                for (int j = 0; j < KCH; ++j) {
-                    if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) break;
-                    ptx::tc_fence_after();
-                    const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
-                    const uint32_t a_addr = base + L.a + (uint32_t)j * 16384u;
+                for (int i = 0; i < RF && ok; ++i) {
+                    for (int j = 0; j < KCH; ++j) {
+                        if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) break;
+                        ptx::tc_fence_after();
+                        const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
+                        // window of 128 rows whose block i is H_j
+                        const uint32_t a_addr = base + L.a + (uint32_t)((RF - 1) + j * RF - i) * blk;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // A: K-major rows of 128 B, 8-row groups 1 KB apart (SBO); 16 ranks = 32 B.
-                        const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                        // B: MN-major, 64-entry swizzle atoms 8 KB apart along N (LBO),
-                        //    8-rank groups 1 KB apart along K (SBO); 16 ranks = 2 KB.
-                        const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
-                        ptx::mma_f16(d_tmem, ad, bd, idesc, (j | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // A: K-major rows of 128 B, 8-row groups 1 KB apart (SBO); 16 ranks = 32 B.
+                            const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                            // B: MN-major, 64-entry swizzle atoms 8 KB apart along N (LBO),
+                            //    8-rank groups 1 KB apart along K (SBO); 16 ranks = 2 KB.
+                            const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
+                            ptx::mma_f16(d_tmem, ad, bd, idesc, (i | j | kk) != 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(empty(stage));
+                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
                     }
-                    ptx::mma_commit(empty(stage));
-                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 ptx::mma_commit(tfull(acc));
@@ -239,11 +264,12 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3, cb = warp >> 2;     // lane quarter, 32-column block of the tile
-        const int row = 32 * q + lane;              // request row within the chunk (TMEM lane)
-        const bool active = q < nq;
-        const int b = b_base + row;
-        const bool real = active && row < nb && (!kResid || s_row[row] >= 0);
-        const int urow = kResid ? (real ? s_row[row] : 0) : (k - 1);      // row of U (and of the target)
+        const int row = 32 * q + lane;              // TMEM lane
+        const int ti = row / NC, nrow = row % NC;   // vocabulary tile of the super-tile, request row
+        const bool active = (32 * q) % NC < nb;     // the warp's rows hold at least one request
+        const int b = b_base + nrow;
+        const bool real = active && nrow < nb && (!kResid || s_row[nrow] >= 0);
+        const int urow = kResid ? (real ? s_row[nrow] : 0) : (k - 1);     // row of U (and of the target)
         const Stream rng(p.seed, p.step, kResid ? 2u : 0u,
                          (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)urow);
         const size_t out_row = ((size_t)b * gamma + (k - 1)) * V;
@@ -270,8 +296,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty(acc));
             if (++acc == 2) { acc = 0; aph ^= 1u; }
-            if (!active) continue;
-            const int v0 = t * kTN + 32 * cb;
+            if (kResid && !active) continue;
+            const int v0 = t * kTN * RF + ti * kTN + 32 * cb;
             if constexpr (kResid) {
                 // The rejected rows differ per request, so the warp stages its 32
                 // rows of U and then of the target through a 4 KB shared buffer:
@@ -334,10 +360,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                                 const float zz = z[4 * c + e];
                                 const float tv = ts[e] * p.inv_tau;
                                 const float g = gumbel_of(ws[e]);
-                                const float pr = expf(tv - lse.x) - expf(zz - lse.y);
+                                const float pr = __expf(tv - lse.x) - __expf(zz - lse.y);
                                 const int idx = vq + e;
                                 if (pr > 0.f) {
-                                    const float sc = logf(pr) + g;
+                                    const float sc = __logf(pr) + g;
                                     if (wins(sc, idx, st2.best_r, st2.idx_r)) { st2.best_r = sc; st2.idx_r = idx; }
                                 }
                                 const float sp = tv + g;
@@ -398,18 +424,20 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, 256u);
     }
-    // fold the four column blocks of each request row
+    // fold the RF tiles x 4 column blocks of each request row
     if (tid < nb) {
         if constexpr (kResid) {
             const Draw2* m2 = reinterpret_cast<const Draw2*>(s_merge);
-            Draw2 s2 = m2[tid];
+            Draw2 s2 = draw2_empty();
+            for (int i = 0; i < RF; ++i)
 #pragma unroll
-            for (int cb = 1; cb < 4; ++cb) s2 = draw2_merge(s2, m2[cb * 128 + tid]);
+                for (int cb = 0; cb < 4; ++cb) s2 = draw2_merge(s2, m2[cb * 128 + i * NC + tid]);
             if (s_row[tid] >= 0) p.ws.resid_part[(size_t)(b_base + tid) * p.ws.parts + blockIdx.x] = s2;
         } else {
-            DrawLse s1 = s_merge[tid];
+            DrawLse s1 = drawlse_empty();
+            for (int i = 0; i < RF; ++i)
 #pragma unroll
-            for (int cb = 1; cb < 4; ++cb) s1 = drawlse_merge(s1, s_merge[cb * 128 + tid]);
+                for (int cb = 0; cb < 4; ++cb) s1 = drawlse_merge(s1, s_merge[cb * 128 + i * NC + tid]);
             p.ws.draft_part[(size_t)(b_base + tid) * p.ws.parts + blockIdx.x] = s1;
         }
     }
@@ -514,7 +542,7 @@ static cudaError_t launch_rows(const DraftParams& p, int k, bool resid, const vo
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nchunks = (p.B + a.NC - 1) / a.NC;
-    const int ntiles = (p.V + kTN - 1) / kTN;
+    const int ntiles = (p.V + kTN * (128 / a.NC) - 1) / (kTN * (128 / a.NC));
     int gx = num_sms() / nchunks;
     gx = gx < 1 ? 1 : gx;
     gx = gx > ntiles ? ntiles : gx;

@@ -16,7 +16,7 @@ struct Draw2;
 
 constexpr int kMaxParts = 1024;        // cap on partial states per request per launch
 constexpr int kPartTile = 128;         // vocabulary entries per tile of the partial-producing kernels
-constexpr int kVerifySeg = 8192;       // vocabulary entries per verify-stream work item
+constexpr int kVerifySeg = 32768;      // vocabulary entries per verify-stream work item
 constexpr int kChunk = 16;             // requests per chunk of the partial-producing kernels
 
 // Byte offsets of the workspace regions (all 256-byte aligned).

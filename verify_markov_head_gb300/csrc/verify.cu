@@ -27,22 +27,27 @@ namespace {
 
 constexpr int kStreamConsumers = 8;                        // consumer warps
 constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;  // + one producer warp
-constexpr int kStreamStages = 6;
-constexpr int kStreamStageBytes = kVerifySeg * 4;            // one fp32 segment (bf16 uses half)
+constexpr int kStreamStages = 3;
+constexpr int kChunk = 8192;                                 // entries per bulk copy
+constexpr int kStreamStageBytes = kChunk * 4;                // fp32 chunk (bf16 uses half)
+constexpr int kPerThread = kChunk / (32 * kStreamConsumers); // 32 entries per consumer per chunk
 constexpr long long kStreamWaitCycles = 4000000000LL;        // ~2 s at 2 GHz
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename T>
 __device__ __forceinline__ float load_scalar(const T* p, size_t i) { return to_f32(p[i]); }
 
 // Persistent streaming pass over the target rows 0..K_b of every request.
-// Work item w = (b, i, seg), seg fastest; CTA c takes items c, c + grid, ...
-// and skips rows i > K_b (producer and consumers apply the same rule).  A
-// producer thread moves each 8192-entry segment into a 6-stage shared-memory
-// ring with one bulk copy (evict-first); 8 consumer warps fold it into an
-// online log-sum-exp (plus the bonus Gumbel-max draw on row K_b) and write
-// one partial per item.  All waits are bounded.
+// Work item w = (b, i, seg), seg fastest, each a kVerifySeg-entry slice of a
+// row; CTA c takes items c, c + grid, ... and skips rows i > K_b (producer and
+// consumers apply the same rule).  A producer thread moves every 8192-entry
+// chunk of the item into a 3-stage shared-memory ring with one bulk copy
+// (evict-first); 8 consumer warps keep their running log-sum-exp in base-2
+// units across the chunks of the item: per chunk a max pass, one rescale, then
+// exp2 of x*log2e/tau - m in four independent partial sums.  The bonus row
+// i = K_b also takes the Gumbel-max draw (domain 3).  One partial per item.
 template <typename TT>
-__global__ void __launch_bounds__(kStreamThreads, 1)
+__global__ void __launch_bounds__(kStreamThreads, 2)
 verify_stream_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -64,14 +69,12 @@ verify_stream_kernel(const VerifyParams p) {
     }
     __syncthreads();
 
-    auto decode = [&](int w, int& b, int& i, int& seg, bool& skip) {
+    auto decode = [&](int w, int& b, int& i, int& seg) {
         seg = w % nseg;
         i = (w / nseg) % (gamma + 1);
         b = w / (nseg * (gamma + 1));
         int Kb = p.K[b];
-        if (Kb < 0 || Kb > gamma) Kb = Kb < 0 ? 0 : gamma;
-        skip = i > Kb;
-        return Kb;
+        return Kb < 0 ? 0 : (Kb > gamma ? gamma : Kb);
     };
 
     if (warp == kStreamConsumers) {
@@ -82,73 +85,102 @@ verify_stream_kernel(const VerifyParams p) {
             uint32_t ph = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x) {
-                int b, i, seg; bool skip;
-                decode(w, b, i, seg, skip);
-                if (skip) continue;
-                if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kStreamWaitCycles))) break;
-                const int v_beg = seg * kVerifySeg;
-                const int n = min(kVerifySeg, V - v_beg);
-                const uint32_t bytes = (uint32_t)(n * (int)sizeof(TT));
-                const TT* src = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V + v_beg;
-                ptx::mbar_arrive_expect_tx(full(stage), bytes);
-                ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes, src, bytes, full(stage), pol);
-                if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
+                int b, i, seg;
+                const int Kb = decode(w, b, i, seg);
+                if (i > Kb) continue;
+                const int v_end = min(V, (seg + 1) * kVerifySeg);
+                const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
+                for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kChunk) {
+                    if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kStreamWaitCycles))) break;
+                    const uint32_t bytes = (uint32_t)(min(kChunk, v_end - v0) * (int)sizeof(TT));
+                    ptx::mbar_arrive_expect_tx(full(stage), bytes);
+                    ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes, row + v0, bytes, full(stage), pol);
+                    if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
+                }
             }
             if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ consumers
-        const int ctid = tid;                            // 0 .. 255
+        const float scale = p.inv_tau * kLog2e;          // x * log2(e) / tau
         int stage = 0;
         uint32_t ph = 0;
-        for (int w = blockIdx.x; w < items; w += gridDim.x) {
-            int b, i, seg; bool skip;
-            const int Kb = decode(w, b, i, seg, skip);
-            if (p.K[b] < 0 || p.K[b] > gamma) {
-                if (seg == 0 && i == 0 && ctid == 0) raise_status(p.ws.status, kBadLength);
-            }
-            if (skip) continue;
-            bool ok = ptx::mbar_wait(full(stage), ph, abort_flag, kStreamWaitCycles);
-            ok = __all_sync(0xffffffffu, ok);
-            LseDraw st = lsedraw_empty();
-            if (ok) {
-                const bool bonus = (i == Kb);
-                const int v_beg = seg * kVerifySeg;
-                const int n = min(kVerifySeg, V - v_beg);
-                const TT* sbuf = reinterpret_cast<const TT*>(gbase + (size_t)stage * kStreamStageBytes);
-                const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
-#pragma unroll 4
-                for (int j = 0; j < kVerifySeg / (4 * 32 * kStreamConsumers); ++j) {
-                    const int e0 = 4 * (ctid + j * 32 * kStreamConsumers);
-                    if (e0 < n) {
-                        const float4 x4 = Vec4<TT>::load(sbuf + e0);
-                        const float xs[4] = {x4.x * p.inv_tau, x4.y * p.inv_tau, x4.z * p.inv_tau, x4.w * p.inv_tau};
-                        const float mx = fmaxf(fmaxf(xs[0], xs[1]), fmaxf(xs[2], xs[3]));
-                        if (mx > st.m) { st.s = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mx); st.m = mx; }
+        bool failed = false;
+        for (int w = blockIdx.x; w < items && !failed; w += gridDim.x) {
+            int b, i, seg;
+            const int Kb = decode(w, b, i, seg);
+            if (seg == 0 && i == 0 && tid == 0 && (p.K[b] < 0 || p.K[b] > gamma)) raise_status(p.ws.status, kBadLength);
+            if (i > Kb) continue;
+            const bool bonus = (i == Kb);
+            const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
+            const int v_end = min(V, (seg + 1) * kVerifySeg);
+            float m2 = -INFINITY;                        // running max of x*log2e/tau
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};          // sum of 2^(x*log2e/tau - m2), four chains
+            float best = -INFINITY;
+            int bidx = 0x7fffffff;
+            for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kChunk) {
+                bool ok = ptx::mbar_wait(full(stage), ph, abort_flag, kStreamWaitCycles);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    const int n = min(kChunk, v_end - v0);
+                    const TT* sbuf = reinterpret_cast<const TT*>(gbase + (size_t)stage * kStreamStageBytes);
+                    float x[kPerThread];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) st.s += __expf(xs[e] - st.m);
-                        if (bonus) {
-                            const int v = v_beg + e0;
-                            const uint4 wq = rng.quad((uint32_t)v >> 2);
-                            const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
+                    for (int j = 0; j < kPerThread / 4; ++j) {
+                        const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
+                        const float4 x4 = (e0 < n) ? Vec4<TT>::load(sbuf + e0)
+                                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                        x[4 * j] = x4.x * scale; x[4 * j + 1] = x4.y * scale;
+                        x[4 * j + 2] = x4.z * scale; x[4 * j + 3] = x4.w * scale;
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(empty(stage));     // the chunk is in registers
+                    float cm = x[0];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float sc = xs[e] + gumbel_of(ws[e]);
-                                if (wins(sc, v + e, st.best, st.idx)) { st.best = sc; st.idx = v + e; }
+                    for (int e = 1; e < kPerThread; ++e) cm = fmaxf(cm, x[e]);
+                    if (cm > m2) {
+                        const float r = fast_exp2(m2 - cm);      // 0 when m2 = -inf
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) s4[c] *= r;
+                        m2 = cm;
+                    }
+                    if (m2 > -INFINITY) {
+#pragma unroll
+                        for (int e = 0; e < kPerThread; ++e) s4[e & 3] += fast_exp2(x[e] - m2);
+                    }
+                    if (bonus) {
+#pragma unroll
+                        for (int j = 0; j < kPerThread / 4; ++j) {
+                            const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
+                            if (e0 < n) {
+                                const int v = v0 + e0;
+                                const uint4 wq = rng.quad((uint32_t)v >> 2);
+                                const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float sc = x[4 * j + e] * kLn2 + gumbel_of(ws[e]);   // x/tau + G
+                                    if (wins(sc, v + e, best, bidx)) { best = sc; bidx = v + e; }
+                                }
                             }
                         }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(empty(stage));      // this warp is done with the stage
-#pragma unroll
-                for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
+                if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
+                if (!ok) { failed = true; break; }
             }
-            if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
+            // the item's partial, in natural-log units
+            LseDraw st;
+            st.m = m2 * kLn2;
+            st.s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            st.best = best;
+            st.idx = bidx;
+            if (m2 == -INFINITY) { st.m = -INFINITY; st.s = 0.f; }
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
             if (lane == 0) s_part[warp] = st;
             // one barrier publishes s_part and makes a failed wait a group decision
-            if (ptx::bar_red_or(1, 32 * kStreamConsumers, !ok)) { *abort_flag = 1u; break; }
+            if (ptx::bar_red_or(1, 32 * kStreamConsumers, failed)) { *abort_flag = 1u; break; }
             if (warp == 0) {
                 st = lane < kStreamConsumers ? s_part[lane] : lsedraw_empty();
 #pragma unroll
@@ -428,7 +460,7 @@ verify_compact_kernel(const VerifyParams p) {
 template <typename TT>
 cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     const long long items = (long long)p.B * (p.gamma + 1) * p.ws.nseg;
-    const int g1 = (int)(items < (long long)num_sms() ? items : (long long)num_sms());
+    const int g1 = (int)(items < 2LL * num_sms() ? items : 2LL * num_sms());
     const size_t smem1 = 128 + (size_t)kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16 +
                          sizeof(LseDraw) * kStreamConsumers;
     cudaError_t e1 = cudaFuncSetAttribute(verify_stream_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
