@@ -85,6 +85,27 @@ __device__ __forceinline__ float gumbel_of(uint32_t x) {
     return -kLn2 * __log2f(E);
 }
 
+// The same variate in base-2 units, for kernels that keep their scores as
+// z*log2(e):  G2 = log2(e) * G + log2(ln 2) = -log2(E2), E2 = -log2(u).
+// argmax_v (z_v*log2e + G2_v) is argmax_v (z_v + G_v): the map is monotone.
+// E2 takes the series of -ln(1 - w) times log2(e) (coefficients log2(e)/n)
+// for w = 1 - u < 1/8 and the hardware log2 elsewhere, as in gumbel_of.
+constexpr float kLog2ofLn2 = -0.52876637294640327f;   // log2(ln 2)
+__device__ __forceinline__ float gumbel2_of(uint32_t x) {
+    const float u = uniform_of(x);
+    const float w = one_minus_uniform_of(x);
+    const float e_log = -__log2f(u);
+    float poly = fmaf(w, 0.18033688011112042f, 0.20609929155556619f);   // log2e/8, log2e/7
+    poly = fmaf(w, poly, 0.24044917348149389f);                          // log2e/6
+    poly = fmaf(w, poly, 0.28853900817779268f);                          // log2e/5
+    poly = fmaf(w, poly, 0.36067376022224085f);                          // log2e/4
+    poly = fmaf(w, poly, 0.48089834696298783f);                          // log2e/3
+    poly = fmaf(w, poly, 0.72134752044448170f);                          // log2e/2
+    poly = fmaf(w, poly, 1.4426950408889634f);                           // log2e
+    const float E2 = (w < 0.125f) ? w * poly : e_log;
+    return -__log2f(E2);
+}
+
 // 2^x on the special-function unit (relative error about 2^-22, subnormal
 // results flushed to zero).
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -279,6 +279,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
         if (kResid && real) lse = p.ws.lse_rej[b];
         DrawLse st = drawlse_empty();
         Draw2 st2 = draw2_empty();
+        const float scale2 = p.inv_tau * 1.4426950408889634f;      // z -> z * log2(e)
         int acc = 0;
         uint32_t aph = 0;
         int lt = 0;
@@ -379,29 +380,32 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 if (real) {
+                    // scores in base-2 units: z2 = z*log2e, G2 = log2e*G + log2(ln 2)
                     const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const int vq = v0 + 4 * c;
                         if (vq < V) {
                             const float4 u4 = *reinterpret_cast<const float4*>(srow + ((c ^ (row & 7)) << 4));
-                            const float zs[4] = {(u4.x + bias[4 * c]) * p.inv_tau, (u4.y + bias[4 * c + 1]) * p.inv_tau,
-                                                 (u4.z + bias[4 * c + 2]) * p.inv_tau, (u4.w + bias[4 * c + 3]) * p.inv_tau};
+                            const float us[4] = {u4.x + bias[4 * c], u4.y + bias[4 * c + 1],
+                                                 u4.z + bias[4 * c + 2], u4.w + bias[4 * c + 3]};
                             if (p.logits_out)
-                                *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(zs[0], zs[1], zs[2], zs[3]);
+                                *reinterpret_cast<float4*>(p.logits_out + out_row + vq) =
+                                    make_float4(us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
                             const uint4 w = rng.quad((uint32_t)vq >> 2);
                             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float sc = zs[e] + gumbel_of(ws[e]);
+                                const float z2 = us[e] * scale2;
+                                const float sc = z2 + gumbel2_of(ws[e]);
                                 const int idx = vq + e;
                                 // an empty state has best = -inf and s = 0, so the first
-                                // entry takes the first branch with exp(-inf) = 0
+                                // entry takes the first branch with 2^-inf = 0
                                 if (wins(sc, idx, st.best, st.idx)) {
-                                    st.s = st.s * __expf(st.best - sc) + __expf(zs[e] - sc);
-                                    st.best = sc; st.idx = idx; st.zb = zs[e];
+                                    st.s = st.s * fast_exp2(st.best - sc) + fast_exp2(z2 - sc);
+                                    st.best = sc; st.idx = idx; st.zb = us[e];
                                 } else {
-                                    st.s += __expf(zs[e] - st.best);
+                                    st.s += fast_exp2(z2 - st.best);
                                 }
                             }
                         }
@@ -411,8 +415,18 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                 if (lane == 0) ptx::mbar_arrive(uempty(s));
             }
         }
-        if constexpr (kResid) reinterpret_cast<Draw2*>(s_merge)[cb * 128 + row] = st2;
-        else s_merge[cb * 128 + row] = st;
+        if constexpr (kResid) {
+            reinterpret_cast<Draw2*>(s_merge)[cb * 128 + row] = st2;
+        } else {
+            // back to natural-log units: best = (best2 - log2(ln 2)) * ln 2, s = s2 * ln 2
+            DrawLse sn = st;
+            if (st.best > -INFINITY) {
+                sn.best = (st.best - kLog2ofLn2) * kLn2;
+                sn.s = st.s * kLn2;
+                sn.zb = st.zb * p.inv_tau;
+            }
+            s_merge[cb * 128 + row] = sn;
+        }
     }
 
     if (*abort_flag) {

@@ -28,9 +28,9 @@ namespace {
 constexpr int kStreamConsumers = 8;                        // consumer warps
 constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;  // + one producer warp
 constexpr int kStreamStages = 3;
-constexpr int kChunk = 8192;                                 // entries per bulk copy
-constexpr int kStreamStageBytes = kChunk * 4;                // fp32 chunk (bf16 uses half)
-constexpr int kPerThread = kChunk / (32 * kStreamConsumers); // 32 entries per consumer per chunk
+constexpr int kStreamChunk = 8192;                           // entries per bulk copy
+constexpr int kStreamStageBytes = kStreamChunk * 4;          // fp32 chunk (bf16 uses half)
+constexpr int kPerThread = kStreamChunk / (32 * kStreamConsumers);   // 32 entries per consumer per chunk
 constexpr long long kStreamWaitCycles = 4000000000LL;        // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -90,9 +90,9 @@ verify_stream_kernel(const VerifyParams p) {
                 if (i > Kb) continue;
                 const int v_end = min(V, (seg + 1) * kVerifySeg);
                 const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
-                for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kChunk) {
+                for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kStreamChunk) {
                     if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kStreamWaitCycles))) break;
-                    const uint32_t bytes = (uint32_t)(min(kChunk, v_end - v0) * (int)sizeof(TT));
+                    const uint32_t bytes = (uint32_t)(min(kStreamChunk, v_end - v0) * (int)sizeof(TT));
                     ptx::mbar_arrive_expect_tx(full(stage), bytes);
                     ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes, row + v0, bytes, full(stage), pol);
                     if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
@@ -119,11 +119,11 @@ verify_stream_kernel(const VerifyParams p) {
             float s4[4] = {0.f, 0.f, 0.f, 0.f};          // sum of 2^(x*log2e/tau - m2), four chains
             float best = -INFINITY;
             int bidx = 0x7fffffff;
-            for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kChunk) {
+            for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kStreamChunk) {
                 bool ok = ptx::mbar_wait(full(stage), ph, abort_flag, kStreamWaitCycles);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
-                    const int n = min(kChunk, v_end - v0);
+                    const int n = min(kStreamChunk, v_end - v0);
                     const TT* sbuf = reinterpret_cast<const TT*>(gbase + (size_t)stage * kStreamStageBytes);
                     float x[kPerThread];
 #pragma unroll
@@ -255,7 +255,7 @@ verify_accept_kernel(const VerifyParams p) {
 
 // ----------------------------------------------------------------- residual
 constexpr int kTV = 128;
-constexpr int kBC = kChunk;
+constexpr int kBC = dspark::kChunk;   // requests per residual chunk
 constexpr int kResThreads = 256;
 
 template <typename WT, typename UT, typename TT>
