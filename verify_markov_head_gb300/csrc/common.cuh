@@ -48,6 +48,32 @@ struct Stream {
     }
 };
 
+// The same stream with the ten round keys computed once, for loops that draw
+// many quads of one row.
+struct StreamRK {
+    uint32_t rk0[10], rk1[10];
+    uint32_t row, step_lo, dom_hi;
+    __device__ __forceinline__ StreamRK(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row_)
+        : row(row_), step_lo((uint32_t)step), dom_hi(domain + 4u * (uint32_t)(step >> 32)) {
+        uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+        for (int i = 0; i < 10; ++i) {
+            rk0[i] = k0; rk1[i] = k1;
+            k0 += Philox::kW0; k1 += Philox::kW1;
+        }
+    }
+    __device__ __forceinline__ uint4 quad(uint32_t q) const {
+        uint4 c = make_uint4(q, row, step_lo, dom_hi);
+#pragma unroll
+        for (int i = 0; i < 10; ++i) {
+            const uint32_t hi0 = __umulhi(Philox::kM0, c.x), lo0 = Philox::kM0 * c.x;
+            const uint32_t hi1 = __umulhi(Philox::kM1, c.z), lo1 = Philox::kM1 * c.z;
+            c = make_uint4(hi1 ^ c.y ^ rk0[i], lo1, hi0 ^ c.w ^ rk1[i], lo0);
+        }
+        return c;
+    }
+};
+
 // u = (2*(x >> 9) + 1) * 2^-24, exact in binary32, strictly inside (0, 1):
 // with j = x >> 9, the float 1 + j*2^-23 (exponent 127, mantissa j) minus
 // 1 - 2^-24 is exactly (2j + 1) * 2^-24.

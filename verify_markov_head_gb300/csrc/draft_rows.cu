@@ -270,8 +270,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
         const int b = b_base + nrow;
         const bool real = active && nrow < nb && (!kResid || s_row[nrow] >= 0);
         const int urow = kResid ? (real ? s_row[nrow] : 0) : (k - 1);     // row of U (and of the target)
-        const Stream rng(p.seed, p.step, kResid ? 2u : 0u,
-                         (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)urow);
+        const StreamRK rng(p.seed, p.step, kResid ? 2u : 0u,
+                           (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)urow);
         const size_t out_row = ((size_t)b * gamma + (k - 1)) * V;
         const float* Urow = static_cast<const float*>(p.U) + ((size_t)b * gamma + urow) * V;
         const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + urow) * V;
@@ -399,9 +399,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                                 const float z2 = us[e] * scale2;
                                 const float sc = z2 + gumbel2_of(ws[e]);
                                 const int idx = vq + e;
-                                // an empty state has best = -inf and s = 0, so the first
-                                // entry takes the first branch with 2^-inf = 0
-                                if (wins(sc, idx, st.best, st.idx)) {
+                                // A thread meets its entries in increasing v, so a strict
+                                // comparison keeps the lowest index on exact ties.  An empty
+                                // state has best = -inf and s = 0: the first entry takes the
+                                // first branch with 2^-inf = 0.
+                                if (sc > st.best) {
                                     st.s = st.s * fast_exp2(st.best - sc) + fast_exp2(z2 - sc);
                                     st.best = sc; st.idx = idx; st.zb = us[e];
                                 } else {

@@ -125,20 +125,20 @@ verify_stream_kernel(const VerifyParams p) {
                 if (ok) {
                     const int n = min(kStreamChunk, v_end - v0);
                     const TT* sbuf = reinterpret_cast<const TT*>(gbase + (size_t)stage * kStreamStageBytes);
-                    float x[kPerThread];
+                    float x[kPerThread];                  // raw target logits
 #pragma unroll
                     for (int j = 0; j < kPerThread / 4; ++j) {
                         const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
                         const float4 x4 = (e0 < n) ? Vec4<TT>::load(sbuf + e0)
                                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                        x[4 * j] = x4.x * scale; x[4 * j + 1] = x4.y * scale;
-                        x[4 * j + 2] = x4.z * scale; x[4 * j + 3] = x4.w * scale;
+                        x[4 * j] = x4.x; x[4 * j + 1] = x4.y; x[4 * j + 2] = x4.z; x[4 * j + 3] = x4.w;
                     }
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(empty(stage));     // the chunk is in registers
                     float cm = x[0];
 #pragma unroll
                     for (int e = 1; e < kPerThread; ++e) cm = fmaxf(cm, x[e]);
+                    cm *= scale;                              // scale > 0 keeps the maximum
                     if (cm > m2) {
                         const float r = fast_exp2(m2 - cm);      // 0 when m2 = -inf
 #pragma unroll
@@ -147,7 +147,7 @@ verify_stream_kernel(const VerifyParams p) {
                     }
                     if (m2 > -INFINITY) {
 #pragma unroll
-                        for (int e = 0; e < kPerThread; ++e) s4[e & 3] += fast_exp2(x[e] - m2);
+                        for (int e = 0; e < kPerThread; ++e) s4[e & 3] += fast_exp2(fmaf(x[e], scale, -m2));
                     }
                     if (bonus) {
 #pragma unroll
@@ -159,7 +159,7 @@ verify_stream_kernel(const VerifyParams p) {
                                 const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const float sc = x[4 * j + e] * kLn2 + gumbel_of(ws[e]);   // x/tau + G
+                                    const float sc = x[4 * j + e] * p.inv_tau + gumbel_of(ws[e]);   // x/tau + G
                                     if (wins(sc, v + e, best, bidx)) { best = sc; bidx = v + e; }
                                 }
                             }
