@@ -86,6 +86,14 @@ __device__ __forceinline__ float one_minus_uniform_of(uint32_t x) {
     return __uint_as_float((~x >> 9) | 0x3f800000u) - kOneMinusHalfUlp;
 }
 
+// log2(x) on the special-function unit, flush-to-zero form (the arguments
+// here are normal numbers >= 2^-24, so no subnormal fix-up is needed).
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Standard Gumbel variate G = -ln(E), E = -ln(u).
 //   E: for u <= 7/8, -ln2 * log2(u) with the hardware log2 (absolute error
 //      <= 2^-22 on [1/2, 2], 2 ulp elsewhere, so E keeps ~1e-6 relative
@@ -99,7 +107,7 @@ constexpr float kLn2 = 0.69314718055994531f;
 __device__ __forceinline__ float gumbel_of(uint32_t x) {
     const float u = uniform_of(x);
     const float w = one_minus_uniform_of(x);
-    const float e_log = -kLn2 * __log2f(u);
+    const float e_log = -kLn2 * fast_log2(u);
     float poly = fmaf(w, 0.125f, 0.142857143f);
     poly = fmaf(w, poly, 0.166666667f);
     poly = fmaf(w, poly, 0.2f);
@@ -108,7 +116,7 @@ __device__ __forceinline__ float gumbel_of(uint32_t x) {
     poly = fmaf(w, poly, 0.5f);
     poly = fmaf(w, poly, 1.0f);
     const float E = (w < 0.125f) ? w * poly : e_log;
-    return -kLn2 * __log2f(E);
+    return -kLn2 * fast_log2(E);
 }
 
 // The same variate in base-2 units, for kernels that keep their scores as
@@ -120,7 +128,7 @@ constexpr float kLog2ofLn2 = -0.52876637294640327f;   // log2(ln 2)
 __device__ __forceinline__ float gumbel2_of(uint32_t x) {
     const float u = uniform_of(x);
     const float w = one_minus_uniform_of(x);
-    const float e_log = -__log2f(u);
+    const float e_log = -fast_log2(u);
     float poly = fmaf(w, 0.18033688011112042f, 0.20609929155556619f);   // log2e/8, log2e/7
     poly = fmaf(w, poly, 0.24044917348149389f);                          // log2e/6
     poly = fmaf(w, poly, 0.28853900817779268f);                          // log2e/5
@@ -129,7 +137,7 @@ __device__ __forceinline__ float gumbel2_of(uint32_t x) {
     poly = fmaf(w, poly, 0.72134752044448170f);                          // log2e/2
     poly = fmaf(w, poly, 1.4426950408889634f);                           // log2e
     const float E2 = (w < 0.125f) ? w * poly : e_log;
-    return -__log2f(E2);
+    return -fast_log2(E2);
 }
 
 // 2^x on the special-function unit (relative error about 2^-22, subnormal
