@@ -182,6 +182,36 @@ dspark_status dspark_verify(
     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The draft loop of dspark_draft_markov for callers that cannot allocate
+ * device memory -- for example code inside a framework that owns all device
+ * allocations, or a latency-critical loop that must not enter an allocator
+ * (cudaMalloc may take locks and synchronise the device).  Arguments and
+ * results are those of dspark_draft_markov without the workspace: the
+ * kernels' scratch (status word, arrival counters, partial states) lives in
+ * a fixed array inside the library, 4 MiB + 64 KiB per GPU, held until the
+ * process exits.  No counterpart on the pages: it is a deployment option.
+ *   - Sizes whose scratch exceeds the array (B * ceil(V/128) partial states
+ *     of 16 bytes plus counters, e.g. beyond B = 256 at V = 131072) return
+ *     DSPARK_ERR_UNSUPPORTED with a message on stderr.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array and clears its counters
+ *     first: calls that may overlap on the GPU (different streams, or
+ *     concurrent host threads) race and must be serialised by the caller.
+ *   - Device-side range checks set bits in the array's status word, which
+ *     this entry point does not report.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ */
+dspark_status dspark_draft_markov_noalloc(
+    const void* U, dspark_dtype U_t,
+    const void* W1, const void* W2, dspark_dtype W_t,
+    const int32_t* anchor,
+    int B, int gamma, int V, int r, int req_base, float tau,
+    uint64_t seed, uint64_t step,
+    int32_t* draft_tok, float* lse_q, float* z_tok, float* logits_out,
+    void* stream);
+
+/*
  * Diagnostics: the random stream as the kernels draw it.  For columns
  * v = 0..n-1 of stream (seed, step, domain, row) writes the uniform
  * u = (2*(x div 2^9) + 1) * 2^-24 and the Gumbel variate G = -log(-log u) the

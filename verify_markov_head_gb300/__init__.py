@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "dspark_gumbel_stream", "Workspace", "StepBuffers", "run_step", "run_step_host",
+    "dspark_schedule", "dspark_verify", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
@@ -54,6 +54,9 @@ _lib.dspark_verify.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _v
                                _i, _i, _i, _i, _i, _f, _u64, _u64,
                                _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.dspark_verify.restype = _i
+_lib.dspark_draft_markov_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
+                                             _vp, _vp, _vp, _vp, _vp]
+_lib.dspark_draft_markov_noalloc.restype = _i
 _lib.dspark_gumbel_stream.argtypes = [_u64, _u64, C.c_uint32, C.c_uint32, _i, _vp, _vp, _vp]
 _lib.dspark_gumbel_stream.restype = _i
 
@@ -181,6 +184,19 @@ def dspark_verify(target, U, W1, W2, anchor, draft_tok, lse_q, z_tok, K, accepte
         _p(lse_q), _p(z_tok), _p(K), B, gamma, V, r, req_base, float(tau), int(seed), int(step),
         _p(accepted), _p(out_tok), _p(out_req), _p(out_pos), _p(out_off), _p(next_anchor),
         _p(p_tok), _p(near_ties), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def dspark_draft_markov_noalloc(U, W1, W2, anchor, draft_tok, lse_q, z_tok, *, tau=1.0, seed=0, step=0,
+                                req_base=0, logits_out=None, stream=None):
+    """dspark_draft_markov without a workspace, for callers that cannot
+    allocate device memory: the library keeps the scratch in a fixed array."""
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if W1.shape != (V, r) or W2.shape != (r, V) or W1.dtype != W2.dtype:
+        raise ValueError("W1 [V,r] and W2 [r,V] must share a dtype")
+    _check("dspark_draft_markov_noalloc", _lib.dspark_draft_markov_noalloc(
+        _p(U), _dt(U), _p(W1), _p(W2), _dt(W1), _p(anchor), B, gamma, V, r, req_base, float(tau),
+        int(seed), int(step), _p(draft_tok), _p(lse_q), _p(z_tok), _p(logits_out), _stream(stream)))
 
 
 def dspark_gumbel_stream(seed, step, domain, row, n, gumbel_out=None, uniform_out=None, stream=None):
