@@ -394,3 +394,16 @@ def test_device_random_stream_matches_definition():
         # the extreme tail (1 - u < 2^-10), where the winners come from
         tail = gu > 1 - 2.0 ** -10
         assert tail.sum() > 100 and err[tail].max() < 3e-6
+
+
+def test_draft_single_launch_matches_per_position_launches(monkeypatch):
+    """All positions in one cooperative launch give the same drafts as one
+    launch per position."""
+    w = workload.custom("tiny", B=96, V=4104, r=256, w_dtype=torch.bfloat16, w_std=0.1, seed=31)
+    inp = workload.inputs(w, device=DEV)
+    a = _draft_gpu(inp, w.B, w.gamma, w.V, w.r, seed=5, step=1)
+    monkeypatch.setenv("DSPARK_DRAFT_PER_POSITION", "1")
+    b = _draft_gpu(inp, w.B, w.gamma, w.V, w.r, seed=5, step=1)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_allclose(a[1], b[1], atol=LOGIT_ATOL, rtol=0)
+    np.testing.assert_allclose(a[2], b[2], atol=LOGIT_ATOL, rtol=0)

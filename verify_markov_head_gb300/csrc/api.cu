@@ -33,7 +33,8 @@ WsLayout ws_layout(int B, int gamma, int V) {
     const size_t nchunks = ((size_t)B + kChunk - 1) / kChunk;
     L.status = o;      o = align256(o + 16);
     L.tickets = o;     o = align256(o + sizeof(uint32_t) * 2 * nchunks);
-    L.draft_part = o;  o = align256(o + sizeof(DrawLse) * (size_t)B * L.parts);
+    L.gbar = o;        o = align256(o + sizeof(uint32_t) * (kGridBarrierSlots + 1));
+    L.draft_part = o;  o = align256(o + sizeof(DrawLse) * 2 * (size_t)B * L.parts);
     L.verify_part = o; o = align256(o + sizeof(LseDraw) * (size_t)B * (gamma + 1) * L.nseg);
     L.rej = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
     L.acc = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
@@ -51,6 +52,7 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     P.status = reinterpret_cast<uint32_t*>(base + L.status);
     P.tickets_draft = reinterpret_cast<uint32_t*>(base + L.tickets);
     P.tickets_resid = P.tickets_draft + ((size_t)B + kChunk - 1) / kChunk;
+    P.gbar = reinterpret_cast<uint32_t*>(base + L.gbar);
     P.draft_part = reinterpret_cast<DrawLse*>(base + L.draft_part);
     P.verify_part = reinterpret_cast<LseDraw*>(base + L.verify_part);
     P.rej = reinterpret_cast<int32_t*>(base + L.rej);
@@ -163,12 +165,7 @@ dspark_status dspark_draft_markov(const void* U, dspark_dtype U_t, const void* W
     p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.logits_out = logits_out;
     p.ws = ws_ptrs(ws, B, gamma, V);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool tc = draft_tc_supported(p);
-    for (int k = 1; k <= gamma; ++k) {
-        const cudaError_t e = tc ? launch_draft_tc(p, k, s) : launch_draft_simt(p, k, s);
-        if (e != cudaSuccess) return launch_status(e);
-    }
-    return DSPARK_OK;
+    return launch_status(launch_draft(p, s));
 }
 
 dspark_status dspark_confidence_sts(const float* h, int d, const void* emb, dspark_dtype emb_t, int e,

@@ -21,10 +21,10 @@
 namespace dspark {
 namespace {
 
-// Fixed scratch: 4 MiB + 64 KiB covers the draft's status word, arrival
-// counters and partial states for B * ceil(V/128) <= 262144 (for example
-// B = 64 with V up to 131072 * 4, or B = 256 with V = 131072).
-constexpr size_t kStaticScratchBytes = (size_t)4 * 1024 * 1024 + 64 * 1024;
+// Fixed scratch: 8 MiB + 64 KiB covers the draft's status word, counters
+// and two buffers of partial states for B * min(1024, ceil(V/128)) <= 262144
+// (for example B = 256 with V up to 131072, or B = 64 at any V).
+constexpr size_t kStaticScratchBytes = (size_t)8 * 1024 * 1024 + 64 * 1024;
 static __device__ __align__(256) unsigned char g_draft_scratch[kStaticScratchBytes];
 
 // The array's device address on each device, looked up once with that
@@ -100,13 +100,10 @@ extern "C" dspark_status dspark_draft_markov_noalloc(
     p.seed = seed; p.step = step;
     p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.logits_out = logits_out;
     p.ws = ws_ptrs(ws, B, gamma, V);
-    const bool tc = draft_tc_supported(p);
-    for (int k = 1; k <= gamma; ++k) {
-        e = tc ? launch_draft_tc(p, k, s) : launch_draft_simt(p, k, s);
-        if (e != cudaSuccess) {
-            fprintf(stderr, "dspark_draft_markov_noalloc: launch failed: %s\n", cudaGetErrorString(e));
-            return DSPARK_ERR_CUDA;
-        }
+    e = launch_draft(p, s);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "dspark_draft_markov_noalloc: launch failed: %s\n", cudaGetErrorString(e));
+        return DSPARK_ERR_CUDA;
     }
     return DSPARK_OK;
 }

@@ -80,7 +80,7 @@ __host__ __device__ inline Layout rows_layout(int NC, int r) {
     L.uslots = kURingBytes / kSlotBytes;
     L.merge = L.u + (uint32_t)(L.uslots * kSlotBytes);
     L.bar = L.merge + 4u * 128u * 16u;
-    L.misc = L.bar + 8u * (2 * kStages + 2 * L.uslots + 5);
+    L.misc = L.bar + 8u * (2 * kStages + 2 * L.uslots + 6);
     L.misc = (L.misc + 15u) & ~15u;
     L.total = L.misc + 16u + 8u * 128u;
     return L;
@@ -96,9 +96,63 @@ struct RowsArgs {
     uint32_t* near_ties;
 };
 
+// Bounded grid-wide barrier on a counter in global memory: every CTA adds 1,
+// then waits until all `target` CTAs have.  The kernel is launched
+// cooperatively, so all CTAs are resident.  Returns false on expiry or abort.
+__device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target, const volatile uint32_t* abort,
+                                             long long limit_cycles) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) break;
+        if (*abort) return false;
+        if (clock64() - t0 > limit_cycles) return false;
+        __nanosleep(100);
+    }
+    __threadfence();
+    return true;
+}
+
+// h rows -> A operand (K-major, 128-byte swizzle).  Block H_j (K-chunk j, 64
+// ranks) is [NC rows][128 B] at block index (RF - 1) + j * RF; the zero
+// blocks between them are written only when with_zero_blocks is set.
+// 16-byte unit u of row n sits at unit u ^ (n mod 8).
+__device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC, int RF,
+                                        int KCH, int r, int t0, int nthreads, bool with_zero_blocks) {
+    const uint32_t blk = (uint32_t)NC * 128u;
+    const int nblocks = (RF - 1) + RF * KCH;
+    const int units = nblocks * NC * 8;
+    for (int idx = t0; idx < units; idx += nthreads) {
+        const int bi = idx / (NC * 8), rem = idx - bi * (NC * 8);
+        const int rel = bi - (RF - 1);
+        const bool h_block = rel >= 0 && rel % RF == 0;
+        if (!h_block && !with_zero_blocks) continue;
+        const int n = rem >> 3, uu = rem & 7;     // row in block, physical 16-byte unit
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (h_block) {
+            const int j = rel / RF;
+            const int u = uu ^ (n & 7);            // logical unit stored at this position
+            const int x = s_tok[n];
+            if (x >= 0) val = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)(j * 64 + u * 8));
+        }
+        *reinterpret_cast<uint4*>(a_region + (size_t)bi * blk + (size_t)n * 128 + (uu << 4)) = val;
+    }
+}
+
+// Positions k_first..k_last in one launch.  With more than one position the
+// launch is cooperative: after each position every CTA publishes its partial
+// states, waits at a grid barrier, merges the partials of its own requests
+// (every CTA of a chunk does the same merge, so no second barrier is needed),
+// stages h = W1[x~_k] for the next position and releases the MMA issuer.  The
+// TMA producer never stops at the boundaries: W2 and the next position's U
+// do not depend on the drawn tokens.  Partial states alternate between two
+// buffers so a fast CTA never overwrites the ones a slow CTA still merges.
 template <bool kResid, typename TT>
 __global__ void __launch_bounds__(kThreads, 1)
-rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
+rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_last) {
     const DraftParams& p = a.p;
     const int NC = a.NC;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -111,6 +165,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     const int US = L.uslots;
     const uint32_t slot_bytes = (uint32_t)kSlotBytes;
     const uint32_t blk = (uint32_t)NC * 128u;     // bytes of one A block
+    const bool persistent = k_last > k_first;
 
     const uint32_t bar0 = base + L.bar;
     auto full = [&](int i) { return bar0 + 8u * i; };
@@ -120,29 +175,33 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     auto tfull = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + i); };
     auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + 2 + i); };
     const uint32_t drain = bar0 + 8u * (2 * kStages + 2 * US + 4);
+    const uint32_t a_ready = bar0 + 8u * (2 * kStages + 2 * US + 5);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L.misc);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 4);
     volatile uint32_t* never = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 8);
     int* s_tok = reinterpret_cast<int*>(gbase + L.misc + 16);
+    int* s_row = s_tok + 128;                       // residual mode: rejected row per request, or -1
     DrawLse* s_merge = reinterpret_cast<DrawLse*>(gbase + L.merge);   // [4 column blocks][128 rows]
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int chunk = blockIdx.y, b_base = chunk * NC;
     const int nb = min(NC, p.B - b_base);
     const int V = p.V, gamma = p.gamma, r = p.r;
+    const uint16_t* W1 = static_cast<const uint16_t*>(p.W1);
+    const uint32_t nctas = gridDim.x * gridDim.y;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), 1); }
         for (int i = 0; i < US; ++i) { ptx::mbar_init(ufull(i), 1); ptx::mbar_init(uempty(i), 4u); }
         for (int i = 0; i < 2; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
         ptx::mbar_init(drain, 1);
+        ptx::mbar_init(a_ready, 1);
         *abort_flag = 0u;
         *never = 0u;
         ptx::fence_mbar_init();
     }
     if (tid == kProducerWarp * 32) { ptx::prefetch_tmap(&a.w2map); ptx::prefetch_tmap(&a.umap); }
     if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 256u); ptx::tmem_relinquish(); }
-    int* s_row = s_tok + 128;                       // residual mode: rejected row per request, or -1
     for (int n = tid; n < 128; n += kThreads) {
         int x = -1, prow = -1;
         if (n < nb) {
@@ -151,7 +210,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                 prow = __ldcg(&p.ws.rej[b]);
                 if (prow >= 0) x = (prow == 0) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (prow - 1)];
             } else {
-                x = (k == 1) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (k - 2)];
+                x = (k_first == 1) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (k_first - 2)];
             }
             if (x >= V || (x < 0 && !kResid)) { raise_status(p.ws.status, kBadToken); x = -1; }
         }
@@ -159,27 +218,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
         s_row[n] = prow;
     }
     __syncthreads();
-    // A operand: h rows, K-major with 128-byte swizzle.  Block H_j (K-chunk j,
-    // 64 ranks) is [NC rows][128 B] at block index (RF - 1) + j * RF; the other
-    // blocks are zero.  16-byte unit u of row n sits at unit u ^ (n mod 8).
-    {
-        const uint16_t* W1 = static_cast<const uint16_t*>(p.W1);
-        const int nblocks = (RF - 1) + RF * KCH;
-        const int units = nblocks * NC * 8;
-        for (int idx = tid; idx < units; idx += kThreads) {
-            const int bi = idx / (NC * 8), rem = idx - bi * (NC * 8);
-            const int n = rem >> 3, uu = rem & 7;     // row in block, physical 16-byte unit
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            const int rel = bi - (RF - 1);
-            if (rel >= 0 && rel % RF == 0) {
-                const int j = rel / RF;
-                const int u = uu ^ (n & 7);            // logical unit stored at this position
-                const int x = s_tok[n];
-                if (x >= 0) val = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)(j * 64 + u * 8));
-            }
-            *reinterpret_cast<uint4*>(gbase + L.a + (size_t)bi * blk + (size_t)n * 128 + (uu << 4)) = val;
-        }
-    }
+    stage_h(gbase + L.a, W1, s_tok, NC, RF, KCH, r, tid, kThreads, true);
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
@@ -194,28 +233,30 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
-            int lt = 0;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
-                const int vs = t * kTN * RF;
-                for (int i = 0; i < RF && ok; ++i) {
-                    for (int j = 0; j < KCH; ++j) {
-                        if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kWaitCycles))) break;
-                        ptx::mbar_arrive_expect_tx(full(stage), kBBytes);
-                        const uint32_t dst = base + L.b + (uint32_t)stage * kBBytes;
-                        const int v0 = vs + i * kTN;
-                        ptx::tma_load_2d(dst, &a.w2map, v0, j * 64, full(stage), pol_w);
-                        ptx::tma_load_2d(dst + kBBytes / 2, &a.w2map, v0 + 64, j * 64, full(stage), pol_w);
-                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
+            int lt = 0;                                  // U slices issued / 4, over all positions
+            for (int k = k_first; k <= k_last && ok; ++k) {
+                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+                    const int vs = t * kTN * RF;
+                    for (int i = 0; i < RF && ok; ++i) {
+                        for (int j = 0; j < KCH; ++j) {
+                            if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kWaitCycles))) break;
+                            ptx::mbar_arrive_expect_tx(full(stage), kBBytes);
+                            const uint32_t dst = base + L.b + (uint32_t)stage * kBBytes;
+                            const int v0 = vs + i * kTN;
+                            ptx::tma_load_2d(dst, &a.w2map, v0, j * 64, full(stage), pol_w);
+                            ptx::tma_load_2d(dst + kBBytes / 2, &a.w2map, v0 + 64, j * 64, full(stage), pol_w);
+                            if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                        }
                     }
-                }
-                for (int c = 0; c < 4 && ok && !kResid; ++c) {
-                    const int n = lt * 4 + c, s = n % US;
-                    const uint32_t par = (uint32_t)((n / US) & 1);
-                    if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) break;
-                    ptx::mbar_arrive_expect_tx(ufull(s), slot_bytes);
-                    for (int i = 0; i < RF; ++i)      // rows [i*NC, (i+1)*NC) hold tile i's U slice
-                        ptx::tma_load_3d(base + L.u + (uint32_t)s * slot_bytes + (uint32_t)i * blk, &a.umap,
-                                         vs + i * kTN + 32 * c, k - 1, b_base, ufull(s), pol_u);
+                    for (int c = 0; c < 4 && ok && !kResid; ++c) {
+                        const int n = lt * 4 + c, s = n % US;
+                        const uint32_t par = (uint32_t)((n / US) & 1);
+                        if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) break;
+                        ptx::mbar_arrive_expect_tx(ufull(s), slot_bytes);
+                        for (int i = 0; i < RF; ++i)      // rows [i*NC, (i+1)*NC) hold tile i's U slice
+                            ptx::tma_load_3d(base + L.u + (uint32_t)s * slot_bytes + (uint32_t)i * blk, &a.umap,
+                                             vs + i * kTN + 32 * c, k - 1, b_base, ufull(s), pol_u);
+                    }
                 }
             }
             if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
@@ -228,33 +269,38 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
             int stage = 0, acc = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) break;
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTN);
-                for (int i = 0; i < RF && ok; ++i) {
-                    for (int j = 0; j < KCH; ++j) {
-                        if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) break;
-                        ptx::tc_fence_after();
-                        const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
-                        // window of 128 rows whose block i is H_j
-                        const uint32_t a_addr = base + L.a + (uint32_t)((RF - 1) + j * RF - i) * blk;
+            for (int k = k_first; k <= k_last && ok; ++k) {
+                if (k > k_first &&   // h of this position staged by the epilogue warps
+                    !(ok = ptx::mbar_wait(a_ready, (uint32_t)((k - k_first - 1) & 1), abort_flag, kWaitCycles)))
+                    break;
+                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                    if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) break;
+                    ptx::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTN);
+                    for (int i = 0; i < RF && ok; ++i) {
+                        for (int j = 0; j < KCH; ++j) {
+                            if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) break;
+                            ptx::tc_fence_after();
+                            const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
+                            // window of 128 rows whose block i is H_j
+                            const uint32_t a_addr = base + L.a + (uint32_t)((RF - 1) + j * RF - i) * blk;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            // A: K-major rows of 128 B, 8-row groups 1 KB apart (SBO); 16 ranks = 32 B.
-                            const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                            // B: MN-major, 64-entry swizzle atoms 8 KB apart along N (LBO),
-                            //    8-rank groups 1 KB apart along K (SBO); 16 ranks = 2 KB.
-                            const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
-                            ptx::mma_f16(d_tmem, ad, bd, idesc, (i | j | kk) != 0 ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk) {
+                                // A: K-major rows of 128 B, 8-row groups 1 KB apart (SBO); 16 ranks = 32 B.
+                                const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                                // B: MN-major, 64-entry swizzle atoms 8 KB apart along N (LBO),
+                                //    8-rank groups 1 KB apart along K (SBO); 16 ranks = 2 KB.
+                                const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
+                                ptx::mma_f16(d_tmem, ad, bd, idesc, (i | j | kk) != 0 ? 1u : 0u);
+                            }
+                            ptx::mma_commit(empty(stage));
+                            if (++stage == kStages) { stage = 0; ph ^= 1u; }
                         }
-                        ptx::mma_commit(empty(stage));
-                        if (++stage == kStages) { stage = 0; ph ^= 1u; }
                     }
+                    if (!ok) break;
+                    ptx::mma_commit(tfull(acc));
+                    if (++acc == 2) { acc = 0; aph ^= 1u; }
                 }
-                if (!ok) break;
-                ptx::mma_commit(tfull(acc));
-                if (++acc == 2) { acc = 0; aph ^= 1u; }
             }
             if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
             ptx::mma_commit(drain);                 // every MMA above completes before TMEM is freed
@@ -263,51 +309,52 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        const int etid = tid;                       // 0 .. 511
         const int q = warp & 3, cb = warp >> 2;     // lane quarter, 32-column block of the tile
         const int row = 32 * q + lane;              // TMEM lane
         const int ti = row / NC, nrow = row % NC;   // vocabulary tile of the super-tile, request row
         const bool active = (32 * q) % NC < nb;     // the warp's rows hold at least one request
         const int b = b_base + nrow;
         const bool real = active && nrow < nb && (!kResid || s_row[nrow] >= 0);
-        const int urow = kResid ? (real ? s_row[nrow] : 0) : (k - 1);     // row of U (and of the target)
-        const StreamRK rng(p.seed, p.step, kResid ? 2u : 0u,
-                           (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)urow);
-        const size_t out_row = ((size_t)b * gamma + (k - 1)) * V;
-        const float* Urow = static_cast<const float*>(p.U) + ((size_t)b * gamma + urow) * V;
-        const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + urow) * V;
-        float2 lse = make_float2(0.f, 0.f);
-        if (kResid && real) lse = p.ws.lse_rej[b];
-        DrawLse st = drawlse_empty();
-        Draw2 st2 = draw2_empty();
         const float scale2 = p.inv_tau * 1.4426950408889634f;      // z -> z * log2(e)
-        int acc = 0;
+        int acc = 0, lt = 0;
         uint32_t aph = 0;
-        int lt = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
-            bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            float bias[32];
-            if (active) {
-                ptx::tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kTN + 32 * cb), bias);
-                ptx::tmem_wait_ld();
-            }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(tempty(acc));
-            if (++acc == 2) { acc = 0; aph ^= 1u; }
-            if (kResid && !active) continue;
-            const int v0 = t * kTN * RF + ti * kTN + 32 * cb;
-            if constexpr (kResid) {
-                // The rejected rows differ per request, so the warp stages its 32
-                // rows of U and then of the target through a 4 KB shared buffer:
-                // coalesced loads (8 lanes per 128-byte row segment), 128-byte
-                // swizzle on the chunk index, then each lane reads its own row.
-                uint8_t* wbuf = gbase + L.u + (size_t)warp * 4096;
-                const unsigned real_mask = __ballot_sync(0xffffffffu, real);
-                float* z = bias;                           // z overwrites the bias in place
-                {
+        bool failed = false;
+        for (int k = k_first; k <= k_last && !failed; ++k) {
+            const int urow = kResid ? (real ? s_row[nrow] : 0) : (k - 1);     // row of U (and of the target)
+            const StreamRK rng(p.seed, p.step, kResid ? 2u : 0u,
+                               (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)urow);
+            const size_t out_row = ((size_t)b * gamma + (k - 1)) * V;
+            const float* Urow = static_cast<const float*>(p.U) + ((size_t)b * gamma + urow) * V;
+            const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + urow) * V;
+            float2 lse = make_float2(0.f, 0.f);
+            if (kResid && real) lse = p.ws.lse_rej[b];
+            DrawLse st = drawlse_empty();
+            Draw2 st2 = draw2_empty();
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+                bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) { failed = true; break; }
+                ptx::tc_fence_after();
+                float bias[32];
+                if (active) {
+                    ptx::tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kTN + 32 * cb), bias);
+                    ptx::tmem_wait_ld();
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(tempty(acc));
+                if (++acc == 2) { acc = 0; aph ^= 1u; }
+                if (kResid && !active) continue;
+                const int v0 = t * kTN * RF + ti * kTN + 32 * cb;
+                if constexpr (kResid) {
+                    // The rejected rows differ per request, so the warp stages its 32
+                    // rows of U and then of the target through a 4 KB shared buffer:
+                    // coalesced loads (8 lanes per 128-byte row segment), 128-byte
+                    // swizzle on the chunk index, then each lane reads its own row.
+                    uint8_t* wbuf = gbase + L.u + (size_t)warp * 4096;
+                    const unsigned real_mask = __ballot_sync(0xffffffffu, real);
+                    float* z = bias;                           // z overwrites the bias in place
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int rr = 4 * j + (lane >> 3), c = lane & 7;
@@ -332,8 +379,6 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                         }
                     }
                     __syncwarp();
-                }
-                {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int rr = 4 * j + (lane >> 3), c = lane & 7;
@@ -346,89 +391,152 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                         }
                     }
                     __syncwarp();
-                }
-                if (real) {
+                    if (real) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const int vq = v0 + 4 * c;
-                        if (vq < V) {
-                            const float4 t4 = *reinterpret_cast<const float4*>(wbuf + lane * 128 + ((c ^ (lane & 7)) << 4));
-                            const float ts[4] = {t4.x, t4.y, t4.z, t4.w};
-                            const uint4 w = rng.quad((uint32_t)vq >> 2);
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                        for (int c = 0; c < 8; ++c) {
+                            const int vq = v0 + 4 * c;
+                            if (vq < V) {
+                                const float4 t4 = *reinterpret_cast<const float4*>(wbuf + lane * 128 + ((c ^ (lane & 7)) << 4));
+                                const float ts[4] = {t4.x, t4.y, t4.z, t4.w};
+                                const uint4 w = rng.quad((uint32_t)vq >> 2);
+                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float zz = z[4 * c + e];
-                                const float tv = ts[e] * p.inv_tau;
-                                const float g = gumbel_of(ws[e]);
-                                const float pr = __expf(tv - lse.x) - __expf(zz - lse.y);
-                                const int idx = vq + e;
-                                if (pr > 0.f) {
-                                    const float sc = __logf(pr) + g;
-                                    if (wins(sc, idx, st2.best_r, st2.idx_r)) { st2.best_r = sc; st2.idx_r = idx; }
+                                for (int e = 0; e < 4; ++e) {
+                                    const float zz = z[4 * c + e];
+                                    const float tv = ts[e] * p.inv_tau;
+                                    const float g = gumbel_of(ws[e]);
+                                    const float pr = __expf(tv - lse.x) - __expf(zz - lse.y);
+                                    const int idx = vq + e;
+                                    if (pr > 0.f) {
+                                        const float sc = __logf(pr) + g;
+                                        if (wins(sc, idx, st2.best_r, st2.idx_r)) { st2.best_r = sc; st2.idx_r = idx; }
+                                    }
+                                    const float sp = tv + g;
+                                    if (wins(sp, idx, st2.best_p, st2.idx_p)) { st2.best_p = sp; st2.idx_p = idx; }
                                 }
-                                const float sp = tv + g;
-                                if (wins(sp, idx, st2.best_p, st2.idx_p)) { st2.best_p = sp; st2.idx_p = idx; }
                             }
                         }
                     }
+                    __syncwarp();
+                } else {
+                    const int n = lt * 4 + cb, s = n % US;
+                    ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) { failed = true; break; }
+                    if (real) {
+                        // scores in base-2 units: z2 = z*log2e, G2 = log2e*G + log2(ln 2)
+                        const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int vq = v0 + 4 * c;
+                            if (vq < V) {
+                                const float4 u4 = *reinterpret_cast<const float4*>(srow + ((c ^ (row & 7)) << 4));
+                                const float us[4] = {u4.x + bias[4 * c], u4.y + bias[4 * c + 1],
+                                                     u4.z + bias[4 * c + 2], u4.w + bias[4 * c + 3]};
+                                if (p.logits_out)
+                                    *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(
+                                        us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
+                                const uint4 w = rng.quad((uint32_t)vq >> 2);
+                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float z2 = us[e] * scale2;
+                                    const float sc = z2 + gumbel2_of(ws[e]);
+                                    const int idx = vq + e;
+                                    // A thread meets its entries in increasing v, so a strict
+                                    // comparison keeps the lowest index on exact ties.  An empty
+                                    // state has best = -inf and s = 0: the first entry takes the
+                                    // first branch with 2^-inf = 0.
+                                    if (sc > st.best) {
+                                        st.s = st.s * fast_exp2(st.best - sc) + fast_exp2(z2 - sc);
+                                        st.best = sc; st.idx = idx; st.zb = us[e];
+                                    } else {
+                                        st.s += fast_exp2(z2 - st.best);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(uempty(s));
                 }
-                __syncwarp();
+            }
+            // ---- this position's partial state per request: fold RF tiles x 4 column blocks
+            if constexpr (kResid) {
+                reinterpret_cast<Draw2*>(s_merge)[cb * 128 + row] = st2;
             } else {
-                const int n = lt * 4 + cb, s = n % US;
-                ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                if (real) {
-                    // scores in base-2 units: z2 = z*log2e, G2 = log2e*G + log2(ln 2)
-                    const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
+                // back to natural-log units: best = (best2 - log2(ln 2)) * ln 2, s = s2 * ln 2
+                DrawLse sn = st;
+                if (st.best > -INFINITY) {
+                    sn.best = (st.best - kLog2ofLn2) * kLn2;
+                    sn.s = st.s * kLn2;
+                    sn.zb = st.zb * p.inv_tau;
+                }
+                s_merge[cb * 128 + row] = sn;
+            }
+            // one barrier publishes s_merge and makes a failure a group decision
+            if (ptx::bar_red_or(1, 32 * kEpiWarps, failed)) { failed = true; *abort_flag = 1u; break; }
+            DrawLse* part_buf = p.ws.draft_part + (size_t)((k - 1) & 1) * p.B * p.ws.parts;
+            if (etid < nb) {
+                if constexpr (kResid) {
+                    const Draw2* m2 = reinterpret_cast<const Draw2*>(s_merge);
+                    Draw2 s2 = draw2_empty();
+                    for (int i = 0; i < RF; ++i)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const int vq = v0 + 4 * c;
-                        if (vq < V) {
-                            const float4 u4 = *reinterpret_cast<const float4*>(srow + ((c ^ (row & 7)) << 4));
-                            const float us[4] = {u4.x + bias[4 * c], u4.y + bias[4 * c + 1],
-                                                 u4.z + bias[4 * c + 2], u4.w + bias[4 * c + 3]};
-                            if (p.logits_out)
-                                *reinterpret_cast<float4*>(p.logits_out + out_row + vq) =
-                                    make_float4(us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
-                            const uint4 w = rng.quad((uint32_t)vq >> 2);
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                        for (int c = 0; c < 4; ++c) s2 = draw2_merge(s2, m2[c * 128 + i * NC + etid]);
+                    if (s_row[etid] >= 0) p.ws.resid_part[(size_t)(b_base + etid) * p.ws.parts + blockIdx.x] = s2;
+                } else {
+                    DrawLse s1 = drawlse_empty();
+                    for (int i = 0; i < RF; ++i)
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float z2 = us[e] * scale2;
-                                const float sc = z2 + gumbel2_of(ws[e]);
-                                const int idx = vq + e;
-                                // A thread meets its entries in increasing v, so a strict
-                                // comparison keeps the lowest index on exact ties.  An empty
-                                // state has best = -inf and s = 0: the first entry takes the
-                                // first branch with 2^-inf = 0.
-                                if (sc > st.best) {
-                                    st.s = st.s * fast_exp2(st.best - sc) + fast_exp2(z2 - sc);
-                                    st.best = sc; st.idx = idx; st.zb = us[e];
-                                } else {
-                                    st.s += fast_exp2(z2 - st.best);
-                                }
-                            }
-                        }
+                        for (int c = 0; c < 4; ++c) s1 = drawlse_merge(s1, s_merge[c * 128 + i * NC + etid]);
+                    part_buf[(size_t)(b_base + etid) * p.ws.parts + blockIdx.x] = s1;
+                }
+                __threadfence();
+            }
+            if (!persistent) break;
+            // ---- grid barrier, then every CTA merges the partials of its own requests
+            ptx::named_barrier(1, 32 * kEpiWarps);
+            __shared__ int s_gb_ok;
+            if (etid == 0) s_gb_ok = grid_barrier(p.ws.gbar + (k - k_first), nctas, abort_flag, kWaitCycles) ? 1 : 0;
+            ptx::named_barrier(1, 32 * kEpiWarps);
+            if (!s_gb_ok) {
+                if (etid == 0) raise_status(p.ws.status, kTimeout);
+                failed = true;
+                *abort_flag = 1u;
+                break;
+            }
+            for (int n = warp; n < nb; n += kEpiWarps) {
+                const DrawLse* part = part_buf + (size_t)(b_base + n) * p.ws.parts;
+                DrawLse m = drawlse_empty();
+                for (int i = lane; i < (int)gridDim.x; i += 32) {
+                    DrawLse c;
+                    c.best = __ldcg(&part[i].best); c.idx = __ldcg(&part[i].idx);
+                    c.zb = __ldcg(&part[i].zb); c.s = __ldcg(&part[i].s);
+                    m = drawlse_merge(m, c);
+                }
+#pragma unroll
+                for (int sh = 1; sh < 32; sh <<= 1) m = drawlse_merge(m, shfl_xor(m, sh));
+                if (lane == 0) {
+                    s_tok[n] = m.idx;
+                    if (blockIdx.x == 0) {
+                        const size_t o = (size_t)(b_base + n) * gamma + (k - 1);
+                        p.draft_tok[o] = m.idx;
+                        p.lse_q[o] = m.best + logf(m.s);
+                        p.z_tok[o] = m.zb;
                     }
                 }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(uempty(s));
             }
+            if (k == k_last) break;
+            ptx::named_barrier(1, 32 * kEpiWarps);
+            // ---- h = W1[x~_k] for the next position (the MMA of this one is complete:
+            //      its last commit released the final tile the warps just read)
+            stage_h(gbase + L.a, W1, s_tok, NC, RF, KCH, r, etid, 32 * kEpiWarps, false);
+            ptx::fence_proxy_async_smem();
+            ptx::named_barrier(1, 32 * kEpiWarps);
+            if (etid == 0) ptx::mbar_arrive(a_ready);
         }
-        if constexpr (kResid) {
-            reinterpret_cast<Draw2*>(s_merge)[cb * 128 + row] = st2;
-        } else {
-            // back to natural-log units: best = (best2 - log2(ln 2)) * ln 2, s = s2 * ln 2
-            DrawLse sn = st;
-            if (st.best > -INFINITY) {
-                sn.best = (st.best - kLog2ofLn2) * kLn2;
-                sn.s = st.s * kLn2;
-                sn.zb = st.zb * p.inv_tau;
-            }
-            s_merge[cb * 128 + row] = sn;
-        }
+        if (failed) *abort_flag = 1u;
     }
 
     if (*abort_flag) {
@@ -440,25 +548,21 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, 256u);
     }
-    // fold the RF tiles x 4 column blocks of each request row
-    if (tid < nb) {
-        if constexpr (kResid) {
-            const Draw2* m2 = reinterpret_cast<const Draw2*>(s_merge);
-            Draw2 s2 = draw2_empty();
-            for (int i = 0; i < RF; ++i)
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) s2 = draw2_merge(s2, m2[cb * 128 + i * NC + tid]);
-            if (s_row[tid] >= 0) p.ws.resid_part[(size_t)(b_base + tid) * p.ws.parts + blockIdx.x] = s2;
-        } else {
-            DrawLse s1 = drawlse_empty();
-            for (int i = 0; i < RF; ++i)
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) s1 = drawlse_merge(s1, s_merge[cb * 128 + i * NC + tid]);
-            p.ws.draft_part[(size_t)(b_base + tid) * p.ws.parts + blockIdx.x] = s1;
+
+    if (persistent) {
+        // the last CTA out clears the barrier counters for the next call
+        if (tid == 0) {
+            __threadfence();
+            const unsigned prev = atomicAdd(p.ws.gbar + kGridBarrierSlots, 1u);
+            if (prev == nctas - 1) {
+                for (int i = 0; i <= kGridBarrierSlots; ++i) p.ws.gbar[i] = 0u;
+                __threadfence();
+            }
         }
+        return;
     }
 
-    // last-arriving CTA of this request chunk merges the partial states
+    // single position: the last-arriving CTA of this request chunk merges the partial states
     uint32_t* ticket = kResid ? &p.ws.tickets_resid[chunk] : &p.ws.tickets_draft[chunk];
     __shared__ int s_last;
     __threadfence();
@@ -470,6 +574,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    const int k = k_first;
     for (int n = warp; n < nb; n += kThreads / 32) {
         const int bb = b_base + n;
         if constexpr (kResid) {
@@ -493,7 +598,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k) {
                 }
             }
         } else {
-            const DrawLse* part = p.ws.draft_part + (size_t)bb * p.ws.parts;
+            const DrawLse* part = p.ws.draft_part + (size_t)((k - 1) & 1) * p.B * p.ws.parts + (size_t)bb * p.ws.parts;
             DrawLse m = drawlse_empty();
             for (int i = lane; i < (int)gridDim.x; i += 32) {
                 DrawLse c;
@@ -523,8 +628,20 @@ bool rows_supported(const DraftParams& p) {
 
 bool draft_rows_supported(const DraftParams& p) { return rows_supported(p); }
 
-static cudaError_t launch_rows(const DraftParams& p, int k, bool resid, const void* target, bool target_bf16,
-                               uint32_t* near_ties, cudaStream_t s) {
+bool cooperative_supported() {
+    static int cached[64] = {0};     // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev);
+        cached[dev] = v ? 1 : 2;
+    }
+    return cached[dev] == 1;
+}
+
+static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bool resid, const void* target,
+                               bool target_bf16, uint32_t* near_ties, cudaStream_t s) {
     auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
     if (!enc) return cudaErrorNotSupported;
     RowsArgs a;
@@ -563,12 +680,18 @@ static cudaError_t launch_rows(const DraftParams& p, int k, bool resid, const vo
     gx = gx < 1 ? 1 : gx;
     gx = gx > ntiles ? ntiles : gx;
     gx = gx > p.ws.parts ? p.ws.parts : gx;
-    kern<<<dim3(gx, nchunks), kThreads, smem, s>>>(a, k);
+    const dim3 grid(gx, nchunks);
+    if (k_last > k_first) {
+        // every CTA waits for all others between positions: they must be co-resident
+        void* args[] = {&a, const_cast<int*>(&k_first), const_cast<int*>(&k_last)};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), args, smem, s);
+    }
+    kern<<<grid, kThreads, smem, s>>>(a, k_first, k_last);
     return cudaGetLastError();
 }
 
-cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s) {
-    return launch_rows(p, k, false, nullptr, false, nullptr, s);
+cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cudaStream_t s) {
+    return launch_rows(p, k_first, k_last, false, nullptr, false, nullptr, s);
 }
 
 bool resid_rows_supported(const VerifyParams& v) {
@@ -577,7 +700,7 @@ bool resid_rows_supported(const VerifyParams& v) {
 }
 
 cudaError_t launch_resid_rows(const VerifyParams& v, cudaStream_t s) {
-    return launch_rows(draft_view(v), 1, true, v.target, v.target_bf16 != 0, v.near_ties, s);
+    return launch_rows(draft_view(v), 1, 1, true, v.target, v.target_bf16 != 0, v.near_ties, s);
 }
 
 }  // namespace dspark

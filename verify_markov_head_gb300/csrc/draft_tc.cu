@@ -434,7 +434,7 @@ bool draft_tc_supported(const DraftParams& p) {
 }
 
 cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s) {
-    if (draft_rows_supported(p) && !getenv("DSPARK_DRAFT_VOCAB_LANES")) return launch_draft_rows(p, k, s);
+    if (draft_rows_supported(p) && !getenv("DSPARK_DRAFT_VOCAB_LANES")) return launch_draft_rows(p, k, k, s);
     switch (pick_nc(p.B, p.r)) {
         case 16: return launch_nc<16>(p, k, s);
         case 32: return launch_nc<32>(p, k, s);
@@ -442,6 +442,21 @@ cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s) {
         case 128: return launch_nc<128>(p, k, s);
         default: return launch_nc<256>(p, k, s);
     }
+}
+
+// All gamma positions of the draft.  The requests-on-lanes tensor-core kernel
+// runs them in one cooperative launch when the device supports it; otherwise
+// one launch per position.
+cudaError_t launch_draft(const DraftParams& p, cudaStream_t s) {
+    const bool tc = draft_tc_supported(p);
+    if (tc && draft_rows_supported(p) && !getenv("DSPARK_DRAFT_VOCAB_LANES") && p.gamma > 1 &&
+        cooperative_supported() && !getenv("DSPARK_DRAFT_PER_POSITION"))
+        return launch_draft_rows(p, 1, p.gamma, s);
+    for (int k = 1; k <= p.gamma; ++k) {
+        const cudaError_t e = tc ? launch_draft_tc(p, k, s) : launch_draft_simt(p, k, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace dspark

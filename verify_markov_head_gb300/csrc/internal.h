@@ -18,10 +18,11 @@ constexpr int kMaxParts = 1024;        // cap on partial states per request per 
 constexpr int kPartTile = 128;         // vocabulary entries per tile of the partial-producing kernels
 constexpr int kVerifySeg = 32768;      // vocabulary entries per verify-stream work item
 constexpr int kChunk = 16;             // requests per chunk of the partial-producing kernels
+constexpr int kGridBarrierSlots = DSPARK_MAX_GAMMA;   // one grid-barrier counter per draft position
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, tickets, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, total;
+    size_t status, tickets, gbar, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -31,7 +32,8 @@ struct WsPtrs {
     uint32_t* status;
     uint32_t* tickets_draft;   // [ceil(B/kChunk)] arrival counters, zero between launches
     uint32_t* tickets_resid;   // [ceil(B/kChunk)]
-    DrawLse* draft_part;
+    uint32_t* gbar;            // [kGridBarrierSlots + 1] grid-barrier counters, then the exit counter
+    DrawLse* draft_part;       // [2][B][parts] (two buffers alternate between positions)
     LseDraw* verify_part;
     int32_t* rej;        // [B] 0-based rejected row, -1 if every walked draft was accepted
     int32_t* acc;        // [B] accepted count
@@ -90,10 +92,12 @@ int num_sms();
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_draft_simt(const DraftParams& p, int k, cudaStream_t s);
+cudaError_t launch_draft(const DraftParams& p, cudaStream_t s);   // all gamma positions
 bool draft_tc_supported(const DraftParams& p);
 cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s);
 bool draft_rows_supported(const DraftParams& p);
-cudaError_t launch_draft_rows(const DraftParams& p, int k, cudaStream_t s);
+cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cudaStream_t s);
+bool cooperative_supported();
 void* tma_encoder();   // cuTensorMapEncodeTiled from the driver, or NULL
 bool resid_rows_supported(const VerifyParams& v);
 cudaError_t launch_resid_rows(const VerifyParams& v, cudaStream_t s);
