@@ -119,13 +119,14 @@ __device__ __forceinline__ float gumbel_of(uint32_t x) {
     return -kLn2 * fast_log2(E);
 }
 
-// The same variate in base-2 units, for kernels that keep their scores as
-// z*log2(e):  G2 = log2(e) * G + log2(ln 2) = -log2(E2), E2 = -log2(u).
-// argmax_v (z_v*log2e + G2_v) is argmax_v (z_v + G_v): the map is monotone.
-// E2 takes the series of -ln(1 - w) times log2(e) (coefficients log2(e)/n)
-// for w = 1 - u < 1/8 and the hardware log2 elsewhere, as in gumbel_of.
-constexpr float kLog2ofLn2 = -0.52876637294640327f;   // log2(ln 2)
-__device__ __forceinline__ float gumbel2_of(uint32_t x) {
+// E2 = -log2(u) (the exponential variate -ln u in base-2 units), for the
+// exponential-race form of Gumbel-max:
+//   argmax_v z_v + G_v  =  argmin_v E_v * e^(-z_v)  =  argmin_v E2_v * 2^(-z_v*log2e),
+// the same draw without the outer logarithm.  E2 takes the series
+// -ln(1 - w) * log2e = sum_{n>=1} (log2e/n) w^n to n = 8 for w = 1 - u < 1/8
+// (exact w, so E2 keeps its relative accuracy as u -> 1) and the hardware
+// log2 elsewhere, as in gumbel_of.
+__device__ __forceinline__ float exp2_variate_of(uint32_t x) {
     const float u = uniform_of(x);
     const float w = one_minus_uniform_of(x);
     const float e_log = -fast_log2(u);
@@ -136,8 +137,7 @@ __device__ __forceinline__ float gumbel2_of(uint32_t x) {
     poly = fmaf(w, poly, 0.48089834696298783f);                          // log2e/3
     poly = fmaf(w, poly, 0.72134752044448170f);                          // log2e/2
     poly = fmaf(w, poly, 1.4426950408889634f);                           // log2e
-    const float E2 = (w < 0.125f) ? w * poly : e_log;
-    return -fast_log2(E2);
+    return (w < 0.125f) ? w * poly : e_log;
 }
 
 // 2^x on the special-function unit (relative error about 2^-22, subnormal

@@ -329,7 +329,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + urow) * V;
             float2 lse = make_float2(0.f, 0.f);
             if (kResid && real) lse = p.ws.lse_rej[b];
-            DrawLse st = drawlse_empty();
+            DrawLse st = drawlse_empty();            // idx, zb (u + bias of the winner), s
+            float rz2 = -INFINITY, rE2 = INFINITY;     // winner's z*log2e and E2
             Draw2 st2 = draw2_empty();
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
                 bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
@@ -424,7 +425,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) { failed = true; break; }
                     if (real) {
-                        // scores in base-2 units: z2 = z*log2e, G2 = log2e*G + log2(ln 2)
+                        // Exponential race in base-2 units: the winner minimises
+                        // E2_v * 2^(-z2_v), z2 = z*log2e; with the winner's z2 as the
+                        // log-sum-exp reference the race and the sum share one exp2:
+                        //   t_v = 2^(z2_v - z2_best),  v wins iff E2_v < E2_best * t_v.
                         const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
@@ -441,17 +445,16 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
                                     const float z2 = us[e] * scale2;
-                                    const float sc = z2 + gumbel2_of(ws[e]);
-                                    const int idx = vq + e;
-                                    // A thread meets its entries in increasing v, so a strict
-                                    // comparison keeps the lowest index on exact ties.  An empty
-                                    // state has best = -inf and s = 0: the first entry takes the
-                                    // first branch with 2^-inf = 0.
-                                    if (sc > st.best) {
-                                        st.s = st.s * fast_exp2(st.best - sc) + fast_exp2(z2 - sc);
-                                        st.best = sc; st.idx = idx; st.zb = us[e];
+                                    const float E2 = exp2_variate_of(ws[e]);
+                                    const float t = fast_exp2(z2 - rz2);
+                                    // Entries come in increasing v, so the strict comparison keeps
+                                    // the lowest index on exact ties.  The empty state (rz2 = -inf,
+                                    // rE2 = +inf, s = 0) makes the first entry win with s = 1.
+                                    if (E2 < rE2 * t) {
+                                        st.s = st.s * fast_exp2(rz2 - z2) + 1.f;
+                                        rz2 = z2; rE2 = E2; st.idx = vq + e; st.zb = us[e];
                                     } else {
-                                        st.s += fast_exp2(z2 - st.best);
+                                        st.s += t;
                                     }
                                 }
                             }
@@ -465,12 +468,15 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             if constexpr (kResid) {
                 reinterpret_cast<Draw2*>(s_merge)[cb * 128 + row] = st2;
             } else {
-                // back to natural-log units: best = (best2 - log2(ln 2)) * ln 2, s = s2 * ln 2
-                DrawLse sn = st;
-                if (st.best > -INFINITY) {
-                    sn.best = (st.best - kLog2ofLn2) * kLn2;
-                    sn.s = st.s * kLn2;
+                // back to the Gumbel score in natural units: with E = E2 * ln 2 the
+                // winner's score is z_best - ln E, and sum_v e^(z_v - score) = s * E
+                DrawLse sn = drawlse_empty();
+                if (rE2 < INFINITY) {
+                    const float E = rE2 * kLn2;
                     sn.zb = st.zb * p.inv_tau;
+                    sn.best = sn.zb - logf(E);
+                    sn.s = st.s * E;
+                    sn.idx = st.idx;
                 }
                 s_merge[cb * 128 + row] = sn;
             }
