@@ -21,13 +21,24 @@ struct Philox {
     static constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;   // key increments
 };
 
+// 32 x 32 -> 64-bit product; one wide multiply yields both halves.
+__device__ __forceinline__ uint64_t mul_wide(uint32_t a, uint32_t b) {
+    uint64_t r;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint4 philox_round(uint4 c, uint32_t k0, uint32_t k1) {
+    const uint64_t p0 = mul_wide(Philox::kM0, c.x);
+    const uint64_t p1 = mul_wide(Philox::kM1, c.z);
+    return make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
+}
+
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
         if (i) { k0 += Philox::kW0; k1 += Philox::kW1; }
-        const uint32_t hi0 = __umulhi(Philox::kM0, c.x), lo0 = Philox::kM0 * c.x;
-        const uint32_t hi1 = __umulhi(Philox::kM1, c.z), lo1 = Philox::kM1 * c.z;
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        c = philox_round(c, k0, k1);
     }
     return c;
 }
@@ -65,11 +76,7 @@ struct StreamRK {
     __device__ __forceinline__ uint4 quad(uint32_t q) const {
         uint4 c = make_uint4(q, row, step_lo, dom_hi);
 #pragma unroll
-        for (int i = 0; i < 10; ++i) {
-            const uint32_t hi0 = __umulhi(Philox::kM0, c.x), lo0 = Philox::kM0 * c.x;
-            const uint32_t hi1 = __umulhi(Philox::kM1, c.z), lo1 = Philox::kM1 * c.z;
-            c = make_uint4(hi1 ^ c.y ^ rk0[i], lo1, hi0 ^ c.w ^ rk1[i], lo0);
-        }
+        for (int i = 0; i < 10; ++i) c = philox_round(c, rk0[i], rk1[i]);
         return c;
     }
 };

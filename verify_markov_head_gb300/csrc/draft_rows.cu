@@ -430,10 +430,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         // log-sum-exp reference the race and the sum share one exp2:
                         //   t_v = 2^(z2_v - z2_best),  v wins iff E2_v < E2_best * t_v.
                         const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
+                        const int nq = min(8, (V - v0) >> 2);   // quads inside the vocabulary
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
-                            const int vq = v0 + 4 * c;
-                            if (vq < V) {
+                            if (c < nq) {
+                                const int vq = v0 + 4 * c;
                                 const float4 u4 = *reinterpret_cast<const float4*>(srow + ((c ^ (row & 7)) << 4));
                                 const float us[4] = {u4.x + bias[4 * c], u4.y + bias[4 * c + 1],
                                                      u4.z + bias[4 * c + 2], u4.w + bias[4 * c + 3]};
@@ -442,19 +443,31 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                                         us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
                                 const uint4 w = rng.quad((uint32_t)vq >> 2);
                                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                                float z2[4], E2[4], t[4];
+                                bool any_win = false;
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const float z2 = us[e] * scale2;
-                                    const float E2 = exp2_variate_of(ws[e]);
-                                    const float t = fast_exp2(z2 - rz2);
-                                    // Entries come in increasing v, so the strict comparison keeps
-                                    // the lowest index on exact ties.  The empty state (rz2 = -inf,
-                                    // rE2 = +inf, s = 0) makes the first entry win with s = 1.
-                                    if (E2 < rE2 * t) {
-                                        st.s = st.s * fast_exp2(rz2 - z2) + 1.f;
-                                        rz2 = z2; rE2 = E2; st.idx = vq + e; st.zb = us[e];
-                                    } else {
-                                        st.s += t;
+                                    z2[e] = us[e] * scale2;
+                                    E2[e] = exp2_variate_of(ws[e]);
+                                    t[e] = fast_exp2(z2[e] - rz2);
+                                    any_win |= E2[e] < rE2 * t[e];
+                                }
+                                if (!any_win) {
+                                    st.s += (t[0] + t[1]) + (t[2] + t[3]);
+                                } else {
+                                    // rare: re-run the quad one entry at a time.  Entries come in
+                                    // increasing v, so the strict comparison keeps the lowest index
+                                    // on exact ties.  The empty state (rz2 = -inf, rE2 = +inf, s = 0)
+                                    // makes the first entry win with s = 1.
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float te = fast_exp2(z2[e] - rz2);
+                                        if (E2[e] < rE2 * te) {
+                                            st.s = st.s * fast_exp2(rz2 - z2[e]) + 1.f;
+                                            rz2 = z2[e]; rE2 = E2[e]; st.idx = vq + e; st.zb = us[e];
+                                        } else {
+                                            st.s += te;
+                                        }
                                     }
                                 }
                             }
