@@ -104,13 +104,15 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target, con
     __threadfence();
     atomicAdd(ctr, 1u);
     const long long t0 = clock64();
+    uint32_t ns = 64;
     for (;;) {
         uint32_t v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
         if (v >= target) break;
         if (*abort) return false;
         if (clock64() - t0 > limit_cycles) return false;
-        __nanosleep(100);
+        __nanosleep(ns);
+        if (ns < 512) ns <<= 1;
     }
     __threadfence();
     return true;

@@ -44,14 +44,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: gives up after ~limit_cycles SM clocks, or at once when
-// *abort is set by another thread.  Returns false on either.
+// *abort is set by another thread.  Returns false on either.  Between tries
+// the thread sleeps (32 ns doubling to 256 ns), so a waiting warp leaves the
+// issue slots of its scheduler to the warps that have work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile uint32_t* abort,
                                           long long limit_cycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
+    uint32_t ns = 32;
     for (uint32_t it = 0;; ++it) {
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if ((it & 15u) == 0) {
             if (*abort) return false;
             if (clock64() - t0 > limit_cycles) return false;
         }
