@@ -57,30 +57,40 @@ constexpr int kEpiWarps = 16;
 constexpr int kThreads = (kEpiWarps + 2) * 32;   // 576
 constexpr int kProducerWarp = 16, kMmaWarp = 17;
 constexpr int kTN = 128;                          // vocabulary entries per tile
-constexpr int kStages = 4;                        // W2 K-chunk ring
+constexpr int kMaxStages = 8;                     // W2 K-chunk ring depth (as shared memory allows)
+constexpr int kAcc = 4;                           // TMEM accumulators (4 x 128 columns)
 constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile (bf16), 16 KB
-constexpr int kURingBytes = 64 * 1024;
+constexpr int kUSlots = 3;                        // U slice ring (draft)
+constexpr int kUSlotsResid = 4;                   // residual: 16 warps x 4 KB row staging
+constexpr int kSmemBudget = 227 * 1024;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 
 struct Layout {
     uint32_t b, a, u, merge, bar, misc, total;
-    int uslots;
+    int uslots, stages;
 };
 
 constexpr int kSlotBytes = 128 * 128;             // one U slice: 128 rows x 32 fp32
 
 // RF = 128 / NC vocabulary tiles per accumulator; the A region holds
-// (RF - 1) + RF * (r / 64) blocks of NC rows x 128 B.
-__host__ __device__ inline Layout rows_layout(int NC, int r) {
+// (RF - 1) + RF * (r / 64) blocks of NC rows x 128 B.  The W2 ring takes
+// whatever shared memory is left (up to kMaxStages K-chunks).  The residual
+// mode uses the U region as 16 per-warp 4 KB row-staging buffers.
+__host__ __device__ inline Layout rows_layout(int NC, int r, bool resid) {
     Layout L;
     const int RF = 128 / NC;
+    const uint32_t a_bytes = (uint32_t)((RF - 1) + RF * (r / 64)) * (uint32_t)NC * 128u;
+    L.uslots = resid ? kUSlotsResid : kUSlots;
+    const uint32_t fixed = a_bytes + (uint32_t)(L.uslots * kSlotBytes) + 4u * 128u * 16u +
+                           8u * (2 * kMaxStages + 2 * L.uslots + 2 * kAcc + 2) + 16u + 8u * 128u + 1024u + 64u;
+    int st = (int)((kSmemBudget - (int)fixed) / kBBytes);
+    L.stages = st > kMaxStages ? kMaxStages : st;
     L.b = 0;
-    L.a = L.b + kStages * kBBytes;
-    L.u = L.a + (uint32_t)((RF - 1) + RF * (r / 64)) * (uint32_t)NC * 128u;
-    L.uslots = kURingBytes / kSlotBytes;
+    L.a = L.b + (uint32_t)L.stages * kBBytes;
+    L.u = L.a + a_bytes;
     L.merge = L.u + (uint32_t)(L.uslots * kSlotBytes);
     L.bar = L.merge + 4u * 128u * 16u;
-    L.misc = L.bar + 8u * (2 * kStages + 2 * L.uslots + 6);
+    L.misc = L.bar + 8u * (2 * L.stages + 2 * L.uslots + 2 * kAcc + 2);
     L.misc = (L.misc + 15u) & ~15u;
     L.total = L.misc + 16u + 8u * 128u;
     return L;
@@ -161,7 +171,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const Layout L = rows_layout(NC, p.r);
+    const Layout L = rows_layout(NC, p.r, kResid);
     const int KCH = p.r / 64;
     const int RF = 128 / NC;                      // vocabulary tiles per accumulator
     const int US = L.uslots;
@@ -169,15 +179,16 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     const uint32_t blk = (uint32_t)NC * 128u;     // bytes of one A block
     const bool persistent = k_last > k_first;
 
+    const int kStages = L.stages;
     const uint32_t bar0 = base + L.bar;
     auto full = [&](int i) { return bar0 + 8u * i; };
     auto empty = [&](int i) { return bar0 + 8u * (kStages + i); };
     auto ufull = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
     auto uempty = [&](int i) { return bar0 + 8u * (2 * kStages + US + i); };
     auto tfull = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + i); };
-    auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + 2 + i); };
-    const uint32_t drain = bar0 + 8u * (2 * kStages + 2 * US + 4);
-    const uint32_t a_ready = bar0 + 8u * (2 * kStages + 2 * US + 5);
+    auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + kAcc + i); };
+    const uint32_t drain = bar0 + 8u * (2 * kStages + 2 * US + 2 * kAcc);
+    const uint32_t a_ready = bar0 + 8u * (2 * kStages + 2 * US + 2 * kAcc + 1);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L.misc);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 4);
     volatile uint32_t* never = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 8);
@@ -195,7 +206,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), 1); }
         for (int i = 0; i < US; ++i) { ptx::mbar_init(ufull(i), 1); ptx::mbar_init(uempty(i), 4u); }
-        for (int i = 0; i < 2; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
+        for (int i = 0; i < kAcc; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(a_ready, 1);
         *abort_flag = 0u;
@@ -203,7 +214,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         ptx::fence_mbar_init();
     }
     if (tid == kProducerWarp * 32) { ptx::prefetch_tmap(&a.w2map); ptx::prefetch_tmap(&a.umap); }
-    if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 256u); ptx::tmem_relinquish(); }
+    if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 128u * kAcc); ptx::tmem_relinquish(); }
     for (int n = tid; n < 128; n += kThreads) {
         int x = -1, prow = -1;
         if (n < nb) {
@@ -301,7 +312,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     }
                     if (!ok) break;
                     ptx::mma_commit(tfull(acc));
-                    if (++acc == 2) { acc = 0; aph ^= 1u; }
+                    if (++acc == kAcc) { acc = 0; aph ^= 1u; }
                 }
             }
             if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
@@ -347,7 +358,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty(acc));
-                if (++acc == 2) { acc = 0; aph ^= 1u; }
+                if (++acc == kAcc) { acc = 0; aph ^= 1u; }
                 if (kResid && !active) continue;
                 const int v0 = t * kTN * RF + ti * kTN + 32 * cb;
                 if constexpr (kResid) {
@@ -567,7 +578,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     __syncthreads();
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, 256u);
+        ptx::tmem_dealloc(tmem_base, 128u * kAcc);
     }
 
     if (persistent) {
@@ -690,7 +701,7 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const Layout L = rows_layout(a.NC, p.r);
+    const Layout L = rows_layout(a.NC, p.r, resid);
     const size_t smem = L.total + 1024;
     auto kern = !resid ? rows_kernel<false, float> : (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
