@@ -79,7 +79,9 @@ dspark_status dspark_workspace_init(void* ws, size_t ws_bytes, void* stream);
 /* Synchronise `stream`, then read and clear the workspace status word.
  * Returns DSPARK_OK, DSPARK_ERR_DEVICE (range check fired), DSPARK_ERR_TIMEOUT,
  * or DSPARK_ERR_CUDA (the stream reported an error).  If bits is non-NULL the
- * raw status bits are stored there. */
+ * raw status bits are stored there: bit 0 a token out of [0, V), bit 1 a
+ * block length out of [0, gamma], bit 2 a bounded wait expired, and with
+ * bit 2 the bits 8-23 name the wait that gave up (for diagnosis only). */
 dspark_status dspark_sync_status(void* ws, void* stream, uint32_t* bits);
 
 /*
@@ -188,11 +190,12 @@ dspark_status dspark_verify(
  * (cudaMalloc may take locks and synchronise the device).  Arguments and
  * results are those of dspark_draft_markov without the workspace: the
  * kernels' scratch (status word, arrival counters, partial states) lives in
- * a fixed array inside the library, 4 MiB + 64 KiB per GPU, held until the
+ * a fixed array inside the library, 8 MiB + 64 KiB per GPU, held until the
  * process exits.  No counterpart on the pages: it is a deployment option.
- *   - Sizes whose scratch exceeds the array (B * ceil(V/128) partial states
- *     of 16 bytes plus counters, e.g. beyond B = 256 at V = 131072) return
- *     DSPARK_ERR_UNSUPPORTED with a message on stderr.
+ *   - Sizes whose scratch exceeds the array (two buffers of
+ *     B * min(1024, ceil(V/128)) partial states of 16 bytes plus counters;
+ *     the limit is B * min(1024, ceil(V/128)) <= 262144: any V for
+ *     B <= 256) return DSPARK_ERR_UNSUPPORTED with a message on stderr.
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *   - Every call on a device shares the one array and clears its counters

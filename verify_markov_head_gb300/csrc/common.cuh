@@ -288,4 +288,10 @@ __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
     if (status) atomicOr(status, bit);
 }
 
+// A bounded wait expired: the timeout bit, plus bit (8 + site) naming the
+// wait that gave up (sites 0..23, see the kernel that raises it).
+__device__ __forceinline__ void raise_timeout(uint32_t* status, int site) {
+    if (status) atomicOr(status, kTimeout | (1u << (8 + (site & 15))));
+}
+
 }  // namespace dspark

@@ -60,10 +60,17 @@ constexpr int kTN = 128;                          // vocabulary entries per tile
 constexpr int kMaxStages = 8;                     // W2 K-chunk ring depth (as shared memory allows)
 constexpr int kAcc = 4;                           // TMEM accumulators (4 x 128 columns)
 constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile (bf16), 16 KB
-constexpr int kUSlots = 3;                        // U slice ring (draft)
+// U slice ring (draft).  Slice n = 4 * tile + column block goes to slot
+// n % kUSlots and is read by the four warps of that column block.  The slot
+// count is a multiple of 4 so that every slot is read by one column block
+// only, in fill order: a reader then never waits more than one fill ahead of
+// the slot's barrier, which the barrier's phase parity cannot tell apart.
+constexpr int kUSlots = 4;
 constexpr int kUSlotsResid = 4;                   // residual: 16 warps x 4 KB row staging
+static_assert(kUSlots % 4 == 0, "each U slot must belong to one column block");
 constexpr int kSmemBudget = 227 * 1024;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
+constexpr long long kDrainCycles = 200000000LL;   // ~0.1 s: copies already issued landing
 
 struct Layout {
     uint32_t b, a, u, merge, bar, misc, total;
@@ -243,56 +250,74 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol_w = ptx::policy_evict_last(), pol_u = ptx::policy_evict_first();
-            int stage = 0;
+            int stage = 0, site = 0;
             uint32_t ph = 0;
             bool ok = true;
             int lt = 0;                                  // U slices issued / 4, over all positions
+            long long nw = 0, nu = 0;                    // W2 chunks and U slices issued
             for (int k = k_first; k <= k_last && ok; ++k) {
                 for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
                     const int vs = t * kTN * RF;
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
-                            if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kWaitCycles))) break;
+                            if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kWaitCycles))) { site = 1; break; }
                             ptx::mbar_arrive_expect_tx(full(stage), kBBytes);
                             const uint32_t dst = base + L.b + (uint32_t)stage * kBBytes;
                             const int v0 = vs + i * kTN;
                             ptx::tma_load_2d(dst, &a.w2map, v0, j * 64, full(stage), pol_w);
                             ptx::tma_load_2d(dst + kBBytes / 2, &a.w2map, v0 + 64, j * 64, full(stage), pol_w);
+                            ++nw;
                             if (++stage == kStages) { stage = 0; ph ^= 1u; }
                         }
                     }
                     for (int c = 0; c < 4 && ok && !kResid; ++c) {
                         const int n = lt * 4 + c, s = n % US;
                         const uint32_t par = (uint32_t)((n / US) & 1);
-                        if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) break;
+                        if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) { site = 2; break; }
                         ptx::mbar_arrive_expect_tx(ufull(s), slot_bytes);
                         for (int i = 0; i < RF; ++i)      // rows [i*NC, (i+1)*NC) hold tile i's U slice
                             ptx::tma_load_3d(base + L.u + (uint32_t)s * slot_bytes + (uint32_t)i * blk, &a.umap,
                                              vs + i * kTN + 32 * c, k - 1, b_base, ufull(s), pol_u);
+                        ++nu;
                     }
                 }
             }
-            if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
+            if (!ok) { raise_timeout(p.ws.status, site); *abort_flag = 1u; }
+            // Every copy issued lands before the CTA leaves: wait for the last
+            // fill of each stage and slot (already complete on the normal path,
+            // where the readers waited for them).
+            for (int i = 0; i < kStages; ++i)
+                if (nw > i) {
+                    const long long m = (nw - 1) - ((nw - 1 - i) % kStages);
+                    ptx::mbar_wait(full(i), (uint32_t)((m / kStages) & 1), never, kDrainCycles);
+                }
+            for (int i = 0; i < US; ++i)
+                if (nu > i) {
+                    const long long m = (nu - 1) - ((nu - 1 - i) % US);
+                    ptx::mbar_wait(ufull(i), (uint32_t)((m / US) & 1), never, kDrainCycles);
+                }
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTN, /*A K-major*/ false, /*B MN-major*/ true);
-            int stage = 0, acc = 0;
+            int stage = 0, acc = 0, site = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
             for (int k = k_first; k <= k_last && ok; ++k) {
                 if (k > k_first &&   // h of this position staged by the epilogue warps
-                    !(ok = ptx::mbar_wait(a_ready, (uint32_t)((k - k_first - 1) & 1), abort_flag, kWaitCycles)))
+                    !(ok = ptx::mbar_wait(a_ready, (uint32_t)((k - k_first - 1) & 1), abort_flag, kWaitCycles))) {
+                    site = 3;
                     break;
+                }
                 for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                    if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) break;
+                    if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) { site = 4; break; }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTN);
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
-                            if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) break;
+                            if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) { site = 5; break; }
                             ptx::tc_fence_after();
                             const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
                             // window of 128 rows whose block i is H_j
@@ -315,7 +340,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     if (++acc == kAcc) { acc = 0; aph ^= 1u; }
                 }
             }
-            if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
+            if (!ok) { raise_timeout(p.ws.status, site); *abort_flag = 1u; }
             ptx::mma_commit(drain);                 // every MMA above completes before TMEM is freed
             ptx::mbar_wait(drain, 0u, never, kWaitCycles);
         }
@@ -348,7 +373,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
                 bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
                 ok = __all_sync(0xffffffffu, ok);
-                if (!ok) { failed = true; break; }
+                if (!ok) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 6); failed = true; break; }
                 ptx::tc_fence_after();
                 float bias[32];
                 if (active) {
@@ -436,7 +461,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     const int n = lt * 4 + cb, s = n % US;
                     ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles);
                     ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) { failed = true; break; }
+                    if (!ok) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 7); failed = true; break; }
                     if (real) {
                         // Exponential race in base-2 units: the winner minimises
                         // E2_v * 2^(-z2_v), z2 = z*log2e; with the winner's z2 as the
@@ -533,7 +558,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             if (etid == 0) s_gb_ok = grid_barrier(p.ws.gbar + (k - k_first), nctas, abort_flag, kWaitCycles) ? 1 : 0;
             ptx::named_barrier(1, 32 * kEpiWarps);
             if (!s_gb_ok) {
-                if (etid == 0) raise_status(p.ws.status, kTimeout);
+                if (etid == 0) raise_timeout(p.ws.status, 8);
                 failed = true;
                 *abort_flag = 1u;
                 break;
@@ -571,9 +596,6 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         if (failed) *abort_flag = 1u;
     }
 
-    if (*abort_flag) {
-        for (int i = 0; i < 64; ++i) __nanosleep(1000);    // let copies in flight land
-    }
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
