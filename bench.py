@@ -2,19 +2,25 @@
 """Draft + verify throughput of the DSpark step on GB300.
 
 A step is one pass of the whole hot path over one batch of synthetic input:
-Markov-head draft loop (gamma launches), confidence + STS + survival,
-prefix scheduler, verification stream + accept walk + residual draw +
-compaction.  Default workload: B=64, V=151936, r=256, gamma=7, d=4096,
-bf16 draft-head weights, fp32 base and target logits, full-prefix
-verification (scheduler call made in OFF mode, K_b = 7).
+Markov-head draft loop (one cooperative launch over the gamma positions),
+confidence + STS + survival, prefix scheduler, verification stream + accept
+walk + residual draw + compaction: 7 kernel launches.  Default workload:
+B=64, V=151936, r=256, gamma=7, d=4096, bf16 draft-head weights, fp32 base
+and target logits, full-prefix verification (scheduler call made in OFF
+mode, K_b = 7).
 
 Prints one JSON line (rank 0).  `value` = emitted tokens per second over all
 ranks with inputs resident in HBM (CUDA-graph replay of the step, CUDA
 events on the launching stream, inputs 1.13 GB > L2 so no flush).
 `e2e` = the same metric through the public API with the step's activations
 copied from pinned host memory and the emitted tokens copied back inside the
-timed region.  `roofline` = the draft kernel (the dominant one: gamma
-launches per step, each streaming W2 and one row block of U).
+timed region.  `roofline` = the draft kernel (the dominant one: per launch
+it streams W2 and one row block of U for each of the gamma positions).
+
+With several ranks each owns B requests of a batch of B * ranks (weak
+scaling).  With the scheduler off no data crosses ranks; with it on
+(--sched spec) the survival lists are all-gathered and every rank runs the
+scheduler on the whole list.
 
 --impl reference times the float64 CPU oracle on a bounded sample of the
 same workload on the host cores (the reference arm of this tier).
@@ -50,7 +56,7 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons while running."""
 
     def __init__(self, index=0):
         self.index = index
@@ -64,7 +70,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
@@ -73,7 +79,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, "t_" + which, time.monotonic())
 
     def __exit__(self, *a):
         if self.proc:
@@ -84,9 +93,14 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        """Median SM clock and the throttle reasons seen in the samples taken
+        between mark("start") and mark("end") (the timed region)."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t_start", None), getattr(self, "t_end", None)
+        for t, ln in self.lines:
+            if t0 is not None and not (t0 <= t <= t1):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -100,7 +114,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "timed region"}
 
 
 def _dist():
@@ -150,8 +164,16 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device=dev)
     seed = w.seed
 
-    def one_step():
-        vm.run_step(inp, buf, mode=mode, seed=seed, step=0, req_base=req_base, stream=stream)
+    if world > 1 and mode != 0:
+        # the scheduler ranks the whole batch: a capacity table for B * world
+        inp["sps"] = workload.custom(w.name, B=B * world).sps_table().to(dev)
+        sched = vm.GlobalSchedule(B, gamma, world, device=dev)
+
+        def one_step():
+            vm.run_step_dp(inp, buf, sched, mode=mode, seed=seed, step=0, stream=stream)
+    else:
+        def one_step():
+            vm.run_step(inp, buf, mode=mode, seed=seed, step=0, req_base=req_base, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -173,14 +195,24 @@ def run_gpu(args):
     _barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # the same replays for ~1 s first: the sampler starts and the clocks
+        # settle under load before the timed region
+        t_pre = time.monotonic()
+        with torch.cuda.stream(stream):
+            while time.monotonic() - t_pre < 1.0:
+                for _ in range(20):
+                    graph.replay()
+                stream.synchronize()
+        _barrier(dist)
+        torch.cuda.synchronize()
+        clk.mark("start")
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(args.steps):
                 graph.replay()
             e1.record(stream)
         stream.synchronize()
-        if args.steps * 0.2 < 1.0:     # keep sampling long enough for a few clock readings
-            time.sleep(0.5)
+        clk.mark("end")
     torch.cuda.synchronize()
     _barrier(dist)
     ms = e0.elapsed_time(e1) / args.steps
@@ -189,8 +221,9 @@ def run_gpu(args):
     emitted_all = _sum_over_ranks(dist, emitted, dev)
     value = emitted_all / (ms_max / 1e3)
 
-    # ---- dominant kernel: the draft launches, timed alone on the same stream
-    reps = max(5, args.steps)
+    # ---- dominant kernel: the draft call, timed alone on the same stream
+    draft_launches = gamma if os.environ.get("DSPARK_DRAFT_PER_POSITION") else 1
+    reps = max(5, min(args.steps, 1000))
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         d0.record(stream)
@@ -199,10 +232,11 @@ def run_gpu(args):
                                    buf.z_tok, buf.ws, seed=seed, req_base=req_base, stream=stream)
         d1.record(stream)
     stream.synchronize()
-    draft_launch_ms = d0.elapsed_time(d1) / (reps * gamma)
+    draft_launch_ms = d0.elapsed_time(d1) / (reps * draft_launches)
     w2_bytes = r * V * inp["W2"].element_size()
     u_bytes_k = B * V * inp["U"].element_size()
-    draft_bytes = w2_bytes + u_bytes_k                   # per launch: W2 once + one position of U
+    # per position: W2 once + one row block of U; a launch covers gamma / draft_launches positions
+    draft_bytes = (w2_bytes + u_bytes_k) * gamma // draft_launches
     peak, peak_kind = _peaks()
     achieved = draft_bytes / (draft_launch_ms / 1e3) / 1e9
     formula_bytes = gamma * w2_bytes + inp["U"].numel() * inp["U"].element_size() + \
@@ -233,10 +267,11 @@ def run_gpu(args):
     if st != 0:
         raise SystemExit(f"device status {st} bits {bits}")
 
-    launches_per_step = gamma + 1 + 1 + 4
+    # draft, confidence, schedule, verify stream, accept walk, residual draw, compaction
+    launches_per_step = draft_launches + 6
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, mode, budget_s=args.cpu_budget, dev_inp=inp)
+        cpu = cpu_baseline(w, mode, budget_s=args.cpu_budget, dev_inp=inp, min_seconds=10.0)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -249,10 +284,12 @@ def run_gpu(args):
             "emitted_tokens_per_step": emitted_all, "drafted_tokens_per_step": B * gamma * world,
             "step_formula_bytes": formula_bytes, "step_formula_gbs": step_gbs,
             "step_formula_frac": step_gbs / peak,
-            "roofline": {"kernel": "draft_markov (per position launch)", "bound": "hbm", "achieved": achieved,
-                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": None, "algorithmic_bytes_per_launch": draft_bytes,
-                         "launch_ms": draft_launch_ms},
+            "roofline": {"kernel": "rows_kernel<draft> (dspark_draft_markov, %d position(s) per launch)"
+                                   % (gamma // draft_launches),
+                         "bound": "hbm", "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": _draft_traffic(w.name) if draft_launches == 1 else None,
+                         "algorithmic_bytes_per_launch": draft_bytes, "launch_ms": draft_launch_ms},
             "e2e": {"value": e2e_emitted / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
@@ -266,6 +303,39 @@ def run_gpu(args):
 
 def d_of(w):
     return w.d
+
+
+# Sources the draft kernel is compiled from: DRAM traffic taken from an ncu
+# capture is reported only while they are unchanged since the capture.
+_DRAFT_SOURCES = ("draft_rows.cu", "common.cuh", "sm100_ptx.cuh", "internal.h")
+
+
+def _draft_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in _DRAFT_SOURCES:
+        with open(os.path.join(ROOT, "verify_markov_head_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _draft_traffic(workload_name):
+    """dram__bytes_read.sum + dram__bytes_write.sum per draft launch from the
+    committed ncu summary of this workload, or None when there is none or
+    the kernel's sources changed after it was taken."""
+    path = os.path.join(ROOT, "profiles", f"draft_rows_{workload_name}.md")
+    try:
+        fields = {}
+        with open(path) as f:
+            for ln in f:
+                if ":" in ln and ln.startswith("- `"):
+                    k, v = ln[3:].split("`", 1)
+                    fields[k] = v.split(":", 1)[1].strip().strip("`")
+        if fields.get("source_sha256") != _draft_source_hash():
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 _CPU_INPUTS = {}
@@ -284,12 +354,11 @@ def _cpu_inputs(w, dev_inp=None):
     return _CPU_INPUTS[w.name]
 
 
-def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None):
+def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None, min_seconds=0.0):
     """The float64 oracle, as it stands, on a bounded sample of the workload:
     the first S requests of the batch through the whole step (draft,
-    confidence, schedule, verify, compaction), S sized to a ~budget_s run."""
-    import numpy as np
-
+    confidence, schedule, verify, compaction), S sized to a ~budget_s run,
+    repeated until min_seconds have passed."""
     import oracle
 
     inp = _cpu_inputs(w, dev_inp)
@@ -302,7 +371,23 @@ def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None):
     if S >= threads:
         S = (S // threads) * threads
     sub = {k: inp[k][:S] for k in ("U", "target", "h", "anchor")}
-    t = time.perf_counter()
+    reps, tokens, dt = 0, 0, 0.0
+    while reps == 0 or dt < min_seconds:
+        t = time.perf_counter()
+        tokens += _oracle_sample_step(w, mode, inp, sub, W1, W2, S)
+        dt += time.perf_counter() - t
+        reps += 1
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{S} of {w.B} requests of {w.name}, whole step (draft+confidence+schedule+verify+compact), "
+                      f"{reps} run(s), {dt:.1f} s", "seconds": dt / reps}
+
+
+def _oracle_sample_step(w, mode, inp, sub, W1, W2, S):
+    """One oracle step over the sample; returns the tokens it emits."""
+    import numpy as np
+
+    import oracle
+
     d = oracle.draft_markov(sub["U"], W1, W2, sub["anchor"], seed=w.seed)
     # the confidence head reads emb rows of the anchors and drafts only
     prev = np.concatenate([sub["anchor"].numpy()[:, None], d["tok"][:, :-1]], axis=1)
@@ -319,10 +404,7 @@ def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None):
         K = oracle.schedule(c["log_surv"], inp["sps"], mode)["K"]
     v = oracle.verify(sub["target"], sub["U"], W1, W2, sub["anchor"], d["tok"], K, seed=w.seed)
     o = oracle.compact(d["tok"], v["accepted"], v["final_tok"])
-    dt = time.perf_counter() - t
-    return {"value": int(o["out_off"][-1]) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{S} of {w.B} requests of {w.name}, whole step (draft+confidence+schedule+verify+compact), "
-                      f"{dt:.1f} s", "seconds": dt}
+    return int(o["out_off"][-1])
 
 
 def run_reference(args):
@@ -331,7 +413,9 @@ def run_reference(args):
         return
     w = workload.WORKLOADS[args.workload]
     mode = {"off": 0, "spec": w.mode}[args.sched]
-    budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    # each step a sample sized so the whole run stays within a few minutes
+    # (at least one request: about 0.3 s on 16 cores at the b64 sizes)
+    budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_baseline(w, mode, budget_s=budget)
     vals, secs = [], 0.0
@@ -354,8 +438,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="b64", choices=sorted(workload.WORKLOADS))
     ap.add_argument("--sched", default="off", choices=["off", "spec"],

@@ -246,6 +246,66 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
                   p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
 
 
+class GlobalSchedule:
+    """Device buffers of the scheduler over the survival lists of `world`
+    ranks of B requests each (see run_step_dp)."""
+
+    def __init__(self, B, gamma, world, device="cuda"):
+        Bg = B * world
+        f32 = dict(dtype=torch.float32, device=device)
+        self.log_surv = torch.empty((Bg, gamma), **f32)
+        self.hist = torch.empty((Bg, gamma), **f32)
+        self.K = torch.empty((Bg,), dtype=torch.int32, device=device)
+        self.n_total = torch.empty((1,), dtype=torch.int32, device=device)
+        self.theta = torch.empty((1,), **f32)
+        # the scheduler's scratch depends on the list length only: the
+        # smallest vocabulary and rank the workspace sizing accepts
+        self.ws = Workspace(Bg, gamma, 8, 1, device)
+
+
+def run_step_dp(inp: dict, buf: StepBuffers, sched: GlobalSchedule, *, mode, seed, step=0, tau=1.0,
+                log_surv_hist=None, group=None, stream=None, p_tok=False):
+    """One step on this rank's block of a batch sharded over the ranks of
+    `group`: rank r owns global requests [r*B, (r+1)*B) and draws their
+    random streams.  With the scheduler on, the survival lists (and the
+    history, in async mode) are all-gathered and every rank runs the device
+    scheduler on the whole list, then verifies its own block with its share
+    of the verify lengths; inp["sps"] must cover the global batch.  With the
+    scheduler off no data crosses ranks."""
+    import torch.distributed as dist
+
+    from . import shard
+
+    rank = dist.get_rank(group)
+    B = buf.B
+    req_base = rank * B
+    dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
+                        buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, stream=stream)
+    dspark_confidence_sts(inp["h"], inp["emb"], inp["anchor"], buf.draft_tok, inp["w_c"], inp["b_c"], inp["T"],
+                          buf.conf_cal, buf.log_surv, buf.ws, stream=stream)
+    if int(mode) == 0:
+        dspark_schedule(buf.log_surv, inp["sps"], 0, buf.K, buf.n_total, buf.theta, buf.ws, stream=stream)
+        K = buf.K
+    else:
+        def device_schedule(all_surv, all_hist):
+            dspark_schedule(all_surv, inp["sps"], mode, sched.K, sched.n_total, sched.theta, sched.ws,
+                            log_surv_hist=all_hist, stream=stream)
+            return sched.K, sched.n_total, sched.theta
+
+        # the gather and the copies are ordered on the step's stream
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+            K, _, _, _ = shard.global_schedule(buf.log_surv, log_surv_hist, device_schedule, group,
+                                               surv_out=sched.log_surv, hist_out=sched.hist)
+            buf.K.copy_(K)
+            buf.n_total.copy_(sched.n_total)
+            buf.theta.copy_(sched.theta)
+    dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
+                  buf.z_tok, K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
+                  buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
+                  p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
+    return K
+
+
 _PER_STEP = ("U", "target", "h", "anchor")
 
 
