@@ -61,22 +61,29 @@ struct Stream {
 
 // The same stream with the ten round keys computed once, for loops that draw
 // many quads of one row.
+// Only the first counter word varies along a row, so half of the first
+// round (the product of the third word and its XOR with the second word and
+// key) is the same for every quad and is formed once here.
 struct StreamRK {
     uint32_t rk0[10], rk1[10];
-    uint32_t row, step_lo, dom_hi;
-    __device__ __forceinline__ StreamRK(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row_)
-        : row(row_), step_lo((uint32_t)step), dom_hi(domain + 4u * (uint32_t)(step >> 32)) {
+    uint32_t r1x, r1y, dom_k1;    // round 1: hi(M1*step_lo) ^ row ^ k0, lo(M1*step_lo), dom_hi ^ k1
+    __device__ __forceinline__ StreamRK(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row) {
         uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
 #pragma unroll
         for (int i = 0; i < 10; ++i) {
             rk0[i] = k0; rk1[i] = k1;
             k0 += Philox::kW0; k1 += Philox::kW1;
         }
+        const uint64_t p1 = mul_wide(Philox::kM1, (uint32_t)step);
+        r1x = (uint32_t)(p1 >> 32) ^ row ^ rk0[0];
+        r1y = (uint32_t)p1;
+        dom_k1 = (domain + 4u * (uint32_t)(step >> 32)) ^ rk1[0];
     }
     __device__ __forceinline__ uint4 quad(uint32_t q) const {
-        uint4 c = make_uint4(q, row, step_lo, dom_hi);
+        const uint64_t p0 = mul_wide(Philox::kM0, q);
+        uint4 c = make_uint4(r1x, r1y, (uint32_t)(p0 >> 32) ^ dom_k1, (uint32_t)p0);
 #pragma unroll
-        for (int i = 0; i < 10; ++i) c = philox_round(c, rk0[i], rk1[i]);
+        for (int i = 1; i < 10; ++i) c = philox_round(c, rk0[i], rk1[i]);
         return c;
     }
 };

@@ -7,13 +7,17 @@
 //   z[b, v]    = (U[b, k-1, v] + bias[b, v]) / tau
 //   x~_k       = argmax_v z + G,  lse_q = log sum exp z,  z_tok = z[x~_k]
 //
-// D[M = 128 rows, N = 128 vocabulary entries] accumulates h * W2tile over K = r:
+// D[M = 128 rows, N = 128 vocabulary entries] = U tile + h * W2tile over K = r:
 //   A = the gathered rows h = W1[x~_{k-1}] (K-major, 128-byte swizzle, staged
-//       once per CTA; rows past the batch are zero),
+//       once per position; rows past the batch are zero),
 //   B = a 128-entry slice of W2 read by TMA straight from the [r, V] row-major
 //       tensor (MN-major, 128-byte swizzle), in 64-rank K-chunks,
-//   D = fp32 in TMEM, two buffers so the MMA of tile t+1 overlaps the
-//       epilogue of tile t.
+//   D = fp32 in TMEM, four buffers so the MMAs of later tiles overlap the
+//       epilogue of a tile.  Before the MMAs D is loaded with the tile's U:
+//       the U slices arrive by TMA (128 rows x 32 fp32, 128-byte swizzle) and
+//       tcgen05.cp copies them into the accumulator, so the epilogue reads
+//       U + bias in one tcgen05.ld and the U ring turns over as soon as the
+//       copies have read it.
 // A chunk of NC < 128 requests would leave TMEM lanes NC..127 (and the warps
 // that read them) idle, so the 128 lanes hold RF = 128 / NC vocabulary tiles
 // at once: the A operand is block diagonal, rows [i*NC, (i+1)*NC) carry h
@@ -22,18 +26,18 @@
 // holds Z^(RF-1) H_0 Z^(RF-1) H_1 ... H_last Z^(RF-1) and the window for
 // (tile i, K-chunk j) starts i blocks before H_j.
 // With the request on the TMEM lane, every epilogue thread owns one request
-// row and reads 32 consecutive vocabulary entries of it in one tcgen05.ld; the
-// matching U slice arrives by TMA (128-byte swizzle, so the 32 lanes of a warp
-// read 32 rows without bank conflicts).  Each thread folds z + Gumbel into its
-// own running Gumbel-max + log-sum-exp state: no transposition, no per-tile
-// cross-thread reduction.
+// row and reads 32 consecutive vocabulary entries of it in one tcgen05.ld.
+// Each thread folds z + Gumbel into its own running Gumbel-max + log-sum-exp
+// state: no transposition, no per-tile cross-thread reduction.
 //
-// CTA = 18 warps: warps 0-15 epilogue (warp w reads TMEM lane quarter w % 4
-// and the 32-column block w / 4 of each tile), warp 16 TMA producer, warp 17
-// TMEM owner and single-thread MMA issuer.  Every mbarrier wait is bounded;
-// on expiry the kernel raises the timeout bit, lets its copies land, frees
-// TMEM and returns.  Partial states go to the workspace and the last CTA of a
-// request chunk to arrive merges them (atomic ticket, no waiting).
+// CTA = 19 warps: warps 0-15 epilogue (warp w reads TMEM lane quarter w % 4
+// and the 32-column block w / 4 of each tile), warp 16 W2 producer (TMA),
+// warp 17 TMEM owner and single-thread issuer of the U copies and the MMAs,
+// warp 18 U producer (TMA).  Every mbarrier wait is bounded; on expiry the
+// kernel raises the timeout bit, lets its copies land, frees TMEM and
+// returns.  With one position per launch the partial states go to the
+// workspace and the last CTA of a request chunk to arrive merges them
+// (atomic ticket, no waiting).
 //
 // The same pipeline serves the residual draw of verification
 // ("DSpark：半自回归生成与置信度调度的投机解码" section 形式化定义): for every
@@ -42,7 +46,7 @@
 // then draws argmax_v log(max(0, p - q)) + G (domain 2), with the draw from p
 // kept for the case p <= q everywhere.  Each thread reads its own row of U and
 // of the target logits (the rejected rows differ per request, so no common
-// TMA box exists); no U slice ring is used.
+// TMA box exists): D is h.W2 alone and no U slice ring is used.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -54,23 +58,26 @@ namespace dspark {
 namespace {
 
 constexpr int kEpiWarps = 16;
-constexpr int kThreads = (kEpiWarps + 2) * 32;   // 576
-constexpr int kProducerWarp = 16, kMmaWarp = 17;
+constexpr int kThreads = (kEpiWarps + 3) * 32;   // 608
+constexpr int kProducerWarp = 16, kMmaWarp = 17, kUWarp = 18;
 constexpr int kTN = 128;                          // vocabulary entries per tile
 constexpr int kMaxStages = 8;                     // W2 K-chunk ring depth (as shared memory allows)
 constexpr int kAcc = 4;                           // TMEM accumulators (4 x 128 columns)
 constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile (bf16), 16 KB
-// U slice ring (draft).  Slice n = 4 * tile + column block goes to slot
-// n % kUSlots and is read by the four warps of that column block.  The slot
-// count is a multiple of 4 so that every slot is read by one column block
-// only, in fill order: a reader then never waits more than one fill ahead of
-// the slot's barrier, which the barrier's phase parity cannot tell apart.
+// U slice ring (draft): slice n = 4 * tile + column block goes to slot
+// n % kUSlots; the MMA warp alone reads the slots (copying them into TMEM),
+// in fill order.
 constexpr int kUSlots = 4;
 constexpr int kUSlotsResid = 4;                   // residual: 16 warps x 4 KB row staging
-static_assert(kUSlots % 4 == 0, "each U slot must belong to one column block");
 constexpr int kSmemBudget = 227 * 1024;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 constexpr long long kDrainCycles = 200000000LL;   // ~0.1 s: copies already issued landing
+// Margins of the exponential-race screen (relative on the winner's E2,
+// absolute on the candidate's): far above the hardware log2's error and the
+// rounding of the products, so every entry the exact test would accept is
+// passed to it.
+constexpr float kRaceRel = 1.0000152587890625f;   // 1 + 2^-16
+constexpr float kRaceSlack = 1.52587890625e-05f;  // 2^-16
 
 struct Layout {
     uint32_t b, a, u, merge, bar, misc, total;
@@ -106,6 +113,7 @@ __host__ __device__ inline Layout rows_layout(int NC, int r, bool resid) {
 struct RowsArgs {
     CUtensorMap w2map;   // bf16 [r][V], box {64 vocab, 64 rank}, 128-byte swizzle
     CUtensorMap umap;    // fp32 [B][gamma][V], box {32 vocab, 1, NC requests}, 128-byte swizzle
+    CUtensorMap upf;     // the same tensor, box {128 vocab, 1, NC requests}: L2 prefetch of a tile
     DraftParams p;
     int NC;              // request rows per CTA (32, 64 or 128)
     // residual mode only
@@ -135,12 +143,12 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target, con
     return true;
 }
 
-// h rows -> A operand (K-major, 128-byte swizzle).  Block H_j (K-chunk j, 64
-// ranks) is [NC rows][128 B] at block index (RF - 1) + j * RF; the zero
-// blocks between them are written only when with_zero_blocks is set.
-// 16-byte unit u of row n sits at unit u ^ (n mod 8).
+// h rows -> A operand (K-major, 128-byte swizzle), the whole region: block
+// H_j (K-chunk j, 64 ranks) is [NC rows][128 B] at block index
+// (RF - 1) + j * RF, zero blocks between them.  16-byte unit u of row n sits
+// at unit u ^ (n mod 8).
 __device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC, int RF,
-                                        int KCH, int r, int t0, int nthreads, bool with_zero_blocks) {
+                                        int KCH, int r, int t0, int nthreads) {
     const uint32_t blk = (uint32_t)NC * 128u;
     const int nblocks = (RF - 1) + RF * KCH;
     const int units = nblocks * NC * 8;
@@ -148,7 +156,6 @@ __device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, c
         const int bi = idx / (NC * 8), rem = idx - bi * (NC * 8);
         const int rel = bi - (RF - 1);
         const bool h_block = rel >= 0 && rel % RF == 0;
-        if (!h_block && !with_zero_blocks) continue;
         const int n = rem >> 3, uu = rem & 7;     // row in block, physical 16-byte unit
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         if (h_block) {
@@ -161,14 +168,74 @@ __device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, c
     }
 }
 
+// The h blocks alone (the zero blocks are already in place): every thread
+// issues its loads of W1 rows first, then stores them, so the gathers of one
+// thread are in flight together.
+__device__ __forceinline__ void stage_h_rows(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC,
+                                             int RF, int KCH, int r, int t0, int nthreads) {
+    const uint32_t blk = (uint32_t)NC * 128u;
+    const int units = KCH * NC * 8;
+    constexpr int kBatch = 4;
+    for (int first = t0; first < units; first += kBatch * nthreads) {
+        uint4 val[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int idx = first + u * nthreads;
+            val[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (idx < units) {
+                const int j = idx / (NC * 8), rem = idx - j * (NC * 8);
+                const int n = rem >> 3, uu = rem & 7;
+                const int x = s_tok[n];
+                if (x >= 0)
+                    val[u] = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)(j * 64 + (uu ^ (n & 7)) * 8));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int idx = first + u * nthreads;
+            if (idx < units) {
+                const int j = idx / (NC * 8), rem = idx - j * (NC * 8);
+                const int n = rem >> 3, uu = rem & 7;
+                *reinterpret_cast<uint4*>(a_region + (size_t)((RF - 1) + j * RF) * blk + (size_t)n * 128 + (uu << 4)) =
+                    val[u];
+            }
+        }
+    }
+}
+
+// Winner key of a partial draw: larger best first, then the lower index, as
+// in wins(); an unsigned 64-bit maximum over the keys picks the draw.  -0 is
+// folded into +0, which wins() does not tell apart.
+__device__ __forceinline__ unsigned long long win_key(const DrawLse& d) {
+    const uint32_t bits = __float_as_uint(d.best == 0.f ? 0.f : d.best);
+    const uint32_t ord = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)d.idx);
+}
+__device__ __forceinline__ int win_token(unsigned long long key) {
+    return (int)(0xFFFFFFFFu - (uint32_t)key);
+}
+
+__device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
+    DrawLse d;
+    d.best = c.x; d.idx = __float_as_int(c.y); d.zb = c.z; d.s = c.w;
+    return d;
+}
+
 // Positions k_first..k_last in one launch.  With more than one position the
-// launch is cooperative: after each position every CTA publishes its partial
-// states, waits at a grid barrier, merges the partials of its own requests
-// (every CTA of a chunk does the same merge, so no second barrier is needed),
-// stages h = W1[x~_k] for the next position and releases the MMA issuer.  The
-// TMA producer never stops at the boundaries: W2 and the next position's U
-// do not depend on the drawn tokens.  Partial states alternate between two
-// buffers so a fast CTA never overwrites the ones a slow CTA still merges.
+// launch is cooperative: after each position every CTA writes its partial
+// states and folds its draw of each request into a 64-bit atomic maximum
+// (score, then lowest index), waits at a grid barrier, reads the winners of
+// its requests (one load each), stages h = W1[x~_k] for the next position
+// and releases the MMA issuer.  The log-sum-exp and the drawn logit need the
+// full merge of the partials; the CTAs share it out by request and do it
+// while the MMA starts the next position.  The TMA producer never stops at
+// the boundaries: W2 and the next position's U do not depend on the drawn
+// tokens.  Partial states alternate between two buffers, so a fast CTA
+// never overwrites the ones a slow CTA still merges: the buffer of position
+// k is written again at k + 2, after the grid barrier of k + 1, which no CTA
+// reaches before its merges of k are done.
+// 19 warps over 4 schedulers put 5 warps on three of them, whose 16384
+// registers then allow 96 a thread.
 template <bool kResid, typename TT>
 __global__ void __launch_bounds__(kThreads, 1)
 rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_last) {
@@ -212,7 +279,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), 1); }
-        for (int i = 0; i < US; ++i) { ptx::mbar_init(ufull(i), 1); ptx::mbar_init(uempty(i), 4u); }
+        for (int i = 0; i < US; ++i) { ptx::mbar_init(ufull(i), 1); ptx::mbar_init(uempty(i), 1); }
         for (int i = 0; i < kAcc; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(a_ready, 1);
@@ -220,7 +287,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         *never = 0u;
         ptx::fence_mbar_init();
     }
-    if (tid == kProducerWarp * 32) { ptx::prefetch_tmap(&a.w2map); ptx::prefetch_tmap(&a.umap); }
+    if (tid == kProducerWarp * 32) ptx::prefetch_tmap(&a.w2map);
+    if (tid == kUWarp * 32 && !kResid) {
+        ptx::prefetch_tmap(&a.umap);
+        ptx::prefetch_tmap(&a.upf);
+    }
     if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 128u * kAcc); ptx::tmem_relinquish(); }
     for (int n = tid; n < 128; n += kThreads) {
         int x = -1, prow = -1;
@@ -238,7 +309,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         s_row[n] = prow;
     }
     __syncthreads();
-    stage_h(gbase + L.a, W1, s_tok, NC, RF, KCH, r, tid, kThreads, true);
+    stage_h(gbase + L.a, W1, s_tok, NC, RF, KCH, r, tid, kThreads);
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
@@ -247,16 +318,15 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     const int ntiles = (V + kTN * RF - 1) / (kTN * RF);   // super-tiles of RF vocabulary tiles
 
     if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ W2 producer
         if (lane == 0) {
-            const uint64_t pol_w = ptx::policy_evict_last(), pol_u = ptx::policy_evict_first();
+            const uint64_t pol_w = ptx::policy_evict_last();
             int stage = 0, site = 0;
             uint32_t ph = 0;
             bool ok = true;
-            int lt = 0;                                  // U slices issued / 4, over all positions
-            long long nw = 0, nu = 0;                    // W2 chunks and U slices issued
+            long long nw = 0;                            // W2 chunks issued
             for (int k = k_first; k <= k_last && ok; ++k) {
-                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                     const int vs = t * kTN * RF;
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
@@ -270,7 +340,30 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                             if (++stage == kStages) { stage = 0; ph ^= 1u; }
                         }
                     }
-                    for (int c = 0; c < 4 && ok && !kResid; ++c) {
+                }
+            }
+            if (!ok) { raise_timeout(p.ws.status, site); *abort_flag = 1u; }
+            // every copy issued lands before the CTA leaves: wait for the last
+            // fill of each stage (already complete on the normal path)
+            for (int i = 0; i < kStages; ++i)
+                if (nw > i) {
+                    const long long m = (nw - 1) - ((nw - 1 - i) % kStages);
+                    ptx::mbar_wait(full(i), (uint32_t)((m / kStages) & 1), never, kDrainCycles);
+                }
+        }
+        __syncwarp();
+    } else if (warp == kUWarp) {
+        // ------------------------------------------------------------ U producer (draft)
+        if (lane == 0 && !kResid) {
+            const uint64_t pol_u = ptx::policy_evict_first();
+            int site = 0;
+            bool ok = true;
+            int lt = 0;                                  // tiles issued, over all positions
+            long long nu = 0;                            // U slices issued
+            for (int k = k_first; k <= k_last && ok; ++k) {
+                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+                    const int vs = t * kTN * RF;
+                    for (int c = 0; c < 4 && ok; ++c) {
                         const int n = lt * 4 + c, s = n % US;
                         const uint32_t par = (uint32_t)((n / US) & 1);
                         if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) { site = 2; break; }
@@ -280,17 +373,18 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                                              vs + i * kTN + 32 * c, k - 1, b_base, ufull(s), pol_u);
                         ++nu;
                     }
+                    if (ok) {
+                        // the U of this CTA's next tile into L2: its slot loads
+                        // then wait on L2 rather than HBM
+                        int tn = t + (int)gridDim.x, kn = k;
+                        if (tn >= ntiles) { tn = blockIdx.x; ++kn; }
+                        if (kn <= k_last)
+                            for (int i = 0; i < RF; ++i)
+                                ptx::tma_prefetch_3d(&a.upf, tn * kTN * RF + i * kTN, kn - 1, b_base);
+                    }
                 }
             }
             if (!ok) { raise_timeout(p.ws.status, site); *abort_flag = 1u; }
-            // Every copy issued lands before the CTA leaves: wait for the last
-            // fill of each stage and slot (already complete on the normal path,
-            // where the readers waited for them).
-            for (int i = 0; i < kStages; ++i)
-                if (nw > i) {
-                    const long long m = (nw - 1) - ((nw - 1 - i) % kStages);
-                    ptx::mbar_wait(full(i), (uint32_t)((m / kStages) & 1), never, kDrainCycles);
-                }
             for (int i = 0; i < US; ++i)
                 if (nu > i) {
                     const long long m = (nu - 1) - ((nu - 1 - i) % US);
@@ -302,7 +396,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTN, /*A K-major*/ false, /*B MN-major*/ true);
-            int stage = 0, acc = 0, site = 0;
+            int stage = 0, acc = 0, site = 0, lt = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
             for (int k = k_first; k <= k_last && ok; ++k) {
@@ -311,10 +405,30 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     site = 3;
                     break;
                 }
-                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
                     if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) { site = 4; break; }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTN);
+                    if constexpr (!kResid) {
+                        // the accumulator starts as the tile's U: four 32-column slices
+                        // (128 rows x 128 B, 128-byte swizzle) copied 32 bytes a row at a
+                        // time; the MMAs below then add h.W2 on top
+                        for (int c = 0; c < 4 && ok; ++c) {
+                            const int n = lt * 4 + c, s = n % US;
+                            if (!(ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles))) {
+                                site = 9;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            const uint32_t src = base + L.u + (uint32_t)s * slot_bytes;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                ptx::tmem_cp_128x256b(d_tmem + (uint32_t)(32 * c + 8 * j),
+                                                      ptx::smem_desc_sw128(src + 32 * j, 16, 1024));
+                            ptx::mma_commit(uempty(s));     // the slot is free once the copies have read it
+                        }
+                        if (!ok) break;
+                    }
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
                             if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) { site = 5; break; }
@@ -329,7 +443,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                                 // B: MN-major, 64-entry swizzle atoms 8 KB apart along N (LBO),
                                 //    8-rank groups 1 KB apart along K (SBO); 16 ranks = 2 KB.
                                 const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
-                                ptx::mma_f16(d_tmem, ad, bd, idesc, (i | j | kk) != 0 ? 1u : 0u);
+                                ptx::mma_f16(d_tmem, ad, bd, idesc, (!kResid || (i | j | kk) != 0) ? 1u : 0u);
                             }
                             ptx::mma_commit(empty(stage));
                             if (++stage == kStages) { stage = 0; ph ^= 1u; }
@@ -355,7 +469,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         const int b = b_base + nrow;
         const bool real = active && nrow < nb && (!kResid || s_row[nrow] >= 0);
         const float scale2 = p.inv_tau * 1.4426950408889634f;      // z -> z * log2(e)
-        int acc = 0, lt = 0;
+        int acc = 0;
         uint32_t aph = 0;
         bool failed = false;
         for (int k = k_first; k <= k_last && !failed; ++k) {
@@ -369,13 +483,14 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             if (kResid && real) lse = p.ws.lse_rej[b];
             DrawLse st = drawlse_empty();            // idx, zb (u + bias of the winner), s
             float rz2 = -INFINITY, rE2 = INFINITY;     // winner's z*log2e and E2
+            float rE2h = INFINITY;                     // rE2 * kRaceRel: the screen's threshold
             Draw2 st2 = draw2_empty();
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
                 bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 6); failed = true; break; }
                 ptx::tc_fence_after();
-                float bias[32];
+                float bias[32];              // draft: U + h.W2; residual: h.W2
                 if (active) {
                     ptx::tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kTN + 32 * cb), bias);
                     ptx::tmem_wait_ld();
@@ -457,62 +572,55 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         }
                     }
                     __syncwarp();
-                } else {
-                    const int n = lt * 4 + cb, s = n % US;
-                    ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 7); failed = true; break; }
-                    if (real) {
-                        // Exponential race in base-2 units: the winner minimises
-                        // E2_v * 2^(-z2_v), z2 = z*log2e; with the winner's z2 as the
-                        // log-sum-exp reference the race and the sum share one exp2:
-                        //   t_v = 2^(z2_v - z2_best),  v wins iff E2_v < E2_best * t_v.
-                        const uint8_t* srow = gbase + L.u + (size_t)s * slot_bytes + (size_t)row * 128;
-                        const int nq = min(8, (V - v0) >> 2);   // quads inside the vocabulary
+                } else if (real) {
+                    // The accumulator holds z*tau = U + h.W2 (it started as the tile's U).
+                    // Exponential race in base-2 units: the winner minimises
+                    // E2_v * 2^(-z2_v), z2 = z*log2e; with the winner's z2 as the
+                    // log-sum-exp reference the race and the sum share one exp2:
+                    //   t_v = 2^(z2_v - z2_best),  v wins iff E2_v < E2_best * t_v.
+                    const int nq = min(8, (V - v0) >> 2);   // quads inside the vocabulary
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            if (c < nq) {
-                                const int vq = v0 + 4 * c;
-                                const float4 u4 = *reinterpret_cast<const float4*>(srow + ((c ^ (row & 7)) << 4));
-                                const float us[4] = {u4.x + bias[4 * c], u4.y + bias[4 * c + 1],
-                                                     u4.z + bias[4 * c + 2], u4.w + bias[4 * c + 3]};
-                                if (p.logits_out)
-                                    *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(
-                                        us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
-                                const uint4 w = rng.quad((uint32_t)vq >> 2);
-                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                                float z2[4], E2[4], t[4];
-                                bool any_win = false;
+                    for (int c = 0; c < 8; ++c) {
+                        if (c < nq) {
+                            const int vq = v0 + 4 * c;
+                            const float us[4] = {bias[4 * c], bias[4 * c + 1], bias[4 * c + 2], bias[4 * c + 3]};
+                            if (p.logits_out)
+                                *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(
+                                    us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
+                            const uint4 w = rng.quad((uint32_t)vq >> 2);
+                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                            float t[4];
+                            bool cand = false;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                t[e] = fast_exp2(fmaf(us[e], scale2, -rz2));
+                                // screen with the bare hardware log2: it equals E2 for
+                                // u <= 7/8 and is within ~2^-22 of it above, which the
+                                // margins of rE2h and kRaceSlack cover
+                                cand |= -fast_log2(uniform_of(ws[e])) < fmaf(rE2h, t[e], kRaceSlack);
+                            }
+                            if (!cand) {
+                                st.s += (t[0] + t[1]) + (t[2] + t[3]);
+                            } else {
+                                // rare: the quad one entry at a time with the exact E2.
+                                // Entries come in increasing v, so the strict comparison keeps
+                                // the lowest index on exact ties.  The empty state (rz2 = -inf,
+                                // rE2 = +inf, s = 0) makes the first entry win with s = 1.
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    z2[e] = us[e] * scale2;
-                                    E2[e] = exp2_variate_of(ws[e]);
-                                    t[e] = fast_exp2(z2[e] - rz2);
-                                    any_win |= E2[e] < rE2 * t[e];
-                                }
-                                if (!any_win) {
-                                    st.s += (t[0] + t[1]) + (t[2] + t[3]);
-                                } else {
-                                    // rare: re-run the quad one entry at a time.  Entries come in
-                                    // increasing v, so the strict comparison keeps the lowest index
-                                    // on exact ties.  The empty state (rz2 = -inf, rE2 = +inf, s = 0)
-                                    // makes the first entry win with s = 1.
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const float te = fast_exp2(z2[e] - rz2);
-                                        if (E2[e] < rE2 * te) {
-                                            st.s = st.s * fast_exp2(rz2 - z2[e]) + 1.f;
-                                            rz2 = z2[e]; rE2 = E2[e]; st.idx = vq + e; st.zb = us[e];
-                                        } else {
-                                            st.s += te;
-                                        }
+                                    const float E2 = exp2_variate_of(ws[e]);
+                                    const float te = fast_exp2(fmaf(us[e], scale2, -rz2));
+                                    if (E2 < rE2 * te) {
+                                        st.s = st.s * fast_exp2(fmaf(-us[e], scale2, rz2)) + 1.f;
+                                        rz2 = us[e] * scale2; rE2 = E2; rE2h = E2 * kRaceRel;
+                                        st.idx = vq + e; st.zb = us[e];
+                                    } else {
+                                        st.s += te;
                                     }
                                 }
                             }
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(uempty(s));
                 }
             }
             // ---- this position's partial state per request: fold RF tiles x 4 column blocks
@@ -548,10 +656,13 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 #pragma unroll
                         for (int c = 0; c < 4; ++c) s1 = drawlse_merge(s1, s_merge[c * 128 + i * NC + etid]);
                     part_buf[(size_t)(b_base + etid) * p.ws.parts + blockIdx.x] = s1;
+                    // the draw itself is decided by an atomic maximum over the CTAs
+                    if (persistent)
+                        atomicMax(&p.ws.win[((size_t)(k - 1) * p.B + b_base + etid) * kWinStride], win_key(s1));
                 }
                 __threadfence();
             }
-            if (!persistent) break;
+            if (kResid || !persistent) break;
             // ---- grid barrier, then every CTA merges the partials of its own requests
             ptx::named_barrier(1, 32 * kEpiWarps);
             __shared__ int s_gb_ok;
@@ -563,35 +674,43 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 *abort_flag = 1u;
                 break;
             }
-            for (int n = warp; n < nb; n += kEpiWarps) {
-                const DrawLse* part = part_buf + (size_t)(b_base + n) * p.ws.parts;
+            // this position's draws: one load per request
+            for (int n = etid; n < nb; n += 32 * kEpiWarps)
+                s_tok[n] = win_token(__ldcg(&p.ws.win[((size_t)(k - 1) * p.B + b_base + n) * kWinStride]));
+            ptx::named_barrier(1, 32 * kEpiWarps);
+            if (k < k_last) {
+                // ---- h = W1[x~_k] for the next position (the MMA of this one is
+                //      complete: its last commit released the final tile just read)
+                stage_h_rows(gbase + L.a, W1, s_tok, NC, RF, KCH, r, etid, 32 * kEpiWarps);
+                ptx::fence_proxy_async_smem();
+                ptx::named_barrier(1, 32 * kEpiWarps);
+                if (etid == 0) ptx::mbar_arrive(a_ready);
+            }
+            // ---- this position's outputs, while the MMA starts the next one: the
+            //      CTAs share the requests, a warp folds one request's partials
+            for (int n = blockIdx.x + warp * (int)gridDim.x; n < nb; n += kEpiWarps * (int)gridDim.x) {
+                const float4* part = reinterpret_cast<const float4*>(part_buf + (size_t)(b_base + n) * p.ws.parts);
                 DrawLse m = drawlse_empty();
-                for (int i = lane; i < (int)gridDim.x; i += 32) {
-                    DrawLse c;
-                    c.best = __ldcg(&part[i].best); c.idx = __ldcg(&part[i].idx);
-                    c.zb = __ldcg(&part[i].zb); c.s = __ldcg(&part[i].s);
-                    m = drawlse_merge(m, c);
+                for (int i0 = lane; i0 < (int)gridDim.x; i0 += 4 * 32) {
+                    float4 c[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = i0 + 32 * u;
+                        c[u] = i < (int)gridDim.x ? __ldcg(part + i) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) m = drawlse_merge(m, drawlse_of(c[u]));
                 }
 #pragma unroll
                 for (int sh = 1; sh < 32; sh <<= 1) m = drawlse_merge(m, shfl_xor(m, sh));
                 if (lane == 0) {
-                    s_tok[n] = m.idx;
-                    if (blockIdx.x == 0) {
-                        const size_t o = (size_t)(b_base + n) * gamma + (k - 1);
-                        p.draft_tok[o] = m.idx;
-                        p.lse_q[o] = m.best + logf(m.s);
-                        p.z_tok[o] = m.zb;
-                    }
+                    const size_t o = (size_t)(b_base + n) * gamma + (k - 1);
+                    p.draft_tok[o] = m.idx;
+                    p.lse_q[o] = m.best + logf(m.s);
+                    p.z_tok[o] = m.zb;
                 }
             }
             if (k == k_last) break;
-            ptx::named_barrier(1, 32 * kEpiWarps);
-            // ---- h = W1[x~_k] for the next position (the MMA of this one is complete:
-            //      its last commit released the final tile the warps just read)
-            stage_h(gbase + L.a, W1, s_tok, NC, RF, KCH, r, etid, 32 * kEpiWarps, false);
-            ptx::fence_proxy_async_smem();
-            ptx::named_barrier(1, 32 * kEpiWarps);
-            if (etid == 0) ptx::mbar_arrive(a_ready);
         }
         if (failed) *abort_flag = 1u;
     }
@@ -604,14 +723,19 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     }
 
     if (persistent) {
-        // the last CTA out clears the barrier counters for the next call
+        // the last CTA out clears the barrier counters and the winner keys for
+        // the next call (every CTA has read its winners before it got here)
+        __shared__ int s_out_last;
         if (tid == 0) {
             __threadfence();
-            const unsigned prev = atomicAdd(p.ws.gbar + kGridBarrierSlots, 1u);
-            if (prev == nctas - 1) {
-                for (int i = 0; i <= kGridBarrierSlots; ++i) p.ws.gbar[i] = 0u;
-                __threadfence();
-            }
+            s_out_last = atomicAdd(p.ws.gbar + kGridBarrierSlots, 1u) == nctas - 1;
+        }
+        __syncthreads();
+        if (s_out_last) {
+            __threadfence();
+            for (int i = tid; i < p.gamma * p.B; i += kThreads) p.ws.win[(size_t)i * kWinStride] = 0ull;
+            if (tid <= kGridBarrierSlots) p.ws.gbar[tid] = 0u;
+            __threadfence();
         }
         return;
     }
@@ -720,6 +844,16 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
         const cuuint32_t es[3] = {1, 1, 1};
         if (enc(&a.umap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(p.U), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)p.gamma, (cuuint64_t)p.B};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.V * 4, (cuuint64_t)p.gamma * p.V * 4};
+        const cuuint32_t box[3] = {(cuuint32_t)kTN, 1, (cuuint32_t)a.NC};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&a.upf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(p.U), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }

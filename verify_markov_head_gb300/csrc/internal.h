@@ -19,10 +19,11 @@ constexpr int kPartTile = 128;         // vocabulary entries per tile of the par
 constexpr int kVerifySeg = 32768;      // vocabulary entries per verify-stream work item
 constexpr int kChunk = 16;             // requests per chunk of the partial-producing kernels
 constexpr int kGridBarrierSlots = DSPARK_MAX_GAMMA;   // one grid-barrier counter per draft position
+constexpr int kWinStride = 16;          // winner keys 128 bytes apart: one cache line each
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, tickets, gbar, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, total;
+    size_t status, tickets, gbar, win, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -33,6 +34,8 @@ struct WsPtrs {
     uint32_t* tickets_draft;   // [ceil(B/kChunk)] arrival counters, zero between launches
     uint32_t* tickets_resid;   // [ceil(B/kChunk)]
     uint32_t* gbar;            // [kGridBarrierSlots + 1] grid-barrier counters, then the exit counter
+    unsigned long long* win;   // [gamma][B][kWinStride] winner keys of the persistent draft (first of
+                               // each line used), zero between launches
     DrawLse* draft_part;       // [2][B][parts] (two buffers alternate between positions)
     LseDraw* verify_part;
     int32_t* rej;        // [B] 0-based rejected row, -1 if every walked draft was accepted
