@@ -129,15 +129,13 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target, con
     __threadfence();
     atomicAdd(ctr, 1u);
     const long long t0 = clock64();
-    uint32_t ns = 64;
     for (;;) {
         uint32_t v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
         if (v >= target) break;
         if (*abort) return false;
         if (clock64() - t0 > limit_cycles) return false;
-        __nanosleep(ns);
-        if (ns < 512) ns <<= 1;
+        __nanosleep(32);
     }
     __threadfence();
     return true;
@@ -147,6 +145,8 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target, con
 // H_j (K-chunk j, 64 ranks) is [NC rows][128 B] at block index
 // (RF - 1) + j * RF, zero blocks between them.  16-byte unit u of row n sits
 // at unit u ^ (n mod 8).
+__device__ __forceinline__ void stage_h_rows(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC,
+                                             int RF, int KCH, int r, int t0, int nthreads);
 __device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC, int RF,
                                         int KCH, int r, int t0, int nthreads) {
     const uint32_t blk = (uint32_t)NC * 128u;
@@ -155,17 +155,10 @@ __device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, c
     for (int idx = t0; idx < units; idx += nthreads) {
         const int bi = idx / (NC * 8), rem = idx - bi * (NC * 8);
         const int rel = bi - (RF - 1);
-        const bool h_block = rel >= 0 && rel % RF == 0;
-        const int n = rem >> 3, uu = rem & 7;     // row in block, physical 16-byte unit
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (h_block) {
-            const int j = rel / RF;
-            const int u = uu ^ (n & 7);            // logical unit stored at this position
-            const int x = s_tok[n];
-            if (x >= 0) val = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)(j * 64 + u * 8));
-        }
-        *reinterpret_cast<uint4*>(a_region + (size_t)bi * blk + (size_t)n * 128 + (uu << 4)) = val;
+        if (rel >= 0 && rel % RF == 0) continue;             // an h block
+        *reinterpret_cast<uint4*>(a_region + (size_t)bi * blk + (size_t)rem * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
+    stage_h_rows(a_region, W1, s_tok, NC, RF, KCH, r, t0, nthreads);
 }
 
 // The h blocks alone (the zero blocks are already in place): every thread
@@ -213,6 +206,35 @@ __device__ __forceinline__ unsigned long long win_key(const DrawLse& d) {
 }
 __device__ __forceinline__ int win_token(unsigned long long key) {
     return (int)(0xFFFFFFFFu - (uint32_t)key);
+}
+
+// One warp stages a 32-entry segment [v0, v0 + 32) of 32 rows (one per lane,
+// row pointers in the lanes' `row`) into a shared buffer of 32 x (32 * sizeof(T))
+// bytes: 16-byte asynchronous copies, a row's segment spread over consecutive
+// lanes, rows of lanes outside `mask` skipped, entries past V zero-filled.
+// The 16-byte chunk index is swizzled with the row (XOR with row % 8 for
+// 128-byte rows, (row / 2) % 4 for 64-byte rows) so that a lane reading its
+// own row meets no bank conflict.  On return the whole buffer is visible to
+// the warp.
+template <typename T>
+__device__ __forceinline__ void stage_rows(uint32_t buf, const T* row, unsigned mask, int v0, int V, int lane) {
+    constexpr int kRowBytes = 32 * (int)sizeof(T);
+    constexpr int kChunks = kRowBytes / 16;           // 8 (fp32) or 4 (bf16)
+    constexpr int kRowsPerPass = 32 / kChunks;
+    constexpr int kPerChunk = 16 / (int)sizeof(T);    // entries per chunk
+#pragma unroll
+    for (int j = 0; j < 32 / kRowsPerPass; ++j) {
+        const int rr = j * kRowsPerPass + lane / kChunks, c = lane % kChunks;
+        const T* src = reinterpret_cast<const T*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(row), rr));
+        if ((mask >> rr) & 1u) {
+            const int vq = v0 + c * kPerChunk;
+            const int swz = kChunks == 8 ? (rr & 7) : ((rr >> 1) & 3);
+            const bool in = vq < V;
+            ptx::cp_async_16(buf + (uint32_t)(rr * kRowBytes + ((c ^ swz) << 4)), in ? src + vq : src, in ? 16u : 0u);
+        }
+    }
+    ptx::cp_async_wait_all();
+    __syncwarp();
 }
 
 __device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
@@ -374,13 +396,14 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         ++nu;
                     }
                     if (ok) {
-                        // the U of this CTA's next tile into L2: its slot loads
-                        // then wait on L2 rather than HBM
+                        // the U of this CTA's next tile into L2 (evict-first, like
+                        // its loads, so W2 keeps its place): its slot loads then
+                        // wait on L2 rather than HBM
                         int tn = t + (int)gridDim.x, kn = k;
                         if (tn >= ntiles) { tn = blockIdx.x; ++kn; }
                         if (kn <= k_last)
                             for (int i = 0; i < RF; ++i)
-                                ptx::tma_prefetch_3d(&a.upf, tn * kTN * RF + i * kTN, kn - 1, b_base);
+                                ptx::tma_prefetch_3d(&a.upf, tn * kTN * RF + i * kTN, kn - 1, b_base, pol_u);
                     }
                 }
             }
@@ -481,6 +504,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + urow) * V;
             float2 lse = make_float2(0.f, 0.f);
             if (kResid && real) lse = p.ws.lse_rej[b];
+            const float lse_p2 = lse.x * 1.4426950408889634f, lse_q2 = lse.y * 1.4426950408889634f;
+            // residual mode: E / r of the r-draw's winner, E / p of the p-draw's
+            // (+inf: none yet), and the screens' thresholds
+            float Kr = INFINITY, Kp = INFINITY, Krh = INFINITY, Kph = INFINITY;
             DrawLse st = drawlse_empty();            // idx, zb (u + bias of the winner), s
             float rz2 = -INFINITY, rE2 = INFINITY;     // winner's z*log2e and E2
             float rE2h = INFINITY;                     // rE2 * kRaceRel: the screen's threshold
@@ -504,69 +531,72 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 if constexpr (kResid) {
                     // The rejected rows differ per request, so the warp stages its 32
                     // rows of U and then of the target through a 4 KB shared buffer:
-                    // coalesced loads (8 lanes per 128-byte row segment), 128-byte
-                    // swizzle on the chunk index, then each lane reads its own row.
+                    // asynchronous 16-byte copies (a row segment spread over
+                    // consecutive lanes, all of them in flight at once), swizzled on
+                    // the chunk index, then each lane reads its own row.
                     uint8_t* wbuf = gbase + L.u + (size_t)warp * 4096;
                     const unsigned real_mask = __ballot_sync(0xffffffffu, real);
                     float* z = bias;                           // z overwrites the bias in place
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int rr = 4 * j + (lane >> 3), c = lane & 7;
-                        const float* src = reinterpret_cast<const float*>(
-                            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(Urow), rr));
-                        if ((real_mask >> rr) & 1u) {
-                            const int vq = v0 + 4 * c;
-                            const float4 x = (vq < V) ? __ldcs(reinterpret_cast<const float4*>(src + vq))
-                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                            *reinterpret_cast<float4*>(wbuf + rr * 128 + ((c ^ (rr & 7)) << 4)) = x;
-                        }
-                    }
-                    __syncwarp();
+                    stage_rows<float>(base + L.u + (uint32_t)warp * 4096u, Urow, real_mask, v0, V, lane);
                     if (real) {
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             const float4 u4 = *reinterpret_cast<const float4*>(wbuf + lane * 128 + ((c ^ (lane & 7)) << 4));
-                            z[4 * c] = (u4.x + bias[4 * c]) * p.inv_tau;
-                            z[4 * c + 1] = (u4.y + bias[4 * c + 1]) * p.inv_tau;
-                            z[4 * c + 2] = (u4.z + bias[4 * c + 2]) * p.inv_tau;
-                            z[4 * c + 3] = (u4.w + bias[4 * c + 3]) * p.inv_tau;
+                            z[4 * c] = u4.x + bias[4 * c];               // z * tau
+                            z[4 * c + 1] = u4.y + bias[4 * c + 1];
+                            z[4 * c + 2] = u4.z + bias[4 * c + 2];
+                            z[4 * c + 3] = u4.w + bias[4 * c + 3];
                         }
                     }
                     __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int rr = 4 * j + (lane >> 3), c = lane & 7;
-                        const TT* src = reinterpret_cast<const TT*>(
-                            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(Trow), rr));
-                        if ((real_mask >> rr) & 1u) {
-                            const int vq = v0 + 4 * c;
-                            const float4 x = (vq < V) ? Vec4<TT>::load_stream(src + vq) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            *reinterpret_cast<float4*>(wbuf + rr * 128 + ((c ^ (rr & 7)) << 4)) = x;
-                        }
-                    }
-                    __syncwarp();
+                    stage_rows<TT>(base + L.u + (uint32_t)warp * 4096u, Trow, real_mask, v0, V, lane);
                     if (real) {
+                        // Both draws as exponential races (argmax log w_v + G_v =
+                        // argmin E_v / w_v, E = -ln u): the residual law r = max(0, p - q)
+                        // and the fallback law p share E.  A quad is screened with the
+                        // bound E >= 1 - u (exact from the bits, no logarithm) against
+                        // the running minima, with margins above the rounding of the
+                        // products and of E; quads that pass are re-run with the exact
+                        // E, entries in increasing v (strict comparisons keep the lowest
+                        // index on exact ties).
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             const int vq = v0 + 4 * c;
                             if (vq < V) {
-                                const float4 t4 = *reinterpret_cast<const float4*>(wbuf + lane * 128 + ((c ^ (lane & 7)) << 4));
-                                const float ts[4] = {t4.x, t4.y, t4.z, t4.w};
+                                float ts[4];
+                                if constexpr (sizeof(TT) == 4) {
+                                    const float4 t4 =
+                                        *reinterpret_cast<const float4*>(wbuf + lane * 128 + ((c ^ (lane & 7)) << 4));
+                                    ts[0] = t4.x; ts[1] = t4.y; ts[2] = t4.z; ts[3] = t4.w;
+                                } else {
+                                    const uint2 h4 = *reinterpret_cast<const uint2*>(
+                                        wbuf + lane * 64 + (((c >> 1) ^ ((lane >> 1) & 3)) << 4) + ((c & 1) << 3));
+                                    ts[0] = __uint_as_float(h4.x << 16); ts[1] = __uint_as_float(h4.x & 0xffff0000u);
+                                    ts[2] = __uint_as_float(h4.y << 16); ts[3] = __uint_as_float(h4.y & 0xffff0000u);
+                                }
                                 const uint4 w = rng.quad((uint32_t)vq >> 2);
                                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                                float pv[4], rv[4];
+                                bool cand = false;
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const float zz = z[4 * c + e];
-                                    const float tv = ts[e] * p.inv_tau;
-                                    const float g = gumbel_of(ws[e]);
-                                    const float pr = __expf(tv - lse.x) - __expf(zz - lse.y);
-                                    const int idx = vq + e;
-                                    if (pr > 0.f) {
-                                        const float sc = __logf(pr) + g;
-                                        if (wins(sc, idx, st2.best_r, st2.idx_r)) { st2.best_r = sc; st2.idx_r = idx; }
+                                    pv[e] = fast_exp2(fmaf(ts[e], scale2, -lse_p2));
+                                    rv[e] = pv[e] - fast_exp2(fmaf(z[4 * c + e], scale2, -lse_q2));
+                                    const float wv = one_minus_uniform_of(ws[e]);
+                                    cand |= (rv[e] > 0.f && wv < fmaf(Krh, rv[e], kRaceSlack)) ||
+                                            wv < fmaf(Kph, pv[e], kRaceSlack);
+                                }
+                                if (cand) {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float E = exp2_variate_of(ws[e]) * kLn2;
+                                        if (rv[e] > 0.f && E < rv[e] * Kr) {
+                                            Kr = E / rv[e]; Krh = Kr * kRaceRel; st2.idx_r = vq + e;
+                                        }
+                                        if (E < pv[e] * Kp) {
+                                            Kp = E / pv[e]; Kph = Kp * kRaceRel; st2.idx_p = vq + e;
+                                        }
                                     }
-                                    const float sp = tv + g;
-                                    if (wins(sp, idx, st2.best_p, st2.idx_p)) { st2.best_p = sp; st2.idx_p = idx; }
                                 }
                             }
                         }
@@ -625,6 +655,9 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             }
             // ---- this position's partial state per request: fold RF tiles x 4 column blocks
             if constexpr (kResid) {
+                // back to scores: log w_v + G_v = -ln(E_v / w_v)
+                st2.best_r = Kr < INFINITY ? -logf(Kr) : -INFINITY;
+                st2.best_p = Kp < INFINITY ? -logf(Kp) : -INFINITY;
                 reinterpret_cast<Draw2*>(s_merge)[cb * 128 + row] = st2;
             } else {
                 // back to the Gumbel score in natural units: with E = E2 * ln 2 the
@@ -660,7 +693,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     if (persistent)
                         atomicMax(&p.ws.win[((size_t)(k - 1) * p.B + b_base + etid) * kWinStride], win_key(s1));
                 }
-                __threadfence();
+                // one launch per position: the ticket merge below reads these; the
+                // persistent loop orders them by the grid barrier's fence instead
+                // (after the epilogue's barrier, the fence covers the whole CTA's writes)
+                if (!persistent) __threadfence();
             }
             if (kResid || !persistent) break;
             // ---- grid barrier, then every CTA merges the partials of its own requests
@@ -752,22 +788,39 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    // TM = 512 / NC consecutive threads per request, each folding every TM-th
+    // partial with all loads of a batch in flight, then a shuffle merge
     const int k = k_first;
-    for (int n = warp; n < nb; n += kThreads / 32) {
+    const int TM = (32 * kEpiWarps) / NC;
+    const int n = tid / TM, sub = tid - n * TM;
+    const int nparts = (int)gridDim.x;
+    constexpr int kBatch = 5;
+    if (tid < 32 * kEpiWarps) {
         const int bb = b_base + n;
         if constexpr (kResid) {
-            if (s_row[n] < 0) continue;
-            const Draw2* part = p.ws.resid_part + (size_t)bb * p.ws.parts;
             Draw2 m = draw2_empty();
-            for (int i = lane; i < (int)gridDim.x; i += 32) {
-                Draw2 c;
-                c.best_r = __ldcg(&part[i].best_r); c.idx_r = __ldcg(&part[i].idx_r);
-                c.best_p = __ldcg(&part[i].best_p); c.idx_p = __ldcg(&part[i].idx_p);
-                m = draw2_merge(m, c);
-            }
+            if (n < nb && s_row[n] >= 0) {
+                const float4* part = reinterpret_cast<const float4*>(p.ws.resid_part + (size_t)bb * p.ws.parts);
+                for (int i0 = sub; i0 < nparts; i0 += kBatch * TM) {
+                    float4 c[kBatch];
 #pragma unroll
-            for (int sh = 1; sh < 32; sh <<= 1) m = draw2_merge(m, shfl_xor(m, sh));
-            if (lane == 0) {
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int i = i0 + u * TM;
+                        c[u] = i < nparts ? __ldcg(part + i)
+                                          : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY,
+                                                        __int_as_float(0x7fffffff));
+                    }
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        Draw2 d;
+                        d.best_r = c[u].x; d.idx_r = __float_as_int(c[u].y);
+                        d.best_p = c[u].z; d.idx_p = __float_as_int(c[u].w);
+                        m = draw2_merge(m, d);
+                    }
+                }
+            }
+            for (int sh = 1; sh < TM; sh <<= 1) m = draw2_merge(m, shfl_xor(m, sh));
+            if (sub == 0 && n < nb && s_row[n] >= 0) {
                 if (m.best_r > -INFINITY) {
                     p.ws.fin[bb] = m.idx_r;
                 } else {
@@ -776,17 +829,23 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 }
             }
         } else {
-            const DrawLse* part = p.ws.draft_part + (size_t)((k - 1) & 1) * p.B * p.ws.parts + (size_t)bb * p.ws.parts;
             DrawLse m = drawlse_empty();
-            for (int i = lane; i < (int)gridDim.x; i += 32) {
-                DrawLse c;
-                c.best = __ldcg(&part[i].best); c.idx = __ldcg(&part[i].idx);
-                c.zb = __ldcg(&part[i].zb); c.s = __ldcg(&part[i].s);
-                m = drawlse_merge(m, c);
-            }
+            if (n < nb) {
+                const float4* part = reinterpret_cast<const float4*>(
+                    p.ws.draft_part + (size_t)((k - 1) & 1) * p.B * p.ws.parts + (size_t)bb * p.ws.parts);
+                for (int i0 = sub; i0 < nparts; i0 += kBatch * TM) {
+                    float4 c[kBatch];
 #pragma unroll
-            for (int sh = 1; sh < 32; sh <<= 1) m = drawlse_merge(m, shfl_xor(m, sh));
-            if (lane == 0) {
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int i = i0 + u * TM;
+                        c[u] = i < nparts ? __ldcg(part + i) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) m = drawlse_merge(m, drawlse_of(c[u]));
+                }
+            }
+            for (int sh = 1; sh < TM; sh <<= 1) m = drawlse_merge(m, shfl_xor(m, sh));
+            if (sub == 0 && n < nb) {
                 const size_t o = (size_t)bb * gamma + (k - 1);
                 p.draft_tok[o] = m.idx;
                 p.lse_q[o] = m.best + logf(m.s);
