@@ -120,6 +120,9 @@ dspark_status dspark_draft_markov(
  *          definition (an embedding table); passing W1 with e = r follows
  *          [P2], which reuses the Markov head's W1 rows.
  * Outputs: conf_cal [B,gamma], log_surv [B,gamma] (non-increasing in k).
+ * ws     : a workspace of at least dspark_workspace_bytes(B, gamma, V, r) bytes
+ *          (any r), 256-byte aligned, cleared once: the call keeps per-request
+ *          arrival counters and the raw scores there.
  */
 dspark_status dspark_confidence_sts(
     const float* h, int d,

@@ -42,6 +42,7 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.fin = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
     L.lse_rej = o;     o = align256(o + sizeof(float2) * (size_t)B);
     L.resid_part = o;  o = align256(o + sizeof(Draw2) * (size_t)B * L.parts);
+    L.conf = o;        o = align256(o + sizeof(uint32_t) * (size_t)B + sizeof(float) * (size_t)B * gamma);
     L.total = o;
     return L;
 }
@@ -62,6 +63,8 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     P.fin = reinterpret_cast<int32_t*>(base + L.fin);
     P.lse_rej = reinterpret_cast<float2*>(base + L.lse_rej);
     P.resid_part = reinterpret_cast<Draw2*>(base + L.resid_part);
+    P.conf_tickets = reinterpret_cast<uint32_t*>(base + L.conf);
+    P.conf_score = reinterpret_cast<float*>(base + L.conf + sizeof(uint32_t) * (size_t)B);
     P.nseg = L.nseg;
     P.parts = L.parts;
     return P;
@@ -180,12 +183,16 @@ dspark_status dspark_confidence_sts(const float* h, int d, const void* emb, dspa
         !is_device_ptr(w_c) || !is_device_ptr(T) || !is_device_ptr(conf_cal) || !is_device_ptr(log_surv) ||
         !is_device_ptr(ws))
         return DSPARK_ERR_INVALID;
-    if (!aligned(h, 16) || !aligned(emb, 16) || !aligned(w_c, 16) || ws_bytes < 256) return DSPARK_ERR_INVALID;
+    if (!aligned(h, 16) || !aligned(emb, 16) || !aligned(w_c, 16) || !aligned(ws, 256)) return DSPARK_ERR_INVALID;
+    if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;
     ConfParams p;
     p.h = h; p.d = d; p.emb = emb; p.emb_bf16 = (emb_t == DSPARK_BF16); p.e = e;
     p.anchor = anchor; p.draft_tok = draft_tok; p.w_c = w_c; p.b_c = b_c; p.T = T;
     p.B = B; p.gamma = gamma; p.V = V; p.conf_cal = conf_cal; p.log_surv = log_surv;
-    p.status = static_cast<uint32_t*>(ws);
+    const WsPtrs w = ws_ptrs(ws, B, gamma, V);
+    p.status = w.status;
+    p.tickets = w.conf_tickets;
+    p.score = w.conf_score;
     return launch_status(launch_confidence(p, static_cast<cudaStream_t>(stream)));
 }
 

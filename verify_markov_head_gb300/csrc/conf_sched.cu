@@ -1,8 +1,9 @@
 // conf_sched.cu -- confidence head + sequential temperature scaling + prefix
 // survival, and the hardware-aware greedy prefix scheduler.
 //
-// confidence_kernel: one CTA per request, one warp per draft position k.
-//   s_k = w_c . [h_k ; emb(x~_{k-1})] + b_c  (float4 loads, warp-shuffle sum);
+// confidence_kernel: one CTA per (draft position k, request).
+//   s_k = w_c . [h_k ; emb(x~_{k-1})] + b_c  (float4 loads, block sum); the
+//   last CTA of a request forms
 //   conf_cal = sigmoid(s_k / T_k), log_surv = running sum of log conf_cal
 //   ("DSpark：半自回归生成与置信度调度的投机解码" sections 置信度头 and 校准问题;
 //    "DeepSeek-AI与北京大学联手破局" section 四).  logit(sigmoid(s)) = s, so the
@@ -22,67 +23,70 @@
 namespace dspark {
 namespace {
 
-constexpr int kConfThreads = 512;
+constexpr int kConfThreads = 256;
 
-// One CTA per request; position k's dot product over [h_k ; emb(x~_{k-1})]
-// is a block reduction, all positions handled in one pass over the inputs.
+// One CTA per (position k, request b): s_k = w_c . [h_k ; emb(x~_{k-1})] + b_c
+// as a block reduction with the loads of a thread in flight together; the
+// last CTA of a request to finish (atomic ticket) turns the gamma scores into
+// calibrated confidences and the running log-survival.
 template <typename ET>
 __global__ void __launch_bounds__(kConfThreads) confidence_kernel(const ConfParams p) {
-    const int b = blockIdx.x;
+    const int k = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int gamma = p.gamma, d = p.d, e = p.e;
-    __shared__ float s_part[kConfThreads / 32][DSPARK_MAX_GAMMA];
-    __shared__ int s_x[DSPARK_MAX_GAMMA];
-    if (tid < gamma) {
-        int x = (tid == 0) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (tid - 1)];
-        if (x < 0 || x >= p.V) { raise_status(p.status, kBadToken); x = -1; }
-        s_x[tid] = x;
+    __shared__ float s_red[kConfThreads / 32];
+    int x = (k == 0) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (k - 1)];
+    if (x < 0 || x >= p.V) {
+        if (tid == 0) raise_status(p.status, kBadToken);
+        x = -1;
     }
-    __syncthreads();
-    const bool vec = (d % 4) == 0 && (e % 4) == 0;
-    for (int k = 0; k < gamma; ++k) {
-        const float* hk = p.h + ((size_t)b * gamma + k) * d;
-        const int x = s_x[k];
-        const ET* ek = static_cast<const ET*>(p.emb) + (size_t)(x < 0 ? 0 : x) * e;
-        float acc = 0.f;
-        if (vec) {
-            for (int i = 4 * tid; i < d; i += 4 * kConfThreads) {
-                const float4 w = __ldg(reinterpret_cast<const float4*>(p.w_c + i));
-                const float4 hv = __ldcs(reinterpret_cast<const float4*>(hk + i));
-                acc = fmaf(w.x, hv.x, fmaf(w.y, hv.y, fmaf(w.z, hv.z, fmaf(w.w, hv.w, acc))));
+    const float* hk = p.h + ((size_t)b * gamma + k) * d;
+    const ET* ek = static_cast<const ET*>(p.emb) + (size_t)(x < 0 ? 0 : x) * e;
+    float acc = 0.f;
+    if ((d % 4) == 0 && (e % 4) == 0) {
+#pragma unroll 4
+        for (int i = 4 * tid; i < d; i += 4 * kConfThreads) {
+            const float4 w = __ldg(reinterpret_cast<const float4*>(p.w_c + i));
+            const float4 hv = __ldcs(reinterpret_cast<const float4*>(hk + i));
+            acc = fmaf(w.x, hv.x, fmaf(w.y, hv.y, fmaf(w.z, hv.z, fmaf(w.w, hv.w, acc))));
+        }
+        if (x >= 0) {
+#pragma unroll 4
+            for (int i = 4 * tid; i < e; i += 4 * kConfThreads) {
+                const float4 w = __ldg(reinterpret_cast<const float4*>(p.w_c + d + i));
+                const float4 ev = Vec4<ET>::load(ek + i);
+                acc = fmaf(w.x, ev.x, fmaf(w.y, ev.y, fmaf(w.z, ev.z, fmaf(w.w, ev.w, acc))));
             }
-            if (x >= 0)
-                for (int i = 4 * tid; i < e; i += 4 * kConfThreads) {
-                    const float4 w = __ldg(reinterpret_cast<const float4*>(p.w_c + d + i));
-                    const float4 ev = Vec4<ET>::load(ek + i);
-                    acc = fmaf(w.x, ev.x, fmaf(w.y, ev.y, fmaf(w.z, ev.z, fmaf(w.w, ev.w, acc))));
-                }
-        } else {
-            for (int i = tid; i < d; i += kConfThreads) acc = fmaf(p.w_c[i], hk[i], acc);
-            if (x >= 0)
-                for (int i = tid; i < e; i += kConfThreads) acc = fmaf(p.w_c[d + i], to_f32(ek[i]), acc);
         }
+    } else {
+        for (int i = tid; i < d; i += kConfThreads) acc = fmaf(p.w_c[i], hk[i], acc);
+        if (x >= 0)
+            for (int i = tid; i < e; i += kConfThreads) acc = fmaf(p.w_c[d + i], to_f32(ek[i]), acc);
+    }
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (lane == 0) s_part[warp][k] = acc;
-    }
+    for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (lane == 0) s_red[warp] = acc;
     __syncthreads();
-    if (tid == 0) {
-        float run = 0.f;
-        for (int k = 1; k <= gamma; ++k) {
-            float sk = 0.f;
-            for (int w = 0; w < kConfThreads / 32; ++w) sk += s_part[w][k - 1];
-            const float x = (sk + p.b_c) / p.T[k - 1];
-            // sigmoid and its log, stable for either sign of x
-            const float en = expf(-fabsf(x));
-            const float c = (x >= 0.f) ? 1.f / (1.f + en) : en / (1.f + en);
-            const float logc = (x >= 0.f) ? -log1pf(en) : x - log1pf(en);
-            run += logc;
-            const size_t o = (size_t)b * gamma + (k - 1);
-            p.conf_cal[o] = c;
-            p.log_surv[o] = run;
-        }
+    if (tid != 0) return;
+    float sk = p.b_c;
+    for (int w = 0; w < kConfThreads / 32; ++w) sk += s_red[w];
+    p.score[(size_t)b * gamma + k] = sk;
+    __threadfence();
+    if (atomicAdd(&p.tickets[b], 1u) != (unsigned)(gamma - 1)) return;
+    __threadfence();
+    float run = 0.f;
+    for (int i = 0; i < gamma; ++i) {
+        const float xi = __ldcg(&p.score[(size_t)b * gamma + i]) / p.T[i];
+        // sigmoid and its log, stable for either sign of x
+        const float en = expf(-fabsf(xi));
+        const float c = (xi >= 0.f) ? 1.f / (1.f + en) : en / (1.f + en);
+        const float logc = (xi >= 0.f) ? -log1pf(en) : xi - log1pf(en);
+        run += logc;
+        const size_t o = (size_t)b * gamma + i;
+        p.conf_cal[o] = c;
+        p.log_surv[o] = run;
     }
+    p.tickets[b] = 0u;
 }
 
 // ----------------------------------------------------------------- scheduler
@@ -337,8 +341,9 @@ __global__ void __launch_bounds__(kST) schedule_kernel(const SchedParams p) {
 }  // namespace
 
 cudaError_t launch_confidence(const ConfParams& p, cudaStream_t s) {
-    if (p.emb_bf16) confidence_kernel<uint16_t><<<p.B, kConfThreads, 0, s>>>(p);
-    else confidence_kernel<float><<<p.B, kConfThreads, 0, s>>>(p);
+    const dim3 grid(p.gamma, p.B);
+    if (p.emb_bf16) confidence_kernel<uint16_t><<<grid, kConfThreads, 0, s>>>(p);
+    else confidence_kernel<float><<<grid, kConfThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -23,7 +23,7 @@ constexpr int kWinStride = 16;          // winner keys 128 bytes apart: one cach
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, tickets, gbar, win, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, total;
+    size_t status, tickets, gbar, win, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, conf, total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -43,6 +43,8 @@ struct WsPtrs {
     int32_t* fin;        // [B] final token
     float2* lse_rej;     // [B] (lse_p, lse_q) of the rejected row
     Draw2* resid_part;   // [B][parts]
+    uint32_t* conf_tickets;  // [B] confidence-head arrival counters, zero between launches
+    float* conf_score;       // [B][gamma]
     int nseg;
     int parts;
 };
@@ -67,6 +69,8 @@ struct ConfParams {
     int B, gamma, V;
     float* conf_cal; float* log_surv;
     uint32_t* status;
+    uint32_t* tickets;   // [B] arrival counters, zero between launches
+    float* score;        // [B][gamma] s_k before calibration
 };
 
 struct SchedParams {

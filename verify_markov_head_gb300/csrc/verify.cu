@@ -196,6 +196,8 @@ verify_stream_kernel(const VerifyParams p) {
     __syncthreads();
 }
 
+constexpr int kAcceptStaged = 1024;   // segment partials staged in shared memory (16 KB)
+
 // One warp per request: lse_p of rows 0..K_b from the segment partials, then
 // the accept test of every walked position at once (lane k-1 tests draft k),
 // the first rejection found by a ballot.
@@ -222,14 +224,46 @@ verify_accept_kernel(const VerifyParams p) {
     }
     float lse_mine = 0.f;        // lse_p of row `lane`
     int bonus_idx = 0;
-    for (int i = 0; i <= Kb; ++i) {
-        const LseDraw* part = p.ws.verify_part + ((size_t)b * (gamma + 1) + i) * nseg;
-        LseDraw a = lsedraw_empty();
-        for (int s = lane; s < nseg; s += 32) a = lsedraw_merge(a, part[s]);
+    const LseDraw* parts = p.ws.verify_part + (size_t)b * (gamma + 1) * nseg;
+    const int nparts = (Kb + 1) * nseg;
+    if (nparts <= kAcceptStaged) {
+        // the segment partials of rows 0..K_b, every load in flight, through
+        // shared memory; then lane i folds row i
+        __shared__ float4 s_part[kAcceptStaged];
+        for (int i0 = lane; i0 < nparts; i0 += 4 * 32) {
+            float4 c[4];
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
-        if (lane == i) lse_mine = a.m + logf(a.s);
-        if (i == Kb) bonus_idx = a.idx;
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 32 * u;
+                if (i < nparts) c[u] = __ldcg(reinterpret_cast<const float4*>(parts) + i);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 32 * u;
+                if (i < nparts) s_part[i] = c[u];
+            }
+        }
+        __syncwarp();
+        if (lane <= Kb) {
+            LseDraw a = lsedraw_empty();
+            for (int sg = 0; sg < nseg; ++sg) {
+                const float4 c = s_part[lane * nseg + sg];
+                a = lsedraw_merge(a, LseDraw{c.x, c.y, c.z, __float_as_int(c.w)});
+            }
+            lse_mine = a.m + logf(a.s);
+            bonus_idx = a.idx;
+        }
+        bonus_idx = __shfl_sync(0xffffffffu, bonus_idx, Kb);
+    } else {
+        for (int i = 0; i <= Kb; ++i) {
+            const LseDraw* part = parts + (size_t)i * nseg;
+            LseDraw a = lsedraw_empty();
+            for (int sg = lane; sg < nseg; sg += 32) a = lsedraw_merge(a, part[sg]);
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
+            if (lane == i) lse_mine = a.m + logf(a.s);
+            if (i == Kb) bonus_idx = a.idx;
+        }
     }
     bool reject = false, near = false;
     if (walk) {
