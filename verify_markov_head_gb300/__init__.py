@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host",
+    "dspark_schedule", "dspark_verify", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
@@ -326,3 +326,55 @@ def run_step_host(host_inp: dict, dev_inp: dict, buf: StepBuffers, host_out: dic
         host_out[name].copy_(src, non_blocking=True)
         d2h += src.numel() * src.element_size()
     return h2d, d2h
+
+
+class HostPipeline:
+    """Steps from pinned host memory with the copy of the next step's inputs
+    overlapping the current step's compute.
+
+    Two device copies of the per-step inputs (U, target logits, hidden
+    states, anchors) alternate: step t computes from slot t % 2 on the
+    compute stream while the copy stream fills slot (t + 1) % 2, which the
+    step before last has finished reading.  Each step's emitted tokens,
+    offsets and next anchors are copied back to the pinned `host_out`
+    tensors on the compute stream.  The weights and every other device input
+    are shared by both slots."""
+
+    def __init__(self, dev_inp: dict, buf: StepBuffers, compute_stream, copy_stream=None):
+        dev = dev_inp["U"].device
+        second = dict(dev_inp)
+        for k in _PER_STEP:
+            second[k] = torch.empty_like(dev_inp[k])
+        self.slots = [dev_inp, second]
+        self.buf = buf
+        self.compute_stream = compute_stream
+        self.copy_stream = copy_stream if copy_stream is not None else torch.cuda.Stream(device=dev)
+        self.copied = [torch.cuda.Event(), torch.cuda.Event()]
+        self.consumed = [torch.cuda.Event(), torch.cuda.Event()]
+        self.used = [False, False]
+        self.next = 0
+
+    def step(self, host_inp: dict, host_out: dict, *, mode, seed, step=0, tau=1.0):
+        """Enqueue one step; returns (h2d_bytes, d2h_bytes)."""
+        i = self.next
+        slot = self.slots[i]
+        if self.used[i]:
+            self.copy_stream.wait_event(self.consumed[i])     # the step that last read slot i is done
+        h2d = 0
+        with torch.cuda.stream(self.copy_stream):
+            for k in _PER_STEP:
+                slot[k].copy_(host_inp[k], non_blocking=True)
+                h2d += host_inp[k].numel() * host_inp[k].element_size()
+        self.copied[i].record(self.copy_stream)
+        self.compute_stream.wait_event(self.copied[i])
+        d2h = 0
+        with torch.cuda.stream(self.compute_stream):
+            run_step(slot, self.buf, mode=mode, seed=seed, step=step, tau=tau, stream=self.compute_stream)
+            for name in ("out_tok", "out_off", "next_anchor"):
+                src = getattr(self.buf, name)
+                host_out[name].copy_(src, non_blocking=True)
+                d2h += src.numel() * src.element_size()
+        self.consumed[i].record(self.compute_stream)
+        self.used[i] = True
+        self.next = i ^ 1
+        return h2d, d2h
