@@ -146,9 +146,9 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target, con
 // (RF - 1) + j * RF, zero blocks between them.  16-byte unit u of row n sits
 // at unit u ^ (n mod 8).
 __device__ __forceinline__ void stage_h_rows(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC,
-                                             int RF, int KCH, int r, int t0, int nthreads);
+                                             int RF, int KCH, int r, int V, int t0, int nthreads);
 __device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC, int RF,
-                                        int KCH, int r, int t0, int nthreads) {
+                                        int KCH, int r, int V, int t0, int nthreads) {
     const uint32_t blk = (uint32_t)NC * 128u;
     const int nblocks = (RF - 1) + RF * KCH;
     const int units = nblocks * NC * 8;
@@ -158,14 +158,14 @@ __device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, c
         if (rel >= 0 && rel % RF == 0) continue;             // an h block
         *reinterpret_cast<uint4*>(a_region + (size_t)bi * blk + (size_t)rem * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
-    stage_h_rows(a_region, W1, s_tok, NC, RF, KCH, r, t0, nthreads);
+    stage_h_rows(a_region, W1, s_tok, NC, RF, KCH, r, V, t0, nthreads);
 }
 
 // The h blocks alone (the zero blocks are already in place): every thread
 // issues its loads of W1 rows first, then stores them, so the gathers of one
 // thread are in flight together.
 __device__ __forceinline__ void stage_h_rows(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC,
-                                             int RF, int KCH, int r, int t0, int nthreads) {
+                                             int RF, int KCH, int r, int V, int t0, int nthreads) {
     const uint32_t blk = (uint32_t)NC * 128u;
     const int units = KCH * NC * 8;
     constexpr int kBatch = 4;
@@ -178,8 +178,8 @@ __device__ __forceinline__ void stage_h_rows(uint8_t* a_region, const uint16_t* 
             if (idx < units) {
                 const int j = idx / (NC * 8), rem = idx - j * (NC * 8);
                 const int n = rem >> 3, uu = rem & 7;
-                const int x = s_tok[n];
-                if (x >= 0)
+                const int x = s_tok[n];            // rows outside [0, V) stay zero
+                if (x >= 0 && x < V)
                     val[u] = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)(j * 64 + (uu ^ (n & 7)) * 8));
             }
         }
@@ -331,7 +331,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         s_row[n] = prow;
     }
     __syncthreads();
-    stage_h(gbase + L.a, W1, s_tok, NC, RF, KCH, r, tid, kThreads);
+    stage_h(gbase + L.a, W1, s_tok, NC, RF, KCH, r, V, tid, kThreads);
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
@@ -711,13 +711,18 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 break;
             }
             // this position's draws: one load per request
-            for (int n = etid; n < nb; n += 32 * kEpiWarps)
-                s_tok[n] = win_token(__ldcg(&p.ws.win[((size_t)(k - 1) * p.B + b_base + n) * kWinStride]));
+            for (int n = etid; n < nb; n += 32 * kEpiWarps) {
+                // no draw at all (every score NaN, say) leaves the empty index:
+                // flagged, and the next position sees a zero row
+                int x = win_token(__ldcg(&p.ws.win[((size_t)(k - 1) * p.B + b_base + n) * kWinStride]));
+                if (x < 0 || x >= V) { raise_status(p.ws.status, kBadToken); x = -1; }
+                s_tok[n] = x;
+            }
             ptx::named_barrier(1, 32 * kEpiWarps);
             if (k < k_last) {
                 // ---- h = W1[x~_k] for the next position (the MMA of this one is
                 //      complete: its last commit released the final tile just read)
-                stage_h_rows(gbase + L.a, W1, s_tok, NC, RF, KCH, r, etid, 32 * kEpiWarps);
+                stage_h_rows(gbase + L.a, W1, s_tok, NC, RF, KCH, r, V, etid, 32 * kEpiWarps);
                 ptx::fence_proxy_async_smem();
                 ptx::named_barrier(1, 32 * kEpiWarps);
                 if (etid == 0) ptx::mbar_arrive(a_ready);
