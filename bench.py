@@ -164,6 +164,7 @@ def run_gpu(args):
     buf = vm.StepBuffers(B, gamma, V, r, device=dev)
     stream = torch.cuda.Stream(device=dev)
     seed = w.seed
+    torch.cuda.synchronize(dev)       # inputs are made on the default stream; the step runs on `stream`
 
     if world > 1 and mode != 0:
         # the scheduler ranks the whole batch: a capacity table for B * world

@@ -128,6 +128,9 @@ class Workspace:
         off = (-self.tensor.data_ptr()) % 256
         self.buf = self.tensor[off:off + n]
         dspark_workspace_init(self.buf, stream)
+        # cleared before any stream uses it (side streams do not wait for the
+        # stream the clear was issued on)
+        torch.cuda.synchronize(self.buf.device)
 
     def ptr(self):
         return self.buf.data_ptr()
@@ -353,6 +356,10 @@ class HostPipeline:
         self.consumed = [torch.cuda.Event(), torch.cuda.Event()]
         self.used = [False, False]
         self.next = 0
+        # the weights, buffers and second slot were made on the current stream
+        cur = torch.cuda.current_stream(dev)
+        self.compute_stream.wait_stream(cur)
+        self.copy_stream.wait_stream(cur)
 
     def step(self, host_inp: dict, host_out: dict, *, mode, seed, step=0, tau=1.0):
         """Enqueue one step; returns (h2d_bytes, d2h_bytes)."""
