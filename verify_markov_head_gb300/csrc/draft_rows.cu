@@ -61,8 +61,10 @@ constexpr int kEpiWarps = 16;
 constexpr int kThreads = (kEpiWarps + 3) * 32;   // 608
 constexpr int kProducerWarp = 16, kMmaWarp = 17, kUWarp = 18;
 constexpr int kTN = 128;                          // vocabulary entries per tile
-constexpr int kMaxStages = 8;                     // W2 K-chunk ring depth (as shared memory allows)
-constexpr int kAcc = 4;                           // TMEM accumulators (4 x 128 columns)
+constexpr int kMaxStages = 12;                    // W2 K-chunk ring depth (as shared memory allows)
+// TMEM (512 columns): RF A operands of 128 columns, then 4 - RF accumulators
+// of 128 columns (three at RF = 1, two at RF = 2).
+constexpr int kMaxAcc = 3;
 constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile (bf16), 16 KB
 // U slice ring (draft): slice n = 4 * tile + column block goes to slot
 // n % kUSlots; the MMA warp alone reads the slots (copying them into TMEM),
@@ -86,25 +88,24 @@ struct Layout {
 
 constexpr int kSlotBytes = 128 * 128;             // one U slice: 128 rows x 32 fp32
 
-// RF = 128 / NC vocabulary tiles per accumulator; the A region holds
-// (RF - 1) + RF * (r / 64) blocks of NC rows x 128 B.  The W2 ring takes
-// whatever shared memory is left (up to kMaxStages K-chunks).  The residual
-// mode uses the U region as 16 per-warp 4 KB row-staging buffers.
+// The A operands live in TMEM, so shared memory holds the W2 ring (whatever
+// is left, up to kMaxStages K-chunks), the U slots (the residual mode uses
+// that region as 16 per-warp 4 KB row-staging buffers), the fold buffer,
+// the barriers and a few words.
 __host__ __device__ inline Layout rows_layout(int NC, int r, bool resid) {
+    (void)NC; (void)r;
     Layout L;
-    const int RF = 128 / NC;
-    const uint32_t a_bytes = (uint32_t)((RF - 1) + RF * (r / 64)) * (uint32_t)NC * 128u;
     L.uslots = resid ? kUSlotsResid : kUSlots;
-    const uint32_t fixed = a_bytes + (uint32_t)(L.uslots * kSlotBytes) + 4u * 128u * 16u +
-                           8u * (2 * kMaxStages + 2 * L.uslots + 2 * kAcc + 2) + 16u + 8u * 128u + 1024u + 64u;
+    const uint32_t fixed = (uint32_t)(L.uslots * kSlotBytes) + 4u * 128u * 16u +
+                           8u * (2 * kMaxStages + 2 * L.uslots + 2 * kMaxAcc + 2) + 16u + 8u * 128u + 1024u + 64u;
     int st = (int)((kSmemBudget - (int)fixed) / kBBytes);
     L.stages = st > kMaxStages ? kMaxStages : st;
     L.b = 0;
-    L.a = L.b + (uint32_t)L.stages * kBBytes;
-    L.u = L.a + a_bytes;
+    L.a = 0;
+    L.u = L.b + (uint32_t)L.stages * kBBytes;
     L.merge = L.u + (uint32_t)(L.uslots * kSlotBytes);
     L.bar = L.merge + 4u * 128u * 16u;
-    L.misc = L.bar + 8u * (2 * L.stages + 2 * L.uslots + 2 * kAcc + 2);
+    L.misc = L.bar + 8u * (2 * L.stages + 2 * L.uslots + 2 * kMaxAcc + 2);
     L.misc = (L.misc + 15u) & ~15u;
     L.total = L.misc + 16u + 8u * 128u;
     return L;
@@ -141,58 +142,40 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target, con
     return true;
 }
 
-// h rows -> A operand (K-major, 128-byte swizzle), the whole region: block
-// H_j (K-chunk j, 64 ranks) is [NC rows][128 B] at block index
-// (RF - 1) + j * RF, zero blocks between them.  16-byte unit u of row n sits
-// at unit u ^ (n mod 8).
-__device__ __forceinline__ void stage_h_rows(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC,
-                                             int RF, int KCH, int r, int V, int t0, int nthreads);
-__device__ __forceinline__ void stage_h(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC, int RF,
-                                        int KCH, int r, int V, int t0, int nthreads) {
-    const uint32_t blk = (uint32_t)NC * 128u;
-    const int nblocks = (RF - 1) + RF * KCH;
-    const int units = nblocks * NC * 8;
-    for (int idx = t0; idx < units; idx += nthreads) {
-        const int bi = idx / (NC * 8), rem = idx - bi * (NC * 8);
-        const int rel = bi - (RF - 1);
-        if (rel >= 0 && rel % RF == 0) continue;             // an h block
-        *reinterpret_cast<uint4*>(a_region + (size_t)bi * blk + (size_t)rem * 16) = make_uint4(0u, 0u, 0u, 0u);
+// A operands in TMEM.  A_i (i < RF, columns [128 i, 128 i + 128)) carries
+// h = W1[x~] on the lanes of vocabulary tile i, rows [i NC, (i + 1) NC), and
+// zeros on the other lanes: the block-diagonal operand that lets one
+// accumulator take RF tiles.  A row is r bf16 packed two to a 32-bit column
+// in rank order.  Epilogue warp (q, cb) writes lanes [32 q, 32 q + 32) and
+// columns [32 cb, 32 cb + 32), ranks [64 cb, 64 cb + 64): the h slice of its
+// lanes' requests into the A of their tile, and zeros into the other A
+// operands when `zeros` is set (once per launch: later positions rewrite the
+// h parts only).
+__device__ __forceinline__ void stage_a_tmem(uint32_t tmem_base, const uint16_t* W1, const int* s_tok, int NC,
+                                             int RF, int r, int V, int q, int cb, int lane, bool zeros) {
+    if (64 * cb >= r) return;                       // ranks past r are never read
+    const int row = 32 * q + lane, ti = row / NC, n = row % NC;
+    const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * cb);
+    uint32_t v[32];
+    const int x = s_tok[n];
+    if (x >= 0 && x < V) {                          // rows outside [0, V) stay zero
+        const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)(64 * cb));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint4 w = src[u];
+            v[4 * u] = w.x; v[4 * u + 1] = w.y; v[4 * u + 2] = w.z; v[4 * u + 3] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) v[u] = 0u;
     }
-    stage_h_rows(a_region, W1, s_tok, NC, RF, KCH, r, V, t0, nthreads);
-}
-
-// The h blocks alone (the zero blocks are already in place): every thread
-// issues its loads of W1 rows first, then stores them, so the gathers of one
-// thread are in flight together.
-__device__ __forceinline__ void stage_h_rows(uint8_t* a_region, const uint16_t* W1, const int* s_tok, int NC,
-                                             int RF, int KCH, int r, int V, int t0, int nthreads) {
-    const uint32_t blk = (uint32_t)NC * 128u;
-    const int units = KCH * NC * 8;
-    constexpr int kBatch = 4;
-    for (int first = t0; first < units; first += kBatch * nthreads) {
-        uint4 val[kBatch];
+    // the 32 lanes of a warp belong to one tile (NC >= 32)
+    ptx::tmem_st32(taddr + (uint32_t)(128 * ti), v);
+    if (zeros) {
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int idx = first + u * nthreads;
-            val[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (idx < units) {
-                const int j = idx / (NC * 8), rem = idx - j * (NC * 8);
-                const int n = rem >> 3, uu = rem & 7;
-                const int x = s_tok[n];            // rows outside [0, V) stay zero
-                if (x >= 0 && x < V)
-                    val[u] = *reinterpret_cast<const uint4*>(W1 + (size_t)x * r + (size_t)(j * 64 + (uu ^ (n & 7)) * 8));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int idx = first + u * nthreads;
-            if (idx < units) {
-                const int j = idx / (NC * 8), rem = idx - j * (NC * 8);
-                const int n = rem >> 3, uu = rem & 7;
-                *reinterpret_cast<uint4*>(a_region + (size_t)((RF - 1) + j * RF) * blk + (size_t)n * 128 + (uu << 4)) =
-                    val[u];
-            }
-        }
+        for (int u = 0; u < 32; ++u) v[u] = 0u;
+        for (int i = 0; i < RF; ++i)
+            if (i != ti) ptx::tmem_st32(taddr + (uint32_t)(128 * i), v);
     }
 }
 
@@ -272,8 +255,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     const int RF = 128 / NC;                      // vocabulary tiles per accumulator
     const int US = L.uslots;
     const uint32_t slot_bytes = (uint32_t)kSlotBytes;
-    const uint32_t blk = (uint32_t)NC * 128u;     // bytes of one A block
+    const uint32_t blk = (uint32_t)NC * 128u;     // bytes of one U box (NC rows x 128 B)
     const bool persistent = k_last > k_first;
+    const int nacc = 4 - RF;                      // accumulators after the RF A operands
+    const uint32_t acc0 = 128u * (uint32_t)RF;    // TMEM column of accumulator 0
 
     const int kStages = L.stages;
     const uint32_t bar0 = base + L.bar;
@@ -282,9 +267,9 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     auto ufull = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
     auto uempty = [&](int i) { return bar0 + 8u * (2 * kStages + US + i); };
     auto tfull = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + i); };
-    auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + kAcc + i); };
-    const uint32_t drain = bar0 + 8u * (2 * kStages + 2 * US + 2 * kAcc);
-    const uint32_t a_ready = bar0 + 8u * (2 * kStages + 2 * US + 2 * kAcc + 1);
+    auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + kMaxAcc + i); };
+    const uint32_t drain = bar0 + 8u * (2 * kStages + 2 * US + 2 * kMaxAcc);
+    const uint32_t a_ready = bar0 + 8u * (2 * kStages + 2 * US + 2 * kMaxAcc + 1);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L.misc);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 4);
     volatile uint32_t* never = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 8);
@@ -302,7 +287,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), 1); }
         for (int i = 0; i < US; ++i) { ptx::mbar_init(ufull(i), 1); ptx::mbar_init(uempty(i), 1); }
-        for (int i = 0; i < kAcc; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
+        for (int i = 0; i < kMaxAcc; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(a_ready, 1);
         *abort_flag = 0u;
@@ -314,7 +299,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         ptx::prefetch_tmap(&a.umap);
         ptx::prefetch_tmap(&a.upf);
     }
-    if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 128u * kAcc); ptx::tmem_relinquish(); }
+    if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 512u); ptx::tmem_relinquish(); }
     for (int n = tid; n < 128; n += kThreads) {
         int x = -1, prow = -1;
         if (n < nb) {
@@ -330,13 +315,17 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         s_tok[n] = x;
         s_row[n] = prow;
     }
-    __syncthreads();
-    stage_h(gbase + L.a, W1, s_tok, NC, RF, KCH, r, V, tid, kThreads);
-    ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (warp < kEpiWarps) {                        // the A operands of the first position
+        stage_a_tmem(tmem_base, W1, s_tok, NC, RF, r, V, warp & 3, warp >> 2, lane, true);
+        ptx::tmem_wait_st();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
     const int ntiles = (V + kTN * RF - 1) / (kTN * RF);   // super-tiles of RF vocabulary tiles
 
     if (warp == kProducerWarp) {
@@ -428,10 +417,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     site = 3;
                     break;
                 }
+                ptx::tc_fence_after();
                 for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
                     if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) { site = 4; break; }
                     ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTN);
+                    const uint32_t d_tmem = tmem_base + acc0 + (uint32_t)(acc * kTN);
                     if constexpr (!kResid) {
                         // the accumulator starts as the tile's U: four 32-column slices
                         // (128 rows x 128 B, 128-byte swizzle) copied 32 bytes a row at a
@@ -457,16 +447,15 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                             if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) { site = 5; break; }
                             ptx::tc_fence_after();
                             const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
-                            // window of 128 rows whose block i is H_j
-                            const uint32_t a_addr = base + L.a + (uint32_t)((RF - 1) + j * RF - i) * blk;
+                            // A_i in TMEM: K-chunk j = 32 columns, 16 ranks = 8 columns
+                            const uint32_t a_tmem = tmem_base + (uint32_t)(128 * i + 32 * j);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk) {
-                                // A: K-major rows of 128 B, 8-row groups 1 KB apart (SBO); 16 ranks = 32 B.
-                                const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
                                 // B: MN-major, 64-entry swizzle atoms 8 KB apart along N (LBO),
                                 //    8-rank groups 1 KB apart along K (SBO); 16 ranks = 2 KB.
                                 const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
-                                ptx::mma_f16(d_tmem, ad, bd, idesc, (!kResid || (i | j | kk) != 0) ? 1u : 0u);
+                                ptx::mma_f16_ts(d_tmem, a_tmem + (uint32_t)(8 * kk), bd, idesc,
+                                                (!kResid || (i | j | kk) != 0) ? 1u : 0u);
                             }
                             ptx::mma_commit(empty(stage));
                             if (++stage == kStages) { stage = 0; ph ^= 1u; }
@@ -474,7 +463,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     }
                     if (!ok) break;
                     ptx::mma_commit(tfull(acc));
-                    if (++acc == kAcc) { acc = 0; aph ^= 1u; }
+                    if (++acc == nacc) { acc = 0; aph ^= 1u; }
                 }
             }
             if (!ok) { raise_timeout(p.ws.status, site); *abort_flag = 1u; }
@@ -519,13 +508,13 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 ptx::tc_fence_after();
                 float bias[32];              // draft: U + h.W2; residual: h.W2
                 if (active) {
-                    ptx::tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kTN + 32 * cb), bias);
+                    ptx::tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + acc0 + (uint32_t)(acc * kTN + 32 * cb), bias);
                     ptx::tmem_wait_ld();
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty(acc));
-                if (++acc == kAcc) { acc = 0; aph ^= 1u; }
+                if (++acc == nacc) { acc = 0; aph ^= 1u; }
                 if (kResid && !active) continue;
                 const int v0 = t * kTN * RF + ti * kTN + 32 * cb;
                 if constexpr (kResid) {
@@ -720,10 +709,12 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             }
             ptx::named_barrier(1, 32 * kEpiWarps);
             if (k < k_last) {
-                // ---- h = W1[x~_k] for the next position (the MMA of this one is
-                //      complete: its last commit released the final tile just read)
-                stage_h_rows(gbase + L.a, W1, s_tok, NC, RF, KCH, r, V, etid, 32 * kEpiWarps);
-                ptx::fence_proxy_async_smem();
+                // ---- h = W1[x~_k] into the A operands for the next position (the
+                //      MMAs of this one are complete: the last commit released the
+                //      final tile the warps just read)
+                stage_a_tmem(tmem_base, W1, s_tok, NC, RF, r, V, q, cb, lane, false);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
                 ptx::named_barrier(1, 32 * kEpiWarps);
                 if (etid == 0) ptx::mbar_arrive(a_ready);
             }
@@ -760,7 +751,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     __syncthreads();
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, 128u * kAcc);
+        ptx::tmem_dealloc(tmem_base, 512u);
     }
 
     if (persistent) {
@@ -888,7 +879,7 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
     if (!enc) return cudaErrorNotSupported;
     RowsArgs a;
     a.p = p;
-    a.NC = p.B <= 32 ? 32 : (p.B <= 64 ? 64 : 128);
+    a.NC = p.B <= 64 ? 64 : 128;           // RF = 2 or 1: RF = 4 would leave no TMEM for accumulators
     a.target = target;
     a.near_ties = near_ties;
     {
