@@ -74,10 +74,10 @@ constexpr int kUSlotsResid = 4;                   // residual: 16 warps x 4 KB r
 constexpr int kSmemBudget = 227 * 1024;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 constexpr long long kDrainCycles = 200000000LL;   // ~0.1 s: copies already issued landing
-// Margins of the exponential-race screen (relative on the winner's E2,
-// absolute on the candidate's): far above the hardware log2's error and the
-// rounding of the products, so every entry the exact test would accept is
-// passed to it.
+// Margins of the exponential-race screens (relative on the running winner's
+// variate, absolute on the candidate's bound): far above the rounding of the
+// products and of the exact variates, so every entry the exact test would
+// accept is passed to it.
 constexpr float kRaceRel = 1.0000152587890625f;   // 1 + 2^-16
 constexpr float kRaceSlack = 1.52587890625e-05f;  // 2^-16
 
@@ -613,10 +613,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 t[e] = fast_exp2(fmaf(us[e], scale2, -rz2));
-                                // screen with the bare hardware log2: it equals E2 for
-                                // u <= 7/8 and is within ~2^-22 of it above, which the
-                                // margins of rE2h and kRaceSlack cover
-                                cand |= -fast_log2(uniform_of(ws[e])) < fmaf(rE2h, t[e], kRaceSlack);
+                                // screen with the bound E2 = -log2(u) >= (1 - u) * log2e
+                                // (no logarithm; 1 - u exact from the bits): an entry can
+                                // win only if (1 - u) * log2e <= E2 < E2_best * t, and the
+                                // margins of rE2h and kRaceSlack cover the rounding
+                                cand |= one_minus_uniform_of(ws[e]) < fmaf(rE2h * kLn2, t[e], kRaceSlack);
                             }
                             if (!cand) {
                                 st.s += (t[0] + t[1]) + (t[2] + t[3]);
