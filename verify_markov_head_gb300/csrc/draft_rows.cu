@@ -70,7 +70,7 @@ constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile 
 // n % kUSlots; the MMA warp alone reads the slots (copying them into TMEM),
 // in fill order.
 constexpr int kUSlots = 4;
-constexpr int kUSlotsResid = 4;                   // residual: 16 warps x 4 KB row staging
+constexpr int kUSlotsResid = 8;                   // residual: 16 warps x (4 KB U + 4 KB target) row staging
 constexpr int kSmemBudget = 227 * 1024;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 constexpr long long kDrainCycles = 200000000LL;   // ~0.1 s: copies already issued landing
@@ -197,10 +197,10 @@ __device__ __forceinline__ int win_token(unsigned long long key) {
 // lanes, rows of lanes outside `mask` skipped, entries past V zero-filled.
 // The 16-byte chunk index is swizzled with the row (XOR with row % 8 for
 // 128-byte rows, (row / 2) % 4 for 64-byte rows) so that a lane reading its
-// own row meets no bank conflict.  On return the whole buffer is visible to
-// the warp.
+// own row meets no bank conflict.  The copies form one cp.async group; the
+// caller waits for it and syncs the warp before reading.
 template <typename T>
-__device__ __forceinline__ void stage_rows(uint32_t buf, const T* row, unsigned mask, int v0, int V, int lane) {
+__device__ __forceinline__ void issue_rows(uint32_t buf, const T* row, unsigned mask, int v0, int V, int lane) {
     constexpr int kRowBytes = 32 * (int)sizeof(T);
     constexpr int kChunks = kRowBytes / 16;           // 8 (fp32) or 4 (bf16)
     constexpr int kRowsPerPass = 32 / kChunks;
@@ -216,8 +216,7 @@ __device__ __forceinline__ void stage_rows(uint32_t buf, const T* row, unsigned 
             ptx::cp_async_16(buf + (uint32_t)(rr * kRowBytes + ((c ^ swz) << 4)), in ? src + vq : src, in ? 16u : 0u);
         }
     }
-    ptx::cp_async_wait_all();
-    __syncwarp();
+    ptx::cp_async_commit();
 }
 
 __device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
@@ -519,18 +518,24 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 const int v0 = t * kTN * RF + ti * kTN + 32 * cb;
                 if constexpr (kResid) {
                     // The rejected rows differ per request, so the warp stages its 32
-                    // rows of U and then of the target through a 4 KB shared buffer:
+                    // rows of U and of the target through two 4 KB shared buffers with
                     // asynchronous 16-byte copies (a row segment spread over
-                    // consecutive lanes, all of them in flight at once), swizzled on
-                    // the chunk index, then each lane reads its own row.
-                    uint8_t* wbuf = gbase + L.u + (size_t)warp * 4096;
+                    // consecutive lanes, all of them in flight at once, swizzled on the
+                    // chunk index); each lane then reads its own row.  The U rows of
+                    // the warp's next tile are fetched while this tile is computed.
+                    const uint32_t ubuf = base + L.u + (uint32_t)warp * 8192u, tbuf = ubuf + 4096u;
+                    uint8_t* wbuf = gbase + L.u + (size_t)warp * 8192 + 4096;      // target rows
+                    const uint8_t* ubuf_g = gbase + L.u + (size_t)warp * 8192;
                     const unsigned real_mask = __ballot_sync(0xffffffffu, real);
                     float* z = bias;                           // z overwrites the bias in place
-                    stage_rows<float>(base + L.u + (uint32_t)warp * 4096u, Urow, real_mask, v0, V, lane);
+                    if (t == (int)blockIdx.x) issue_rows<float>(ubuf, Urow, real_mask, v0, V, lane);
+                    issue_rows<TT>(tbuf, Trow, real_mask, v0, V, lane);
+                    ptx::cp_async_wait_group<1>();             // this tile's U rows
+                    __syncwarp();
                     if (real) {
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
-                            const float4 u4 = *reinterpret_cast<const float4*>(wbuf + lane * 128 + ((c ^ (lane & 7)) << 4));
+                            const float4 u4 = *reinterpret_cast<const float4*>(ubuf_g + lane * 128 + ((c ^ (lane & 7)) << 4));
                             z[4 * c] = u4.x + bias[4 * c];               // z * tau
                             z[4 * c + 1] = u4.y + bias[4 * c + 1];
                             z[4 * c + 2] = u4.z + bias[4 * c + 2];
@@ -538,7 +543,14 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         }
                     }
                     __syncwarp();
-                    stage_rows<TT>(base + L.u + (uint32_t)warp * 4096u, Trow, real_mask, v0, V, lane);
+                    const int tn = t + (int)gridDim.x;
+                    if (tn < ntiles) {
+                        issue_rows<float>(ubuf, Urow, real_mask, tn * kTN * RF + ti * kTN + 32 * cb, V, lane);
+                        ptx::cp_async_wait_group<1>();         // this tile's target rows
+                    } else {
+                        ptx::cp_async_wait_group<0>();
+                    }
+                    __syncwarp();
                     if (real) {
                         // Both draws as exponential races (argmax log w_v + G_v =
                         // argmin E_v / w_v, E = -ln u): the residual law r = max(0, p - q)
