@@ -36,7 +36,7 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.gbar = o;        o = align256(o + sizeof(uint32_t) * (kGridBarrierSlots + 1));
     L.win = o;         o = align256(o + sizeof(unsigned long long) * kWinStride * (size_t)gamma * B);
     L.draft_part = o;  o = align256(o + sizeof(DrawLse) * 2 * (size_t)B * L.parts);
-    L.verify_part = o; o = align256(o + sizeof(LseDraw) * (size_t)B * (gamma + 1) * L.nseg);
+    L.verify_part = o; o = align256(o + sizeof(LseDraw) * (size_t)B * (gamma + 1) * L.nseg * kVerifySub);
     L.rej = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
     L.acc = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
     L.fin = o;         o = align256(o + sizeof(int32_t) * (size_t)B);

@@ -17,6 +17,7 @@ struct Draw2;
 constexpr int kMaxParts = 1024;        // cap on partial states per request per launch
 constexpr int kPartTile = 128;         // vocabulary entries per tile of the partial-producing kernels
 constexpr int kVerifySeg = 32768;      // vocabulary entries per verify-stream work item
+constexpr int kVerifySub = 8;          // partial states per work item (one per consumer warp)
 constexpr int kChunk = 16;             // requests per chunk of the partial-producing kernels
 constexpr int kGridBarrierSlots = DSPARK_MAX_GAMMA;   // one grid-barrier counter per draft position
 constexpr int kWinStride = 16;          // winner keys 128 bytes apart: one cache line each

@@ -26,6 +26,7 @@ namespace dspark {
 namespace {
 
 constexpr int kStreamConsumers = 8;                        // consumer warps
+static_assert(kStreamConsumers == kVerifySub, "one partial state per consumer warp");
 constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;  // + one producer warp
 constexpr int kStreamStages = 3;
 constexpr int kStreamChunk = 8192;                           // entries per bulk copy
@@ -33,6 +34,7 @@ constexpr int kStreamStageBytes = kStreamChunk * 4;          // fp32 chunk (bf16
 constexpr int kPerThread = kStreamChunk / (32 * kStreamConsumers);   // 32 entries per consumer per chunk
 constexpr long long kStreamWaitCycles = 4000000000LL;        // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kStreamKCache = 2048;                          // verify lengths kept in shared memory up to this B (8 KB)
 
 template <typename T>
 __device__ __forceinline__ float load_scalar(const T* p, size_t i) { return to_f32(p[i]); }
@@ -45,7 +47,8 @@ __device__ __forceinline__ float load_scalar(const T* p, size_t i) { return to_f
 // (evict-first); 8 consumer warps keep their running log-sum-exp in base-2
 // units across the chunks of the item: per chunk a max pass, one rescale, then
 // exp2 of x*log2e/tau - m in four independent partial sums.  The bonus row
-// i = K_b also takes the Gumbel-max draw (domain 3).  One partial per item.
+// i = K_b also takes the Gumbel-max draw (domain 3).  Each consumer warp
+// writes its own partial per item, so no block-wide step separates items.
 template <typename TT>
 __global__ void __launch_bounds__(kStreamThreads, 2)
 verify_stream_kernel(const VerifyParams p) {
@@ -58,6 +61,10 @@ verify_stream_kernel(const VerifyParams p) {
     auto empty = [&](int i) { return bar0 + 8u * (kStreamStages + i); };
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages);
     LseDraw* s_part = reinterpret_cast<LseDraw*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16);
+    // the verify lengths, read once (every item needs its request's K_b; a
+    // global load per item would stall the producer between items)
+    int* s_K = reinterpret_cast<int*>(s_part + kStreamConsumers);
+    const bool k_cached = p.B <= kStreamKCache;
 
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
     const int items = p.B * (gamma + 1) * nseg;
@@ -67,13 +74,15 @@ verify_stream_kernel(const VerifyParams p) {
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
+    if (k_cached)
+        for (int b = tid; b < p.B; b += kStreamThreads) s_K[b] = p.K[b];
     __syncthreads();
 
     auto decode = [&](int w, int& b, int& i, int& seg) {
         seg = w % nseg;
         i = (w / nseg) % (gamma + 1);
         b = w / (nseg * (gamma + 1));
-        int Kb = p.K[b];
+        int Kb = k_cached ? s_K[b] : p.K[b];
         return Kb < 0 ? 0 : (Kb > gamma ? gamma : Kb);
     };
 
@@ -110,7 +119,7 @@ verify_stream_kernel(const VerifyParams p) {
         for (int w = blockIdx.x; w < items && !failed; w += gridDim.x) {
             int b, i, seg;
             const int Kb = decode(w, b, i, seg);
-            if (seg == 0 && i == 0 && tid == 0 && (p.K[b] < 0 || p.K[b] > gamma)) raise_status(p.ws.status, kBadLength);
+            if (seg == 0 && i == 0 && tid == 0 && (Kb != (k_cached ? s_K[b] : p.K[b]))) raise_status(p.ws.status, kBadLength);
             if (i > Kb) continue;
             const bool bonus = (i == Kb);
             const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
@@ -178,16 +187,10 @@ verify_stream_kernel(const VerifyParams p) {
             if (m2 == -INFINITY) { st.m = -INFINITY; st.s = 0.f; }
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
-            if (lane == 0) s_part[warp] = st;
-            // one barrier publishes s_part and makes a failed wait a group decision
-            if (ptx::bar_red_or(1, 32 * kStreamConsumers, failed)) { *abort_flag = 1u; break; }
-            if (warp == 0) {
-                st = lane < kStreamConsumers ? s_part[lane] : lsedraw_empty();
-#pragma unroll
-                for (int m = 1; m < kStreamConsumers; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
-                if (lane == 0) p.ws.verify_part[((size_t)b * (gamma + 1) + i) * nseg + seg] = st;
-            }
-            ptx::named_barrier(1, 32 * kStreamConsumers);
+            // one partial per consumer warp: no block-wide step between items
+            if (lane == 0 && !failed)
+                p.ws.verify_part[(((size_t)b * (gamma + 1) + i) * nseg + seg) * kVerifySub + warp] = st;
+            if (failed) { *abort_flag = 1u; break; }
         }
     }
     if (*abort_flag) {
@@ -224,41 +227,47 @@ verify_accept_kernel(const VerifyParams p) {
     }
     float lse_mine = 0.f;        // lse_p of row `lane`
     int bonus_idx = 0;
-    const LseDraw* parts = p.ws.verify_part + (size_t)b * (gamma + 1) * nseg;
-    const int nparts = (Kb + 1) * nseg;
+    const int nsub = nseg * kVerifySub;            // partial states per row
+    const LseDraw* parts = p.ws.verify_part + (size_t)b * (gamma + 1) * nsub;
+    const int nparts = (Kb + 1) * nsub;
     if (nparts <= kAcceptStaged) {
         // the segment partials of rows 0..K_b, every load in flight, through
         // shared memory; then lane i folds row i
         __shared__ float4 s_part[kAcceptStaged];
-        for (int i0 = lane; i0 < nparts; i0 += 4 * 32) {
-            float4 c[4];
+        for (int i0 = lane; i0 < nparts; i0 += 12 * 32) {
+            float4 c[12];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 12; ++u) {
                 const int i = i0 + 32 * u;
                 if (i < nparts) c[u] = __ldcg(reinterpret_cast<const float4*>(parts) + i);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 12; ++u) {
                 const int i = i0 + 32 * u;
                 if (i < nparts) s_part[i] = c[u];
             }
         }
         __syncwarp();
-        if (lane <= Kb) {
-            LseDraw a = lsedraw_empty();
-            for (int sg = 0; sg < nseg; ++sg) {
-                const float4 c = s_part[lane * nseg + sg];
+        // LPR lanes per row (a power of two with (K_b + 1) * LPR <= 32) fold
+        // every LPR-th partial of their row, then a shuffle tree joins them
+        int LPR = 32;
+        while (LPR > 1 && (Kb + 1) * LPR > 32) LPR >>= 1;
+        const int row = lane / LPR, sub = lane - row * LPR;
+        LseDraw a = lsedraw_empty();
+        if (row <= Kb)
+            for (int sg = sub; sg < nsub; sg += LPR) {
+                const float4 c = s_part[row * nsub + sg];
                 a = lsedraw_merge(a, LseDraw{c.x, c.y, c.z, __float_as_int(c.w)});
             }
-            lse_mine = a.m + logf(a.s);
-            bonus_idx = a.idx;
-        }
-        bonus_idx = __shfl_sync(0xffffffffu, bonus_idx, Kb);
+        for (int m = 1; m < LPR; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
+        const float lse_row = a.m + logf(a.s);         // on lanes row * LPR
+        lse_mine = __shfl_sync(0xffffffffu, lse_row, (lane * LPR) & 31);
+        bonus_idx = __shfl_sync(0xffffffffu, a.idx, Kb * LPR);
     } else {
         for (int i = 0; i <= Kb; ++i) {
-            const LseDraw* part = parts + (size_t)i * nseg;
+            const LseDraw* part = parts + (size_t)i * nsub;
             LseDraw a = lsedraw_empty();
-            for (int sg = lane; sg < nseg; sg += 32) a = lsedraw_merge(a, part[sg]);
+            for (int sg = lane; sg < nsub; sg += 32) a = lsedraw_merge(a, part[sg]);
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
             if (lane == i) lse_mine = a.m + logf(a.s);
@@ -496,7 +505,7 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     const long long items = (long long)p.B * (p.gamma + 1) * p.ws.nseg;
     const int g1 = (int)(items < 2LL * num_sms() ? items : 2LL * num_sms());
     const size_t smem1 = 128 + (size_t)kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16 +
-                         sizeof(LseDraw) * kStreamConsumers;
+                         sizeof(LseDraw) * kStreamConsumers + (p.B <= kStreamKCache ? sizeof(int) * (size_t)p.B : 0);
     cudaError_t e1 = cudaFuncSetAttribute(verify_stream_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
     if (e1 != cudaSuccess) return e1;
     verify_stream_kernel<TT><<<g1, kStreamThreads, smem1, s>>>(p);
