@@ -35,6 +35,7 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.tickets = o;     o = align256(o + sizeof(uint32_t) * 2 * nchunks);
     L.gbar = o;        o = align256(o + sizeof(uint32_t) * (kGridBarrierSlots + 1));
     L.win = o;         o = align256(o + sizeof(unsigned long long) * kWinStride * (size_t)gamma * B);
+    L.vq = o;          o = align256(o + sizeof(uint32_t) * 2);
     L.draft_part = o;  o = align256(o + sizeof(DrawLse) * 2 * (size_t)B * L.parts);
     L.verify_part = o; o = align256(o + sizeof(LseDraw) * (size_t)B * (gamma + 1) * L.nseg * kVerifySub);
     L.rej = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
@@ -56,6 +57,7 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     P.tickets_resid = P.tickets_draft + ((size_t)B + kChunk - 1) / kChunk;
     P.gbar = reinterpret_cast<uint32_t*>(base + L.gbar);
     P.win = reinterpret_cast<unsigned long long*>(base + L.win);
+    P.vq = reinterpret_cast<uint32_t*>(base + L.vq);
     P.draft_part = reinterpret_cast<DrawLse*>(base + L.draft_part);
     P.verify_part = reinterpret_cast<LseDraw*>(base + L.verify_part);
     P.rej = reinterpret_cast<int32_t*>(base + L.rej);

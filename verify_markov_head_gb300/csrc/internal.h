@@ -24,7 +24,7 @@ constexpr int kWinStride = 16;          // winner keys 128 bytes apart: one cach
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, tickets, gbar, win, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, conf, total;
+    size_t status, tickets, gbar, win, vq, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, conf, total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -35,6 +35,7 @@ struct WsPtrs {
     uint32_t* tickets_draft;   // [ceil(B/kChunk)] arrival counters, zero between launches
     uint32_t* tickets_resid;   // [ceil(B/kChunk)]
     uint32_t* gbar;            // [kGridBarrierSlots + 1] grid-barrier counters, then the exit counter
+    uint32_t* vq;              // [2] verify-stream work counter and exit counter, zero between launches
     unsigned long long* win;   // [gamma][B][kWinStride] winner keys of the persistent draft (first of
                                // each line used), zero between launches
     DrawLse* draft_part;       // [2][B][parts] (two buffers alternate between positions)

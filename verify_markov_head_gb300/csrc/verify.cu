@@ -40,15 +40,18 @@ template <typename T>
 __device__ __forceinline__ float load_scalar(const T* p, size_t i) { return to_f32(p[i]); }
 
 // Persistent streaming pass over the target rows 0..K_b of every request.
-// Work item w = (b, i, seg), seg fastest, each a kVerifySeg-entry slice of a
-// row; CTA c takes items c, c + grid, ... and skips rows i > K_b (producer and
-// consumers apply the same rule).  A producer thread moves every 8192-entry
-// chunk of the item into a 3-stage shared-memory ring with one bulk copy
-// (evict-first); 8 consumer warps keep their running log-sum-exp in base-2
-// units across the chunks of the item: per chunk a max pass, one rescale, then
-// exp2 of x*log2e/tau - m in four independent partial sums.  The bonus row
-// i = K_b also takes the Gumbel-max draw (domain 3).  Each consumer warp
-// writes its own partial per item, so no block-wide step separates items.
+// Work item = (b, i, seg), a kVerifySeg-entry slice of a row.  CTAs take items
+// from a global counter in the order: the bonus rows i = K_b of every request
+// first (they also draw, so they cost several times a plain item), then the
+// other rows; items with i > K_b are skipped.  Heavy items first and dynamic
+// claiming keep the CTAs' loads even.  A producer thread moves every
+// 8192-entry chunk of its items into a 3-stage shared-memory ring with one
+// bulk copy (evict-first) and tags the stage with the item; 8 consumer warps
+// keep their running log-sum-exp in base-2 units across the chunks of an item:
+// per chunk a max pass, one rescale, then exp2 of x*log2e/tau - m in four
+// independent partial sums.  The bonus row also takes the Gumbel-max draw
+// (domain 3).  Each consumer warp writes its own partial per item.  A stage
+// tagged -1 ends the stream.
 template <typename TT>
 __global__ void __launch_bounds__(kStreamThreads, 2)
 verify_stream_kernel(const VerifyParams p) {
@@ -60,10 +63,10 @@ verify_stream_kernel(const VerifyParams p) {
     auto full = [&](int i) { return bar0 + 8u * i; };
     auto empty = [&](int i) { return bar0 + 8u * (kStreamStages + i); };
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages);
-    LseDraw* s_part = reinterpret_cast<LseDraw*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16);
+    int2* s_meta = reinterpret_cast<int2*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16);
     // the verify lengths, read once (every item needs its request's K_b; a
     // global load per item would stall the producer between items)
-    int* s_K = reinterpret_cast<int*>(s_part + kStreamConsumers);
+    int* s_K = reinterpret_cast<int*>(s_meta + kStreamStages);
     const bool k_cached = p.B <= kStreamKCache;
 
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
@@ -76,14 +79,31 @@ verify_stream_kernel(const VerifyParams p) {
     }
     if (k_cached)
         for (int b = tid; b < p.B; b += kStreamThreads) s_K[b] = p.K[b];
+    if (blockIdx.x == 0)
+        for (int b = tid; b < p.B; b += kStreamThreads)
+            if (p.K[b] < 0 || p.K[b] > gamma) raise_status(p.ws.status, kBadLength);
     __syncthreads();
 
-    auto decode = [&](int w, int& b, int& i, int& seg) {
-        seg = w % nseg;
-        i = (w / nseg) % (gamma + 1);
-        b = w / (nseg * (gamma + 1));
-        int Kb = k_cached ? s_K[b] : p.K[b];
+    auto clampK = [&](int b) {
+        const int Kb = k_cached ? s_K[b] : p.K[b];
         return Kb < 0 ? 0 : (Kb > gamma ? gamma : Kb);
+    };
+    // item u -> (b, i, seg): the B * nseg bonus items first, then the rest
+    auto decode = [&](int u, int& b, int& i, int& seg) {
+        const int nbonus = p.B * nseg;
+        if (u < nbonus) {
+            b = u / nseg;
+            seg = u - b * nseg;
+            i = clampK(b);
+        } else {
+            const int v = u - nbonus, per = gamma * nseg;
+            b = v / per;
+            const int rest = v - b * per, in = rest / nseg;
+            seg = rest - in * nseg;
+            const int Kb = clampK(b);
+            i = in < Kb ? in : in + 1;
+        }
+        return clampK(b);
     };
 
     if (warp == kStreamConsumers) {
@@ -93,19 +113,28 @@ verify_stream_kernel(const VerifyParams p) {
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < items && ok; w += gridDim.x) {
+            for (;;) {
+                const int u = (int)atomicAdd(&p.ws.vq[0], 1u);
+                if (u >= items) break;
                 int b, i, seg;
-                const int Kb = decode(w, b, i, seg);
+                const int Kb = decode(u, b, i, seg);
                 if (i > Kb) continue;
                 const int v_end = min(V, (seg + 1) * kVerifySeg);
                 const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
                 for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kStreamChunk) {
                     if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kStreamWaitCycles))) break;
+                    s_meta[stage] = make_int2(u, v0);
                     const uint32_t bytes = (uint32_t)(min(kStreamChunk, v_end - v0) * (int)sizeof(TT));
                     ptx::mbar_arrive_expect_tx(full(stage), bytes);
                     ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes, row + v0, bytes, full(stage), pol);
                     if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
                 }
+                if (!ok) break;
+            }
+            // the end-of-stream tag
+            if (ok && (ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kStreamWaitCycles))) {
+                s_meta[stage] = make_int2(-1, 0);
+                ptx::mbar_arrive(full(stage));
             }
             if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
         }
@@ -115,70 +144,14 @@ verify_stream_kernel(const VerifyParams p) {
         const float scale = p.inv_tau * kLog2e;          // x * log2(e) / tau
         int stage = 0;
         uint32_t ph = 0;
-        bool failed = false;
-        for (int w = blockIdx.x; w < items && !failed; w += gridDim.x) {
-            int b, i, seg;
-            const int Kb = decode(w, b, i, seg);
-            if (seg == 0 && i == 0 && tid == 0 && (Kb != (k_cached ? s_K[b] : p.K[b]))) raise_status(p.ws.status, kBadLength);
-            if (i > Kb) continue;
-            const bool bonus = (i == Kb);
-            const Stream rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
-            const int v_end = min(V, (seg + 1) * kVerifySeg);
-            float m2 = -INFINITY;                        // running max of x*log2e/tau
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};          // sum of 2^(x*log2e/tau - m2), four chains
-            float best = -INFINITY;
-            int bidx = 0x7fffffff;
-            for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kStreamChunk) {
-                bool ok = ptx::mbar_wait(full(stage), ph, abort_flag, kStreamWaitCycles);
-                ok = __all_sync(0xffffffffu, ok);
-                if (ok) {
-                    const int n = min(kStreamChunk, v_end - v0);
-                    const TT* sbuf = reinterpret_cast<const TT*>(gbase + (size_t)stage * kStreamStageBytes);
-                    float x[kPerThread];                  // raw target logits
-#pragma unroll
-                    for (int j = 0; j < kPerThread / 4; ++j) {
-                        const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
-                        const float4 x4 = (e0 < n) ? Vec4<TT>::load(sbuf + e0)
-                                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                        x[4 * j] = x4.x; x[4 * j + 1] = x4.y; x[4 * j + 2] = x4.z; x[4 * j + 3] = x4.w;
-                    }
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(empty(stage));     // the chunk is in registers
-                    float cm = x[0];
-#pragma unroll
-                    for (int e = 1; e < kPerThread; ++e) cm = fmaxf(cm, x[e]);
-                    cm *= scale;                              // scale > 0 keeps the maximum
-                    if (cm > m2) {
-                        const float r = fast_exp2(m2 - cm);      // 0 when m2 = -inf
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) s4[c] *= r;
-                        m2 = cm;
-                    }
-                    if (m2 > -INFINITY) {
-#pragma unroll
-                        for (int e = 0; e < kPerThread; ++e) s4[e & 3] += fast_exp2(fmaf(x[e], scale, -m2));
-                    }
-                    if (bonus) {
-#pragma unroll
-                        for (int j = 0; j < kPerThread / 4; ++j) {
-                            const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
-                            if (e0 < n) {
-                                const int v = v0 + e0;
-                                const uint4 wq = rng.quad((uint32_t)v >> 2);
-                                const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float sc = x[4 * j + e] * p.inv_tau + gumbel_of(ws[e]);   // x/tau + G
-                                    if (wins(sc, v + e, best, bidx)) { best = sc; bidx = v + e; }
-                                }
-                            }
-                        }
-                    }
-                }
-                if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
-                if (!ok) { failed = true; break; }
-            }
-            // the item's partial, in natural-log units
+        int cur = -1, b = 0, i = 0, seg = 0;
+        bool bonus = false;
+        float m2 = -INFINITY;                            // running max of x*log2e/tau
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};              // sum of 2^(x*log2e/tau - m2), four chains
+        float best = -INFINITY;
+        int bidx = 0x7fffffff;
+        // the finished item's partial, in natural-log units
+        auto flush = [&]() {
             LseDraw st;
             st.m = m2 * kLn2;
             st.s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
@@ -187,16 +160,86 @@ verify_stream_kernel(const VerifyParams p) {
             if (m2 == -INFINITY) { st.m = -INFINITY; st.s = 0.f; }
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
-            // one partial per consumer warp: no block-wide step between items
-            if (lane == 0 && !failed)
-                p.ws.verify_part[(((size_t)b * (gamma + 1) + i) * nseg + seg) * kVerifySub + warp] = st;
-            if (failed) { *abort_flag = 1u; break; }
+            if (lane == 0) p.ws.verify_part[(((size_t)b * (gamma + 1) + i) * nseg + seg) * kVerifySub + warp] = st;
+        };
+        for (;;) {
+            bool ok = ptx::mbar_wait(full(stage), ph, abort_flag, kStreamWaitCycles);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { *abort_flag = 1u; break; }
+            const int2 meta = s_meta[stage];
+            if (meta.x < 0) break;                       // end of stream
+            if (meta.x != cur) {                         // a new item
+                if (cur >= 0) flush();
+                cur = meta.x;
+                const int Kb = decode(cur, b, i, seg);
+                bonus = (i == Kb);
+                m2 = -INFINITY;
+                s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
+                best = -INFINITY;
+                bidx = 0x7fffffff;
+            }
+            const int v0 = meta.y;
+            const int v_end = min(V, (seg + 1) * kVerifySeg);
+            const int n = min(kStreamChunk, v_end - v0);
+            const TT* sbuf = reinterpret_cast<const TT*>(gbase + (size_t)stage * kStreamStageBytes);
+            float x[kPerThread];                          // raw target logits
+#pragma unroll
+            for (int j = 0; j < kPerThread / 4; ++j) {
+                const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
+                const float4 x4 = (e0 < n) ? Vec4<TT>::load(sbuf + e0)
+                                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                x[4 * j] = x4.x; x[4 * j + 1] = x4.y; x[4 * j + 2] = x4.z; x[4 * j + 3] = x4.w;
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty(stage));     // the chunk is in registers
+            if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
+            float cm = x[0];
+#pragma unroll
+            for (int e = 1; e < kPerThread; ++e) cm = fmaxf(cm, x[e]);
+            cm *= scale;                                  // scale > 0 keeps the maximum
+            if (cm > m2) {
+                const float r = fast_exp2(m2 - cm);          // 0 when m2 = -inf
+#pragma unroll
+                for (int c = 0; c < 4; ++c) s4[c] *= r;
+                m2 = cm;
+            }
+            if (m2 > -INFINITY) {
+#pragma unroll
+                for (int e = 0; e < kPerThread; ++e) s4[e & 3] += fast_exp2(fmaf(x[e], scale, -m2));
+            }
+            if (bonus) {
+                const StreamRK rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
+#pragma unroll
+                for (int j = 0; j < kPerThread / 4; ++j) {
+                    const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
+                    if (e0 < n) {
+                        const int v = v0 + e0;
+                        const uint4 wq = rng.quad((uint32_t)v >> 2);
+                        const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float sc = x[4 * j + e] * p.inv_tau + gumbel_of(ws[e]);   // x/tau + G
+                            if (wins(sc, v + e, best, bidx)) { best = sc; bidx = v + e; }
+                        }
+                    }
+                }
+            }
         }
+        if (cur >= 0 && !*abort_flag) flush();
     }
     if (*abort_flag) {
         for (int i = 0; i < 64; ++i) __nanosleep(1000);   // let copies in flight land
     }
     __syncthreads();
+    // the last CTA out clears the work counter for the next launch
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&p.ws.vq[1], 1u) == gridDim.x - 1) {
+            p.ws.vq[0] = 0u;
+            p.ws.vq[1] = 0u;
+            __threadfence();
+        }
+    }
 }
 
 constexpr int kAcceptStaged = 1024;   // segment partials staged in shared memory (16 KB)
@@ -505,7 +548,7 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     const long long items = (long long)p.B * (p.gamma + 1) * p.ws.nseg;
     const int g1 = (int)(items < 2LL * num_sms() ? items : 2LL * num_sms());
     const size_t smem1 = 128 + (size_t)kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16 +
-                         sizeof(LseDraw) * kStreamConsumers + (p.B <= kStreamKCache ? sizeof(int) * (size_t)p.B : 0);
+                         sizeof(int2) * kStreamStages + (p.B <= kStreamKCache ? sizeof(int) * (size_t)p.B : 0);
     cudaError_t e1 = cudaFuncSetAttribute(verify_stream_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
     if (e1 != cudaSuccess) return e1;
     verify_stream_kernel<TT><<<g1, kStreamThreads, smem1, s>>>(p);
