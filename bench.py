@@ -315,11 +315,17 @@ _DRAFT_SOURCES = ("draft_rows.cu", "common.cuh", "sm100_ptx.cuh", "internal.h")
 
 
 def _draft_source_hash():
+    """SHA-256 (first 16 hex digits) of the draft kernel's sources with
+    comments and blank space removed: edits to comments keep the hash."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in _DRAFT_SOURCES:
-        with open(os.path.join(ROOT, "verify_markov_head_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "verify_markov_head_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,23 +8,22 @@
 //   x~_k       = argmax_v z + G,  lse_q = log sum exp z,  z_tok = z[x~_k]
 //
 // D[M = 128 rows, N = 128 vocabulary entries] = U tile + h * W2tile over K = r:
-//   A = the gathered rows h = W1[x~_{k-1}] (K-major, 128-byte swizzle, staged
-//       once per position; rows past the batch are zero),
+//   A = the gathered rows h = W1[x~_{k-1}] in TMEM (r bf16 per lane packed two
+//       to a column, written by the epilogue warps with tcgen05.st once per
+//       position; rows past the batch are zero),
 //   B = a 128-entry slice of W2 read by TMA straight from the [r, V] row-major
 //       tensor (MN-major, 128-byte swizzle), in 64-rank K-chunks,
-//   D = fp32 in TMEM, four buffers so the MMAs of later tiles overlap the
+//   D = fp32 in TMEM, 4 - RF buffers so the MMAs of later tiles overlap the
 //       epilogue of a tile.  Before the MMAs D is loaded with the tile's U:
 //       the U slices arrive by TMA (128 rows x 32 fp32, 128-byte swizzle) and
 //       tcgen05.cp copies them into the accumulator, so the epilogue reads
 //       U + bias in one tcgen05.ld and the U ring turns over as soon as the
 //       copies have read it.
-// A chunk of NC < 128 requests would leave TMEM lanes NC..127 (and the warps
+// A chunk of NC = 64 requests would leave TMEM lanes 64..127 (and the warps
 // that read them) idle, so the 128 lanes hold RF = 128 / NC vocabulary tiles
-// at once: the A operand is block diagonal, rows [i*NC, (i+1)*NC) carry h
-// against tile i and zeros elsewhere, so one accumulator takes RF tiles
-// through RF * r/64 K-chunk MMAs.  The zero blocks are shared: shared memory
-// holds Z^(RF-1) H_0 Z^(RF-1) H_1 ... H_last Z^(RF-1) and the window for
-// (tile i, K-chunk j) starts i blocks before H_j.
+// at once: the A operand of tile i is block diagonal, lanes [i*NC, (i+1)*NC)
+// carry h and the others zeros, so one accumulator takes RF tiles through
+// RF * r/64 K-chunk MMAs.  Each A operand takes 128 TMEM columns.
 // With the request on the TMEM lane, every epilogue thread owns one request
 // row and reads 32 consecutive vocabulary entries of it in one tcgen05.ld.
 // Each thread folds z + Gumbel into its own running Gumbel-max + log-sum-exp
