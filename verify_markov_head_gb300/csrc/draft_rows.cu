@@ -410,12 +410,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             uint32_t ph = 0, aph = 0;
             bool ok = true;
             for (int k = k_first; k <= k_last && ok; ++k) {
-                if (k > k_first &&   // h of this position staged by the epilogue warps
-                    !(ok = ptx::mbar_wait(a_ready, (uint32_t)((k - k_first - 1) & 1), abort_flag, kWaitCycles))) {
-                    site = 3;
-                    break;
-                }
-                ptx::tc_fence_after();
+                bool wait_a = k > k_first;   // h of this position is staged by the epilogue warps
                 for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
                     if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) { site = 4; break; }
                     ptx::tc_fence_after();
@@ -439,6 +434,14 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                             ptx::mma_commit(uempty(s));     // the slot is free once the copies have read it
                         }
                         if (!ok) break;
+                    }
+                    if (wait_a) {   // the first tile's U copies above do not need h
+                        if (!(ok = ptx::mbar_wait(a_ready, (uint32_t)((k - k_first - 1) & 1), abort_flag, kWaitCycles))) {
+                            site = 3;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        wait_a = false;
                     }
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
