@@ -1,5 +1,6 @@
 // draft_rows.cu -- Markov-head draft position on the tcgen05 tensor cores,
-// requests on the TMEM lanes (batches of 32 requests and more).
+// requests on the TMEM lanes (any batch with bf16 weights, fp32 U and
+// r a multiple of 64 up to 256).
 //
 // Per position k ("DSpark：半自回归生成与置信度调度的投机解码" sections 整体架构 and
 // Markov Head; "拒绝盲猜与算力空转" section on the low-rank Markov head):
@@ -870,7 +871,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 }  // namespace
 
 bool rows_supported(const DraftParams& p) {
-    return p.W_bf16 && !p.U_bf16 && p.B >= 32 && p.r % 64 == 0 && p.r <= 256 && p.V % 8 == 0 &&
+    return p.W_bf16 && !p.U_bf16 && p.B >= 1 && p.r % 64 == 0 && p.r <= 256 && p.V % 8 == 0 &&
            tma_encoder() != nullptr;
 }
 
