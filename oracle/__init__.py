@@ -16,7 +16,9 @@ Parity pins (see tests/test_oracle_*.py): Philox known-answer vectors, the
 bias equal to a numpy matmul, log-sum-exp normalisation, Gumbel-max
 chi-square, survival monotonicity, STS identity and rank preservation,
 scheduler equal to exhaustive search, lossless chi-square of the whole
-draft + verify chain.  Acceptance length on the synthetic workloads has no
+draft + verify chain; the STS fit against closed-form survivals, the
+half-open bin rule, the ratio form of the calibration error by brute force
+and recovery of known temperatures from calibrated synthetic data.  Acceptance length on the synthetic workloads has no
 published value: parity unpinned there (reported only).
 """
 from __future__ import annotations
@@ -87,6 +89,11 @@ def _load():
             lib.oracle_verify.restype = C.c_int
             lib.oracle_compact.argtypes = [i32p, i32p, i32p, C.c_int, C.c_int, i32p, i32p, i32p, i32p, i32p]
             lib.oracle_compact.restype = None
+            lib.oracle_sts_survival.argtypes = [f64p, C.c_int, C.c_int, f64p, C.c_int, f64p, C.c_int, f64p]
+            lib.oracle_sts_survival.restype = None
+            lib.oracle_sts_fit.argtypes = [f64p, i32p, C.c_int, C.c_int, f64p, C.c_int, C.c_int, opt_f64,
+                                           f64p, i32p, f64p]
+            lib.oracle_sts_fit.restype = C.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = C.c_int
             _lib = lib
@@ -174,6 +181,37 @@ def confidence_sts(h, emb, anchor, draft_tok, w_c, b_c, T):
     _load().oracle_confidence_sts(h, d, emb, e, anchor, draft_tok, w_c, float(b_c), T,
                                   nb, gamma, raw, cal, ls)
     return dict(conf_raw=raw, conf_cal=cal, log_surv=ls)
+
+
+def sts_survival(score, T_prev, k, grid):
+    """Survival of prefix k under each grid temperature, the earlier positions
+    at T_prev[:k-1]: [N, G] (oracle_sts_survival; [P2 §校准问题], [P4 §四])."""
+    score = _f64(score); grid = _f64(grid)
+    N, gamma = score.shape
+    T_prev = _f64(np.asarray(T_prev, dtype=np.float64).reshape(-1)[:max(k - 1, 0)])
+    T_pad = np.ones(gamma); T_pad[:T_prev.size] = T_prev
+    out = np.zeros((N, grid.size))
+    _load().oracle_sts_survival(score, N, gamma, np.ascontiguousarray(T_pad), int(k), grid, grid.size, out)
+    return out
+
+
+def sts_fit(score, acc_len, grid, M=15, T_fixed=None):
+    """Left-to-right STS fit (oracle_sts_fit; [P2 §校准问题], [P4 §四]).
+
+    score [N, gamma] = logit of the raw confidences, acc_len [N] accepted
+    drafts, grid [G] candidate temperatures, M equal-width ECE bins.  With
+    T_fixed [gamma] the earlier positions use those temperatures instead of
+    the chosen ones.  Returns dict(ece [gamma, G], idx [gamma], T [gamma])."""
+    score = _f64(score); acc_len = _i32(acc_len); grid = _f64(grid)
+    N, gamma = score.shape
+    assert acc_len.shape == (N,) and grid.ndim == 1
+    ece = np.zeros((gamma, grid.size)); idx = np.zeros(gamma, np.int32); T = np.zeros(gamma)
+    fixed = None if T_fixed is None else _f64(T_fixed)
+    rc = _load().oracle_sts_fit(score, acc_len, N, gamma, grid, grid.size, int(M),
+                                None if fixed is None else fixed.ctypes.data, ece, idx, T)
+    if rc != 0:
+        raise ValueError("oracle_sts_fit: bad sizes")
+    return dict(ece=ece, idx=idx, T=T)
 
 
 # --------------------------------------------------------------------------- #

@@ -427,6 +427,85 @@ void oracle_compact(const int32_t* draft_tok, const int32_t* accepted, const int
     out_off[nb] = off;
 }
 
+/* ------------------------------------------------------------------------ */
+/* STS fitting [P2 §校准问题：原始置信度不可靠], [P4 §四].                      */
+/* A validation set of N drafted blocks: score[n][i] = logit(c_i) of the      */
+/* confidence head (its pre-sigmoid score), acc_len[n] = the number of drafts */
+/* the target accepted.  The label of prefix j is acc_len >= j.  Positions    */
+/* are fitted left to right; at position k the earlier temperatures stay as   */
+/* chosen, and the survival of prefix k under candidate temperature T is      */
+/*   a_n(T) = prod_{i<k} sigma(score[n][i] / T_i) * sigma(score[n][k] / T),   */
+/* multiplied in order of i.  Its expected calibration error over M equal-    */
+/* width bins on [0, 1] (bin m holds m/M <= a < (m+1)/M, a = 1 in bin M-1) is */
+/*   ECE = sum_m |B_m|/N * |mean label - mean a over B_m|                    */
+/*       = (1/N) sum_m | sum_{n in B_m} (label_n - a_n) |.                   */
+/* T_k is the grid value with the smallest ECE (the lowest grid index among  */
+/* equal values).                                                            */
+/* ------------------------------------------------------------------------ */
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* Survival of prefix k (1-based) for every sample and every grid value:
+ * out[n][g] = a_n(grid[g]) with the earlier temperatures T_prev[0..k-2]. */
+void oracle_sts_survival(const double* score, int N, int gamma, const double* T_prev, int k,
+                         const double* grid, int G, double* out)
+{
+    for (int n = 0; n < N; ++n) {
+        const double* s = score + (size_t)n * gamma;
+        double prefix = 1.0;
+        for (int i = 1; i < k; ++i) prefix *= sigmoid(s[i - 1] / T_prev[i - 1]);
+        for (int g = 0; g < G; ++g) out[(size_t)n * G + g] = prefix * sigmoid(s[k - 1] / grid[g]);
+    }
+}
+
+/* ECE of predictions a[n] against labels y[n] in {0, 1} over M bins. */
+static double ece_of(const double* a, const int* y, int N, int M, double* sums)
+{
+    for (int m = 0; m < M; ++m) sums[m] = 0.0;
+    for (int n = 0; n < N; ++n) {
+        int m = (int)floor(a[n] * M);
+        if (m > M - 1) m = M - 1;
+        if (m < 0) m = 0;
+        sums[m] += (double)y[n] - a[n];
+    }
+    double e = 0.0;
+    for (int m = 0; m < M; ++m) e += fabs(sums[m]);
+    return e / N;
+}
+
+/* The left-to-right fit.  ece[k-1][g] = ECE of prefix k under grid[g];
+ * idx[k-1] and T_out[k-1] the chosen grid entry.  T_fixed, when non-NULL,
+ * replaces the chosen temperatures as the earlier positions' T_i (the
+ * choices are still reported), so that another fit's choices can be
+ * re-evaluated.  Returns 0, or -1 for bad sizes / out-of-memory. */
+int oracle_sts_fit(const double* score, const int32_t* acc_len, int N, int gamma,
+                   const double* grid, int G, int M, const double* T_fixed,
+                   double* ece, int32_t* idx, double* T_out)
+{
+    if (N < 1 || gamma < 1 || G < 1 || M < 1) return -1;
+    double* a = (double*)malloc(sizeof(double) * (size_t)N * G);
+    double* col = (double*)malloc(sizeof(double) * (size_t)N);
+    double* sums = (double*)malloc(sizeof(double) * (size_t)M);
+    double* T_prev = (double*)malloc(sizeof(double) * (size_t)gamma);
+    int* y = (int*)malloc(sizeof(int) * (size_t)N);
+    if (!a || !col || !sums || !T_prev || !y) { free(a); free(col); free(sums); free(T_prev); free(y); return -1; }
+    for (int k = 1; k <= gamma; ++k) {
+        oracle_sts_survival(score, N, gamma, T_prev, k, grid, G, a);
+        for (int n = 0; n < N; ++n) y[n] = acc_len[n] >= k;
+        int best = 0;
+        for (int g = 0; g < G; ++g) {
+            for (int n = 0; n < N; ++n) col[n] = a[(size_t)n * G + g];
+            const double e = ece_of(col, y, N, M, sums);
+            ece[(size_t)(k - 1) * G + g] = e;
+            if (e < ece[(size_t)(k - 1) * G + best]) best = g;
+        }
+        idx[k - 1] = best;
+        T_out[k - 1] = grid[best];
+        T_prev[k - 1] = T_fixed ? T_fixed[k - 1] : grid[best];
+    }
+    free(a); free(col); free(sums); free(T_prev); free(y);
+    return 0;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
