@@ -399,6 +399,141 @@ def run_chain(args):
     print(json.dumps(line), flush=True)
 
 
+# Special-function-unit (XU pipe) results per SM per clock on GB300: ncu
+# rates the pipe at one warp instruction per clock per SM.
+SFU_PER_SM_CLK = 32
+
+
+def run_sts(args):
+    """The STS temperature fit (dspark_sts_fit) on the benchmark's validation
+    set: 2^20 blocks, 256 candidate temperatures, 15 bins, gamma = 7.  One
+    fit is gamma launches of the evaluation kernel; each fit is timed alone
+    with CUDA events, L2 flushed in between (the inputs, 33 MB, fit in L2)."""
+    import verify_markov_head_gb300 as vm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    c = dict(workload.STS_FIT)
+    if args.sts_blocks:
+        c["N"] = args.sts_blocks
+    N, gamma, G, M = c["N"], c["gamma"], c["G"], c["M"]
+    score, acc_len = workload.sts_validation(N, gamma=gamma, seed=c["seed"], device=dev)
+    grid = workload.sts_grid(G, c["lo"], c["hi"]).to(dev)
+    T = torch.empty(gamma, dtype=torch.float32, device=dev)
+    idx = torch.empty(gamma, dtype=torch.int32, device=dev)
+    ece = torch.empty(gamma, G, dtype=torch.float64, device=dev)
+    ws = torch.zeros(vm.dspark_sts_workspace_bytes(gamma, G, M), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize(dev)
+
+    def fit():
+        vm.dspark_sts_fit(score, acc_len, grid, M=M, T_out=T, idx_out=idx, ece_out=ece, ws=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            fit()
+    st, bits = vm.dspark_sync_status(ws, stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} bits {bits}")
+    reps = max(3, min(args.steps, 200))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with ClockSampler(0) as clk:
+        t_pre = time.monotonic()
+        with torch.cuda.stream(stream):
+            while time.monotonic() - t_pre < 1.0:
+                fit()
+                stream.synchronize()
+        clk.mark("start")
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                flush.fill_(1)
+                a.record(stream)
+                fit()
+                b.record(stream)
+        stream.synchronize()
+        clk.mark("end")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    evals = N * G * gamma
+    value = evals / (ms / 1e3)
+    clocks = clk.summary()
+    mhz = clocks.get("sm_max_mhz") or 2070.0
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = n_sm * SFU_PER_SM_CLK * mhz * 1e6 / 2 / 1e9      # two SFU operations per evaluation
+
+    # end to end: host (pinned) inputs copied in, results read back, per fit
+    h_score, h_acc = score.cpu().pin_memory(), acc_len.cpu().pin_memory()
+    h_T = torch.empty(gamma, dtype=torch.float32).pin_memory()
+    h_idx = torch.empty(gamma, dtype=torch.int32).pin_memory()
+    h_ece = torch.empty(gamma, G, dtype=torch.float64).pin_memory()
+    d_score, d_acc = torch.empty_like(score), torch.empty_like(acc_len)
+
+    def fit_e2e():
+        d_score.copy_(h_score, non_blocking=True)
+        d_acc.copy_(h_acc, non_blocking=True)
+        vm.dspark_sts_fit(d_score, d_acc, grid, M=M, T_out=T, idx_out=idx, ece_out=ece, ws=ws, stream=stream)
+        h_T.copy_(T, non_blocking=True)
+        h_idx.copy_(idx, non_blocking=True)
+        h_ece.copy_(ece, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        fit_e2e()
+    stream.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_reps = max(3, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for _ in range(e2e_reps):
+            fit_e2e()
+        f1.record(stream)
+    stream.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / e2e_reps
+    if not torch.equal(h_idx, idx.cpu()):
+        raise SystemExit("end-to-end fit disagrees with the device-resident fit")
+    st, bits = vm.dspark_sync_status(ws, stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} bits {bits}")
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = sts_cpu_baseline(score.cpu(), acc_len.cpu(), grid.cpu(), M, budget_s=args.cpu_budget)
+    line = {"metric": f"STS fit candidate evaluations/s (N={N} blocks, G={G}, M={M}, γ={gamma})",
+            "value": value, "unit": "evaluations/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 survivals and bins, int64 fixed-point bin totals", "data": "synthetic",
+            "config": {"workload": f"sts_fit: N={N} gamma={gamma} G={G} M={M}, grid [{c['lo']}, {c['hi']}]",
+                       "l2": "256 MB buffer written between timed fits", "parallelism": "dp1"},
+            "roofline": {"kernel": "sts_eval_kernel<4> (dspark_sts_fit, one launch per position)",
+                         "note": "2^x + reciprocal per evaluation on the SFU; the shared-memory bin update shares their issue path",
+                         "bound": "alu", "achieved": value / 1e9, "peak": peak,
+                         "peak_kind": f"derived: {n_sm} SMs x {SFU_PER_SM_CLK} SFU results/clk x "
+                                      f"{mhz:.0f} MHz / 2 per evaluation",
+                         "unit": "Geval/s", "frac": value / 1e9 / peak, "traffic": None,
+                         "launch_ms": ms / gamma},
+            "e2e": {"value": evals / (e2e_ms / 1e3), "unit": "evaluations/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h_score.numel() * 4 + h_acc.numel() * 4,
+                    "d2h_bytes_per_step": h_T.numel() * 4 + h_idx.numel() * 4 + h_ece.numel() * 8},
+            "gpu_launches": gamma * reps, "clocks": clocks, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+
+
+def sts_cpu_baseline(score, acc_len, grid, M, budget_s=20.0):
+    """The oracle's STS fit, as it stands, on the first S blocks of the
+    validation set with the whole grid (S sized to a ~budget_s run)."""
+    import oracle
+
+    gamma, G = score.shape[1], grid.numel()
+    t = time.perf_counter()
+    oracle.sts_fit(score[:4096], acc_len[:4096], grid.double(), M=M)
+    per_block = (time.perf_counter() - t) / 4096
+    S = int(max(4096, min(score.shape[0], budget_s / max(per_block, 1e-9))))
+    t = time.perf_counter()
+    oracle.sts_fit(score[:S], acc_len[:S], grid.double(), M=M)
+    dt = time.perf_counter() - t
+    return {"value": S * G * gamma / dt, "unit": "evaluations/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {S} of {score.shape[0]} blocks, all {G} temperatures, {dt:.1f} s", "seconds": dt}
+
+
 def d_of(w):
     return w.d
 
@@ -552,6 +687,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chain", action="store_true",
                     help="time the workload's chained steps (b512: 16 steps, async scheduler) instead of one step")
+    ap.add_argument("--sts", action="store_true",
+                    help="time the STS temperature fit (2^20 validation blocks, 256 temperatures)")
+    ap.add_argument("--sts-blocks", type=int, default=None,
+                    help="validation blocks of the STS fit (default 2^20; smaller for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -559,6 +698,8 @@ def main():
         run_reference(args)
     elif args.chain:
         run_chain(args)
+    elif args.sts:
+        run_sts(args)
     else:
         run_gpu(args)
 

@@ -61,6 +61,8 @@ typedef enum {
 /* Limits of this build. */
 #define DSPARK_MAX_GAMMA 16
 #define DSPARK_MAX_SCHED_ITEMS 4096   /* B * gamma for dspark_schedule */
+#define DSPARK_MAX_STS_GRID 65536     /* candidate temperatures for dspark_sts_fit */
+#define DSPARK_MAX_STS_BINS 64        /* calibration-error bins for dspark_sts_fit */
 
 /* Library version (major*10000 + minor*100 + patch). */
 int dspark_version(void);
@@ -80,8 +82,10 @@ dspark_status dspark_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * Returns DSPARK_OK, DSPARK_ERR_DEVICE (range check fired), DSPARK_ERR_TIMEOUT,
  * or DSPARK_ERR_CUDA (the stream reported an error).  If bits is non-NULL the
  * raw status bits are stored there: bit 0 a token out of [0, V), bit 1 a
- * block length out of [0, gamma], bit 2 a bounded wait expired, and with
- * bit 2 the bits 8-23 name the wait that gave up (for diagnosis only). */
+ * block length out of [0, gamma], bit 2 a bounded wait expired, bit 3 a
+ * non-finite score or a temperature that is not positive and finite
+ * (dspark_sts_fit), and with bit 2 the bits 8-23 name the wait that gave up
+ * (for diagnosis only). */
 dspark_status dspark_sync_status(void* ws, void* stream, uint32_t* bits);
 
 /*
@@ -216,6 +220,37 @@ dspark_status dspark_draft_markov_noalloc(
     uint64_t seed, uint64_t step,
     int32_t* draft_tok, float* lse_q, float* z_tok, float* logits_out,
     void* stream);
+
+/*
+ * Sequential temperature scaling fit [P2 §校准问题：原始置信度不可靠], [P4 §四].
+ * Off the decode path: it chooses the temperatures T that
+ * dspark_confidence_sts applies, from a validation set of N drafted blocks.
+ *   score   [N,gamma] fp32: logit(c_k), the confidence head's pre-sigmoid
+ *           score of each draft position (finite).
+ *   acc_len [N] int32: drafts of the block the target accepted (0..gamma);
+ *           prefix k counts as accepted when acc_len >= k.
+ *   grid    [G] fp32: candidate temperatures (positive, finite).
+ * Left to right, for k = 1..gamma, with T_1..T_{k-1} already chosen:
+ *   a_n(T)   = prod_{i<k} sigmoid(score[n,i] / T_i) * sigmoid(score[n,k] / T)
+ *   ECE_k(T) = (1/N) sum_m | sum_{n: bin(a_n) = m} ([acc_len_n >= k] - a_n) |,
+ *              bin(a) = min(floor(a*M), M-1)  (M equal-width bins of [0, 1])
+ *   T_k      = grid[idx_k], idx_k the lowest index minimising ECE_k.
+ * Outputs: T_out [gamma] fp32, idx_out [gamma] int32, ece_out [gamma,G] fp64.
+ * Precision: survivals and bins in binary32 (a sample within about
+ *   M*k*6e-7 of a bin edge in units of 1/M may land in the neighbouring
+ *   bin), bin totals in 2^-24 fixed point, so equal candidates tie exactly.
+ * ws     : dspark_sts_workspace_bytes(gamma, G, M) bytes, 256-byte aligned;
+ *          the call clears it (no init needed) and keeps its status word at
+ *          offset 0 (read it with dspark_sync_status: bit 3 reports a bad
+ *          score or temperature; the results are then unspecified).
+ * Limits : 1 <= gamma <= DSPARK_MAX_GAMMA, 1 <= G <= DSPARK_MAX_STS_GRID,
+ *          1 <= M <= DSPARK_MAX_STS_BINS, N >= 1.  gamma launches on stream.
+ */
+size_t dspark_sts_workspace_bytes(int gamma, int G, int M);
+dspark_status dspark_sts_fit(const float* score, const int32_t* acc_len, int N, int gamma,
+                             const float* grid, int G, int M,
+                             float* T_out, int32_t* idx_out, double* ece_out,
+                             void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Diagnostics: the random stream as the kernels draw it.  For columns

@@ -51,6 +51,11 @@ def test_workspace_sizes(lib):
     assert lib.dspark_workspace_bytes(0, 7, 1024, 32) == 0        # B < 1
     assert lib.dspark_workspace_bytes(4, 17, 1024, 32) == 0       # gamma above the limit
     assert lib.dspark_workspace_bytes(4, 7, 1020, 32) == 0        # V not a multiple of 8
+    lib.dspark_sts_workspace_bytes.restype = C.c_size_t
+    assert lib.dspark_sts_workspace_bytes(7, 256, 15) >= 7 * 256 * 15 * 8   # int64 bin totals
+    assert lib.dspark_sts_workspace_bytes(7, 65537, 15) == 0      # grid above the limit
+    assert lib.dspark_sts_workspace_bytes(7, 256, 65) == 0        # bins above the limit
+    assert lib.dspark_sts_workspace_bytes(0, 256, 15) == 0        # gamma < 1
 
 
 def test_null_pointers_are_rejected_without_a_device(lib):

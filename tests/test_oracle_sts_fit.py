@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
+import workload
 
 LN3 = math.log(3.0)
 
@@ -99,28 +100,16 @@ def test_ratio_form_by_brute_force():
         prev.append(r["T"][k - 1])
 
 
-def _calibrated_data(N, T_true, seed):
-    """Blocks whose drafts are accepted with probability sigmoid(score_k / T*_k),
-    left to right until the first rejection: P(acc_len >= k) is exactly the
-    STS survival at T = T*."""
-    rng = np.random.default_rng(seed)
-    gamma = len(T_true)
-    score = rng.normal(1.5, 2.0, size=(N, gamma))
-    p = 1 / (1 + np.exp(-score / np.asarray(T_true)))
-    ok = rng.random((N, gamma)) < p
-    acc_len = np.where(ok.all(axis=1), gamma, np.argmin(ok, axis=1))
-    return score, acc_len
-
-
 def test_recovers_known_temperatures():
     T_true = [0.5, 2.0, 1.0, 3.0]
-    score, acc_len = _calibrated_data(100_000, T_true, seed=3)
+    score, acc_len = workload.sts_validation(100_000, gamma=4, seed=3, T_true=T_true)
     grid = np.round(np.arange(0.25, 4.01, 0.25), 2)
     r = oracle.sts_fit(score, acc_len, grid, M=15)
     np.testing.assert_allclose(r["T"], T_true, atol=0.25)
     assert (r["ece"].min(axis=1) < 0.01).all()
-    # A single shared temperature on every factor (the wrong reading) cannot
-    # calibrate position 2 as well as the sequential fit does.
+    # The raw confidences (T = 1) are clearly miscalibrated wherever T* != 1.
+    # (Reading the page's formula with T_k on every factor instead would need
+    # one temperature to fit 0.5 and 2.0 at once at position 2, and misses T*.)
     one = np.where(grid == 1.0)[0][0]
     assert (r["ece"][[0, 1, 3], one] > 3 * r["ece"].min(axis=1)[[0, 1, 3]]).all()
 

@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
+    "dspark_schedule", "dspark_verify", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
@@ -57,6 +57,10 @@ _lib.dspark_verify.restype = _i
 _lib.dspark_draft_markov_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
                                              _vp, _vp, _vp, _vp, _vp]
 _lib.dspark_draft_markov_noalloc.restype = _i
+_lib.dspark_sts_workspace_bytes.argtypes = [_i, _i, _i]
+_lib.dspark_sts_workspace_bytes.restype = _sz
+_lib.dspark_sts_fit.argtypes = [_vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_sts_fit.restype = _i
 _lib.dspark_gumbel_stream.argtypes = [_u64, _u64, C.c_uint32, C.c_uint32, _i, _vp, _vp, _vp]
 _lib.dspark_gumbel_stream.restype = _i
 
@@ -163,6 +167,38 @@ def dspark_confidence_sts(h, emb, anchor, draft_tok, w_c, b_c, T, conf_cal, log_
     _check("dspark_confidence_sts", _lib.dspark_confidence_sts(
         _p(h), d, _p(emb), _dt(emb), e, _p(anchor), _p(draft_tok), _p(w_c), float(b_c), _p(T),
         B, gamma, V, _p(conf_cal), _p(log_surv), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def dspark_sts_workspace_bytes(gamma, G, M) -> int:
+    return int(_lib.dspark_sts_workspace_bytes(gamma, G, M))
+
+
+def dspark_sts_fit(score, acc_len, grid, *, M=15, T_out=None, idx_out=None, ece_out=None, ws=None,
+                   stream=None):
+    """Left-to-right STS temperature fit on the device: score [N, gamma] fp32,
+    acc_len [N] int32, grid [G] fp32.  Returns (T [gamma] fp32, idx [gamma]
+    int32, ece [gamma, G] fp64); outputs and the workspace (a uint8 tensor)
+    are allocated on score's device when not given."""
+    N, gamma = score.shape
+    G = grid.numel()
+    if score.dtype != torch.float32 or grid.dtype != torch.float32 or acc_len.dtype != torch.int32:
+        raise TypeError("score and grid must be float32, acc_len int32")
+    if acc_len.numel() != N:
+        raise ValueError("acc_len must hold one length per block")
+    dev = score.device
+    nbytes = dspark_sts_workspace_bytes(gamma, G, M)
+    if nbytes == 0:
+        raise ValueError("gamma, grid size or bin count out of range")
+    T_out = torch.empty(gamma, dtype=torch.float32, device=dev) if T_out is None else T_out
+    idx_out = torch.empty(gamma, dtype=torch.int32, device=dev) if idx_out is None else idx_out
+    ece_out = torch.empty(gamma, G, dtype=torch.float64, device=dev) if ece_out is None else ece_out
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if ws is None else ws
+    if T_out.numel() != gamma or idx_out.numel() != gamma or ece_out.numel() != gamma * G:
+        raise ValueError("output buffers have the wrong size")
+    _check("dspark_sts_fit", _lib.dspark_sts_fit(
+        _p(score), _p(acc_len), N, gamma, _p(grid), G, int(M), _p(T_out), _p(idx_out), _p(ece_out),
+        _p(ws), ws.numel(), _stream(stream)))
+    return T_out, idx_out, ece_out
 
 
 def dspark_schedule(log_surv, sps, mode, K, n_total, theta, ws: Workspace, *, log_surv_hist=None,

@@ -260,4 +260,42 @@ dspark_status dspark_gumbel_stream(uint64_t seed, uint64_t step, uint32_t domain
                                               static_cast<cudaStream_t>(stream)));
 }
 
+static size_t sts_tickets_off() { return 256; }
+static size_t sts_acc_off(int gamma) { return align256(sts_tickets_off() + sizeof(uint32_t) * (size_t)gamma); }
+static size_t sts_ws_total(int gamma, int G, int M) {
+    return align256(sts_acc_off(gamma) + sizeof(long long) * (size_t)gamma * M * G);
+}
+
+size_t dspark_sts_workspace_bytes(int gamma, int G, int M) {
+    if (gamma < 1 || gamma > DSPARK_MAX_GAMMA || G < 1 || G > DSPARK_MAX_STS_GRID || M < 1 || M > DSPARK_MAX_STS_BINS)
+        return 0;
+    return sts_ws_total(gamma, G, M);
+}
+
+dspark_status dspark_sts_fit(const float* score, const int32_t* acc_len, int N, int gamma, const float* grid,
+                             int G, int M, float* T_out, int32_t* idx_out, double* ece_out, void* ws,
+                             size_t ws_bytes, void* stream) {
+    if (N < 1 || dspark_sts_workspace_bytes(gamma, G, M) == 0) return DSPARK_ERR_INVALID;
+    if (!is_device_ptr(score) || !is_device_ptr(acc_len) || !is_device_ptr(grid) || !is_device_ptr(T_out) ||
+        !is_device_ptr(idx_out) || !is_device_ptr(ece_out) || !is_device_ptr(ws))
+        return DSPARK_ERR_INVALID;
+    if (!aligned(score, 4) || !aligned(acc_len, 4) || !aligned(grid, 4) || !aligned(T_out, 4) ||
+        !aligned(idx_out, 4) || !aligned(ece_out, 8) || !aligned(ws, 256))
+        return DSPARK_ERR_INVALID;
+    const size_t total = sts_ws_total(gamma, G, M);
+    if (ws_bytes < total) return DSPARK_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(ws, 0, total, s);
+    if (e != cudaSuccess) return launch_status(e);
+    char* base = static_cast<char*>(ws);
+    StsFitParams p;
+    p.score = score; p.acc_len = acc_len; p.N = N; p.gamma = gamma;
+    p.grid = grid; p.G = G; p.M = M;
+    p.T_out = T_out; p.idx_out = idx_out; p.ece_out = ece_out;
+    p.status = reinterpret_cast<uint32_t*>(base);
+    p.tickets = reinterpret_cast<uint32_t*>(base + sts_tickets_off());
+    p.acc = reinterpret_cast<long long*>(base + sts_acc_off(gamma));
+    return launch_status(launch_sts_fit(p, s));
+}
+
 }  // extern "C"

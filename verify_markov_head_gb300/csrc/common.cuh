@@ -289,6 +289,7 @@ enum StatusBits : uint32_t {
     kBadToken = 1u << 0,     // a token id outside [0, V)
     kBadLength = 1u << 1,    // a verify length outside [0, gamma]
     kTimeout = 1u << 2,      // a bounded wait expired
+    kBadInput = 1u << 3,     // a non-finite score or a temperature that is not positive and finite
 };
 
 __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {

@@ -97,6 +97,15 @@ struct VerifyParams {
     WsPtrs ws;
 };
 
+struct StsFitParams {
+    const float* score; const int32_t* acc_len; int N, gamma;
+    const float* grid; int G, M;
+    float* T_out; int32_t* idx_out; double* ece_out;
+    long long* acc;      // [gamma][M][G] fixed-point bin totals, zero before the fit
+    uint32_t* tickets;   // [gamma] arrival tickets, zero before the fit
+    uint32_t* status;
+};
+
 int num_sms();
 
 // Launchers (return cudaSuccess or the launch error).
@@ -126,5 +135,6 @@ cudaError_t launch_gumbel_stream(uint64_t seed, uint64_t step, uint32_t domain, 
 cudaError_t launch_confidence(const ConfParams& p, cudaStream_t s);
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_sts_fit(const StsFitParams& p, cudaStream_t s);
 
 }  // namespace dspark

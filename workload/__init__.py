@@ -155,3 +155,36 @@ def inputs(w: Workload, step: int = 0, device="cpu") -> dict:
     d = weights(w, device)
     d.update(step_inputs(w, step, device))
     return d
+
+
+def sts_validation(N: int, gamma: int = GAMMA, seed: int = 0, T_true=None, device="cpu"):
+    """A synthetic validation set for the STS fit: raw confidence scores
+    [N, gamma] fp32 (the logits of c_k) and accepted lengths [N] int32.
+
+    Scores s_k ~ N(3 - 0.3k, 2.5^2), confidence falling along the block.  The
+    target accepts draft k with probability 1 / (1 + exp(-s_k / T*_k)), left
+    to right until its first rejection, so the probability that prefix k is
+    accepted is the STS survival at T = T*, and the raw confidences are
+    over-confident wherever T*_k > 1.  T* defaults to the workloads' inference
+    temperatures 1 + 0.1k."""
+    if T_true is None:
+        T_true = [1.0 + 0.1 * k for k in range(1, gamma + 1)]
+    T_true = torch.tensor(T_true, dtype=torch.float64, device=device)
+    assert T_true.numel() == gamma
+    g = _gen(device, seed, 7, N, gamma)
+    mean = torch.tensor([3.0 - 0.3 * k for k in range(1, gamma + 1)], dtype=torch.float64, device=device)
+    score = (torch.randn((N, gamma), generator=g, device=device, dtype=torch.float64) * 2.5 + mean).float()
+    p_acc = torch.sigmoid(score.double() / T_true)
+    ok = torch.rand((N, gamma), generator=g, device=device, dtype=torch.float64) < p_acc
+    first_rej = torch.where(ok.all(dim=1), torch.full((N,), gamma, device=device),
+                            torch.argmin(ok.to(torch.int8), dim=1))
+    return score.contiguous(), first_rej.to(torch.int32).contiguous()
+
+
+# The STS fit measured by the benchmark: a validation set of 2^20 drafted
+# blocks, 256 candidate temperatures evenly spaced on [0.25, 4], 15 bins.
+STS_FIT = dict(N=1 << 20, gamma=GAMMA, G=256, M=15, lo=0.25, hi=4.0, seed=0)
+
+
+def sts_grid(G: int, lo: float = 0.25, hi: float = 4.0) -> torch.Tensor:
+    return torch.linspace(lo, hi, G, dtype=torch.float32)
