@@ -83,8 +83,16 @@ def _load():
                 f64p, opt_f64, f64p, C.c_int, C.c_int, C.c_int, C.c_int,
                 i32p, i32p, f64p, i32p, f64p]
             lib.oracle_schedule.restype = C.c_int
+            lib.oracle_gru_cell.argtypes = [f64p, f64p, f64p, f64p, f64p, f64p, C.c_int, C.c_int, f64p]
+            lib.oracle_gru_cell.restype = None
+            lib.oracle_bf16_round.argtypes = [C.c_double]
+            lib.oracle_bf16_round.restype = C.c_double
+            lib.oracle_draft_rnn.argtypes = [
+                f64p, f64p, f64p, f64p, f64p, f64p, f64p, f64p, i32p, i32p, C.c_int, C.c_int, C.c_int,
+                C.c_int, C.c_double, C.c_uint64, C.c_uint64, i32p, f64p, f64p, f64p, f64p, f64p]
+            lib.oracle_draft_rnn.restype = C.c_int
             lib.oracle_verify.argtypes = [
-                f64p, f64p, f64p, f64p, i32p, i32p, i32p, i32p, C.c_int, C.c_int, C.c_int, C.c_int,
+                f64p, f64p, opt_f64, f64p, opt_f64, i32p, i32p, i32p, i32p, C.c_int, C.c_int, C.c_int, C.c_int,
                 C.c_double, C.c_uint64, C.c_uint64, i32p, i32p, f64p, f64p, f64p]
             lib.oracle_verify.restype = C.c_int
             lib.oracle_compact.argtypes = [i32p, i32p, i32p, C.c_int, C.c_int, i32p, i32p, i32p, i32p, i32p]
@@ -167,6 +175,42 @@ def draft_markov(U, W1, W2, anchor, *, seed, step=0, tau=1.0, req=None, want_log
     return out
 
 
+def gru_cell(x, h, W_ih, W_hh, b_ih, b_hh):
+    """One GRU step h' = GRU(h, x) (oracle_gru_cell; [P2 §RNN Head：长程依赖])."""
+    x = _f64(x); h = _f64(h); W_ih = _f64(W_ih); W_hh = _f64(W_hh); b_ih = _f64(b_ih); b_hh = _f64(b_hh)
+    r, r_in = h.size, x.size
+    assert W_ih.shape == (3 * r, r_in) and W_hh.shape == (3 * r, r) and b_ih.size == b_hh.size == 3 * r
+    out = np.zeros(r)
+    _load().oracle_gru_cell(x, h, W_ih, W_hh, b_ih, b_hh, r_in, r, out)
+    return out
+
+
+def bf16_round(x) -> float:
+    return float(_load().oracle_bf16_round(float(x)))
+
+
+def draft_rnn(U, E, W_ih, W_hh, b_ih, b_hh, s0, W2, anchor, *, seed, step=0, tau=1.0, req=None):
+    """The draft loop with the RNN head (oracle_draft_rnn; [P2 §RNN Head：长程依赖], [P4 §三]).
+
+    U [nb,gamma,V], E [V,r], W_ih/W_hh [3r,r], b_ih/b_hh [3r], s0 [r], W2 [r,V].
+    Returns tok, lse_q, z_tok, gap, states [nb,gamma,r] (s_k) and arows
+    [nb,gamma,r] (s_k rounded to bfloat16: the rows the biases are formed from)."""
+    U = _f64(U); E = _f64(E); W_ih = _f64(W_ih); W_hh = _f64(W_hh); b_ih = _f64(b_ih)
+    b_hh = _f64(b_hh); s0 = _f64(s0); W2 = _f64(W2); anchor = _i32(anchor)
+    nb, gamma, V = U.shape
+    r = s0.size
+    assert E.shape == (V, r) and W2.shape == (r, V) and W_ih.shape == (3 * r, r) and W_hh.shape == (3 * r, r)
+    req = np.arange(nb, dtype=np.int32) if req is None else _i32(req)
+    tok = np.zeros((nb, gamma), np.int32)
+    lse = np.zeros((nb, gamma)); ztok = np.zeros((nb, gamma)); gap = np.zeros((nb, gamma))
+    states = np.zeros((nb, gamma, r)); arows = np.zeros((nb, gamma, r))
+    rc = _load().oracle_draft_rnn(U, E, W_ih, W_hh, b_ih, b_hh, s0, W2, anchor, req, nb, gamma, V, r,
+                                  float(tau), int(seed), int(step), tok, lse, ztok, gap, states, arows)
+    if rc != 0:
+        raise ValueError("oracle_draft_rnn: invalid arguments")
+    return dict(tok=tok, lse_q=lse, z_tok=ztok, gap=gap, states=states, arows=arows)
+
+
 # --------------------------------------------------------------------------- #
 # a4 confidence + STS + survival [P2 §置信度头, §校准问题], [P4 §四]            #
 # --------------------------------------------------------------------------- #
@@ -238,19 +282,24 @@ def schedule(log_surv, sps, mode, log_surv_hist=None):
 # --------------------------------------------------------------------------- #
 # a6-a8 verification and compaction [P2 §形式化定义], [P4 §四, §五]               #
 # --------------------------------------------------------------------------- #
-def verify(target, U, W1, W2, anchor, draft_tok, K, *, seed, step=0, tau=1.0, req=None):
+def verify(target, U, W1, W2, anchor, draft_tok, K, *, seed, step=0, tau=1.0, req=None, arows=None):
     """target [nb,gamma+1,V], U [nb,gamma,V]; returns accepted, final_tok,
-    p_tok, q_tok and diag [nb,6] (see dspark_oracle.c)."""
-    target = _f64(target); U = _f64(U); W1 = _f64(W1); W2 = _f64(W2)
+    p_tok, q_tok and diag [nb,6] (see dspark_oracle.c).  With arows
+    [nb,gamma,r] (the RNN head's bias rows) W1 may be None."""
+    target = _f64(target); U = _f64(U); W2 = _f64(W2)
+    W1 = None if W1 is None else _f64(W1)
+    arows = None if arows is None else _f64(arows)
     anchor = _i32(anchor); draft_tok = _i32(draft_tok); K = _i32(K)
     nb, gamma, V = U.shape
-    r = W1.shape[1]
+    r = W2.shape[0]
+    assert (W1 is None or W1.shape == (V, r)) and (arows is None or arows.shape == (nb, gamma, r))
     assert target.shape == (nb, gamma + 1, V) and K.shape == (nb,)
     req = np.arange(nb, dtype=np.int32) if req is None else _i32(req)
     acc = np.zeros(nb, np.int32); fin = np.zeros(nb, np.int32)
     pt = np.full((nb, gamma), np.nan); qt = np.full((nb, gamma), np.nan)
     diag = np.zeros((nb, 6))
-    rc = _load().oracle_verify(target, U, W1, W2, anchor, draft_tok, K, req, nb, gamma, V, r,
+    rc = _load().oracle_verify(target, U, None if W1 is None else W1.ctypes.data, W2,
+                               None if arows is None else arows.ctypes.data, anchor, draft_tok, K, req, nb, gamma, V, r,
                                float(tau), int(seed), int(step), acc, fin, pt, qt, diag)
     if rc != 0:
         raise ValueError("oracle_verify: invalid arguments")

@@ -122,13 +122,12 @@ static int gumbel_argmax(const double* score, int n, uint64_t seed, uint64_t ste
     return best;
 }
 
-/* Transition bias of the Markov head, [P2 §Markov Head：一阶转移偏置] and
- * [P3 §DSpark 的解法 ... 低秩马尔可夫头]: h = W1[x] (a row of rank r), then
- * B(v) = h . W2[:, v] for every vocabulary entry v.  Accumulated row by row of
- * W2, i.e. in increasing rho for every v. */
-static void markov_bias(const double* W1, const double* W2, int V, int r, int x, double* bias)
+/* Transition bias [P2 §Markov Head：一阶转移偏置], [P3 §DSpark 的解法 ...
+ * 低秩马尔可夫头]: B(v) = h . W2[:, v] for every vocabulary entry v, from a
+ * rank-r row h: the Markov head's h = W1[x~_{k-1}], the RNN head's state.
+ * Accumulated row by row of W2, i.e. in increasing rho for every v. */
+static void bias_of_row(const double* h, const double* W2, int V, int r, double* bias)
 {
-    const double* h = W1 + (size_t)x * r;
     for (int v = 0; v < V; ++v) bias[v] = 0.0;
     for (int rho = 0; rho < r; ++rho) {
         const double hr = h[rho];
@@ -137,12 +136,12 @@ static void markov_bias(const double* W1, const double* W2, int V, int r, int x,
     }
 }
 
-/* Draft logits of one position: z = (U_k + B_k(x_prev)) / tau
+/* Draft logits of one position: z = (U_k + B_k) / tau, B_k from the row h
  * [P2 §整体架构: the draft distribution is built from U_k plus B_k]. */
-static void draft_logits(const double* U_row, const double* W1, const double* W2, int V, int r,
-                         int x_prev, double tau, double* z)
+static void draft_logits(const double* U_row, const double* h, const double* W2, int V, int r,
+                         double tau, double* z)
 {
-    markov_bias(W1, W2, V, r, x_prev, z);
+    bias_of_row(h, W2, V, r, z);
     for (int v = 0; v < V; ++v) z[v] = (U_row[v] + z[v]) / tau;
 }
 
@@ -168,7 +167,7 @@ int oracle_draft_markov(const double* U, const double* W1, const double* W2,
         for (int k = 1; k <= gamma; ++k) {
             if (x_prev < 0 || x_prev >= V) { bad = 1; break; }
             const size_t row = (size_t)b * gamma + (size_t)(k - 1);
-            draft_logits(U + row * V, W1, W2, V, r, x_prev, tau, z);
+            draft_logits(U + row * V, W1 + (size_t)x_prev * r, W2, V, r, tau, z);
             if (logits) memcpy(logits + row * V, z, sizeof(double) * (size_t)V);
             double g;
             const uint32_t prow = (uint32_t)req[b] * (uint32_t)(gamma + 1) + (uint32_t)(k - 1);
@@ -315,6 +314,96 @@ int oracle_schedule(const double* log_surv, const double* log_surv_hist,
 }
 
 /* ------------------------------------------------------------------------ */
+/* RNN head [P2 §RNN Head：长程依赖], [P4 §三].  The pages name a GRU-style    */
+/* recurrent state started from a learned vector and mapped to the           */
+/* vocabulary like the Markov head's row; the cell's formula is not printed. */
+/* Taken here: the standard GRU cell (Cho et al. 2014, in the form with the  */
+/* reset gate applied to the hidden projection, as PyTorch's GRUCell),       */
+/*   r  = sigma(W_ir x + b_ir + W_hr h + b_hr)                               */
+/*   z  = sigma(W_iz x + b_iz + W_hz h + b_hz)                               */
+/*   n  = tanh(W_in x + b_in + r * (W_hn h + b_hn))                          */
+/*   h' = (1 - z) * n + z * h,                                               */
+/* gate rows stacked (r, z, n) in W_ih [3r][r_in], W_hh [3r][r], b_ih, b_hh. */
+/* For k = 1..gamma: s_k = GRU(s_{k-1}, E[x~_{k-1}]) with s_0 the learned     */
+/* vector and x~_0 the anchor; B_k is formed from s_k rounded to bfloat16,   */
+/* the dtype of W2 (and of the Markov head's W1 rows).                      */
+/* ------------------------------------------------------------------------ */
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+void oracle_gru_cell(const double* x, const double* h, const double* W_ih, const double* W_hh,
+                     const double* b_ih, const double* b_hh, int r_in, int r, double* h_out)
+{
+    for (int j = 0; j < r; ++j) {
+        double gi[3], gh[3];
+        for (int g = 0; g < 3; ++g) {
+            const double* wi = W_ih + ((size_t)g * r + j) * r_in;
+            const double* wh = W_hh + ((size_t)g * r + j) * r;
+            double si = b_ih[g * r + j], sh = b_hh[g * r + j];
+            for (int i = 0; i < r_in; ++i) si += wi[i] * x[i];
+            for (int i = 0; i < r; ++i) sh += wh[i] * h[i];
+            gi[g] = si;
+            gh[g] = sh;
+        }
+        const double rg = sigmoid(gi[0] + gh[0]);
+        const double zg = sigmoid(gi[1] + gh[1]);
+        const double ng = tanh(gi[2] + rg * gh[2]);
+        h_out[j] = (1.0 - zg) * ng + zg * h[j];
+    }
+}
+
+/* Nearest bfloat16 value (8 significant bits, ties to even). */
+double oracle_bf16_round(double x)
+{
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    frexp(x, &e);                       /* |x| = f 2^e, f in [1/2, 1) */
+    const double q = ldexp(1.0, e - 8);  /* spacing of 8-bit significands at |x| */
+    return rint(x / q) * q;
+}
+
+int oracle_draft_rnn(const double* U, const double* E, const double* W_ih, const double* W_hh,
+                     const double* b_ih, const double* b_hh, const double* s0, const double* W2,
+                     const int32_t* anchor, const int32_t* req,
+                     int nb, int gamma, int V, int r, double tau,
+                     uint64_t seed, uint64_t step,
+                     int32_t* draft_tok, double* lse_q, double* z_tok, double* gap,
+                     double* states, double* arows)
+{
+    if (nb < 0 || gamma < 1 || V < 1 || r < 1 || !(tau > 0.0)) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int b = 0; b < nb; ++b) {
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        double* h = (double*)malloc(sizeof(double) * (size_t)r);
+        double* hn = (double*)malloc(sizeof(double) * (size_t)r);
+        double* hq = (double*)malloc(sizeof(double) * (size_t)r);
+        if (!z || !h || !hn || !hq) { bad = 1; free(z); free(h); free(hn); free(hq); continue; }
+        memcpy(h, s0, sizeof(double) * (size_t)r);
+        int x_prev = anchor[b];
+        for (int k = 1; k <= gamma; ++k) {
+            if (x_prev < 0 || x_prev >= V) { bad = 1; break; }
+            const size_t row = (size_t)b * gamma + (size_t)(k - 1);
+            oracle_gru_cell(E + (size_t)x_prev * r, h, W_ih, W_hh, b_ih, b_hh, r, r, hn);
+            memcpy(h, hn, sizeof(double) * (size_t)r);
+            for (int i = 0; i < r; ++i) hq[i] = oracle_bf16_round(h[i]);
+            if (states) memcpy(states + row * r, h, sizeof(double) * (size_t)r);
+            if (arows) memcpy(arows + row * r, hq, sizeof(double) * (size_t)r);
+            draft_logits(U + row * V, hq, W2, V, r, tau, z);
+            double g;
+            const uint32_t prow = (uint32_t)req[b] * (uint32_t)(gamma + 1) + (uint32_t)(k - 1);
+            const int x = gumbel_argmax(z, V, seed, step, 0u, prow, &g);
+            draft_tok[row] = x;
+            lse_q[row] = logsumexp(z, V);
+            z_tok[row] = z[x];
+            if (gap) gap[row] = g;
+            x_prev = x;
+        }
+        free(z); free(h); free(hn); free(hq);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Steps a6-a8: lossless verification and ragged output [P2 §形式化定义],      */
 /* [P4 §四, §五].  For request b with verify length K_b:                       */
 /*   p_i = softmax(target[b, i] / tau) for rows i = 0..K_b (p_{i+1});         */
@@ -323,6 +412,8 @@ int oracle_schedule(const double* log_surv, const double* log_surv_hist,
 /*   at the first rejection j draw from norm(max(0, p_j - q_j)) (from p_j if   */
 /*   that residual is identically zero); if all K_b are accepted draw the      */
 /*   bonus token from p_{K_b + 1}.                                            */
+/* q_k is rebuilt from the same bias row as the draft: W1[x~_{k-1}], or, when  */
+/* arows [nb][gamma][r] is given (the RNN head), arows[b][k-1].              */
 /* Outputs are laid out flat: offsets = exclusive scan of (A_b + 1).          */
 /* diag[b*6 + .] = { min |u_k - min(1, p/q)| over the walk, gap of the final   */
 /*   draw, residual mass sum max(0, p - q) (0 if none), final-draw row,         */
@@ -330,13 +421,14 @@ int oracle_schedule(const double* log_surv, const double* log_surv_hist,
 /*   accepted count }.                                                          */
 /* ------------------------------------------------------------------------ */
 int oracle_verify(const double* target, const double* U, const double* W1, const double* W2,
+                  const double* arows,
                   const int32_t* anchor, const int32_t* draft_tok, const int32_t* K,
                   const int32_t* req, int nb, int gamma, int V, int r, double tau,
                   uint64_t seed, uint64_t step,
                   int32_t* accepted, int32_t* final_tok, double* p_tok, double* q_tok,
                   double* diag)
 {
-    if (nb < 0 || gamma < 1 || V < 1 || r < 1 || !(tau > 0.0)) return -1;
+    if (nb < 0 || gamma < 1 || V < 1 || r < 1 || !(tau > 0.0) || (!W1 && !arows)) return -1;
     int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
     for (int b = 0; b < nb; ++b) {
@@ -355,7 +447,8 @@ int oracle_verify(const double* target, const double* U, const double* W1, const
             const double* trow = target + ((size_t)b * (gamma + 1) + (size_t)(k - 1)) * V;
             for (int v = 0; v < V; ++v) t[v] = trow[v] / tau;
             const double lse_p = logsumexp(t, V);
-            draft_logits(U + drow * V, W1, W2, V, r, x_prev, tau, z);
+            const double* hrow = arows ? arows + drow * (size_t)r : W1 + (size_t)x_prev * r;
+            draft_logits(U + drow * V, hrow, W2, V, r, tau, z);
             const double lse_q = logsumexp(z, V);
             const double p = exp(t[x] - lse_p);
             const double q = exp(z[x] - lse_q);
@@ -442,8 +535,6 @@ void oracle_compact(const int32_t* draft_tok, const int32_t* accepted, const int
 /* T_k is the grid value with the smallest ECE (the lowest grid index among  */
 /* equal values).                                                            */
 /* ------------------------------------------------------------------------ */
-static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
-
 /* Survival of prefix k (1-based) for every sample and every grid value:
  * out[n][g] = a_n(grid[g]) with the earlier temperatures T_prev[0..k-2]. */
 void oracle_sts_survival(const double* score, int N, int gamma, const double* T_prev, int k,

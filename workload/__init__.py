@@ -188,3 +188,22 @@ STS_FIT = dict(N=1 << 20, gamma=GAMMA, G=256, M=15, lo=0.25, hi=4.0, seed=0)
 
 def sts_grid(G: int, lo: float = 0.25, hi: float = 4.0) -> torch.Tensor:
     return torch.linspace(lo, hi, G, dtype=torch.float32)
+
+
+def rnn_head(w: Workload, device="cpu") -> dict:
+    """Parameters of the RNN draft head for workload w (rank r): input
+    embedding E [V,r] ~ N(0,1), W_ih and W_hh [3r,r] and the biases [3r]
+    ~ U(-1/sqrt(r), 1/sqrt(r)) (the usual GRU initialisation), s0 [r] ~
+    N(0, 0.5^2).  Matrices in bf16 (the head's weight dtype), vectors fp32."""
+    g = _gen(device, w.seed, 5)
+    r = w.r
+    a = 1.0 / math.sqrt(r)
+
+    def unif(shape):
+        return (torch.rand(shape, generator=g, device=device) * 2 - 1) * a
+
+    return dict(E=torch.randn((w.V, r), generator=g, device=device).to(torch.bfloat16).contiguous(),
+                W_ih=unif((3 * r, r)).to(torch.bfloat16).contiguous(),
+                W_hh=unif((3 * r, r)).to(torch.bfloat16).contiguous(),
+                b_ih=unif((3 * r,)).float().contiguous(), b_hh=unif((3 * r,)).float().contiguous(),
+                s0=(torch.randn((r,), generator=g, device=device) * 0.5).float().contiguous())
