@@ -161,6 +161,9 @@ def run_gpu(args):
     B, gamma, V, r = w.B, w.gamma, w.V, w.r
     req_base = rank * B        # each rank owns its own B requests (weak scaling)
     inp = workload.inputs(w, step=rank, device=dev)
+    head = args.head
+    if head == "rnn":
+        inp["rnn"] = workload.rnn_head(w, device=dev)
     buf = vm.StepBuffers(B, gamma, V, r, device=dev)
     stream = torch.cuda.Stream(device=dev)
     seed = w.seed
@@ -171,11 +174,14 @@ def run_gpu(args):
         inp["sps"] = workload.custom(w.name, B=B * world).sps_table().to(dev)
         sched = vm.GlobalSchedule(B, gamma, world, device=dev)
 
+        if head != "markov":
+            raise SystemExit("the scheduled multi-rank step runs the Markov head only")
+
         def one_step():
             vm.run_step_dp(inp, buf, sched, mode=mode, seed=seed, step=0, stream=stream)
     else:
         def one_step():
-            vm.run_step(inp, buf, mode=mode, seed=seed, step=0, req_base=req_base, stream=stream)
+            vm.run_step(inp, buf, mode=mode, seed=seed, step=0, req_base=req_base, stream=stream, head=head)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -224,14 +230,21 @@ def run_gpu(args):
     value = emitted_all / (ms_max / 1e3)
 
     # ---- dominant kernel: the draft call, timed alone on the same stream
-    draft_launches = gamma if os.environ.get("DSPARK_DRAFT_PER_POSITION") else 1
+    if head == "rnn":
+        draft_launches = gamma        # one draft launch per position (plus a GRU launch each)
+    else:
+        draft_launches = gamma if os.environ.get("DSPARK_DRAFT_PER_POSITION") else 1
     reps = max(5, min(args.steps, 1000))
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         d0.record(stream)
         for _ in range(reps):
-            vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
-                                   buf.z_tok, buf.ws, seed=seed, req_base=req_base, stream=stream)
+            if head == "rnn":
+                vm.dspark_draft_rnn(inp["U"], inp["rnn"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
+                                    buf.z_tok, buf.state, buf.ws, seed=seed, req_base=req_base, stream=stream)
+            else:
+                vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
+                                       buf.z_tok, buf.ws, seed=seed, req_base=req_base, stream=stream)
         d1.record(stream)
     stream.synchronize()
     draft_launch_ms = d0.elapsed_time(d1) / (reps * draft_launches)
@@ -254,14 +267,14 @@ def run_gpu(args):
     e2e_steps = max(3, min(args.steps, 20))
     pipe = vm.HostPipeline(inp, buf, stream)
     for _ in range(2):
-        pipe.step(host, host_out, mode=mode, seed=seed)
+        pipe.step(host, host_out, mode=mode, seed=seed, head=head)
     torch.cuda.synchronize()
     _barrier(dist)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     pipe.copy_stream.wait_event(f0)
     for _ in range(e2e_steps):
-        h2d, d2h = pipe.step(host, host_out, mode=mode, seed=seed)
+        h2d, d2h = pipe.step(host, host_out, mode=mode, seed=seed, head=head)
     f1.record(stream)
     stream.synchronize()
     e2e_ms = _max_over_ranks(dist, f0.elapsed_time(f1) / e2e_steps, dev)
@@ -272,27 +285,30 @@ def run_gpu(args):
         raise SystemExit(f"device status {st} bits {bits}")
 
     # draft, confidence, schedule, verify stream, accept walk, residual draw, compaction
-    launches_per_step = draft_launches + 6
+    launches_per_step = draft_launches * (2 if head == "rnn" else 1) + 6
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, mode, budget_s=args.cpu_budget, dev_inp=inp, min_seconds=10.0)
+        cpu = cpu_baseline(w, mode, budget_s=args.cpu_budget, dev_inp=inp, min_seconds=10.0, head=head)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 weights, f32 logits, f32 accumulate", "data": "synthetic",
             "config": {"workload": f"{w.name}: B={B} V={V} r={r} gamma={gamma} d={d_of(w)} "
-                                   f"verify={'full prefix (scheduler off)' if mode == 0 else 'scheduled'}",
+                                   f"verify={'full prefix (scheduler off)' if mode == 0 else 'scheduled'}"
+                                   + (", RNN draft head" if head == "rnn" else ""),
                        "global_batch": B * world, "seq_len": gamma, "parallelism": f"dp{world} over requests",
                        "l2": "inputs 1.13 GB per step > 129 MB L2; no flush", "graph": "CUDA graph replay"},
             "emitted_tokens_per_step": emitted_all, "drafted_tokens_per_step": B * gamma * world,
             "step_formula_bytes": formula_bytes, "step_formula_gbs": step_gbs,
             "step_formula_frac": step_gbs / peak,
-            "roofline": {"kernel": "rows_kernel<draft> (dspark_draft_markov, %d position(s) per launch)"
-                                   % (gamma // draft_launches),
+            "roofline": {"kernel": ("rows_kernel<draft> (dspark_draft_markov, %d position(s) per launch)"
+                                    % (gamma // draft_launches)) if head == "markov" else
+                                   "gru_kernel + rows_kernel<draft> per position (dspark_draft_rnn); "
+                                   "launch_ms = the two launches of one position",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": _draft_traffic(w.name) if draft_launches == 1 else None,
+                         "traffic": _draft_traffic(w.name) if draft_launches == 1 and head == "markov" else None,
                          "algorithmic_bytes_per_launch": draft_bytes, "launch_ms": draft_launch_ms},
             "e2e": {"value": e2e_emitted / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -593,7 +609,7 @@ def _cpu_inputs(w, dev_inp=None):
     return _CPU_INPUTS[w.name]
 
 
-def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None, min_seconds=0.0):
+def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None, min_seconds=0.0, head="markov"):
     """The float64 oracle, as it stands, on a bounded sample of the workload:
     the first S requests of the batch through the whole step (draft,
     confidence, schedule, verify, compaction), S sized to a ~budget_s run,
@@ -602,6 +618,9 @@ def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None, min_seconds=0.0):
 
     inp = _cpu_inputs(w, dev_inp)
     W1, W2 = inp["W1_64"], inp["W2_64"]
+    if head == "rnn" and "rnn64" not in inp:
+        src = dev_inp["rnn"] if dev_inp is not None and "rnn" in dev_inp else workload.rnn_head(w)
+        inp["rnn64"] = {k: v.double().cpu().numpy() for k, v in src.items()}
     threads = oracle.num_threads()
     t = time.perf_counter()
     _ = oracle.draft_markov(inp["U"][:1], W1, W2, inp["anchor"][:1], seed=w.seed)
@@ -613,21 +632,28 @@ def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None, min_seconds=0.0):
     reps, tokens, dt = 0, 0, 0.0
     while reps == 0 or dt < min_seconds:
         t = time.perf_counter()
-        tokens += _oracle_sample_step(w, mode, inp, sub, W1, W2, S)
+        tokens += _oracle_sample_step(w, mode, inp, sub, W1, W2, S, head)
         dt += time.perf_counter() - t
         reps += 1
     return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{S} of {w.B} requests of {w.name}, whole step (draft+confidence+schedule+verify+compact), "
-                      f"{reps} run(s), {dt:.1f} s", "seconds": dt / reps}
+            "sample": f"{S} of {w.B} requests of {w.name}, whole step (draft+confidence+schedule+verify+compact"
+                      f"{', RNN head' if head == 'rnn' else ''}), {reps} run(s), {dt:.1f} s", "seconds": dt / reps}
 
 
-def _oracle_sample_step(w, mode, inp, sub, W1, W2, S):
+def _oracle_sample_step(w, mode, inp, sub, W1, W2, S, head="markov"):
     """One oracle step over the sample; returns the tokens it emits."""
     import numpy as np
 
     import oracle
 
-    d = oracle.draft_markov(sub["U"], W1, W2, sub["anchor"], seed=w.seed)
+    arows = None
+    if head == "rnn":
+        p = inp["rnn64"]
+        d = oracle.draft_rnn(sub["U"], p["E"], p["W_ih"], p["W_hh"], p["b_ih"], p["b_hh"], p["s0"], W2,
+                             sub["anchor"], seed=w.seed)
+        arows = d["arows"]
+    else:
+        d = oracle.draft_markov(sub["U"], W1, W2, sub["anchor"], seed=w.seed)
     # the confidence head reads emb rows of the anchors and drafts only
     prev = np.concatenate([sub["anchor"].numpy()[:, None], d["tok"][:, :-1]], axis=1)
     ids, remap = np.unique(prev, return_inverse=True)
@@ -641,7 +667,8 @@ def _oracle_sample_step(w, mode, inp, sub, W1, W2, S):
         K = np.full(S, w.gamma, np.int32)
     else:
         K = oracle.schedule(c["log_surv"], inp["sps"], mode)["K"]
-    v = oracle.verify(sub["target"], sub["U"], W1, W2, sub["anchor"], d["tok"], K, seed=w.seed)
+    v = oracle.verify(sub["target"], sub["U"], None if arows is not None else W1, W2, sub["anchor"], d["tok"], K,
+                      seed=w.seed, arows=arows)
     o = oracle.compact(d["tok"], v["accepted"], v["final_tok"])
     return int(o["out_off"][-1])
 
@@ -687,6 +714,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chain", action="store_true",
                     help="time the workload's chained steps (b512: 16 steps, async scheduler) instead of one step")
+    ap.add_argument("--head", default="markov", choices=["markov", "rnn"],
+                    help="draft head: the Markov head (default) or the RNN head")
     ap.add_argument("--sts", action="store_true",
                     help="time the STS temperature fit (2^20 validation blocks, 256 temperatures)")
     ap.add_argument("--sts-blocks", type=int, default=None,

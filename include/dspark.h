@@ -191,6 +191,55 @@ dspark_status dspark_verify(
     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The draft loop with the RNN head [P2 §RNN Head：长程依赖], [P4 §三] in place
+ * of the Markov head.  A GRU state carries every token of the block so far:
+ *     s_k = GRU(s_{k-1}, E[x~_{k-1}])   (s_0 learned, x~_0 = anchor[b])
+ *     z_k = (U[b,k-1,:] + bf16(s_k) . W2) / tau,  x~_k drawn as in
+ *     dspark_draft_markov (same random stream, same outputs).
+ * The GRU cell is the standard one (the pages print no formula), gate rows
+ * stacked (r, z, n):
+ *     r = sigma(W_ir x + b_ir + W_hr h + b_hr), z = sigma(W_iz x + b_iz + W_hz h + b_hz),
+ *     n = tanh(W_in x + b_in + r * (W_hn h + b_hn)), h' = (1 - z) n + z h.
+ * Inputs : U [B,gamma,V] fp32, E [V,r] bf16 (input embedding; W1 may be
+ *          passed), W_ih [3r,r] and W_hh [3r,r] bf16, b_ih [3r], b_hh [3r],
+ *          s0 [r] fp32, W2 [r,V] bf16 (W_t must be DSPARK_BF16), anchor [B].
+ * Outputs: draft_tok, lse_q, z_tok as dspark_draft_markov; state
+ *          [gamma,B,r] fp32 receives s_1..s_gamma (dspark_verify_rnn reads it).
+ * Limits : those of dspark_draft_markov, plus r % 64 == 0, r <= 256, fp32 U
+ *          (else DSPARK_ERR_UNSUPPORTED).  2*gamma launches on stream (a GRU
+ *          step and a draft step per position).
+ */
+dspark_status dspark_draft_rnn(
+    const void* U, dspark_dtype U_t,
+    const void* E, const void* W_ih, const void* W_hh,
+    const float* b_ih, const float* b_hh, const float* s0,
+    const void* W2, dspark_dtype W_t,
+    const int32_t* anchor,
+    int B, int gamma, int V, int r, int req_base, float tau,
+    uint64_t seed, uint64_t step,
+    int32_t* draft_tok, float* lse_q, float* z_tok, float* state,
+    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dspark_verify for drafts of the RNN head: identical, except that the
+ * draft distribution of a rejected position k is rebuilt from
+ * bf16(state[k-1]) . W2 (state as written by dspark_draft_rnn) instead of
+ * W1[x~_{k-1}] . W2.  Same limits as dspark_draft_rnn.
+ */
+dspark_status dspark_verify_rnn(
+    const void* target, dspark_dtype target_t,
+    const void* U, dspark_dtype U_t,
+    const float* state, const void* W2, dspark_dtype W_t,
+    const int32_t* anchor, const int32_t* draft_tok,
+    const float* lse_q, const float* z_tok, const int32_t* K,
+    int B, int gamma, int V, int r, int req_base, float tau,
+    uint64_t seed, uint64_t step,
+    int32_t* accepted, int32_t* out_tok, int32_t* out_req, int32_t* out_pos,
+    int32_t* out_off, int32_t* next_anchor,
+    float* p_tok, uint32_t* near_ties,
+    void* ws, size_t ws_bytes, void* stream);
+
+/*
  * The draft loop of dspark_draft_markov for callers that cannot allocate
  * device memory -- for example code inside a framework that owns all device
  * allocations, or a latency-critical loop that must not enter an allocator

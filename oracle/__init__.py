@@ -87,6 +87,9 @@ def _load():
             lib.oracle_gru_cell.restype = None
             lib.oracle_bf16_round.argtypes = [C.c_double]
             lib.oracle_bf16_round.restype = C.c_double
+            lib.oracle_rnn_states.argtypes = [f64p, f64p, f64p, f64p, f64p, f64p, i32p, i32p, C.c_int, C.c_int,
+                                              C.c_int, C.c_int, f64p, f64p]
+            lib.oracle_rnn_states.restype = C.c_int
             lib.oracle_draft_rnn.argtypes = [
                 f64p, f64p, f64p, f64p, f64p, f64p, f64p, f64p, i32p, i32p, C.c_int, C.c_int, C.c_int,
                 C.c_int, C.c_double, C.c_uint64, C.c_uint64, i32p, f64p, f64p, f64p, f64p, f64p]
@@ -187,6 +190,19 @@ def gru_cell(x, h, W_ih, W_hh, b_ih, b_hh):
 
 def bf16_round(x) -> float:
     return float(_load().oracle_bf16_round(float(x)))
+
+
+def rnn_states(E, W_ih, W_hh, b_ih, b_hh, s0, anchor, tok):
+    """The RNN head's states along the tokens tok [nb,gamma] (oracle_rnn_states):
+    returns (states, arows), both [nb,gamma,r], arows rounded to bfloat16."""
+    E = _f64(E); W_ih = _f64(W_ih); W_hh = _f64(W_hh); b_ih = _f64(b_ih); b_hh = _f64(b_hh); s0 = _f64(s0)
+    anchor = _i32(anchor); tok = _i32(tok)
+    nb, gamma = tok.shape
+    V, r = E.shape
+    states = np.zeros((nb, gamma, r)); arows = np.zeros((nb, gamma, r))
+    if _load().oracle_rnn_states(E, W_ih, W_hh, b_ih, b_hh, s0, anchor, tok, nb, gamma, V, r, states, arows):
+        raise ValueError("oracle_rnn_states: token out of range")
+    return states, arows
 
 
 def draft_rnn(U, E, W_ih, W_hh, b_ih, b_hh, s0, W2, anchor, *, seed, step=0, tau=1.0, req=None):

@@ -361,6 +361,34 @@ double oracle_bf16_round(double x)
     return rint(x / q) * q;
 }
 
+/* The RNN head's states along given tokens (the drafts of another run):
+ * states[b][k-1] = s_k = GRU(s_{k-1}, E[tok_{k-1}]) with tok_0 = anchor[b],
+ * arows = the states rounded to bfloat16.  Returns -1 on a token outside [0, V). */
+int oracle_rnn_states(const double* E, const double* W_ih, const double* W_hh, const double* b_ih,
+                      const double* b_hh, const double* s0, const int32_t* anchor, const int32_t* tok,
+                      int nb, int gamma, int V, int r, double* states, double* arows)
+{
+    double* h = (double*)malloc(sizeof(double) * (size_t)r);
+    double* hn = (double*)malloc(sizeof(double) * (size_t)r);
+    int bad = (!h || !hn);
+    for (int b = 0; b < nb && !bad; ++b) {
+        memcpy(h, s0, sizeof(double) * (size_t)r);
+        for (int k = 1; k <= gamma; ++k) {
+            const size_t row = (size_t)b * gamma + (size_t)(k - 1);
+            const int x = (k == 1) ? anchor[b] : tok[row - 1];
+            if (x < 0 || x >= V) { bad = 1; break; }
+            oracle_gru_cell(E + (size_t)x * r, h, W_ih, W_hh, b_ih, b_hh, r, r, hn);
+            memcpy(h, hn, sizeof(double) * (size_t)r);
+            for (int i = 0; i < r; ++i) {
+                states[row * r + i] = h[i];
+                arows[row * r + i] = oracle_bf16_round(h[i]);
+            }
+        }
+    }
+    free(h); free(hn);
+    return bad ? -1 : 0;
+}
+
 int oracle_draft_rnn(const double* U, const double* E, const double* W_ih, const double* W_hh,
                      const double* b_ih, const double* b_hh, const double* s0, const double* W2,
                      const int32_t* anchor, const int32_t* req,

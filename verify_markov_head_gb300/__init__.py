@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
+    "dspark_schedule", "dspark_verify", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
@@ -57,6 +57,13 @@ _lib.dspark_verify.restype = _i
 _lib.dspark_draft_markov_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
                                              _vp, _vp, _vp, _vp, _vp]
 _lib.dspark_draft_markov_noalloc.restype = _i
+_lib.dspark_draft_rnn.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f,
+                                  _u64, _u64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_draft_rnn.restype = _i
+_lib.dspark_verify_rnn.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
+                                   _i, _i, _i, _i, _i, _f, _u64, _u64,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_verify_rnn.restype = _i
 _lib.dspark_sts_workspace_bytes.argtypes = [_i, _i, _i]
 _lib.dspark_sts_workspace_bytes.restype = _sz
 _lib.dspark_sts_fit.argtypes = [_vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]
@@ -225,6 +232,44 @@ def dspark_verify(target, U, W1, W2, anchor, draft_tok, lse_q, z_tok, K, accepte
         _p(p_tok), _p(near_ties), ws.ptr(), ws.nbytes(), _stream(stream)))
 
 
+def dspark_draft_rnn(U, rnn, W2, anchor, draft_tok, lse_q, z_tok, state, ws: Workspace, *,
+                     tau=1.0, seed=0, step=0, req_base=0, stream=None):
+    """The draft loop with the RNN head.  rnn = dict(E [V,r], W_ih [3r,r],
+    W_hh [3r,r] (bf16), b_ih [3r], b_hh [3r], s0 [r] (fp32)); state
+    [gamma,B,r] fp32 receives the states s_1..s_gamma."""
+    B, gamma, V = U.shape
+    r = W2.shape[0]
+    E, W_ih, W_hh = rnn["E"], rnn["W_ih"], rnn["W_hh"]
+    if tuple(E.shape) != (V, r) or tuple(W_ih.shape) != (3 * r, r) or tuple(W_hh.shape) != (3 * r, r):
+        raise ValueError("E [V,r], W_ih [3r,r] and W_hh [3r,r] expected")
+    if not (E.dtype == W_ih.dtype == W_hh.dtype == W2.dtype == torch.bfloat16):
+        raise TypeError("the RNN head's matrices and W2 must be bfloat16")
+    if rnn["b_ih"].numel() != 3 * r or rnn["b_hh"].numel() != 3 * r or rnn["s0"].numel() != r:
+        raise ValueError("b_ih, b_hh [3r] and s0 [r] expected")
+    if tuple(state.shape) != (gamma, B, r) or state.dtype != torch.float32:
+        raise ValueError("state must be float32 [gamma, B, r]")
+    _check("dspark_draft_rnn", _lib.dspark_draft_rnn(
+        _p(U), _dt(U), _p(E), _p(W_ih), _p(W_hh), _p(rnn["b_ih"]), _p(rnn["b_hh"]), _p(rnn["s0"]), _p(W2),
+        _dt(W2), _p(anchor), B, gamma, V, r, req_base, float(tau), int(seed), int(step), _p(draft_tok),
+        _p(lse_q), _p(z_tok), _p(state), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def dspark_verify_rnn(target, U, state, W2, anchor, draft_tok, lse_q, z_tok, K, accepted, out_tok, out_req,
+                      out_pos, out_off, next_anchor, ws: Workspace, *, tau=1.0, seed=0, step=0, req_base=0,
+                      p_tok=None, near_ties=None, stream=None):
+    B, gamma, V = U.shape
+    r = W2.shape[0]
+    if tuple(target.shape) != (B, gamma + 1, V) or tuple(state.shape) != (gamma, B, r):
+        raise ValueError("target must be [B, gamma+1, V] and state [gamma, B, r]")
+    if out_tok.numel() < B * (gamma + 1) or out_off.numel() != B + 1:
+        raise ValueError("output buffers too small")
+    _check("dspark_verify_rnn", _lib.dspark_verify_rnn(
+        _p(target), _dt(target), _p(U), _dt(U), _p(state), _p(W2), _dt(W2), _p(anchor), _p(draft_tok),
+        _p(lse_q), _p(z_tok), _p(K), B, gamma, V, r, req_base, float(tau), int(seed), int(step),
+        _p(accepted), _p(out_tok), _p(out_req), _p(out_pos), _p(out_off), _p(next_anchor),
+        _p(p_tok), _p(near_ties), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
 def dspark_draft_markov_noalloc(U, W1, W2, anchor, draft_tok, lse_q, z_tok, *, tau=1.0, seed=0, step=0,
                                 req_base=0, logits_out=None, stream=None):
     """dspark_draft_markov without a workspace, for callers that cannot
@@ -266,23 +311,37 @@ class StepBuffers:
         self.next_anchor = torch.empty((B,), **i32)
         self.p_tok = torch.empty((B, gamma), **f32)
         self.near_ties = torch.zeros((4,), dtype=torch.int32, device=device)
+        self.state = torch.empty((gamma, B, r), **f32)    # RNN head states s_1..s_gamma
         self.ws = Workspace(B, gamma, V, r, device)
 
 
 def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_base=0, log_surv_hist=None,
-         stream=None, p_tok=False):
+         stream=None, p_tok=False, head="markov"):
     """One whole draft + verify step (a1-a8) on device-resident inputs: the
-    four ABI calls in order, all on `stream`."""
-    dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
-                        buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, stream=stream)
+    four ABI calls in order, all on `stream`.  head="rnn" drafts with the RNN
+    head (parameters in inp["rnn"]) and verifies against its states."""
+    if head == "rnn":
+        dspark_draft_rnn(inp["U"], inp["rnn"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
+                         buf.state, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, stream=stream)
+    elif head == "markov":
+        dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
+                            buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, stream=stream)
+    else:
+        raise ValueError(f"unknown head {head!r}")
     dspark_confidence_sts(inp["h"], inp["emb"], inp["anchor"], buf.draft_tok, inp["w_c"], inp["b_c"], inp["T"],
                           buf.conf_cal, buf.log_surv, buf.ws, stream=stream)
     dspark_schedule(buf.log_surv, inp["sps"], mode, buf.K, buf.n_total, buf.theta, buf.ws,
                     log_surv_hist=log_surv_hist, stream=stream)
-    dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
-                  buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
-                  buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
-                  p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
+    if head == "rnn":
+        dspark_verify_rnn(inp["target"], inp["U"], buf.state, inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
+                          buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
+                          buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
+                          p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
+    else:
+        dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
+                      buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
+                      buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
+                      p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
 
 
 class GlobalSchedule:
@@ -397,7 +456,7 @@ class HostPipeline:
         self.compute_stream.wait_stream(cur)
         self.copy_stream.wait_stream(cur)
 
-    def step(self, host_inp: dict, host_out: dict, *, mode, seed, step=0, tau=1.0):
+    def step(self, host_inp: dict, host_out: dict, *, mode, seed, step=0, tau=1.0, head="markov"):
         """Enqueue one step; returns (h2d_bytes, d2h_bytes)."""
         i = self.next
         slot = self.slots[i]
@@ -412,7 +471,8 @@ class HostPipeline:
         self.compute_stream.wait_event(self.copied[i])
         d2h = 0
         with torch.cuda.stream(self.compute_stream):
-            run_step(slot, self.buf, mode=mode, seed=seed, step=step, tau=tau, stream=self.compute_stream)
+            run_step(slot, self.buf, mode=mode, seed=seed, step=step, tau=tau, stream=self.compute_stream,
+                     head=head)
             for name in ("out_tok", "out_off", "next_anchor"):
                 src = getattr(self.buf, name)
                 host_out[name].copy_(src, non_blocking=True)

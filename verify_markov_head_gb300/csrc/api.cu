@@ -217,23 +217,25 @@ dspark_status dspark_schedule(const float* log_surv, const float* log_surv_hist,
     return launch_status(launch_schedule(p, static_cast<cudaStream_t>(stream)));
 }
 
-dspark_status dspark_verify(const void* target, dspark_dtype target_t, const void* U, dspark_dtype U_t,
-                            const void* W1, const void* W2, dspark_dtype W_t, const int32_t* anchor,
-                            const int32_t* draft_tok, const float* lse_q, const float* z_tok,
-                            const int32_t* K, int B, int gamma, int V, int r, int req_base, float tau,
-                            uint64_t seed, uint64_t step, int32_t* accepted, int32_t* out_tok,
-                            int32_t* out_req, int32_t* out_pos, int32_t* out_off, int32_t* next_anchor,
-                            float* p_tok, uint32_t* near_ties, void* ws, size_t ws_bytes, void* stream) {
+static dspark_status verify_impl(const void* target, dspark_dtype target_t, const void* U, dspark_dtype U_t,
+                                 const void* W1, const float* state, const void* W2, dspark_dtype W_t,
+                                 const int32_t* anchor, const int32_t* draft_tok, const float* lse_q,
+                                 const float* z_tok, const int32_t* K, int B, int gamma, int V, int r,
+                                 int req_base, float tau, uint64_t seed, uint64_t step, int32_t* accepted,
+                                 int32_t* out_tok, int32_t* out_req, int32_t* out_pos, int32_t* out_off,
+                                 int32_t* next_anchor, float* p_tok, uint32_t* near_ties, void* ws,
+                                 size_t ws_bytes, void* stream) {
     if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
     if ((target_t != DSPARK_F32 && target_t != DSPARK_BF16) || (U_t != DSPARK_F32 && U_t != DSPARK_BF16) ||
         (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
         return DSPARK_ERR_UNSUPPORTED;
-    const void* need[] = {target, U, W1, W2, anchor, draft_tok, lse_q, z_tok, K, accepted,
+    const void* rows = state ? static_cast<const void*>(state) : W1;
+    const void* need[] = {target, U, rows, W2, anchor, draft_tok, lse_q, z_tok, K, accepted,
                           out_tok, out_req, out_pos, out_off, next_anchor, ws};
     for (const void* q : need)
         if (!is_device_ptr(q)) return DSPARK_ERR_INVALID;
     if ((p_tok && !is_device_ptr(p_tok)) || (near_ties && !is_device_ptr(near_ties))) return DSPARK_ERR_INVALID;
-    if (!aligned(target, 16) || !aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(ws, 256))
+    if (!aligned(target, 16) || !aligned(U, 16) || !aligned(rows, 16) || !aligned(W2, 16) || !aligned(ws, 256))
         return DSPARK_ERR_INVALID;
     if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;
     if ((double)(req_base + (double)B) * (gamma + 1) >= 4294967295.0) return DSPARK_ERR_INVALID;
@@ -247,7 +249,72 @@ dspark_status dspark_verify(const void* target, dspark_dtype target_t, const voi
     p.accepted = accepted; p.out_tok = out_tok; p.out_req = out_req; p.out_pos = out_pos;
     p.out_off = out_off; p.next_anchor = next_anchor; p.p_tok = p_tok; p.near_ties = near_ties;
     p.ws = ws_ptrs(ws, B, gamma, V);
+    p.state = state;
+    if (state && !resid_rows_supported(p)) return DSPARK_ERR_UNSUPPORTED;
     return launch_status(launch_verify(p, static_cast<cudaStream_t>(stream)));
+}
+
+dspark_status dspark_verify(const void* target, dspark_dtype target_t, const void* U, dspark_dtype U_t,
+                            const void* W1, const void* W2, dspark_dtype W_t, const int32_t* anchor,
+                            const int32_t* draft_tok, const float* lse_q, const float* z_tok,
+                            const int32_t* K, int B, int gamma, int V, int r, int req_base, float tau,
+                            uint64_t seed, uint64_t step, int32_t* accepted, int32_t* out_tok,
+                            int32_t* out_req, int32_t* out_pos, int32_t* out_off, int32_t* next_anchor,
+                            float* p_tok, uint32_t* near_ties, void* ws, size_t ws_bytes, void* stream) {
+    return verify_impl(target, target_t, U, U_t, W1, nullptr, W2, W_t, anchor, draft_tok, lse_q, z_tok, K, B,
+                       gamma, V, r, req_base, tau, seed, step, accepted, out_tok, out_req, out_pos, out_off,
+                       next_anchor, p_tok, near_ties, ws, ws_bytes, stream);
+}
+
+dspark_status dspark_verify_rnn(const void* target, dspark_dtype target_t, const void* U, dspark_dtype U_t,
+                                const float* state, const void* W2, dspark_dtype W_t, const int32_t* anchor,
+                                const int32_t* draft_tok, const float* lse_q, const float* z_tok,
+                                const int32_t* K, int B, int gamma, int V, int r, int req_base, float tau,
+                                uint64_t seed, uint64_t step, int32_t* accepted, int32_t* out_tok,
+                                int32_t* out_req, int32_t* out_pos, int32_t* out_off, int32_t* next_anchor,
+                                float* p_tok, uint32_t* near_ties, void* ws, size_t ws_bytes, void* stream) {
+    if (!state) return DSPARK_ERR_INVALID;
+    return verify_impl(target, target_t, U, U_t, nullptr, state, W2, W_t, anchor, draft_tok, lse_q, z_tok, K, B,
+                       gamma, V, r, req_base, tau, seed, step, accepted, out_tok, out_req, out_pos, out_off,
+                       next_anchor, p_tok, near_ties, ws, ws_bytes, stream);
+}
+
+dspark_status dspark_draft_rnn(const void* U, dspark_dtype U_t, const void* E, const void* W_ih, const void* W_hh,
+                               const float* b_ih, const float* b_hh, const float* s0, const void* W2,
+                               dspark_dtype W_t, const int32_t* anchor, int B, int gamma, int V, int r,
+                               int req_base, float tau, uint64_t seed, uint64_t step, int32_t* draft_tok,
+                               float* lse_q, float* z_tok, float* state, void* ws, size_t ws_bytes,
+                               void* stream) {
+    if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
+    if ((U_t != DSPARK_F32 && U_t != DSPARK_BF16) || (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
+        return DSPARK_ERR_UNSUPPORTED;
+    const void* need[] = {U, E, W_ih, W_hh, b_ih, b_hh, s0, W2, anchor, draft_tok, lse_q, z_tok, state, ws};
+    for (const void* q : need)
+        if (!is_device_ptr(q)) return DSPARK_ERR_INVALID;
+    if (!aligned(U, 16) || !aligned(E, 16) || !aligned(W_ih, 16) || !aligned(W_hh, 16) || !aligned(W2, 16) ||
+        !aligned(state, 16) || !aligned(ws, 256))
+        return DSPARK_ERR_INVALID;
+    if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;
+    if ((double)(req_base + (double)B) * (gamma + 1) >= 4294967295.0) return DSPARK_ERR_INVALID;
+    DraftParams p;
+    p.U = U; p.U_bf16 = (U_t == DSPARK_BF16);
+    p.W1 = nullptr; p.W2 = W2; p.W_bf16 = (W_t == DSPARK_BF16);
+    p.anchor = anchor;
+    p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.req_base = req_base;
+    p.inv_tau = 1.f / tau;
+    p.seed = seed; p.step = step;
+    p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.logits_out = nullptr;
+    p.ws = ws_ptrs(ws, B, gamma, V);
+    p.state = state;
+    if (!draft_rows_supported(p)) return DSPARK_ERR_UNSUPPORTED;   // bf16 weights, fp32 U, r % 64 == 0, r <= 256
+    GruParams g;
+    g.E = static_cast<const uint16_t*>(E);
+    g.W_ih = static_cast<const uint16_t*>(W_ih); g.W_hh = static_cast<const uint16_t*>(W_hh);
+    g.b_ih = b_ih; g.b_hh = b_hh; g.s0 = s0;
+    g.anchor = anchor; g.draft_tok = draft_tok; g.state = state;
+    g.B = B; g.gamma = gamma; g.V = V; g.r = r;
+    g.status = p.ws.status;
+    return launch_status(launch_draft_rnn(p, g, static_cast<cudaStream_t>(stream)));
 }
 
 dspark_status dspark_gumbel_stream(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row, int n,

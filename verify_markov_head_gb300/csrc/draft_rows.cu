@@ -48,6 +48,7 @@
 // of the target logits (the rejected rows differ per request, so no common
 // TMA box exists): D is h.W2 alone and no U slice ring is used.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -151,11 +152,24 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target, con
 // lanes' requests into the A of their tile, and zeros into the other A
 // operands when `zeros` is set (once per launch: later positions rewrite the
 // h parts only).
+__device__ __forceinline__ void store_a_slice(uint32_t tmem_base, int NC, int RF, int q, int cb, int lane,
+                                              bool zeros, uint32_t (&v)[32]) {
+    const int row = 32 * q + lane, ti = row / NC;
+    const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * cb);
+    // the 32 lanes of a warp belong to one tile (NC >= 32)
+    ptx::tmem_st32(taddr + (uint32_t)(128 * ti), v);
+    if (zeros) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) v[u] = 0u;
+        for (int i = 0; i < RF; ++i)
+            if (i != ti) ptx::tmem_st32(taddr + (uint32_t)(128 * i), v);
+    }
+}
+
 __device__ __forceinline__ void stage_a_tmem(uint32_t tmem_base, const uint16_t* W1, const int* s_tok, int NC,
                                              int RF, int r, int V, int q, int cb, int lane, bool zeros) {
     if (64 * cb >= r) return;                       // ranks past r are never read
-    const int row = 32 * q + lane, ti = row / NC, n = row % NC;
-    const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * cb);
+    const int n = (32 * q + lane) % NC;
     uint32_t v[32];
     const int x = s_tok[n];
     if (x >= 0 && x < V) {                          // rows outside [0, V) stay zero
@@ -169,14 +183,35 @@ __device__ __forceinline__ void stage_a_tmem(uint32_t tmem_base, const uint16_t*
 #pragma unroll
         for (int u = 0; u < 32; ++u) v[u] = 0u;
     }
-    // the 32 lanes of a warp belong to one tile (NC >= 32)
-    ptx::tmem_st32(taddr + (uint32_t)(128 * ti), v);
-    if (zeros) {
+    store_a_slice(tmem_base, NC, RF, q, cb, lane, zeros, v);
+}
+
+// The same A operands for the RNN head: h is the request's fp32 state row
+// st_base[pos][n] (pos < 0: the row's own position s_row[n]) rounded to
+// bf16; rows whose token is invalid stay zero.
+__device__ __forceinline__ void stage_a_state(uint32_t tmem_base, const float* st_base, size_t pos_stride,
+                                              int pos, const int* s_row, const int* s_tok, int NC, int RF, int r,
+                                              int V, int q, int cb, int lane, bool zeros) {
+    if (64 * cb >= r) return;
+    const int n = (32 * q + lane) % NC;
+    uint32_t v[32];
+    const int x = s_tok[n];
+    if (x >= 0 && x < V) {
+        const int ps = pos >= 0 ? pos : s_row[n];
+        const float4* src =
+            reinterpret_cast<const float4*>(st_base + (size_t)ps * pos_stride + (size_t)n * r + (size_t)(64 * cb));
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const float4 f = src[u];
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(f.x, f.y), hi = __floats2bfloat162_rn(f.z, f.w);
+            v[2 * u] = *reinterpret_cast<const uint32_t*>(&lo);
+            v[2 * u + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        }
+    } else {
 #pragma unroll
         for (int u = 0; u < 32; ++u) v[u] = 0u;
-        for (int i = 0; i < RF; ++i)
-            if (i != ti) ptx::tmem_st32(taddr + (uint32_t)(128 * i), v);
     }
+    store_a_slice(tmem_base, NC, RF, q, cb, lane, zeros, v);
 }
 
 // Winner key of a partial draw: larger best first, then the lower index, as
@@ -281,6 +316,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     const int nb = min(NC, p.B - b_base);
     const int V = p.V, gamma = p.gamma, r = p.r;
     const uint16_t* W1 = static_cast<const uint16_t*>(p.W1);
+    const float* st_base = p.state ? p.state + (size_t)b_base * p.r : nullptr;   // RNN head rows of this chunk
     const uint32_t nctas = gridDim.x * gridDim.y;
 
     if (tid == 0) {
@@ -319,7 +355,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (warp < kEpiWarps) {                        // the A operands of the first position
-        stage_a_tmem(tmem_base, W1, s_tok, NC, RF, r, V, warp & 3, warp >> 2, lane, true);
+        if (st_base)
+            stage_a_state(tmem_base, st_base, (size_t)p.B * r, kResid ? -1 : k_first - 1, s_row, s_tok, NC, RF, r,
+                          V, warp & 3, warp >> 2, lane, true);
+        else
+            stage_a_tmem(tmem_base, W1, s_tok, NC, RF, r, V, warp & 3, warp >> 2, lane, true);
         ptx::tmem_wait_st();
     }
     ptx::tc_fence_before();

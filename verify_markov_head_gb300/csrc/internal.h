@@ -61,6 +61,22 @@ struct DraftParams {
     uint64_t seed, step;
     int32_t* draft_tok; float* lse_q; float* z_tok; float* logits_out;
     WsPtrs ws;
+    // RNN head: the bias of position k is formed from state[k-1][b] ([gamma][B][r]
+    // fp32, rounded to bf16 when staged) instead of W1[x~_{k-1}]
+    const float* state = nullptr;
+};
+
+// One GRU step of the RNN head for every request: state[k-1] = GRU(state[k-2]
+// (s0 for k = 1), E[x~_{k-1}]).
+struct GruParams {
+    const uint16_t* E;                       // [V][r] bf16 input embedding
+    const uint16_t* W_ih; const uint16_t* W_hh;   // [3r][r] bf16, gate rows (r, z, n)
+    const float* b_ih; const float* b_hh;    // [3r]
+    const float* s0;                         // [r] learned initial state
+    const int32_t* anchor; const int32_t* draft_tok;
+    float* state;                            // [gamma][B][r]
+    int B, gamma, V, r;
+    uint32_t* status;
 };
 
 struct ConfParams {
@@ -95,6 +111,7 @@ struct VerifyParams {
     int32_t* out_off; int32_t* next_anchor;
     float* p_tok; uint32_t* near_ties;
     WsPtrs ws;
+    const float* state = nullptr;   // RNN head bias rows (see DraftParams)
 };
 
 struct StsFitParams {
@@ -128,6 +145,7 @@ inline DraftParams draft_view(const VerifyParams& v) {
     p.inv_tau = v.inv_tau; p.seed = v.seed; p.step = v.step;
     p.draft_tok = const_cast<int32_t*>(v.draft_tok); p.lse_q = nullptr; p.z_tok = nullptr; p.logits_out = nullptr;
     p.ws = v.ws;
+    p.state = v.state;
     return p;
 }
 cudaError_t launch_gumbel_stream(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row, int n, float* g,
@@ -136,5 +154,7 @@ cudaError_t launch_confidence(const ConfParams& p, cudaStream_t s);
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
 cudaError_t launch_sts_fit(const StsFitParams& p, cudaStream_t s);
+cudaError_t launch_gru(const GruParams& g, int k, cudaStream_t s);
+cudaError_t launch_draft_rnn(const DraftParams& p, const GruParams& g, cudaStream_t s);
 
 }  // namespace dspark

@@ -560,7 +560,8 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     gx = gx > p.ws.parts ? p.ws.parts : gx;
     const size_t smem = sizeof(float) * ((size_t)kBC * p.r + (size_t)kBC * (kTV + 4));
     const dim3 g2(gx, nchunks);
-    if (resid_rows_supported(p) && !getenv("DSPARK_RESID_SIMT")) {
+    if (p.state && !resid_rows_supported(p)) return cudaErrorNotSupported;   // RNN rows: tensor-core path only
+    if (p.state || (resid_rows_supported(p) && !getenv("DSPARK_RESID_SIMT"))) {
         const cudaError_t e = launch_resid_rows(p, s);
         if (e != cudaSuccess) return e;
         verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
