@@ -33,7 +33,7 @@ WsLayout ws_layout(int B, int gamma, int V) {
     const size_t nchunks = ((size_t)B + kChunk - 1) / kChunk;
     L.status = o;      o = align256(o + 16);
     L.tickets = o;     o = align256(o + sizeof(uint32_t) * 2 * nchunks);
-    L.gbar = o;        o = align256(o + sizeof(uint32_t) * (kGridBarrierSlots + 1));
+    L.gbar = o;        o = align256(o + sizeof(uint32_t) * (kGbarExit + 1));
     L.win = o;         o = align256(o + sizeof(unsigned long long) * kWinStride * (size_t)gamma * B);
     L.vq = o;          o = align256(o + sizeof(uint32_t) * 2);
     L.draft_part = o;  o = align256(o + sizeof(DrawLse) * 2 * (size_t)B * L.parts);

@@ -121,6 +121,8 @@ struct RowsArgs {
     // residual mode only
     const void* target;  // [B][gamma+1][V]
     uint32_t* near_ties;
+    // RNN head (kRnn only): the GRU step run at every position boundary
+    GruParams gru;
 };
 
 // Bounded grid-wide barrier on a counter in global memory: every CTA adds 1,
@@ -260,6 +262,69 @@ __device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
     return d;
 }
 
+// The RNN head's GRU step inside the persistent draft, at the boundary after
+// position k (its draws x~_k are the winner keys of index k - 1): state[k] =
+// GRU(state[k - 1], E[x~_k]) for every request, this CTA taking the hidden
+// units u = cta, cta + nctas, ...  One epilogue thread per (unit, request)
+// pair runs the six dot products (W_ih and W_hh rows of gates r, z, n) over
+// the rank in 16-byte steps: every load of the loop is independent, so a
+// thread keeps many in flight, and the unit's weight rows, shared by the
+// threads of consecutive requests, stay in L1.  x~_k comes from the CTA's
+// own copy of the draws when its request chunk covers the whole batch.
+// state[k - 1] was written by other CTAs (or by the GRU launch before the
+// kernel), so it is read through L2.
+__device__ __forceinline__ float bf16f_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16f_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float a) {
+    a = fmaf(bf16f_lo(w.x), bf16f_lo(x.x), a); a = fmaf(bf16f_hi(w.x), bf16f_hi(x.x), a);
+    a = fmaf(bf16f_lo(w.y), bf16f_lo(x.y), a); a = fmaf(bf16f_hi(w.y), bf16f_hi(x.y), a);
+    a = fmaf(bf16f_lo(w.z), bf16f_lo(x.z), a); a = fmaf(bf16f_hi(w.z), bf16f_hi(x.z), a);
+    a = fmaf(bf16f_lo(w.w), bf16f_lo(x.w), a); a = fmaf(bf16f_hi(w.w), bf16f_hi(x.w), a);
+    return a;
+}
+__device__ __forceinline__ float dot8(const uint4 w, const float4 h0, const float4 h1, float a) {
+    a = fmaf(bf16f_lo(w.x), h0.x, a); a = fmaf(bf16f_hi(w.x), h0.y, a);
+    a = fmaf(bf16f_lo(w.y), h0.z, a); a = fmaf(bf16f_hi(w.y), h0.w, a);
+    a = fmaf(bf16f_lo(w.z), h1.x, a); a = fmaf(bf16f_hi(w.z), h1.y, a);
+    a = fmaf(bf16f_lo(w.w), h1.z, a); a = fmaf(bf16f_hi(w.w), h1.w, a);
+    return a;
+}
+
+__device__ __noinline__ void gru_slice(const GruParams& g, int k, int cta, int nctas, int etid, int nthreads,
+                                       const int* s_tok_all, const unsigned long long* win) {
+    const int r = g.r, B = g.B;
+    if (cta >= r) return;
+    const float* hprev = g.state + (size_t)(k - 1) * B * r;
+    float* hout = g.state + (size_t)k * B * r;
+    const int nu = (r - 1 - cta) / nctas + 1;
+    for (int pr = etid; pr < nu * B; pr += nthreads) {
+        const int ui = pr / B, b = pr - ui * B, u = cta + ui * nctas;
+        const int x = s_tok_all ? s_tok_all[b] : win_token(__ldcg(&win[((size_t)(k - 1) * B + b) * kWinStride]));
+        const bool xin = x >= 0 && x < g.V;
+        const uint16_t* xr = g.E + (size_t)(xin ? x : 0) * r;
+        const float* hr = hprev + (size_t)b * r;
+        const uint16_t* wi0 = g.W_ih + (size_t)u * r;
+        const uint16_t* wh0 = g.W_hh + (size_t)u * r;
+        const size_t gs = (size_t)r * r;   // one gate block of rows
+        float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int c = 0; c < r; c += 8) {
+            const uint4 xe = xin ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0, 0, 0, 0);
+            const float4 h0 = __ldcg(reinterpret_cast<const float4*>(hr + c));
+            const float4 h1 = __ldcg(reinterpret_cast<const float4*>(hr + c + 4));
+#pragma unroll
+            for (int gt = 0; gt < 3; ++gt) {
+                acc[gt] = dot8(*reinterpret_cast<const uint4*>(wi0 + gt * gs + c), xe, acc[gt]);
+                acc[3 + gt] = dot8(*reinterpret_cast<const uint4*>(wh0 + gt * gs + c), h0, h1, acc[3 + gt]);
+            }
+        }
+        const float rg = 1.f / (1.f + expf(-(acc[0] + g.b_ih[u] + acc[3] + g.b_hh[u])));
+        const float zg = 1.f / (1.f + expf(-(acc[1] + g.b_ih[r + u] + acc[4] + g.b_hh[r + u])));
+        const float ng = tanhf(acc[2] + g.b_ih[2 * r + u] + rg * (acc[5] + g.b_hh[2 * r + u]));
+        hout[(size_t)b * r + u] = (1.f - zg) * ng + zg * __ldcg(hr + u);
+    }
+}
+
 // Positions k_first..k_last in one launch.  With more than one position the
 // launch is cooperative: after each position every CTA writes its partial
 // states and folds its draw of each request into a 64-bit atomic maximum
@@ -275,7 +340,7 @@ __device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
 // reaches before its merges of k are done.
 // 19 warps over 4 schedulers put 5 warps on three of them, whose 16384
 // registers then allow 96 a thread.
-template <bool kResid, typename TT>
+template <bool kResid, typename TT, bool kRnn = false>
 __global__ void __launch_bounds__(kThreads, 1)
 rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_last) {
     const DraftParams& p = a.p;
@@ -768,7 +833,25 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 // ---- h = W1[x~_k] into the A operands for the next position (the
                 //      MMAs of this one are complete: the last commit released the
                 //      final tile the warps just read)
-                stage_a_tmem(tmem_base, W1, s_tok, NC, RF, r, V, q, cb, lane, false);
+                if constexpr (kRnn) {
+                    // RNN head: the GRU step for every request, shared out by
+                    // hidden unit over the CTAs, then a second grid barrier
+                    gru_slice(a.gru, k, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, etid, 32 * kEpiWarps,
+                              gridDim.y == 1 ? s_tok : nullptr, p.ws.win);
+                    ptx::named_barrier(1, 32 * kEpiWarps);
+                    if (etid == 0)
+                        s_gb_ok = grid_barrier(p.ws.gbar + kGbarGru + (k - k_first), nctas, abort_flag, kWaitCycles) ? 1 : 0;
+                    ptx::named_barrier(1, 32 * kEpiWarps);
+                    if (!s_gb_ok) {
+                        if (etid == 0) raise_timeout(p.ws.status, 9);
+                        failed = true;
+                        *abort_flag = 1u;
+                        break;
+                    }
+                    stage_a_state(tmem_base, st_base, (size_t)p.B * r, k, s_row, s_tok, NC, RF, r, V, q, cb, lane, false);
+                } else {
+                    stage_a_tmem(tmem_base, W1, s_tok, NC, RF, r, V, q, cb, lane, false);
+                }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 ptx::named_barrier(1, 32 * kEpiWarps);
@@ -816,13 +899,13 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         __shared__ int s_out_last;
         if (tid == 0) {
             __threadfence();
-            s_out_last = atomicAdd(p.ws.gbar + kGridBarrierSlots, 1u) == nctas - 1;
+            s_out_last = atomicAdd(p.ws.gbar + kGbarExit, 1u) == nctas - 1;
         }
         __syncthreads();
         if (s_out_last) {
             __threadfence();
             for (int i = tid; i < p.gamma * p.B; i += kThreads) p.ws.win[(size_t)i * kWinStride] = 0ull;
-            if (tid <= kGridBarrierSlots) p.ws.gbar[tid] = 0u;
+            if (tid <= kGbarExit) p.ws.gbar[tid] = 0u;
             __threadfence();
         }
         return;
@@ -930,7 +1013,8 @@ bool cooperative_supported() {
 }
 
 static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bool resid, const void* target,
-                               bool target_bf16, uint32_t* near_ties, cudaStream_t s) {
+                               bool target_bf16, uint32_t* near_ties, cudaStream_t s,
+                               const GruParams* gru = nullptr) {
     auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
     if (!enc) return cudaErrorNotSupported;
     RowsArgs a;
@@ -938,6 +1022,7 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
     a.NC = p.B <= 64 ? 64 : 128;           // RF = 2 or 1: RF = 4 would leave no TMEM for accumulators
     a.target = target;
     a.near_ties = near_ties;
+    if (gru) a.gru = *gru;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.r};
         const cuuint64_t strides[1] = {(cuuint64_t)p.V * 2};
@@ -970,7 +1055,8 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
     }
     const Layout L = rows_layout(a.NC, p.r, resid);
     const size_t smem = L.total + 1024;
-    auto kern = !resid ? rows_kernel<false, float> : (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>);
+    auto kern = resid ? (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>)
+                      : (gru ? rows_kernel<false, float, true> : rows_kernel<false, float>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nchunks = (p.B + a.NC - 1) / a.NC;
@@ -991,6 +1077,14 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
 
 cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cudaStream_t s) {
     return launch_rows(p, k_first, k_last, false, nullptr, false, nullptr, s);
+}
+
+// The RNN head's draft in one cooperative launch: positions k_first..k_last,
+// the GRU step for position k + 1 run inside the kernel after position k's
+// draws (state[k_first - 1] must be ready).
+cudaError_t launch_draft_rows_rnn(const DraftParams& p, const GruParams& g, int k_first, int k_last,
+                                  cudaStream_t s) {
+    return launch_rows(p, k_first, k_last, false, nullptr, false, nullptr, s, &g);
 }
 
 bool resid_rows_supported(const VerifyParams& v) {

@@ -20,6 +20,8 @@ constexpr int kVerifySeg = 32768;      // vocabulary entries per verify-stream w
 constexpr int kVerifySub = 8;          // partial states per work item (one per consumer warp)
 constexpr int kChunk = 16;             // requests per chunk of the partial-producing kernels
 constexpr int kGridBarrierSlots = DSPARK_MAX_GAMMA;   // one grid-barrier counter per draft position
+constexpr int kGbarGru = kGridBarrierSlots;           // then one per position for the RNN head's GRU step
+constexpr int kGbarExit = 2 * kGridBarrierSlots;      // then the exit counter
 constexpr int kWinStride = 16;          // winner keys 128 bytes apart: one cache line each
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
@@ -34,7 +36,7 @@ struct WsPtrs {
     uint32_t* status;
     uint32_t* tickets_draft;   // [ceil(B/kChunk)] arrival counters, zero between launches
     uint32_t* tickets_resid;   // [ceil(B/kChunk)]
-    uint32_t* gbar;            // [kGridBarrierSlots + 1] grid-barrier counters, then the exit counter
+    uint32_t* gbar;            // [kGbarExit + 1] grid-barrier counters, then the exit counter
     uint32_t* vq;              // [2] verify-stream work counter and exit counter, zero between launches
     unsigned long long* win;   // [gamma][B][kWinStride] winner keys of the persistent draft (first of
                                // each line used), zero between launches
@@ -156,5 +158,7 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
 cudaError_t launch_sts_fit(const StsFitParams& p, cudaStream_t s);
 cudaError_t launch_gru(const GruParams& g, int k, cudaStream_t s);
 cudaError_t launch_draft_rnn(const DraftParams& p, const GruParams& g, cudaStream_t s);
+cudaError_t launch_draft_rows_rnn(const DraftParams& p, const GruParams& g, int k_first, int k_last,
+                                  cudaStream_t s);
 
 }  // namespace dspark
