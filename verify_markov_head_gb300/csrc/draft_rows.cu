@@ -121,7 +121,7 @@ struct RowsArgs {
     // residual mode only
     const void* target;  // [B][gamma+1][V]
     uint32_t* near_ties;
-    // RNN head (kRnn only): the GRU step run at every position boundary
+    // RNN head (kRnn only): the GRU steps run in the prologue and at the position boundaries
     GruParams gru;
 };
 
@@ -262,17 +262,19 @@ __device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
     return d;
 }
 
-// The RNN head's GRU step inside the persistent draft, at the boundary after
-// position k (its draws x~_k are the winner keys of index k - 1): state[k] =
-// GRU(state[k - 1], E[x~_k]) for every request, this CTA taking the hidden
-// units u = cta, cta + nctas, ...  One epilogue thread per (unit, request)
-// pair runs the six dot products (W_ih and W_hh rows of gates r, z, n) over
-// the rank in 16-byte steps: every load of the loop is independent, so a
-// thread keeps many in flight, and the unit's weight rows, shared by the
-// threads of consecutive requests, stay in L1.  x~_k comes from the CTA's
-// own copy of the draws when its request chunk covers the whole batch.
-// state[k - 1] was written by other CTAs (or by the GRU launch before the
-// kernel), so it is read through L2.
+// The RNN head's GRU step inside the persistent draft: state[ks] =
+// GRU(h, E[x]) for every request, with h = s0 and x = the anchor for ks = 0
+// (in the prologue), else h = state[ks - 1] and x = x~_ks, the draws of
+// position ks (winner keys of index ks - 1).  This CTA takes the hidden units
+// u = cta, cta + nctas, ...; an epilogue warp takes one request at a time,
+// lane l holding ranks [8 l, 8 l + 8) of x, of h and of the six weight rows
+// of each unit (W_ih and W_hh, gates r, z, n).  The partial dot products of
+// two units (12 values) are summed across the warp by recursive halving over
+// 16 slots (16 shuffles instead of 60: at each level a lane keeps half of its
+// slots and receives its partner's share of them), which leaves slot s in
+// lanes 2s and 2s + 1; lanes 0 and 1 then gather the six sums of their unit
+// and apply the gates.  The request's x and h are loaded one request ahead.
+// state[ks - 1] was written by other CTAs, so it is read through L2.
 __device__ __forceinline__ float bf16f_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16f_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float a) {
@@ -290,38 +292,95 @@ __device__ __forceinline__ float dot8(const uint4 w, const float4 h0, const floa
     return a;
 }
 
-__device__ __noinline__ void gru_slice(const GruParams& g, int k, int cta, int nctas, int etid, int nthreads,
-                                       const int* s_tok_all, const unsigned long long* win) {
+__device__ __forceinline__ void gru_step(const GruParams& g, int ks, int cta, int nctas, int ewarp, int lane,
+                                      const int* s_tok_all, const unsigned long long* win) {
     const int r = g.r, B = g.B;
-    if (cta >= r) return;
-    const float* hprev = g.state + (size_t)(k - 1) * B * r;
-    float* hout = g.state + (size_t)k * B * r;
+    if (cta >= r || ewarp >= B) return;
+    const unsigned full = 0xffffffffu;
+    const float* hprev = ks == 0 ? nullptr : g.state + (size_t)(ks - 1) * B * r;
+    float* hout = g.state + (size_t)ks * B * r;
     const int nu = (r - 1 - cta) / nctas + 1;
-    for (int pr = etid; pr < nu * B; pr += nthreads) {
-        const int ui = pr / B, b = pr - ui * B, u = cta + ui * nctas;
-        const int x = s_tok_all ? s_tok_all[b] : win_token(__ldcg(&win[((size_t)(k - 1) * B + b) * kWinStride]));
-        const bool xin = x >= 0 && x < g.V;
-        const uint16_t* xr = g.E + (size_t)(xin ? x : 0) * r;
-        const float* hr = hprev + (size_t)b * r;
-        const uint16_t* wi0 = g.W_ih + (size_t)u * r;
-        const uint16_t* wh0 = g.W_hh + (size_t)u * r;
-        const size_t gs = (size_t)r * r;   // one gate block of rows
-        float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int c = 0; c < r; c += 8) {
-            const uint4 xe = xin ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0, 0, 0, 0);
-            const float4 h0 = __ldcg(reinterpret_cast<const float4*>(hr + c));
-            const float4 h1 = __ldcg(reinterpret_cast<const float4*>(hr + c + 4));
+    const int e0 = 8 * lane;
+    const bool act = e0 < r;
+    const size_t gs = (size_t)r * r;   // one gate block of weight rows
+    auto token = [&](int b) {
+        if (ks == 0) return g.anchor[b];
+        return s_tok_all ? s_tok_all[b] : win_token(__ldcg(&win[((size_t)(ks - 1) * B + b) * kWinStride]));
+    };
+    auto load = [&](int b, uint4& xe, float4& h0, float4& h1) {
+        xe = make_uint4(0, 0, 0, 0);
+        h0 = make_float4(0.f, 0.f, 0.f, 0.f);
+        h1 = h0;
+        if (!act) return;
+        const int x = token(b);
+        if (x >= 0 && x < g.V) xe = *reinterpret_cast<const uint4*>(g.E + (size_t)x * r + e0);
+        const float* hr = hprev ? hprev + (size_t)b * r : g.s0;
+        h0 = __ldcg(reinterpret_cast<const float4*>(hr + e0));
+        h1 = __ldcg(reinterpret_cast<const float4*>(hr + e0 + 4));
+    };
+    uint4 xn; float4 hn0, hn1;
+    load(ewarp, xn, hn0, hn1);
+    for (int b = ewarp; b < B; b += kEpiWarps) {
+        const uint4 xe = xn;
+        const float4 h0 = hn0, h1 = hn1;
+        if (b + kEpiWarps < B) load(b + kEpiWarps, xn, hn0, hn1);
+        const float* hr = hprev ? hprev + (size_t)b * r : g.s0;
+        for (int j0 = 0; j0 < nu; j0 += 2) {
+            float v[16];
 #pragma unroll
-            for (int gt = 0; gt < 3; ++gt) {
-                acc[gt] = dot8(*reinterpret_cast<const uint4*>(wi0 + gt * gs + c), xe, acc[gt]);
-                acc[3 + gt] = dot8(*reinterpret_cast<const uint4*>(wh0 + gt * gs + c), h0, h1, acc[3 + gt]);
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            if (act) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (j0 + t >= nu) break;
+                    const int u = cta + (j0 + t) * nctas;
+                    const uint16_t* wi = g.W_ih + (size_t)u * r + e0;
+                    const uint16_t* wh = g.W_hh + (size_t)u * r + e0;
+#pragma unroll
+                    for (int gt = 0; gt < 3; ++gt) {
+                        v[6 * t + gt] = dot8(*reinterpret_cast<const uint4*>(wi + gt * gs), xe, 0.f);
+                        v[6 * t + 3 + gt] = dot8(*reinterpret_cast<const uint4*>(wh + gt * gs), h0, h1, 0.f);
+                    }
+                }
+            }
+            // recursive halving: 16 slots -> 8 -> 4 -> 2 -> 1
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const bool up = lane & 16;
+                const float send = up ? v[i] : v[i + 8], keep = up ? v[i + 8] : v[i];
+                v[i] = keep + __shfl_xor_sync(full, send, 16);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool up = lane & 8;
+                const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
+                v[i] = keep + __shfl_xor_sync(full, send, 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const bool up = lane & 4;
+                const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(full, send, 4);
+            }
+            {
+                const bool up = lane & 2;
+                const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
+                v[0] = keep + __shfl_xor_sync(full, send, 2);
+            }
+            v[0] += __shfl_xor_sync(full, v[0], 1);
+            // lanes 0 and 1 gather the six sums of units j0 and j0 + 1 (slot s sits in lane 2 s)
+            float a[6];
+#pragma unroll
+            for (int i = 0; i < 6; ++i) a[i] = __shfl_sync(full, v[0], 2 * (6 * (lane & 1) + i));
+            if (lane < 2 && j0 + lane < nu) {
+                const int u = cta + (j0 + lane) * nctas;
+                const float rg = 1.f / (1.f + expf(-(a[0] + g.b_ih[u] + a[3] + g.b_hh[u])));
+                const float zg = 1.f / (1.f + expf(-(a[1] + g.b_ih[r + u] + a[4] + g.b_hh[r + u])));
+                const float ng = tanhf(a[2] + g.b_ih[2 * r + u] + rg * (a[5] + g.b_hh[2 * r + u]));
+                const float hu = hprev ? __ldcg(hr + u) : g.s0[u];
+                hout[(size_t)b * r + u] = (1.f - zg) * ng + zg * hu;
             }
         }
-        const float rg = 1.f / (1.f + expf(-(acc[0] + g.b_ih[u] + acc[3] + g.b_hh[u])));
-        const float zg = 1.f / (1.f + expf(-(acc[1] + g.b_ih[r + u] + acc[4] + g.b_hh[r + u])));
-        const float ng = tanhf(acc[2] + g.b_ih[2 * r + u] + rg * (acc[5] + g.b_hh[2 * r + u]));
-        hout[(size_t)b * r + u] = (1.f - zg) * ng + zg * __ldcg(hr + u);
     }
 }
 
@@ -419,6 +478,23 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if constexpr (kRnn) {
+        // RNN head: the GRU step of the first position (from s0 and the
+        // anchors), shared out over the CTAs like the later ones
+        if (warp < kEpiWarps) {
+            __shared__ int s_pro_ok;
+            gru_step(a.gru, k_first - 1, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, warp, lane, nullptr,
+                     p.ws.win);
+            ptx::named_barrier(1, 32 * kEpiWarps);
+            if (tid == 0)
+                s_pro_ok = grid_barrier(p.ws.gbar + kGbarGru + (kGridBarrierSlots - 1), nctas, abort_flag, kWaitCycles);
+            ptx::named_barrier(1, 32 * kEpiWarps);
+            if (!s_pro_ok && tid == 0) {
+                raise_timeout(p.ws.status, 10);
+                *abort_flag = 1u;
+            }
+        }
+    }
     if (warp < kEpiWarps) {                        // the A operands of the first position
         if (st_base)
             stage_a_state(tmem_base, st_base, (size_t)p.B * r, kResid ? -1 : k_first - 1, s_row, s_tok, NC, RF, r,
@@ -836,8 +912,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 if constexpr (kRnn) {
                     // RNN head: the GRU step for every request, shared out by
                     // hidden unit over the CTAs, then a second grid barrier
-                    gru_slice(a.gru, k, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, etid, 32 * kEpiWarps,
-                              gridDim.y == 1 ? s_tok : nullptr, p.ws.win);
+                    gru_step(a.gru, k, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, warp, lane,
+                             gridDim.y == 1 ? s_tok : nullptr, p.ws.win);
                     ptx::named_barrier(1, 32 * kEpiWarps);
                     if (etid == 0)
                         s_gb_ok = grid_barrier(p.ws.gbar + kGbarGru + (k - k_first), nctas, abort_flag, kWaitCycles) ? 1 : 0;

@@ -11,11 +11,11 @@
 //     n  = tanh(W_in x + b_in + r * (W_hn h + b_hn))
 //     h' = (1 - z) * n + z * h.
 // The draft rows kernel stages its A operands from state[k-1] instead of W1
-// rows.  Position 1's GRU step is one launch of gru_kernel (below) before the
-// cooperative draft launch, which runs the later GRU steps itself at its
-// position boundaries (each CTA a slice of the hidden units, then a grid
-// barrier).  Without cooperative launch, each position is a gru_kernel
-// launch followed by a single-position draft launch.
+// rows.  In the cooperative draft launch the kernel runs every GRU step
+// itself: the first in its prologue, the others at its position boundaries
+// (each CTA a slice of the hidden units, then a grid barrier).  Without
+// cooperative launch, each position is a gru_kernel launch (below) followed
+// by a single-position draft launch.
 //
 // gru_kernel: the two [B x r] x [r x 3r] products per position are small
 // (6 B r^2 multiply-adds, 25 M at B = 64, r = 256) and latency-bound, so they
@@ -121,16 +121,12 @@ cudaError_t launch_gru(const GruParams& g, int k, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// The draft loop with the RNN head.  The GRU step of position 1, then one
-// cooperative draft launch that runs the GRU steps of the later positions at
-// its position boundaries; without cooperative launch, a GRU launch and a
+// The draft loop with the RNN head: one cooperative draft launch that runs
+// the GRU steps itself; without cooperative launch, a GRU launch and a
 // single-position draft launch per position.
 cudaError_t launch_draft_rnn(const DraftParams& p, const GruParams& g, cudaStream_t s) {
-    if (p.gamma > 1 && cooperative_supported() && !getenv("DSPARK_DRAFT_PER_POSITION")) {
-        cudaError_t e = launch_gru(g, 1, s);
-        if (e != cudaSuccess) return e;
+    if (p.gamma > 1 && cooperative_supported() && !getenv("DSPARK_DRAFT_PER_POSITION"))
         return launch_draft_rows_rnn(p, g, 1, p.gamma, s);
-    }
     for (int k = 1; k <= p.gamma; ++k) {
         cudaError_t e = launch_gru(g, k, s);
         if (e != cudaSuccess) return e;
