@@ -163,7 +163,7 @@ def run_gpu(args):
     inp = workload.inputs(w, step=rank, device=dev)
     head = args.head
     if head == "rnn":
-        inp["rnn"] = workload.rnn_head(w, device=dev)
+        inp["rnn"] = vm.rnn_prepare(workload.rnn_head(w, device=dev))
     buf = vm.StepBuffers(B, gamma, V, r, device=dev)
     stream = torch.cuda.Stream(device=dev)
     seed = w.seed
@@ -620,7 +620,7 @@ def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None, min_seconds=0.0, head="ma
     W1, W2 = inp["W1_64"], inp["W2_64"]
     if head == "rnn" and "rnn64" not in inp:
         src = dev_inp["rnn"] if dev_inp is not None and "rnn" in dev_inp else workload.rnn_head(w)
-        inp["rnn64"] = {k: v.double().cpu().numpy() for k, v in src.items()}
+        inp["rnn64"] = {k: v.double().cpu().numpy() for k, v in src.items() if k != "P"}
     threads = oracle.num_threads()
     t = time.perf_counter()
     _ = oracle.draft_markov(inp["U"][:1], W1, W2, inp["anchor"][:1], seed=w.seed)

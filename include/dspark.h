@@ -200,25 +200,35 @@ dspark_status dspark_verify(
  * stacked (r, z, n):
  *     r = sigma(W_ir x + b_ir + W_hr h + b_hr), z = sigma(W_iz x + b_iz + W_hz h + b_hz),
  *     n = tanh(W_in x + b_in + r * (W_hn h + b_hn)), h' = (1 - z) n + z h.
- * Inputs : U [B,gamma,V] fp32, E [V,r] bf16 (input embedding; W1 may be
- *          passed), W_ih [3r,r] and W_hh [3r,r] bf16, b_ih [3r], b_hh [3r],
- *          s0 [r] fp32, W2 [r,V] bf16 (W_t must be DSPARK_BF16), anchor [B].
+ * The input side enters through its per-token table P = E W_ih^T + b_ih
+ * (dspark_rnn_input_table, computed once per set of weights).
+ * Inputs : U [B,gamma,V] fp32, P [V,3r] fp32 (gate blocks r, z, n), W_hh
+ *          [3r,r] bf16, b_hh [3r] and s0 [r] fp32, W2 [r,V] bf16 (W_t must
+ *          be DSPARK_BF16), anchor [B].
  * Outputs: draft_tok, lse_q, z_tok as dspark_draft_markov; state
  *          [gamma,B,r] fp32 receives s_1..s_gamma (dspark_verify_rnn reads it).
+ * ws     : as dspark_draft_markov (the GRU's scratch lives there too).
  * Limits : those of dspark_draft_markov, plus r % 64 == 0, r <= 256, fp32 U
- *          (else DSPARK_ERR_UNSUPPORTED).  2*gamma launches on stream (a GRU
- *          step and a draft step per position).
+ *          (else DSPARK_ERR_UNSUPPORTED).  One cooperative launch (2*gamma
+ *          launches where cooperative launch is unavailable).
  */
 dspark_status dspark_draft_rnn(
     const void* U, dspark_dtype U_t,
-    const void* E, const void* W_ih, const void* W_hh,
-    const float* b_ih, const float* b_hh, const float* s0,
+    const float* P, const void* W_hh, const float* b_hh, const float* s0,
     const void* W2, dspark_dtype W_t,
     const int32_t* anchor,
     int B, int gamma, int V, int r, int req_base, float tau,
     uint64_t seed, uint64_t step,
     int32_t* draft_tok, float* lse_q, float* z_tok, float* state,
     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The RNN head's input projections for every token: P[v][j] = sum_i E[v][i]
+ * W_ih[j][i] + b_ih[j], j < 3r, fp32 accumulation.  E [V,r] and W_ih [3r,r]
+ * bf16, b_ih [3r] fp32, P [V,3r] fp32 (caller-owned).  r % 8 == 0.
+ */
+dspark_status dspark_rnn_input_table(const void* E, const void* W_ih, const float* b_ih, int V, int r, float* P,
+                                     void* stream);
 
 /*
  * dspark_verify for drafts of the RNN head: identical, except that the

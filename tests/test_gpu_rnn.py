@@ -36,12 +36,12 @@ def _case(B, V, r, seed):
     W = workload.weights(w, device=DEV)
     inp = dict(W)
     inp.update(workload.step_inputs(w, device=DEV))
-    inp["rnn"] = workload.rnn_head(w, device=DEV)
+    inp["rnn"] = vm.rnn_prepare(workload.rnn_head(w, device=DEV))
     return w, inp
 
 
 def _rnn64(inp):
-    return {k: v.double().cpu().numpy() for k, v in inp["rnn"].items()}
+    return {k: v.double().cpu().numpy() for k, v in inp["rnn"].items() if k != "P"}
 
 
 def _draft(w, inp, seed, req_base=0):
@@ -149,7 +149,7 @@ def test_rnn_full_size_b64_sampled_requests():
     sampled requests recomputed by the oracle."""
     w = workload.WORKLOADS["b64"]
     inp = workload.inputs(w, device=DEV)
-    inp["rnn"] = workload.rnn_head(w, device=DEV)
+    inp["rnn"] = vm.rnn_prepare(workload.rnn_head(w, device=DEV))
     buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
     vm.run_step(inp, buf, mode=0, seed=w.seed, head="rnn", p_tok=True)
     st, bits = vm.dspark_sync_status(buf.ws.buf)
@@ -177,6 +177,18 @@ def test_rnn_full_size_b64_sampled_requests():
     allacc = buf.accepted.cpu().numpy()
     off = buf.out_off.cpu().numpy()
     assert (np.diff(off) == allacc + 1).all() and ((allacc >= 0) & (allacc <= w.gamma)).all()
+
+
+def test_rnn_input_table():
+    """P = E W_ih^T + b_ih for every token, against float64 numpy on the same
+    bf16 values (fp32 accumulation over r products)."""
+    for V, r in ((1000, 64), (4099, 256), (77, 128)):
+        w = workload.custom("b64", B=4, V=V - V % 8 if V % 8 else V, r=r, seed=V)
+        rnn = workload.rnn_head(w, device=DEV)
+        P = vm.dspark_rnn_input_table(rnn["E"], rnn["W_ih"], rnn["b_ih"])
+        torch.cuda.synchronize()
+        ref = rnn["E"].double().cpu().numpy() @ rnn["W_ih"].double().cpu().numpy().T + rnn["b_ih"].double().cpu().numpy()
+        np.testing.assert_allclose(P.cpu().numpy(), ref, rtol=0, atol=2e-5)
 
 
 def test_rnn_rejects_unsupported_shapes():

@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
+    "dspark_schedule", "dspark_verify", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_rnn_input_table", "rnn_prepare", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
@@ -57,8 +57,10 @@ _lib.dspark_verify.restype = _i
 _lib.dspark_draft_markov_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
                                              _vp, _vp, _vp, _vp, _vp]
 _lib.dspark_draft_markov_noalloc.restype = _i
-_lib.dspark_draft_rnn.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f,
+_lib.dspark_draft_rnn.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f,
                                   _u64, _u64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_rnn_input_table.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp]
+_lib.dspark_rnn_input_table.restype = _i
 _lib.dspark_draft_rnn.restype = _i
 _lib.dspark_verify_rnn.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
                                    _i, _i, _i, _i, _i, _f, _u64, _u64,
@@ -232,26 +234,50 @@ def dspark_verify(target, U, W1, W2, anchor, draft_tok, lse_q, z_tok, K, accepte
         _p(p_tok), _p(near_ties), ws.ptr(), ws.nbytes(), _stream(stream)))
 
 
+def dspark_rnn_input_table(E, W_ih, b_ih, P=None, *, stream=None):
+    """The RNN head's per-token input projections P = E W_ih^T + b_ih
+    ([V, 3r] fp32), computed on the device once per set of weights."""
+    V, r = E.shape
+    if tuple(W_ih.shape) != (3 * r, r) or b_ih.numel() != 3 * r:
+        raise ValueError("W_ih [3r, r] and b_ih [3r] expected")
+    if E.dtype != torch.bfloat16 or W_ih.dtype != torch.bfloat16 or b_ih.dtype != torch.float32:
+        raise TypeError("E and W_ih must be bfloat16, b_ih float32")
+    P = torch.empty((V, 3 * r), dtype=torch.float32, device=E.device) if P is None else P
+    _check("dspark_rnn_input_table", _lib.dspark_rnn_input_table(_p(E), _p(W_ih), _p(b_ih), V, r, _p(P),
+                                                                 _stream(stream)))
+    return P
+
+
+def rnn_prepare(rnn: dict, *, stream=None) -> dict:
+    """The RNN head's parameters with the input table P added (from E, W_ih
+    and b_ih); returns the same dict."""
+    if "P" not in rnn:
+        rnn["P"] = dspark_rnn_input_table(rnn["E"], rnn["W_ih"], rnn["b_ih"], stream=stream)
+    return rnn
+
+
 def dspark_draft_rnn(U, rnn, W2, anchor, draft_tok, lse_q, z_tok, state, ws: Workspace, *,
                      tau=1.0, seed=0, step=0, req_base=0, stream=None):
-    """The draft loop with the RNN head.  rnn = dict(E [V,r], W_ih [3r,r],
-    W_hh [3r,r] (bf16), b_ih [3r], b_hh [3r], s0 [r] (fp32)); state
+    """The draft loop with the RNN head.  rnn = dict(P [V,3r] fp32 (see
+    rnn_prepare), W_hh [3r,r] bf16, b_hh [3r], s0 [r] fp32); state
     [gamma,B,r] fp32 receives the states s_1..s_gamma."""
     B, gamma, V = U.shape
     r = W2.shape[0]
-    E, W_ih, W_hh = rnn["E"], rnn["W_ih"], rnn["W_hh"]
-    if tuple(E.shape) != (V, r) or tuple(W_ih.shape) != (3 * r, r) or tuple(W_hh.shape) != (3 * r, r):
-        raise ValueError("E [V,r], W_ih [3r,r] and W_hh [3r,r] expected")
-    if not (E.dtype == W_ih.dtype == W_hh.dtype == W2.dtype == torch.bfloat16):
-        raise TypeError("the RNN head's matrices and W2 must be bfloat16")
-    if rnn["b_ih"].numel() != 3 * r or rnn["b_hh"].numel() != 3 * r or rnn["s0"].numel() != r:
-        raise ValueError("b_ih, b_hh [3r] and s0 [r] expected")
+    if "P" not in rnn:
+        raise ValueError("the RNN head needs its input table: call rnn_prepare first")
+    P, W_hh = rnn["P"], rnn["W_hh"]
+    if tuple(P.shape) != (V, 3 * r) or P.dtype != torch.float32 or tuple(W_hh.shape) != (3 * r, r):
+        raise ValueError("P [V,3r] float32 and W_hh [3r,r] expected")
+    if not (W_hh.dtype == W2.dtype == torch.bfloat16):
+        raise TypeError("W_hh and W2 must be bfloat16")
+    if rnn["b_hh"].numel() != 3 * r or rnn["s0"].numel() != r:
+        raise ValueError("b_hh [3r] and s0 [r] expected")
     if tuple(state.shape) != (gamma, B, r) or state.dtype != torch.float32:
         raise ValueError("state must be float32 [gamma, B, r]")
     _check("dspark_draft_rnn", _lib.dspark_draft_rnn(
-        _p(U), _dt(U), _p(E), _p(W_ih), _p(W_hh), _p(rnn["b_ih"]), _p(rnn["b_hh"]), _p(rnn["s0"]), _p(W2),
-        _dt(W2), _p(anchor), B, gamma, V, r, req_base, float(tau), int(seed), int(step), _p(draft_tok),
-        _p(lse_q), _p(z_tok), _p(state), ws.ptr(), ws.nbytes(), _stream(stream)))
+        _p(U), _dt(U), _p(P), _p(W_hh), _p(rnn["b_hh"]), _p(rnn["s0"]), _p(W2), _dt(W2), _p(anchor),
+        B, gamma, V, r, req_base, float(tau), int(seed), int(step), _p(draft_tok), _p(lse_q), _p(z_tok),
+        _p(state), ws.ptr(), ws.nbytes(), _stream(stream)))
 
 
 def dspark_verify_rnn(target, U, state, W2, anchor, draft_tok, lse_q, z_tok, K, accepted, out_tok, out_req,

@@ -44,6 +44,7 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.lse_rej = o;     o = align256(o + sizeof(float2) * (size_t)B);
     L.resid_part = o;  o = align256(o + sizeof(Draw2) * (size_t)B * L.parts);
     L.conf = o;        o = align256(o + sizeof(uint32_t) * (size_t)B + sizeof(float) * (size_t)B * gamma);
+    L.rnn_gh = o;      o = align256(o + sizeof(float) * (size_t)B * 3 * kMaxRnnRank);
     L.total = o;
     return L;
 }
@@ -67,6 +68,7 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     P.resid_part = reinterpret_cast<Draw2*>(base + L.resid_part);
     P.conf_tickets = reinterpret_cast<uint32_t*>(base + L.conf);
     P.conf_score = reinterpret_cast<float*>(base + L.conf + sizeof(uint32_t) * (size_t)B);
+    P.rnn_gh = reinterpret_cast<float*>(base + L.rnn_gh);
     P.nseg = L.nseg;
     P.parts = L.parts;
     return P;
@@ -279,20 +281,28 @@ dspark_status dspark_verify_rnn(const void* target, dspark_dtype target_t, const
                        next_anchor, p_tok, near_ties, ws, ws_bytes, stream);
 }
 
-dspark_status dspark_draft_rnn(const void* U, dspark_dtype U_t, const void* E, const void* W_ih, const void* W_hh,
-                               const float* b_ih, const float* b_hh, const float* s0, const void* W2,
-                               dspark_dtype W_t, const int32_t* anchor, int B, int gamma, int V, int r,
-                               int req_base, float tau, uint64_t seed, uint64_t step, int32_t* draft_tok,
-                               float* lse_q, float* z_tok, float* state, void* ws, size_t ws_bytes,
-                               void* stream) {
+dspark_status dspark_rnn_input_table(const void* E, const void* W_ih, const float* b_ih, int V, int r, float* P,
+                                     void* stream) {
+    if (V < 1 || r < 1 || r > 1024 || (r % 8) != 0) return DSPARK_ERR_INVALID;
+    if (!is_device_ptr(E) || !is_device_ptr(W_ih) || !is_device_ptr(b_ih) || !is_device_ptr(P))
+        return DSPARK_ERR_INVALID;
+    return launch_status(launch_rnn_input_table(static_cast<const uint16_t*>(E), static_cast<const uint16_t*>(W_ih),
+                                                b_ih, V, r, P, static_cast<cudaStream_t>(stream)));
+}
+
+dspark_status dspark_draft_rnn(const void* U, dspark_dtype U_t, const float* P, const void* W_hh, const float* b_hh,
+                               const float* s0, const void* W2, dspark_dtype W_t, const int32_t* anchor, int B,
+                               int gamma, int V, int r, int req_base, float tau, uint64_t seed, uint64_t step,
+                               int32_t* draft_tok, float* lse_q, float* z_tok, float* state, void* ws,
+                               size_t ws_bytes, void* stream) {
     if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
     if ((U_t != DSPARK_F32 && U_t != DSPARK_BF16) || (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
         return DSPARK_ERR_UNSUPPORTED;
-    const void* need[] = {U, E, W_ih, W_hh, b_ih, b_hh, s0, W2, anchor, draft_tok, lse_q, z_tok, state, ws};
+    const void* need[] = {U, P, W_hh, b_hh, s0, W2, anchor, draft_tok, lse_q, z_tok, state, ws};
     for (const void* q : need)
         if (!is_device_ptr(q)) return DSPARK_ERR_INVALID;
-    if (!aligned(U, 16) || !aligned(E, 16) || !aligned(W_ih, 16) || !aligned(W_hh, 16) || !aligned(W2, 16) ||
-        !aligned(state, 16) || !aligned(ws, 256))
+    if (!aligned(U, 16) || !aligned(P, 16) || !aligned(W_hh, 16) || !aligned(W2, 16) || !aligned(state, 16) ||
+        !aligned(ws, 256))
         return DSPARK_ERR_INVALID;
     if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;
     if ((double)(req_base + (double)B) * (gamma + 1) >= 4294967295.0) return DSPARK_ERR_INVALID;
@@ -306,12 +316,14 @@ dspark_status dspark_draft_rnn(const void* U, dspark_dtype U_t, const void* E, c
     p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.logits_out = nullptr;
     p.ws = ws_ptrs(ws, B, gamma, V);
     p.state = state;
-    if (!draft_rows_supported(p)) return DSPARK_ERR_UNSUPPORTED;   // bf16 weights, fp32 U, r % 64 == 0, r <= 256
+    // bf16 weights, fp32 U, r % 64 == 0, r <= 256 (= kMaxRnnRank, the size of the gh scratch rows)
+    if (!draft_rows_supported(p) || r > kMaxRnnRank) return DSPARK_ERR_UNSUPPORTED;
     GruParams g;
-    g.E = static_cast<const uint16_t*>(E);
-    g.W_ih = static_cast<const uint16_t*>(W_ih); g.W_hh = static_cast<const uint16_t*>(W_hh);
-    g.b_ih = b_ih; g.b_hh = b_hh; g.s0 = s0;
+    g.P = P;
+    g.W_hh = static_cast<const uint16_t*>(W_hh);
+    g.b_hh = b_hh; g.s0 = s0;
     g.anchor = anchor; g.draft_tok = draft_tok; g.state = state;
+    g.gh = p.ws.rnn_gh;
     g.B = B; g.gamma = gamma; g.V = V; g.r = r;
     g.status = p.ws.status;
     return launch_status(launch_draft_rnn(p, g, static_cast<cudaStream_t>(stream)));

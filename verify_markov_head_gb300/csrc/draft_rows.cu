@@ -262,19 +262,24 @@ __device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
     return d;
 }
 
-// The RNN head's GRU step inside the persistent draft: state[ks] =
-// GRU(h, E[x]) for every request, with h = s0 and x = the anchor for ks = 0
-// (in the prologue), else h = state[ks - 1] and x = x~_ks, the draws of
-// position ks (winner keys of index ks - 1).  This CTA takes the hidden units
-// u = cta, cta + nctas, ...; an epilogue warp takes one request at a time,
-// lane l holding ranks [8 l, 8 l + 8) of x, of h and of the six weight rows
-// of each unit (W_ih and W_hh, gates r, z, n).  The partial dot products of
-// two units (12 values) are summed across the warp by recursive halving over
-// 16 slots (16 shuffles instead of 60: at each level a lane keeps half of its
-// slots and receives its partner's share of them), which leaves slot s in
-// lanes 2s and 2s + 1; lanes 0 and 1 then gather the six sums of their unit
-// and apply the gates.  The request's x and h are loaded one request ahead.
-// state[ks - 1] was written by other CTAs, so it is read through L2.
+// The RNN head's GRU steps inside the persistent draft.  Step ks writes
+// state[ks] = GRU(h, x) for every request, h = s0 and x = the anchor for
+// ks = 0 (in the prologue), else h = state[ks - 1] and x = x~_ks, the draws
+// of position ks (winner keys of index ks - 1).  This CTA takes the hidden
+// units u = cta, cta + nctas, ... for every request, in two parts:
+//   gh_compute: gh[b][g r + u] = W_hh[g r + u] . h_b + b_hh (gates g = r, z,
+//     n) as soon as h is known, i.e. right after the previous step, while
+//     the MMA already runs the next position.  An epilogue warp takes one
+//     request at a time, lane l holding ranks [8 l, 8 l + 8) of h and of the
+//     unit's three W_hh rows; the six partial sums of two units are summed
+//     across the warp by recursive halving over 8 slots (9 shuffles), which
+//     leaves slot s in lanes 4 s .. 4 s + 3.  For h = s0 one row serves
+//     every request.
+//   gate_step: once x is drawn, one thread per (unit, request) gathers the
+//     three input projections P[x][g r + u] (a table computed once from E,
+//     W_ih and b_ih), applies the gates and writes the new state.
+// The step's critical path (draws known -> new state published) is thus a
+// gather and the gate arithmetic.  Other CTAs' state rows are read through L2.
 __device__ __forceinline__ float bf16f_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16f_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float a) {
@@ -292,95 +297,90 @@ __device__ __forceinline__ float dot8(const uint4 w, const float4 h0, const floa
     return a;
 }
 
-__device__ __forceinline__ void gru_step(const GruParams& g, int ks, int cta, int nctas, int ewarp, int lane,
-                                      const int* s_tok_all, const unsigned long long* win) {
-    const int r = g.r, B = g.B;
+__device__ __forceinline__ void gh_compute(const GruParams& g, int ks_h, int cta, int nctas, int ewarp, int lane) {
+    const int r = g.r;
+    const float* hsrc = ks_h < 0 ? nullptr : g.state + (size_t)ks_h * g.B * r;
+    const int B = hsrc ? g.B : 1;                 // s0: one row serves every request
     if (cta >= r || ewarp >= B) return;
     const unsigned full = 0xffffffffu;
-    const float* hprev = ks == 0 ? nullptr : g.state + (size_t)(ks - 1) * B * r;
-    float* hout = g.state + (size_t)ks * B * r;
     const int nu = (r - 1 - cta) / nctas + 1;
     const int e0 = 8 * lane;
     const bool act = e0 < r;
-    const size_t gs = (size_t)r * r;   // one gate block of weight rows
-    auto token = [&](int b) {
-        if (ks == 0) return g.anchor[b];
-        return s_tok_all ? s_tok_all[b] : win_token(__ldcg(&win[((size_t)(ks - 1) * B + b) * kWinStride]));
-    };
-    auto load = [&](int b, uint4& xe, float4& h0, float4& h1) {
-        xe = make_uint4(0, 0, 0, 0);
-        h0 = make_float4(0.f, 0.f, 0.f, 0.f);
-        h1 = h0;
-        if (!act) return;
-        const int x = token(b);
-        if (x >= 0 && x < g.V) xe = *reinterpret_cast<const uint4*>(g.E + (size_t)x * r + e0);
-        const float* hr = hprev ? hprev + (size_t)b * r : g.s0;
-        h0 = __ldcg(reinterpret_cast<const float4*>(hr + e0));
-        h1 = __ldcg(reinterpret_cast<const float4*>(hr + e0 + 4));
-    };
-    uint4 xn; float4 hn0, hn1;
-    load(ewarp, xn, hn0, hn1);
+    const size_t gs = (size_t)r * r;
     for (int b = ewarp; b < B; b += kEpiWarps) {
-        const uint4 xe = xn;
-        const float4 h0 = hn0, h1 = hn1;
-        if (b + kEpiWarps < B) load(b + kEpiWarps, xn, hn0, hn1);
-        const float* hr = hprev ? hprev + (size_t)b * r : g.s0;
+        float4 h0 = make_float4(0.f, 0.f, 0.f, 0.f), h1 = h0;
+        if (act) {
+            const float* hr = hsrc ? hsrc + (size_t)b * r : g.s0;
+            h0 = __ldcg(reinterpret_cast<const float4*>(hr + e0));
+            h1 = __ldcg(reinterpret_cast<const float4*>(hr + e0 + 4));
+        }
         for (int j0 = 0; j0 < nu; j0 += 2) {
-            float v[16];
+            float v[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
             if (act) {
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (j0 + t >= nu) break;
-                    const int u = cta + (j0 + t) * nctas;
-                    const uint16_t* wi = g.W_ih + (size_t)u * r + e0;
-                    const uint16_t* wh = g.W_hh + (size_t)u * r + e0;
+                    const uint16_t* wh = g.W_hh + (size_t)(cta + (j0 + t) * nctas) * r + e0;
 #pragma unroll
-                    for (int gt = 0; gt < 3; ++gt) {
-                        v[6 * t + gt] = dot8(*reinterpret_cast<const uint4*>(wi + gt * gs), xe, 0.f);
-                        v[6 * t + 3 + gt] = dot8(*reinterpret_cast<const uint4*>(wh + gt * gs), h0, h1, 0.f);
-                    }
+                    for (int gt = 0; gt < 3; ++gt)
+                        v[3 * t + gt] = dot8(*reinterpret_cast<const uint4*>(wh + gt * gs), h0, h1, 0.f);
                 }
             }
-            // recursive halving: 16 slots -> 8 -> 4 -> 2 -> 1
+            // recursive halving: 8 slots -> 4 -> 2 -> 1, then the last two levels
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4; ++i) {
                 const bool up = lane & 16;
-                const float send = up ? v[i] : v[i + 8], keep = up ? v[i + 8] : v[i];
+                const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
                 v[i] = keep + __shfl_xor_sync(full, send, 16);
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
                 const bool up = lane & 8;
-                const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
+                const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
                 v[i] = keep + __shfl_xor_sync(full, send, 8);
             }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const bool up = lane & 4;
-                const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
-                v[i] = keep + __shfl_xor_sync(full, send, 4);
-            }
             {
-                const bool up = lane & 2;
+                const bool up = lane & 4;
                 const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
-                v[0] = keep + __shfl_xor_sync(full, send, 2);
+                v[0] = keep + __shfl_xor_sync(full, send, 4);
             }
+            v[0] += __shfl_xor_sync(full, v[0], 2);
             v[0] += __shfl_xor_sync(full, v[0], 1);
-            // lanes 0 and 1 gather the six sums of units j0 and j0 + 1 (slot s sits in lane 2 s)
-            float a[6];
-#pragma unroll
-            for (int i = 0; i < 6; ++i) a[i] = __shfl_sync(full, v[0], 2 * (6 * (lane & 1) + i));
-            if (lane < 2 && j0 + lane < nu) {
-                const int u = cta + (j0 + lane) * nctas;
-                const float rg = 1.f / (1.f + expf(-(a[0] + g.b_ih[u] + a[3] + g.b_hh[u])));
-                const float zg = 1.f / (1.f + expf(-(a[1] + g.b_ih[r + u] + a[4] + g.b_hh[r + u])));
-                const float ng = tanhf(a[2] + g.b_ih[2 * r + u] + rg * (a[5] + g.b_hh[2 * r + u]));
-                const float hu = hprev ? __ldcg(hr + u) : g.s0[u];
-                hout[(size_t)b * r + u] = (1.f - zg) * ng + zg * hu;
+            // slot s = 3 t + gate sits in lanes 4 s .. 4 s + 3
+            const int slot = lane >> 2, t = slot / 3, gt = slot - 3 * t;
+            if ((lane & 3) == 0 && slot < 6 && j0 + t < nu) {
+                const int row = gt * r + cta + (j0 + t) * nctas;
+                g.gh[(size_t)b * 3 * r + row] = v[0] + g.b_hh[row];
             }
         }
+    }
+}
+
+__device__ __forceinline__ void gate_step(const GruParams& g, int ks, int cta, int nctas, int etid, int nthreads,
+                                          const int* s_tok_all, const unsigned long long* win) {
+    const int r = g.r, B = g.B;
+    if (cta >= r) return;
+    const float* hprev = ks == 0 ? nullptr : g.state + (size_t)(ks - 1) * B * r;
+    float* hout = g.state + (size_t)ks * B * r;
+    const int nu = (r - 1 - cta) / nctas + 1;
+    for (int pr = etid; pr < nu * B; pr += nthreads) {
+        const int ui = pr / B, b = pr - ui * B, u = cta + ui * nctas;
+        const int x = ks == 0 ? g.anchor[b]
+                              : (s_tok_all ? s_tok_all[b]
+                                           : win_token(__ldcg(&win[((size_t)(ks - 1) * B + b) * kWinStride])));
+        float gi0 = 0.f, gi1 = 0.f, gi2 = 0.f;
+        if (x >= 0 && x < g.V) {
+            const float* Pr = g.P + (size_t)x * 3 * r;
+            gi0 = Pr[u]; gi1 = Pr[r + u]; gi2 = Pr[2 * r + u];
+        }
+        const float* ghr = g.gh + (size_t)(hprev ? b : 0) * 3 * r;
+        const float hu = hprev ? __ldcg(hprev + (size_t)b * r + u) : g.s0[u];
+        const float rg = 1.f / (1.f + expf(-(gi0 + ghr[u])));
+        const float zg = 1.f / (1.f + expf(-(gi1 + ghr[r + u])));
+        const float ng = tanhf(gi2 + rg * ghr[2 * r + u]);
+        hout[(size_t)b * r + u] = (1.f - zg) * ng + zg * hu;
     }
 }
 
@@ -483,8 +483,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         // anchors), shared out over the CTAs like the later ones
         if (warp < kEpiWarps) {
             __shared__ int s_pro_ok;
-            gru_step(a.gru, k_first - 1, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, warp, lane, nullptr,
-                     p.ws.win);
+            const int cta_id = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+            gh_compute(a.gru, -1, cta_id, (int)nctas, warp, lane);
+            ptx::named_barrier(1, 32 * kEpiWarps);
+            gate_step(a.gru, 0, cta_id, (int)nctas, tid, 32 * kEpiWarps, nullptr, p.ws.win);
             ptx::named_barrier(1, 32 * kEpiWarps);
             if (tid == 0)
                 s_pro_ok = grid_barrier(p.ws.gbar + kGbarGru + (kGridBarrierSlots - 1), nctas, abort_flag, kWaitCycles);
@@ -664,6 +666,12 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         const int b = b_base + nrow;
         const bool real = active && nrow < nb && (!kResid || s_row[nrow] >= 0);
         const float scale2 = p.inv_tau * 1.4426950408889634f;      // z -> z * log2(e)
+        if constexpr (kRnn) {
+            // W_hh . state[0] for the first boundary's GRU step, while the MMA
+            // starts the first position
+            if (k_first < k_last)
+                gh_compute(a.gru, k_first - 1, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, warp, lane);
+        }
         int acc = 0;
         uint32_t aph = 0;
         bool failed = false;
@@ -912,8 +920,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 if constexpr (kRnn) {
                     // RNN head: the GRU step for every request, shared out by
                     // hidden unit over the CTAs, then a second grid barrier
-                    gru_step(a.gru, k, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, warp, lane,
-                             gridDim.y == 1 ? s_tok : nullptr, p.ws.win);
+                    gate_step(a.gru, k, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, etid,
+                              32 * kEpiWarps, gridDim.y == 1 ? s_tok : nullptr, p.ws.win);
                     ptx::named_barrier(1, 32 * kEpiWarps);
                     if (etid == 0)
                         s_gb_ok = grid_barrier(p.ws.gbar + kGbarGru + (k - k_first), nctas, abort_flag, kWaitCycles) ? 1 : 0;
@@ -932,6 +940,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 ptx::tc_fence_before();
                 ptx::named_barrier(1, 32 * kEpiWarps);
                 if (etid == 0) ptx::mbar_arrive(a_ready);
+                if constexpr (kRnn) {
+                    // W_hh . state[k] for the next boundary's GRU step, off its critical path
+                    if (k + 1 < k_last)
+                        gh_compute(a.gru, k, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, warp, lane);
+                }
             }
             // ---- this position's outputs, while the MMA starts the next one: the
             //      CTAs share the requests, a warp folds one request's partials

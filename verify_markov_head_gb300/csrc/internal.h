@@ -26,7 +26,8 @@ constexpr int kWinStride = 16;          // winner keys 128 bytes apart: one cach
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, tickets, gbar, win, vq, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, conf, total;
+    size_t status, tickets, gbar, win, vq, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, conf, rnn_gh,
+        total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -49,6 +50,7 @@ struct WsPtrs {
     Draw2* resid_part;   // [B][parts]
     uint32_t* conf_tickets;  // [B] confidence-head arrival counters, zero between launches
     float* conf_score;       // [B][gamma]
+    float* rnn_gh;           // [B][3 kMaxRnnRank] RNN head scratch
     int nseg;
     int parts;
 };
@@ -71,15 +73,17 @@ struct DraftParams {
 // One GRU step of the RNN head for every request: state[k-1] = GRU(state[k-2]
 // (s0 for k = 1), E[x~_{k-1}]).
 struct GruParams {
-    const uint16_t* E;                       // [V][r] bf16 input embedding
-    const uint16_t* W_ih; const uint16_t* W_hh;   // [3r][r] bf16, gate rows (r, z, n)
-    const float* b_ih; const float* b_hh;    // [3r]
+    const float* P;                          // [V][3r] input projections E W_ih^T + b_ih, gate blocks (r, z, n)
+    const uint16_t* W_hh;                    // [3r][r] bf16, gate rows (r, z, n)
+    const float* b_hh;                       // [3r]
     const float* s0;                         // [r] learned initial state
     const int32_t* anchor; const int32_t* draft_tok;
     float* state;                            // [gamma][B][r]
+    float* gh;                               // [B][3r] scratch: W_hh h + b_hh of the coming step
     int B, gamma, V, r;
     uint32_t* status;
 };
+constexpr int kMaxRnnRank = 256;             // the draft rows kernel's limit on r
 
 struct ConfParams {
     const float* h; int d;
@@ -157,6 +161,8 @@ cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
 cudaError_t launch_sts_fit(const StsFitParams& p, cudaStream_t s);
 cudaError_t launch_gru(const GruParams& g, int k, cudaStream_t s);
+cudaError_t launch_rnn_input_table(const uint16_t* E, const uint16_t* W_ih, const float* b_ih, int V, int r,
+                                   float* P, cudaStream_t s);
 cudaError_t launch_draft_rnn(const DraftParams& p, const GruParams& g, cudaStream_t s);
 cudaError_t launch_draft_rows_rnn(const DraftParams& p, const GruParams& g, int k_first, int k_last,
                                   cudaStream_t s);

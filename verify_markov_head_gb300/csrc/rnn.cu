@@ -10,21 +10,17 @@
 //     z  = sigma(W_iz x + b_iz + W_hz h + b_hz)
 //     n  = tanh(W_in x + b_in + r * (W_hn h + b_hn))
 //     h' = (1 - z) * n + z * h.
+// The input x is an embedding row, so its projection W_ih x + b_ih depends on
+// the token alone: rnn_input_table_kernel (below) computes it once for every
+// token, P[v] = W_ih E[v] + b_ih ([V][3r] fp32), and a GRU step then gathers
+// three entries of P where it would take three dot products.
+//
 // The draft rows kernel stages its A operands from state[k-1] instead of W1
 // rows.  In the cooperative draft launch the kernel runs every GRU step
 // itself: the first in its prologue, the others at its position boundaries
 // (each CTA a slice of the hidden units, then a grid barrier).  Without
 // cooperative launch, each position is a gru_kernel launch (below) followed
 // by a single-position draft launch.
-//
-// gru_kernel: the two [B x r] x [r x 3r] products per position are small
-// (6 B r^2 multiply-adds, 25 M at B = 64, r = 256) and latency-bound, so they
-// run on the CUDA cores.  A CTA takes 32 hidden units (one per lane) for 8
-// requests (one per warp).  The K dimension goes in chunks of 64: the 6 weight
-// rows of the CTA's units (W_ih and W_hh, three gates each) are staged in
-// shared memory with a one-word pad per row, so lane j reading its row meets
-// no bank conflict, and the chunk of x = E[x~] and h of each request is
-// staged as fp32 and read as a broadcast.
 #include <cuda_runtime.h>
 #include <stdlib.h>
 
@@ -34,18 +30,72 @@
 namespace dspark {
 namespace {
 
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// P[v][j] = sum_i E[v][i] W_ih[j][i] + b_ih[j] for v < V, j < 3r: a
+// [V x r] x [r x 3r] product, run once per set of weights (30 GFLOP at
+// V = 151936, r = 256).  Tiles of 64 tokens x 64 outputs, K in chunks of 32
+// staged in shared memory as fp32 (rows padded by one word), 16 x 16 threads
+// with 4 x 4 outputs each.
+constexpr int kTT = 64, kTK = 32;
+
+__global__ void __launch_bounds__(256)
+rnn_input_table_kernel(const uint16_t* __restrict__ E, const uint16_t* __restrict__ W_ih,
+                       const float* __restrict__ b_ih, int V, int r, float* __restrict__ P) {
+    __shared__ float Es[kTT][kTK + 1];
+    __shared__ float Ws[kTT][kTK + 1];
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    const int v0 = blockIdx.y * kTT, j0 = blockIdx.x * kTT, J = 3 * r;
+    float acc[4][4] = {};
+    for (int kc = 0; kc < r; kc += kTK) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < kTT * kTK; i += 256) {
+            const int row = i / kTK, c = i % kTK;
+            const int v = v0 + row, j = j0 + row;
+            Es[row][c] = v < V ? __uint_as_float((uint32_t)E[(size_t)v * r + kc + c] << 16) : 0.f;
+            Ws[row][c] = j < J ? __uint_as_float((uint32_t)W_ih[(size_t)j * r + kc + c] << 16) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int c = 0; c < kTK; ++c) {
+            float e[4], w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { e[i] = Es[ty + 16 * i][c]; w[i] = Ws[tx + 16 * i][c]; }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[i][q] = fmaf(e[i], w[q], acc[i][q]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int v = v0 + ty + 16 * i;
+        if (v >= V) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = j0 + tx + 16 * q;
+            if (j < J) P[(size_t)v * J + j] = acc[i][q] + b_ih[j];
+        }
+    }
+}
+
+// One GRU step for every request, the launch form of the step (used without
+// cooperative launch): state[k-1] = GRU(h, x~_{k-1}), h = state[k-2] (s0 for
+// k = 1).  The hidden side W_hh h is a [B x r] x [r x 3r] product: a CTA
+// takes 32 hidden units (one per lane) for 8 requests (one per warp), K in
+// chunks of 64 with the three W_hh rows of each unit staged in shared memory
+// (one pad word per row, so lane j reading its row meets no bank conflict)
+// and the chunk of each request's h staged as fp32 and read as a broadcast.
+// The input side is three entries of P.
 constexpr int kUnits = 32;     // hidden units per CTA (one per lane)
 constexpr int kReqs = 8;       // requests per CTA (one per warp)
 constexpr int kKc = 64;        // K chunk
 constexpr int kRowWords = kKc / 2 + 1;   // a staged weight row: 32 bf16 pairs and one pad word
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 __global__ void __launch_bounds__(kReqs * 32)
 gru_kernel(const GruParams g, const int k) {
-    __shared__ uint32_t Ws[6][kUnits][kRowWords];   // gate rows of W_ih (0..2) and W_hh (3..5)
-    __shared__ float xs[kReqs][kKc];
+    __shared__ uint32_t Ws[3][kUnits][kRowWords];
     __shared__ float hs[kReqs][kKc];
     __shared__ int s_x[kReqs];
 
@@ -61,59 +111,59 @@ gru_kernel(const GruParams g, const int k) {
         int x = -1;
         if (bb < B) {
             x = (k == 1) ? g.anchor[bb] : g.draft_tok[(size_t)bb * g.gamma + (k - 2)];
-            if (x < 0 || x >= g.V) { raise_status(g.status, kBadToken); x = -1; }   // zero input row
+            if (x < 0 || x >= g.V) { raise_status(g.status, kBadToken); x = -1; }   // no input projection
         }
         s_x[threadIdx.x] = x;
     }
 
-    float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float acc[3] = {0.f, 0.f, 0.f};
     for (int kc = 0; kc < r; kc += kKc) {
         __syncthreads();   // s_x ready / the previous chunk fully read
-        // weight rows: 6 gates x 32 units x 32 words, 16-byte loads
-        for (int i = threadIdx.x; i < 6 * kUnits * (kKc / 8); i += blockDim.x) {
+        for (int i = threadIdx.x; i < 3 * kUnits * (kKc / 8); i += blockDim.x) {
             const int seg = i % (kKc / 8), row = i / (kKc / 8), gate = row / kUnits, u = row % kUnits;
-            const uint16_t* Wm = gate < 3 ? g.W_ih : g.W_hh;
-            const int grow = (gate % 3) * r + j0 + u;
-            const uint4 w = *reinterpret_cast<const uint4*>(Wm + (size_t)grow * r + kc + 8 * seg);
+            const uint4 w = *reinterpret_cast<const uint4*>(g.W_hh + (size_t)(gate * r + j0 + u) * r + kc + 8 * seg);
             uint32_t* dst = &Ws[gate][u][4 * seg];
             dst[0] = w.x; dst[1] = w.y; dst[2] = w.z; dst[3] = w.w;
         }
-        // x and h chunks of the CTA's requests
         for (int i = threadIdx.x; i < kReqs * kKc; i += blockDim.x) {
             const int q = i / kKc, c = i % kKc, bb = b0 + q;
-            float xv = 0.f, hv = 0.f;
-            if (bb < B) {
-                const int x = s_x[q];
-                if (x >= 0) xv = __uint_as_float((uint32_t)g.E[(size_t)x * r + kc + c] << 16);
-                hv = hprev ? hprev[(size_t)bb * r + kc + c] : g.s0[kc + c];
-            }
-            xs[q][c] = xv;
+            float hv = 0.f;
+            if (bb < B) hv = hprev ? hprev[(size_t)bb * r + kc + c] : g.s0[kc + c];
             hs[q][c] = hv;
         }
         __syncthreads();
 #pragma unroll 4
         for (int c2 = 0; c2 < kKc / 2; ++c2) {
-            const float x0 = xs[warp][2 * c2], x1 = xs[warp][2 * c2 + 1];
             const float h0 = hs[warp][2 * c2], h1 = hs[warp][2 * c2 + 1];
 #pragma unroll
             for (int gt = 0; gt < 3; ++gt) {
-                const uint32_t wi = Ws[gt][lane][c2], wh = Ws[3 + gt][lane][c2];
-                acc[gt] = fmaf(bf16_lo(wi), x0, fmaf(bf16_hi(wi), x1, acc[gt]));
-                acc[3 + gt] = fmaf(bf16_lo(wh), h0, fmaf(bf16_hi(wh), h1, acc[3 + gt]));
+                const uint32_t wh = Ws[gt][lane][c2];
+                acc[gt] = fmaf(bf16_lo(wh), h0, fmaf(bf16_hi(wh), h1, acc[gt]));
             }
         }
     }
     if (b >= B || j >= r) return;
-    const float gi_r = acc[0] + g.b_ih[j], gi_z = acc[1] + g.b_ih[r + j], gi_n = acc[2] + g.b_ih[2 * r + j];
-    const float gh_r = acc[3] + g.b_hh[j], gh_z = acc[4] + g.b_hh[r + j], gh_n = acc[5] + g.b_hh[2 * r + j];
-    const float rg = 1.f / (1.f + expf(-(gi_r + gh_r)));
-    const float zg = 1.f / (1.f + expf(-(gi_z + gh_z)));
-    const float ng = tanhf(gi_n + rg * gh_n);
+    const int x = s_x[warp];
+    float gi[3] = {0.f, 0.f, 0.f};
+    if (x >= 0) {
+        const float* Pr = g.P + (size_t)x * 3 * r;
+        gi[0] = Pr[j]; gi[1] = Pr[r + j]; gi[2] = Pr[2 * r + j];
+    }
+    const float rg = 1.f / (1.f + expf(-(gi[0] + acc[0] + g.b_hh[j])));
+    const float zg = 1.f / (1.f + expf(-(gi[1] + acc[1] + g.b_hh[r + j])));
+    const float ng = tanhf(gi[2] + rg * (acc[2] + g.b_hh[2 * r + j]));
     const float hj = hprev ? hprev[(size_t)b * r + j] : g.s0[j];
     g.state[((size_t)(k - 1) * B + b) * r + j] = (1.f - zg) * ng + zg * hj;
 }
 
 }  // namespace
+
+cudaError_t launch_rnn_input_table(const uint16_t* E, const uint16_t* W_ih, const float* b_ih, int V, int r,
+                                   float* P, cudaStream_t s) {
+    const dim3 grid((unsigned)((3 * r + kTT - 1) / kTT), (unsigned)((V + kTT - 1) / kTT));
+    rnn_input_table_kernel<<<grid, 256, 0, s>>>(E, W_ih, b_ih, V, r, P);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gru(const GruParams& g, int k, cudaStream_t s) {
     const dim3 grid((unsigned)((g.r + kUnits - 1) / kUnits), (unsigned)((g.B + kReqs - 1) / kReqs));
