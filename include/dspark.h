@@ -191,6 +191,28 @@ dspark_status dspark_verify(
     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * dspark_verify with the draft's own logits: draft_logits [B,gamma,V] fp32 is
+ * the z / tau that dspark_draft_markov wrote to its logits_out for these
+ * drafts.  The residual draw of a rejected position reads its row there
+ * instead of rebuilding it from W1, W2 and U, which saves a pass over W2 when
+ * B * gamma * V is small enough to store (the latency path).  Otherwise
+ * identical to dspark_verify (same outputs, same random streams).
+ */
+dspark_status dspark_verify_logits(
+    const void* target, dspark_dtype target_t,
+    const void* U, dspark_dtype U_t,
+    const void* W1, const void* W2, dspark_dtype W_t,
+    const float* draft_logits,
+    const int32_t* anchor, const int32_t* draft_tok,
+    const float* lse_q, const float* z_tok, const int32_t* K,
+    int B, int gamma, int V, int r, int req_base, float tau,
+    uint64_t seed, uint64_t step,
+    int32_t* accepted, int32_t* out_tok, int32_t* out_req, int32_t* out_pos,
+    int32_t* out_off, int32_t* next_anchor,
+    float* p_tok, uint32_t* near_ties,
+    void* ws, size_t ws_bytes, void* stream);
+
+/*
  * The draft loop with the RNN head [P2 §RNN Head：长程依赖], [P4 §三] in place
  * of the Markov head.  A GRU state carries every token of the block so far:
  *     s_k = GRU(s_{k-1}, E[x~_{k-1}])   (s_0 learned, x~_0 = anchor[b])

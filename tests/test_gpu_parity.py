@@ -407,3 +407,39 @@ def test_draft_single_launch_matches_per_position_launches(monkeypatch):
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_allclose(a[1], b[1], atol=LOGIT_ATOL, rtol=0)
     np.testing.assert_allclose(a[2], b[2], atol=LOGIT_ATOL, rtol=0)
+
+
+@pytest.mark.parametrize("B,V,r,wdt", [(1, 151936, 256, torch.bfloat16), (3, 4104, 64, torch.bfloat16),
+                                       (5, 2048, 32, torch.float32)])
+def test_verify_from_stored_draft_logits(B, V, r, wdt):
+    """dspark_verify_logits: the residual draw reads the rejected row from the
+    draft's own stored logits; checked against the oracle on the device's drafts."""
+    w = workload.custom("tiny", B=B, V=V, r=r, w_dtype=wdt, w_std=0.1, seed=B * 7 + r)
+    inp = workload.inputs(w, device=DEV)
+    seed = B + 3
+    ws = vm.Workspace(w.B, w.gamma, w.V, w.r)
+    buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
+    logits = torch.empty((w.B, w.gamma, w.V), device=DEV)
+    vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok, ws,
+                           seed=seed, logits_out=logits)
+    K = np.random.default_rng(seed).integers(0, w.gamma + 1, w.B).astype(np.int32)
+    K[0] = w.gamma
+    vm.dspark_verify_logits(inp["target"], inp["U"], inp["W1"], inp["W2"], logits, inp["anchor"], buf.draft_tok,
+                            buf.lse_q, buf.z_tok, torch.tensor(K, device=DEV), buf.accepted, buf.out_tok,
+                            buf.out_req, buf.out_pos, buf.out_off, buf.next_anchor, ws, seed=seed, p_tok=buf.p_tok,
+                            near_ties=buf.near_ties)
+    st, bits = vm.dspark_sync_status(ws.buf)
+    assert st == 0, bits
+    ci = _cpu(inp)
+    tok = buf.draft_tok.cpu().numpy()
+    ref = oracle.verify(ci["target"], ci["U"], ci["W1"], ci["W2"], ci["anchor"], tok, K, seed=seed)
+    acc = buf.accepted.cpu().numpy()
+    bad = acc != ref["accepted"]
+    for b in np.nonzero(bad)[0]:
+        assert ref["diag"][b, 0] < U_EPS, f"unflagged accept mismatch at request {b}"
+    off = buf.out_off.cpu().numpy()
+    fin = buf.out_tok.cpu().numpy()[off[1:] - 1]
+    for b in range(w.B):
+        if not bad[b] and fin[b] != ref["final_tok"][b]:
+            assert ref["diag"][b, 1] < GAP_EPS, f"unflagged final-token mismatch at request {b}"
+    assert (np.diff(off) == acc + 1).all()

@@ -20,11 +20,12 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_rnn_input_table", "rnn_prepare", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
+    "dspark_schedule", "dspark_verify", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_verify_logits", "dspark_rnn_input_table", "rnn_prepare", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
 SCHED_OFF, SCHED_SYNC, SCHED_ASYNC = 0, 1, 2
+STORE_LOGITS_BYTES = 64 << 20   # StepBuffers keeps the draft logits up to this size
 _F32, _BF16 = 0, 1
 
 lib_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libdspark.so")
@@ -62,6 +63,10 @@ _lib.dspark_draft_rnn.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
 _lib.dspark_rnn_input_table.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp]
 _lib.dspark_rnn_input_table.restype = _i
 _lib.dspark_draft_rnn.restype = _i
+_lib.dspark_verify_logits.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _i, _i, _i, _i, _i, _f, _u64, _u64,
+                                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_verify_logits.restype = _i
 _lib.dspark_verify_rnn.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
                                    _i, _i, _i, _i, _i, _f, _u64, _u64,
                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
@@ -280,6 +285,24 @@ def dspark_draft_rnn(U, rnn, W2, anchor, draft_tok, lse_q, z_tok, state, ws: Wor
         _p(state), ws.ptr(), ws.nbytes(), _stream(stream)))
 
 
+def dspark_verify_logits(target, U, W1, W2, draft_logits, anchor, draft_tok, lse_q, z_tok, K, accepted, out_tok,
+                         out_req, out_pos, out_off, next_anchor, ws: Workspace, *, tau=1.0, seed=0, step=0,
+                         req_base=0, p_tok=None, near_ties=None, stream=None):
+    """dspark_verify reading rejected rows from the draft's stored logits
+    draft_logits [B, gamma, V] (the draft's logits_out)."""
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if tuple(target.shape) != (B, gamma + 1, V) or tuple(draft_logits.shape) != (B, gamma, V):
+        raise ValueError("target must be [B, gamma+1, V] and draft_logits [B, gamma, V]")
+    if out_tok.numel() < B * (gamma + 1) or out_off.numel() != B + 1:
+        raise ValueError("output buffers too small")
+    _check("dspark_verify_logits", _lib.dspark_verify_logits(
+        _p(target), _dt(target), _p(U), _dt(U), _p(W1), _p(W2), _dt(W1), _p(draft_logits), _p(anchor),
+        _p(draft_tok), _p(lse_q), _p(z_tok), _p(K), B, gamma, V, r, req_base, float(tau), int(seed), int(step),
+        _p(accepted), _p(out_tok), _p(out_req), _p(out_pos), _p(out_off), _p(next_anchor),
+        _p(p_tok), _p(near_ties), ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
 def dspark_verify_rnn(target, U, state, W2, anchor, draft_tok, lse_q, z_tok, K, accepted, out_tok, out_req,
                       out_pos, out_off, next_anchor, ws: Workspace, *, tau=1.0, seed=0, step=0, req_base=0,
                       p_tok=None, near_ties=None, stream=None):
@@ -338,6 +361,9 @@ class StepBuffers:
         self.p_tok = torch.empty((B, gamma), **f32)
         self.near_ties = torch.zeros((4,), dtype=torch.int32, device=device)
         self.state = torch.empty((gamma, B, r), **f32)    # RNN head states s_1..s_gamma
+        # the draft's logits, kept when small enough: the residual draw then
+        # reads the rejected row instead of rebuilding it (the latency path)
+        self.logits = (torch.empty((B, gamma, V), **f32) if B * gamma * V * 4 <= STORE_LOGITS_BYTES else None)
         self.ws = Workspace(B, gamma, V, r, device)
 
 
@@ -351,7 +377,8 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
                          buf.state, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, stream=stream)
     elif head == "markov":
         dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
-                            buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, stream=stream)
+                            buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, logits_out=buf.logits,
+                            stream=stream)
     else:
         raise ValueError(f"unknown head {head!r}")
     dspark_confidence_sts(inp["h"], inp["emb"], inp["anchor"], buf.draft_tok, inp["w_c"], inp["b_c"], inp["T"],
@@ -363,6 +390,12 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
                           buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
                           buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
                           p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
+    elif buf.logits is not None:
+        dspark_verify_logits(inp["target"], inp["U"], inp["W1"], inp["W2"], buf.logits, inp["anchor"],
+                             buf.draft_tok, buf.lse_q, buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req,
+                             buf.out_pos, buf.out_off, buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step,
+                             req_base=req_base, p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties,
+                             stream=stream)
     else:
         dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
                       buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,

@@ -220,7 +220,8 @@ dspark_status dspark_schedule(const float* log_surv, const float* log_surv_hist,
 }
 
 static dspark_status verify_impl(const void* target, dspark_dtype target_t, const void* U, dspark_dtype U_t,
-                                 const void* W1, const float* state, const void* W2, dspark_dtype W_t,
+                                 const void* W1, const float* state, const float* zlog, const void* W2,
+                                 dspark_dtype W_t,
                                  const int32_t* anchor, const int32_t* draft_tok, const float* lse_q,
                                  const float* z_tok, const int32_t* K, int B, int gamma, int V, int r,
                                  int req_base, float tau, uint64_t seed, uint64_t step, int32_t* accepted,
@@ -252,7 +253,9 @@ static dspark_status verify_impl(const void* target, dspark_dtype target_t, cons
     p.out_off = out_off; p.next_anchor = next_anchor; p.p_tok = p_tok; p.near_ties = near_ties;
     p.ws = ws_ptrs(ws, B, gamma, V);
     p.state = state;
-    if (state && !resid_rows_supported(p)) return DSPARK_ERR_UNSUPPORTED;
+    p.zlog = zlog;
+    if (zlog && (!is_device_ptr(zlog) || !aligned(zlog, 16))) return DSPARK_ERR_INVALID;
+    if (state && !zlog && !resid_rows_supported(p)) return DSPARK_ERR_UNSUPPORTED;
     return launch_status(launch_verify(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -263,9 +266,23 @@ dspark_status dspark_verify(const void* target, dspark_dtype target_t, const voi
                             uint64_t seed, uint64_t step, int32_t* accepted, int32_t* out_tok,
                             int32_t* out_req, int32_t* out_pos, int32_t* out_off, int32_t* next_anchor,
                             float* p_tok, uint32_t* near_ties, void* ws, size_t ws_bytes, void* stream) {
-    return verify_impl(target, target_t, U, U_t, W1, nullptr, W2, W_t, anchor, draft_tok, lse_q, z_tok, K, B,
+    return verify_impl(target, target_t, U, U_t, W1, nullptr, nullptr, W2, W_t, anchor, draft_tok, lse_q, z_tok, K, B,
                        gamma, V, r, req_base, tau, seed, step, accepted, out_tok, out_req, out_pos, out_off,
                        next_anchor, p_tok, near_ties, ws, ws_bytes, stream);
+}
+
+dspark_status dspark_verify_logits(const void* target, dspark_dtype target_t, const void* U, dspark_dtype U_t,
+                                   const void* W1, const void* W2, dspark_dtype W_t, const float* draft_logits,
+                                   const int32_t* anchor, const int32_t* draft_tok, const float* lse_q,
+                                   const float* z_tok, const int32_t* K, int B, int gamma, int V, int r,
+                                   int req_base, float tau, uint64_t seed, uint64_t step, int32_t* accepted,
+                                   int32_t* out_tok, int32_t* out_req, int32_t* out_pos, int32_t* out_off,
+                                   int32_t* next_anchor, float* p_tok, uint32_t* near_ties, void* ws,
+                                   size_t ws_bytes, void* stream) {
+    if (!draft_logits) return DSPARK_ERR_INVALID;
+    return verify_impl(target, target_t, U, U_t, W1, nullptr, draft_logits, W2, W_t, anchor, draft_tok, lse_q,
+                       z_tok, K, B, gamma, V, r, req_base, tau, seed, step, accepted, out_tok, out_req, out_pos,
+                       out_off, next_anchor, p_tok, near_ties, ws, ws_bytes, stream);
 }
 
 dspark_status dspark_verify_rnn(const void* target, dspark_dtype target_t, const void* U, dspark_dtype U_t,
@@ -276,7 +293,7 @@ dspark_status dspark_verify_rnn(const void* target, dspark_dtype target_t, const
                                 int32_t* out_req, int32_t* out_pos, int32_t* out_off, int32_t* next_anchor,
                                 float* p_tok, uint32_t* near_ties, void* ws, size_t ws_bytes, void* stream) {
     if (!state) return DSPARK_ERR_INVALID;
-    return verify_impl(target, target_t, U, U_t, nullptr, state, W2, W_t, anchor, draft_tok, lse_q, z_tok, K, B,
+    return verify_impl(target, target_t, U, U_t, nullptr, state, nullptr, W2, W_t, anchor, draft_tok, lse_q, z_tok, K, B,
                        gamma, V, r, req_base, tau, seed, step, accepted, out_tok, out_req, out_pos, out_off,
                        next_anchor, p_tok, near_ties, ws, ws_bytes, stream);
 }

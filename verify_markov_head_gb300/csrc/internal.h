@@ -118,6 +118,7 @@ struct VerifyParams {
     float* p_tok; uint32_t* near_ties;
     WsPtrs ws;
     const float* state = nullptr;   // RNN head bias rows (see DraftParams)
+    const float* zlog = nullptr;    // the draft's stored logits [B][gamma][V] (z / tau), or null
 };
 
 struct StsFitParams {

@@ -344,13 +344,16 @@ constexpr int kTV = 128;
 constexpr int kBC = dspark::kChunk;   // requests per residual chunk
 constexpr int kResThreads = 256;
 
-template <typename WT, typename UT, typename TT>
+// kStored: the draft logits z [B][gamma][V] (already divided by tau) were
+// stored by the draft (p.zlog): the rejected row is read from there instead
+// of being rebuilt from W1, W2 and U.
+template <typename WT, typename UT, typename TT, bool kStored = false>
 __global__ void __launch_bounds__(kResThreads)
 verify_residual_simt_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) float smem[];
     const int r = p.r, V = p.V, gamma = p.gamma;
-    float* sh = smem;                         // [kBC][r]
-    float* tile = smem + kBC * r;             // [kBC][kTV + 4] draft logits z
+    float* sh = smem;                                   // [kBC][r] (not in the stored mode)
+    float* tile = smem + (kStored ? 0 : kBC * r);       // [kBC][kTV + 4] draft logits z
     constexpr int kLd = kTV + 4;
     __shared__ int s_row[kBC];
     __shared__ int s_any;
@@ -374,7 +377,7 @@ verify_residual_simt_kernel(const VerifyParams p) {
     const int bl_e = tid / 16, seg = tid % 16;
     Draw2 st = draw2_empty();
     if (s_any) {
-        for (int i = tid; i < kBC * r; i += kResThreads) {
+        for (int i = tid; i < (kStored ? 0 : kBC * r); i += kResThreads) {
             const int bl = i / r, rho = i - bl * r;
             float v = 0.f;
             const int row = s_row[bl];
@@ -399,7 +402,7 @@ verify_residual_simt_kernel(const VerifyParams p) {
             float acc[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-            if (v < V) {
+            if (!kStored && v < V) {
                 const float* hb = sh + (bh * 8) * r;
                 for (int rho = 0; rho < r; ++rho) {
                     const float w = to_f32(W2[(size_t)rho * V + v]);
@@ -412,8 +415,12 @@ verify_residual_simt_kernel(const VerifyParams p) {
                 const int bl = bh * 8 + j;
                 const int row = s_row[bl];
                 float z = 0.f;
-                if (row >= 0 && v < V)
-                    z = (to_f32(U[((size_t)(b0 + bl) * gamma + row) * V + v]) + acc[j]) * p.inv_tau;
+                if (row >= 0 && v < V) {
+                    if constexpr (kStored)
+                        z = p.zlog[((size_t)(b0 + bl) * gamma + row) * V + v];
+                    else
+                        z = (to_f32(U[((size_t)(b0 + bl) * gamma + row) * V + v]) + acc[j]) * p.inv_tau;
+                }
                 tile[bl * kLd + v_local] = z;
             }
             __syncthreads();
@@ -560,6 +567,14 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     gx = gx > p.ws.parts ? p.ws.parts : gx;
     const size_t smem = sizeof(float) * ((size_t)kBC * p.r + (size_t)kBC * (kTV + 4));
     const dim3 g2(gx, nchunks);
+    if (p.zlog) {
+        // the draft's own logits: the rejected rows are read, not rebuilt
+        auto kern = verify_residual_simt_kernel<float, float, TT, true>;
+        const size_t smem_z = sizeof(float) * (size_t)kBC * (kTV + 4);
+        kern<<<g2, kResThreads, smem_z, s>>>(p);
+        verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
     if (p.state && !resid_rows_supported(p)) return cudaErrorNotSupported;   // RNN rows: tensor-core path only
     if (p.state || (resid_rows_supported(p) && !getenv("DSPARK_RESID_SIMT"))) {
         const cudaError_t e = launch_resid_rows(p, s);
