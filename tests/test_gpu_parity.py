@@ -102,6 +102,7 @@ def test_tiny_workload_all_scheduler_modes(mode):
     (1, 1024, 32, torch.float32),
     (5, 4104, 64, torch.float32),        # ragged last tile (4104 = 32*128 + 8)
     (1, 2048, 256, torch.bfloat16),
+    (1, 4104, 64, torch.bfloat16),       # one request, ragged vocabulary tail
     (3, 4104, 256, torch.bfloat16),
     (17, 1032, 128, torch.bfloat16),     # ragged request chunk
     (64, 4096, 256, torch.bfloat16),

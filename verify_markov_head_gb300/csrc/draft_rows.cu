@@ -399,7 +399,12 @@ __device__ __forceinline__ void gate_step(const GruParams& g, int ks, int cta, i
 // reaches before its merges of k are done.
 // 19 warps over 4 schedulers put 5 warps on three of them, whose 16384
 // registers then allow 96 a thread.
-template <bool kResid, typename TT, bool kRnn = false>
+// kOneRow (B = 1, the latency case): the chunk holds one request, so only
+// lane 0 of the warps on its TMEM rows carries data.  Those warps spread each
+// tile's 32 columns of that row over their lanes (one shuffle per column) and
+// every lane races its own column; the lanes' partial states are merged at
+// the end of the position.
+template <bool kResid, typename TT, bool kRnn = false, bool kOneRow = false>
 __global__ void __launch_bounds__(kThreads, 1)
 rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_last) {
     const DraftParams& p = a.p;
@@ -680,6 +685,9 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             const StreamRK rng(p.seed, p.step, kResid ? 2u : 0u,
                                (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)urow);
             const size_t out_row = ((size_t)b * gamma + (k - 1)) * V;
+            // kOneRow: every lane works on the chunk's one request
+            const StreamRK rng1(p.seed, p.step, 0u, (uint32_t)(p.req_base + b_base) * (uint32_t)(gamma + 1) + (uint32_t)(k - 1));
+            const size_t out_row1 = ((size_t)b_base * gamma + (k - 1)) * V;
             const float* Urow = static_cast<const float*>(p.U) + ((size_t)b * gamma + urow) * V;
             const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + urow) * V;
             float2 lse = make_float2(0.f, 0.f);
@@ -795,6 +803,33 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         }
                     }
                     __syncwarp();
+                } else if (kOneRow && active) {
+                    // lane c takes column c of the row lane 0 loaded
+                    float u = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float x = __shfl_sync(0xffffffffu, bias[c], 0);
+                        if (lane == c) u = x;
+                    }
+                    const int v = v0 + lane;
+                    if (v < V) {
+                        if (p.logits_out) p.logits_out[out_row1 + v] = u * p.inv_tau;
+                        const uint4 w = rng1.quad((uint32_t)v >> 2);
+                        const uint32_t wd = (v & 2) ? ((v & 1) ? w.w : w.z) : ((v & 1) ? w.y : w.x);
+                        const float te = fast_exp2(fmaf(u, scale2, -rz2));
+                        if (one_minus_uniform_of(wd) < fmaf(rE2h * kLn2, te, kRaceSlack)) {
+                            const float E2 = exp2_variate_of(wd);
+                            if (E2 < rE2 * te) {
+                                st.s = st.s * fast_exp2(fmaf(-u, scale2, rz2)) + 1.f;
+                                rz2 = u * scale2; rE2 = E2; rE2h = E2 * kRaceRel;
+                                st.idx = v; st.zb = u;
+                            } else {
+                                st.s += te;
+                            }
+                        } else {
+                            st.s += te;
+                        }
+                    }
                 } else if (real) {
                     // The accumulator holds z*tau = U + h.W2 (it started as the tile's U).
                     // Exponential race in base-2 units: the winner minimises
@@ -863,6 +898,12 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     sn.best = sn.zb - logf(E);
                     sn.s = st.s * E;
                     sn.idx = st.idx;
+                }
+                if constexpr (kOneRow) {
+                    // the lanes raced columns of the one request: merge them into lane 0's row
+#pragma unroll
+                    for (int m = 16; m > 0; m >>= 1) sn = drawlse_merge(sn, shfl_xor(sn, m));
+                    if (lane != 0) sn = drawlse_empty();
                 }
                 s_merge[cb * 128 + row] = sn;
             }
@@ -1145,7 +1186,8 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
     const Layout L = rows_layout(a.NC, p.r, resid);
     const size_t smem = L.total + 1024;
     auto kern = resid ? (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>)
-                      : (gru ? rows_kernel<false, float, true> : rows_kernel<false, float>);
+                      : (gru ? rows_kernel<false, float, true>
+                             : (p.B == 1 ? rows_kernel<false, float, false, true> : rows_kernel<false, float>));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nchunks = (p.B + a.NC - 1) / a.NC;
