@@ -208,7 +208,14 @@ verify_stream_kernel(const VerifyParams p) {
                 for (int e = 0; e < kPerThread; ++e) s4[e & 3] += fast_exp2(fmaf(x[e], scale, -m2));
             }
             if (bonus) {
+                // Gumbel-max as an exponential race against this thread's chunk
+                // maximum cm: argmax x/tau + G = argmin E2 * 2^(cm - x*log2e/tau),
+                // E2 = -log2 u (no outer logarithm, no divergent screen); the
+                // chunk's winner goes back to a score for the running draw:
+                //   x/tau + G = cm ln2 - ln(key ln2).
                 const StreamRK rng(p.seed, p.step, 3u, (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)i);
+                float kbest = INFINITY;
+                int kidx = 0x7fffffff;
 #pragma unroll
                 for (int j = 0; j < kPerThread / 4; ++j) {
                     const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
@@ -218,10 +225,14 @@ verify_stream_kernel(const VerifyParams p) {
                         const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float sc = x[4 * j + e] * p.inv_tau + gumbel_of(ws[e]);   // x/tau + G
-                            if (wins(sc, v + e, best, bidx)) { best = sc; bidx = v + e; }
+                            const float key = exp2_variate_of(ws[e]) * fast_exp2(fmaf(-x[4 * j + e], scale, cm));
+                            if (key < kbest) { kbest = key; kidx = v + e; }   // increasing v: lowest index on ties
                         }
                     }
+                }
+                if (kbest < INFINITY) {
+                    const float sc = cm * kLn2 - logf(kbest * kLn2);
+                    if (wins(sc, kidx, best, bidx)) { best = sc; bidx = kidx; }
                 }
             }
         }
