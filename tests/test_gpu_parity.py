@@ -127,6 +127,18 @@ def test_draft_temperature_and_request_base():
     compare_draft(tok, ref["tok"], ref["gap"])
 
 
+def test_draft_one_request_temperature_and_request_base():
+    """B = 1 takes the one-request epilogue (every lane races one column)."""
+    w = workload.custom("tiny", B=1, V=2056, r=128, w_dtype=torch.bfloat16, seed=12)
+    inp = workload.inputs(w, device=DEV)
+    _check_draft(inp, w, seed=21, tau=0.7)
+    tok, lse, zt, _ = _draft_gpu(inp, w.B, w.gamma, w.V, w.r, seed=21, req_base=40)
+    ci = _cpu(inp)
+    ref = oracle.draft_markov(ci["U"], ci["W1"], ci["W2"], ci["anchor"], seed=21, req=[40])
+    compared, flagged, valid = compare_draft(tok, ref["tok"], ref["gap"])
+    assert_close_where(lse, ref["lse_q"], valid, atol=LOGIT_ATOL, what="lse_q")
+
+
 def test_draft_gamma_one_and_sixteen():
     for g in (1, 16):
         w = workload.custom("tiny", B=2, V=1024, r=32, gamma=g, seed=g)
