@@ -204,8 +204,17 @@ verify_stream_kernel(const VerifyParams p) {
                 m2 = cm;
             }
             if (m2 > -INFINITY) {
+                // two entries per packed multiply-add and add
+                const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m2, -m2);
+                float2 a01 = make_float2(s4[0], s4[1]), a23 = make_float2(s4[2], s4[3]);
 #pragma unroll
-                for (int e = 0; e < kPerThread; ++e) s4[e & 3] += fast_exp2(fmaf(x[e], scale, -m2));
+                for (int e = 0; e < kPerThread; e += 4) {
+                    const float2 y01 = __ffma2_rn(make_float2(x[e], x[e + 1]), sc2, nm2);
+                    const float2 y23 = __ffma2_rn(make_float2(x[e + 2], x[e + 3]), sc2, nm2);
+                    a01 = __fadd2_rn(a01, make_float2(fast_exp2(y01.x), fast_exp2(y01.y)));
+                    a23 = __fadd2_rn(a23, make_float2(fast_exp2(y23.x), fast_exp2(y23.y)));
+                }
+                s4[0] = a01.x; s4[1] = a01.y; s4[2] = a23.x; s4[3] = a23.y;
             }
             if (bonus) {
                 // Gumbel-max as an exponential race against this thread's chunk
