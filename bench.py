@@ -181,7 +181,8 @@ def run_gpu(args):
             vm.run_step_dp(inp, buf, sched, mode=mode, seed=seed, step=0, stream=stream)
     else:
         def one_step():
-            vm.run_step(inp, buf, mode=mode, seed=seed, step=0, req_base=req_base, stream=stream, head=head)
+            vm.run_step(inp, buf, mode=mode, seed=seed, step=0, req_base=req_base, stream=stream, head=head,
+                        fuse_target=args.fuse_target)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -229,7 +230,10 @@ def run_gpu(args):
     emitted_all = _sum_over_ranks(dist, emitted, dev)
     value = emitted_all / (ms_max / 1e3)
 
-    # ---- dominant kernel: the draft call, timed alone on the same stream
+    # ---- dominant kernel: the draft call, timed alone on the same stream (with
+    #      the scheduler off the step drafts with the target stream: the call
+    #      run_step makes)
+    fused = args.fuse_target and head == "markov" and mode == 0 and vm.target_stream_supported(inp)
     if head == "rnn":
         draft_launches = gamma        # one draft launch per position (plus a GRU launch each)
     else:
@@ -242,6 +246,10 @@ def run_gpu(args):
             if head == "rnn":
                 vm.dspark_draft_rnn(inp["U"], inp["rnn"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
                                     buf.z_tok, buf.state, buf.ws, seed=seed, req_base=req_base, stream=stream)
+            elif fused:
+                vm.dspark_draft_markov_target(inp["U"], inp["W1"], inp["W2"], inp["target"], inp["anchor"],
+                                              buf.draft_tok, buf.lse_q, buf.z_tok, buf.ws, seed=seed,
+                                              req_base=req_base, logits_out=buf.logits, stream=stream)
             else:
                 vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
                                        buf.z_tok, buf.ws, seed=seed, req_base=req_base, stream=stream)
@@ -250,8 +258,10 @@ def run_gpu(args):
     draft_launch_ms = d0.elapsed_time(d1) / (reps * draft_launches)
     w2_bytes = r * V * inp["W2"].element_size()
     u_bytes_k = B * V * inp["U"].element_size()
-    # per position: W2 once + one row block of U; a launch covers gamma / draft_launches positions
-    draft_bytes = (w2_bytes + u_bytes_k) * gamma // draft_launches
+    t_bytes_k = B * V * inp["target"].element_size() if fused else 0
+    # per position: W2 once + one row block of U (and of the target); a launch
+    # covers gamma / draft_launches positions
+    draft_bytes = (w2_bytes + u_bytes_k + t_bytes_k) * gamma // draft_launches
     peak, peak_kind = _peaks()
     achieved = draft_bytes / (draft_launch_ms / 1e3) / 1e9
     formula_bytes = gamma * w2_bytes + inp["U"].numel() * inp["U"].element_size() + \
@@ -267,14 +277,14 @@ def run_gpu(args):
     e2e_steps = max(3, min(args.steps, 20))
     pipe = vm.HostPipeline(inp, buf, stream)
     for _ in range(2):
-        pipe.step(host, host_out, mode=mode, seed=seed, head=head)
+        pipe.step(host, host_out, mode=mode, seed=seed, head=head, fuse_target=args.fuse_target)
     torch.cuda.synchronize()
     _barrier(dist)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     pipe.copy_stream.wait_event(f0)
     for _ in range(e2e_steps):
-        h2d, d2h = pipe.step(host, host_out, mode=mode, seed=seed, head=head)
+        h2d, d2h = pipe.step(host, host_out, mode=mode, seed=seed, head=head, fuse_target=args.fuse_target)
     f1.record(stream)
     stream.synchronize()
     e2e_ms = _max_over_ranks(dist, f0.elapsed_time(f1) / e2e_steps, dev)
@@ -284,7 +294,8 @@ def run_gpu(args):
     if st != 0:
         raise SystemExit(f"device status {st} bits {bits}")
 
-    # draft, confidence, schedule, verify stream, accept walk, residual draw, compaction
+    # draft, confidence, schedule, verify stream (bonus rows only when fused), accept walk,
+    # residual draw, compaction
     launches_per_step = draft_launches * (2 if head == "rnn" else 1) + 6
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -302,7 +313,9 @@ def run_gpu(args):
             "emitted_tokens_per_step": emitted_all, "drafted_tokens_per_step": B * gamma * world,
             "step_formula_bytes": formula_bytes, "step_formula_gbs": step_gbs,
             "step_formula_frac": step_gbs / peak,
-            "roofline": {"kernel": ("rows_kernel<draft> (dspark_draft_markov, %d position(s) per launch)"
+            "roofline": {"kernel": ("rows_kernel<draft, target stream> (dspark_draft_markov_target, %d "
+                                    "position(s) per launch)" % (gamma // draft_launches)) if fused else
+                                   ("rows_kernel<draft> (dspark_draft_markov, %d position(s) per launch)"
                                     % (gamma // draft_launches)) if head == "markov" else
                                    "gru_kernel + rows_kernel<draft> per position (dspark_draft_rnn); "
                                    "launch_ms = the two launches of one position",
@@ -716,6 +729,9 @@ def main():
                     help="time the workload's chained steps (b512: 16 steps, async scheduler) instead of one step")
     ap.add_argument("--head", default="markov", choices=["markov", "rnn"],
                     help="draft head: the Markov head (default) or the RNN head")
+    ap.add_argument("--fuse-target", action="store_true",
+                    help="scheduler off: draft with the target stream (dspark_draft_markov_target) and verify "
+                         "in full-prefix mode")
     ap.add_argument("--sts", action="store_true",
                     help="time the STS temperature fit (2^20 validation blocks, 256 temperatures)")
     ap.add_argument("--sts-blocks", type=int, default=None,

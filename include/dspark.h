@@ -114,6 +114,32 @@ dspark_status dspark_draft_markov(
     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The draft of dspark_draft_markov fused with the first pass of a full-prefix
+ * verification [P2 §形式化定义] (every draft position is checked against the
+ * target's distribution at that position).  While position k streams U[b,k-1,:], the same launch streams
+ * target[b,k-1,:] and reduces it to partial log-sum-exps of target/tau,
+ * kept in ws; a following dspark_verify or dspark_verify_logits with K = NULL
+ * uses them instead of reading rows 0..gamma-1 of the target again.
+ * Inputs : those of dspark_draft_markov, plus target [B,gamma+1,V] fp32
+ *          (target_t = DSPARK_F32; row gamma, the bonus row, is not read here).
+ * Outputs: those of dspark_draft_markov (identical values); ws holds the
+ *          target partials and a token naming (target, seed, step, req_base,
+ *          B, gamma, V, tau).  Leave the target unchanged until the verify call.
+ * Limits : those of dspark_draft_markov's tensor-core path (bf16 weights, fp32
+ *          U, r % 64 == 0, r <= 256); otherwise, or for a bf16 target,
+ *          DSPARK_ERR_UNSUPPORTED.
+ */
+dspark_status dspark_draft_markov_target(
+    const void* U, dspark_dtype U_t,
+    const void* W1, const void* W2, dspark_dtype W_t,
+    const void* target, dspark_dtype target_t,
+    const int32_t* anchor,
+    int B, int gamma, int V, int r, int req_base, float tau,
+    uint64_t seed, uint64_t step,
+    int32_t* draft_tok, float* lse_q, float* z_tok, float* logits_out,
+    void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Step a4: confidence head, sequential temperature scaling and prefix survival
  * [P2 §置信度头：预测自己的命运, §校准问题：原始置信度不可靠], [P4 §四].
  *     s_k        = w_c . [h[b,k-1,:] ; emb[x~_{k-1},:]] + b_c
@@ -172,6 +198,12 @@ dspark_status dspark_schedule(
  *   is the last emitted token; accepted [B] = A_b.
  * Inputs : target [B,gamma+1,V] (target_t), U, W1, W2 as for the draft, anchor,
  *          draft_tok, lse_q, z_tok from dspark_draft_markov, K [B] in [0,gamma].
+ * K NULL : full prefix (every K_b = gamma) after dspark_draft_markov_target on
+ *          the same workspace, target, seed, step, req_base and tau: the
+ *          log-sum-exps of rows 0..gamma-1 come from that call, and only the
+ *          bonus rows are streamed here.  A workspace whose last target-stream
+ *          draft had other inputs sets status bit 3 (results unspecified).
+ *          Not for dspark_verify_rnn (DSPARK_ERR_UNSUPPORTED).
  * Optional: p_tok [B,gamma] receives p_k(x~_k) for walked rows (others untouched);
  *          near_ties [4] (zeroed by the caller) counts: [0] acceptance
  *          uniforms within 1e-5 of their threshold, [1] residual draws that

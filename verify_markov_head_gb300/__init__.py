@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_verify_logits", "dspark_rnn_input_table", "rnn_prepare", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
+    "dspark_schedule", "dspark_verify", "dspark_draft_markov_target", "target_stream_supported", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_verify_logits", "dspark_rnn_input_table", "rnn_prepare", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
@@ -46,6 +46,9 @@ _lib.dspark_sync_status.restype = _i
 _lib.dspark_draft_markov.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
                                      _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.dspark_draft_markov.restype = _i
+_lib.dspark_draft_markov_target.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64,
+                                            _u64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.dspark_draft_markov_target.restype = _i
 _lib.dspark_confidence_sts.argtypes = [_vp, _i, _vp, _i, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i,
                                        _vp, _vp, _vp, _sz, _vp]
 _lib.dspark_confidence_sts.restype = _i
@@ -170,6 +173,34 @@ def dspark_draft_markov(U, W1, W2, anchor, draft_tok, lse_q, z_tok, ws: Workspac
         _p(U), _dt(U), _p(W1), _p(W2), _dt(W1), _p(anchor), B, gamma, V, r, req_base, float(tau),
         int(seed), int(step), _p(draft_tok), _p(lse_q), _p(z_tok), _p(logits_out),
         ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def dspark_draft_markov_target(U, W1, W2, target, anchor, draft_tok, lse_q, z_tok, ws: Workspace, *,
+                               tau=1.0, seed=0, step=0, req_base=0, logits_out=None, stream=None):
+    """dspark_draft_markov that also reduces target rows 0..gamma-1 for a
+    full-prefix verify (dspark_verify / dspark_verify_logits with K=None,
+    same workspace, target, seed, step, req_base and tau)."""
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if W1.shape != (V, r) or W2.shape != (r, V) or W1.dtype != W2.dtype:
+        raise ValueError("W1 [V,r] and W2 [r,V] must share a dtype")
+    if tuple(target.shape) != (B, gamma + 1, V):
+        raise ValueError("target must be [B, gamma+1, V]")
+    for t, shp in ((anchor, (B,)), (draft_tok, (B, gamma)), (lse_q, (B, gamma)), (z_tok, (B, gamma))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"shape {tuple(t.shape)} != {shp}")
+    _check("dspark_draft_markov_target", _lib.dspark_draft_markov_target(
+        _p(U), _dt(U), _p(W1), _p(W2), _dt(W1), _p(target), _dt(target), _p(anchor), B, gamma, V, r, req_base,
+        float(tau), int(seed), int(step), _p(draft_tok), _p(lse_q), _p(z_tok), _p(logits_out),
+        ws.ptr(), ws.nbytes(), _stream(stream)))
+
+
+def target_stream_supported(inp: dict) -> bool:
+    """Whether dspark_draft_markov_target takes these inputs: bf16 weights
+    with r % 64 == 0 and r <= 256, fp32 U and an fp32 target."""
+    r = inp["W1"].shape[1]
+    return (inp["W1"].dtype == torch.bfloat16 and inp["U"].dtype == torch.float32
+            and inp["target"].dtype == torch.float32 and r % 64 == 0 and r <= 256)
 
 
 def dspark_confidence_sts(h, emb, anchor, draft_tok, w_c, b_c, T, conf_cal, log_surv, ws: Workspace,
@@ -368,13 +399,22 @@ class StepBuffers:
 
 
 def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_base=0, log_surv_hist=None,
-         stream=None, p_tok=False, head="markov"):
+         stream=None, p_tok=False, head="markov", fuse_target=False):
     """One whole draft + verify step (a1-a8) on device-resident inputs: the
     four ABI calls in order, all on `stream`.  head="rnn" drafts with the RNN
-    head (parameters in inp["rnn"]) and verifies against its states."""
+    head (parameters in inp["rnn"]) and verifies against its states.  With
+    the scheduler off (every K_b = gamma) and fuse_target, the Markov draft
+    also reduces the target rows it drafts against
+    (dspark_draft_markov_target) and the verify runs in full-prefix mode
+    (off by default: on one GB300 the separate verify stream is faster)."""
+    fused = fuse_target and head == "markov" and int(mode) == 0 and target_stream_supported(inp)
     if head == "rnn":
         dspark_draft_rnn(inp["U"], inp["rnn"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
                          buf.state, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, stream=stream)
+    elif fused:
+        dspark_draft_markov_target(inp["U"], inp["W1"], inp["W2"], inp["target"], inp["anchor"], buf.draft_tok,
+                                   buf.lse_q, buf.z_tok, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
+                                   logits_out=buf.logits, stream=stream)
     elif head == "markov":
         dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
                             buf.ws, tau=tau, seed=seed, step=step, req_base=req_base, logits_out=buf.logits,
@@ -385,6 +425,7 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
                           buf.conf_cal, buf.log_surv, buf.ws, stream=stream)
     dspark_schedule(buf.log_surv, inp["sps"], mode, buf.K, buf.n_total, buf.theta, buf.ws,
                     log_surv_hist=log_surv_hist, stream=stream)
+    K = None if fused else buf.K    # full-prefix mode: K_b = gamma, rows 0..gamma-1 already reduced
     if head == "rnn":
         dspark_verify_rnn(inp["target"], inp["U"], buf.state, inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
                           buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
@@ -392,13 +433,13 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
                           p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
     elif buf.logits is not None:
         dspark_verify_logits(inp["target"], inp["U"], inp["W1"], inp["W2"], buf.logits, inp["anchor"],
-                             buf.draft_tok, buf.lse_q, buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req,
+                             buf.draft_tok, buf.lse_q, buf.z_tok, K, buf.accepted, buf.out_tok, buf.out_req,
                              buf.out_pos, buf.out_off, buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step,
                              req_base=req_base, p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties,
                              stream=stream)
     else:
         dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
-                      buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
+                      buf.z_tok, K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
                       buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
                       p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
 
@@ -515,7 +556,8 @@ class HostPipeline:
         self.compute_stream.wait_stream(cur)
         self.copy_stream.wait_stream(cur)
 
-    def step(self, host_inp: dict, host_out: dict, *, mode, seed, step=0, tau=1.0, head="markov"):
+    def step(self, host_inp: dict, host_out: dict, *, mode, seed, step=0, tau=1.0, head="markov",
+             fuse_target=False):
         """Enqueue one step; returns (h2d_bytes, d2h_bytes)."""
         i = self.next
         slot = self.slots[i]
@@ -531,7 +573,7 @@ class HostPipeline:
         d2h = 0
         with torch.cuda.stream(self.compute_stream):
             run_step(slot, self.buf, mode=mode, seed=seed, step=step, tau=tau, stream=self.compute_stream,
-                     head=head)
+                     head=head, fuse_target=fuse_target)
             for name in ("out_tok", "out_off", "next_anchor"):
                 src = getattr(self.buf, name)
                 host_out[name].copy_(src, non_blocking=True)

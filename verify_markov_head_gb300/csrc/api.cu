@@ -2,6 +2,7 @@
 // checks, workspace layout and the launch sequence of each call.
 #include <cuda_runtime.h>
 #include <stdio.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -38,6 +39,8 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.vq = o;          o = align256(o + sizeof(uint32_t) * 2);
     L.draft_part = o;  o = align256(o + sizeof(DrawLse) * 2 * (size_t)B * L.parts);
     L.verify_part = o; o = align256(o + sizeof(LseDraw) * (size_t)B * (gamma + 1) * L.nseg * kVerifySub);
+    L.tgt_part = o;    o = align256(o + sizeof(LseDraw) * (size_t)B * gamma * kTgtSlots);
+    L.tgt_token = o;   o = align256(o + sizeof(unsigned long long));
     L.rej = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
     L.acc = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
     L.fin = o;         o = align256(o + sizeof(int32_t) * (size_t)B);
@@ -61,6 +64,8 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     P.vq = reinterpret_cast<uint32_t*>(base + L.vq);
     P.draft_part = reinterpret_cast<DrawLse*>(base + L.draft_part);
     P.verify_part = reinterpret_cast<LseDraw*>(base + L.verify_part);
+    P.tgt_part = reinterpret_cast<LseDraw*>(base + L.tgt_part);
+    P.tgt_token = reinterpret_cast<unsigned long long*>(base + L.tgt_token);
     P.rej = reinterpret_cast<int32_t*>(base + L.rej);
     P.acc = reinterpret_cast<int32_t*>(base + L.acc);
     P.fin = reinterpret_cast<int32_t*>(base + L.fin);
@@ -96,6 +101,25 @@ static bool sizes_ok(int B, int gamma, int V, int r) {
     if ((double)B * (gamma + 1) >= 4294967295.0) return false;
     if (B > 1000000) return false;
     return true;
+}
+
+// Identifies the inputs of a target-stream draft: the verify call in
+// full-prefix mode recomputes it and checks the one the draft left in the
+// workspace.  Odd, so a cleared workspace never matches.
+static unsigned long long tgt_token_of(const void* target, uint64_t seed, uint64_t step, int req_base, int B,
+                                       int gamma, int V, float tau) {
+    uint32_t tau_bits;
+    memcpy(&tau_bits, &tau, sizeof(tau_bits));
+    const uint64_t words[] = {(uint64_t)reinterpret_cast<uintptr_t>(target), seed, step, (uint64_t)(uint32_t)req_base,
+                              ((uint64_t)(uint32_t)B << 32) | (uint32_t)gamma, ((uint64_t)(uint32_t)V << 32) | tau_bits};
+    uint64_t h = 0x6a09e667f3bcc909ull;
+    for (uint64_t w : words) {
+        h ^= w + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        h = (h ^ (h >> 30)) * 0xbf58476d1ce4e5b9ull;
+        h = (h ^ (h >> 27)) * 0x94d049bb133111ebull;
+        h ^= h >> 31;
+    }
+    return h | 1ull;
 }
 
 }  // namespace dspark
@@ -177,6 +201,40 @@ dspark_status dspark_draft_markov(const void* U, dspark_dtype U_t, const void* W
     return launch_status(launch_draft(p, s));
 }
 
+dspark_status dspark_draft_markov_target(const void* U, dspark_dtype U_t, const void* W1, const void* W2,
+                                         dspark_dtype W_t, const void* target, dspark_dtype target_t,
+                                         const int32_t* anchor, int B, int gamma, int V, int r, int req_base,
+                                         float tau, uint64_t seed, uint64_t step, int32_t* draft_tok, float* lse_q,
+                                         float* z_tok, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
+    if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
+    if ((U_t != DSPARK_F32 && U_t != DSPARK_BF16) || (W_t != DSPARK_F32 && W_t != DSPARK_BF16) ||
+        (target_t != DSPARK_F32 && target_t != DSPARK_BF16))
+        return DSPARK_ERR_UNSUPPORTED;
+    if (!is_device_ptr(U) || !is_device_ptr(W1) || !is_device_ptr(W2) || !is_device_ptr(target) ||
+        !is_device_ptr(anchor) || !is_device_ptr(draft_tok) || !is_device_ptr(lse_q) || !is_device_ptr(z_tok) ||
+        !is_device_ptr(ws))
+        return DSPARK_ERR_INVALID;
+    if (logits_out && !is_device_ptr(logits_out)) return DSPARK_ERR_INVALID;
+    if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(target, 16) || !aligned(ws, 256))
+        return DSPARK_ERR_INVALID;
+    if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;
+    if ((double)(req_base + (double)B) * (gamma + 1) >= 4294967295.0) return DSPARK_ERR_INVALID;
+
+    DraftParams p;
+    p.U = U; p.U_bf16 = (U_t == DSPARK_BF16);
+    p.W1 = W1; p.W2 = W2; p.W_bf16 = (W_t == DSPARK_BF16);
+    p.anchor = anchor;
+    p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.req_base = req_base;
+    p.inv_tau = 1.f / tau;
+    p.seed = seed; p.step = step;
+    p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.logits_out = logits_out;
+    p.ws = ws_ptrs(ws, B, gamma, V);
+    p.target = static_cast<const float*>(target);
+    p.tgt_token = tgt_token_of(target, seed, step, req_base, B, gamma, V, tau);
+    if (target_t != DSPARK_F32 || !draft_target_supported(p)) return DSPARK_ERR_UNSUPPORTED;
+    return launch_status(launch_draft_target(p, static_cast<cudaStream_t>(stream)));
+}
+
 dspark_status dspark_confidence_sts(const float* h, int d, const void* emb, dspark_dtype emb_t, int e,
                                     const int32_t* anchor, const int32_t* draft_tok, const float* w_c,
                                     float b_c, const float* T, int B, int gamma, int V, float* conf_cal,
@@ -233,10 +291,11 @@ static dspark_status verify_impl(const void* target, dspark_dtype target_t, cons
         (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
         return DSPARK_ERR_UNSUPPORTED;
     const void* rows = state ? static_cast<const void*>(state) : W1;
-    const void* need[] = {target, U, rows, W2, anchor, draft_tok, lse_q, z_tok, K, accepted,
+    const void* need[] = {target, U, rows, W2, anchor, draft_tok, lse_q, z_tok, accepted,
                           out_tok, out_req, out_pos, out_off, next_anchor, ws};
     for (const void* q : need)
         if (!is_device_ptr(q)) return DSPARK_ERR_INVALID;
+    if (K && !is_device_ptr(K)) return DSPARK_ERR_INVALID;
     if ((p_tok && !is_device_ptr(p_tok)) || (near_ties && !is_device_ptr(near_ties))) return DSPARK_ERR_INVALID;
     if (!aligned(target, 16) || !aligned(U, 16) || !aligned(rows, 16) || !aligned(W2, 16) || !aligned(ws, 256))
         return DSPARK_ERR_INVALID;
@@ -254,6 +313,14 @@ static dspark_status verify_impl(const void* target, dspark_dtype target_t, cons
     p.ws = ws_ptrs(ws, B, gamma, V);
     p.state = state;
     p.zlog = zlog;
+    if (!K) {
+        // full prefix: rows 0..gamma-1 were reduced by dspark_draft_markov_target
+        // on these inputs (the accept kernel checks the token it left)
+        if (state) return DSPARK_ERR_UNSUPPORTED;
+        p.tgt_slots = draft_rows_grid_x(B, V, p.ws.parts);
+        if (p.tgt_slots > kTgtSlots) return DSPARK_ERR_UNSUPPORTED;
+        p.tgt_token = tgt_token_of(target, seed, step, req_base, B, gamma, V, tau);
+    }
     if (zlog && (!is_device_ptr(zlog) || !aligned(zlog, 16))) return DSPARK_ERR_INVALID;
     if (state && !zlog && !resid_rows_supported(p)) return DSPARK_ERR_UNSUPPORTED;
     return launch_status(launch_verify(p, static_cast<cudaStream_t>(stream)));

@@ -50,6 +50,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -71,6 +72,7 @@ constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile 
 // n % kUSlots; the MMA warp alone reads the slots (copying them into TMEM),
 // in fill order.
 constexpr int kUSlots = 4;
+constexpr int kTBufBytes = 32 * 128;              // target stream: one warp's 32 rows x 32 fp32 of a tile
 constexpr int kUSlotsResid = 8;                   // residual: 16 warps x (4 KB U + 4 KB target) row staging
 constexpr int kSmemBudget = 227 * 1024;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
@@ -83,30 +85,35 @@ constexpr float kRaceRel = 1.0000152587890625f;   // 1 + 2^-16
 constexpr float kRaceSlack = 1.52587890625e-05f;  // 2^-16
 
 struct Layout {
-    uint32_t b, a, u, merge, bar, misc, total;
-    int uslots, stages;
+    uint32_t b, a, u, t, merge, tmerge, bar, misc, total;
+    int uslots, tslots, stages;
 };
 
 constexpr int kSlotBytes = 128 * 128;             // one U slice: 128 rows x 32 fp32
 
 // The A operands live in TMEM, so shared memory holds the W2 ring (whatever
 // is left, up to kMaxStages K-chunks), the U slots (the residual mode uses
-// that region as 16 per-warp 4 KB row-staging buffers), the fold buffer,
+// that region as 16 per-warp 4 KB row-staging buffers), the fold buffers,
 // the barriers and a few words.
-__host__ __device__ inline Layout rows_layout(int NC, int r, bool resid) {
+__host__ __device__ inline Layout rows_layout(int NC, int r, bool resid, bool tgt = false) {
     (void)NC; (void)r;
     Layout L;
     L.uslots = resid ? kUSlotsResid : kUSlots;
-    const uint32_t fixed = (uint32_t)(L.uslots * kSlotBytes) + 4u * 128u * 16u +
-                           8u * (2 * kMaxStages + 2 * L.uslots + 2 * kMaxAcc + 2) + 16u + 8u * 128u + 1024u + 64u;
+    L.tslots = tgt ? kEpiWarps : 0;                            // one target buffer and barrier per epilogue warp
+    const uint32_t tmerge_bytes = tgt ? 4u * 128u * 8u : 0u;   // target fold: [4 column blocks][128 rows] float2
+    const uint32_t fixed = (uint32_t)(L.uslots * kSlotBytes + L.tslots * kTBufBytes) + 4u * 128u * 16u +
+                           tmerge_bytes + 8u * (2 * kMaxStages + 2 * L.uslots + 2 * kMaxAcc + 2 + L.tslots) + 16u +
+                           8u * 128u + 1024u + 64u;
     int st = (int)((kSmemBudget - (int)fixed) / kBBytes);
     L.stages = st > kMaxStages ? kMaxStages : st;
     L.b = 0;
     L.a = 0;
     L.u = L.b + (uint32_t)L.stages * kBBytes;
-    L.merge = L.u + (uint32_t)(L.uslots * kSlotBytes);
-    L.bar = L.merge + 4u * 128u * 16u;
-    L.misc = L.bar + 8u * (2 * L.stages + 2 * L.uslots + 2 * kMaxAcc + 2);
+    L.t = L.u + (uint32_t)(L.uslots * kSlotBytes);
+    L.merge = L.t + (uint32_t)(L.tslots * kTBufBytes);
+    L.tmerge = L.merge + 4u * 128u * 16u;
+    L.bar = L.tmerge + tmerge_bytes;
+    L.misc = L.bar + 8u * (2 * L.stages + 2 * L.uslots + 2 * kMaxAcc + 2 + L.tslots);
     L.misc = (L.misc + 15u) & ~15u;
     L.total = L.misc + 16u + 8u * 128u;
     return L;
@@ -115,7 +122,9 @@ __host__ __device__ inline Layout rows_layout(int NC, int r, bool resid) {
 struct RowsArgs {
     CUtensorMap w2map;   // bf16 [r][V], box {64 vocab, 64 rank}, 128-byte swizzle
     CUtensorMap umap;    // fp32 [B][gamma][V], box {32 vocab, 1, NC requests}, 128-byte swizzle
-    CUtensorMap upf;     // the same tensor, box {128 vocab, 1, NC requests}: L2 prefetch of a tile
+    // target stream only: fp32 [B][gamma+1][V], box {32 vocab, 1, 32 requests}
+    // (one epilogue warp's rows, 128-byte swizzle)
+    CUtensorMap tmap;
     DraftParams p;
     int NC;              // request rows per CTA (32, 64 or 128)
     // residual mode only
@@ -124,6 +133,67 @@ struct RowsArgs {
     // RNN head (kRnn only): the GRU steps run in the prologue and at the position boundaries
     GruParams gru;
 };
+
+// Target stream: adds 2^(x_j * sc - m) over the entries j < n of N columns
+// of one row to its running base-2 log-sum-exp state (m, s).  The reference m
+// is set from the first tile's maximum and moves only when a tile's sum would
+// leave the safe range (an entry more than 64 above m: rare, the tile is then
+// redone against its own maximum); entries far below m flush to zero, which
+// leaves the sum unchanged in binary32.  kMask: entries j >= n lie past the
+// vocabulary and count as -inf.
+template <bool kMask, int N>
+__device__ __forceinline__ void tgt_lse_add(const float (&x)[N], int n, float sc, float& m, float& s) {
+    float xv[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) xv[j] = (!kMask || j < n) ? x[j] : -INFINITY;
+    if (m == -INFINITY) {
+        float cm = xv[0];
+#pragma unroll
+        for (int j = 1; j < N; ++j) cm = fmaxf(cm, xv[j]);
+        m = cm * sc;                                 // sc > 0 keeps the maximum
+        if (m == -INFINITY) return;
+    }
+    const float2 sc2 = make_float2(sc, sc);
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+    float2 nm = make_float2(-m, -m);
+#pragma unroll
+    for (int j = 0; j < N; j += 4) {
+        const float2 d01 = __ffma2_rn(make_float2(xv[j], xv[j + 1]), sc2, nm);
+        const float2 d23 = __ffma2_rn(make_float2(xv[j + 2], xv[j + 3]), sc2, nm);
+        a01 = __fadd2_rn(a01, make_float2(fast_exp2(d01.x), fast_exp2(d01.y)));
+        a23 = __fadd2_rn(a23, make_float2(fast_exp2(d23.x), fast_exp2(d23.y)));
+    }
+    float sum = (a01.x + a01.y) + (a23.x + a23.y);
+    if (!(sum < 18446744073709551616.f)) {   // 2^64, or inf / NaN
+        float cm = xv[0];
+#pragma unroll
+        for (int j = 1; j < N; ++j) cm = fmaxf(cm, xv[j]);
+        cm *= sc;
+        if (cm > m) {
+            s *= fast_exp2(m - cm);
+            m = cm;
+        }
+        sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) sum += fast_exp2(fmaf(xv[j], sc, -m));
+    }
+    s += sum;
+}
+
+// 16-byte load from a shared-memory address.
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+// (m, s) += (e.x, e.y) for base-2 log-sum-exp states (m = -inf: empty).
+__device__ __forceinline__ void lse2_merge(float& m, float& s, const float2 e) {
+    if (e.x == -INFINITY) return;
+    if (m == -INFINITY) { m = e.x; s = e.y; return; }
+    if (e.x > m) { s = s * fast_exp2(m - e.x) + e.y; m = e.x; }
+    else s += e.y * fast_exp2(e.x - m);
+}
 
 // Bounded grid-wide barrier on a counter in global memory: every CTA adds 1,
 // then waits until all `target` CTAs have.  The kernel is launched
@@ -404,16 +474,27 @@ __device__ __forceinline__ void gate_step(const GruParams& g, int ks, int cta, i
 // tile's 32 columns of that row over their lanes (one shuffle per column) and
 // every lane races its own column; the lanes' partial states are merged at
 // the end of the position.
-template <bool kResid, typename TT, bool kRnn = false, bool kOneRow = false>
+// kTgt (full-prefix verification): position k also reduces target row k-1
+// to log-sum-exp partials, the work of the verify stream on those rows.
+// Every epilogue warp keeps its own 4 KB buffer: after its race on a tile
+// it reads the tile's target block (its 32 request rows x 32 columns, lane =
+// row, 128-byte swizzle), issues the TMA load of its next tile's block into
+// the same buffer and folds the values into a running base-2 log-sum-exp
+// per request row.  The load has a whole tile's race to land, and no warp
+// waits on another's progress.  Nothing prefetches U or the target into L2:
+// the extra L2 footprint evicts W2, whose re-reads from HBM cost more than
+// the latency a prefetch hides.
+template <bool kResid, typename TT, bool kRnn = false, bool kOneRow = false, bool kTgt = false>
 __global__ void __launch_bounds__(kThreads, 1)
 rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_last) {
+    static_assert(!(kTgt && (kResid || kRnn)), "the target stream belongs to the Markov draft");
     const DraftParams& p = a.p;
     const int NC = a.NC;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const Layout L = rows_layout(NC, p.r, kResid);
+    const Layout L = rows_layout(NC, p.r, kResid, kTgt);
     const int KCH = p.r / 64;
     const int RF = 128 / NC;                      // vocabulary tiles per accumulator
     const int US = L.uslots;
@@ -433,6 +514,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * US + kMaxAcc + i); };
     const uint32_t drain = bar0 + 8u * (2 * kStages + 2 * US + 2 * kMaxAcc);
     const uint32_t a_ready = bar0 + 8u * (2 * kStages + 2 * US + 2 * kMaxAcc + 1);
+    auto tbar = [&](int w) { return bar0 + 8u * (2 * kStages + 2 * US + 2 * kMaxAcc + 2 + w); };   // kTgt
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L.misc);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 4);
     volatile uint32_t* never = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 8);
@@ -454,6 +536,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         for (int i = 0; i < kMaxAcc; ++i) { ptx::mbar_init(tfull(i), 1); ptx::mbar_init(tempty(i), kEpiWarps); }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(a_ready, 1);
+        if constexpr (kTgt)
+            for (int w = 0; w < kEpiWarps; ++w) ptx::mbar_init(tbar(w), 1);
         *abort_flag = 0u;
         *never = 0u;
         ptx::fence_mbar_init();
@@ -461,8 +545,9 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     if (tid == kProducerWarp * 32) ptx::prefetch_tmap(&a.w2map);
     if (tid == kUWarp * 32 && !kResid) {
         ptx::prefetch_tmap(&a.umap);
-        ptx::prefetch_tmap(&a.upf);
+        if constexpr (kTgt) ptx::prefetch_tmap(&a.tmap);
     }
+    if (kTgt && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.ws.tgt_token = p.tgt_token;
     if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 512u); ptx::tmem_relinquish(); }
     for (int n = tid; n < 128; n += kThreads) {
         int x = -1, prow = -1;
@@ -571,16 +656,6 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                                              vs + i * kTN + 32 * c, k - 1, b_base, ufull(s), pol_u);
                         ++nu;
                     }
-                    if (ok) {
-                        // the U of this CTA's next tile into L2 (evict-first, like
-                        // its loads, so W2 keeps its place): its slot loads then
-                        // wait on L2 rather than HBM
-                        int tn = t + (int)gridDim.x, kn = k;
-                        if (tn >= ntiles) { tn = blockIdx.x; ++kn; }
-                        if (kn <= k_last)
-                            for (int i = 0; i < RF; ++i)
-                                ptx::tma_prefetch_3d(&a.upf, tn * kTN * RF + i * kTN, kn - 1, b_base, pol_u);
-                    }
                 }
             }
             if (!ok) { raise_timeout(p.ws.status, site); *abort_flag = 1u; }
@@ -589,6 +664,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     const long long m = (nu - 1) - ((nu - 1 - i) % US);
                     ptx::mbar_wait(ufull(i), (uint32_t)((m / US) & 1), never, kDrainCycles);
                 }
+
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -680,6 +756,19 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         int acc = 0;
         uint32_t aph = 0;
         bool failed = false;
+        // target stream (kTgt): this warp's buffer, its loads consumed, one in flight
+        const uint32_t tbuf = base + L.t + (uint32_t)warp * (uint32_t)kTBufBytes;
+        int ltile = 0;
+        bool tinfl = false;
+        auto tgt_issue = [&](int tn, int kn) {
+            // rows (32 q) % NC .. + 31 of the chunk: TMEM lanes 32 q .. 32 q + 31
+            ptx::fence_proxy_async_smem();          // the lanes' reads of the buffer come first
+            ptx::mbar_arrive_expect_tx(tbar(warp), (uint32_t)kTBufBytes);
+            ptx::tma_load_3d(tbuf, &a.tmap, tn * kTN * RF + ti * kTN + 32 * cb, kn - 1, b_base + (32 * q) % NC,
+                             tbar(warp), ptx::policy_evict_first());
+        };
+        if (kTgt && active && lane == 0) tgt_issue(blockIdx.x, k_first);
+        if (kTgt && active) tinfl = true;
         for (int k = k_first; k <= k_last && !failed; ++k) {
             const int urow = kResid ? (real ? s_row[nrow] : 0) : (k - 1);     // row of U (and of the target)
             const StreamRK rng(p.seed, p.step, kResid ? 2u : 0u,
@@ -700,6 +789,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             float rz2 = -INFINITY, rE2 = INFINITY;     // winner's z*log2e and E2
             float rE2h = INFINITY;                     // rE2 * kRaceRel: the screen's threshold
             Draw2 st2 = draw2_empty();
+            float tm2 = -INFINITY, tsum = 0.f;         // target stream: this row's base-2 log-sum-exp state
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
                 bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
                 ok = __all_sync(0xffffffffu, ok);
@@ -881,6 +971,39 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         }
                     }
                 }
+                if constexpr (kTgt) {
+                    // target row k-1 on this warp's 32 rows x 32 columns (after the
+                    // race: the bias is dead by now), then the next tile's block into
+                    // the same buffer
+                    if (active) {
+                        bool okt = ptx::mbar_wait(tbar(warp), (uint32_t)(ltile & 1), abort_flag, kWaitCycles);
+                        okt = __all_sync(0xffffffffu, okt);
+                        if (!okt) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 12); failed = true; break; }
+                        tinfl = false;
+                        ++ltile;
+                        const uint32_t srow = tbuf + (uint32_t)lane * 128u;
+                        const int nv = V - (t * kTN * RF + ti * kTN + 32 * cb);   // entries inside the vocabulary
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {           // two halves of 16 columns
+                            float tv[16];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const float4 v4 = lds_f4(srow + ((uint32_t)((4 * h + c) ^ (lane & 7)) << 4));
+                                tv[4 * c] = v4.x; tv[4 * c + 1] = v4.y; tv[4 * c + 2] = v4.z; tv[4 * c + 3] = v4.w;
+                            }
+                            const int nh = nv - 16 * h;
+                            if (nh >= 16) tgt_lse_add<false>(tv, 16, scale2, tm2, tsum);
+                            else if (nh > 0) tgt_lse_add<true>(tv, nh, scale2, tm2, tsum);
+                        }
+                        __syncwarp();
+                        int tn = t + (int)gridDim.x, kn = k;
+                        if (tn >= ntiles) { tn = blockIdx.x; ++kn; }
+                        if (kn <= k_last) {
+                            if (lane == 0) tgt_issue(tn, kn);
+                            tinfl = true;
+                        }
+                    }
+                }
             }
             // ---- this position's partial state per request: fold RF tiles x 4 column blocks
             if constexpr (kResid) {
@@ -907,6 +1030,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 }
                 s_merge[cb * 128 + row] = sn;
             }
+            if constexpr (kTgt) reinterpret_cast<float2*>(gbase + L.tmerge)[cb * 128 + row] = make_float2(tm2, tsum);
             // one barrier publishes s_merge and makes a failure a group decision
             if (ptx::bar_red_or(1, 32 * kEpiWarps, failed)) { failed = true; *abort_flag = 1u; break; }
             DrawLse* part_buf = p.ws.draft_part + (size_t)((k - 1) & 1) * p.B * p.ws.parts;
@@ -924,6 +1048,17 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 #pragma unroll
                         for (int c = 0; c < 4; ++c) s1 = drawlse_merge(s1, s_merge[c * 128 + i * NC + etid]);
                     part_buf[(size_t)(b_base + etid) * p.ws.parts + blockIdx.x] = s1;
+                    if constexpr (kTgt) {
+                        // this CTA's log-sum-exp partial of target row k-1, in natural units
+                        const float2* tmg = reinterpret_cast<const float2*>(gbase + L.tmerge);
+                        float mm = -INFINITY, ss = 0.f;
+                        for (int i = 0; i < RF; ++i)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) lse2_merge(mm, ss, tmg[c * 128 + i * NC + etid]);
+                        LseDraw o = lsedraw_empty();
+                        if (mm > -INFINITY) { o.m = mm * kLn2; o.s = ss; }
+                        p.ws.tgt_part[((size_t)(b_base + etid) * gamma + (k - 1)) * kTgtSlots + blockIdx.x] = o;
+                    }
                     // the draw itself is decided by an atomic maximum over the CTAs
                     if (persistent)
                         atomicMax(&p.ws.win[((size_t)(k - 1) * p.B + b_base + etid) * kWinStride], win_key(s1));
@@ -1014,6 +1149,9 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             if (k == k_last) break;
         }
         if (failed) *abort_flag = 1u;
+        // a target load still in flight (after a failure) lands before the CTA leaves
+        if (kTgt && tinfl && lane == 0) ptx::mbar_wait(tbar(warp), (uint32_t)(ltile & 1), never, kDrainCycles);
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -1130,6 +1268,17 @@ bool rows_supported(const DraftParams& p) {
 
 bool draft_rows_supported(const DraftParams& p) { return rows_supported(p); }
 
+int draft_rows_grid_x(int B, int V, int parts) {
+    const int NC = B <= 64 ? 64 : 128;
+    const int nchunks = (B + NC - 1) / NC;
+    const int ntiles = (V + kTN * (128 / NC) - 1) / (kTN * (128 / NC));
+    int gx = num_sms() / nchunks;
+    gx = gx < 1 ? 1 : gx;
+    gx = gx > ntiles ? ntiles : gx;
+    gx = gx > parts ? parts : gx;
+    return gx;
+}
+
 bool cooperative_supported() {
     static int cached[64] = {0};     // 0 unknown, 1 yes, 2 no
     int dev = 0;
@@ -1173,29 +1322,30 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)p.gamma, (cuuint64_t)p.B};
-        const cuuint64_t strides[2] = {(cuuint64_t)p.V * 4, (cuuint64_t)p.gamma * p.V * 4};
-        const cuuint32_t box[3] = {(cuuint32_t)kTN, 1, (cuuint32_t)a.NC};
+    // the target stream (Markov draft only): target [B][gamma+1][V] fp32, one
+    // epilogue warp's block
+    const bool tgt = !resid && !gru && p.target != nullptr;
+    if (tgt) {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)(p.gamma + 1), (cuuint64_t)p.B};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.V * 4, (cuuint64_t)(p.gamma + 1) * p.V * 4};
         const cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&a.upf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(p.U), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        const cuuint32_t box[3] = {32, 1, 32};
+        if (enc(&a.tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p.target), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const Layout L = rows_layout(a.NC, p.r, resid);
+    const Layout L = rows_layout(a.NC, p.r, resid, tgt);
     const size_t smem = L.total + 1024;
     auto kern = resid ? (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>)
-                      : (gru ? rows_kernel<false, float, true>
-                             : (p.B == 1 ? rows_kernel<false, float, false, true> : rows_kernel<false, float>));
+                : gru ? rows_kernel<false, float, true>
+                : tgt ? (p.B == 1 ? rows_kernel<false, float, false, true, true> : rows_kernel<false, float, false, false, true>)
+                      : (p.B == 1 ? rows_kernel<false, float, false, true> : rows_kernel<false, float>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nchunks = (p.B + a.NC - 1) / a.NC;
-    const int ntiles = (p.V + kTN * (128 / a.NC) - 1) / (kTN * (128 / a.NC));
-    int gx = num_sms() / nchunks;
-    gx = gx < 1 ? 1 : gx;
-    gx = gx > ntiles ? ntiles : gx;
-    gx = gx > p.ws.parts ? p.ws.parts : gx;
+    const int gx = draft_rows_grid_x(p.B, p.V, p.ws.parts);
+    if (tgt && gx > kTgtSlots) return cudaErrorInvalidConfiguration;
     const dim3 grid(gx, nchunks);
     if (k_last > k_first) {
         // every CTA waits for all others between positions: they must be co-resident
@@ -1208,6 +1358,24 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
 
 cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cudaStream_t s) {
     return launch_rows(p, k_first, k_last, false, nullptr, false, nullptr, s);
+}
+
+bool draft_target_supported(const DraftParams& p) {
+    return rows_supported(p) && p.target != nullptr && draft_rows_grid_x(p.B, p.V, p.ws.parts) <= kTgtSlots;
+}
+
+// The Markov draft with the target stream: one cooperative launch for the
+// gamma positions, else one launch per position (the rows kernel merges a
+// single position's partials itself).
+cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s) {
+    if (!draft_target_supported(p)) return cudaErrorNotSupported;
+    if (p.gamma > 1 && cooperative_supported() && !getenv("DSPARK_DRAFT_PER_POSITION"))
+        return launch_rows(p, 1, p.gamma, false, nullptr, false, nullptr, s);
+    for (int k = 1; k <= p.gamma; ++k) {
+        const cudaError_t e = launch_rows(p, k, k, false, nullptr, false, nullptr, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // The RNN head's draft in one cooperative launch: positions k_first..k_last,

@@ -23,11 +23,13 @@ constexpr int kGridBarrierSlots = DSPARK_MAX_GAMMA;   // one grid-barrier counte
 constexpr int kGbarGru = kGridBarrierSlots;           // then one per position for the RNN head's GRU step
 constexpr int kGbarExit = 2 * kGridBarrierSlots;      // then the exit counter
 constexpr int kWinStride = 16;          // winner keys 128 bytes apart: one cache line each
+constexpr int kTgtSlots = 256;          // partial states per (request, target row) of the draft's target
+                                        // stream (>= the draft's CTAs along V)
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, tickets, gbar, win, vq, draft_part, verify_part, rej, acc, fin, lse_rej, resid_part, conf, rnn_gh,
-        total;
+    size_t status, tickets, gbar, win, vq, draft_part, verify_part, tgt_part, tgt_token, rej, acc, fin, lse_rej,
+        resid_part, conf, rnn_gh, total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -42,7 +44,9 @@ struct WsPtrs {
     unsigned long long* win;   // [gamma][B][kWinStride] winner keys of the persistent draft (first of
                                // each line used), zero between launches
     DrawLse* draft_part;       // [2][B][parts] (two buffers alternate between positions)
-    LseDraw* verify_part;
+    LseDraw* verify_part;      // [B][gamma+1][nseg * kVerifySub] verify-stream partials
+    LseDraw* tgt_part;         // [B][gamma][kTgtSlots] target-row partials of the draft's target stream
+    unsigned long long* tgt_token;   // [1] identifies the call that wrote tgt_part
     int32_t* rej;        // [B] 0-based rejected row, -1 if every walked draft was accepted
     int32_t* acc;        // [B] accepted count
     int32_t* fin;        // [B] final token
@@ -68,6 +72,10 @@ struct DraftParams {
     // RNN head: the bias of position k is formed from state[k-1][b] ([gamma][B][r]
     // fp32, rounded to bf16 when staged) instead of W1[x~_{k-1}]
     const float* state = nullptr;
+    // target stream (full-prefix verification): position k also reduces target
+    // row k-1 ([B][gamma+1][V] fp32) to log-sum-exp partials in ws.tgt_part
+    const float* target = nullptr;
+    unsigned long long tgt_token = 0;
 };
 
 // One GRU step of the RNN head for every request: state[k-1] = GRU(state[k-2]
@@ -119,6 +127,12 @@ struct VerifyParams {
     WsPtrs ws;
     const float* state = nullptr;   // RNN head bias rows (see DraftParams)
     const float* zlog = nullptr;    // the draft's stored logits [B][gamma][V] (z / tau), or null
+    // full-prefix mode (K == null, every K_b = gamma): rows 0..gamma-1 take
+    // their log-sum-exp from the draft's target stream (tgt_slots partials a
+    // row in ws.tgt_part, written by the call whose token is tgt_token); the
+    // verify stream covers only the bonus rows
+    int tgt_slots = 0;
+    unsigned long long tgt_token = 0;
 };
 
 struct StsFitParams {
@@ -139,6 +153,9 @@ bool draft_tc_supported(const DraftParams& p);
 cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s);
 bool draft_rows_supported(const DraftParams& p);
 cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cudaStream_t s);
+int draft_rows_grid_x(int B, int V, int parts);   // CTAs along V of a draft rows launch
+bool draft_target_supported(const DraftParams& p);
+cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s);   // the draft with the target stream
 bool cooperative_supported();
 void* tma_encoder();   // cuTensorMapEncodeTiled from the driver, or NULL
 bool resid_rows_supported(const VerifyParams& v);

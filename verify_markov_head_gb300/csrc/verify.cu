@@ -70,7 +70,8 @@ verify_stream_kernel(const VerifyParams p) {
     const bool k_cached = p.B <= kStreamKCache;
 
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
-    const int items = p.B * (gamma + 1) * nseg;
+    // full-prefix mode: the draft reduced rows 0..gamma-1, only the bonus rows remain
+    const int items = p.tgt_slots > 0 ? p.B * nseg : p.B * (gamma + 1) * nseg;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     if (tid == 0) {
         for (int i = 0; i < kStreamStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), kStreamConsumers); }
@@ -78,14 +79,14 @@ verify_stream_kernel(const VerifyParams p) {
         ptx::fence_mbar_init();
     }
     if (k_cached)
-        for (int b = tid; b < p.B; b += kStreamThreads) s_K[b] = p.K[b];
-    if (blockIdx.x == 0)
+        for (int b = tid; b < p.B; b += kStreamThreads) s_K[b] = p.K ? p.K[b] : gamma;
+    if (blockIdx.x == 0 && p.K)
         for (int b = tid; b < p.B; b += kStreamThreads)
             if (p.K[b] < 0 || p.K[b] > gamma) raise_status(p.ws.status, kBadLength);
     __syncthreads();
 
     auto clampK = [&](int b) {
-        const int Kb = k_cached ? s_K[b] : p.K[b];
+        const int Kb = k_cached ? s_K[b] : (p.K ? p.K[b] : gamma);
         return Kb < 0 ? 0 : (Kb > gamma ? gamma : Kb);
     };
     // item u -> (b, i, seg): the B * nseg bonus items first, then the rest
@@ -262,18 +263,24 @@ verify_stream_kernel(const VerifyParams p) {
     }
 }
 
-constexpr int kAcceptStaged = 1024;   // segment partials staged in shared memory (16 KB)
+constexpr int kAcceptStaged = 2048;   // partials staged in shared memory (32 KB)
 
-// One warp per request: lse_p of rows 0..K_b from the segment partials, then
-// the accept test of every walked position at once (lane k-1 tests draft k),
-// the first rejection found by a ballot.
+// One warp per request: lse_p of rows 0..K_b from the partials, then the
+// accept test of every walked position at once (lane k-1 tests draft k), the
+// first rejection found by a ballot.  The partials of a row are the verify
+// stream's segment partials, or in full-prefix mode (K null) the draft's
+// target-stream partials for rows 0..gamma-1 and the stream's for the bonus
+// row gamma.
 template <typename TT>
 __global__ void __launch_bounds__(32)
 verify_accept_kernel(const VerifyParams p) {
     const int b = blockIdx.x, lane = threadIdx.x;
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
-    int Kb = p.K[b];
+    const bool full = p.tgt_slots > 0;
+    int Kb = full ? gamma : p.K[b];
     Kb = Kb < 0 ? 0 : (Kb > gamma ? gamma : Kb);
+    // full-prefix mode needs the target-stream partials of this very call's inputs
+    if (full && b == 0 && lane == 0 && *p.ws.tgt_token != p.tgt_token) raise_status(p.ws.status, kBadInput);
     const TT* target = static_cast<const TT*>(p.target);
     const uint32_t row0 = (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1);
     // per-lane draft data for position k = lane + 1 (issued before the merges)
@@ -290,19 +297,32 @@ verify_accept_kernel(const VerifyParams p) {
     }
     float lse_mine = 0.f;        // lse_p of row `lane`
     int bonus_idx = 0;
-    const int nsub = nseg * kVerifySub;            // partial states per row
+    const int nsub = nseg * kVerifySub;            // verify-stream partials per row
     const LseDraw* parts = p.ws.verify_part + (size_t)b * (gamma + 1) * nsub;
-    const int nparts = (Kb + 1) * nsub;
+    const int ns = full ? p.tgt_slots : nsub;      // partials per row below the bonus row
+    const LseDraw* tparts = p.ws.tgt_part + (size_t)b * gamma * kTgtSlots;
+    // row i's partials: the draft's (full mode, i < gamma) or the stream's
+    auto row_src = [&](int i, int& cnt) -> const LseDraw* {
+        if (full && i < gamma) { cnt = ns; return tparts + (size_t)i * kTgtSlots; }
+        cnt = nsub;
+        return parts + (size_t)i * nsub;
+    };
+    const int nparts = Kb * ns + nsub;             // rows 0..K_b, staged row after row
     if (nparts <= kAcceptStaged) {
-        // the segment partials of rows 0..K_b, every load in flight, through
-        // shared memory; then lane i folds row i
+        // the partials of rows 0..K_b, every load in flight, through shared
+        // memory (row i from index i * ns); then lane i folds row i
         __shared__ float4 s_part[kAcceptStaged];
         for (int i0 = lane; i0 < nparts; i0 += 12 * 32) {
             float4 c[12];
 #pragma unroll
             for (int u = 0; u < 12; ++u) {
                 const int i = i0 + 32 * u;
-                if (i < nparts) c[u] = __ldcg(reinterpret_cast<const float4*>(parts) + i);
+                if (i < nparts) {
+                    const int row = i / ns < Kb ? i / ns : Kb;
+                    int cnt;
+                    const LseDraw* src = row_src(row, cnt);
+                    c[u] = __ldcg(reinterpret_cast<const float4*>(src) + (i - row * ns));
+                }
             }
 #pragma unroll
             for (int u = 0; u < 12; ++u) {
@@ -317,20 +337,23 @@ verify_accept_kernel(const VerifyParams p) {
         while (LPR > 1 && (Kb + 1) * LPR > 32) LPR >>= 1;
         const int row = lane / LPR, sub = lane - row * LPR;
         LseDraw a = lsedraw_empty();
-        if (row <= Kb)
-            for (int sg = sub; sg < nsub; sg += LPR) {
-                const float4 c = s_part[row * nsub + sg];
+        if (row <= Kb) {
+            const int cnt = row < Kb ? ns : nsub;
+            for (int sg = sub; sg < cnt; sg += LPR) {
+                const float4 c = s_part[row * ns + sg];
                 a = lsedraw_merge(a, LseDraw{c.x, c.y, c.z, __float_as_int(c.w)});
             }
+        }
         for (int m = 1; m < LPR; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
         const float lse_row = a.m + logf(a.s);         // on lanes row * LPR
         lse_mine = __shfl_sync(0xffffffffu, lse_row, (lane * LPR) & 31);
         bonus_idx = __shfl_sync(0xffffffffu, a.idx, Kb * LPR);
     } else {
         for (int i = 0; i <= Kb; ++i) {
-            const LseDraw* part = parts + (size_t)i * nsub;
+            int cnt;
+            const LseDraw* part = row_src(i, cnt);
             LseDraw a = lsedraw_empty();
-            for (int sg = lane; sg < nsub; sg += 32) a = lsedraw_merge(a, part[sg]);
+            for (int sg = lane; sg < cnt; sg += 32) a = lsedraw_merge(a, part[sg]);
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
             if (lane == i) lse_mine = a.m + logf(a.s);
@@ -572,7 +595,7 @@ verify_compact_kernel(const VerifyParams p) {
 
 template <typename TT>
 cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
-    const long long items = (long long)p.B * (p.gamma + 1) * p.ws.nseg;
+    const long long items = (long long)p.B * (p.tgt_slots > 0 ? 1 : p.gamma + 1) * p.ws.nseg;
     const int g1 = (int)(items < 2LL * num_sms() ? items : 2LL * num_sms());
     const size_t smem1 = 128 + (size_t)kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16 +
                          sizeof(int2) * kStreamStages + (p.B <= kStreamKCache ? sizeof(int) * (size_t)p.B : 0);
