@@ -48,6 +48,7 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.resid_part = o;  o = align256(o + sizeof(Draw2) * (size_t)B * L.parts);
     L.conf = o;        o = align256(o + sizeof(uint32_t) * (size_t)B + sizeof(float) * (size_t)B * gamma);
     L.rnn_gh = o;      o = align256(o + sizeof(float) * (size_t)B * 3 * kMaxRnnRank);
+    L.bonus_tickets = o; o = align256(o + sizeof(uint32_t) * (size_t)B);
     L.total = o;
     return L;
 }
@@ -74,6 +75,7 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     P.conf_tickets = reinterpret_cast<uint32_t*>(base + L.conf);
     P.conf_score = reinterpret_cast<float*>(base + L.conf + sizeof(uint32_t) * (size_t)B);
     P.rnn_gh = reinterpret_cast<float*>(base + L.rnn_gh);
+    P.bonus_tickets = reinterpret_cast<uint32_t*>(base + L.bonus_tickets);
     P.nseg = L.nseg;
     P.parts = L.parts;
     return P;

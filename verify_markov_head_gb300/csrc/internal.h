@@ -29,7 +29,7 @@ constexpr int kTgtSlots = 256;          // partial states per (request, target r
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
     size_t status, tickets, gbar, win, vq, draft_part, verify_part, tgt_part, tgt_token, rej, acc, fin, lse_rej,
-        resid_part, conf, rnn_gh, total;
+        resid_part, conf, rnn_gh, bonus_tickets, total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -55,6 +55,7 @@ struct WsPtrs {
     uint32_t* conf_tickets;  // [B] confidence-head arrival counters, zero between launches
     float* conf_score;       // [B][gamma]
     float* rnn_gh;           // [B][3 kMaxRnnRank] RNN head scratch
+    uint32_t* bonus_tickets; // [B] bonus-draw arrival counters, zero between launches
     int nseg;
     int parts;
 };

@@ -2,20 +2,29 @@
 // ("DSpark：半自回归生成与置信度调度的投机解码" section 形式化定义;
 //  "DeepSeek-AI与北京大学联手破局" sections 四 and 五).
 //
-// Four launches, all stream-ordered and free of waits:
-//   verify_stream   rows i = 0..K_b of the target logits, split in 4096-entry
-//                   segments: online log-sum-exp of t/tau and, on the bonus
-//                   row i = K_b, a Gumbel-max draw (domain 3).  128-bit
-//                   streaming loads (evict-first), warp-shuffle reductions.
-//   verify_accept   one warp per request: merges the segment partials into
-//                   lse_p per row, walks k = 1..K_b with the acceptance
-//                   uniforms (domain 1), records the first rejection.
+// Four or five launches, all stream-ordered and free of waits:
+//   verify_stream   rows i = 0..K_b-1 of the target logits in 32768-entry
+//                   segments: online log-sum-exp of t/tau, bulk copies into
+//                   shared memory (evict-first).  With an fp32 target it also
+//                   draws the bonus token of every request on row K_b
+//                   (Gumbel-max, domain 3), hidden under the streaming.
+//                   Full-prefix mode skips it (the draft reduced the rows).
+//   verify_accept   one warp per request: merges the partials into lse_p per
+//                   row, walks k = 1..K_b with the acceptance uniforms
+//                   (domain 1), records the first rejection.
 //   verify_residual rejected requests only: recomputes the draft logits of
 //                   the rejected row (bias h . W2 plus U), forms
 //                   max(0, p - q) and draws from it by Gumbel-max (domain 2),
 //                   with the draw from p kept as the fallback.
+//   verify_stream   (bf16 target, full-prefix mode, stored logits) the bonus
+//                   draw of the requests that accepted all K_b drafts only:
+//                   the draw needs a random number per entry, and with
+//                   nothing to hide it, drawing it only where it is emitted
+//                   saves most of that work.
 //   verify_compact  one CTA: exclusive scan of A_b + 1, scatter of the
 //                   accepted drafts and the final token of every request.
+// The last warp to finish a request's bonus segments merges them into its
+// token.
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -39,22 +48,32 @@ constexpr int kStreamKCache = 2048;                          // verify lengths k
 template <typename T>
 __device__ __forceinline__ float load_scalar(const T* p, size_t i) { return to_f32(p[i]); }
 
-// Persistent streaming pass over the target rows 0..K_b of every request.
-// Work item = (b, i, seg), a kVerifySeg-entry slice of a row.  CTAs take items
-// from a global counter in the order: the bonus rows i = K_b of every request
-// first (they also draw, so they cost several times a plain item), then the
-// other rows; items with i > K_b are skipped.  Heavy items first and dynamic
-// claiming keep the CTAs' loads even.  A producer thread moves every
+// Persistent streaming pass over target rows.  Two kinds of work item:
+//   log-sum-exp item (b, i, seg): a kVerifySeg-entry slice of row i < K_b
+//     (a walked row); items with i >= K_b are skipped;
+//   bonus item (b, seg): a kVerifySeg-entry slice of row K_b, the Gumbel-max
+//     draw (domain 3) of the token emitted when all K_b drafts are accepted.
+// kMode selects them: kStreamAll takes the bonus items of every request
+// first (they cost several times a plain item) and then the log-sum-exp
+// items, so the draws hide under the streaming of the other rows;
+// kStreamLse the log-sum-exp items alone; kStreamBonus, launched after the
+// accept walk, only the bonus items of the requests whose walk rejected
+// nothing (ws.rej[b] < 0).  CTAs take items from a global counter (dynamic
+// claiming keeps their loads even).  A producer thread moves every
 // 8192-entry chunk of its items into a 3-stage shared-memory ring with one
 // bulk copy (evict-first) and tags the stage with the item; 8 consumer warps
-// keep their running log-sum-exp in base-2 units across the chunks of an item:
-// per chunk a max pass, one rescale, then exp2 of x*log2e/tau - m in four
-// independent partial sums.  The bonus row also takes the Gumbel-max draw
-// (domain 3).  Each consumer warp writes its own partial per item.  A stage
-// tagged -1 ends the stream.
-template <typename TT>
+// keep per item either their running log-sum-exp in base-2 units across the
+// chunks (per chunk a max pass, one rescale, then exp2 of x*log2e/tau - m in
+// four independent partial sums) or their Gumbel-max draw.  Each consumer
+// warp writes its own partial per item; for the bonus rows the warp that
+// completes a request's partials (an arrival ticket per request) merges them
+// and writes the request's final token.  A stage tagged -1 ends the stream.
+constexpr int kStreamAll = 0, kStreamLse = 1, kStreamBonus = 2;
+
+template <typename TT, int kMode>
 __global__ void __launch_bounds__(kStreamThreads, 2)
 verify_stream_kernel(const VerifyParams p) {
+    constexpr bool kHasBonus = kMode != kStreamLse, kHasLse = kMode != kStreamBonus;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
@@ -69,9 +88,10 @@ verify_stream_kernel(const VerifyParams p) {
     int* s_K = reinterpret_cast<int*>(s_meta + kStreamStages);
     const bool k_cached = p.B <= kStreamKCache;
 
-    const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
-    // full-prefix mode: the draft reduced rows 0..gamma-1, only the bonus rows remain
-    const int items = p.tgt_slots > 0 ? p.B * nseg : p.B * (gamma + 1) * nseg;
+    const int gamma = p.gamma, V = p.V;
+    const int nseg = p.ws.nseg;
+    const int nbonus = kHasBonus ? p.B * nseg : 0;           // bonus items come first
+    const int items = nbonus + (kHasLse ? p.B * gamma * nseg : 0);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     if (tid == 0) {
         for (int i = 0; i < kStreamStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), kStreamConsumers); }
@@ -89,22 +109,20 @@ verify_stream_kernel(const VerifyParams p) {
         const int Kb = k_cached ? s_K[b] : (p.K ? p.K[b] : gamma);
         return Kb < 0 ? 0 : (Kb > gamma ? gamma : Kb);
     };
-    // item u -> (b, i, seg): the B * nseg bonus items first, then the rest
+    // item u -> (b, i, seg); returns whether the item has work
     auto decode = [&](int u, int& b, int& i, int& seg) {
-        const int nbonus = p.B * nseg;
         if (u < nbonus) {
             b = u / nseg;
             seg = u - b * nseg;
             i = clampK(b);
-        } else {
-            const int v = u - nbonus, per = gamma * nseg;
-            b = v / per;
-            const int rest = v - b * per, in = rest / nseg;
-            seg = rest - in * nseg;
-            const int Kb = clampK(b);
-            i = in < Kb ? in : in + 1;
+            return kMode != kStreamBonus || __ldcg(&p.ws.rej[b]) < 0;
         }
-        return clampK(b);
+        const int v = u - nbonus, per = gamma * nseg;
+        b = v / per;
+        const int rest = v - b * per;
+        i = rest / nseg;
+        seg = rest - i * nseg;
+        return i < clampK(b);
     };
 
     if (warp == kStreamConsumers) {
@@ -118,8 +136,7 @@ verify_stream_kernel(const VerifyParams p) {
                 const int u = (int)atomicAdd(&p.ws.vq[0], 1u);
                 if (u >= items) break;
                 int b, i, seg;
-                const int Kb = decode(u, b, i, seg);
-                if (i > Kb) continue;
+                if (!decode(u, b, i, seg)) continue;
                 const int v_end = min(V, (seg + 1) * kVerifySeg);
                 const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
                 for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kStreamChunk) {
@@ -146,7 +163,7 @@ verify_stream_kernel(const VerifyParams p) {
         int stage = 0;
         uint32_t ph = 0;
         int cur = -1, b = 0, i = 0, seg = 0;
-        bool bonus = false;
+        bool bonus = false;                              // the current item is a bonus item
         float m2 = -INFINITY;                            // running max of x*log2e/tau
         float s4[4] = {0.f, 0.f, 0.f, 0.f};              // sum of 2^(x*log2e/tau - m2), four chains
         float best = -INFINITY;
@@ -161,7 +178,31 @@ verify_stream_kernel(const VerifyParams p) {
             if (m2 == -INFINITY) { st.m = -INFINITY; st.s = 0.f; }
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
-            if (lane == 0) p.ws.verify_part[(((size_t)b * (gamma + 1) + i) * nseg + seg) * kVerifySub + warp] = st;
+            LseDraw* row_part = p.ws.verify_part + ((size_t)b * (gamma + 1) + i) * nseg * kVerifySub;
+            if (lane == 0) row_part[seg * kVerifySub + warp] = st;
+            if (kHasBonus && bonus) {
+                // the warp that completes request b's partials merges them into its token
+                const int nsub = nseg * kVerifySub;
+                unsigned last = 0u;
+                if (lane == 0) {
+                    __threadfence();
+                    last = atomicAdd(&p.ws.bonus_tickets[b], 1u) == (unsigned)(nsub - 1) ? 1u : 0u;
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence();
+                    LseDraw a = lsedraw_empty();
+                    for (int sg = lane; sg < nsub; sg += 32) {
+                        const float4 c = __ldcg(reinterpret_cast<const float4*>(row_part) + sg);
+                        a = lsedraw_merge(a, LseDraw{c.x, c.y, c.z, __float_as_int(c.w)});
+                    }
+#pragma unroll
+                    for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
+                    if (lane == 0) {
+                        p.ws.fin[b] = a.idx;
+                        p.ws.bonus_tickets[b] = 0u;      // zero again for the next launch
+                    }
+                }
+            }
         };
         for (;;) {
             bool ok = ptx::mbar_wait(full(stage), ph, abort_flag, kStreamWaitCycles);
@@ -172,8 +213,8 @@ verify_stream_kernel(const VerifyParams p) {
             if (meta.x != cur) {                         // a new item
                 if (cur >= 0) flush();
                 cur = meta.x;
-                const int Kb = decode(cur, b, i, seg);
-                bonus = (i == Kb);
+                decode(cur, b, i, seg);
+                bonus = cur < nbonus;
                 m2 = -INFINITY;
                 s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
                 best = -INFINITY;
@@ -198,13 +239,13 @@ verify_stream_kernel(const VerifyParams p) {
 #pragma unroll
             for (int e = 1; e < kPerThread; ++e) cm = fmaxf(cm, x[e]);
             cm *= scale;                                  // scale > 0 keeps the maximum
-            if (cm > m2) {
+            if (!bonus && cm > m2) {
                 const float r = fast_exp2(m2 - cm);          // 0 when m2 = -inf
 #pragma unroll
                 for (int c = 0; c < 4; ++c) s4[c] *= r;
                 m2 = cm;
             }
-            if (m2 > -INFINITY) {
+            if (!bonus && m2 > -INFINITY) {
                 // two entries per packed multiply-add and add
                 const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m2, -m2);
                 float2 a01 = make_float2(s4[0], s4[1]), a23 = make_float2(s4[2], s4[3]);
@@ -217,7 +258,7 @@ verify_stream_kernel(const VerifyParams p) {
                 }
                 s4[0] = a01.x; s4[1] = a01.y; s4[2] = a23.x; s4[3] = a23.y;
             }
-            if (bonus) {
+            if (kHasBonus && bonus) {
                 // Gumbel-max as an exponential race against this thread's chunk
                 // maximum cm: argmax x/tau + G = argmin E2 * 2^(cm - x*log2e/tau),
                 // E2 = -log2 u (no outer logarithm, no divergent screen); the
@@ -265,12 +306,11 @@ verify_stream_kernel(const VerifyParams p) {
 
 constexpr int kAcceptStaged = 2048;   // partials staged in shared memory (32 KB)
 
-// One warp per request: lse_p of rows 0..K_b from the partials, then the
-// accept test of every walked position at once (lane k-1 tests draft k), the
-// first rejection found by a ballot.  The partials of a row are the verify
-// stream's segment partials, or in full-prefix mode (K null) the draft's
-// target-stream partials for rows 0..gamma-1 and the stream's for the bonus
-// row gamma.
+// One warp per request: lse_p of the walked rows 0..K_b-1 from the partials,
+// then the accept test of every walked position at once (lane k-1 tests draft
+// k), the first rejection found by a ballot.  The partials of a row are the
+// verify stream's segment partials, or in full-prefix mode (K null) the
+// draft's target-stream partials.
 template <typename TT>
 __global__ void __launch_bounds__(32)
 verify_accept_kernel(const VerifyParams p) {
@@ -295,22 +335,16 @@ verify_accept_kernel(const VerifyParams p) {
         lq = p.z_tok[o] - p.lse_q[o];
         u = uniform_of(Stream(p.seed, p.step, 1u, row0 + (uint32_t)lane).word(0));
     }
-    float lse_mine = 0.f;        // lse_p of row `lane`
-    int bonus_idx = 0;
+    float lse_mine = 0.f;        // lse_p of row `lane` (walked rows 0..K_b-1)
     const int nsub = nseg * kVerifySub;            // verify-stream partials per row
     const LseDraw* parts = p.ws.verify_part + (size_t)b * (gamma + 1) * nsub;
-    const int ns = full ? p.tgt_slots : nsub;      // partials per row below the bonus row
-    const LseDraw* tparts = p.ws.tgt_part + (size_t)b * gamma * kTgtSlots;
-    // row i's partials: the draft's (full mode, i < gamma) or the stream's
-    auto row_src = [&](int i, int& cnt) -> const LseDraw* {
-        if (full && i < gamma) { cnt = ns; return tparts + (size_t)i * kTgtSlots; }
-        cnt = nsub;
-        return parts + (size_t)i * nsub;
-    };
-    const int nparts = Kb * ns + nsub;             // rows 0..K_b, staged row after row
-    if (nparts <= kAcceptStaged) {
-        // the partials of rows 0..K_b, every load in flight, through shared
-        // memory (row i from index i * ns); then lane i folds row i
+    const int ns = full ? p.tgt_slots : nsub;      // partials per walked row
+    const LseDraw* rows = full ? p.ws.tgt_part + (size_t)b * gamma * kTgtSlots : parts;
+    const size_t rstride = full ? (size_t)kTgtSlots : (size_t)nsub;
+    const int nparts = Kb * ns;                    // rows 0..K_b-1, staged row after row
+    if (Kb > 0 && nparts <= kAcceptStaged) {
+        // the partials of the walked rows, every load in flight, through shared
+        // memory (row i from index i * ns); then lanes fold their row
         __shared__ float4 s_part[kAcceptStaged];
         for (int i0 = lane; i0 < nparts; i0 += 12 * 32) {
             float4 c[12];
@@ -318,10 +352,8 @@ verify_accept_kernel(const VerifyParams p) {
             for (int u = 0; u < 12; ++u) {
                 const int i = i0 + 32 * u;
                 if (i < nparts) {
-                    const int row = i / ns < Kb ? i / ns : Kb;
-                    int cnt;
-                    const LseDraw* src = row_src(row, cnt);
-                    c[u] = __ldcg(reinterpret_cast<const float4*>(src) + (i - row * ns));
+                    const int row = i / ns;
+                    c[u] = __ldcg(reinterpret_cast<const float4*>(rows + row * rstride) + (i - row * ns));
                 }
             }
 #pragma unroll
@@ -331,33 +363,28 @@ verify_accept_kernel(const VerifyParams p) {
             }
         }
         __syncwarp();
-        // LPR lanes per row (a power of two with (K_b + 1) * LPR <= 32) fold
-        // every LPR-th partial of their row, then a shuffle tree joins them
+        // LPR lanes per row (a power of two with K_b * LPR <= 32) fold every
+        // LPR-th partial of their row, then a shuffle tree joins them
         int LPR = 32;
-        while (LPR > 1 && (Kb + 1) * LPR > 32) LPR >>= 1;
+        while (LPR > 1 && Kb * LPR > 32) LPR >>= 1;
         const int row = lane / LPR, sub = lane - row * LPR;
         LseDraw a = lsedraw_empty();
-        if (row <= Kb) {
-            const int cnt = row < Kb ? ns : nsub;
-            for (int sg = sub; sg < cnt; sg += LPR) {
+        if (row < Kb)
+            for (int sg = sub; sg < ns; sg += LPR) {
                 const float4 c = s_part[row * ns + sg];
                 a = lsedraw_merge(a, LseDraw{c.x, c.y, c.z, __float_as_int(c.w)});
             }
-        }
         for (int m = 1; m < LPR; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
         const float lse_row = a.m + logf(a.s);         // on lanes row * LPR
         lse_mine = __shfl_sync(0xffffffffu, lse_row, (lane * LPR) & 31);
-        bonus_idx = __shfl_sync(0xffffffffu, a.idx, Kb * LPR);
     } else {
-        for (int i = 0; i <= Kb; ++i) {
-            int cnt;
-            const LseDraw* part = row_src(i, cnt);
+        for (int i = 0; i < Kb; ++i) {
+            const LseDraw* part = rows + i * rstride;
             LseDraw a = lsedraw_empty();
-            for (int sg = lane; sg < cnt; sg += 32) a = lsedraw_merge(a, part[sg]);
+            for (int sg = lane; sg < ns; sg += 32) a = lsedraw_merge(a, part[sg]);
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
             if (lane == i) lse_mine = a.m + logf(a.s);
-            if (i == Kb) bonus_idx = a.idx;
         }
     }
     bool reject = false, near = false;
@@ -375,8 +402,7 @@ verify_accept_kernel(const VerifyParams p) {
     if (lane == 0) {
         const int A = rej < 0 ? Kb : rej;
         p.ws.acc[b] = A;
-        p.ws.rej[b] = rej;
-        p.ws.fin[b] = bonus_idx;
+        p.ws.rej[b] = rej;      // the final token: the residual draw (rej >= 0) or the bonus pass
         if (rej >= 0) p.ws.lse_rej[b] = make_float2(lse_rej, p.lse_q[(size_t)b * gamma + rej]);
         p.accepted[b] = A;
     }
@@ -595,14 +621,45 @@ verify_compact_kernel(const VerifyParams p) {
 
 template <typename TT>
 cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
-    const long long items = (long long)p.B * (p.tgt_slots > 0 ? 1 : p.gamma + 1) * p.ws.nseg;
-    const int g1 = (int)(items < 2LL * num_sms() ? items : 2LL * num_sms());
     const size_t smem1 = 128 + (size_t)kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16 +
                          sizeof(int2) * kStreamStages + (p.B <= kStreamKCache ? sizeof(int) * (size_t)p.B : 0);
-    cudaError_t e1 = cudaFuncSetAttribute(verify_stream_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-    if (e1 != cudaSuccess) return e1;
-    verify_stream_kernel<TT><<<g1, kStreamThreads, smem1, s>>>(p);
+    auto stream_grid = [&](long long items) {
+        return (int)(items < 2LL * num_sms() ? items : 2LL * num_sms());
+    };
+    // The bonus draws ride in the log-sum-exp stream (kStreamAll) while its
+    // fp32 rows keep it bound by HBM, which hides them.  A bf16 target halves
+    // the bytes and leaves the draws exposed, full-prefix mode has no stream
+    // before the accept walk, and the stored-logits path serves small steps:
+    // there the draws run after the walk, for the requests that emit them.
+    const bool deferred = p.target_bf16 || p.tgt_slots > 0 || p.zlog != nullptr;
+    const long long lse_items = (long long)p.B * p.gamma * p.ws.nseg;
+    const long long bonus_items = (long long)p.B * p.ws.nseg;
+    cudaError_t e0 = cudaSuccess;
+    if (!deferred) {
+        e0 = cudaFuncSetAttribute(verify_stream_kernel<TT, kStreamAll>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem1);
+        if (e0 != cudaSuccess) return e0;
+        verify_stream_kernel<TT, kStreamAll>
+            <<<stream_grid(bonus_items + lse_items), kStreamThreads, smem1, s>>>(p);
+    } else if (p.tgt_slots == 0) {
+        e0 = cudaFuncSetAttribute(verify_stream_kernel<TT, kStreamLse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem1);
+        if (e0 != cudaSuccess) return e0;
+        verify_stream_kernel<TT, kStreamLse><<<stream_grid(lse_items), kStreamThreads, smem1, s>>>(p);
+    }
     verify_accept_kernel<TT><<<p.B, 32, 0, s>>>(p);
+    // the final token: the residual draw of the rejected requests (and, when
+    // deferred, the bonus draw of the others), then the ragged layout
+    auto finish = [&]() {
+        if (deferred) {
+            cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<TT, kStreamBonus>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+            if (e != cudaSuccess) return e;
+            verify_stream_kernel<TT, kStreamBonus><<<stream_grid(bonus_items), kStreamThreads, smem1, s>>>(p);
+        }
+        verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    };
     const int nchunks = (p.B + kBC - 1) / kBC;
     const int ntiles = (p.V + kTV - 1) / kTV;
     int gx = (4 * num_sms()) / nchunks;
@@ -615,15 +672,13 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
         auto kern = verify_residual_simt_kernel<float, float, TT, true>;
         const size_t smem_z = sizeof(float) * (size_t)kBC * (kTV + 4);
         kern<<<g2, kResThreads, smem_z, s>>>(p);
-        verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
-        return cudaGetLastError();
+        return finish();
     }
     if (p.state && !resid_rows_supported(p)) return cudaErrorNotSupported;   // RNN rows: tensor-core path only
     if (p.state || (resid_rows_supported(p) && !getenv("DSPARK_RESID_SIMT"))) {
         const cudaError_t e = launch_resid_rows(p, s);
         if (e != cudaSuccess) return e;
-        verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
-        return cudaGetLastError();
+        return finish();
     }
 #define DSPARK_RES_LAUNCH(WT, UT)                                                                    \
     do {                                                                                             \
@@ -637,8 +692,7 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
         if (p.U_bf16) DSPARK_RES_LAUNCH(float, uint16_t); else DSPARK_RES_LAUNCH(float, float);
     }
 #undef DSPARK_RES_LAUNCH
-    verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return finish();
 }
 
 }  // namespace
