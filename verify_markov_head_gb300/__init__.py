@@ -396,6 +396,15 @@ class StepBuffers:
         # reads the rejected row instead of rebuilding it (the latency path)
         self.logits = (torch.empty((B, gamma, V), **f32) if B * gamma * V * 4 <= STORE_LOGITS_BYTES else None)
         self.ws = Workspace(B, gamma, V, r, device)
+        # scheduler off: the verify lengths are gamma for every request, and
+        # the confidence head and the scheduler run beside the verify on a
+        # side stream (nothing the verify reads depends on them)
+        self.K_full = torch.full((B,), gamma, **i32)
+        self.verify_items = B * (gamma + 1) * -(-V // 32768)     # verify-stream work items (32768-entry segments)
+        self.sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.side = torch.cuda.Stream(device=device)
+        self.fork = torch.cuda.Event()
+        self.join = torch.cuda.Event()
 
 
 def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_base=0, log_surv_hist=None,
@@ -421,14 +430,28 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
                             stream=stream)
     else:
         raise ValueError(f"unknown head {head!r}")
+    main = stream if stream is not None else torch.cuda.current_stream()
+    # confidence and scheduler off the verify's critical path: with the
+    # scheduler off nothing the verify reads depends on them, and a verify
+    # stream too small to fill the GPU leaves SMs for them to run beside it
+    # (a full one holds every SM's registers, and they would only run later)
+    side = int(mode) == 0 and buf.verify_items < 2 * buf.sms
+    if side:
+        buf.fork.record(main)
+        buf.side.wait_event(buf.fork)
+    conf_stream = buf.side if side else stream
     dspark_confidence_sts(inp["h"], inp["emb"], inp["anchor"], buf.draft_tok, inp["w_c"], inp["b_c"], inp["T"],
-                          buf.conf_cal, buf.log_surv, buf.ws, stream=stream)
+                          buf.conf_cal, buf.log_surv, buf.ws, stream=conf_stream)
     dspark_schedule(buf.log_surv, inp["sps"], mode, buf.K, buf.n_total, buf.theta, buf.ws,
-                    log_surv_hist=log_surv_hist, stream=stream)
-    K = None if fused else buf.K    # full-prefix mode: K_b = gamma, rows 0..gamma-1 already reduced
+                    log_surv_hist=log_surv_hist, stream=conf_stream)
+    if side:
+        buf.join.record(buf.side)
+    # full-prefix mode: rows 0..gamma-1 already reduced by the draft (K = None);
+    # scheduler off: K_b = gamma from the constant buffer
+    K = None if fused else (buf.K_full if side else buf.K)
     if head == "rnn":
         dspark_verify_rnn(inp["target"], inp["U"], buf.state, inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q,
-                          buf.z_tok, buf.K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
+                          buf.z_tok, K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
                           buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
                           p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
     elif buf.logits is not None:
@@ -442,6 +465,8 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
                       buf.z_tok, K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off,
                       buf.next_anchor, buf.ws, tau=tau, seed=seed, step=step, req_base=req_base,
                       p_tok=buf.p_tok if p_tok else None, near_ties=buf.near_ties, stream=stream)
+    if side:
+        main.wait_event(buf.join)      # the step ends when both streams have
 
 
 class GlobalSchedule:
