@@ -116,10 +116,12 @@ dspark_status dspark_draft_markov(
 /*
  * The draft of dspark_draft_markov fused with the first pass of a full-prefix
  * verification [P2 §形式化定义] (every draft position is checked against the
- * target's distribution at that position).  While position k streams U[b,k-1,:], the same launch streams
- * target[b,k-1,:] and reduces it to partial log-sum-exps of target/tau,
- * kept in ws; a following dspark_verify or dspark_verify_logits with K = NULL
- * uses them instead of reading rows 0..gamma-1 of the target again.
+ * target's distribution at that position).  The same launch reads target rows
+ * 0..gamma-1 and reduces them to partial log-sum-exps of target/tau, kept in
+ * ws: at B <= 64 on a few SMs of its own beside the draft, otherwise in the
+ * draft's epilogue as position k streams U[b,k-1,:].  A following
+ * dspark_verify or dspark_verify_logits with K = NULL uses them instead of
+ * reading those rows again, and draws the bonus tokens after its accept walk.
  * Inputs : those of dspark_draft_markov, plus target [B,gamma+1,V] fp32
  *          (target_t = DSPARK_F32; row gamma, the bonus row, is not read here).
  * Outputs: those of dspark_draft_markov (identical values); ws holds the

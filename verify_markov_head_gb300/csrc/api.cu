@@ -316,11 +316,18 @@ static dspark_status verify_impl(const void* target, dspark_dtype target_t, cons
     p.state = state;
     p.zlog = zlog;
     if (!K) {
-        // full prefix: rows 0..gamma-1 were reduced by dspark_draft_markov_target
-        // on these inputs (the accept kernel checks the token it left)
+        // full prefix after dspark_draft_markov_target on these inputs (the
+        // accept kernel checks the token it left): either its launch ran the
+        // verify stream as a role, or its epilogue reduced rows 0..gamma-1
         if (state) return DSPARK_ERR_UNSUPPORTED;
-        p.tgt_slots = draft_rows_grid_x(B, V, p.ws.parts);
-        if (p.tgt_slots > kTgtSlots) return DSPARK_ERR_UNSUPPORTED;
+        DraftParams d = draft_view(p);
+        d.target = static_cast<const float*>(target);
+        if (target_t == DSPARK_F32 && draft_target_vs(d)) {
+            p.vs_full = 1;
+        } else {
+            p.tgt_slots = draft_rows_grid_x(B, V, p.ws.parts);
+            if (p.tgt_slots > kTgtSlots) return DSPARK_ERR_UNSUPPORTED;
+        }
         p.tgt_token = tgt_token_of(target, seed, step, req_base, B, gamma, V, tau);
     }
     if (zlog && (!is_device_ptr(zlog) || !aligned(zlog, 16))) return DSPARK_ERR_INVALID;

@@ -55,6 +55,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
+#include "vstream.cuh"
 
 namespace dspark {
 namespace {
@@ -132,7 +133,16 @@ struct RowsArgs {
     uint32_t* near_ties;
     // RNN head (kRnn only): the GRU steps run in the prologue and at the position boundaries
     GruParams gru;
+    // verify-stream role (kVs only): CTAs gxd .. gridDim.x-1 run the verify
+    // stream of a full-prefix verification with these parameters
+    int gxd;
+    VerifyParams vp;
 };
+
+// Shared memory of one verify-stream instance in the stream role, 128-byte aligned.
+__host__ __device__ constexpr uint32_t vs_inst_bytes(int B) {
+    return (uint32_t)((vstream_smem_bytes(B) + 127) & ~(size_t)127);
+}
 
 // Target stream: adds 2^(x_j * sc - m) over the entries j < n of N columns
 // of one row to its running base-2 log-sum-exp state (m, s).  The reference m
@@ -352,13 +362,6 @@ __device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
 // gather and the gate arithmetic.  Other CTAs' state rows are read through L2.
 __device__ __forceinline__ float bf16f_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16f_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float a) {
-    a = fmaf(bf16f_lo(w.x), bf16f_lo(x.x), a); a = fmaf(bf16f_hi(w.x), bf16f_hi(x.x), a);
-    a = fmaf(bf16f_lo(w.y), bf16f_lo(x.y), a); a = fmaf(bf16f_hi(w.y), bf16f_hi(x.y), a);
-    a = fmaf(bf16f_lo(w.z), bf16f_lo(x.z), a); a = fmaf(bf16f_hi(w.z), bf16f_hi(x.z), a);
-    a = fmaf(bf16f_lo(w.w), bf16f_lo(x.w), a); a = fmaf(bf16f_hi(w.w), bf16f_hi(x.w), a);
-    return a;
-}
 __device__ __forceinline__ float dot8(const uint4 w, const float4 h0, const float4 h1, float a) {
     a = fmaf(bf16f_lo(w.x), h0.x, a); a = fmaf(bf16f_hi(w.x), h0.y, a);
     a = fmaf(bf16f_lo(w.y), h0.z, a); a = fmaf(bf16f_hi(w.y), h0.w, a);
@@ -484,16 +487,35 @@ __device__ __forceinline__ void gate_step(const GruParams& g, int ks, int cta, i
 // waits on another's progress.  Nothing prefetches U or the target into L2:
 // the extra L2 footprint evicts W2, whose re-reads from HBM cost more than
 // the latency a prefetch hides.
-template <bool kResid, typename TT, bool kRnn = false, bool kOneRow = false, bool kTgt = false>
+template <bool kResid, typename TT, bool kRnn = false, bool kOneRow = false, bool kTgt = false, bool kVs = false>
 __global__ void __launch_bounds__(kThreads, 1)
 rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_last) {
     static_assert(!(kTgt && (kResid || kRnn)), "the target stream belongs to the Markov draft");
+    static_assert(!(kVs && (kResid || kRnn || kTgt)), "the stream role belongs to the plain Markov draft");
     const DraftParams& p = a.p;
     const int NC = a.NC;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
+    if constexpr (kVs) {
+        if ((int)blockIdx.x >= a.gxd) {
+            // verify-stream role: the walked rows' log-sum-exps (the bonus
+            // draws, a random number per entry, wait for the accept walk and
+            // its rejections); two instances of 9 warps, each with its own
+            // ring (warp 18 idles); they share the stream's work counter with
+            // the other stream CTAs and never touch the draft's state
+            const int inst = (int)threadIdx.x / kStreamThreads;
+            if (inst < 2) {
+                const uint32_t off = (uint32_t)inst * vs_inst_bytes(a.vp.B);
+                vstream_run<float, kStreamLse>(a.vp, gbase + off, base + off, (int)threadIdx.x - inst * kStreamThreads,
+                                               1 + inst, blockIdx.x == (unsigned)a.gxd && inst == 0,
+                                               2u * (gridDim.x - (unsigned)a.gxd));
+            }
+            return;
+        }
+    }
+    const int GX = kVs ? a.gxd : (int)gridDim.x;   // CTAs of the draft itself
     const Layout L = rows_layout(NC, p.r, kResid, kTgt);
     const int KCH = p.r / 64;
     const int RF = 128 / NC;                      // vocabulary tiles per accumulator
@@ -528,7 +550,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     const int V = p.V, gamma = p.gamma, r = p.r;
     const uint16_t* W1 = static_cast<const uint16_t*>(p.W1);
     const float* st_base = p.state ? p.state + (size_t)b_base * p.r : nullptr;   // RNN head rows of this chunk
-    const uint32_t nctas = gridDim.x * gridDim.y;
+    const uint32_t nctas = (uint32_t)GX * gridDim.y;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), 1); }
@@ -547,7 +569,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         ptx::prefetch_tmap(&a.umap);
         if constexpr (kTgt) ptx::prefetch_tmap(&a.tmap);
     }
-    if (kTgt && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.ws.tgt_token = p.tgt_token;
+    if ((kTgt || kVs) && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.ws.tgt_token = p.tgt_token;
     if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 512u); ptx::tmem_relinquish(); }
     for (int n = tid; n < 128; n += kThreads) {
         int x = -1, prow = -1;
@@ -573,7 +595,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         // anchors), shared out over the CTAs like the later ones
         if (warp < kEpiWarps) {
             __shared__ int s_pro_ok;
-            const int cta_id = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+            const int cta_id = (int)(blockIdx.y * GX + blockIdx.x);
             gh_compute(a.gru, -1, cta_id, (int)nctas, warp, lane);
             ptx::named_barrier(1, 32 * kEpiWarps);
             gate_step(a.gru, 0, cta_id, (int)nctas, tid, 32 * kEpiWarps, nullptr, p.ws.win);
@@ -609,7 +631,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             bool ok = true;
             long long nw = 0;                            // W2 chunks issued
             for (int k = k_first; k <= k_last && ok; ++k) {
-                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                for (int t = blockIdx.x; t < ntiles && ok; t += GX) {
                     const int vs = t * kTN * RF;
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
@@ -644,7 +666,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             int lt = 0;                                  // tiles issued, over all positions
             long long nu = 0;                            // U slices issued
             for (int k = k_first; k <= k_last && ok; ++k) {
-                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+                for (int t = blockIdx.x; t < ntiles && ok; t += GX, ++lt) {
                     const int vs = t * kTN * RF;
                     for (int c = 0; c < 4 && ok; ++c) {
                         const int n = lt * 4 + c, s = n % US;
@@ -676,7 +698,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             bool ok = true;
             for (int k = k_first; k <= k_last && ok; ++k) {
                 bool wait_a = k > k_first;   // h of this position is staged by the epilogue warps
-                for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+                for (int t = blockIdx.x; t < ntiles && ok; t += GX, ++lt) {
                     if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) { site = 4; break; }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc0 + (uint32_t)(acc * kTN);
@@ -751,7 +773,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             // W_hh . state[0] for the first boundary's GRU step, while the MMA
             // starts the first position
             if (k_first < k_last)
-                gh_compute(a.gru, k_first - 1, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, warp, lane);
+                gh_compute(a.gru, k_first - 1, (int)(blockIdx.y * GX + blockIdx.x), (int)nctas, warp, lane);
         }
         int acc = 0;
         uint32_t aph = 0;
@@ -790,7 +812,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             float rE2h = INFINITY;                     // rE2 * kRaceRel: the screen's threshold
             Draw2 st2 = draw2_empty();
             float tm2 = -INFINITY, tsum = 0.f;         // target stream: this row's base-2 log-sum-exp state
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            for (int t = blockIdx.x; t < ntiles; t += GX) {
                 bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 6); failed = true; break; }
@@ -833,7 +855,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         }
                     }
                     __syncwarp();
-                    const int tn = t + (int)gridDim.x;
+                    const int tn = t + GX;
                     if (tn < ntiles) {
                         issue_rows<float>(ubuf, Urow, real_mask, tn * kTN * RF + ti * kTN + 32 * cb, V, lane);
                         ptx::cp_async_wait_group<1>();         // this tile's target rows
@@ -996,7 +1018,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                             else if (nh > 0) tgt_lse_add<true>(tv, nh, scale2, tm2, tsum);
                         }
                         __syncwarp();
-                        int tn = t + (int)gridDim.x, kn = k;
+                        int tn = t + GX, kn = k;
                         if (tn >= ntiles) { tn = blockIdx.x; ++kn; }
                         if (kn <= k_last) {
                             if (lane == 0) tgt_issue(tn, kn);
@@ -1096,7 +1118,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 if constexpr (kRnn) {
                     // RNN head: the GRU step for every request, shared out by
                     // hidden unit over the CTAs, then a second grid barrier
-                    gate_step(a.gru, k, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, etid,
+                    gate_step(a.gru, k, (int)(blockIdx.y * GX + blockIdx.x), (int)nctas, etid,
                               32 * kEpiWarps, gridDim.y == 1 ? s_tok : nullptr, p.ws.win);
                     ptx::named_barrier(1, 32 * kEpiWarps);
                     if (etid == 0)
@@ -1119,20 +1141,20 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 if constexpr (kRnn) {
                     // W_hh . state[k] for the next boundary's GRU step, off its critical path
                     if (k + 1 < k_last)
-                        gh_compute(a.gru, k, (int)(blockIdx.y * gridDim.x + blockIdx.x), (int)nctas, warp, lane);
+                        gh_compute(a.gru, k, (int)(blockIdx.y * GX + blockIdx.x), (int)nctas, warp, lane);
                 }
             }
             // ---- this position's outputs, while the MMA starts the next one: the
             //      CTAs share the requests, a warp folds one request's partials
-            for (int n = blockIdx.x + warp * (int)gridDim.x; n < nb; n += kEpiWarps * (int)gridDim.x) {
+            for (int n = blockIdx.x + warp * GX; n < nb; n += kEpiWarps * GX) {
                 const float4* part = reinterpret_cast<const float4*>(part_buf + (size_t)(b_base + n) * p.ws.parts);
                 DrawLse m = drawlse_empty();
-                for (int i0 = lane; i0 < (int)gridDim.x; i0 += 4 * 32) {
+                for (int i0 = lane; i0 < GX; i0 += 4 * 32) {
                     float4 c[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int i = i0 + 32 * u;
-                        c[u] = i < (int)gridDim.x ? __ldcg(part + i) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+                        c[u] = i < GX ? __ldcg(part + i) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
                     }
 #pragma unroll
                     for (int u = 0; u < 4; ++u) m = drawlse_merge(m, drawlse_of(c[u]));
@@ -1186,7 +1208,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     __syncthreads();
     if (tid == 0) {
         const unsigned prev = atomicAdd(ticket, 1u);
-        s_last = (prev == gridDim.x - 1);
+        s_last = (prev == (unsigned)GX - 1);
     }
     __syncthreads();
     if (!s_last) return;
@@ -1196,7 +1218,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     const int k = k_first;
     const int TM = (32 * kEpiWarps) / NC;
     const int n = tid / TM, sub = tid - n * TM;
-    const int nparts = (int)gridDim.x;
+    const int nparts = GX;
     constexpr int kBatch = 5;
     if (tid < 32 * kEpiWarps) {
         const int bb = b_base + n;
@@ -1291,9 +1313,11 @@ bool cooperative_supported() {
     return cached[dev] == 1;
 }
 
+constexpr int kVsCtas = 16;   // CTAs of the verify-stream role (two stream instances each)
+
 static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bool resid, const void* target,
                                bool target_bf16, uint32_t* near_ties, cudaStream_t s,
-                               const GruParams* gru = nullptr) {
+                               const GruParams* gru = nullptr, const VerifyParams* vp = nullptr) {
     auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
     if (!enc) return cudaErrorNotSupported;
     RowsArgs a;
@@ -1324,7 +1348,8 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
     }
     // the target stream (Markov draft only): target [B][gamma+1][V] fp32, one
     // epilogue warp's block
-    const bool tgt = !resid && !gru && p.target != nullptr;
+    const bool vs = vp != nullptr;                  // verify-stream role beside the plain draft
+    const bool tgt = !resid && !gru && !vs && p.target != nullptr;
     if (tgt) {
         const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)(p.gamma + 1), (cuuint64_t)p.B};
         const cuuint64_t strides[2] = {(cuuint64_t)p.V * 4, (cuuint64_t)(p.gamma + 1) * p.V * 4};
@@ -1336,17 +1361,28 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
             return cudaErrorInvalidValue;
     }
     const Layout L = rows_layout(a.NC, p.r, resid, tgt);
-    const size_t smem = L.total + 1024;
+    size_t smem = L.total + 1024;
+    if (vs) smem = smem > 1024 + 2 * (size_t)vs_inst_bytes(p.B) ? smem : 1024 + 2 * (size_t)vs_inst_bytes(p.B);
     auto kern = resid ? (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>)
                 : gru ? rows_kernel<false, float, true>
                 : tgt ? (p.B == 1 ? rows_kernel<false, float, false, true, true> : rows_kernel<false, float, false, false, true>)
+                : vs ? (p.B == 1 ? rows_kernel<false, float, false, true, false, true>
+                                 : rows_kernel<false, float, false, false, false, true>)
                       : (p.B == 1 ? rows_kernel<false, float, false, true> : rows_kernel<false, float>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nchunks = (p.B + a.NC - 1) / a.NC;
-    const int gx = draft_rows_grid_x(p.B, p.V, p.ws.parts);
+    int gx = draft_rows_grid_x(p.B, p.V, p.ws.parts);
     if (tgt && gx > kTgtSlots) return cudaErrorInvalidConfiguration;
-    const dim3 grid(gx, nchunks);
+    int gs = 0;                                     // stream-role CTAs
+    if (vs) {
+        if (nchunks != 1 || k_last == k_first) return cudaErrorInvalidConfiguration;
+        if (gx > num_sms() - kVsCtas) gx = num_sms() - kVsCtas;
+        a.gxd = gx;
+        a.vp = *vp;
+        gs = kVsCtas;
+    }
+    const dim3 grid(gx + gs, nchunks);
     if (k_last > k_first) {
         // every CTA waits for all others between positions: they must be co-resident
         void* args[] = {&a, const_cast<int*>(&k_first), const_cast<int*>(&k_last)};
@@ -1364,10 +1400,34 @@ bool draft_target_supported(const DraftParams& p) {
     return rows_supported(p) && p.target != nullptr && draft_rows_grid_x(p.B, p.V, p.ws.parts) <= kTgtSlots;
 }
 
-// The Markov draft with the target stream: one cooperative launch for the
-// gamma positions, else one launch per position (the rows kernel merges a
-// single position's partials itself).
+// One chunk of requests (B <= 64), several positions in one cooperative
+// launch, and SMs to spare: the verify stream runs as a role of the draft
+// launch, on kVsCtas SMs of its own.
+bool draft_target_vs(const DraftParams& p) {
+    return rows_supported(p) && p.target != nullptr && p.B <= 64 && p.gamma > 1 && cooperative_supported() &&
+           !getenv("DSPARK_DRAFT_PER_POSITION") && num_sms() >= 4 * kVsCtas;
+}
+
+// The Markov draft with the target stream: with the verify-stream role when
+// draft_target_vs holds; otherwise the epilogue warps reduce the target rows
+// themselves, in one cooperative launch for the gamma positions or one
+// launch per position (the rows kernel merges a single position's partials
+// itself).
 cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s) {
+    if (draft_target_vs(p)) {
+        VerifyParams v;
+        v.target = p.target; v.target_bf16 = 0;
+        v.U = p.U; v.U_bf16 = p.U_bf16; v.W1 = p.W1; v.W2 = p.W2; v.W_bf16 = p.W_bf16;
+        v.anchor = p.anchor; v.draft_tok = p.draft_tok; v.lse_q = p.lse_q; v.z_tok = p.z_tok; v.K = nullptr;
+        v.B = p.B; v.gamma = p.gamma; v.V = p.V; v.r = p.r; v.req_base = p.req_base;
+        v.inv_tau = p.inv_tau; v.seed = p.seed; v.step = p.step;
+        v.accepted = nullptr; v.out_tok = nullptr; v.out_req = nullptr; v.out_pos = nullptr;
+        v.out_off = nullptr; v.next_anchor = nullptr; v.p_tok = nullptr; v.near_ties = nullptr;
+        v.ws = p.ws;
+        DraftParams q = p;
+        q.target = nullptr;                         // the draft part is the plain draft (it keeps the token)
+        return launch_rows(q, 1, p.gamma, false, nullptr, false, nullptr, s, nullptr, &v);
+    }
     if (!draft_target_supported(p)) return cudaErrorNotSupported;
     if (p.gamma > 1 && cooperative_supported() && !getenv("DSPARK_DRAFT_PER_POSITION"))
         return launch_rows(p, 1, p.gamma, false, nullptr, false, nullptr, s);

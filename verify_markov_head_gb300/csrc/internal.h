@@ -134,6 +134,10 @@ struct VerifyParams {
     // verify stream covers only the bonus rows
     int tgt_slots = 0;
     unsigned long long tgt_token = 0;
+    // full-prefix mode after a draft that ran the verify stream in its own
+    // launch (the stream role): the walked rows' partials are already in the
+    // workspace; the bonus draws follow the accept walk
+    int vs_full = 0;
 };
 
 struct StsFitParams {
@@ -156,6 +160,7 @@ bool draft_rows_supported(const DraftParams& p);
 cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cudaStream_t s);
 int draft_rows_grid_x(int B, int V, int parts);   // CTAs along V of a draft rows launch
 bool draft_target_supported(const DraftParams& p);
+bool draft_target_vs(const DraftParams& p);       // the target-stream draft runs the verify stream as a role
 cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s);   // the draft with the target stream
 bool cooperative_supported();
 void* tma_encoder();   // cuTensorMapEncodeTiled from the driver, or NULL
