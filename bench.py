@@ -569,7 +569,7 @@ def d_of(w):
 
 # Sources the draft kernel is compiled from: DRAM traffic taken from an ncu
 # capture is reported only while they are unchanged since the capture.
-_DRAFT_SOURCES = ("draft_rows.cu", "common.cuh", "sm100_ptx.cuh", "internal.h")
+_DRAFT_SOURCES = ("draft_rows.cu", "common.cuh", "sm100_ptx.cuh", "internal.h", "vstream.cuh")
 
 
 def _draft_source_hash():
