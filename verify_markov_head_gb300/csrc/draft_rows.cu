@@ -47,6 +47,12 @@
 // kept for the case p <= q everywhere.  Each thread reads its own row of U and
 // of the target logits (the rejected rows differ per request, so no common
 // TMA box exists): D is h.W2 alone and no U slice ring is used.
+//
+// Two variants also do the first pass of a full-prefix verification (every
+// draft checked against the target, section 形式化定义), the log-sum-exps of
+// target rows 0..gamma-1: kVs runs it as a role of the launch, on 16 CTAs of
+// its own beside the draft's (the verify stream's body, vstream.cuh); kTgt
+// has the epilogue warps fold each tile's target block after their race.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
