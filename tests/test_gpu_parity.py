@@ -456,3 +456,42 @@ def test_verify_from_stored_draft_logits(B, V, r, wdt):
         if not bad[b] and fin[b] != ref["final_tok"][b]:
             assert ref["diag"][b, 1] < GAP_EPS, f"unflagged final-token mismatch at request {b}"
     assert (np.diff(off) == acc + 1).all()
+
+
+@pytest.mark.parametrize("wdt", [torch.bfloat16, torch.float32])
+def test_residual_without_mass_draws_from_p(wdt):
+    """The fallback of the residual draw ("DSpark：半自回归生成与置信度调度的投机解码",
+    section 形式化定义: at the first rejection the token comes from
+    max(0, p - q), and from p when that has no mass).  lse_q is passed 20
+    nats too low, so q = e^20 q_true: the first draft is rejected and
+    p - q < 0 at every entry.  The emitted token must be the draw from p on
+    the rejected row with the residual's noise, argmax_v t_v / tau + G(domain
+    2, row (b)(gamma+1) + 0, v), computed here with the oracle's Gumbel
+    stream; every request is counted as a fallback draw."""
+    w = workload.custom("tiny", B=5, V=4104, r=64, w_dtype=wdt, w_std=0.1, seed=61)
+    inp = workload.inputs(w, device=DEV)
+    seed, tau = 7, 1.0
+    buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
+    vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok, buf.ws,
+                           seed=seed)
+    lse_fake = (buf.lse_q - 20.0).contiguous()
+    K = torch.full((w.B,), w.gamma, dtype=torch.int32, device=DEV)
+    buf.near_ties.zero_()
+    vm.dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], buf.draft_tok, lse_fake,
+                     buf.z_tok, K, buf.accepted, buf.out_tok, buf.out_req, buf.out_pos, buf.out_off, buf.next_anchor,
+                     buf.ws, seed=seed, tau=tau, near_ties=buf.near_ties)
+    st, bits = vm.dspark_sync_status(buf.ws.buf)
+    assert st == 0, bits
+    acc = buf.accepted.cpu().numpy()
+    assert (acc == 0).all()
+    assert int(buf.near_ties[1]) == w.B
+    off = buf.out_off.cpu().numpy()
+    fin = buf.out_tok.cpu().numpy()[off[:-1]]
+    t = inp["target"].double().cpu().numpy()
+    for b in range(w.B):
+        row = b * (w.gamma + 1) + 0
+        g = np.array([oracle.gumbel(seed, 0, 2, row, v) for v in range(w.V)])
+        score = t[b, 0] / tau + g
+        order = np.argsort(-score, kind="stable")
+        if fin[b] != order[0]:
+            assert score[order[0]] - score[order[1]] < GAP_EPS, f"request {b}: {fin[b]} != {order[0]}"

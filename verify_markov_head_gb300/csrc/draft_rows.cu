@@ -211,6 +211,49 @@ __device__ __forceinline__ void lse2_merge(float& m, float& s, const float2 e) {
     else s += e.y * fast_exp2(e.x - m);
 }
 
+// The residual draw's fallback law p for request bb, whose residual
+// max(0, p - q) had no mass at all (only rounding produces that): the draw
+// from p on the rejected row urow with the residual's noise E (domain 2), by
+// the whole CTA over the row, lowest index on ties.  Kept out of line so its
+// registers do not weigh on the kernel's tile loop.
+template <typename TT>
+__device__ __noinline__ void resid_fallback_draw(const DraftParams& p, const void* target, int bb, int urow) {
+    __shared__ float s_fkey[32];
+    __shared__ int s_fidx[32];
+    const int tid = (int)threadIdx.x, lane = tid % 32, warp = tid / 32, nwarps = (int)blockDim.x / 32;
+    const int gamma = p.gamma, V = p.V;
+    const float scale2 = p.inv_tau * 1.4426950408889634f;
+    const StreamRK rng(p.seed, p.step, 2u, (uint32_t)(p.req_base + bb) * (uint32_t)(gamma + 1) + (uint32_t)urow);
+    const TT* trow = static_cast<const TT*>(target) + ((size_t)bb * (gamma + 1) + urow) * V;
+    const float lse_p2 = p.ws.lse_rej[bb].x * 1.4426950408889634f;
+    float key = INFINITY;
+    int idx = 0x7fffffff;
+    for (int qd = tid; qd < V / 4; qd += (int)blockDim.x) {
+        const uint4 w = rng.quad((uint32_t)qd);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float pv = fast_exp2(fmaf(to_f32(trow[4 * qd + e]), scale2, -lse_p2));
+            const float E = exp2_variate_of(ws[e]) * kLn2;
+            if (pv > 0.f && E < key * pv) { key = E / pv; idx = 4 * qd + e; }
+        }
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, key, sh);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, sh);
+        if (ok < key || (ok == key && oi < idx)) { key = ok; idx = oi; }
+    }
+    if (lane == 0) { s_fkey[warp] = key; s_fidx[warp] = idx; }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w2 = 1; w2 < nwarps; ++w2)
+            if (s_fkey[w2] < key || (s_fkey[w2] == key && s_fidx[w2] < idx)) { key = s_fkey[w2]; idx = s_fidx[w2]; }
+        p.ws.fin[bb] = idx;
+    }
+    __syncthreads();
+}
+
 // Bounded grid-wide barrier on a counter in global memory: every CTA adds 1,
 // then waits until all `target` CTAs have.  The kernel is launched
 // cooperatively, so all CTAs are resident.  Returns false on expiry or abort.
@@ -812,7 +855,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             const float lse_p2 = lse.x * 1.4426950408889634f, lse_q2 = lse.y * 1.4426950408889634f;
             // residual mode: E / r of the r-draw's winner, E / p of the p-draw's
             // (+inf: none yet), and the screens' thresholds
-            float Kr = INFINITY, Kp = INFINITY, Krh = INFINITY, Kph = INFINITY;
+            float Kr = INFINITY, Krh = INFINITY;
             DrawLse st = drawlse_empty();            // idx, zb (u + bias of the winner), s
             float rz2 = -INFINITY, rE2 = INFINITY;     // winner's z*log2e and E2
             float rE2h = INFINITY;                     // rE2 * kRaceRel: the screen's threshold
@@ -870,14 +913,16 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     }
                     __syncwarp();
                     if (real) {
-                        // Both draws as exponential races (argmax log w_v + G_v =
-                        // argmin E_v / w_v, E = -ln u): the residual law r = max(0, p - q)
-                        // and the fallback law p share E.  A quad is screened with the
-                        // bound E >= 1 - u (exact from the bits, no logarithm) against
-                        // the running minima, with margins above the rounding of the
+                        // The draw as an exponential race (argmax log w_v + G_v =
+                        // argmin E_v / w_v, E = -ln u) on the residual law
+                        // r = max(0, p - q).  A quad is screened with the bound
+                        // E >= 1 - u (exact from the bits, no logarithm) against the
+                        // running minimum, with margins above the rounding of the
                         // products and of E; quads that pass are re-run with the exact
                         // E, entries in increasing v (strict comparisons keep the lowest
-                        // index on exact ties).
+                        // index on exact ties).  The fallback law p (no residual mass
+                        // at all, which only rounding can produce) is drawn by the
+                        // merging CTA, on the same E, when no CTA found a winner.
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             const int vq = v0 + 4 * c;
@@ -902,8 +947,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                                     pv[e] = fast_exp2(fmaf(ts[e], scale2, -lse_p2));
                                     rv[e] = pv[e] - fast_exp2(fmaf(z[4 * c + e], scale2, -lse_q2));
                                     const float wv = one_minus_uniform_of(ws[e]);
-                                    cand |= (rv[e] > 0.f && wv < fmaf(Krh, rv[e], kRaceSlack)) ||
-                                            wv < fmaf(Kph, pv[e], kRaceSlack);
+                                    cand |= rv[e] > 0.f && wv < fmaf(Krh, rv[e], kRaceSlack);
                                 }
                                 if (cand) {
 #pragma unroll
@@ -911,9 +955,6 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                                         const float E = exp2_variate_of(ws[e]) * kLn2;
                                         if (rv[e] > 0.f && E < rv[e] * Kr) {
                                             Kr = E / rv[e]; Krh = Kr * kRaceRel; st2.idx_r = vq + e;
-                                        }
-                                        if (E < pv[e] * Kp) {
-                                            Kp = E / pv[e]; Kph = Kp * kRaceRel; st2.idx_p = vq + e;
                                         }
                                     }
                                 }
@@ -1037,7 +1078,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             if constexpr (kResid) {
                 // back to scores: log w_v + G_v = -ln(E_v / w_v)
                 st2.best_r = Kr < INFINITY ? -logf(Kr) : -INFINITY;
-                st2.best_p = Kp < INFINITY ? -logf(Kp) : -INFINITY;
+                st2.best_p = -INFINITY;                      // drawn by the merging CTA if needed
                 reinterpret_cast<Draw2*>(s_merge)[cb * 128 + row] = st2;
             } else {
                 // back to the Gumbel score in natural units: with E = E2 * ln 2 the
@@ -1210,6 +1251,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     // single position: the last-arriving CTA of this request chunk merges the partial states
     uint32_t* ticket = kResid ? &p.ws.tickets_resid[chunk] : &p.ws.tickets_draft[chunk];
     __shared__ int s_last;
+    __shared__ int s_fb[128];                        // residual mode: request needs the fallback draw
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -1251,11 +1293,12 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 }
             }
             for (int sh = 1; sh < TM; sh <<= 1) m = draw2_merge(m, shfl_xor(m, sh));
+            if (n < nb && sub == 0) s_fb[n] = 0;
             if (sub == 0 && n < nb && s_row[n] >= 0) {
                 if (m.best_r > -INFINITY) {
                     p.ws.fin[bb] = m.idx_r;
                 } else {
-                    p.ws.fin[bb] = m.idx_p;
+                    s_fb[n] = 1;                         // no residual mass: draw from p below
                     if (a.near_ties) atomicAdd(&a.near_ties[1], 1u);
                 }
             }
@@ -1283,6 +1326,14 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 p.z_tok[o] = m.zb;
             }
         }
+    }
+    if constexpr (kResid) {
+        // The fallback law p for the requests whose residual r = max(0, p - q)
+        // had no mass at all: the draw from p with the same E (domain 2, the
+        // rejected row), by the whole CTA over the row; lowest index on ties.
+        __syncthreads();
+        for (int nf = 0; nf < nb; ++nf)
+            if (s_fb[nf]) resid_fallback_draw<TT>(p, a.target, b_base + nf, s_row[nf]);   // uniform branch
     }
     if (tid == 0) *ticket = 0u;
 }
