@@ -76,6 +76,37 @@ def test_null_pointers_are_rejected_without_a_device(lib):
     assert lib.dspark_schedule(None, None, None, 32, 4, 7, 9, None, None, None, None, 0, None) == -1
 
 
+def test_target_stream_and_full_prefix_verify_reject_bad_arguments(lib):
+    """dspark_draft_markov_target and a full-prefix dspark_verify (K = NULL)
+    check their arguments on the host: null or host pointers, a bad
+    temperature or an unknown target type return before any launch."""
+    vp = C.c_void_p
+    lib.dspark_draft_markov_target.argtypes = [vp, C.c_int, vp, vp, C.c_int, vp, C.c_int, vp, C.c_int, C.c_int,
+                                               C.c_int, C.c_int, C.c_int, C.c_float, C.c_uint64, C.c_uint64,
+                                               vp, vp, vp, vp, vp, C.c_size_t, vp]
+    args = [None, 0, None, None, 1, None, 0, None, 4, 7, 1024, 64, 0, 1.0, 0, 0, None, None, None, None, None, 0,
+            None]
+    assert lib.dspark_draft_markov_target(*args) == -1          # null pointers
+    host = (C.c_float * 64)()
+    args_host = list(args)
+    for i in (0, 2, 3, 5, 7, 16, 17, 18, 20):
+        args_host[i] = C.cast(host, vp)
+    assert lib.dspark_draft_markov_target(*args_host) == -1     # host memory is not device memory
+    bad_tau = list(args)
+    bad_tau[13] = 0.0
+    assert lib.dspark_draft_markov_target(*bad_tau) == -1
+    bad_type = list(args)
+    bad_type[6] = 7
+    assert lib.dspark_draft_markov_target(*bad_type) == -4      # unknown target type: unsupported
+    lib.dspark_verify.argtypes = [vp, C.c_int, vp, C.c_int, vp, vp, C.c_int, vp, vp, vp, vp, vp,
+                                  C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_float, C.c_uint64, C.c_uint64,
+                                  vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_size_t, vp]
+    st = lib.dspark_verify(None, 0, None, 0, None, None, 1, None, None, None, None, None,   # K = NULL
+                           4, 7, 1024, 64, 0, 1.0, 0, 0, None, None, None, None, None, None, None, None, None,
+                           0, None)
+    assert st == -1
+
+
 def test_package_imports_and_fails_loudly_without_library(tmp_path):
     import subprocess
     import sys
