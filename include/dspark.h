@@ -58,7 +58,7 @@ typedef enum {
     DSPARK_SCHED_ASYNC = 2   /* capacity from survivals two steps old, no early stop [P4 §五] */
 } dspark_sched_mode;
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define DSPARK_MAX_GAMMA 16
 #define DSPARK_MAX_SCHED_ITEMS 4096   /* B * gamma for dspark_schedule */
 #define DSPARK_MAX_STS_GRID 65536     /* candidate temperatures for dspark_sts_fit */
