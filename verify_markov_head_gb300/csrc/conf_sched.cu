@@ -19,6 +19,7 @@
 //   first n with Theta(n+1) <= Theta(n)) or a block argmax (asynchronous).
 #include "common.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace dspark {
 namespace {
@@ -31,6 +32,7 @@ constexpr int kConfThreads = 256;
 // calibrated confidences and the running log-survival.
 template <typename ET>
 __global__ void __launch_bounds__(kConfThreads) confidence_kernel(const ConfParams p) {
+    grid_dependency_wait();
     const int k = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int gamma = p.gamma, d = p.d, e = p.e;
@@ -234,6 +236,7 @@ __device__ void theta_items(SchedSmem& S, const float* ls, const float* sps, int
 }
 
 __global__ void __launch_bounds__(kST) schedule_kernel(const SchedParams p) {
+    grid_dependency_wait();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SchedSmem& S = *reinterpret_cast<SchedSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
@@ -342,16 +345,16 @@ __global__ void __launch_bounds__(kST) schedule_kernel(const SchedParams p) {
 
 cudaError_t launch_confidence(const ConfParams& p, cudaStream_t s) {
     const dim3 grid(p.gamma, p.B);
-    if (p.emb_bf16) confidence_kernel<uint16_t><<<grid, kConfThreads, 0, s>>>(p);
-    else confidence_kernel<float><<<grid, kConfThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    const cudaError_t e = p.emb_bf16 ? launch_dependent(confidence_kernel<uint16_t>, grid, dim3(kConfThreads), 0, s, p)
+                                     : launch_dependent(confidence_kernel<float>, grid, dim3(kConfThreads), 0, s, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s) {
     const size_t smem = sizeof(SchedSmem);
     cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    schedule_kernel<<<1, kST, smem, s>>>(p);
-    return cudaGetLastError();
+    const cudaError_t e = launch_dependent(schedule_kernel, dim3(1), dim3(kST), smem, s, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dspark

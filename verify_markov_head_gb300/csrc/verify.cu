@@ -31,6 +31,7 @@
 #include "internal.h"
 #include "sm100_ptx.cuh"
 #include "vstream.cuh"
+#include "pdl.cuh"
 
 namespace dspark {
 namespace {
@@ -45,6 +46,7 @@ verify_stream_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
+    grid_dependency_wait();
     vstream_run<TT, kMode>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1, blockIdx.x == 0, gridDim.x);
 }
 
@@ -58,6 +60,7 @@ constexpr int kAcceptStaged = 2048;   // partials staged in shared memory (32 KB
 template <typename TT>
 __global__ void __launch_bounds__(32)
 verify_accept_kernel(const VerifyParams p) {
+    grid_dependency_wait();
     const int b = blockIdx.x, lane = threadIdx.x;
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
     const bool full = p.tgt_slots > 0;              // the walked rows' partials are the draft's own
@@ -313,6 +316,7 @@ __global__ void __launch_bounds__(kCompactThreads)
 verify_compact_kernel(const VerifyParams p) {
     __shared__ int s_warp[kCompactThreads / 32];
     __shared__ int s_carry;
+    grid_dependency_wait();
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int gamma = p.gamma;
     if (tid == 0) s_carry = 0;
@@ -384,15 +388,19 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
         e0 = cudaFuncSetAttribute(verify_stream_kernel<TT, kStreamAll>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem1);
         if (e0 != cudaSuccess) return e0;
-        verify_stream_kernel<TT, kStreamAll>
-            <<<stream_grid(bonus_items + lse_items), kStreamThreads, smem1, s>>>(p);
+        e0 = launch_dependent(verify_stream_kernel<TT, kStreamAll>, dim3(stream_grid(bonus_items + lse_items)),
+                              dim3(kStreamThreads), smem1, s, p);
+        if (e0 != cudaSuccess) return e0;
     } else if (p.tgt_slots == 0) {
         e0 = cudaFuncSetAttribute(verify_stream_kernel<TT, kStreamLse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem1);
         if (e0 != cudaSuccess) return e0;
-        verify_stream_kernel<TT, kStreamLse><<<stream_grid(lse_items), kStreamThreads, smem1, s>>>(p);
+        e0 = launch_dependent(verify_stream_kernel<TT, kStreamLse>, dim3(stream_grid(lse_items)), dim3(kStreamThreads),
+                              smem1, s, p);
+        if (e0 != cudaSuccess) return e0;
     }
-    verify_accept_kernel<TT><<<p.B, 32, 0, s>>>(p);
+    e0 = launch_dependent(verify_accept_kernel<TT>, dim3(p.B), dim3(32), 0, s, p);
+    if (e0 != cudaSuccess) return e0;
     // the final token: the residual draw of the rejected requests (and, when
     // deferred, the bonus draw of the others), then the ragged layout
     auto finish = [&]() {
@@ -400,10 +408,12 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
             cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<TT, kStreamBonus>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
             if (e != cudaSuccess) return e;
-            verify_stream_kernel<TT, kStreamBonus><<<stream_grid(bonus_items), kStreamThreads, smem1, s>>>(p);
+            e = launch_dependent(verify_stream_kernel<TT, kStreamBonus>, dim3(stream_grid(bonus_items)),
+                                 dim3(kStreamThreads), smem1, s, p);
+            if (e != cudaSuccess) return e;
         }
-        verify_compact_kernel<<<1, kCompactThreads, 0, s>>>(p);
-        return cudaGetLastError();
+        const cudaError_t e = launch_dependent(verify_compact_kernel, dim3(1), dim3(kCompactThreads), 0, s, p);
+        return e != cudaSuccess ? e : cudaGetLastError();
     };
     const int nchunks = (p.B + kBC - 1) / kBC;
     const int ntiles = (p.V + kTV - 1) / kTV;
