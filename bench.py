@@ -30,6 +30,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -44,6 +45,7 @@ import torch  # noqa: E402
 
 import workload  # noqa: E402
 
+MIN_TIMED_S = 0.5      # the timed region lasts at least this long (clock samples inside it)
 METRIC = "draft+verify tokens/s (B=64, V=151936, γ=7) and % of HBM roofline on 1 GB300"
 
 
@@ -199,7 +201,9 @@ def run_gpu(args):
             graph.replay()
     stream.synchronize()
 
-    # ---- timed region: K graph replays of the whole step
+    # ---- timed region: graph replays of the whole step, at least K of them
+    #      and at least MIN_TIMED_S seconds' worth, so the clock sampler (one
+    #      sample every 50 ms) sees the timed region itself
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(dist)
     torch.cuda.synchronize()
@@ -207,24 +211,29 @@ def run_gpu(args):
         # the same replays for ~1 s first: the sampler starts and the clocks
         # settle under load before the timed region
         t_pre = time.monotonic()
+        n_pre = 0
         with torch.cuda.stream(stream):
             while time.monotonic() - t_pre < 1.0:
                 for _ in range(20):
                     graph.replay()
+                n_pre += 20
                 stream.synchronize()
+        est_s = (time.monotonic() - t_pre) / max(1, n_pre)
+        steps = int(max(args.steps, math.ceil(MIN_TIMED_S / max(est_s, 1e-6))))
+        steps = int(_max_over_ranks(dist, steps, dev))
         _barrier(dist)
         torch.cuda.synchronize()
         clk.mark("start")
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for _ in range(args.steps):
+            for _ in range(steps):
                 graph.replay()
             e1.record(stream)
         stream.synchronize()
         clk.mark("end")
     torch.cuda.synchronize()
     _barrier(dist)
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     ms_max = _max_over_ranks(dist, ms, dev)
     emitted = int(buf.out_off[-1].item())
     emitted_all = _sum_over_ranks(dist, emitted, dev)
@@ -237,7 +246,7 @@ def run_gpu(args):
     if head == "rnn":
         draft_launches = gamma        # one draft launch per position (plus a GRU launch each)
     else:
-        draft_launches = gamma if os.environ.get("DSPARK_DRAFT_PER_POSITION") else 1
+        draft_launches = 1            # one cooperative launch covers the gamma positions
     reps = max(5, min(args.steps, 1000))
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -302,7 +311,8 @@ def run_gpu(args):
         cpu = cpu_baseline(w, mode, budget_s=args.cpu_budget, dev_inp=inp, min_seconds=10.0, head=head)
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+            "steps_requested": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 weights, f32 logits, f32 accumulate", "data": "synthetic",
             "config": {"workload": f"{w.name}: B={B} V={V} r={r} gamma={gamma} d={d_of(w)} "
@@ -325,7 +335,7 @@ def run_gpu(args):
                          "algorithmic_bytes_per_launch": draft_bytes, "launch_ms": draft_launch_ms},
             "e2e": {"value": e2e_emitted / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches_per_step * steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }
@@ -588,21 +598,18 @@ def _draft_source_hash():
 
 
 def _draft_traffic(workload_name):
-    """dram__bytes_read.sum + dram__bytes_write.sum per draft launch from the
-    committed ncu summary of this workload, or None when there is none or
-    the kernel's sources changed after it was taken."""
-    path = os.path.join(ROOT, "profiles", f"draft_rows_{workload_name}.md")
+    """dram__bytes_read.sum + dram__bytes_write.sum per draft launch from one
+    ncu capture, recorded in profiles/traffic.json beside the summaries, or
+    None when there is none or the kernel's sources changed after it was
+    taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        fields = {}
         with open(path) as f:
-            for ln in f:
-                if ":" in ln and ln.startswith("- `"):
-                    k, v = ln[3:].split("`", 1)
-                    fields[k] = v.split(":", 1)[1].strip().strip("`")
-        if fields.get("source_sha256") != _draft_source_hash():
+            rec = json.load(f)["draft_rows"][workload_name]
+        if rec.get("source_sha256") != _draft_source_hash():
             return None
-        return int(fields["dram_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+        return int(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 

@@ -311,20 +311,23 @@ dspark_status dspark_verify_rnn(
  * allocations, or a latency-critical loop that must not enter an allocator
  * (cudaMalloc may take locks and synchronise the device).  Arguments and
  * results are those of dspark_draft_markov without the workspace: the
- * kernels' scratch (status word, arrival counters, partial states) lives in
- * a fixed array inside the library, 8 MiB + 64 KiB per GPU, held until the
- * process exits.  No counterpart on the pages: it is a deployment option.
- *   - Sizes whose scratch exceeds the array (two buffers of
- *     B * min(1024, ceil(V/128)) partial states of 16 bytes plus counters;
- *     the limit is B * min(1024, ceil(V/128)) <= 262144: any V for
- *     B <= 256) return DSPARK_ERR_UNSUPPORTED with a message on stderr.
+ * kernels' scratch (status word, arrival and barrier counters, winner keys,
+ * partial states) lives in a fixed array inside the library, 8.5 MiB + 1 KiB
+ * per GPU, held until the process exits.  No counterpart on the pages: it is
+ * a deployment option.
+ *   - Limit: B <= 256 (any V, any gamma <= DSPARK_MAX_GAMMA).  Larger batches
+ *     return DSPARK_ERR_UNSUPPORTED with a message on stderr.
+ *   - Argument checks and error codes are those of dspark_draft_markov (host
+ *     pointers: DSPARK_ERR_INVALID).
  *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *     that device current and keeps it for the life of the process; make
+ *     that first call before any stream capture.  A cudaDeviceReset after it
+ *     is not supported (the kept address would be stale).
  *   - Every call on a device shares the one array and clears its counters
  *     first: calls that may overlap on the GPU (different streams, or
  *     concurrent host threads) race and must be serialised by the caller.
- *   - Device-side range checks set bits in the array's status word, which
- *     this entry point does not report.
+ *   - Device-side range checks set bits in the array's status word; read and
+ *     clear it with dspark_noalloc_sync_status.
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  */
 dspark_status dspark_draft_markov_noalloc(
@@ -335,6 +338,13 @@ dspark_status dspark_draft_markov_noalloc(
     uint64_t seed, uint64_t step,
     int32_t* draft_tok, float* lse_q, float* z_tok, float* logits_out,
     void* stream);
+
+/*
+ * dspark_sync_status for the fixed array of dspark_draft_markov_noalloc on
+ * the current device: synchronise `stream`, read and clear the array's status
+ * word, same return values and bits.  Allocates nothing.
+ */
+dspark_status dspark_noalloc_sync_status(void* stream, uint32_t* bits);
 
 /*
  * Sequential temperature scaling fit [P2 §校准问题：原始置信度不可靠], [P4 §四].

@@ -107,6 +107,26 @@ def test_target_stream_and_full_prefix_verify_reject_bad_arguments(lib):
     assert st == -1
 
 
+def test_noalloc_draft_rejects_host_pointers_and_large_batches(lib):
+    """dspark_draft_markov_noalloc checks its arguments as dspark_draft_markov
+    does: host memory is not device memory (DSPARK_ERR_INVALID, before any
+    launch), and a batch beyond its fixed array is unsupported."""
+    vp = C.c_void_p
+    lib.dspark_draft_markov_noalloc.argtypes = [vp, C.c_int, vp, vp, C.c_int, vp, C.c_int, C.c_int, C.c_int,
+                                                C.c_int, C.c_int, C.c_float, C.c_uint64, C.c_uint64,
+                                                vp, vp, vp, vp, vp]
+    host = (C.c_float * 64)()
+    h = C.cast(host, vp)
+    args = [h, 0, h, h, 1, h, 4, 7, 1024, 64, 0, 1.0, 0, 0, h, h, h, None, None]
+    assert lib.dspark_draft_markov_noalloc(*args) == -1          # host pointers
+    args_null = list(args)
+    args_null[0] = None
+    assert lib.dspark_draft_markov_noalloc(*args_null) == -1
+    bad_tau = list(args)
+    bad_tau[11] = float("nan")
+    assert lib.dspark_draft_markov_noalloc(*bad_tau) == -1
+
+
 def test_package_imports_and_fails_loudly_without_library(tmp_path):
     import subprocess
     import sys

@@ -140,21 +140,17 @@ def test_temperature_request_base_and_stored_logits():
     _check_against_oracle(inp, w, buf, seed=4, step=3, req_base=500, tau=0.7)
 
 
-def test_per_position_launches_match_the_cooperative_launch(monkeypatch):
-    w = workload.custom("tiny", B=20, V=4104, r=128, w_dtype=torch.bfloat16, w_std=0.1, seed=8)
+def test_single_position_target_stream():
+    """gamma = 1 runs the target-stream draft as one single-position launch
+    (the epilogue form, the launch every position uses where cooperative
+    launch is unavailable), then the full-prefix verify."""
+    w = workload.custom("tiny", B=20, V=4104, r=128, gamma=1, w_dtype=torch.bfloat16, w_std=0.1, seed=8)
     inp = workload.inputs(w, device=DEV)
-    a = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
-    _fused_draft(inp, w, a, seed=6)
-    _full_verify(inp, a, seed=6)
-    assert vm.dspark_sync_status(a.ws.buf)[0] == 0
-    monkeypatch.setenv("DSPARK_DRAFT_PER_POSITION", "1")
-    b = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
-    _fused_draft(inp, w, b, seed=6)
-    _full_verify(inp, b, seed=6)
-    assert vm.dspark_sync_status(b.ws.buf)[0] == 0
-    np.testing.assert_array_equal(a.draft_tok.cpu().numpy(), b.draft_tok.cpu().numpy())
-    np.testing.assert_array_equal(a.accepted.cpu().numpy(), b.accepted.cpu().numpy())
-    np.testing.assert_allclose(a.p_tok.cpu().numpy(), b.p_tok.cpu().numpy(), rtol=1e-5, atol=0)
+    buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
+    _fused_draft(inp, w, buf, seed=6)
+    _full_verify(inp, buf, seed=6)
+    assert vm.dspark_sync_status(buf.ws.buf)[0] == 0
+    _check_against_oracle(inp, w, buf, seed=6)
 
 
 def test_full_size_b64_step_sampled_requests():

@@ -51,8 +51,27 @@ def test_noalloc_matches_workspace_entry_point_twice(B, V, r, wdt):
         np.testing.assert_allclose(z.cpu().numpy(), ref_z.cpu().numpy(), atol=LOGIT_ATOL, rtol=0)
 
 
+def test_noalloc_at_its_batch_limit_matches_workspace_entry_point():
+    """B = 256 is the documented limit at any vocabulary: the b256 vocabulary
+    (V = 129280) and the full one (V = 151936) with gamma = 7 must run and
+    reproduce dspark_draft_markov."""
+    for V, r in ((129280, 128), (151936, 256)):
+        w = workload.custom("b256", B=256, V=V, r=r, seed=V)
+        inp = workload.inputs(w, device="cuda")
+        ws = vm.Workspace(w.B, w.gamma, V, r)
+        ref = _outputs(w.B, w.gamma)
+        got = _outputs(w.B, w.gamma)
+        vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], *ref, ws, seed=3, step=1)
+        vm.dspark_draft_markov_noalloc(inp["U"], inp["W1"], inp["W2"], inp["anchor"], *got, seed=3, step=1)
+        assert vm.dspark_noalloc_sync_status() == (0, 0)
+        np.testing.assert_array_equal(got[0].cpu().numpy(), ref[0].cpu().numpy())
+        np.testing.assert_allclose(got[1].cpu().numpy(), ref[1].cpu().numpy(), atol=LOGIT_ATOL, rtol=0)
+        del inp, ws
+        torch.cuda.empty_cache()
+
+
 def test_noalloc_rejects_sizes_beyond_its_array():
-    B, gamma, V, r = 512, 7, 151936, 256
+    B, gamma, V, r = 257, 7, 1024, 64
     tok, lse, z = _outputs(B, gamma)
     U = torch.empty((B, gamma, V), device="cuda")
     W1 = torch.empty((V, r), dtype=torch.bfloat16, device="cuda")
@@ -61,3 +80,16 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     with pytest.raises(vm.DsparkError) as ei:
         vm.dspark_draft_markov_noalloc(U, W1, W2, anchor, tok, lse, z, seed=0)
     assert ei.value.status == -4
+
+
+def test_noalloc_status_word_reports_range_checks():
+    """An anchor outside [0, V) sets the token bit in the fixed array's status
+    word; dspark_noalloc_sync_status reports it once and clears it."""
+    w = workload.custom("tiny", B=4, V=1024, r=64, w_dtype=torch.bfloat16, seed=9)
+    inp = workload.inputs(w, device="cuda")
+    inp["anchor"][1] = w.V + 3
+    tok, lse, z = _outputs(w.B, w.gamma)
+    vm.dspark_draft_markov_noalloc(inp["U"], inp["W1"], inp["W2"], inp["anchor"], tok, lse, z, seed=1)
+    st, bits = vm.dspark_noalloc_sync_status()
+    assert st == -5 and bits & 1
+    assert vm.dspark_noalloc_sync_status() == (0, 0)

@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
     "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
-    "dspark_schedule", "dspark_verify", "dspark_draft_markov_target", "target_stream_supported", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_verify_logits", "dspark_rnn_input_table", "rnn_prepare", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
+    "dspark_schedule", "dspark_verify", "dspark_draft_markov_target", "target_stream_supported", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_verify_logits", "dspark_rnn_input_table", "rnn_prepare", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "dspark_noalloc_sync_status", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
 
@@ -61,6 +61,8 @@ _lib.dspark_verify.restype = _i
 _lib.dspark_draft_markov_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
                                              _vp, _vp, _vp, _vp, _vp]
 _lib.dspark_draft_markov_noalloc.restype = _i
+_lib.dspark_noalloc_sync_status.argtypes = [_vp, C.POINTER(C.c_uint32)]
+_lib.dspark_noalloc_sync_status.restype = _i
 _lib.dspark_draft_rnn.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f,
                                   _u64, _u64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.dspark_rnn_input_table.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp]
@@ -361,6 +363,14 @@ def dspark_draft_markov_noalloc(U, W1, W2, anchor, draft_tok, lse_q, z_tok, *, t
     _check("dspark_draft_markov_noalloc", _lib.dspark_draft_markov_noalloc(
         _p(U), _dt(U), _p(W1), _p(W2), _dt(W1), _p(anchor), B, gamma, V, r, req_base, float(tau),
         int(seed), int(step), _p(draft_tok), _p(lse_q), _p(z_tok), _p(logits_out), _stream(stream)))
+
+
+def dspark_noalloc_sync_status(stream=None):
+    """Synchronise the stream; return (status, bits) of the fixed array's
+    status word (the scratch of dspark_draft_markov_noalloc)."""
+    bits = C.c_uint32(0)
+    st = _lib.dspark_noalloc_sync_status(_stream(stream), C.byref(bits))
+    return int(st), int(bits.value)
 
 
 def dspark_gumbel_stream(seed, step, domain, row, n, gumbel_out=None, uniform_out=None, stream=None):

@@ -30,14 +30,10 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.nseg = (V + kVerifySeg - 1) / kVerifySeg;
     const int ntiles = (V + kPartTile - 1) / kPartTile;
     L.parts = ntiles < kMaxParts ? ntiles : kMaxParts;
-    size_t o = 0;
-    const size_t nchunks = ((size_t)B + kChunk - 1) / kChunk;
-    L.status = o;      o = align256(o + 16);
-    L.tickets = o;     o = align256(o + sizeof(uint32_t) * 2 * nchunks);
-    L.gbar = o;        o = align256(o + sizeof(uint32_t) * (kGbarExit + 1));
-    L.win = o;         o = align256(o + sizeof(unsigned long long) * kWinStride * (size_t)gamma * B);
-    L.vq = o;          o = align256(o + sizeof(uint32_t) * 2);
-    L.draft_part = o;  o = align256(o + sizeof(DrawLse) * 2 * (size_t)B * L.parts);
+    const WsDraftPrefix P = ws_draft_prefix(B, gamma, L.parts);
+    L.status = P.status; L.tickets = P.tickets; L.gbar = P.gbar; L.win = P.win; L.vq = P.vq;
+    L.draft_part = P.draft_part;
+    size_t o = P.end;
     L.verify_part = o; o = align256(o + sizeof(LseDraw) * (size_t)B * (gamma + 1) * L.nseg * kVerifySub);
     L.tgt_part = o;    o = align256(o + sizeof(LseDraw) * (size_t)B * gamma * kTgtSlots);
     L.tgt_token = o;   o = align256(o + sizeof(unsigned long long));
@@ -82,7 +78,7 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
 }
 
 // A pointer the device can dereference: device memory or managed memory.
-static bool is_device_ptr(const void* p) {
+bool is_device_ptr(const void* p) {
     if (!p) return false;
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) { cudaGetLastError(); return false; }
@@ -91,13 +87,13 @@ static bool is_device_ptr(const void* p) {
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-static dspark_status launch_status(cudaError_t e) {
+dspark_status launch_status(cudaError_t e) {
     if (e == cudaSuccess) return DSPARK_OK;
     fprintf(stderr, "dspark: launch failed: %s\n", cudaGetErrorString(e));
     return DSPARK_ERR_CUDA;
 }
 
-static bool sizes_ok(int B, int gamma, int V, int r) {
+bool sizes_ok(int B, int gamma, int V, int r) {
     if (B < 1 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 8 || (V % 8) != 0 || r < 1 || r > 1024)
         return false;
     if ((double)B * (gamma + 1) >= 4294967295.0) return false;
@@ -122,6 +118,24 @@ static unsigned long long tgt_token_of(const void* target, uint64_t seed, uint64
         h ^= h >> 31;
     }
     return h | 1ull;
+}
+
+dspark_status read_status_word(void* word, cudaStream_t s, uint32_t* bits) {
+    uint32_t host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, word, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "dspark: %s\n", cudaGetErrorString(e));
+        return DSPARK_ERR_CUDA;
+    }
+    if (host) {
+        e = cudaMemsetAsync(word, 0, sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    if (bits) *bits = host;
+    if (host & kTimeout) return DSPARK_ERR_TIMEOUT;
+    if (host) return DSPARK_ERR_DEVICE;
+    return DSPARK_OK;
 }
 
 }  // namespace dspark
@@ -156,22 +170,7 @@ dspark_status dspark_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 
 dspark_status dspark_sync_status(void* ws, void* stream, uint32_t* bits) {
     if (!is_device_ptr(ws)) return DSPARK_ERR_INVALID;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint32_t host = 0;
-    cudaError_t e = cudaMemcpyAsync(&host, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) {
-        fprintf(stderr, "dspark: %s\n", cudaGetErrorString(e));
-        return DSPARK_ERR_CUDA;
-    }
-    if (host) {
-        e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    }
-    if (bits) *bits = host;
-    if (host & kTimeout) return DSPARK_ERR_TIMEOUT;
-    if (host) return DSPARK_ERR_DEVICE;
-    return DSPARK_OK;
+    return read_status_word(ws, static_cast<cudaStream_t>(stream), bits);
 }
 
 dspark_status dspark_draft_markov(const void* U, dspark_dtype U_t, const void* W1, const void* W2,

@@ -12,6 +12,7 @@
 #include <stdint.h>
 
 #include "../../include/dspark.h"
+#include "internal.h"
 
 namespace dspark {
 
@@ -174,6 +175,8 @@ struct DrawLse {
     float zb;
     float s;
 };
+
+static_assert(sizeof(DrawLse) == kDrawLseBytes, "the workspace layout counts 16 bytes per partial state");
 
 __device__ __forceinline__ DrawLse drawlse_empty() { return DrawLse{-INFINITY, 0x7fffffff, 0.f, 0.f}; }
 

@@ -7,9 +7,9 @@
 // take an allocator's locks or its implicit device synchronisation, or
 // environments that forbid allocation after start-up.  This entry point runs
 // the same draft kernels with their scratch (status word, arrival counters,
-// per-CTA partial states) in a fixed array that lives in the library's own
-// device data segment.  Every GPU that loads the library holds the array
-// until the process exits.
+// grid-barrier counters, winner keys, per-CTA partial states) in a fixed
+// array that lives in the library's own device data segment.  Every GPU that
+// loads the library holds the array until the process exits.
 #include <cuda_runtime.h>
 #include <stdio.h>
 
@@ -21,10 +21,15 @@
 namespace dspark {
 namespace {
 
-// Fixed scratch: 8 MiB + 64 KiB covers the draft's status word, counters
-// and two buffers of partial states for B * min(1024, ceil(V/128)) <= 262144
-// (for example B = 256 with V up to 131072, or B = 64 at any V).
-constexpr size_t kStaticScratchBytes = (size_t)8 * 1024 * 1024 + 64 * 1024;
+// The array covers the draft's workspace prefix (ws_draft_prefix: status
+// word, tickets, barrier counters, winner keys, stream counters and the two
+// buffers of partial states) for every call with B <= kNoallocMaxB and
+// gamma <= DSPARK_MAX_GAMMA, at any V: the partial states per request are
+// capped at kMaxParts whatever the vocabulary.  8.5 MiB + 1 KiB.
+constexpr int kNoallocMaxB = 256;
+constexpr size_t kStaticScratchBytes = ws_draft_prefix(kNoallocMaxB, DSPARK_MAX_GAMMA, kMaxParts).end;
+static_assert(kStaticScratchBytes == (size_t)8 * 1024 * 1024 + 512 * 1024 + 1024,
+              "fixed scratch size changed: update the limit stated in dspark.h");
 static __device__ __align__(256) unsigned char g_draft_scratch[kStaticScratchBytes];
 
 // The array's device address on each device, looked up once with that
@@ -60,22 +65,24 @@ extern "C" dspark_status dspark_draft_markov_noalloc(
     const int32_t* anchor, int B, int gamma, int V, int r, int req_base, float tau,
     uint64_t seed, uint64_t step, int32_t* draft_tok, float* lse_q, float* z_tok, float* logits_out,
     void* stream) {
-    if (B < 1 || B > 1000000 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 8 || (V % 8) != 0 || r < 1 ||
-        r > 1024 || !(tau > 0.f) || req_base < 0)
-        return DSPARK_ERR_INVALID;
+    // the checks of dspark_draft_markov, workspace aside
+    if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
     if ((double)(req_base + (double)B) * (gamma + 1) >= 4294967295.0) return DSPARK_ERR_INVALID;
     if ((U_t != DSPARK_F32 && U_t != DSPARK_BF16) || (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
         return DSPARK_ERR_UNSUPPORTED;
-    if (!U || !W1 || !W2 || !anchor || !draft_tok || !lse_q || !z_tok) return DSPARK_ERR_INVALID;
+    if (!is_device_ptr(U) || !is_device_ptr(W1) || !is_device_ptr(W2) || !is_device_ptr(anchor) ||
+        !is_device_ptr(draft_tok) || !is_device_ptr(lse_q) || !is_device_ptr(z_tok))
+        return DSPARK_ERR_INVALID;
+    if (logits_out && !is_device_ptr(logits_out)) return DSPARK_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(U) | reinterpret_cast<uintptr_t>(W1) | reinterpret_cast<uintptr_t>(W2)) & 15)
         return DSPARK_ERR_INVALID;
     // the draft kernels touch the workspace up to the end of their partial states
-    const WsLayout L = ws_layout(B, gamma, V);
-    if (L.verify_part > kStaticScratchBytes) {
+    const size_t need = ws_draft_prefix(B, gamma, ws_layout(B, gamma, V).parts).end;
+    if (B > kNoallocMaxB || need > kStaticScratchBytes) {
         fprintf(stderr,
-                "dspark_draft_markov_noalloc: B=%d, V=%d need %zu bytes of scratch but the fixed array holds %zu; "
-                "use dspark_draft_markov with a workspace\n",
-                B, V, (size_t)L.verify_part, kStaticScratchBytes);
+                "dspark_draft_markov_noalloc: B=%d (at most %d), gamma=%d, V=%d need %zu bytes of scratch; the "
+                "fixed array holds %zu; use dspark_draft_markov with a workspace\n",
+                B, kNoallocMaxB, gamma, V, need, kStaticScratchBytes);
         return DSPARK_ERR_UNSUPPORTED;
     }
     void* ws = nullptr;
@@ -85,11 +92,13 @@ extern "C" dspark_status dspark_draft_markov_noalloc(
         return DSPARK_ERR_CUDA;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps whatever the previous call left.  The status word and
-    // the arrival counters must start at zero; the partial states are fully
-    // rewritten by every launch.
-    e = cudaMemsetAsync(ws, 0, L.draft_part, s);
-    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    // The array keeps whatever the previous call left.  The counters must
+    // start at zero; the partial states are fully rewritten by every launch.
+    // The status word is left alone: dspark_noalloc_sync_status reads and
+    // clears it.
+    const WsDraftPrefix P = ws_draft_prefix(B, gamma, ws_layout(B, gamma, V).parts);
+    e = cudaMemsetAsync(static_cast<char*>(ws) + P.tickets, 0, P.draft_part - P.tickets, s);
+    if (e != cudaSuccess) return launch_status(e);
 
     DraftParams p;
     p.U = U; p.U_bf16 = (U_t == DSPARK_BF16);
@@ -100,10 +109,17 @@ extern "C" dspark_status dspark_draft_markov_noalloc(
     p.seed = seed; p.step = step;
     p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.logits_out = logits_out;
     p.ws = ws_ptrs(ws, B, gamma, V);
-    e = launch_draft(p, s);
+    return launch_status(launch_draft(p, s));
+}
+
+// The status word of the fixed array, as dspark_sync_status reads a
+// workspace's: synchronise `stream`, read the word, clear it.
+extern "C" dspark_status dspark_noalloc_sync_status(void* stream, uint32_t* bits) {
+    void* ws = nullptr;
+    cudaError_t e = scratch_for_current_device(&ws);
     if (e != cudaSuccess) {
-        fprintf(stderr, "dspark_draft_markov_noalloc: launch failed: %s\n", cudaGetErrorString(e));
+        fprintf(stderr, "dspark_noalloc_sync_status: scratch lookup failed: %s\n", cudaGetErrorString(e));
         return DSPARK_ERR_CUDA;
     }
-    return DSPARK_OK;
+    return read_status_word(ws, static_cast<cudaStream_t>(stream), bits);
 }

@@ -56,7 +56,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
-#include <stdlib.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -90,6 +89,11 @@ constexpr long long kDrainCycles = 200000000LL;   // ~0.1 s: copies already issu
 // accept is passed to it.
 constexpr float kRaceRel = 1.0000152587890625f;   // 1 + 2^-16
 constexpr float kRaceSlack = 1.52587890625e-05f;  // 2^-16
+// Margin on a winner key shared between the threads of one request row: it
+// crosses two log2 / exp2 conversions and two additions of the winner's z2
+// (kept below 2^10 in magnitude by the caller), each good to ~2^-21.
+constexpr float kShareRel = 1.000244140625f;      // 1 + 2^-12
+constexpr float kShareMaxZ2 = 1024.f;             // |z2| beyond which keys are not shared
 
 struct Layout {
     uint32_t b, a, u, t, merge, tmerge, bar, misc, total;
@@ -110,7 +114,7 @@ __host__ __device__ inline Layout rows_layout(int NC, int r, bool resid, bool tg
     const uint32_t tmerge_bytes = tgt ? 4u * 128u * 8u : 0u;   // target fold: [4 column blocks][128 rows] float2
     const uint32_t fixed = (uint32_t)(L.uslots * kSlotBytes + L.tslots * kTBufBytes) + 4u * 128u * 16u +
                            tmerge_bytes + 8u * (2 * kMaxStages + 2 * L.uslots + 2 * kMaxAcc + 2 + L.tslots) + 16u +
-                           8u * 128u + 1024u + 64u;
+                           12u * 128u + 1024u + 64u;
     int st = (int)((kSmemBudget - (int)fixed) / kBBytes);
     L.stages = st > kMaxStages ? kMaxStages : st;
     L.b = 0;
@@ -122,7 +126,7 @@ __host__ __device__ inline Layout rows_layout(int NC, int r, bool resid, bool tg
     L.bar = L.tmerge + tmerge_bytes;
     L.misc = L.bar + 8u * (2 * L.stages + 2 * L.uslots + 2 * kMaxAcc + 2 + L.tslots);
     L.misc = (L.misc + 15u) & ~15u;
-    L.total = L.misc + 16u + 8u * 128u;
+    L.total = L.misc + 16u + 12u * 128u;   // s_tok, s_row and the shared winner keys, 128 words each
     return L;
 }
 
@@ -541,6 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_last) {
     static_assert(!(kTgt && (kResid || kRnn)), "the target stream belongs to the Markov draft");
     static_assert(!(kVs && (kResid || kRnn || kTgt)), "the stream role belongs to the plain Markov draft");
+    // the draft race reads the accumulator a quad of columns at a time
+    constexpr bool kQuadLoop = !kResid && !kOneRow;
     const DraftParams& p = a.p;
     const int NC = a.NC;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -591,6 +597,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     volatile uint32_t* never = reinterpret_cast<volatile uint32_t*>(gbase + L.misc + 8);
     int* s_tok = reinterpret_cast<int*>(gbase + L.misc + 16);
     int* s_row = s_tok + 128;                       // residual mode: rejected row per request, or -1
+    // draft: the best winner key found so far per request row by any of the
+    // CTA's threads racing that row (order-preserving bits of log2 E2 - z2,
+    // all ones = none yet), reset at every position
+    uint32_t* s_key = reinterpret_cast<uint32_t*>(s_row + 128);
     DrawLse* s_merge = reinterpret_cast<DrawLse*>(gbase + L.merge);   // [4 column blocks][128 rows]
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -634,6 +644,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         }
         s_tok[n] = x;
         s_row[n] = prow;
+        s_key[n] = 0xFFFFFFFFu;
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -858,7 +869,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             float Kr = INFINITY, Krh = INFINITY;
             DrawLse st = drawlse_empty();            // idx, zb (u + bias of the winner), s
             float rz2 = -INFINITY, rE2 = INFINITY;     // winner's z*log2e and E2
-            float rE2h = INFINITY;                     // rE2 * kRaceRel: the screen's threshold
+            float rE2h = INFINITY;                     // rE2 * kRaceRel: the screen's threshold (one-row form)
+            float Kh = INFINITY;                       // the screen's threshold on 1 - u per unit of t (draft form)
             Draw2 st2 = draw2_empty();
             float tm2 = -INFINITY, tsum = 0.f;         // target stream: this row's base-2 log-sum-exp state
             for (int t = blockIdx.x; t < ntiles; t += GX) {
@@ -866,15 +878,26 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 6); failed = true; break; }
                 ptx::tc_fence_after();
-                float bias[32];              // draft: U + h.W2; residual: h.W2
-                if (active) {
-                    ptx::tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + acc0 + (uint32_t)(acc * kTN + 32 * cb), bias);
-                    ptx::tmem_wait_ld();
+                // this warp's 32 lanes x 32 columns of the accumulator
+                const uint32_t acc_tile =
+                    tmem_base + ((uint32_t)(32 * q) << 16) + acc0 + (uint32_t)(acc * kTN + 32 * cb);
+                // the residual and one-request forms read the whole block at once and
+                // free the accumulator; the draft race reads it a quad at a time and
+                // frees it after the race
+                auto release_acc = [&]() {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(tempty(acc));
+                    if (++acc == nacc) { acc = 0; aph ^= 1u; }
+                };
+                float bias[32];              // residual: h.W2; one request: U + h.W2
+                if constexpr (!kQuadLoop) {
+                    if (active) {
+                        ptx::tmem_ld32(acc_tile, bias);
+                        ptx::tmem_wait_ld();
+                    }
+                    release_acc();
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(tempty(acc));
-                if (++acc == nacc) { acc = 0; aph ^= 1u; }
                 if (kResid && !active) continue;
                 const int v0 = t * kTN * RF + ti * kTN + 32 * cb;
                 if constexpr (kResid) {
@@ -989,56 +1012,100 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                             st.s += te;
                         }
                     }
-                } else if (real) {
+                } else if (kQuadLoop) {
                     // The accumulator holds z*tau = U + h.W2 (it started as the tile's U).
                     // Exponential race in base-2 units: the winner minimises
                     // E2_v * 2^(-z2_v), z2 = z*log2e; with the winner's z2 as the
                     // log-sum-exp reference the race and the sum share one exp2:
                     //   t_v = 2^(z2_v - z2_best),  v wins iff E2_v < E2_best * t_v.
-                    const int nq = min(8, (V - v0) >> 2);   // quads inside the vocabulary
+                    // Each quad is screened with the bound E2 = -log2(u) >=
+                    // (1 - u) * log2e (no logarithm; 1 - u exact from the bits)
+                    // against Kh, the smaller of this thread's winner key and the
+                    // best key any thread of the CTA has found on this request row
+                    // (shared every 16 entries): an entry that cannot beat a key
+                    // already found cannot be the row's draw.  The margins of Kh
+                    // and kRaceSlack cover the rounding.  Quads that pass are
+                    // re-run entry by entry, the exact variate formed only for the
+                    // entries that pass.  The quads are read from TMEM one at a
+                    // time, the next one's load in flight during the current one,
+                    // so the loop body exists once in the code.
+                    const int nq = active ? min(8, (V - v0) >> 2) : 0;   // quads inside the vocabulary
+                    // one quad of the race: us = z*tau of entries vq..vq+3, w their words
+                    auto race_quad = [&](const float (&us)[4], int vq, const uint4 w) {
+                        if (p.logits_out)
+                            *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(
+                                us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                        float t[4], wv[4];
+                        bool cand = false;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        if (c < nq) {
-                            const int vq = v0 + 4 * c;
-                            const float us[4] = {bias[4 * c], bias[4 * c + 1], bias[4 * c + 2], bias[4 * c + 3]};
-                            if (p.logits_out)
-                                *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(
-                                    us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
-                            const uint4 w = rng.quad((uint32_t)vq >> 2);
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                            float t[4];
-                            bool cand = false;
+                        for (int e = 0; e < 4; ++e) {
+                            t[e] = fast_exp2(fmaf(us[e], scale2, -rz2));
+                            wv[e] = one_minus_uniform_of(ws[e]);
+                            cand |= wv[e] < fmaf(Kh, t[e], kRaceSlack);
+                        }
+                        if (!cand) {
+                            st.s += (t[0] + t[1]) + (t[2] + t[3]);
+                        } else {
+                            // rare: entries in increasing v (the strict comparison
+                            // keeps the lowest index on exact ties), t against the
+                            // reference as it moves.  The empty state (rz2 = -inf,
+                            // rE2 = Kh = +inf, s = 0) makes the first entry win with
+                            // s = 1.
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                t[e] = fast_exp2(fmaf(us[e], scale2, -rz2));
-                                // screen with the bound E2 = -log2(u) >= (1 - u) * log2e
-                                // (no logarithm; 1 - u exact from the bits): an entry can
-                                // win only if (1 - u) * log2e <= E2 < E2_best * t, and the
-                                // margins of rE2h and kRaceSlack cover the rounding
-                                cand |= one_minus_uniform_of(ws[e]) < fmaf(rE2h * kLn2, t[e], kRaceSlack);
-                            }
-                            if (!cand) {
-                                st.s += (t[0] + t[1]) + (t[2] + t[3]);
-                            } else {
-                                // rare: the quad one entry at a time with the exact E2.
-                                // Entries come in increasing v, so the strict comparison keeps
-                                // the lowest index on exact ties.  The empty state (rz2 = -inf,
-                                // rE2 = +inf, s = 0) makes the first entry win with s = 1.
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
+                                const float arg = fmaf(us[e], scale2, -rz2);
+                                const float te = fast_exp2(arg);
+                                bool won = false;
+                                if (wv[e] < fmaf(Kh, te, kRaceSlack)) {
                                     const float E2 = exp2_variate_of(ws[e]);
-                                    const float te = fast_exp2(fmaf(us[e], scale2, -rz2));
                                     if (E2 < rE2 * te) {
-                                        st.s = st.s * fast_exp2(fmaf(-us[e], scale2, rz2)) + 1.f;
-                                        rz2 = us[e] * scale2; rE2 = E2; rE2h = E2 * kRaceRel;
+                                        st.s = st.s * fast_exp2(-arg) + 1.f;
+                                        rz2 = us[e] * scale2; rE2 = E2; Kh = E2 * (kRaceRel * kLn2);
                                         st.idx = vq + e; st.zb = us[e];
-                                    } else {
-                                        st.s += te;
+                                        won = true;
                                     }
                                 }
+                                if (!won) st.s += te;
                             }
                         }
+                    };
+                    // two quads per step (their random words computed side by side),
+                    // the next step's columns loading meanwhile
+                    uint32_t nx[8];
+                    if (nq > 0) ptx::tmem_ld8(acc_tile, nx);
+#pragma unroll 1
+                    for (int c = 0; c < nq; c += 2) {
+                        ptx::tmem_wait_ld8(nx);
+                        const float ua[4] = {__uint_as_float(nx[0]), __uint_as_float(nx[1]), __uint_as_float(nx[2]),
+                                             __uint_as_float(nx[3])};
+                        const float ub[4] = {__uint_as_float(nx[4]), __uint_as_float(nx[5]), __uint_as_float(nx[6]),
+                                             __uint_as_float(nx[7])};
+                        if (c + 2 < nq) ptx::tmem_ld8(acc_tile + (uint32_t)(4 * (c + 2)), nx);
+                        if (real) {
+                            const int vq = v0 + 4 * c;
+                            const uint4 wa = rng.quad((uint32_t)vq >> 2);
+                            const uint4 wb = rng.quad(((uint32_t)vq >> 2) + 1u);
+                            race_quad(ua, vq, wa);
+                            if (c + 1 < nq) race_quad(ub, vq + 4, wb);
+                            if ((c & 3) == 2 && rE2 < INFINITY && fabsf(rz2) < kShareMaxZ2) {
+                                // share this thread's key with the row's other threads and
+                                // take the best one found so far (the atomic returns the
+                                // previous minimum): key = log2(E2_best) - z2_best, as
+                                // order-preserving bits
+                                const float lk = fast_log2(rE2) - rz2;
+                                const uint32_t kb = __float_as_uint(lk);
+                                const uint32_t ko = (kb & 0x80000000u) ? ~kb : (kb | 0x80000000u);
+                                const uint32_t bo = min(atomicMin(&s_key[nrow], ko), ko);
+                                const float lb = __uint_as_float((bo & 0x80000000u) ? (bo & 0x7fffffffu) : ~bo);
+                                // relative to this thread's reference; an exponent clamped
+                                // at -100 only loosens the screen
+                                Kh = fminf(Kh, fast_exp2(fmaxf(lb + rz2, -100.f)) * (kShareRel * kLn2));
+                            }
+                        }
+                        __syncwarp();          // the next TMEM load and wait are warp-collective
                     }
+                    release_acc();
                 }
                 if constexpr (kTgt) {
                     // target row k-1 on this warp's 32 rows x 32 columns (after the
@@ -1102,6 +1169,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             if constexpr (kTgt) reinterpret_cast<float2*>(gbase + L.tmerge)[cb * 128 + row] = make_float2(tm2, tsum);
             // one barrier publishes s_merge and makes a failure a group decision
             if (ptx::bar_red_or(1, 32 * kEpiWarps, failed)) { failed = true; *abort_flag = 1u; break; }
+            // every thread is past its race: the next position starts with no shared keys
+            if (etid < 128) s_key[etid] = 0xFFFFFFFFu;
             DrawLse* part_buf = p.ws.draft_part + (size_t)((k - 1) & 1) * p.B * p.ws.parts;
             if (etid < nb) {
                 if constexpr (kResid) {
@@ -1340,6 +1409,20 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 
 }  // namespace
 
+void* tma_encoder() {
+    static void* fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = f;
+    }
+    return fn;
+}
+
 bool rows_supported(const DraftParams& p) {
     return p.W_bf16 && !p.U_bf16 && p.B >= 1 && p.r % 64 == 0 && p.r <= 256 && p.V % 8 == 0 &&
            tma_encoder() != nullptr;
@@ -1453,6 +1536,21 @@ cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cud
     return launch_rows(p, k_first, k_last, false, nullptr, false, nullptr, s);
 }
 
+// All gamma positions of the draft.  bf16 weights with fp32 U run the
+// tensor-core rows kernel: one cooperative launch for the gamma positions,
+// or one launch per position where the device lacks cooperative launch (and
+// for gamma = 1); any other combination runs the CUDA-core kernel, one
+// launch per position.
+cudaError_t launch_draft(const DraftParams& p, cudaStream_t s) {
+    const bool rows = rows_supported(p);
+    if (rows && p.gamma > 1 && cooperative_supported()) return launch_draft_rows(p, 1, p.gamma, s);
+    for (int k = 1; k <= p.gamma; ++k) {
+        const cudaError_t e = rows ? launch_draft_rows(p, k, k, s) : launch_draft_simt(p, k, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 bool draft_target_supported(const DraftParams& p) {
     return rows_supported(p) && p.target != nullptr && draft_rows_grid_x(p.B, p.V, p.ws.parts) <= kTgtSlots;
 }
@@ -1462,7 +1560,7 @@ bool draft_target_supported(const DraftParams& p) {
 // launch, on kVsCtas SMs of its own.
 bool draft_target_vs(const DraftParams& p) {
     return rows_supported(p) && p.target != nullptr && p.B <= 64 && p.gamma > 1 && cooperative_supported() &&
-           !getenv("DSPARK_DRAFT_PER_POSITION") && num_sms() >= 4 * kVsCtas;
+           num_sms() >= 4 * kVsCtas;
 }
 
 // The Markov draft with the target stream: with the verify-stream role when
@@ -1486,8 +1584,7 @@ cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s) {
         return launch_rows(q, 1, p.gamma, false, nullptr, false, nullptr, s, nullptr, &v);
     }
     if (!draft_target_supported(p)) return cudaErrorNotSupported;
-    if (p.gamma > 1 && cooperative_supported() && !getenv("DSPARK_DRAFT_PER_POSITION"))
-        return launch_rows(p, 1, p.gamma, false, nullptr, false, nullptr, s);
+    if (p.gamma > 1 && cooperative_supported()) return launch_rows(p, 1, p.gamma, false, nullptr, false, nullptr, s);
     for (int k = 1; k <= p.gamma; ++k) {
         const cudaError_t e = launch_rows(p, k, k, false, nullptr, false, nullptr, s);
         if (e != cudaSuccess) return e;

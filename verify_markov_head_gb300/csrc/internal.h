@@ -26,6 +26,30 @@ constexpr int kWinStride = 16;          // winner keys 128 bytes apart: one cach
 constexpr int kTgtSlots = 256;          // partial states per (request, target row) of the draft's target
                                         // stream (>= the draft's CTAs along V)
 
+constexpr size_t ws_align256(size_t x) { return (x + 255) & ~(size_t)255; }
+constexpr size_t kDrawLseBytes = 16;   // sizeof(DrawLse) (checked in common.cuh)
+
+// The workspace regions the draft kernels touch, in layout order: status
+// word, arrival tickets, grid-barrier counters, winner keys, verify-stream
+// counters, then the draft's two buffers of partial states.  `end` is the
+// first byte past them.  ws_layout places the other regions after these.
+struct WsDraftPrefix {
+    size_t status, tickets, gbar, win, vq, draft_part, end;
+};
+constexpr WsDraftPrefix ws_draft_prefix(int B, int gamma, int parts) {
+    WsDraftPrefix P{};
+    const size_t nchunks = ((size_t)B + kChunk - 1) / kChunk;
+    size_t o = 0;
+    P.status = o;     o = ws_align256(o + 16);
+    P.tickets = o;    o = ws_align256(o + sizeof(uint32_t) * 2 * nchunks);
+    P.gbar = o;       o = ws_align256(o + sizeof(uint32_t) * (kGbarExit + 1));
+    P.win = o;        o = ws_align256(o + sizeof(unsigned long long) * kWinStride * (size_t)gamma * B);
+    P.vq = o;         o = ws_align256(o + sizeof(uint32_t) * 2);
+    P.draft_part = o; o = ws_align256(o + kDrawLseBytes * 2 * (size_t)B * parts);
+    P.end = o;
+    return P;
+}
+
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
     size_t status, tickets, gbar, win, vq, draft_part, verify_part, tgt_part, tgt_token, rej, acc, fin, lse_rej,
@@ -60,6 +84,14 @@ struct WsPtrs {
     int parts;
 };
 WsPtrs ws_ptrs(void* ws, int B, int gamma, int V);
+
+// Host-side argument checks shared by the ABI entry points (api.cu).
+bool is_device_ptr(const void* p);              // device or managed memory
+bool sizes_ok(int B, int gamma, int V, int r);  // the limits of dspark_draft_markov
+dspark_status launch_status(cudaError_t e);     // DSPARK_OK, or DSPARK_ERR_CUDA with a message
+// Synchronise s, read the 32-bit status word at `word` (device memory), clear
+// it if set; the status dspark_sync_status returns.
+dspark_status read_status_word(void* word, cudaStream_t s, uint32_t* bits);
 
 struct DraftParams {
     const void* U; int U_bf16;
@@ -154,8 +186,6 @@ int num_sms();
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_draft_simt(const DraftParams& p, int k, cudaStream_t s);
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t s);   // all gamma positions
-bool draft_tc_supported(const DraftParams& p);
-cudaError_t launch_draft_tc(const DraftParams& p, int k, cudaStream_t s);
 bool draft_rows_supported(const DraftParams& p);
 cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cudaStream_t s);
 int draft_rows_grid_x(int B, int V, int parts);   // CTAs along V of a draft rows launch

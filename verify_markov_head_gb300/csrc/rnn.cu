@@ -22,7 +22,6 @@
 // cooperative launch, each position is a gru_kernel launch (below) followed
 // by a single-position draft launch.
 #include <cuda_runtime.h>
-#include <stdlib.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -175,8 +174,7 @@ cudaError_t launch_gru(const GruParams& g, int k, cudaStream_t s) {
 // the GRU steps itself; without cooperative launch, a GRU launch and a
 // single-position draft launch per position.
 cudaError_t launch_draft_rnn(const DraftParams& p, const GruParams& g, cudaStream_t s) {
-    if (p.gamma > 1 && cooperative_supported() && !getenv("DSPARK_DRAFT_PER_POSITION"))
-        return launch_draft_rows_rnn(p, g, 1, p.gamma, s);
+    if (p.gamma > 1 && cooperative_supported()) return launch_draft_rows_rnn(p, g, 1, p.gamma, s);
     for (int k = 1; k <= p.gamma; ++k) {
         cudaError_t e = launch_gru(g, k, s);
         if (e != cudaSuccess) return e;

@@ -25,8 +25,6 @@
 //                   accepted drafts and the final token of every request.
 // The last warp to finish a request's bonus segments merges them into its
 // token.
-#include <stdlib.h>
-
 #include "common.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -430,7 +428,7 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
         return finish();
     }
     if (p.state && !resid_rows_supported(p)) return cudaErrorNotSupported;   // RNN rows: tensor-core path only
-    if (p.state || (resid_rows_supported(p) && !getenv("DSPARK_RESID_SIMT"))) {
+    if (p.state || resid_rows_supported(p)) {
         const cudaError_t e = launch_resid_rows(p, s);
         if (e != cudaSuccess) return e;
         return finish();
