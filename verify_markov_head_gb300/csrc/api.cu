@@ -184,7 +184,7 @@ dspark_status dspark_draft_markov(const void* U, dspark_dtype U_t, const void* W
     if (!is_device_ptr(U) || !is_device_ptr(W1) || !is_device_ptr(W2) || !is_device_ptr(anchor) ||
         !is_device_ptr(draft_tok) || !is_device_ptr(lse_q) || !is_device_ptr(z_tok) || !is_device_ptr(ws))
         return DSPARK_ERR_INVALID;
-    if (logits_out && !is_device_ptr(logits_out)) return DSPARK_ERR_INVALID;
+    if (logits_out && (!is_device_ptr(logits_out) || !aligned(logits_out, 16))) return DSPARK_ERR_INVALID;
     if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(ws, 256)) return DSPARK_ERR_INVALID;
     if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;
     if ((double)(req_base + (double)B) * (gamma + 1) >= 4294967295.0) return DSPARK_ERR_INVALID;
@@ -215,7 +215,7 @@ dspark_status dspark_draft_markov_target(const void* U, dspark_dtype U_t, const 
         !is_device_ptr(anchor) || !is_device_ptr(draft_tok) || !is_device_ptr(lse_q) || !is_device_ptr(z_tok) ||
         !is_device_ptr(ws))
         return DSPARK_ERR_INVALID;
-    if (logits_out && !is_device_ptr(logits_out)) return DSPARK_ERR_INVALID;
+    if (logits_out && (!is_device_ptr(logits_out) || !aligned(logits_out, 16))) return DSPARK_ERR_INVALID;
     if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(target, 16) || !aligned(ws, 256))
         return DSPARK_ERR_INVALID;
     if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_INVALID;

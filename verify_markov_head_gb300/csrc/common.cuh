@@ -165,36 +165,42 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // ---------------------------------------------------------------- merge states
 // Gumbel-max draw fused with a log-sum-exp: over a set of entries,
-//   best  = max (z_v + G_v), idx = its v (lowest v on ties), zb = z_idx,
-//   s     = sum exp(z_v - best).
-// best is a safe log-sum-exp reference: G lies in [-2.82, 16.64] for the
-// uniforms above, so z_v - best <= 2.82 and exp never overflows.
+//   best = max (z_v + G_v), idx = its v (lowest v on ties), zb = z_idx
+//          (best = -inf, idx = 2^31 - 1: no draw taken in the set),
+//   lse  = log sum_v exp(z_v)  (-inf for an empty set).
+// The two parts merge independently, so the log-sum-exp of a set does not
+// depend on which entries a partial draw examined: a draw may skip entries
+// that cannot win (screened against a bound found elsewhere) while the sum
+// covers every entry.
 struct DrawLse {
     float best;
     int idx;
     float zb;
-    float s;
+    float lse;
 };
 
 static_assert(sizeof(DrawLse) == kDrawLseBytes, "the workspace layout counts 16 bytes per partial state");
 
-__device__ __forceinline__ DrawLse drawlse_empty() { return DrawLse{-INFINITY, 0x7fffffff, 0.f, 0.f}; }
+__device__ __forceinline__ DrawLse drawlse_empty() { return DrawLse{-INFINITY, 0x7fffffff, 0.f, -INFINITY}; }
 
 __device__ __forceinline__ bool wins(float sa, int ia, float sb, int ib) {
     return sa > sb || (sa == sb && ia < ib);
 }
 
+// log(e^x + e^y), with -inf as the empty sum.  log(1 + w) for w in (0, 1]
+// through the hardware log2 of 1 + w: absolute error about 1e-7 (the rounding
+// of 1 + w loses at most w * 2^-24 of it).
+__device__ __forceinline__ float log_add_exp(float x, float y) {
+    const float m = fmaxf(x, y), n = fminf(x, y);
+    if (n == -INFINITY) return m;
+    float l2;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(1.f + __expf(n - m)));
+    return fmaf(l2, 0.69314718055994531f, m);
+}
+
 __device__ __forceinline__ DrawLse drawlse_merge(const DrawLse& a, const DrawLse& b) {
-    if (b.best == -INFINITY) return a;
-    if (a.best == -INFINITY) return b;
-    DrawLse o;
-    if (wins(b.best, b.idx, a.best, a.idx)) {
-        o.best = b.best; o.idx = b.idx; o.zb = b.zb;
-        o.s = b.s + a.s * __expf(a.best - b.best);
-    } else {
-        o.best = a.best; o.idx = a.idx; o.zb = a.zb;
-        o.s = a.s + b.s * __expf(b.best - a.best);
-    }
+    DrawLse o = wins(b.best, b.idx, a.best, a.idx) ? b : a;
+    o.lse = log_add_exp(a.lse, b.lse);
     return o;
 }
 
@@ -203,7 +209,7 @@ __device__ __forceinline__ DrawLse shfl_xor(const DrawLse& a, int m) {
     o.best = __shfl_xor_sync(0xffffffffu, a.best, m);
     o.idx = __shfl_xor_sync(0xffffffffu, a.idx, m);
     o.zb = __shfl_xor_sync(0xffffffffu, a.zb, m);
-    o.s = __shfl_xor_sync(0xffffffffu, a.s, m);
+    o.lse = __shfl_xor_sync(0xffffffffu, a.lse, m);
     return o;
 }
 

@@ -73,7 +73,8 @@ extern "C" dspark_status dspark_draft_markov_noalloc(
     if (!is_device_ptr(U) || !is_device_ptr(W1) || !is_device_ptr(W2) || !is_device_ptr(anchor) ||
         !is_device_ptr(draft_tok) || !is_device_ptr(lse_q) || !is_device_ptr(z_tok))
         return DSPARK_ERR_INVALID;
-    if (logits_out && !is_device_ptr(logits_out)) return DSPARK_ERR_INVALID;
+    if (logits_out && (!is_device_ptr(logits_out) || (reinterpret_cast<uintptr_t>(logits_out) & 15)))
+        return DSPARK_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(U) | reinterpret_cast<uintptr_t>(W1) | reinterpret_cast<uintptr_t>(W2)) & 15)
         return DSPARK_ERR_INVALID;
     // the draft kernels touch the workspace up to the end of their partial states

@@ -70,6 +70,10 @@ constexpr int kThreads = (kEpiWarps + 3) * 32;   // 608
 constexpr int kProducerWarp = 16, kMmaWarp = 17, kUWarp = 18;
 constexpr int kTN = 128;                          // vocabulary entries per tile
 constexpr int kMaxStages = 12;                    // W2 K-chunk ring depth (as shared memory allows)
+// With the race in the epilogue the W2 ring needs no more than 5 stages (measured:
+// 5 stages run faster than 9 at 64 and 512 requests); the one-request form is
+// bound by the ring's turnaround and takes what shared memory allows.
+constexpr int kMaxStagesRace = 5;
 // TMEM (512 columns): RF A operands of 128 columns, then 4 - RF accumulators
 // of 128 columns (three at RF = 1, two at RF = 2).
 constexpr int kMaxAcc = 3;
@@ -79,6 +83,7 @@ constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile 
 // in fill order.
 constexpr int kUSlots = 4;
 constexpr int kTBufBytes = 32 * 128;              // target stream: one warp's 32 rows x 32 fp32 of a tile
+constexpr int kZBufBytes = 32 * 128;              // logits store: one warp's 32 rows x 32 fp32 of a tile
 constexpr int kUSlotsResid = 8;                   // residual: 16 warps x (4 KB U + 4 KB target) row staging
 constexpr int kSmemBudget = 227 * 1024;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
@@ -94,9 +99,13 @@ constexpr float kRaceSlack = 1.52587890625e-05f;  // 2^-16
 // (kept below 2^10 in magnitude by the caller), each good to ~2^-21.
 constexpr float kShareRel = 1.000244140625f;      // 1 + 2^-12
 constexpr float kShareMaxZ2 = 1024.f;             // |z2| beyond which keys are not shared
+// Floor of the screen threshold (per unit of t): an entry with t > 2^64 then
+// always reaches the exact path, which moves the sum's reference before
+// adding it; the floor only loosens the screen.
+constexpr float kKhMin = 8.673617379884035e-19f;  // 2^-60
 
 struct Layout {
-    uint32_t b, a, u, t, merge, tmerge, bar, misc, total;
+    uint32_t b, a, u, t, z, merge, tmerge, bar, misc, total;
     int uslots, tslots, stages;
 };
 
@@ -106,22 +115,26 @@ constexpr int kSlotBytes = 128 * 128;             // one U slice: 128 rows x 32 
 // is left, up to kMaxStages K-chunks), the U slots (the residual mode uses
 // that region as 16 per-warp 4 KB row-staging buffers), the fold buffers,
 // the barriers and a few words.
-__host__ __device__ inline Layout rows_layout(int NC, int r, bool resid, bool tgt = false) {
+__host__ __device__ inline Layout rows_layout(int NC, int r, bool resid, bool tgt = false, bool zst = false,
+                                              bool one_row = false) {
     (void)NC; (void)r;
     Layout L;
     L.uslots = resid ? kUSlotsResid : kUSlots;
     L.tslots = tgt ? kEpiWarps : 0;                            // one target buffer and barrier per epilogue warp
     const uint32_t tmerge_bytes = tgt ? 4u * 128u * 8u : 0u;   // target fold: [4 column blocks][128 rows] float2
-    const uint32_t fixed = (uint32_t)(L.uslots * kSlotBytes + L.tslots * kTBufBytes) + 4u * 128u * 16u +
+    const uint32_t z_bytes = zst ? (uint32_t)(kEpiWarps * kZBufBytes) : 0u;   // logits store staging
+    const uint32_t fixed = (uint32_t)(L.uslots * kSlotBytes + L.tslots * kTBufBytes) + z_bytes + 4u * 128u * 16u +
                            tmerge_bytes + 8u * (2 * kMaxStages + 2 * L.uslots + 2 * kMaxAcc + 2 + L.tslots) + 16u +
                            12u * 128u + 1024u + 64u;
     int st = (int)((kSmemBudget - (int)fixed) / kBBytes);
-    L.stages = st > kMaxStages ? kMaxStages : st;
+    const int cap = (one_row || resid) ? kMaxStages : kMaxStagesRace;
+    L.stages = st > cap ? cap : st;
     L.b = 0;
     L.a = 0;
     L.u = L.b + (uint32_t)L.stages * kBBytes;
     L.t = L.u + (uint32_t)(L.uslots * kSlotBytes);
-    L.merge = L.t + (uint32_t)(L.tslots * kTBufBytes);
+    L.z = L.t + (uint32_t)(L.tslots * kTBufBytes);
+    L.merge = L.z + z_bytes;
     L.tmerge = L.merge + 4u * 128u * 16u;
     L.bar = L.tmerge + tmerge_bytes;
     L.misc = L.bar + 8u * (2 * L.stages + 2 * L.uslots + 2 * kMaxAcc + 2 + L.tslots);
@@ -136,6 +149,9 @@ struct RowsArgs {
     // target stream only: fp32 [B][gamma+1][V], box {32 vocab, 1, 32 requests}
     // (one epilogue warp's rows, 128-byte swizzle)
     CUtensorMap tmap;
+    // logits store (draft with logits_out, requests-on-lanes race): fp32
+    // [B][gamma][V], box {32 vocab, 1, 32 requests}, 128-byte swizzle
+    CUtensorMap zmap;
     DraftParams p;
     int NC;              // request rows per CTA (32, 64 or 128)
     // residual mode only
@@ -391,7 +407,7 @@ __device__ __forceinline__ void issue_rows(uint32_t buf, const T* row, unsigned 
 
 __device__ __forceinline__ DrawLse drawlse_of(const float4 c) {
     DrawLse d;
-    d.best = c.x; d.idx = __float_as_int(c.y); d.zb = c.z; d.s = c.w;
+    d.best = c.x; d.idx = __float_as_int(c.y); d.zb = c.z; d.lse = c.w;
     return d;
 }
 
@@ -571,7 +587,9 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         }
     }
     const int GX = kVs ? a.gxd : (int)gridDim.x;   // CTAs of the draft itself
-    const Layout L = rows_layout(NC, p.r, kResid, kTgt);
+    // the draft's logits leave through a per-warp staging buffer and a tensor store
+    const bool zst = kQuadLoop && !kTgt && p.logits_out != nullptr;
+    const Layout L = rows_layout(NC, p.r, kResid, kTgt, zst, kOneRow);
     const int KCH = p.r / 64;
     const int RF = 128 / NC;                      // vocabulary tiles per accumulator
     const int US = L.uslots;
@@ -867,10 +885,18 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             // residual mode: E / r of the r-draw's winner, E / p of the p-draw's
             // (+inf: none yet), and the screens' thresholds
             float Kr = INFINITY, Krh = INFINITY;
-            DrawLse st = drawlse_empty();            // idx, zb (u + bias of the winner), s
+            DrawLse st = drawlse_empty();            // idx, zb (u + bias of the winner)
+            float osum = 0.f;                          // one-row form: sum of 2^(z2_v - rz2)
             float rz2 = -INFINITY, rE2 = INFINITY;     // winner's z*log2e and E2
             float rE2h = INFINITY;                     // rE2 * kRaceRel: the screen's threshold (one-row form)
-            float Kh = INFINITY;                       // the screen's threshold on 1 - u per unit of t (draft form)
+            // draft form: the log-sum-exp as lsum = sum_v 2^(z2_v - ref2) against a
+            // reference set by the data alone (the first quad's maximum, moved up
+            // by >= 64 only when an entry exceeds it by that much), so the sum does
+            // not depend on the race; the race as K2 = E2_best * 2^(ref2 - z2_best)
+            // (v wins iff E2_v < K2 * t_v, t_v = 2^(z2_v - ref2)) and the screen's
+            // threshold Kh on 1 - u per unit of t
+            float ref2 = -INFINITY, lsum = 0.f, K2 = INFINITY;
+            float Kh = INFINITY;
             Draw2 st2 = draw2_empty();
             float tm2 = -INFINITY, tsum = 0.f;         // target stream: this row's base-2 log-sum-exp state
             for (int t = blockIdx.x; t < ntiles; t += GX) {
@@ -1002,14 +1028,14 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         if (one_minus_uniform_of(wd) < fmaf(rE2h * kLn2, te, kRaceSlack)) {
                             const float E2 = exp2_variate_of(wd);
                             if (E2 < rE2 * te) {
-                                st.s = st.s * fast_exp2(fmaf(-u, scale2, rz2)) + 1.f;
+                                osum = osum * fast_exp2(fmaf(-u, scale2, rz2)) + 1.f;
                                 rz2 = u * scale2; rE2 = E2; rE2h = E2 * kRaceRel;
                                 st.idx = v; st.zb = u;
                             } else {
-                                st.s += te;
+                                osum += te;
                             }
                         } else {
-                            st.s += te;
+                            osum += te;
                         }
                     }
                 } else if (kQuadLoop) {
@@ -1032,7 +1058,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     const int nq = active ? min(8, (V - v0) >> 2) : 0;   // quads inside the vocabulary
                     // one quad of the race: us = z*tau of entries vq..vq+3, w their words
                     auto race_quad = [&](const float (&us)[4], int vq, const uint4 w) {
-                        if (p.logits_out)
+                        if (!zst && p.logits_out)
                             *reinterpret_cast<float4*>(p.logits_out + out_row + vq) = make_float4(
                                 us[0] * p.inv_tau, us[1] * p.inv_tau, us[2] * p.inv_tau, us[3] * p.inv_tau);
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -1040,38 +1066,64 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         bool cand = false;
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            t[e] = fast_exp2(fmaf(us[e], scale2, -rz2));
+                            t[e] = fast_exp2(fmaf(us[e], scale2, -ref2));
                             wv[e] = one_minus_uniform_of(ws[e]);
                             cand |= wv[e] < fmaf(Kh, t[e], kRaceSlack);
                         }
-                        if (!cand) {
-                            st.s += (t[0] + t[1]) + (t[2] + t[3]);
-                        } else {
-                            // rare: entries in increasing v (the strict comparison
-                            // keeps the lowest index on exact ties), t against the
-                            // reference as it moves.  The empty state (rz2 = -inf,
-                            // rE2 = Kh = +inf, s = 0) makes the first entry win with
-                            // s = 1.
+                        const float lsum0 = lsum;
+                        lsum += (t[0] + t[1]) + (t[2] + t[3]);
+                        if (cand) {
+                            // rare.  An entry more than 64 above the reference (and the
+                            // first quad, ref2 = -inf) moves the reference to the quad's
+                            // maximum first and takes the quad's sum again against it;
+                            // otherwise the sum took the quad as the screened path does,
+                            // so it depends on the data alone.
+                            const float zm2 = fmaxf(fmaxf(us[0], us[1]), fmaxf(us[2], us[3])) * scale2;
+                            if (zm2 > ref2 + 64.f) {
+                                float rs = 0.f;
+                                if (ref2 > -INFINITY) {
+                                    rs = fast_exp2(ref2 - zm2);
+                                    K2 *= rs;
+                                    Kh = fmaxf(Kh * rs, kKhMin);
+                                }
+                                ref2 = zm2;
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) t[e] = fast_exp2(fmaf(us[e], scale2, -ref2));
+                                lsum = lsum0 * rs + ((t[0] + t[1]) + (t[2] + t[3]));
+                            }
+                            // entries in increasing v (the strict comparison keeps the
+                            // lowest index on exact ties); the exact variate only for the
+                            // entries that pass the screen
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float arg = fmaf(us[e], scale2, -rz2);
-                                const float te = fast_exp2(arg);
-                                bool won = false;
-                                if (wv[e] < fmaf(Kh, te, kRaceSlack)) {
+                                if (wv[e] < fmaf(Kh, t[e], kRaceSlack)) {
                                     const float E2 = exp2_variate_of(ws[e]);
-                                    if (E2 < rE2 * te) {
-                                        st.s = st.s * fast_exp2(-arg) + 1.f;
-                                        rz2 = us[e] * scale2; rE2 = E2; Kh = E2 * (kRaceRel * kLn2);
+                                    if (E2 < K2 * t[e]) {
+                                        K2 = E2 * fast_exp2(fmaf(-us[e], scale2, ref2));   // E2 / t_v
+                                        Kh = fmaxf(fminf(Kh, K2 * (kRaceRel * kLn2)), kKhMin);
+                                        rz2 = us[e] * scale2; rE2 = E2;
                                         st.idx = vq + e; st.zb = us[e];
-                                        won = true;
                                     }
                                 }
-                                if (!won) st.s += te;
                             }
                         }
                     };
                     // two quads per step (their random words computed side by side),
-                    // the next step's columns loading meanwhile
+                    // the next step's columns loading meanwhile.  After steps 1 and 3
+                    // the thread shares its winner key with the CTA's other threads
+                    // racing the same request row and takes the best found so far
+                    // (an atomic minimum that returns the previous one).  The key read
+                    // depends on timing, but only as a bound for the screen: the draw
+                    // itself is exact and the sum never looks at the race.
+                    // logits store: this warp's 32 rows x 32 columns of z go to its
+                    // staging buffer (row = lane, 16-byte chunk c at c ^ (lane & 7), the
+                    // 128-byte swizzle of the map), then out in one tensor store; the
+                    // previous tile's store must have read the buffer first
+                    const uint32_t zrow = base + L.z + (uint32_t)warp * (uint32_t)kZBufBytes + (uint32_t)lane * 128u;
+                    if (zst && nq > 0) {
+                        if (lane == 0) ptx::bulk_wait_read();
+                        __syncwarp();
+                    }
                     uint32_t nx[8];
                     if (nq > 0) ptx::tmem_ld8(acc_tile, nx);
 #pragma unroll 1
@@ -1082,28 +1134,42 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         const float ub[4] = {__uint_as_float(nx[4]), __uint_as_float(nx[5]), __uint_as_float(nx[6]),
                                              __uint_as_float(nx[7])};
                         if (c + 2 < nq) ptx::tmem_ld8(acc_tile + (uint32_t)(4 * (c + 2)), nx);
+                        if (zst) {
+                            const float it = p.inv_tau;
+                            ptx::sts_f4(zrow + ((uint32_t)(c ^ (lane & 7)) << 4),
+                                        make_float4(ua[0] * it, ua[1] * it, ua[2] * it, ua[3] * it));
+                            ptx::sts_f4(zrow + ((uint32_t)((c + 1) ^ (lane & 7)) << 4),
+                                        make_float4(ub[0] * it, ub[1] * it, ub[2] * it, ub[3] * it));
+                        }
                         if (real) {
                             const int vq = v0 + 4 * c;
                             const uint4 wa = rng.quad((uint32_t)vq >> 2);
                             const uint4 wb = rng.quad(((uint32_t)vq >> 2) + 1u);
                             race_quad(ua, vq, wa);
                             if (c + 1 < nq) race_quad(ub, vq + 4, wb);
-                            if ((c & 3) == 2 && rE2 < INFINITY && fabsf(rz2) < kShareMaxZ2) {
-                                // share this thread's key with the row's other threads and
-                                // take the best one found so far (the atomic returns the
-                                // previous minimum): key = log2(E2_best) - z2_best, as
-                                // order-preserving bits
+                            if ((c & 3) == 2 && rE2 < INFINITY && fabsf(rz2) < kShareMaxZ2 &&
+                                fabsf(ref2) < kShareMaxZ2) {
+                                // key = log2(E2_best) - z2_best, as order-preserving bits
                                 const float lk = fast_log2(rE2) - rz2;
                                 const uint32_t kb = __float_as_uint(lk);
                                 const uint32_t ko = (kb & 0x80000000u) ? ~kb : (kb | 0x80000000u);
                                 const uint32_t bo = min(atomicMin(&s_key[nrow], ko), ko);
                                 const float lb = __uint_as_float((bo & 0x80000000u) ? (bo & 0x7fffffffu) : ~bo);
-                                // relative to this thread's reference; an exponent clamped
-                                // at -100 only loosens the screen
-                                Kh = fminf(Kh, fast_exp2(fmaxf(lb + rz2, -100.f)) * (kShareRel * kLn2));
+                                // per unit of t; an exponent clamped at -100 only loosens
+                                // the screen
+                                Kh = fmaxf(fminf(Kh, fast_exp2(fmaxf(lb + ref2, -100.f)) * (kShareRel * kLn2)), kKhMin);
                             }
                         }
                         __syncwarp();          // the next TMEM load and wait are warp-collective
+                    }
+                    if (zst && nq > 0) {
+                        // columns past V and rows past B are clipped by the store
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_3d(&a.zmap, zrow, v0, k - 1, b_base + (32 * q) % NC);
+                            ptx::bulk_commit();
+                        }
                     }
                     release_acc();
                 }
@@ -1155,9 +1221,12 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     const float E = rE2 * kLn2;
                     sn.zb = st.zb * p.inv_tau;
                     sn.best = sn.zb - logf(E);
-                    sn.s = st.s * E;
                     sn.idx = st.idx;
                 }
+                // log sum_v e^(z_v): the one-request form sums against its winner's
+                // z2 (rz2 * ln2 = the winner's z), the draft form against ref2
+                if constexpr (kOneRow) sn.lse = rE2 < INFINITY ? sn.zb + logf(osum) : -INFINITY;
+                else sn.lse = lsum > 0.f ? ref2 * kLn2 + logf(lsum) : -INFINITY;
                 if constexpr (kOneRow) {
                     // the lanes raced columns of the one request: merge them into lane 0's row
 #pragma unroll
@@ -1270,7 +1339,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int i = i0 + 32 * u;
-                        c[u] = i < GX ? __ldcg(part + i) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+                        c[u] = i < GX ? __ldcg(part + i) : make_float4(-INFINITY, __int_as_float(0x7fffffff), 0.f, -INFINITY);
                     }
 #pragma unroll
                     for (int u = 0; u < 4; ++u) m = drawlse_merge(m, drawlse_of(c[u]));
@@ -1280,13 +1349,15 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 if (lane == 0) {
                     const size_t o = (size_t)(b_base + n) * gamma + (k - 1);
                     p.draft_tok[o] = m.idx;
-                    p.lse_q[o] = m.best + logf(m.s);
+                    p.lse_q[o] = m.lse;
                     p.z_tok[o] = m.zb;
                 }
             }
             if (k == k_last) break;
         }
         if (failed) *abort_flag = 1u;
+        // the logits stores have read their buffers before the CTA leaves
+        if (zst && lane == 0) ptx::bulk_wait_all();
         // a target load still in flight (after a failure) lands before the CTA leaves
         if (kTgt && tinfl && lane == 0) ptx::mbar_wait(tbar(warp), (uint32_t)(ltile & 1), never, kDrainCycles);
         __syncwarp();
@@ -1381,7 +1452,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
 #pragma unroll
                     for (int u = 0; u < kBatch; ++u) {
                         const int i = i0 + u * TM;
-                        c[u] = i < nparts ? __ldcg(part + i) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+                        c[u] = i < nparts ? __ldcg(part + i) : make_float4(-INFINITY, __int_as_float(0x7fffffff), 0.f, -INFINITY);
                     }
 #pragma unroll
                     for (int u = 0; u < kBatch; ++u) m = drawlse_merge(m, drawlse_of(c[u]));
@@ -1391,7 +1462,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             if (sub == 0 && n < nb) {
                 const size_t o = (size_t)bb * gamma + (k - 1);
                 p.draft_tok[o] = m.idx;
-                p.lse_q[o] = m.best + logf(m.s);
+                p.lse_q[o] = m.lse;
                 p.z_tok[o] = m.zb;
             }
         }
@@ -1500,7 +1571,20 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const Layout L = rows_layout(a.NC, p.r, resid, tgt);
+    // the logits leave by tensor stores (the requests-on-lanes race without the
+    // target stream; the one-request form stores its lanes' columns directly)
+    const bool zst = !resid && !tgt && (gru != nullptr || p.B > 1) && p.logits_out != nullptr;
+    if (zst) {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)p.gamma, (cuuint64_t)p.B};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.V * 4, (cuuint64_t)p.gamma * p.V * 4};
+        const cuuint32_t box[3] = {32, 1, 32};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&a.zmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.logits_out, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const Layout L = rows_layout(a.NC, p.r, resid, tgt, zst, !resid && !gru && p.B == 1);
     size_t smem = L.total + 1024;
     if (vs) smem = smem > 1024 + 2 * (size_t)vs_inst_bytes(p.B) ? smem : 1024 + 2 * (size_t)vs_inst_bytes(p.B);
     auto kern = resid ? (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>)

@@ -57,7 +57,9 @@ draft_simt_kernel(const DraftParams p, const int k) {
     const int v_local = tid % kTV, bh = tid / kTV;        // bias mapping: 8 requests per thread
     const int bl_e = tid / 16, seg = tid % 16;              // epilogue mapping: 8 entries per thread
     const int ntiles = (V + kTV - 1) / kTV;
+    // running draw (best, idx, zb) and sum s = sum exp(z - best) of this thread's entries
     DrawLse st = drawlse_empty();
+    float ssum = 0.f;
     const uint32_t prow = (uint32_t)(p.req_base + b0 + bl_e) * (uint32_t)(gamma + 1) + (uint32_t)(k - 1);
     const Stream rng(p.seed, p.step, 0u, prow);
 
@@ -103,12 +105,12 @@ draft_simt_kernel(const DraftParams p, const int k) {
                         const int idx = vq + e;
                         if (st.best == -INFINITY) {
                             st.best = sc; st.idx = idx; st.zb = zs[e];
-                            st.s = __expf(zs[e] - sc);
+                            ssum = __expf(zs[e] - sc);
                         } else if (wins(sc, idx, st.best, st.idx)) {
-                            st.s = st.s * __expf(st.best - sc) + __expf(zs[e] - sc);
+                            ssum = ssum * __expf(st.best - sc) + __expf(zs[e] - sc);
                             st.best = sc; st.idx = idx; st.zb = zs[e];
                         } else {
-                            st.s += __expf(zs[e] - st.best);
+                            ssum += __expf(zs[e] - st.best);
                         }
                     }
                 }
@@ -117,6 +119,7 @@ draft_simt_kernel(const DraftParams p, const int k) {
         __syncthreads();
     }
 
+    st.lse = ssum > 0.f ? st.best + logf(ssum) : -INFINITY;
     // 16 threads share a request: butterfly over lanes xor 1..8
 #pragma unroll
     for (int m = 1; m < 16; m <<= 1) st = drawlse_merge(st, shfl_xor(st, m));
@@ -141,7 +144,7 @@ draft_simt_kernel(const DraftParams p, const int k) {
         for (int i = lane; i < (int)gridDim.x; i += 32) {
             DrawLse c;
             c.best = __ldcg(&part[i].best); c.idx = __ldcg(&part[i].idx);
-            c.zb = __ldcg(&part[i].zb); c.s = __ldcg(&part[i].s);
+            c.zb = __ldcg(&part[i].zb); c.lse = __ldcg(&part[i].lse);
             a = drawlse_merge(a, c);
         }
 #pragma unroll
@@ -149,7 +152,7 @@ draft_simt_kernel(const DraftParams p, const int k) {
         if (lane == 0) {
             const size_t o = (size_t)b * gamma + (k - 1);
             p.draft_tok[o] = a.idx;
-            p.lse_q[o] = a.best + logf(a.s);
+            p.lse_q[o] = a.lse;
             p.z_tok[o] = a.zb;
         }
     }
