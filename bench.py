@@ -307,8 +307,13 @@ def run_gpu(args):
     # residual draw, compaction
     launches_per_step = draft_launches * (2 if head == "rnn" else 1) + 6
     cpu = None
+    ties = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, mode, budget_s=args.cpu_budget, dev_inp=inp, min_seconds=10.0, head=head)
+        if _LAST_SAMPLE and head == "markov" and mode == 0:
+            off = buf.out_off.cpu().numpy()
+            ties = near_ties(buf.draft_tok.cpu().numpy(), buf.z_tok.cpu().numpy(), buf.accepted.cpu().numpy(),
+                             buf.out_tok.cpu().numpy()[off[1:] - 1], _LAST_SAMPLE, device_gumbel_error(vm, dev))
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
@@ -338,6 +343,7 @@ def run_gpu(args):
             "gpu_launches": launches_per_step * steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
+            "near_ties": ties,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -649,6 +655,7 @@ def cpu_baseline(w, mode, budget_s=20.0, dev_inp=None, min_seconds=0.0, head="ma
     if S >= threads:
         S = (S // threads) * threads
     sub = {k: inp[k][:S] for k in ("U", "target", "h", "anchor")}
+    _LAST_SAMPLE.clear()
     reps, tokens, dt = 0, 0, 0.0
     while reps == 0 or dt < min_seconds:
         t = time.perf_counter()
@@ -690,7 +697,69 @@ def _oracle_sample_step(w, mode, inp, sub, W1, W2, S, head="markov"):
     v = oracle.verify(sub["target"], sub["U"], None if arows is not None else W1, W2, sub["anchor"], d["tok"], K,
                       seed=w.seed, arows=arows)
     o = oracle.compact(d["tok"], v["accepted"], v["final_tok"])
+    _LAST_SAMPLE.update(S=S, draft=d, verify=v)
     return int(o["out_off"][-1])
+
+
+_LAST_SAMPLE = {}       # the oracle's outputs of the last cpu_baseline sample (first S requests)
+
+
+def near_ties(g_tok, g_ztok, g_acc, g_fin, sample, dg):
+    """The device's decisions on the cpu_baseline sample against the oracle's:
+    draws compared, mismatches, and near-ties at the published thresholds
+    (Gumbel top-2 gap 1e-3, acceptance margin 1e-5) and at eps = max(4 *
+    (max |z_tok error| + max |Gumbel error|), 1e-5); a mismatch that is no
+    near-tie at 1e-3 / 1e-5 counts as unflagged."""
+    import numpy as np
+    d, v, S = sample["draft"], sample["verify"], sample["S"]
+    tok, gap = d["tok"], d["gap"]
+    g_tok = g_tok[:S]
+    valid = np.ones(tok.shape, bool)
+    for b in range(S):
+        bad = np.nonzero(g_tok[b] != tok[b])[0]
+        if bad.size:
+            valid[b, bad[0]:] = False
+    dz = float(np.abs(g_ztok[:S][valid] - d["z_tok"][valid]).max()) if valid.any() else 0.0
+    eps = max(4.0 * (dz + dg), 1e-5)
+    c = dict(draws=0, mismatches=0, unflagged=0, flagged_1e3=0, flagged_eps=0)
+    for b in range(S):
+        for k in range(tok.shape[1]):
+            c["draws"] += 1
+            c["flagged_1e3"] += int(gap[b, k] < 1e-3)
+            c["flagged_eps"] += int(gap[b, k] < eps)
+            if g_tok[b, k] != tok[b, k]:
+                c["mismatches"] += 1
+                c["unflagged"] += int(gap[b, k] >= 1e-3)
+                break
+    for b in np.nonzero(valid.all(axis=1))[0]:
+        margin, fgap = v["diag"][b, 0], v["diag"][b, 1]
+        c["draws"] += 2                      # the accept walk and the final draw
+        c["flagged_1e3"] += int(margin < 1e-5) + int(fgap < 1e-3)
+        c["flagged_eps"] += int(margin < 1e-5) + int(fgap < eps)
+        if g_acc[b] != v["accepted"][b]:
+            c["mismatches"] += 1
+            c["unflagged"] += int(margin >= 1e-5)
+        elif g_fin[b] != v["final_tok"][b]:
+            c["mismatches"] += 1
+            c["unflagged"] += int(fgap >= 1e-3)
+    c.update(eps=eps, rate_eps=c["flagged_eps"] / max(1, c["draws"]), requests=int(S),
+             sample="the cpu_baseline requests, whole step")
+    return c
+
+
+def device_gumbel_error(vm, dev, n=1 << 18):
+    """max |G_device - G_exact| over n columns of two random streams (the
+    device's uniforms are exact; G_exact = -log(-log u) in binary64)."""
+    import numpy as np
+    g = torch.empty(n, device=dev)
+    u = torch.empty(n, device=dev)
+    worst = 0.0
+    for seed, dom, row in ((0, 0, 0), (2, 2, 77)):
+        vm.dspark_gumbel_stream(seed, 0, dom, row, n, g, u)
+        torch.cuda.synchronize(dev)
+        gu = u.cpu().double().numpy()
+        worst = max(worst, float(np.abs(g.cpu().double().numpy() + np.log(-np.log(gu))).max()))
+    return worst
 
 
 def run_reference(args):

@@ -8,8 +8,8 @@ from scipy import special, stats
 
 import oracle
 import workload
-from tests._parity import (GAP_EPS, LOGIT_ATOL, PROB_RTOL, U_EPS, assert_close_where,
-                           compare_draft)
+from tests._parity import (GAP_EPS, LOGIT_ATOL, PROB_RTOL, U_EPS, NearTieLedger, assert_close_where,
+                           compare_draft, max_abs_where, score_eps)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,17 +39,24 @@ def _draft_gpu(inp, B, gamma, V, r, seed, step=0, logits=False, req_base=0, tau=
     return tok.cpu().numpy(), lse.cpu().numpy(), zt.cpu().numpy(), (lo.cpu().numpy() if logits else None)
 
 
-def _check_draft(inp, w, seed, step=0, tau=1.0):
+def _check_draft(inp, w, seed, step=0, tau=1.0, dg=3e-6):
+    """The draft against the oracle: tokens bit-exact except near-ties, the
+    log-normalisers, drawn logits and the whole logits dump within 1e-3.
+    Every token mismatch must be a near-tie at the device's own error bound
+    eps (from the measured logit error and the device Gumbel error dg).
+    Returns the ledger."""
     tok, lse, zt, lo = _draft_gpu(inp, w.B, w.gamma, w.V, w.r, seed, step, logits=True, tau=tau)
     ci = _cpu(inp)
     ref = oracle.draft_markov(ci["U"], ci["W1"], ci["W2"], ci["anchor"], seed=seed, step=step,
                               want_logits=True, tau=tau)
     compared, flagged, valid = compare_draft(tok, ref["tok"], ref["gap"])
+    vmask = np.broadcast_to(valid[..., None], lo.shape)
     assert_close_where(lse, ref["lse_q"], valid, atol=LOGIT_ATOL, what="lse_q")
     assert_close_where(zt, ref["z_tok"], valid, atol=LOGIT_ATOL, what="z_tok")
-    assert_close_where(lo, ref["logits"], np.broadcast_to(valid[..., None], lo.shape), atol=LOGIT_ATOL,
-                       what="draft logits")
-    return compared, flagged
+    assert_close_where(lo, ref["logits"], vmask, atol=LOGIT_ATOL, what="draft logits")
+    ledger = NearTieLedger(score_eps(max_abs_where(lo, ref["logits"], vmask), dg))
+    ledger.draft(tok, ref["tok"], ref["gap"])
+    return ledger
 
 
 # ----------------------------------------------------------------- whole step
@@ -110,11 +117,11 @@ def test_tiny_workload_all_scheduler_modes(mode):
     (32, 2056, 128, torch.bfloat16),     # 4 vocabulary tiles per accumulator, ragged tail
     (40, 1032, 256, torch.bfloat16),     # 2 tiles per accumulator, partly filled rows
 ])
-def test_draft_parity(B, V, r, wdt):
+def test_draft_parity(B, V, r, wdt, device_gumbel_error):
     w = workload.custom("tiny", B=B, V=V, r=r, w_dtype=wdt, w_std=0.1, seed=B + V + r)
     inp = workload.inputs(w, device=DEV)
-    compared, flagged = _check_draft(inp, w, seed=11, step=2)
-    assert flagged <= max(1, compared // 100)
+    ledger = _check_draft(inp, w, seed=11, step=2, dg=device_gumbel_error)
+    print("near-ties", ledger.summary())
 
 
 def test_draft_temperature_and_request_base():
@@ -380,8 +387,8 @@ def test_draft_single_position_launch_tensor_cores():
     for B in (1, 70):
         w = workload.custom("tiny", B=B, V=2056, r=256, gamma=1, w_dtype=torch.bfloat16, w_std=0.1, seed=5 + B)
         inp = workload.inputs(w, device=DEV)
-        compared, flagged = _check_draft(inp, w, seed=7, step=1)
-        assert compared == B
+        ledger = _check_draft(inp, w, seed=7, step=1)
+        assert ledger.c["draft_draws"] == B
 
 
 def test_device_random_stream_matches_definition():
