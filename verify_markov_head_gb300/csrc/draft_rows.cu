@@ -59,6 +59,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 #include "sm100_ptx.cuh"
 #include "vstream.cuh"
 
@@ -648,6 +649,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     }
     if ((kTgt || kVs) && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.ws.tgt_token = p.tgt_token;
     if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 512u); ptx::tmem_relinquish(); }
+    // the residual draw is launched as a programmatic dependent of the accept
+    // walk: its set-up above overlaps the walk's tail, and it waits here before
+    // reading the rejected rows and log-normalisers the walk writes
+    if constexpr (kResid) grid_dependency_wait();
     for (int n = tid; n < 128; n += kThreads) {
         int x = -1, prow = -1;
         if (n < nb) {
@@ -1003,10 +1008,19 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                                     for (int e = 0; e < 4; ++e) {
                                         const float E = exp2_variate_of(ws[e]) * kLn2;
                                         if (rv[e] > 0.f && E < rv[e] * Kr) {
-                                            Kr = E / rv[e]; Krh = Kr * kRaceRel; st2.idx_r = vq + e;
+                                            Kr = __fdividef(E, rv[e]);
+                                            Krh = fminf(Krh, Kr * kRaceRel);
+                                            st2.idx_r = vq + e;
                                         }
                                     }
                                 }
+                            }
+                            if ((c & 3) == 3 && Kr < INFINITY) {
+                                // the key E / r needs no reference: share it with the row's
+                                // other threads (the bits of positive floats order as the
+                                // values) and screen against the best found so far
+                                const uint32_t bo = min(atomicMin(&s_key[nrow], __float_as_uint(Kr)), __float_as_uint(Kr));
+                                Krh = fminf(Krh, __uint_as_float(bo) * kRaceRel);
                             }
                         }
                     }
@@ -1248,7 +1262,13 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     for (int i = 0; i < RF; ++i)
 #pragma unroll
                         for (int c = 0; c < 4; ++c) s2 = draw2_merge(s2, m2[c * 128 + i * NC + etid]);
-                    if (s_row[etid] >= 0) p.ws.resid_part[(size_t)(b_base + etid) * p.ws.parts + blockIdx.x] = s2;
+                    // the draw is decided by an atomic maximum over the CTAs (score,
+                    // then lowest index), in the first winner-key line of the request
+                    if (s_row[etid] >= 0 && s2.best_r > -INFINITY) {
+                        DrawLse dk = drawlse_empty();
+                        dk.best = s2.best_r; dk.idx = s2.idx_r;
+                        atomicMax(&p.ws.win[(size_t)(b_base + etid) * kWinStride], win_key(dk));
+                    }
                 } else {
                     DrawLse s1 = drawlse_empty();
                     for (int i = 0; i < RF; ++i)
@@ -1411,35 +1431,20 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     if (tid < 32 * kEpiWarps) {
         const int bb = b_base + n;
         if constexpr (kResid) {
-            Draw2 m = draw2_empty();
-            if (n < nb && s_row[n] >= 0) {
-                const float4* part = reinterpret_cast<const float4*>(p.ws.resid_part + (size_t)bb * p.ws.parts);
-                for (int i0 = sub; i0 < nparts; i0 += kBatch * TM) {
-                    float4 c[kBatch];
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) {
-                        const int i = i0 + u * TM;
-                        c[u] = i < nparts ? __ldcg(part + i)
-                                          : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY,
-                                                        __int_as_float(0x7fffffff));
+            // the winner keys hold the draws: decode them and clear the lines for
+            // the next draft; a request without any residual winner draws from p
+            if (sub == 0 && n < nb) {
+                s_fb[n] = 0;
+                if (s_row[n] >= 0) {
+                    unsigned long long* wk = &p.ws.win[(size_t)bb * kWinStride];
+                    const unsigned long long key = __ldcg(wk);
+                    *wk = 0ull;
+                    if (key != 0ull) {
+                        p.ws.fin[bb] = win_token(key);
+                    } else {
+                        s_fb[n] = 1;                     // no residual mass: draw from p below
+                        if (a.near_ties) atomicAdd(&a.near_ties[1], 1u);
                     }
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) {
-                        Draw2 d;
-                        d.best_r = c[u].x; d.idx_r = __float_as_int(c[u].y);
-                        d.best_p = c[u].z; d.idx_p = __float_as_int(c[u].w);
-                        m = draw2_merge(m, d);
-                    }
-                }
-            }
-            for (int sh = 1; sh < TM; sh <<= 1) m = draw2_merge(m, shfl_xor(m, sh));
-            if (n < nb && sub == 0) s_fb[n] = 0;
-            if (sub == 0 && n < nb && s_row[n] >= 0) {
-                if (m.best_r > -INFINITY) {
-                    p.ws.fin[bb] = m.idx_r;
-                } else {
-                    s_fb[n] = 1;                         // no residual mass: draw from p below
-                    if (a.near_ties) atomicAdd(&a.near_ties[1], 1u);
                 }
             }
         } else {
@@ -1612,6 +1617,7 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
         void* args[] = {&a, const_cast<int*>(&k_first), const_cast<int*>(&k_last)};
         return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), args, smem, s);
     }
+    if (resid) return launch_dependent(kern, grid, dim3(kThreads), smem, s, a, k_first, k_last);
     kern<<<grid, kThreads, smem, s>>>(a, k_first, k_last);
     return cudaGetLastError();
 }
