@@ -652,7 +652,20 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     // the residual draw is launched as a programmatic dependent of the accept
     // walk: its set-up above overlaps the walk's tail, and it waits here before
     // reading the rejected rows and log-normalisers the walk writes
-    if constexpr (kResid) grid_dependency_wait();
+    if constexpr (kResid) {
+        // W2 does not depend on the walk: the CTA's first two super-tiles of it
+        // go to L2 before the wait
+        if (tid == kProducerWarp * 32) {
+            const int ntl = (V + kTN * RF - 1) / (kTN * RF);
+            for (int t = blockIdx.x, n = 0; t < ntl && n < 2; t += GX, ++n)
+                for (int i = 0; i < RF; ++i)
+                    for (int j = 0; j < p.r / 64; ++j) {
+                        ptx::tma_prefetch_2d(&a.w2map, t * kTN * RF + i * kTN, j * 64);
+                        ptx::tma_prefetch_2d(&a.w2map, t * kTN * RF + i * kTN + 64, j * 64);
+                    }
+        }
+        grid_dependency_wait();
+    }
     for (int n = tid; n < 128; n += kThreads) {
         int x = -1, prow = -1;
         if (n < nb) {
@@ -693,6 +706,22 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         }
     }
     if (warp < kEpiWarps) {                        // the A operands of the first position
+        if constexpr (kResid) {
+            // the first tile's rows of U and of the target, in flight during the
+            // W1 gathers and the first MMAs (the tile loop issues the later ones)
+            const int q0 = warp & 3, cb0 = warp >> 2, row0 = 32 * q0 + lane, nr0 = row0 % NC;
+            if ((32 * q0) % NC < nb) {
+                const bool real0 = nr0 < nb && s_row[nr0] >= 0;
+                const int ur = real0 ? s_row[nr0] : 0, bq = b_base + nr0;
+                const float* Ur = static_cast<const float*>(p.U) + ((size_t)bq * gamma + ur) * V;
+                const TT* Tr = static_cast<const TT*>(a.target) + ((size_t)bq * (gamma + 1) + ur) * V;
+                const unsigned m0 = __ballot_sync(0xffffffffu, real0);
+                const uint32_t ub = base + L.u + (uint32_t)warp * 8192u;
+                const int v00 = (int)blockIdx.x * kTN * RF + (row0 / NC) * kTN + 32 * cb0;
+                issue_rows<float>(ub, Ur, m0, v00, V, lane);
+                issue_rows<TT>(ub + 4096u, Tr, m0, v00, V, lane);
+            }
+        }
         if (st_base)
             stage_a_state(tmem_base, st_base, (size_t)p.B * r, kResid ? -1 : k_first - 1, s_row, s_tok, NC, RF, r,
                           V, warp & 3, warp >> 2, lane, true);
@@ -943,8 +972,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     const uint8_t* ubuf_g = gbase + L.u + (size_t)warp * 8192;
                     const unsigned real_mask = __ballot_sync(0xffffffffu, real);
                     float* z = bias;                           // z overwrites the bias in place
-                    if (t == (int)blockIdx.x) issue_rows<float>(ubuf, Urow, real_mask, v0, V, lane);
-                    issue_rows<TT>(tbuf, Trow, real_mask, v0, V, lane);
+                    // (the first tile's rows were issued before the W1 gathers)
+                    if (t != (int)blockIdx.x) issue_rows<TT>(tbuf, Trow, real_mask, v0, V, lane);
                     ptx::cp_async_wait_group<1>();             // this tile's U rows
                     __syncwarp();
                     if (real) {

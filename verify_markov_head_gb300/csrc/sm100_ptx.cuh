@@ -63,6 +63,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// Prefetch one box of a 2-D tensor map at (x, y) into L2 (no shared memory,
+// no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y) : "memory");
+}
+
 // Tensor store shared -> global of one box at (x, y, z) (the map's box and
 // swizzle), in this thread's bulk group; elements outside the tensor are not
 // written.  The shared source must stay unchanged until bulk_wait_read.
