@@ -78,6 +78,18 @@ size_t dspark_workspace_bytes(int B, int gamma, int V, int r);
  * use).  Call once after allocating it; the kernels leave it reusable. */
 dspark_status dspark_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
+/* Bound the device waits of the calls that use this workspace: a wait on
+ * another role of a kernel or on other CTAs (copy rings, accumulator
+ * hand-offs, grid barriers, the verify stream's ring) gives up after about
+ * `cycles` SM clock cycles, raises the timeout bit (dspark_sync_status then
+ * returns DSPARK_ERR_TIMEOUT) and the kernel drains the copies it issued,
+ * frees its tensor memory and returns.  0 restores the default, about 2 s
+ * at 2 GHz; dspark_workspace_init also restores it.  A small bound exists
+ * to exercise that path in tests: with it, results are unspecified, and the
+ * workspace needs dspark_workspace_init before its next use.  The value
+ * lives in bytes 8-15 of the workspace.  No counterpart on the pages. */
+dspark_status dspark_workspace_set_wait_limit(void* ws, size_t ws_bytes, uint64_t cycles, void* stream);
+
 /* Synchronise `stream`, then read and clear the workspace status word.
  * Returns DSPARK_OK, DSPARK_ERR_DEVICE (range check fired), DSPARK_ERR_TIMEOUT,
  * or DSPARK_ERR_CUDA (the stream reported an error).  If bits is non-NULL the

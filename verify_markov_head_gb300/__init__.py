@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "DsparkError", "lib_path", "dspark_version", "dspark_status_string", "dspark_workspace_bytes",
-    "dspark_workspace_init", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
+    "dspark_workspace_init", "dspark_workspace_set_wait_limit", "dspark_sync_status", "dspark_draft_markov", "dspark_confidence_sts",
     "dspark_schedule", "dspark_verify", "dspark_draft_markov_target", "target_stream_supported", "dspark_draft_rnn", "dspark_verify_rnn", "dspark_verify_logits", "dspark_rnn_input_table", "rnn_prepare", "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_gumbel_stream", "dspark_draft_markov_noalloc", "dspark_noalloc_sync_status", "Workspace", "StepBuffers", "run_step", "run_step_host", "run_step_dp", "GlobalSchedule", "HostPipeline",
     "SCHED_OFF", "SCHED_SYNC", "SCHED_ASYNC",
 ]
@@ -41,6 +41,8 @@ _lib.dspark_workspace_bytes.argtypes = [_i, _i, _i, _i]
 _lib.dspark_workspace_bytes.restype = _sz
 _lib.dspark_workspace_init.argtypes = [_vp, _sz, _vp]
 _lib.dspark_workspace_init.restype = _i
+_lib.dspark_workspace_set_wait_limit.argtypes = [_vp, _sz, _u64, _vp]
+_lib.dspark_workspace_set_wait_limit.restype = _i
 _lib.dspark_sync_status.argtypes = [_vp, _vp, C.POINTER(C.c_uint32)]
 _lib.dspark_sync_status.restype = _i
 _lib.dspark_draft_markov.argtypes = [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
@@ -131,6 +133,12 @@ def dspark_workspace_bytes(B, gamma, V, r) -> int:
 
 def dspark_workspace_init(ws: torch.Tensor, stream=None):
     _check("dspark_workspace_init", _lib.dspark_workspace_init(_p(ws), ws.numel(), _stream(stream)))
+
+
+def dspark_workspace_set_wait_limit(ws: torch.Tensor, cycles: int, stream=None):
+    """Bound the device waits of calls on this workspace (0: the default)."""
+    _check("dspark_workspace_set_wait_limit",
+           _lib.dspark_workspace_set_wait_limit(_p(ws), ws.numel(), int(cycles), _stream(stream)))
 
 
 def dspark_sync_status(ws: torch.Tensor, stream=None):

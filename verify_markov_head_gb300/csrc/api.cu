@@ -54,6 +54,7 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     char* base = static_cast<char*>(ws);
     WsPtrs P;
     P.status = reinterpret_cast<uint32_t*>(base + L.status);
+    P.wait_limit = reinterpret_cast<unsigned long long*>(base + L.status + 8);
     P.tickets_draft = reinterpret_cast<uint32_t*>(base + L.tickets);
     P.tickets_resid = P.tickets_draft + ((size_t)B + kChunk - 1) / kChunk;
     P.gbar = reinterpret_cast<uint32_t*>(base + L.gbar);
@@ -138,6 +139,8 @@ dspark_status read_status_word(void* word, cudaStream_t s, uint32_t* bits) {
     return DSPARK_OK;
 }
 
+__global__ void set_u64_kernel(unsigned long long* dst, unsigned long long v) { *dst = v; }
+
 }  // namespace dspark
 
 using namespace dspark;
@@ -166,6 +169,13 @@ size_t dspark_workspace_bytes(int B, int gamma, int V, int r) {
 dspark_status dspark_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (!is_device_ptr(ws) || ws_bytes < 256) return DSPARK_ERR_INVALID;
     return launch_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+dspark_status dspark_workspace_set_wait_limit(void* ws, size_t ws_bytes, uint64_t cycles, void* stream) {
+    if (!is_device_ptr(ws) || ws_bytes < 256) return DSPARK_ERR_INVALID;
+    unsigned long long* dst = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + 8);
+    set_u64_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(dst, (unsigned long long)cycles);
+    return launch_status(cudaGetLastError());
 }
 
 dspark_status dspark_sync_status(void* ws, void* stream, uint32_t* bits) {

@@ -305,6 +305,16 @@ __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
     if (status) atomicOr(status, bit);
 }
 
+// The bound on device waits that can block on another role or CTA: the
+// workspace's value (dspark_workspace_set_wait_limit), 0 meaning the default
+// of about 2 s at 2 GHz.  Drains of copies already issued keep their own
+// fixed bounds: those copies always land.
+constexpr long long kDefaultWaitCycles = 4000000000LL;
+__device__ __forceinline__ long long wait_limit_of(const unsigned long long* w) {
+    const unsigned long long v = w ? *w : 0ull;
+    return v ? (long long)v : kDefaultWaitCycles;
+}
+
 // A bounded wait expired: the timeout bit, plus bit (8 + site) naming the
 // wait that gave up (sites 0..23, see the kernel that raises it).
 __device__ __forceinline__ void raise_timeout(uint32_t* status, int site) {

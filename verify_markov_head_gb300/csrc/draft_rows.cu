@@ -87,7 +87,7 @@ constexpr int kTBufBytes = 32 * 128;              // target stream: one warp's 3
 constexpr int kZBufBytes = 32 * 128;              // logits store: one warp's 32 rows x 32 fp32 of a tile
 constexpr int kUSlotsResid = 8;                   // residual: 16 warps x (4 KB U + 4 KB target) row staging
 constexpr int kSmemBudget = 227 * 1024;
-constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
+constexpr long long kWaitCycles = kDefaultWaitCycles;   // the MMA drain: ~2 s at 2 GHz
 constexpr long long kDrainCycles = 200000000LL;   // ~0.1 s: copies already issued landing
 // Margins of the exponential-race screens (relative on the running winner's
 // variate, absolute on the candidate's bound): far above the rounding of the
@@ -566,6 +566,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     constexpr bool kQuadLoop = !kResid && !kOneRow;
     const DraftParams& p = a.p;
     const int NC = a.NC;
+    const long long wl = wait_limit_of(p.ws.wait_limit);   // bound of the waits on other roles and CTAs
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -697,7 +698,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             gate_step(a.gru, 0, cta_id, (int)nctas, tid, 32 * kEpiWarps, nullptr, p.ws.win);
             ptx::named_barrier(1, 32 * kEpiWarps);
             if (tid == 0)
-                s_pro_ok = grid_barrier(p.ws.gbar + kGbarGru + (kGridBarrierSlots - 1), nctas, abort_flag, kWaitCycles);
+                s_pro_ok = grid_barrier(p.ws.gbar + kGbarGru + (kGridBarrierSlots - 1), nctas, abort_flag, wl);
             ptx::named_barrier(1, 32 * kEpiWarps);
             if (!s_pro_ok && tid == 0) {
                 raise_timeout(p.ws.status, 10);
@@ -747,7 +748,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     const int vs = t * kTN * RF;
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
-                            if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kWaitCycles))) { site = 1; break; }
+                            if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, wl))) { site = 1; break; }
                             ptx::mbar_arrive_expect_tx(full(stage), kBBytes);
                             const uint32_t dst = base + L.b + (uint32_t)stage * kBBytes;
                             const int v0 = vs + i * kTN;
@@ -783,7 +784,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     for (int c = 0; c < 4 && ok; ++c) {
                         const int n = lt * 4 + c, s = n % US;
                         const uint32_t par = (uint32_t)((n / US) & 1);
-                        if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, kWaitCycles))) { site = 2; break; }
+                        if (!(ok = ptx::mbar_wait(uempty(s), par ^ 1u, abort_flag, wl))) { site = 2; break; }
                         ptx::mbar_arrive_expect_tx(ufull(s), slot_bytes);
                         for (int i = 0; i < RF; ++i)      // rows [i*NC, (i+1)*NC) hold tile i's U slice
                             ptx::tma_load_3d(base + L.u + (uint32_t)s * slot_bytes + (uint32_t)i * blk, &a.umap,
@@ -811,7 +812,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             for (int k = k_first; k <= k_last && ok; ++k) {
                 bool wait_a = k > k_first;   // h of this position is staged by the epilogue warps
                 for (int t = blockIdx.x; t < ntiles && ok; t += GX, ++lt) {
-                    if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, kWaitCycles))) { site = 4; break; }
+                    if (!(ok = ptx::mbar_wait(tempty(acc), aph ^ 1u, abort_flag, wl))) { site = 4; break; }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc0 + (uint32_t)(acc * kTN);
                     if constexpr (!kResid) {
@@ -820,7 +821,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         // time; the MMAs below then add h.W2 on top
                         for (int c = 0; c < 4 && ok; ++c) {
                             const int n = lt * 4 + c, s = n % US;
-                            if (!(ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, kWaitCycles))) {
+                            if (!(ok = ptx::mbar_wait(ufull(s), (uint32_t)((n / US) & 1), abort_flag, wl))) {
                                 site = 9;
                                 break;
                             }
@@ -835,7 +836,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         if (!ok) break;
                     }
                     if (wait_a) {   // the first tile's U copies above do not need h
-                        if (!(ok = ptx::mbar_wait(a_ready, (uint32_t)((k - k_first - 1) & 1), abort_flag, kWaitCycles))) {
+                        if (!(ok = ptx::mbar_wait(a_ready, (uint32_t)((k - k_first - 1) & 1), abort_flag, wl))) {
                             site = 3;
                             break;
                         }
@@ -844,7 +845,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     }
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
-                            if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, kWaitCycles))) { site = 5; break; }
+                            if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, wl))) { site = 5; break; }
                             ptx::tc_fence_after();
                             const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
                             // A_i in TMEM: K-chunk j = 32 columns, 16 ranks = 8 columns
@@ -934,7 +935,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             Draw2 st2 = draw2_empty();
             float tm2 = -INFINITY, tsum = 0.f;         // target stream: this row's base-2 log-sum-exp state
             for (int t = blockIdx.x; t < ntiles; t += GX) {
-                bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, kWaitCycles);
+                bool ok = ptx::mbar_wait(tfull(acc), aph, abort_flag, wl);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 6); failed = true; break; }
                 ptx::tc_fence_after();
@@ -1221,7 +1222,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     // race: the bias is dead by now), then the next tile's block into
                     // the same buffer
                     if (active) {
-                        bool okt = ptx::mbar_wait(tbar(warp), (uint32_t)(ltile & 1), abort_flag, kWaitCycles);
+                        bool okt = ptx::mbar_wait(tbar(warp), (uint32_t)(ltile & 1), abort_flag, wl);
                         okt = __all_sync(0xffffffffu, okt);
                         if (!okt) { if (lane == 0 && !*abort_flag) raise_timeout(p.ws.status, 12); failed = true; break; }
                         tinfl = false;
@@ -1328,7 +1329,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             // ---- grid barrier, then every CTA merges the partials of its own requests
             ptx::named_barrier(1, 32 * kEpiWarps);
             __shared__ int s_gb_ok;
-            if (etid == 0) s_gb_ok = grid_barrier(p.ws.gbar + (k - k_first), nctas, abort_flag, kWaitCycles) ? 1 : 0;
+            if (etid == 0) s_gb_ok = grid_barrier(p.ws.gbar + (k - k_first), nctas, abort_flag, wl) ? 1 : 0;
             ptx::named_barrier(1, 32 * kEpiWarps);
             if (!s_gb_ok) {
                 if (etid == 0) raise_timeout(p.ws.status, 8);
@@ -1356,7 +1357,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                               32 * kEpiWarps, gridDim.y == 1 ? s_tok : nullptr, p.ws.win);
                     ptx::named_barrier(1, 32 * kEpiWarps);
                     if (etid == 0)
-                        s_gb_ok = grid_barrier(p.ws.gbar + kGbarGru + (k - k_first), nctas, abort_flag, kWaitCycles) ? 1 : 0;
+                        s_gb_ok = grid_barrier(p.ws.gbar + kGbarGru + (k - k_first), nctas, abort_flag, wl) ? 1 : 0;
                     ptx::named_barrier(1, 32 * kEpiWarps);
                     if (!s_gb_ok) {
                         if (etid == 0) raise_timeout(p.ws.status, 9);

@@ -61,6 +61,7 @@ WsLayout ws_layout(int B, int gamma, int V);
 
 struct WsPtrs {
     uint32_t* status;
+    unsigned long long* wait_limit;   // bound on device waits in SM cycles (0: the default, about 2 s)
     uint32_t* tickets_draft;   // [ceil(B/kChunk)] arrival counters, zero between launches
     uint32_t* tickets_resid;   // [ceil(B/kChunk)]
     uint32_t* gbar;            // [kGbarExit + 1] grid-barrier counters, then the exit counter

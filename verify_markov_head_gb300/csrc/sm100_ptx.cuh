@@ -43,10 +43,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: gives up after ~limit_cycles SM clocks, or at once when
 // *abort is set by another thread.  Returns false on either.  Between tries
 // the thread sleeps (32 ns doubling to 256 ns), so a waiting warp leaves the
-// issue slots of its scheduler to the warps that have work.
+// issue slots of its scheduler to the warps that have work.  A try may itself
+// suspend the thread up to ~10 us, so the bound holds to about that.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile uint32_t* abort,
                                           long long limit_cycles) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -61,6 +72,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
             if (clock64() - t0 > limit_cycles) return false;
         }
     }
+}
+
+// mbar_wait that also holds a bound below 2^20 cycles (a test of the timeout
+// path) to the cycle: such a bound polls with non-blocking tests, checked
+// every time.  For waits that are not on a latency-critical path.
+__device__ __forceinline__ bool mbar_wait_strict(uint32_t bar, uint32_t parity, const volatile uint32_t* abort,
+                                                 long long limit_cycles) {
+    if (limit_cycles >= (1LL << 20)) return mbar_wait(bar, parity, abort, limit_cycles);
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity)) {
+        if (*abort || clock64() - t0 > limit_cycles) return false;
+    }
+    return true;
+}
+
+// Bounded wait for a phase that will complete (copies already issued):
+// no abort flag; gives up after ~limit_cycles.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, long long limit_cycles) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(64);
+        if (clock64() - t0 > limit_cycles) return false;
+    }
+    return true;
 }
 
 // Prefetch one box of a 2-D tensor map at (x, y) into L2 (no shared memory,

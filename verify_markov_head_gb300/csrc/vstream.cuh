@@ -19,7 +19,7 @@ constexpr int kStreamStages = 3;
 constexpr int kStreamChunk = 8192;                           // entries per bulk copy
 constexpr int kStreamStageBytes = kStreamChunk * 4;          // fp32 chunk (bf16 uses half)
 constexpr int kPerThread = kStreamChunk / (32 * kStreamConsumers);   // 32 entries per consumer per chunk
-constexpr long long kStreamWaitCycles = 4000000000LL;        // ~2 s at 2 GHz
+constexpr long long kStreamDrainCycles = 200000000LL;        // ~0.1 s: bulk copies already issued landing
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kStreamKCache = 2048;                          // verify lengths kept in shared memory up to this B (8 KB)
 
@@ -68,6 +68,7 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
 
     const int gamma = p.gamma, V = p.V;
     const int nseg = p.ws.nseg;
+    const long long wl = wait_limit_of(p.ws.wait_limit);   // bound of the waits on the other role
     const int nbonus = kHasBonus ? p.B * nseg : 0;           // bonus items come first
     const int items = nbonus + (kHasLse ? p.B * gamma * nseg : 0);
     const int warp = tid / 32, lane = tid % 32;
@@ -110,6 +111,7 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
+            long long nf = 0;                            // bulk copies issued
             for (;;) {
                 const int u = (int)atomicAdd(&p.ws.vq[0], 1u);
                 if (u >= items) break;
@@ -118,21 +120,30 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
                 const int v_end = min(V, (seg + 1) * kVerifySeg);
                 const TT* row = static_cast<const TT*>(p.target) + ((size_t)b * (gamma + 1) + i) * V;
                 for (int v0 = seg * kVerifySeg; v0 < v_end; v0 += kStreamChunk) {
-                    if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kStreamWaitCycles))) break;
+                    if (!(ok = ptx::mbar_wait_strict(empty(stage), ph ^ 1u, abort_flag, wl))) break;
                     s_meta[stage] = make_int2(u, v0);
                     const uint32_t bytes = (uint32_t)(min(kStreamChunk, v_end - v0) * (int)sizeof(TT));
                     ptx::mbar_arrive_expect_tx(full(stage), bytes);
                     ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes, row + v0, bytes, full(stage), pol);
+                    ++nf;
                     if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
             }
             // the end-of-stream tag
-            if (ok && (ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, kStreamWaitCycles))) {
+            if (ok && (ok = ptx::mbar_wait_strict(empty(stage), ph ^ 1u, abort_flag, wl))) {
                 s_meta[stage] = make_int2(-1, 0);
                 ptx::mbar_arrive(full(stage));
+                ++nf;                                    // the tag completes a phase of its stage too
             }
             if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
+            // every copy issued lands before the instance leaves: the last fill of
+            // each stage (complete already unless the consumers gave up)
+            for (int i = 0; i < kStreamStages; ++i)
+                if (nf > i) {
+                    const long long m = (nf - 1) - ((nf - 1 - i) % kStreamStages);
+                    ptx::mbar_wait_drain(full(i), (uint32_t)((m / kStreamStages) & 1), kStreamDrainCycles);
+                }
         }
         __syncwarp();
     } else {
@@ -183,9 +194,13 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
             }
         };
         for (;;) {
-            bool ok = ptx::mbar_wait(full(stage), ph, abort_flag, kStreamWaitCycles);
+            bool ok = ptx::mbar_wait_strict(full(stage), ph, abort_flag, wl);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) { *abort_flag = 1u; break; }
+            if (!ok) {                                   // a consumer gave up: report it too
+                if (lane == 0) raise_status(p.ws.status, kTimeout);
+                *abort_flag = 1u;
+                break;
+            }
             const int2 meta = s_meta[stage];
             if (meta.x < 0) break;                       // end of stream
             if (meta.x != cur) {                         // a new item
@@ -266,9 +281,6 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
             }
         }
         if (cur >= 0 && !*abort_flag) flush();
-    }
-    if (*abort_flag) {
-        for (int i = 0; i < 64; ++i) __nanosleep(1000);   // let copies in flight land
     }
     ptx::named_barrier(bar_id, kStreamThreads);
     // the last instance out clears the work counter for the next launch
