@@ -71,6 +71,9 @@ def _load():
             lib.oracle_uniform.restype = C.c_double
             lib.oracle_gumbel.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint32]
             lib.oracle_gumbel.restype = C.c_double
+            lib.oracle_gumbel_span.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint32, C.c_int,
+                                               f64p]
+            lib.oracle_gumbel_span.restype = None
             lib.oracle_draft_markov.argtypes = [
                 f64p, f64p, f64p, i32p, i32p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_double,
                 C.c_uint64, C.c_uint64, i32p, f64p, f64p, f64p, opt_f64]
@@ -149,6 +152,69 @@ def uniform(seed, step, domain, row, col) -> float:
 
 def gumbel(seed, step, domain, row, col) -> float:
     return float(_load().oracle_gumbel(seed, step, domain, row, col))
+
+
+def gumbel_span(seed, step, domain, row, col0, n) -> np.ndarray:
+    """G for columns col0 .. col0+n-1 of one stream."""
+    out = np.zeros(n)
+    _load().oracle_gumbel_span(seed, step, domain, row, col0, n, out)
+    return out
+
+
+# --------------------------------------------------------------------------- #
+# vocabulary slices: the per-slice states a split of V over ranks exchanges   #
+# [P2 §Markov Head：一阶转移偏置] (the bias spans the whole vocabulary, so a    #
+# split of V shares one draw and one log-sum-exp per position)               #
+# --------------------------------------------------------------------------- #
+def _lse(x) -> float:
+    x = np.asarray(x, np.float64)
+    m = x.max() if x.size else -np.inf
+    if m == -np.inf:
+        return -np.inf
+    return float(m + np.log(np.exp(x - m).sum()))
+
+
+def _argmax_first(score) -> int:
+    """Lowest index among the maxima (the draw's tie rule)."""
+    return int(np.argmax(score))
+
+
+def slice_draft(U_row, h, W2_slice, col0, *, seed, step, row, tau=1.0):
+    """Position draw on columns col0 .. col0+n-1 of one request's row:
+    z = (U + h . W2) / tau over the slice, best = max z + G (domain 0, global
+    column index), its index and z, and lse = log sum exp z of the slice."""
+    z = (_f64(U_row) + _f64(h) @ _f64(W2_slice)) / tau
+    g = gumbel_span(seed, step, 0, row, col0, z.size)
+    s = z + g
+    i = _argmax_first(s)
+    return dict(best=float(s[i]), idx=col0 + i, zb=float(z[i]), lse=_lse(z))
+
+
+def slice_lse(x_slice, tau=1.0) -> float:
+    """log sum exp(x / tau) over a slice of a target row."""
+    return _lse(_f64(x_slice) / tau)
+
+
+def slice_residual(t_slice, z_slice, lse_p, lse_q, col0, *, seed, step, row, tau=1.0):
+    """The residual draw on a slice: p = exp(t / tau - lse_p), q = exp(z -
+    lse_q), argmax log(max(0, p - q)) + G (domain 2) where p > q (best_r =
+    -inf if none), and the fallback draw from p, argmax t / tau + G."""
+    t = _f64(t_slice) / tau
+    r = np.exp(t - lse_p) - np.exp(_f64(z_slice) - lse_q)
+    g = gumbel_span(seed, step, 2, row, col0, t.size)
+    with np.errstate(divide="ignore"):
+        sr = np.where(r > 0, np.log(np.where(r > 0, r, 1.0)) + g, -np.inf)
+    ir = _argmax_first(sr)
+    sp = t + g
+    ip = _argmax_first(sp)
+    return dict(best_r=float(sr[ir]), idx_r=col0 + ir, best_p=float(sp[ip]), idx_p=col0 + ip)
+
+
+def slice_bonus(t_slice, col0, *, seed, step, row, tau=1.0):
+    """The bonus draw on a slice: argmax t / tau + G (domain 3)."""
+    s = _f64(t_slice) / tau + gumbel_span(seed, step, 3, row, col0, np.asarray(t_slice).size)
+    i = _argmax_first(s)
+    return dict(best=float(s[i]), idx=col0 + i)
 
 
 # --------------------------------------------------------------------------- #

@@ -92,6 +92,14 @@ double oracle_gumbel(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row
     return -log(-log(u));
 }
 
+/* G for columns col0 .. col0+n-1 of one stream (the definition above,
+ * column by column; the vocabulary-split checks draw on slices of a row). */
+void oracle_gumbel_span(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row, uint32_t col0, int n,
+                        double* out)
+{
+    for (int i = 0; i < n; ++i) out[i] = oracle_gumbel(seed, step, domain, row, col0 + (uint32_t)i);
+}
+
 /* Two-pass log-sum-exp of x[0..n). */
 static double logsumexp(const double* x, int n)
 {
