@@ -583,6 +583,49 @@ def d_of(w):
     return w.d
 
 
+def run_kernel(args):
+    """One ABI call, repeated, on the workload's shapes with only the inputs it
+    reads on the device (no embedding table), for profiler captures of a
+    single kernel; prints the status and no metric.  draft: dspark_draft_markov;
+    verify: one draft, then dspark_verify with every K_b = gamma (verify
+    stream, accept walk, residual draw, compaction)."""
+    import verify_markov_head_gb300 as vm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = workload.WORKLOADS[args.workload]
+    B, gamma, V, r = w.B, w.gamma, w.V, w.r
+    inp = workload.draft_weights(w, device=dev)
+    st = workload.step_inputs(w, device=dev)
+    inp.update(U=st["U"], target=st["target"], anchor=st["anchor"])
+    ws = vm.Workspace(B, gamma, V, r, dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    tok = torch.empty((B, gamma), **i32)
+    lse = torch.empty((B, gamma), device=dev)
+    zt = torch.empty((B, gamma), device=dev)
+    K = torch.full((B,), gamma, **i32)
+    acc, nxt = torch.empty((B,), **i32), torch.empty((B,), **i32)
+    out_tok, out_req, out_pos = (torch.empty((B * (gamma + 1),), **i32) for _ in range(3))
+    out_off = torch.empty((B + 1,), **i32)
+
+    def draft():
+        vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], tok, lse, zt, ws, seed=w.seed)
+
+    def verify():
+        vm.dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], tok, lse, zt, K, acc,
+                         out_tok, out_req, out_pos, out_off, nxt, ws, seed=w.seed)
+
+    if args.kernel == "verify":
+        draft()
+    for _ in range(args.calls):
+        (draft if args.kernel == "draft" else verify)()
+    status, bits = vm.dspark_sync_status(ws.buf)
+    print(json.dumps({"kernel_run": args.kernel, "workload": w.name, "calls": args.calls, "status": status,
+                      "bits": bits}), flush=True)
+    if status != 0:
+        raise SystemExit(1)
+
+
 # Sources the draft kernel is compiled from: DRAM traffic taken from an ncu
 # capture is reported only while they are unchanged since the capture.
 _DRAFT_SOURCES = ("draft_rows.cu", "common.cuh", "sm100_ptx.cuh", "internal.h", "vstream.cuh")
@@ -810,12 +853,18 @@ def main():
                          "in full-prefix mode")
     ap.add_argument("--sts", action="store_true",
                     help="time the STS temperature fit (2^20 validation blocks, 256 temperatures)")
+    ap.add_argument("--kernel", default=None, choices=["draft", "verify"],
+                    help="run one ABI call --calls times on the workload's shapes (for profiler captures); "
+                         "prints no metric")
+    ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--sts-blocks", type=int, default=None,
                     help="validation blocks of the STS fit (default 2^20; smaller for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.kernel:
+        run_kernel(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.chain:
         run_chain(args)

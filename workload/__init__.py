@@ -123,6 +123,14 @@ def _boosted_logits(B, rows, V, std, boosts, g, device):
     return x
 
 
+def draft_weights(w: Workload, device="cpu") -> dict:
+    """W1 [V,r] and W2 [r,V] alone, the same values weights() draws."""
+    g = _gen(device, w.seed, 1)
+    W1 = (torch.randn((w.V, w.r), generator=g, device=device) * w.w_std).to(w.w_dtype)
+    W2 = (torch.randn((w.r, w.V), generator=g, device=device) * w.w_std).to(w.w_dtype)
+    return dict(W1=W1.contiguous(), W2=W2.contiguous())
+
+
 def weights(w: Workload, device="cpu") -> dict:
     """Draft-head parameters: W1 [V,r], W2 [r,V], emb [V,d], w_c [2d], b_c."""
     g = _gen(device, w.seed, 1)
