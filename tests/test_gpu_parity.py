@@ -155,6 +155,25 @@ def test_draft_gamma_one_and_sixteen():
 
 # ----------------------------------------------------------------- confidence
 
+@pytest.mark.parametrize("jumps", [(16,), (8, 24)])
+def test_draft_reference_moves_after_a_winner(jumps, device_gumbel_error):
+    """Logits that rise by 60 nats (87 in base 2) at the given columns of every
+    32-column block, so that the race's log-sum-exp reference (the first quad's
+    maximum) moves up after the thread has a winner: the winner key and the
+    screen threshold must grow with it, and the draw then comes from the high
+    columns, as the oracle's does."""
+    w = workload.custom("tiny", B=8, V=4096, r=64, w_dtype=torch.bfloat16, seed=21)
+    inp = workload.inputs(w, device=DEV)
+    v = torch.arange(w.V, device=DEV)
+    bump = torch.zeros(w.V, device=DEV)
+    for j in jumps:
+        bump += 60.0 * ((v % 32) >= j).float()
+    inp["U"] = inp["U"] + bump
+    for seed in (3, 4):
+        ledger = _check_draft(inp, w, seed=seed, dg=device_gumbel_error)
+        assert ledger.c["draft_draws"] >= w.B
+
+
 def test_confidence_parity_fp32_and_bf16_embeddings():
     for edt, d in ((torch.float32, 64), (torch.float32, 4096), (torch.bfloat16, 256), (torch.float32, 30)):
         w = workload.custom("tiny", B=9, d=d, seed=d)

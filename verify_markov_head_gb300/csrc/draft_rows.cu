@@ -70,15 +70,21 @@ constexpr int kEpiWarps = 16;
 constexpr int kThreads = (kEpiWarps + 3) * 32;   // 608
 constexpr int kProducerWarp = 16, kMmaWarp = 17, kUWarp = 18;
 constexpr int kTN = 128;                          // vocabulary entries per tile
-constexpr int kMaxStages = 12;                    // W2 K-chunk ring depth (as shared memory allows)
-// With the race in the epilogue the W2 ring needs no more than 5 stages (measured:
-// 5 stages run faster than 9 at 64 and 512 requests); the one-request form is
-// bound by the ring's turnaround and takes what shared memory allows.
-constexpr int kMaxStagesRace = 5;
+constexpr int kMaxStages = 12;                    // W2 K-chunk ring depth (barriers reserved)
 // TMEM (512 columns): RF A operands of 128 columns, then 4 - RF accumulators
 // of 128 columns (three at RF = 1, two at RF = 2).
 constexpr int kMaxAcc = 3;
-constexpr int kBBytes = kTN * 64 * 2;             // one K-chunk of the W2 tile (bf16), 16 KB
+// W2 moves in K-chunks of kc ranks of one 128-entry tile (bf16), two 64-entry
+// boxes per chunk.  The one-request form, bound by the ring's turnaround, takes
+// kc = 128 where r allows (32 KB chunks: half the round trips per tile; measured
+// 153.7 -> 149.3 us a b1 step); the race kernels keep kc = 64 (16 KB), which
+// measured as fast or faster at 64 to 512 requests.
+__host__ __device__ constexpr int w2_kc(int r, bool one_row) { return one_row && r % 128 == 0 ? 128 : 64; }
+// Ring sizes: with the race in the epilogue five 16 KB chunks suffice (measured
+// faster than nine at 64 and 512 requests); the one-request and residual forms
+// take what shared memory allows.
+constexpr int kRingBytesRace = 5 * 16 * 1024;
+constexpr int kRingBytesMax = 12 * 16 * 1024;
 // U slice ring (draft): slice n = 4 * tile + column block goes to slot
 // n % kUSlots; the MMA warp alone reads the slots (copying them into TMEM),
 // in fill order.
@@ -107,7 +113,8 @@ constexpr float kKhMin = 8.673617379884035e-19f;  // 2^-60
 
 struct Layout {
     uint32_t b, a, u, t, z, merge, tmerge, bar, misc, total;
-    int uslots, tslots, stages;
+    int uslots, tslots, stages, kc;
+    uint32_t stage_bytes;
 };
 
 constexpr int kSlotBytes = 128 * 128;             // one U slice: 128 rows x 32 fp32
@@ -118,8 +125,10 @@ constexpr int kSlotBytes = 128 * 128;             // one U slice: 128 rows x 32 
 // the barriers and a few words.
 __host__ __device__ inline Layout rows_layout(int NC, int r, bool resid, bool tgt = false, bool zst = false,
                                               bool one_row = false) {
-    (void)NC; (void)r;
+    (void)NC;
     Layout L;
+    L.kc = w2_kc(r, one_row);
+    L.stage_bytes = (uint32_t)(kTN * L.kc * 2);
     L.uslots = resid ? kUSlotsResid : kUSlots;
     L.tslots = tgt ? kEpiWarps : 0;                            // one target buffer and barrier per epilogue warp
     const uint32_t tmerge_bytes = tgt ? 4u * 128u * 8u : 0u;   // target fold: [4 column blocks][128 rows] float2
@@ -127,12 +136,12 @@ __host__ __device__ inline Layout rows_layout(int NC, int r, bool resid, bool tg
     const uint32_t fixed = (uint32_t)(L.uslots * kSlotBytes + L.tslots * kTBufBytes) + z_bytes + 4u * 128u * 16u +
                            tmerge_bytes + 8u * (2 * kMaxStages + 2 * L.uslots + 2 * kMaxAcc + 2 + L.tslots) + 16u +
                            12u * 128u + 1024u + 64u;
-    int st = (int)((kSmemBudget - (int)fixed) / kBBytes);
-    const int cap = (one_row || resid) ? kMaxStages : kMaxStagesRace;
+    int st = (int)((kSmemBudget - (int)fixed) / L.stage_bytes);
+    const int cap = (int)(((one_row || resid) ? kRingBytesMax : kRingBytesRace) / L.stage_bytes);
     L.stages = st > cap ? cap : st;
     L.b = 0;
     L.a = 0;
-    L.u = L.b + (uint32_t)L.stages * kBBytes;
+    L.u = L.b + (uint32_t)L.stages * L.stage_bytes;
     L.t = L.u + (uint32_t)(L.uslots * kSlotBytes);
     L.z = L.t + (uint32_t)(L.tslots * kTBufBytes);
     L.merge = L.z + z_bytes;
@@ -145,7 +154,7 @@ __host__ __device__ inline Layout rows_layout(int NC, int r, bool resid, bool tg
 }
 
 struct RowsArgs {
-    CUtensorMap w2map;   // bf16 [r][V], box {64 vocab, 64 rank}, 128-byte swizzle
+    CUtensorMap w2map;   // bf16 [r][V], box {64 vocab, kc rank}, 128-byte swizzle
     CUtensorMap umap;    // fp32 [B][gamma][V], box {32 vocab, 1, NC requests}, 128-byte swizzle
     // target stream only: fp32 [B][gamma+1][V], box {32 vocab, 1, 32 requests}
     // (one epilogue warp's rows, 128-byte swizzle)
@@ -592,7 +601,8 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     // the draft's logits leave through a per-warp staging buffer and a tensor store
     const bool zst = kQuadLoop && !kTgt && p.logits_out != nullptr;
     const Layout L = rows_layout(NC, p.r, kResid, kTgt, zst, kOneRow);
-    const int KCH = p.r / 64;
+    const int KC = L.kc, KCH = p.r / KC;
+    const uint32_t sbytes = L.stage_bytes;
     const int RF = 128 / NC;                      // vocabulary tiles per accumulator
     const int US = L.uslots;
     const uint32_t slot_bytes = (uint32_t)kSlotBytes;
@@ -660,9 +670,9 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             const int ntl = (V + kTN * RF - 1) / (kTN * RF);
             for (int t = blockIdx.x, n = 0; t < ntl && n < 2; t += GX, ++n)
                 for (int i = 0; i < RF; ++i)
-                    for (int j = 0; j < p.r / 64; ++j) {
-                        ptx::tma_prefetch_2d(&a.w2map, t * kTN * RF + i * kTN, j * 64);
-                        ptx::tma_prefetch_2d(&a.w2map, t * kTN * RF + i * kTN + 64, j * 64);
+                    for (int j = 0; j < KCH; ++j) {
+                        ptx::tma_prefetch_2d(&a.w2map, t * kTN * RF + i * kTN, j * KC);
+                        ptx::tma_prefetch_2d(&a.w2map, t * kTN * RF + i * kTN + 64, j * KC);
                     }
         }
         grid_dependency_wait();
@@ -749,11 +759,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                     for (int i = 0; i < RF && ok; ++i) {
                         for (int j = 0; j < KCH; ++j) {
                             if (!(ok = ptx::mbar_wait(empty(stage), ph ^ 1u, abort_flag, wl))) { site = 1; break; }
-                            ptx::mbar_arrive_expect_tx(full(stage), kBBytes);
-                            const uint32_t dst = base + L.b + (uint32_t)stage * kBBytes;
+                            ptx::mbar_arrive_expect_tx(full(stage), sbytes);
+                            const uint32_t dst = base + L.b + (uint32_t)stage * sbytes;
                             const int v0 = vs + i * kTN;
-                            ptx::tma_load_2d(dst, &a.w2map, v0, j * 64, full(stage), pol_w);
-                            ptx::tma_load_2d(dst + kBBytes / 2, &a.w2map, v0 + 64, j * 64, full(stage), pol_w);
+                            ptx::tma_load_2d(dst, &a.w2map, v0, j * KC, full(stage), pol_w);
+                            ptx::tma_load_2d(dst + sbytes / 2, &a.w2map, v0 + 64, j * KC, full(stage), pol_w);
                             ++nw;
                             if (++stage == kStages) { stage = 0; ph ^= 1u; }
                         }
@@ -847,14 +857,16 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         for (int j = 0; j < KCH; ++j) {
                             if (!(ok = ptx::mbar_wait(full(stage), ph, abort_flag, wl))) { site = 5; break; }
                             ptx::tc_fence_after();
-                            const uint32_t b_addr = base + L.b + (uint32_t)stage * kBBytes;
-                            // A_i in TMEM: K-chunk j = 32 columns, 16 ranks = 8 columns
-                            const uint32_t a_tmem = tmem_base + (uint32_t)(128 * i + 32 * j);
+                            const uint32_t b_addr = base + L.b + (uint32_t)stage * sbytes;
+                            // A_i in TMEM: K-chunk j = KC/2 columns, 16 ranks = 8 columns
+                            const uint32_t a_tmem = tmem_base + (uint32_t)(128 * i + (KC / 2) * j);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                // B: MN-major, 64-entry swizzle atoms 8 KB apart along N (LBO),
-                                //    8-rank groups 1 KB apart along K (SBO); 16 ranks = 2 KB.
-                                const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
+                            for (int kk = 0; kk < 8; ++kk) {
+                                if (kk == KC / 16) break;
+                                // B: MN-major, the two 64-entry swizzle atoms half a stage
+                                //    apart along N (LBO), 8-rank groups 1 KB apart along K
+                                //    (SBO); 16 ranks = 2 KB.
+                                const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, sbytes / 2, 1024);
                                 ptx::mma_f16_ts(d_tmem, a_tmem + (uint32_t)(8 * kk), bd, idesc,
                                                 (!kResid || (i | j | kk) != 0) ? 1u : 0u);
                             }
@@ -1124,11 +1136,16 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                             // so it depends on the data alone.
                             const float zm2 = fmaxf(fmaxf(us[0], us[1]), fmaxf(us[2], us[3])) * scale2;
                             if (zm2 > ref2 + 64.f) {
+                                // t_v = 2^(z2_v - ref2) shrinks by rs = 2^(ref2 - zm2), so the
+                                // sum takes rs and the keys compared against t (K2, Kh) grow by
+                                // 1 / rs (+inf past the float range: every later candidate
+                                // then beats the old winner, as it must)
                                 float rs = 0.f;
                                 if (ref2 > -INFINITY) {
                                     rs = fast_exp2(ref2 - zm2);
-                                    K2 *= rs;
-                                    Kh = fmaxf(Kh * rs, kKhMin);
+                                    const float up = fast_exp2(zm2 - ref2);
+                                    K2 *= up;
+                                    Kh = fmaxf(Kh * up, kKhMin);
                                 }
                                 ref2 = zm2;
 #pragma unroll
@@ -1575,7 +1592,7 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
     {
         const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.r};
         const cuuint64_t strides[1] = {(cuuint64_t)p.V * 2};
-        const cuuint32_t box[2] = {64, 64};
+        const cuuint32_t box[2] = {64, (cuuint32_t)w2_kc(p.r, !resid && !gru && p.B == 1)};
         const cuuint32_t es[2] = {1, 1};
         if (enc(&a.w2map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.W2), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
