@@ -2,12 +2,14 @@
 """Draft + verify throughput of the DSpark step on GB300.
 
 A step is one pass of the whole hot path over one batch of synthetic input:
-Markov-head draft loop (one cooperative launch over the gamma positions),
-confidence + STS + survival, prefix scheduler, verification stream + accept
-walk + residual draw + compaction: 7 kernel launches.  Default workload:
-B=64, V=151936, r=256, gamma=7, d=4096, bf16 draft-head weights, fp32 base
-and target logits, full-prefix verification (scheduler call made in OFF
-mode, K_b = 7).
+Markov-head draft loop (one cooperative launch over the gamma positions)
+with the verification stream (log-sum-exps of target rows 0..gamma) running
+beside it on the same SMs, confidence + STS + survival, prefix scheduler,
+accept walk, residual and bonus draws, compaction: 7 kernel launches
+(--fuse-target off: the verification stream as its own launch after the
+draft, also 7).  Default workload: B=64, V=151936, r=256, gamma=7, d=4096,
+bf16 draft-head weights, fp32 base and target logits, full-prefix
+verification (scheduler call made in OFF mode, K_b = 7).
 
 Prints one JSON line (rank 0).  `value` = emitted tokens per second over all
 ranks with inputs resident in HBM (CUDA-graph replay of the step, CUDA
@@ -15,8 +17,9 @@ events on the launching stream, inputs 1.13 GB > L2 so no flush).
 `e2e` = the same metric through the public API (HostPipeline) with every
 step's activations copied from pinned host memory and its emitted tokens
 copied back inside the timed region; the copy of step t+1 overlaps the
-compute of step t.  `roofline` = the draft kernel (the dominant one: per launch
-it streams W2 and one row block of U for each of the gamma positions).
+compute of step t.  `roofline` = the draft launch (the dominant one: per launch
+it streams W2 and one row block of U for each of the gamma positions), with
+the target rows its side stream reads when that runs beside it.
 
 With several ranks each owns B requests of a batch of B * ranks (weak
 scaling).  With the scheduler off no data crosses ranks; with it on
@@ -164,6 +167,9 @@ def run_gpu(args):
     req_base = rank * B        # each rank owns its own B requests (weak scaling)
     inp = workload.inputs(w, step=rank, device=dev)
     head = args.head
+    # scheduler off: the target stream runs beside the draft where it fits
+    # (one chunk of B <= 64 requests), else the separate verify stream
+    fuse_target = {"on": True, "off": False, "auto": vm.target_stream_beside(inp)}[args.fuse_target]
     if head == "rnn":
         inp["rnn"] = vm.rnn_prepare(workload.rnn_head(w, device=dev))
     buf = vm.StepBuffers(B, gamma, V, r, device=dev)
@@ -184,7 +190,7 @@ def run_gpu(args):
     else:
         def one_step():
             vm.run_step(inp, buf, mode=mode, seed=seed, step=0, req_base=req_base, stream=stream, head=head,
-                        fuse_target=args.fuse_target)
+                        fuse_target=fuse_target)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -242,7 +248,7 @@ def run_gpu(args):
     # ---- dominant kernel: the draft call, timed alone on the same stream (with
     #      the scheduler off the step drafts with the target stream: the call
     #      run_step makes)
-    fused = args.fuse_target and head == "markov" and mode == 0 and vm.target_stream_supported(inp)
+    fused = fuse_target and head == "markov" and mode == 0 and vm.target_stream_supported(inp)
     if head == "rnn":
         draft_launches = gamma        # one draft launch per position (plus a GRU launch each)
     else:
@@ -267,10 +273,13 @@ def run_gpu(args):
     draft_launch_ms = d0.elapsed_time(d1) / (reps * draft_launches)
     w2_bytes = r * V * inp["W2"].element_size()
     u_bytes_k = B * V * inp["U"].element_size()
-    t_bytes_k = B * V * inp["target"].element_size() if fused else 0
-    # per position: W2 once + one row block of U (and of the target); a launch
-    # covers gamma / draft_launches positions
-    draft_bytes = (w2_bytes + u_bytes_k + t_bytes_k) * gamma // draft_launches
+    # per position: W2 once + one row block of U; a launch covers gamma /
+    # draft_launches positions.  With the target stream (beside the draft,
+    # B <= 64: rows 0..gamma, the bonus row's law included; in the epilogue:
+    # rows 0..gamma-1) the launch also reads those target rows.
+    t_rows = (gamma + 1 if vm.target_stream_beside(inp) else gamma) if fused else 0
+    draft_bytes = (w2_bytes + u_bytes_k) * gamma // draft_launches + \
+        B * t_rows * V * inp["target"].element_size() // draft_launches
     peak, peak_kind = _peaks()
     achieved = draft_bytes / (draft_launch_ms / 1e3) / 1e9
     formula_bytes = gamma * w2_bytes + inp["U"].numel() * inp["U"].element_size() + \
@@ -286,14 +295,14 @@ def run_gpu(args):
     e2e_steps = max(3, min(args.steps, 20))
     pipe = vm.HostPipeline(inp, buf, stream)
     for _ in range(2):
-        pipe.step(host, host_out, mode=mode, seed=seed, head=head, fuse_target=args.fuse_target)
+        pipe.step(host, host_out, mode=mode, seed=seed, head=head, fuse_target=fuse_target)
     torch.cuda.synchronize()
     _barrier(dist)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     pipe.copy_stream.wait_event(f0)
     for _ in range(e2e_steps):
-        h2d, d2h = pipe.step(host, host_out, mode=mode, seed=seed, head=head, fuse_target=args.fuse_target)
+        h2d, d2h = pipe.step(host, host_out, mode=mode, seed=seed, head=head, fuse_target=fuse_target)
     f1.record(stream)
     stream.synchronize()
     e2e_ms = _max_over_ranks(dist, f0.elapsed_time(f1) / e2e_steps, dev)
@@ -328,7 +337,10 @@ def run_gpu(args):
             "emitted_tokens_per_step": emitted_all, "drafted_tokens_per_step": B * gamma * world,
             "step_formula_bytes": formula_bytes, "step_formula_gbs": step_gbs,
             "step_formula_frac": step_gbs / peak,
-            "roofline": {"kernel": ("rows_kernel<draft, target stream> (dspark_draft_markov_target, %d "
+            "roofline": {"kernel": ("rows_kernel<draft> + verify_stream_side_kernel beside it "
+                                    "(dspark_draft_markov_target, %d position(s) per launch)"
+                                    % (gamma // draft_launches)) if fused and vm.target_stream_beside(inp) else
+                                   ("rows_kernel<draft, target stream> (dspark_draft_markov_target, %d "
                                     "position(s) per launch)" % (gamma // draft_launches)) if fused else
                                    ("rows_kernel<draft> (dspark_draft_markov, %d position(s) per launch)"
                                     % (gamma // draft_launches)) if head == "markov" else
@@ -336,7 +348,8 @@ def run_gpu(args):
                                    "launch_ms = the two launches of one position",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": _draft_traffic(w.name) if draft_launches == 1 and head == "markov" else None,
+                         "traffic": _draft_traffic(w.name, fused) if draft_launches == 1 and head == "markov"
+                         else None,
                          "algorithmic_bytes_per_launch": draft_bytes, "launch_ms": draft_launch_ms},
             "e2e": {"value": e2e_emitted / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -588,7 +601,10 @@ def run_kernel(args):
     reads on the device (no embedding table), for profiler captures of a
     single kernel; prints the status and no metric.  draft: dspark_draft_markov;
     verify: one draft, then dspark_verify with every K_b = gamma (verify
-    stream, accept walk, residual draw, compaction)."""
+    stream, accept walk, residual draw, compaction); fused: the draft with the
+    target stream beside it (dspark_draft_markov_target); fused-verify: one
+    such draft, then dspark_verify in full-prefix mode (accept walk, residual
+    and bonus draws, compaction)."""
     import verify_markov_head_gb300 as vm
 
     dev = torch.device("cuda", 0)
@@ -611,14 +627,21 @@ def run_kernel(args):
     def draft():
         vm.dspark_draft_markov(inp["U"], inp["W1"], inp["W2"], inp["anchor"], tok, lse, zt, ws, seed=w.seed)
 
-    def verify():
-        vm.dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], tok, lse, zt, K, acc,
+    def verify(k=K):
+        vm.dspark_verify(inp["target"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], tok, lse, zt, k, acc,
                          out_tok, out_req, out_pos, out_off, nxt, ws, seed=w.seed)
 
+    def fused():
+        vm.dspark_draft_markov_target(inp["U"], inp["W1"], inp["W2"], inp["target"], inp["anchor"], tok, lse, zt,
+                                      ws, seed=w.seed)
+
+    calls = {"draft": draft, "verify": verify, "fused": fused, "fused-verify": lambda: verify(None)}
     if args.kernel == "verify":
         draft()
+    if args.kernel == "fused-verify":
+        fused()
     for _ in range(args.calls):
-        (draft if args.kernel == "draft" else verify)()
+        calls[args.kernel]()
     status, bits = vm.dspark_sync_status(ws.buf)
     print(json.dumps({"kernel_run": args.kernel, "workload": w.name, "calls": args.calls, "status": status,
                       "bits": bits}), flush=True)
@@ -628,7 +651,8 @@ def run_kernel(args):
 
 # Sources the draft kernel is compiled from: DRAM traffic taken from an ncu
 # capture is reported only while they are unchanged since the capture.
-_DRAFT_SOURCES = ("draft_rows.cu", "common.cuh", "sm100_ptx.cuh", "internal.h", "vstream.cuh")
+_DRAFT_SOURCES = ("draft_rows.cu", "verify.cu", "common.cuh", "sm100_ptx.cuh", "internal.h", "vstream.cuh",
+                  "pdl.cuh")
 
 
 def _draft_source_hash():
@@ -646,18 +670,22 @@ def _draft_source_hash():
     return h.hexdigest()[:16]
 
 
-def _draft_traffic(workload_name):
-    """dram__bytes_read.sum + dram__bytes_write.sum per draft launch from one
-    ncu capture, recorded in profiles/traffic.json beside the summaries, or
-    None when there is none or the kernel's sources changed after it was
-    taken."""
+def _draft_traffic(workload_name, fused=False):
+    """dram__bytes_read.sum + dram__bytes_write.sum per draft launch from ncu
+    captures recorded in profiles/traffic.json beside the summaries (with the
+    target stream beside the draft: the two kernels' captures added), or None
+    when one is missing or the kernels' sources changed after it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)["draft_rows"][workload_name]
-        if rec.get("source_sha256") != _draft_source_hash():
-            return None
-        return int(rec["dram_bytes_per_launch"])
+            rec = json.load(f)
+        total = 0
+        for name in (("draft_rows", "target_side") if fused else ("draft_rows",)):
+            r = rec[name][workload_name]
+            if r.get("source_sha256") != _draft_source_hash():
+                return None
+            total += int(r["dram_bytes_per_launch"])
+        return total
     except (OSError, KeyError, ValueError, TypeError):
         return None
 
@@ -848,12 +876,12 @@ def main():
                     help="time the workload's chained steps (b512: 16 steps, async scheduler) instead of one step")
     ap.add_argument("--head", default="markov", choices=["markov", "rnn"],
                     help="draft head: the Markov head (default) or the RNN head")
-    ap.add_argument("--fuse-target", action="store_true",
+    ap.add_argument("--fuse-target", default="auto", choices=["auto", "on", "off"],
                     help="scheduler off: draft with the target stream (dspark_draft_markov_target) and verify "
-                         "in full-prefix mode")
+                         "in full-prefix mode; auto takes it where the stream runs beside the draft (B <= 64)")
     ap.add_argument("--sts", action="store_true",
                     help="time the STS temperature fit (2^20 validation blocks, 256 temperatures)")
-    ap.add_argument("--kernel", default=None, choices=["draft", "verify"],
+    ap.add_argument("--kernel", default=None, choices=["draft", "verify", "fused", "fused-verify"],
                     help="run one ABI call --calls times on the workload's shapes (for profiler captures); "
                          "prints no metric")
     ap.add_argument("--calls", type=int, default=3)

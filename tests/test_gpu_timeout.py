@@ -87,6 +87,40 @@ def test_expired_waits_report_a_timeout_and_the_workspace_recovers():
         assert v["diag"][b, 0] < U_EPS, f"accept mismatch at request {b} after recovery"
 
 
+def test_expired_waits_with_the_target_stream_beside_the_draft():
+    # the draft and the lean target stream on the same SMs, then the
+    # full-prefix verify (residual and bonus draws in one kernel)
+    w = workload.custom("tiny", B=24, V=8200, r=128, w_dtype=torch.bfloat16, w_std=0.1, seed=14)
+    inp = workload.inputs(w, device=DEV)
+    assert vm.target_stream_beside(inp)
+    buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
+    seed = 6
+
+    def fused():
+        vm.dspark_draft_markov_target(inp["U"], inp["W1"], inp["W2"], inp["target"], inp["anchor"], buf.draft_tok,
+                                      buf.lse_q, buf.z_tok, buf.ws, seed=seed)
+        _verify(inp, buf, seed, None)
+
+    vm.dspark_workspace_set_wait_limit(buf.ws.buf, SHORT)
+    fused()
+    st, bits = vm.dspark_sync_status(buf.ws.buf)
+    assert st == TIMEOUT and bits & TIMEOUT_BIT, (st, hex(bits))
+
+    vm.dspark_workspace_init(buf.ws.buf)
+    fused()
+    st, bits = vm.dspark_sync_status(buf.ws.buf)
+    assert st == 0, (st, hex(bits))
+    ci = _cpu(inp)
+    tok = buf.draft_tok.cpu().numpy()
+    ref = oracle.draft_markov(ci["U"], ci["W1"], ci["W2"], ci["anchor"], seed=seed)
+    compare_draft(tok, ref["tok"], ref["gap"])
+    v = oracle.verify(ci["target"], ci["U"], ci["W1"], ci["W2"], ci["anchor"], tok, np.full(w.B, w.gamma, np.int32),
+                      seed=seed)
+    acc = buf.accepted.cpu().numpy()
+    for b in np.nonzero(acc != v["accepted"])[0]:
+        assert v["diag"][b, 0] < U_EPS, f"accept mismatch at request {b} after recovery"
+
+
 def test_default_bound_is_restored_by_zero():
     w = workload.custom("tiny", B=4, V=1024, r=64, w_dtype=torch.bfloat16, seed=2)
     inp = workload.inputs(w, device=DEV)

@@ -213,6 +213,14 @@ def target_stream_supported(inp: dict) -> bool:
             and inp["target"].dtype == torch.float32 and r % 64 == 0 and r <= 256)
 
 
+def target_stream_beside(inp: dict) -> bool:
+    """Whether dspark_draft_markov_target runs the target stream beside the
+    draft on the same SMs (one chunk of B <= 64 requests, gamma > 1): the
+    step's fastest form with the scheduler off."""
+    B, gamma = inp["U"].shape[0], inp["U"].shape[1]
+    return target_stream_supported(inp) and B <= 64 and gamma > 1
+
+
 def dspark_confidence_sts(h, emb, anchor, draft_tok, w_c, b_c, T, conf_cal, log_surv, ws: Workspace,
                           *, stream=None):
     B, gamma, d = h.shape
@@ -426,14 +434,18 @@ class StepBuffers:
 
 
 def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_base=0, log_surv_hist=None,
-         stream=None, p_tok=False, head="markov", fuse_target=False):
+         stream=None, p_tok=False, head="markov", fuse_target=None):
     """One whole draft + verify step (a1-a8) on device-resident inputs: the
     four ABI calls in order, all on `stream`.  head="rnn" drafts with the RNN
     head (parameters in inp["rnn"]) and verifies against its states.  With
     the scheduler off (every K_b = gamma) and fuse_target, the Markov draft
     also reduces the target rows it drafts against
-    (dspark_draft_markov_target) and the verify runs in full-prefix mode
-    (off by default: on one GB300 the separate verify stream is faster)."""
+    (dspark_draft_markov_target) and the verify runs in full-prefix mode.
+    fuse_target=None takes that path where the stream runs beside the draft
+    (target_stream_beside: measured 327 -> 301 us a b64 step), else the
+    separate verify stream."""
+    if fuse_target is None:
+        fuse_target = target_stream_beside(inp)
     fused = fuse_target and head == "markov" and int(mode) == 0 and target_stream_supported(inp)
     if head == "rnn":
         dspark_draft_rnn(inp["U"], inp["rnn"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,
@@ -452,8 +464,9 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
     # confidence and scheduler off the verify's critical path: with the
     # scheduler off nothing the verify reads depends on them, and a verify
     # stream too small to fill the GPU leaves SMs for them to run beside it
-    # (a full one holds every SM's registers, and they would only run later)
-    side = int(mode) == 0 and buf.verify_items < 2 * buf.sms
+    # (a full one holds every SM's registers, and they would only run later;
+    # in full-prefix mode no stream runs in the verify at all)
+    side = int(mode) == 0 and (fused or buf.verify_items < 2 * buf.sms)
     if side:
         buf.fork.record(main)
         buf.side.wait_event(buf.fork)
@@ -600,7 +613,7 @@ class HostPipeline:
         self.copy_stream.wait_stream(cur)
 
     def step(self, host_inp: dict, host_out: dict, *, mode, seed, step=0, tau=1.0, head="markov",
-             fuse_target=False):
+             fuse_target=None):
         """Enqueue one step; returns (h2d_bytes, d2h_bytes)."""
         i = self.next
         slot = self.slots[i]

@@ -48,11 +48,14 @@
 // of the target logits (the rejected rows differ per request, so no common
 // TMA box exists): D is h.W2 alone and no U slice ring is used.
 //
-// Two variants also do the first pass of a full-prefix verification (every
-// draft checked against the target, section 形式化定义), the log-sum-exps of
-// target rows 0..gamma-1: kVs runs it as a role of the launch, on 16 CTAs of
-// its own beside the draft's (the verify stream's body, vstream.cuh); kTgt
-// has the epilogue warps fold each tile's target block after their race.
+// The first pass of a full-prefix verification (every draft checked against
+// the target, section 形式化定义), the log-sum-exps of target rows
+// 0..gamma-1 and the bonus draws of row gamma, either runs beside the draft
+// or inside it.  kSide builds the plain draft for a lean stream kernel that
+// shares its SMs (verify.cu): registers capped so that both fit on an SM,
+// the largest shared-memory carve-out, and an early trigger that lets the
+// stream start once every draft CTA is resident.  kTgt has the epilogue
+// warps fold each tile's target block after their race.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -169,16 +172,15 @@ struct RowsArgs {
     uint32_t* near_ties;
     // RNN head (kRnn only): the GRU steps run in the prologue and at the position boundaries
     GruParams gru;
-    // verify-stream role (kVs only): CTAs gxd .. gridDim.x-1 run the verify
-    // stream of a full-prefix verification with these parameters
-    int gxd;
-    VerifyParams vp;
 };
 
-// Shared memory of one verify-stream instance in the stream role, 128-byte aligned.
-__host__ __device__ constexpr uint32_t vs_inst_bytes(int B) {
-    return (uint32_t)((vstream_smem_bytes(B) + 127) & ~(size_t)127);
-}
+// Registers a thread: 608 threads are 19 warps, at most 5 on each of the 4
+// schedulers, whose register files hold 16384 each: 5 x 32 x 96 fit.  The
+// draft that shares its SMs with the lean target stream keeps 88, which
+// leaves a scheduler room for a stream warp of 72 (5 x 32 x 88 + 32 x 72
+// = 16384).
+constexpr int kMaxRegs = 96;
+constexpr int kSideMaxRegs = 88;
 
 // Target stream: adds 2^(x_j * sc - m) over the entries j < n of N columns
 // of one row to its running base-2 log-sum-exp state (m, s).  The reference m
@@ -243,17 +245,19 @@ __device__ __forceinline__ void lse2_merge(float& m, float& s, const float2 e) {
 
 // The residual draw's fallback law p for request bb, whose residual
 // max(0, p - q) had no mass at all (only rounding produces that): the draw
-// from p on the rejected row urow with the residual's noise E (domain 2), by
-// the whole CTA over the row, lowest index on ties.  Kept out of line so its
+// from p on the rejected row urow with the residual's noise E (domain 2; for a
+// bonus draw, row gamma with the bonus noise, domain 3), by the whole CTA over
+// the row, lowest index on ties.  Kept out of line so its
 // registers do not weigh on the kernel's tile loop.
 template <typename TT>
-__device__ __noinline__ void resid_fallback_draw(const DraftParams& p, const void* target, int bb, int urow) {
+__device__ __noinline__ void resid_fallback_draw(const DraftParams& p, const void* target, int bb, int urow,
+                                                 uint32_t domain) {
     __shared__ float s_fkey[32];
     __shared__ int s_fidx[32];
     const int tid = (int)threadIdx.x, lane = tid % 32, warp = tid / 32, nwarps = (int)blockDim.x / 32;
     const int gamma = p.gamma, V = p.V;
     const float scale2 = p.inv_tau * 1.4426950408889634f;
-    const StreamRK rng(p.seed, p.step, 2u, (uint32_t)(p.req_base + bb) * (uint32_t)(gamma + 1) + (uint32_t)urow);
+    const StreamRK rng(p.seed, p.step, domain, (uint32_t)(p.req_base + bb) * (uint32_t)(gamma + 1) + (uint32_t)urow);
     const TT* trow = static_cast<const TT*>(target) + ((size_t)bb * (gamma + 1) + urow) * V;
     const float lse_p2 = p.ws.lse_rej[bb].x * 1.4426950408889634f;
     float key = INFINITY;
@@ -566,11 +570,11 @@ __device__ __forceinline__ void gate_step(const GruParams& g, int ks, int cta, i
 // waits on another's progress.  Nothing prefetches U or the target into L2:
 // the extra L2 footprint evicts W2, whose re-reads from HBM cost more than
 // the latency a prefetch hides.
-template <bool kResid, typename TT, bool kRnn = false, bool kOneRow = false, bool kTgt = false, bool kVs = false>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kResid, typename TT, bool kRnn = false, bool kOneRow = false, bool kTgt = false, bool kSide = false>
+__global__ void __maxnreg__(kSide ? kSideMaxRegs : kMaxRegs)
 rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_last) {
     static_assert(!(kTgt && (kResid || kRnn)), "the target stream belongs to the Markov draft");
-    static_assert(!(kVs && (kResid || kRnn || kTgt)), "the stream role belongs to the plain Markov draft");
+    static_assert(!(kSide && (kResid || kRnn || kTgt)), "the stream beside the draft belongs to the plain Markov draft");
     // the draft race reads the accumulator a quad of columns at a time
     constexpr bool kQuadLoop = !kResid && !kOneRow;
     const DraftParams& p = a.p;
@@ -580,24 +584,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    if constexpr (kVs) {
-        if ((int)blockIdx.x >= a.gxd) {
-            // verify-stream role: the walked rows' log-sum-exps (the bonus
-            // draws, a random number per entry, wait for the accept walk and
-            // its rejections); two instances of 9 warps, each with its own
-            // ring (warp 18 idles); they share the stream's work counter with
-            // the other stream CTAs and never touch the draft's state
-            const int inst = (int)threadIdx.x / kStreamThreads;
-            if (inst < 2) {
-                const uint32_t off = (uint32_t)inst * vs_inst_bytes(a.vp.B);
-                vstream_run<float, kStreamLse>(a.vp, gbase + off, base + off, (int)threadIdx.x - inst * kStreamThreads,
-                                               1 + inst, blockIdx.x == (unsigned)a.gxd && inst == 0,
-                                               2u * (gridDim.x - (unsigned)a.gxd));
-            }
-            return;
-        }
-    }
-    const int GX = kVs ? a.gxd : (int)gridDim.x;   // CTAs of the draft itself
+    const int GX = (int)gridDim.x;
     // the draft's logits leave through a per-warp staging buffer and a tensor store
     const bool zst = kQuadLoop && !kTgt && p.logits_out != nullptr;
     const Layout L = rows_layout(NC, p.r, kResid, kTgt, zst, kOneRow);
@@ -658,8 +645,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         ptx::prefetch_tmap(&a.umap);
         if constexpr (kTgt) ptx::prefetch_tmap(&a.tmap);
     }
-    if ((kTgt || kVs) && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.ws.tgt_token = p.tgt_token;
+    if (kTgt && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.ws.tgt_token = p.tgt_token;
     if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 512u); ptx::tmem_relinquish(); }
+    // the target stream launched behind this draft runs on the SMs beside it
+    if (kSide && tid == 0) grid_launch_dependents();
     // the residual draw is launched as a programmatic dependent of the accept
     // walk: its set-up above overlaps the walk's tail, and it waits here before
     // reading the rejected rows and log-normalisers the walk writes
@@ -722,10 +711,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             // W1 gathers and the first MMAs (the tile loop issues the later ones)
             const int q0 = warp & 3, cb0 = warp >> 2, row0 = 32 * q0 + lane, nr0 = row0 % NC;
             if ((32 * q0) % NC < nb) {
-                const bool real0 = nr0 < nb && s_row[nr0] >= 0;
-                const int ur = real0 ? s_row[nr0] : 0, bq = b_base + nr0;
+                const bool bon0 = p.resid_bonus && nr0 < nb && s_row[nr0] < 0;
+                const bool real0 = nr0 < nb && (s_row[nr0] >= 0 || bon0);
+                const int tr = bon0 ? gamma : (real0 ? s_row[nr0] : 0), ur = bon0 ? 0 : tr, bq = b_base + nr0;
                 const float* Ur = static_cast<const float*>(p.U) + ((size_t)bq * gamma + ur) * V;
-                const TT* Tr = static_cast<const TT*>(a.target) + ((size_t)bq * (gamma + 1) + ur) * V;
+                const TT* Tr = static_cast<const TT*>(a.target) + ((size_t)bq * (gamma + 1) + tr) * V;
                 const unsigned m0 = __ballot_sync(0xffffffffu, real0);
                 const uint32_t ub = base + L.u + (uint32_t)warp * 8192u;
                 const int v00 = (int)blockIdx.x * kTN * RF + (row0 / NC) * kTN + 32 * cb0;
@@ -892,7 +882,11 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         const int ti = row / NC, nrow = row % NC;   // vocabulary tile of the super-tile, request row
         const bool active = (32 * q) % NC < nb;     // the warp's rows hold at least one request
         const int b = b_base + nrow;
-        const bool real = active && nrow < nb && (!kResid || s_row[nrow] >= 0);
+        // residual mode: the rejected requests, and with resid_bonus the others
+        // (their bonus draw from p on row gamma, with q taken as 0 and the
+        // bonus noise, domain 3)
+        const bool bon = kResid && p.resid_bonus && active && nrow < nb && s_row[nrow] < 0;
+        const bool real = active && nrow < nb && (!kResid || s_row[nrow] >= 0 || bon);
         const float scale2 = p.inv_tau * 1.4426950408889634f;      // z -> z * log2(e)
         if constexpr (kRnn) {
             // W_hh . state[0] for the first boundary's GRU step, while the MMA
@@ -917,15 +911,17 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         if (kTgt && active && lane == 0) tgt_issue(blockIdx.x, k_first);
         if (kTgt && active) tinfl = true;
         for (int k = k_first; k <= k_last && !failed; ++k) {
-            const int urow = kResid ? (real ? s_row[nrow] : 0) : (k - 1);     // row of U (and of the target)
-            const StreamRK rng(p.seed, p.step, kResid ? 2u : 0u,
-                               (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)urow);
+            // row of the target (and of U, except for a bonus draw, which reads U row 0 and scales q to 0)
+            const int trow = kResid ? (bon ? gamma : (real ? s_row[nrow] : 0)) : (k - 1);
+            const int urow = bon ? 0 : trow;
+            const StreamRK rng(p.seed, p.step, kResid ? (bon ? 3u : 2u) : 0u,
+                               (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1) + (uint32_t)trow);
             const size_t out_row = ((size_t)b * gamma + (k - 1)) * V;
             // kOneRow: every lane works on the chunk's one request
             const StreamRK rng1(p.seed, p.step, 0u, (uint32_t)(p.req_base + b_base) * (uint32_t)(gamma + 1) + (uint32_t)(k - 1));
             const size_t out_row1 = ((size_t)b_base * gamma + (k - 1)) * V;
             const float* Urow = static_cast<const float*>(p.U) + ((size_t)b * gamma + urow) * V;
-            const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + urow) * V;
+            const TT* Trow = static_cast<const TT*>(a.target) + ((size_t)b * (gamma + 1) + trow) * V;
             float2 lse = make_float2(0.f, 0.f);
             if (kResid && real) lse = p.ws.lse_rej[b];
             const float lse_p2 = lse.x * 1.4426950408889634f, lse_q2 = lse.y * 1.4426950408889634f;
@@ -1311,7 +1307,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                         for (int c = 0; c < 4; ++c) s2 = draw2_merge(s2, m2[c * 128 + i * NC + etid]);
                     // the draw is decided by an atomic maximum over the CTAs (score,
                     // then lowest index), in the first winner-key line of the request
-                    if (s_row[etid] >= 0 && s2.best_r > -INFINITY) {
+                    if ((s_row[etid] >= 0 || p.resid_bonus) && s2.best_r > -INFINITY) {
                         DrawLse dk = drawlse_empty();
                         dk.best = s2.best_r; dk.idx = s2.idx_r;
                         atomicMax(&p.ws.win[(size_t)(b_base + etid) * kWinStride], win_key(dk));
@@ -1482,7 +1478,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
             // the next draft; a request without any residual winner draws from p
             if (sub == 0 && n < nb) {
                 s_fb[n] = 0;
-                if (s_row[n] >= 0) {
+                if (s_row[n] >= 0 || p.resid_bonus) {
                     unsigned long long* wk = &p.ws.win[(size_t)bb * kWinStride];
                     const unsigned long long key = __ldcg(wk);
                     *wk = 0ull;
@@ -1525,7 +1521,9 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         // rejected row), by the whole CTA over the row; lowest index on ties.
         __syncthreads();
         for (int nf = 0; nf < nb; ++nf)
-            if (s_fb[nf]) resid_fallback_draw<TT>(p, a.target, b_base + nf, s_row[nf]);   // uniform branch
+            if (s_fb[nf])     // uniform branch; a bonus request draws on row gamma with the bonus noise
+                resid_fallback_draw<TT>(p, a.target, b_base + nf, s_row[nf] >= 0 ? s_row[nf] : gamma,
+                                        s_row[nf] >= 0 ? 2u : 3u);
     }
     if (tid == 0) *ticket = 0u;
 }
@@ -1576,11 +1574,9 @@ bool cooperative_supported() {
     return cached[dev] == 1;
 }
 
-constexpr int kVsCtas = 16;   // CTAs of the verify-stream role (two stream instances each)
-
 static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bool resid, const void* target,
                                bool target_bf16, uint32_t* near_ties, cudaStream_t s,
-                               const GruParams* gru = nullptr, const VerifyParams* vp = nullptr) {
+                               const GruParams* gru = nullptr, bool side = false) {
     auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
     if (!enc) return cudaErrorNotSupported;
     RowsArgs a;
@@ -1611,8 +1607,7 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
     }
     // the target stream (Markov draft only): target [B][gamma+1][V] fp32, one
     // epilogue warp's block
-    const bool vs = vp != nullptr;                  // verify-stream role beside the plain draft
-    const bool tgt = !resid && !gru && !vs && p.target != nullptr;
+    const bool tgt = !resid && !gru && !side && p.target != nullptr;
     if (tgt) {
         const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)(p.gamma + 1), (cuuint64_t)p.B};
         const cuuint64_t strides[2] = {(cuuint64_t)p.V * 4, (cuuint64_t)(p.gamma + 1) * p.V * 4};
@@ -1637,28 +1632,26 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
             return cudaErrorInvalidValue;
     }
     const Layout L = rows_layout(a.NC, p.r, resid, tgt, zst, !resid && !gru && p.B == 1);
-    size_t smem = L.total + 1024;
-    if (vs) smem = smem > 1024 + 2 * (size_t)vs_inst_bytes(p.B) ? smem : 1024 + 2 * (size_t)vs_inst_bytes(p.B);
+    const size_t smem = L.total + 1024;
     auto kern = resid ? (target_bf16 ? rows_kernel<true, uint16_t> : rows_kernel<true, float>)
                 : gru ? rows_kernel<false, float, true>
                 : tgt ? (p.B == 1 ? rows_kernel<false, float, false, true, true> : rows_kernel<false, float, false, false, true>)
-                : vs ? (p.B == 1 ? rows_kernel<false, float, false, true, false, true>
-                                 : rows_kernel<false, float, false, false, false, true>)
-                      : (p.B == 1 ? rows_kernel<false, float, false, true> : rows_kernel<false, float>);
+                : side ? (p.B == 1 ? rows_kernel<false, float, false, true, false, true>
+                                   : rows_kernel<false, float, false, false, false, true>)
+                       : (p.B == 1 ? rows_kernel<false, float, false, true> : rows_kernel<false, float>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int nchunks = (p.B + a.NC - 1) / a.NC;
-    int gx = draft_rows_grid_x(p.B, p.V, p.ws.parts);
-    if (tgt && gx > kTgtSlots) return cudaErrorInvalidConfiguration;
-    int gs = 0;                                     // stream-role CTAs
-    if (vs) {
-        if (nchunks != 1 || k_last == k_first) return cudaErrorInvalidConfiguration;
-        if (gx > num_sms() - kVsCtas) gx = num_sms() - kVsCtas;
-        a.gxd = gx;
-        a.vp = *vp;
-        gs = kVsCtas;
+    // the target stream beside the draft needs the rest of the SM's shared
+    // memory: configure the largest shared-memory carve-out
+    if (side) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
     }
-    const dim3 grid(gx + gs, nchunks);
+    const int nchunks = (p.B + a.NC - 1) / a.NC;
+    const int gx = draft_rows_grid_x(p.B, p.V, p.ws.parts);
+    if (tgt && gx > kTgtSlots) return cudaErrorInvalidConfiguration;
+    if (side && (nchunks != 1 || k_last == k_first)) return cudaErrorInvalidConfiguration;
+    const dim3 grid(gx, nchunks);
     if (k_last > k_first) {
         // every CTA waits for all others between positions: they must be co-resident
         void* args[] = {&a, const_cast<int*>(&k_first), const_cast<int*>(&k_last)};
@@ -1692,22 +1685,26 @@ bool draft_target_supported(const DraftParams& p) {
     return rows_supported(p) && p.target != nullptr && draft_rows_grid_x(p.B, p.V, p.ws.parts) <= kTgtSlots;
 }
 
-// One chunk of requests (B <= 64), several positions in one cooperative
-// launch, and SMs to spare: the verify stream runs as a role of the draft
-// launch, on kVsCtas SMs of its own.
+// One chunk of requests (B <= 64) and several positions in one cooperative
+// launch: the verify stream runs beside the draft, on the same SMs.
 bool draft_target_vs(const DraftParams& p) {
-    return rows_supported(p) && p.target != nullptr && p.B <= 64 && p.gamma > 1 && cooperative_supported() &&
-           num_sms() >= 4 * kVsCtas;
+    return rows_supported(p) && p.target != nullptr && p.B <= 64 && p.gamma > 1 && cooperative_supported();
 }
 
-// The Markov draft with the target stream: with the verify-stream role when
-// draft_target_vs holds; otherwise the epilogue warps reduce the target rows
-// themselves, in one cooperative launch for the gamma positions or one
-// launch per position (the rows kernel merges a single position's partials
-// itself).
+// The Markov draft with the target stream: the lean stream kernel beside the
+// draft when draft_target_vs holds; otherwise the epilogue warps reduce the
+// target rows themselves, in one cooperative launch for the gamma positions
+// or one launch per position (the rows kernel merges a single position's
+// partials itself).
 cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s) {
     if (draft_target_vs(p)) {
+        // the plain draft, then the lean target stream on the SMs beside it
+        DraftParams q = p;
+        q.target = nullptr;
+        cudaError_t e = launch_rows(q, 1, p.gamma, false, nullptr, false, nullptr, s, nullptr, true);
+        if (e != cudaSuccess) return e;
         VerifyParams v;
+        v.vs_full = 1;                              // rows 0..gamma: the bonus row too
         v.target = p.target; v.target_bf16 = 0;
         v.U = p.U; v.U_bf16 = p.U_bf16; v.W1 = p.W1; v.W2 = p.W2; v.W_bf16 = p.W_bf16;
         v.anchor = p.anchor; v.draft_tok = p.draft_tok; v.lse_q = p.lse_q; v.z_tok = p.z_tok; v.K = nullptr;
@@ -1716,9 +1713,8 @@ cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s) {
         v.accepted = nullptr; v.out_tok = nullptr; v.out_req = nullptr; v.out_pos = nullptr;
         v.out_off = nullptr; v.next_anchor = nullptr; v.p_tok = nullptr; v.near_ties = nullptr;
         v.ws = p.ws;
-        DraftParams q = p;
-        q.target = nullptr;                         // the draft part is the plain draft (it keeps the token)
-        return launch_rows(q, 1, p.gamma, false, nullptr, false, nullptr, s, nullptr, &v);
+        v.tgt_token = p.tgt_token;
+        return launch_target_stream_side(v, s);
     }
     if (!draft_target_supported(p)) return cudaErrorNotSupported;
     if (p.gamma > 1 && cooperative_supported()) return launch_rows(p, 1, p.gamma, false, nullptr, false, nullptr, s);

@@ -110,6 +110,9 @@ struct DraftParams {
     // row k-1 ([B][gamma+1][V] fp32) to log-sum-exp partials in ws.tgt_part
     const float* target = nullptr;
     unsigned long long tgt_token = 0;
+    // residual draw (full prefix beside the draft): the requests without a
+    // rejection draw their bonus token from row gamma's law p in the same launch
+    int resid_bonus = 0;
 };
 
 // One GRU step of the RNN head for every request: state[k-1] = GRU(state[k-2]
@@ -167,9 +170,8 @@ struct VerifyParams {
     // verify stream covers only the bonus rows
     int tgt_slots = 0;
     unsigned long long tgt_token = 0;
-    // full-prefix mode after a draft that ran the verify stream in its own
-    // launch (the stream role): the walked rows' partials are already in the
-    // workspace; the bonus draws follow the accept walk
+    // full-prefix mode after a draft whose verify stream ran beside it: the
+    // walked rows' partials and the bonus tokens are already in the workspace
     int vs_full = 0;
 };
 
@@ -191,12 +193,16 @@ bool draft_rows_supported(const DraftParams& p);
 cudaError_t launch_draft_rows(const DraftParams& p, int k_first, int k_last, cudaStream_t s);
 int draft_rows_grid_x(int B, int V, int parts);   // CTAs along V of a draft rows launch
 bool draft_target_supported(const DraftParams& p);
-bool draft_target_vs(const DraftParams& p);       // the target-stream draft runs the verify stream as a role
+bool draft_target_vs(const DraftParams& p);       // the target-stream draft runs the verify stream beside it
 cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s);   // the draft with the target stream
 bool cooperative_supported();
 void* tma_encoder();   // cuTensorMapEncodeTiled from the driver, or NULL
 bool resid_rows_supported(const VerifyParams& v);
 cudaError_t launch_resid_rows(const VerifyParams& v, cudaStream_t s);
+// The walked target rows' log-sum-exps and the bonus draws by a lean stream
+// kernel that runs on the SMs beside the draft launched just before it (one
+// instance per SM).
+cudaError_t launch_target_stream_side(const VerifyParams& v, cudaStream_t s);
 
 // The draft-side view of a verify call (same U, W1, W2, tokens and workspace).
 inline DraftParams draft_view(const VerifyParams& v) {
@@ -207,6 +213,7 @@ inline DraftParams draft_view(const VerifyParams& v) {
     p.draft_tok = const_cast<int32_t*>(v.draft_tok); p.lse_q = nullptr; p.z_tok = nullptr; p.logits_out = nullptr;
     p.ws = v.ws;
     p.state = v.state;
+    p.resid_bonus = v.vs_full;
     return p;
 }
 cudaError_t launch_gumbel_stream(uint64_t seed, uint64_t step, uint32_t domain, uint32_t row, int n, float* g,

@@ -13,6 +13,10 @@ namespace dspark {
 // launched the ordinary way.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Lets the launch that depends programmatically on this grid start once every
+// CTA of this grid has issued it (or exited), instead of at the grid's end.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // Launches kern<<<grid, block, smem, s>>>(args...) with programmatic stream
 // serialisation.  The kernel must call grid_dependency_wait() before its
 // first global-memory access.

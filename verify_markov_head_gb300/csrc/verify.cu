@@ -48,6 +48,28 @@ verify_stream_kernel(const VerifyParams p) {
     vstream_run<TT, kMode>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1, blockIdx.x == 0, gridDim.x);
 }
 
+// The lean instance that runs beside the draft: 4 consumer warps and a
+// 2-stage ring (about 65 KB of shared memory, 160 threads of at most 72
+// registers), which fits next to one draft CTA on an SM.  It reduces rows
+// 0..gamma of every request (vs_full): the walked rows and the bonus row,
+// whose draw then runs in the residual kernel (a random number per entry
+// beside the draft would compete with the draft's own).  It needs nothing
+// the draft writes, so it starts without waiting on it; it waits at its end,
+// so that the launches behind it see the draft's outputs too.
+constexpr int kSideCons = 4, kSideStages = 2;
+constexpr int kSideThreads = (kSideCons + 1) * 32;
+
+template <typename TT>
+__global__ void __maxnreg__(72) verify_stream_side_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 127u) & ~127u;
+    vstream_run<TT, kStreamLse, kSideCons, kSideStages>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1,
+                                                        blockIdx.x == 0, gridDim.x);
+    if (threadIdx.x == 0 && blockIdx.x == 0) *p.ws.tgt_token = p.tgt_token;
+    grid_dependency_wait();
+}
+
 constexpr int kAcceptStaged = 2048;   // partials staged in shared memory (32 KB)
 
 // One warp per request: lse_p of the walked rows 0..K_b-1 from the partials,
@@ -86,8 +108,10 @@ verify_accept_kernel(const VerifyParams p) {
     const int ns = full ? p.tgt_slots : nsub;      // partials per walked row
     const LseDraw* rows = full ? p.ws.tgt_part + (size_t)b * gamma * kTgtSlots : parts;
     const size_t rstride = full ? (size_t)kTgtSlots : (size_t)nsub;
-    const int nparts = Kb * ns;                    // rows 0..K_b-1, staged row after row
-    if (Kb > 0 && nparts <= kAcceptStaged) {
+    // full prefix beside the draft: row K_b too (the bonus draw's law)
+    const int nrows = Kb + (p.vs_full ? 1 : 0);
+    const int nparts = nrows * ns;                 // rows 0..nrows-1, staged row after row
+    if (nrows > 0 && nparts <= kAcceptStaged) {
         // the partials of the walked rows, every load in flight, through shared
         // memory (row i from index i * ns); then lanes fold their row
         __shared__ float4 s_part[kAcceptStaged];
@@ -111,10 +135,10 @@ verify_accept_kernel(const VerifyParams p) {
         // LPR lanes per row (a power of two with K_b * LPR <= 32) fold every
         // LPR-th partial of their row, then a shuffle tree joins them
         int LPR = 32;
-        while (LPR > 1 && Kb * LPR > 32) LPR >>= 1;
+        while (LPR > 1 && nrows * LPR > 32) LPR >>= 1;
         const int row = lane / LPR, sub = lane - row * LPR;
         LseDraw a = lsedraw_empty();
-        if (row < Kb)
+        if (row < nrows)
             for (int sg = sub; sg < ns; sg += LPR) {
                 const float4 c = s_part[row * ns + sg];
                 a = lsedraw_merge(a, LseDraw{c.x, c.y, c.z, __float_as_int(c.w)});
@@ -123,7 +147,7 @@ verify_accept_kernel(const VerifyParams p) {
         const float lse_row = a.m + logf(a.s);         // on lanes row * LPR
         lse_mine = __shfl_sync(0xffffffffu, lse_row, (lane * LPR) & 31);
     } else {
-        for (int i = 0; i < Kb; ++i) {
+        for (int i = 0; i < nrows; ++i) {
             const LseDraw* part = rows + i * rstride;
             LseDraw a = lsedraw_empty();
             for (int sg = lane; sg < ns; sg += 32) a = lsedraw_merge(a, part[sg]);
@@ -144,11 +168,14 @@ verify_accept_kernel(const VerifyParams p) {
     const int rej = rej_mask ? __ffs(rej_mask) - 1 : -1;     // 0-based row of the first rejection
     if (p.near_ties && near && (rej < 0 || lane <= rej)) atomicAdd(&p.near_ties[0], 1u);   // decisions taken
     const float lse_rej = __shfl_sync(0xffffffffu, lse_mine, rej < 0 ? 0 : rej);
+    const float lse_bonus = __shfl_sync(0xffffffffu, lse_mine, Kb & 31);   // row K_b (full prefix beside the draft)
     if (lane == 0) {
         const int A = rej < 0 ? Kb : rej;
         p.ws.acc[b] = A;
         p.ws.rej[b] = rej;      // the final token: the residual draw (rej >= 0) or the bonus pass
         if (rej >= 0) p.ws.lse_rej[b] = make_float2(lse_rej, p.lse_q[(size_t)b * gamma + rej]);
+        // the bonus draw in the residual kernel: the law p of row K_b (q taken as 0)
+        else if (p.vs_full) p.ws.lse_rej[b] = make_float2(lse_bonus, INFINITY);
         p.accepted[b] = A;
     }
 }
@@ -376,12 +403,14 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     // the bytes and leaves the draws exposed, full-prefix mode has no stream
     // before the accept walk, and the stored-logits path serves small steps:
     // there the draws run after the walk, for the requests that emit them.
-    const bool deferred = p.vs_full || p.target_bf16 || p.tgt_slots > 0 || p.zlog != nullptr;
+    // Beside the draft (vs_full) the tensor-core residual kernel draws them;
+    // the stored-logits residual does not, so the pass stays there.
+    const bool deferred = p.zlog != nullptr || (!p.vs_full && (p.target_bf16 || p.tgt_slots > 0));
     const long long lse_items = (long long)p.B * p.gamma * p.ws.nseg;
     const long long bonus_items = (long long)p.B * p.ws.nseg;
     cudaError_t e0 = cudaSuccess;
     if (p.vs_full) {
-        // the draft launch ran the stream: nothing to stream here
+        // the stream ran beside the draft: nothing to stream here
     } else if (!deferred) {
         e0 = cudaFuncSetAttribute(verify_stream_kernel<TT, kStreamAll>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem1);
@@ -449,6 +478,17 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_target_stream_side(const VerifyParams& v, cudaStream_t s) {
+    const size_t smem = 128 + vstream_smem_bytes<kSideStages>(v.B);
+    cudaError_t e = cudaFuncSetAttribute(verify_stream_side_kernel<float>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(verify_stream_side_kernel<float>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(verify_stream_side_kernel<float>, dim3(num_sms()), dim3(kSideThreads), smem, s, v);
+}
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
     return p.target_bf16 ? launch_verify_t<uint16_t>(p, s) : launch_verify_t<float>(p, s);

@@ -27,8 +27,9 @@ constexpr int kStreamAll = 0, kStreamLse = 1, kStreamBonus = 2;
 
 // Shared memory of one instance: the ring, its barriers, the abort flag, the
 // stage tags and (B <= kStreamKCache) the verify lengths; 128-byte aligned.
+template <int kStages = kStreamStages>
 __host__ __device__ constexpr size_t vstream_smem_bytes(int B) {
-    return (size_t)kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16 + sizeof(int2) * kStreamStages +
+    return (size_t)kStages * kStreamStageBytes + 16 * kStages + 16 + sizeof(int2) * kStages +
            (B <= kStreamKCache ? sizeof(int) * (size_t)B : 0);
 }
 
@@ -52,37 +53,49 @@ __host__ __device__ constexpr size_t vstream_smem_bytes(int B) {
 // warp writes its own partial per item; for the bonus rows the warp that
 // completes a request's partials (an arrival ticket per request) merges them
 // and writes the request's final token.  A stage tagged -1 ends the stream.
-template <typename TT, int kMode>
+// kCons consumer warps (8, or 4 in the lean instance that runs beside the
+// draft) and a ring of kStages stages: with 4 consumers each warp takes the
+// entries of two of the 8 consumer slots of a chunk, keeps one running state
+// for both, writes the empty state to the second slot's partial and counts
+// for both slots in a bonus row's arrival ticket.
+template <typename TT, int kMode, int kCons = kStreamConsumers, int kStages = kStreamStages>
 __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbase, uint32_t base, int tid, int bar_id,
                                          bool first_instance, unsigned ninst) {
     constexpr bool kHasBonus = kMode != kStreamLse, kHasLse = kMode != kStreamBonus;
-    const uint32_t bar0 = base + kStreamStages * kStreamStageBytes;
+    static_assert(kStreamConsumers % kCons == 0, "consumer slots split evenly over the warps");
+    constexpr int kVirt = kStreamConsumers / kCons;              // consumer slots per warp
+    constexpr int kThr = (kCons + 1) * 32;                       // threads of the instance
+    const uint32_t bar0 = base + kStages * kStreamStageBytes;
     auto full = [&](int i) { return bar0 + 8u * i; };
-    auto empty = [&](int i) { return bar0 + 8u * (kStreamStages + i); };
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages);
-    int2* s_meta = reinterpret_cast<int2*>(gbase + kStreamStages * kStreamStageBytes + 16 * kStreamStages + 16);
+    auto empty = [&](int i) { return bar0 + 8u * (kStages + i); };
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + kStages * kStreamStageBytes + 16 * kStages);
+    int2* s_meta = reinterpret_cast<int2*>(gbase + kStages * kStreamStageBytes + 16 * kStages + 16);
     // the verify lengths, read once (every item needs its request's K_b; a
     // global load per item would stall the producer between items)
-    int* s_K = reinterpret_cast<int*>(s_meta + kStreamStages);
+    int* s_K = reinterpret_cast<int*>(s_meta + kStages);
     const bool k_cached = p.B <= kStreamKCache;
 
     const int gamma = p.gamma, V = p.V;
     const int nseg = p.ws.nseg;
     const long long wl = wait_limit_of(p.ws.wait_limit);   // bound of the waits on the other role
     const int nbonus = kHasBonus ? p.B * nseg : 0;           // bonus items come first
-    const int items = nbonus + (kHasLse ? p.B * gamma * nseg : 0);
+    // rows with log-sum-exp items: the walked rows, and in full-prefix mode
+    // beside the draft also row K_b = gamma (its draw runs with the residual)
+    const int lextra = p.vs_full ? 1 : 0;
+    const int lrows = gamma + lextra;
+    const int items = nbonus + (kHasLse ? p.B * lrows * nseg : 0);
     const int warp = tid / 32, lane = tid % 32;
     if (tid == 0) {
-        for (int i = 0; i < kStreamStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), kStreamConsumers); }
+        for (int i = 0; i < kStages; ++i) { ptx::mbar_init(full(i), 1); ptx::mbar_init(empty(i), kCons); }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
     if (k_cached)
-        for (int b = tid; b < p.B; b += kStreamThreads) s_K[b] = p.K ? p.K[b] : gamma;
+        for (int b = tid; b < p.B; b += kThr) s_K[b] = p.K ? p.K[b] : gamma;
     if (first_instance && p.K)
-        for (int b = tid; b < p.B; b += kStreamThreads)
+        for (int b = tid; b < p.B; b += kThr)
             if (p.K[b] < 0 || p.K[b] > gamma) raise_status(p.ws.status, kBadLength);
-    ptx::named_barrier(bar_id, kStreamThreads);
+    ptx::named_barrier(bar_id, kThr);
 
     auto clampK = [&](int b) {
         const int Kb = k_cached ? s_K[b] : (p.K ? p.K[b] : gamma);
@@ -96,15 +109,15 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
             i = clampK(b);
             return kMode != kStreamBonus || __ldcg(&p.ws.rej[b]) < 0;
         }
-        const int v = u - nbonus, per = gamma * nseg;
+        const int v = u - nbonus, per = lrows * nseg;
         b = v / per;
         const int rest = v - b * per;
         i = rest / nseg;
         seg = rest - i * nseg;
-        return i < clampK(b);
+        return i < clampK(b) + lextra;
     };
 
-    if (warp == kStreamConsumers) {
+    if (warp == kCons) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t pol = ptx::policy_evict_first();
@@ -126,7 +139,7 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
                     ptx::mbar_arrive_expect_tx(full(stage), bytes);
                     ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes, row + v0, bytes, full(stage), pol);
                     ++nf;
-                    if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
+                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
             }
@@ -139,10 +152,10 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
             if (!ok) { raise_status(p.ws.status, kTimeout); *abort_flag = 1u; }
             // every copy issued lands before the instance leaves: the last fill of
             // each stage (complete already unless the consumers gave up)
-            for (int i = 0; i < kStreamStages; ++i)
+            for (int i = 0; i < kStages; ++i)
                 if (nf > i) {
-                    const long long m = (nf - 1) - ((nf - 1 - i) % kStreamStages);
-                    ptx::mbar_wait_drain(full(i), (uint32_t)((m / kStreamStages) & 1), kStreamDrainCycles);
+                    const long long m = (nf - 1) - ((nf - 1 - i) % kStages);
+                    ptx::mbar_wait_drain(full(i), (uint32_t)((m / kStages) & 1), kStreamDrainCycles);
                 }
         }
         __syncwarp();
@@ -168,14 +181,18 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) st = lsedraw_merge(st, shfl_xor(st, m));
             LseDraw* row_part = p.ws.verify_part + ((size_t)b * (gamma + 1) + i) * nseg * kVerifySub;
-            if (lane == 0) row_part[seg * kVerifySub + warp] = st;
+            if (lane == 0) {
+                row_part[seg * kVerifySub + warp] = st;
+#pragma unroll
+                for (int h = 1; h < kVirt; ++h) row_part[seg * kVerifySub + warp + h * kCons] = lsedraw_empty();
+            }
             if (kHasBonus && bonus) {
                 // the warp that completes request b's partials merges them into its token
                 const int nsub = nseg * kVerifySub;
                 unsigned last = 0u;
                 if (lane == 0) {
                     __threadfence();
-                    last = atomicAdd(&p.ws.bonus_tickets[b], 1u) == (unsigned)(nsub - 1) ? 1u : 0u;
+                    last = atomicAdd(&p.ws.bonus_tickets[b], (unsigned)kVirt) == (unsigned)(nsub - kVirt) ? 1u : 0u;
                 }
                 if (__shfl_sync(0xffffffffu, last, 0)) {
                     __threadfence();
@@ -217,17 +234,23 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
             const int v_end = min(V, (seg + 1) * kVerifySeg);
             const int n = min(kStreamChunk, v_end - v0);
             const TT* sbuf = reinterpret_cast<const TT*>(gbase + (size_t)stage * kStreamStageBytes);
+            const int stage_now = stage;
+            if (++stage == kStages) { stage = 0; ph ^= 1u; }
+#pragma unroll 1
+            for (int h = 0; h < kVirt; ++h) {
+            const int vt = tid + h * 32 * kCons;          // the consumer slot's thread index
             float x[kPerThread];                          // raw target logits
 #pragma unroll
             for (int j = 0; j < kPerThread / 4; ++j) {
-                const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
+                const int e0 = 4 * (vt + j * 32 * kStreamConsumers);
                 const float4 x4 = (e0 < n) ? Vec4<TT>::load(sbuf + e0)
                                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                 x[4 * j] = x4.x; x[4 * j + 1] = x4.y; x[4 * j + 2] = x4.z; x[4 * j + 3] = x4.w;
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(empty(stage));     // the chunk is in registers
-            if (++stage == kStreamStages) { stage = 0; ph ^= 1u; }
+            if (h == kVirt - 1) {
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(empty(stage_now));   // the chunk is in registers
+            }
             float cm = x[0];
 #pragma unroll
             for (int e = 1; e < kPerThread; ++e) cm = fmaxf(cm, x[e]);
@@ -262,7 +285,7 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
                 int kidx = 0x7fffffff;
 #pragma unroll
                 for (int j = 0; j < kPerThread / 4; ++j) {
-                    const int e0 = 4 * (tid + j * 32 * kStreamConsumers);
+                    const int e0 = 4 * (vt + j * 32 * kStreamConsumers);
                     if (e0 < n) {
                         const int v = v0 + e0;
                         const uint4 wq = rng.quad((uint32_t)v >> 2);
@@ -279,10 +302,11 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
                     if (wins(sc, kidx, best, bidx)) { best = sc; bidx = kidx; }
                 }
             }
+            }
         }
         if (cur >= 0 && !*abort_flag) flush();
     }
-    ptx::named_barrier(bar_id, kStreamThreads);
+    ptx::named_barrier(bar_id, kThr);
     // the last instance out clears the work counter for the next launch
     if (tid == 0) {
         __threadfence();
