@@ -169,7 +169,7 @@ def run_gpu(args):
     head = args.head
     # scheduler off: the target stream runs beside the draft where it fits
     # (one chunk of B <= 64 requests), else the separate verify stream
-    fuse_target = {"on": True, "off": False, "auto": vm.target_stream_beside(inp)}[args.fuse_target]
+    fuse_target = {"on": True, "off": False, "auto": vm.target_stream_preferred(inp)}[args.fuse_target]
     if head == "rnn":
         inp["rnn"] = vm.rnn_prepare(workload.rnn_head(w, device=dev))
     buf = vm.StepBuffers(B, gamma, V, r, device=dev)
@@ -878,7 +878,7 @@ def main():
                     help="draft head: the Markov head (default) or the RNN head")
     ap.add_argument("--fuse-target", default="auto", choices=["auto", "on", "off"],
                     help="scheduler off: draft with the target stream (dspark_draft_markov_target) and verify "
-                         "in full-prefix mode; auto takes it where the stream runs beside the draft (B <= 64)")
+                         "in full-prefix mode; auto takes it where the stream beside the draft pays (B <= 256)")
     ap.add_argument("--sts", action="store_true",
                     help="time the STS temperature fit (2^20 validation blocks, 256 temperatures)")
     ap.add_argument("--kernel", default=None, choices=["draft", "verify", "fused", "fused-verify"],

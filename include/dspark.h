@@ -126,22 +126,23 @@ dspark_status dspark_draft_markov(
     void* ws, size_t ws_bytes, void* stream);
 
 /*
- * The draft of dspark_draft_markov fused with the first pass of a full-prefix
+ * The draft of dspark_draft_markov with the first pass of a full-prefix
  * verification [P2 §形式化定义] (every draft position is checked against the
- * target's distribution at that position).  The same launch reads target rows
- * 0..gamma-1 and reduces them to partial log-sum-exps of target/tau, kept in
- * ws: at B <= 64 on a few SMs of its own beside the draft, otherwise in the
- * draft's epilogue as position k streams U[b,k-1,:].  A following
- * dspark_verify or dspark_verify_logits with K = NULL uses them instead of
- * reading those rows again, and draws the bonus tokens after its accept walk.
- * Inputs : those of dspark_draft_markov, plus target [B,gamma+1,V] fp32
- *          (target_t = DSPARK_F32; row gamma, the bonus row, is not read here).
+ * target's distribution at that position) done at the same time: target rows
+ * are reduced to partial log-sum-exps of target/tau, kept in ws.  With gamma > 1
+ * and cooperative launch, a stream kernel runs beside the draft on the same
+ * SMs and reduces rows 0..gamma (the bonus row too); otherwise (fp32 target
+ * only) the draft's epilogue reduces rows 0..gamma-1 as position k streams
+ * U[b,k-1,:].  A following dspark_verify or dspark_verify_logits with K = NULL
+ * uses them instead of reading those rows again.
+ * Inputs : those of dspark_draft_markov, plus target [B,gamma+1,V] (target_t:
+ *          fp32, or bf16 where the stream runs beside the draft).
  * Outputs: those of dspark_draft_markov (identical values); ws holds the
  *          target partials and a token naming (target, seed, step, req_base,
  *          B, gamma, V, tau).  Leave the target unchanged until the verify call.
  * Limits : those of dspark_draft_markov's tensor-core path (bf16 weights, fp32
- *          U, r % 64 == 0, r <= 256); otherwise, or for a bf16 target,
- *          DSPARK_ERR_UNSUPPORTED.
+ *          U, r % 64 == 0, r <= 256); otherwise, or for a bf16 target without
+ *          the stream beside the draft, DSPARK_ERR_UNSUPPORTED.
  */
 dspark_status dspark_draft_markov_target(
     const void* U, dspark_dtype U_t,
@@ -214,10 +215,13 @@ dspark_status dspark_schedule(
  *          draft_tok, lse_q, z_tok from dspark_draft_markov, K [B] in [0,gamma].
  * K NULL : full prefix (every K_b = gamma) after dspark_draft_markov_target on
  *          the same workspace, target, seed, step, req_base and tau: the
- *          log-sum-exps of rows 0..gamma-1 come from that call, and only the
- *          bonus rows are streamed here.  A workspace whose last target-stream
- *          draft had other inputs sets status bit 3 (results unspecified).
- *          Not for dspark_verify_rnn (DSPARK_ERR_UNSUPPORTED).
+ *          log-sum-exps of the walked rows come from that call.  After the
+ *          stream beside the draft the bonus draws run with the residual
+ *          draws (dspark_verify) or in a pass after the accept walk
+ *          (dspark_verify_logits); after the epilogue form the bonus rows are
+ *          streamed here.  A workspace whose last target-stream draft had
+ *          other inputs sets status bit 3 (results unspecified).  Not for
+ *          dspark_verify_rnn (DSPARK_ERR_UNSUPPORTED).
  * Optional: p_tok [B,gamma] receives p_k(x~_k) for walked rows (others untouched);
  *          near_ties [4] (zeroed by the caller) counts: [0] acceptance
  *          uniforms within 1e-5 of their threshold, [1] residual draws that

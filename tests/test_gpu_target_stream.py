@@ -82,13 +82,17 @@ def _check_against_oracle(inp, w, buf, seed, step=0, req_base=0, tau=1.0):
     return ref
 
 
-@pytest.mark.parametrize("B,V,r", [(4, 1024, 64), (7, 4104, 64), (64, 2048, 256), (33, 8200, 128),
-                                   (130, 2056, 64), (1, 4104, 128)])
-def test_fused_draft_equals_plain_draft_and_verifies_like_the_oracle(B, V, r):
+@pytest.mark.parametrize("B,V,r,tdt", [(4, 1024, 64, torch.float32), (7, 4104, 64, torch.float32),
+                                       (64, 2048, 256, torch.float32), (33, 8200, 128, torch.float32),
+                                       (130, 2056, 64, torch.float32), (1, 4104, 128, torch.float32),
+                                       (40, 4104, 128, torch.bfloat16), (200, 2056, 64, torch.bfloat16)])
+def test_fused_draft_equals_plain_draft_and_verifies_like_the_oracle(B, V, r, tdt):
     # V = 4104, 8200, 2056: the last tile's column blocks straddle the end of the
-    # vocabulary (masked tail); B = 130: two request chunks (RF = 1); B = 1: the
-    # one-request epilogue
-    w = workload.custom("tiny", B=B, V=V, r=r, w_dtype=torch.bfloat16, w_std=0.1, seed=5 * B + r)
+    # vocabulary (masked tail); B = 130, 200: two request chunks (RF = 1); B = 1:
+    # the one-request epilogue; bf16 targets: the stream beside the draft reads
+    # half the bytes per entry
+    w = workload.custom("tiny", B=B, V=V, r=r, w_dtype=torch.bfloat16, w_std=0.1, seed=5 * B + r,
+                        target_dtype=tdt)
     inp = workload.inputs(w, device=DEV)
     seed = B + 11
     plain = _plain_draft(inp, w, seed)
@@ -204,8 +208,9 @@ def test_unsupported_inputs_are_refused():
     buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
     with pytest.raises(vm.DsparkError):          # fp32 weights: no tensor-core draft
         _fused_draft(inp, w, buf, seed=1)
-    w = workload.custom("tiny", B=4, V=1024, r=64, w_dtype=torch.bfloat16, target_dtype=torch.bfloat16, seed=2)
+    w = workload.custom("tiny", B=4, V=1024, r=64, gamma=1, w_dtype=torch.bfloat16, target_dtype=torch.bfloat16,
+                        seed=2)
     inp = workload.inputs(w, device=DEV)
     buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
-    with pytest.raises(vm.DsparkError):          # bf16 target
+    with pytest.raises(vm.DsparkError):          # bf16 target with the epilogue form (gamma = 1)
         _fused_draft(inp, w, buf, seed=1)

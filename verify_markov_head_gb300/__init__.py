@@ -187,9 +187,10 @@ def dspark_draft_markov(U, W1, W2, anchor, draft_tok, lse_q, z_tok, ws: Workspac
 
 def dspark_draft_markov_target(U, W1, W2, target, anchor, draft_tok, lse_q, z_tok, ws: Workspace, *,
                                tau=1.0, seed=0, step=0, req_base=0, logits_out=None, stream=None):
-    """dspark_draft_markov that also reduces target rows 0..gamma-1 for a
-    full-prefix verify (dspark_verify / dspark_verify_logits with K=None,
-    same workspace, target, seed, step, req_base and tau)."""
+    """dspark_draft_markov that also reduces the target rows of a full-prefix
+    verify (dspark_verify / dspark_verify_logits with K=None, same workspace,
+    target, seed, step, req_base and tau): rows 0..gamma with a stream kernel
+    beside the draft (gamma > 1), else rows 0..gamma-1 in its epilogue."""
     B, gamma, V = U.shape
     r = W1.shape[1]
     if W1.shape != (V, r) or W2.shape != (r, V) or W1.dtype != W2.dtype:
@@ -205,20 +206,33 @@ def dspark_draft_markov_target(U, W1, W2, target, anchor, draft_tok, lse_q, z_to
         ws.ptr(), ws.nbytes(), _stream(stream)))
 
 
-def target_stream_supported(inp: dict) -> bool:
-    """Whether dspark_draft_markov_target takes these inputs: bf16 weights
-    with r % 64 == 0 and r <= 256, fp32 U and an fp32 target."""
+def _target_draft_base(inp: dict) -> bool:
     r = inp["W1"].shape[1]
-    return (inp["W1"].dtype == torch.bfloat16 and inp["U"].dtype == torch.float32
-            and inp["target"].dtype == torch.float32 and r % 64 == 0 and r <= 256)
+    return (inp["W1"].dtype == torch.bfloat16 and inp["U"].dtype == torch.float32 and r % 64 == 0
+            and r <= 256 and inp["target"].dtype in (torch.float32, torch.bfloat16))
 
 
 def target_stream_beside(inp: dict) -> bool:
     """Whether dspark_draft_markov_target runs the target stream beside the
-    draft on the same SMs (one chunk of B <= 64 requests, gamma > 1): the
-    step's fastest form with the scheduler off."""
-    B, gamma = inp["U"].shape[0], inp["U"].shape[1]
-    return target_stream_supported(inp) and B <= 64 and gamma > 1
+    draft on the same SMs (gamma > 1; fp32 or bf16 target): the step's
+    fastest form with the scheduler off."""
+    return _target_draft_base(inp) and inp["U"].shape[1] > 1
+
+
+def target_stream_preferred(inp: dict) -> bool:
+    """Whether the step with the scheduler off should draft with the target
+    stream beside the draft rather than stream the target after it.  Measured
+    on one GB300 (graph replay, same outputs): b64 327 -> 301 us, b256 660 ->
+    627 us, b512 1319 -> 1325 us (its draft already moves 2 TB/s of U), so up
+    to 256 requests."""
+    return target_stream_beside(inp) and inp["U"].shape[0] <= 256
+
+
+def target_stream_supported(inp: dict) -> bool:
+    """Whether dspark_draft_markov_target takes these inputs: bf16 weights
+    with r % 64 == 0 and r <= 256, fp32 U, and a target that is fp32 (or
+    bf16 where the stream runs beside the draft)."""
+    return _target_draft_base(inp) and (inp["target"].dtype == torch.float32 or target_stream_beside(inp))
 
 
 def dspark_confidence_sts(h, emb, anchor, draft_tok, w_c, b_c, T, conf_cal, log_surv, ws: Workspace,
@@ -442,10 +456,9 @@ def run_step(inp: dict, buf: StepBuffers, *, mode, seed, step=0, tau=1.0, req_ba
     also reduces the target rows it drafts against
     (dspark_draft_markov_target) and the verify runs in full-prefix mode.
     fuse_target=None takes that path where the stream runs beside the draft
-    (target_stream_beside: measured 327 -> 301 us a b64 step), else the
-    separate verify stream."""
+    and pays (target_stream_preferred), else the separate verify stream."""
     if fuse_target is None:
-        fuse_target = target_stream_beside(inp)
+        fuse_target = target_stream_preferred(inp)
     fused = fuse_target and head == "markov" and int(mode) == 0 and target_stream_supported(inp)
     if head == "rnn":
         dspark_draft_rnn(inp["U"], inp["rnn"], inp["W2"], inp["anchor"], buf.draft_tok, buf.lse_q, buf.z_tok,

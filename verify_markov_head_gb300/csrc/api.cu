@@ -241,8 +241,9 @@ dspark_status dspark_draft_markov_target(const void* U, dspark_dtype U_t, const 
     p.draft_tok = draft_tok; p.lse_q = lse_q; p.z_tok = z_tok; p.logits_out = logits_out;
     p.ws = ws_ptrs(ws, B, gamma, V);
     p.target = static_cast<const float*>(target);
+    p.target_bf16 = (target_t == DSPARK_BF16);
     p.tgt_token = tgt_token_of(target, seed, step, req_base, B, gamma, V, tau);
-    if (target_t != DSPARK_F32 || !draft_target_supported(p)) return DSPARK_ERR_UNSUPPORTED;
+    if (!draft_target_vs(p) && (p.target_bf16 || !draft_target_supported(p))) return DSPARK_ERR_UNSUPPORTED;
     return launch_status(launch_draft_target(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -326,14 +327,16 @@ static dspark_status verify_impl(const void* target, dspark_dtype target_t, cons
     p.zlog = zlog;
     if (!K) {
         // full prefix after dspark_draft_markov_target on these inputs (the
-        // accept kernel checks the token it left): either its launch ran the
-        // verify stream as a role, or its epilogue reduced rows 0..gamma-1
+        // accept kernel checks the token it left): either the stream ran
+        // beside its draft (rows 0..gamma), or its epilogue reduced rows
+        // 0..gamma-1 (fp32 target)
         if (state) return DSPARK_ERR_UNSUPPORTED;
         DraftParams d = draft_view(p);
         d.target = static_cast<const float*>(target);
-        if (target_t == DSPARK_F32 && draft_target_vs(d)) {
+        if (draft_target_vs(d)) {
             p.vs_full = 1;
         } else {
+            if (target_t != DSPARK_F32) return DSPARK_ERR_UNSUPPORTED;
             p.tgt_slots = draft_rows_grid_x(B, V, p.ws.parts);
             if (p.tgt_slots > kTgtSlots) return DSPARK_ERR_UNSUPPORTED;
         }

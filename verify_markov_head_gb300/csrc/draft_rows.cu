@@ -1650,7 +1650,7 @@ static cudaError_t launch_rows(const DraftParams& p, int k_first, int k_last, bo
     const int nchunks = (p.B + a.NC - 1) / a.NC;
     const int gx = draft_rows_grid_x(p.B, p.V, p.ws.parts);
     if (tgt && gx > kTgtSlots) return cudaErrorInvalidConfiguration;
-    if (side && (nchunks != 1 || k_last == k_first)) return cudaErrorInvalidConfiguration;
+    if (side && (k_last == k_first || (int)(gx * nchunks) > num_sms())) return cudaErrorInvalidConfiguration;
     const dim3 grid(gx, nchunks);
     if (k_last > k_first) {
         // every CTA waits for all others between positions: they must be co-resident
@@ -1685,10 +1685,12 @@ bool draft_target_supported(const DraftParams& p) {
     return rows_supported(p) && p.target != nullptr && draft_rows_grid_x(p.B, p.V, p.ws.parts) <= kTgtSlots;
 }
 
-// One chunk of requests (B <= 64) and several positions in one cooperative
-// launch: the verify stream runs beside the draft, on the same SMs.
+// Several positions in one cooperative launch (one draft CTA per SM): the
+// verify stream runs beside the draft, on the same SMs.
 bool draft_target_vs(const DraftParams& p) {
-    return rows_supported(p) && p.target != nullptr && p.B <= 64 && p.gamma > 1 && cooperative_supported();
+    return rows_supported(p) && p.target != nullptr && p.gamma > 1 && cooperative_supported() &&
+           draft_rows_grid_x(p.B, p.V, p.ws.parts) * ((p.B + (p.B <= 64 ? 64 : 128) - 1) / (p.B <= 64 ? 64 : 128)) <=
+               num_sms();
 }
 
 // The Markov draft with the target stream: the lean stream kernel beside the
@@ -1705,7 +1707,7 @@ cudaError_t launch_draft_target(const DraftParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         VerifyParams v;
         v.vs_full = 1;                              // rows 0..gamma: the bonus row too
-        v.target = p.target; v.target_bf16 = 0;
+        v.target = p.target; v.target_bf16 = p.target_bf16;
         v.U = p.U; v.U_bf16 = p.U_bf16; v.W1 = p.W1; v.W2 = p.W2; v.W_bf16 = p.W_bf16;
         v.anchor = p.anchor; v.draft_tok = p.draft_tok; v.lse_q = p.lse_q; v.z_tok = p.z_tok; v.K = nullptr;
         v.B = p.B; v.gamma = p.gamma; v.V = p.V; v.r = p.r; v.req_base = p.req_base;

@@ -109,6 +109,7 @@ struct DraftParams {
     // target stream (full-prefix verification): position k also reduces target
     // row k-1 ([B][gamma+1][V] fp32) to log-sum-exp partials in ws.tgt_part
     const float* target = nullptr;
+    int target_bf16 = 0;                // the target beside the draft may be bf16
     unsigned long long tgt_token = 0;
     // residual draw (full prefix beside the draft): the requests without a
     // rejection draw their bonus token from row gamma's law p in the same launch

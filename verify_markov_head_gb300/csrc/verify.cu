@@ -479,15 +479,20 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_target_stream_side(const VerifyParams& v, cudaStream_t s) {
+template <typename TT>
+static cudaError_t launch_side_t(const VerifyParams& v, cudaStream_t s) {
     const size_t smem = 128 + vstream_smem_bytes<kSideStages>(v.B);
-    cudaError_t e = cudaFuncSetAttribute(verify_stream_side_kernel<float>,
+    cudaError_t e = cudaFuncSetAttribute(verify_stream_side_kernel<TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(verify_stream_side_kernel<float>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(verify_stream_side_kernel<TT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    return launch_dependent(verify_stream_side_kernel<float>, dim3(num_sms()), dim3(kSideThreads), smem, s, v);
+    return launch_dependent(verify_stream_side_kernel<TT>, dim3(num_sms()), dim3(kSideThreads), smem, s, v);
+}
+
+cudaError_t launch_target_stream_side(const VerifyParams& v, cudaStream_t s) {
+    return v.target_bf16 ? launch_side_t<uint16_t>(v, s) : launch_side_t<float>(v, s);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
