@@ -249,10 +249,9 @@ def run_gpu(args):
     #      the scheduler off the step drafts with the target stream: the call
     #      run_step makes)
     fused = fuse_target and head == "markov" and mode == 0 and vm.target_stream_supported(inp)
-    if head == "rnn":
-        draft_launches = gamma        # one draft launch per position (plus a GRU launch each)
-    else:
-        draft_launches = 1            # one cooperative launch covers the gamma positions
+    # one cooperative launch covers the gamma positions (the RNN head runs its
+    # GRU steps inside it)
+    draft_launches = 1
     reps = max(5, min(args.steps, 1000))
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -314,7 +313,7 @@ def run_gpu(args):
 
     # draft, confidence, schedule, verify stream (bonus rows only when fused), accept walk,
     # residual draw, compaction
-    launches_per_step = draft_launches * (2 if head == "rnn" else 1) + 6
+    launches_per_step = draft_launches + 6
     cpu = None
     ties = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -344,8 +343,8 @@ def run_gpu(args):
                                     "position(s) per launch)" % (gamma // draft_launches)) if fused else
                                    ("rows_kernel<draft> (dspark_draft_markov, %d position(s) per launch)"
                                     % (gamma // draft_launches)) if head == "markov" else
-                                   "gru_kernel + rows_kernel<draft> per position (dspark_draft_rnn); "
-                                   "launch_ms = the two launches of one position",
+                                   ("rows_kernel<draft, RNN head> (dspark_draft_rnn, %d position(s) per "
+                                    "launch, the GRU steps inside)" % (gamma // draft_launches)),
                          "bound": "hbm", "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak,
                          "traffic": _draft_traffic(w.name, fused) if draft_launches == 1 and head == "markov"
