@@ -155,6 +155,58 @@ def _barrier(dist):
         dist.barrier()
 
 
+def _quick_steps(vm, dev):
+    """Extra records beside the headline: the step of the latency case (b1),
+    of b256 and of b64 with its scheduler on (the stepped capacity table,
+    synchronous mode), each by CUDA-graph replay of device-resident inputs
+    for at least 0.3 s."""
+    out = {}
+    for label, name, sched in (("b1", "b1", False), ("b256", "b256", False), ("b64_scheduled", "b64", True)):
+        w = workload.WORKLOADS[name]
+        mode = w.mode if sched else 0
+        inp = workload.inputs(w, device=dev)
+        buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r, device=dev)
+        stream = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize(dev)
+
+        def one():
+            vm.run_step(inp, buf, mode=mode, seed=w.seed, step=0, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                one()
+        stream.synchronize()
+        st, bits = vm.dspark_sync_status(buf.ws.buf, stream)
+        if st != 0:
+            raise SystemExit(f"{label}: device status {st} bits {bits}")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            one()
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                g.replay()
+        stream.synchronize()
+        n, t = 0, 0.0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        while t < 300.0:
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(50):
+                    g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            t += e0.elapsed_time(e1)
+            n += 50
+        emitted = int(buf.out_off[-1].item())
+        ms = t / n
+        out[label] = {"ms_per_step": ms, "tokens_per_s": emitted / (ms / 1e3), "emitted_tokens_per_step": emitted,
+                      "steps": n, "workload": f"B={w.B} V={w.V} r={w.r} gamma={w.gamma}, "
+                      + (f"scheduler mode {mode} ({w.sps_fn.__name__} capacity table)" if sched else "scheduler off")}
+        del inp, buf, g
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import verify_markov_head_gb300 as vm
 
@@ -316,6 +368,9 @@ def run_gpu(args):
     launches_per_step = draft_launches + 6
     cpu = None
     ties = None
+    extra = None
+    if rank == 0 and world == 1 and w.name == "b64" and head == "markov" and mode == 0 and not args.no_extras:
+        extra = _quick_steps(vm, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, mode, budget_s=args.cpu_budget, dev_inp=inp, min_seconds=10.0, head=head)
         if _LAST_SAMPLE and head == "markov" and mode == 0:
@@ -356,6 +411,7 @@ def run_gpu(args):
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "near_ties": ties,
+            "extra_steps": extra,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -871,6 +927,8 @@ def main():
                     help="off: full-prefix verification; spec: the workload's scheduler mode")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the extra step records (b1, b256, b64 with its scheduler) of the default line")
     ap.add_argument("--chain", action="store_true",
                     help="time the workload's chained steps (b512: 16 steps, async scheduler) instead of one step")
     ap.add_argument("--head", default="markov", choices=["markov", "rnn"],

@@ -6,10 +6,19 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace dspark {
+
+// One NVTX range per ABI call (named after the call), for timeline tools; a
+// push and a pop of a few nanoseconds when no tool is attached.
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+};
 
 int num_sms() {
     static int cached[64] = {0};
@@ -188,6 +197,7 @@ dspark_status dspark_draft_markov(const void* U, dspark_dtype U_t, const void* W
                                   int r, int req_base, float tau, uint64_t seed, uint64_t step,
                                   int32_t* draft_tok, float* lse_q, float* z_tok, float* logits_out,
                                   void* ws, size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
     if ((U_t != DSPARK_F32 && U_t != DSPARK_BF16) || (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
         return DSPARK_ERR_UNSUPPORTED;
@@ -217,6 +227,7 @@ dspark_status dspark_draft_markov_target(const void* U, dspark_dtype U_t, const 
                                          const int32_t* anchor, int B, int gamma, int V, int r, int req_base,
                                          float tau, uint64_t seed, uint64_t step, int32_t* draft_tok, float* lse_q,
                                          float* z_tok, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
     if ((U_t != DSPARK_F32 && U_t != DSPARK_BF16) || (W_t != DSPARK_F32 && W_t != DSPARK_BF16) ||
         (target_t != DSPARK_F32 && target_t != DSPARK_BF16))
@@ -251,6 +262,7 @@ dspark_status dspark_confidence_sts(const float* h, int d, const void* emb, dspa
                                     const int32_t* anchor, const int32_t* draft_tok, const float* w_c,
                                     float b_c, const float* T, int B, int gamma, int V, float* conf_cal,
                                     float* log_surv, void* ws, size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     if (B < 1 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || d < 1 || e < 1 || V < 1) return DSPARK_ERR_INVALID;
     if (emb_t != DSPARK_F32 && emb_t != DSPARK_BF16) return DSPARK_ERR_UNSUPPORTED;
     if (!is_device_ptr(h) || !is_device_ptr(emb) || !is_device_ptr(anchor) || !is_device_ptr(draft_tok) ||
@@ -273,6 +285,7 @@ dspark_status dspark_confidence_sts(const float* h, int d, const void* emb, dspa
 dspark_status dspark_schedule(const float* log_surv, const float* log_surv_hist, const float* sps,
                               int sps_len, int B, int gamma, dspark_sched_mode mode, int32_t* K,
                               int32_t* n_total, float* theta, void* ws, size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     (void)ws; (void)ws_bytes;
     if (B < 1 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || B * gamma > DSPARK_MAX_SCHED_ITEMS)
         return DSPARK_ERR_INVALID;
@@ -354,6 +367,7 @@ dspark_status dspark_verify(const void* target, dspark_dtype target_t, const voi
                             uint64_t seed, uint64_t step, int32_t* accepted, int32_t* out_tok,
                             int32_t* out_req, int32_t* out_pos, int32_t* out_off, int32_t* next_anchor,
                             float* p_tok, uint32_t* near_ties, void* ws, size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     return verify_impl(target, target_t, U, U_t, W1, nullptr, nullptr, W2, W_t, anchor, draft_tok, lse_q, z_tok, K, B,
                        gamma, V, r, req_base, tau, seed, step, accepted, out_tok, out_req, out_pos, out_off,
                        next_anchor, p_tok, near_ties, ws, ws_bytes, stream);
@@ -367,6 +381,7 @@ dspark_status dspark_verify_logits(const void* target, dspark_dtype target_t, co
                                    int32_t* out_tok, int32_t* out_req, int32_t* out_pos, int32_t* out_off,
                                    int32_t* next_anchor, float* p_tok, uint32_t* near_ties, void* ws,
                                    size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     if (!draft_logits) return DSPARK_ERR_INVALID;
     return verify_impl(target, target_t, U, U_t, W1, nullptr, draft_logits, W2, W_t, anchor, draft_tok, lse_q,
                        z_tok, K, B, gamma, V, r, req_base, tau, seed, step, accepted, out_tok, out_req, out_pos,
@@ -380,6 +395,7 @@ dspark_status dspark_verify_rnn(const void* target, dspark_dtype target_t, const
                                 uint64_t seed, uint64_t step, int32_t* accepted, int32_t* out_tok,
                                 int32_t* out_req, int32_t* out_pos, int32_t* out_off, int32_t* next_anchor,
                                 float* p_tok, uint32_t* near_ties, void* ws, size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     if (!state) return DSPARK_ERR_INVALID;
     return verify_impl(target, target_t, U, U_t, nullptr, state, nullptr, W2, W_t, anchor, draft_tok, lse_q, z_tok, K, B,
                        gamma, V, r, req_base, tau, seed, step, accepted, out_tok, out_req, out_pos, out_off,
@@ -388,6 +404,7 @@ dspark_status dspark_verify_rnn(const void* target, dspark_dtype target_t, const
 
 dspark_status dspark_rnn_input_table(const void* E, const void* W_ih, const float* b_ih, int V, int r, float* P,
                                      void* stream) {
+    const dspark::CallRange range_(__func__);
     if (V < 1 || r < 1 || r > 1024 || (r % 8) != 0) return DSPARK_ERR_INVALID;
     if (!is_device_ptr(E) || !is_device_ptr(W_ih) || !is_device_ptr(b_ih) || !is_device_ptr(P))
         return DSPARK_ERR_INVALID;
@@ -400,6 +417,7 @@ dspark_status dspark_draft_rnn(const void* U, dspark_dtype U_t, const float* P, 
                                int gamma, int V, int r, int req_base, float tau, uint64_t seed, uint64_t step,
                                int32_t* draft_tok, float* lse_q, float* z_tok, float* state, void* ws,
                                size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     if (!sizes_ok(B, gamma, V, r) || !(tau > 0.f) || req_base < 0) return DSPARK_ERR_INVALID;
     if ((U_t != DSPARK_F32 && U_t != DSPARK_BF16) || (W_t != DSPARK_F32 && W_t != DSPARK_BF16))
         return DSPARK_ERR_UNSUPPORTED;
@@ -459,6 +477,7 @@ size_t dspark_sts_workspace_bytes(int gamma, int G, int M) {
 dspark_status dspark_sts_fit(const float* score, const int32_t* acc_len, int N, int gamma, const float* grid,
                              int G, int M, float* T_out, int32_t* idx_out, double* ece_out, void* ws,
                              size_t ws_bytes, void* stream) {
+    const dspark::CallRange range_(__func__);
     if (N < 1 || dspark_sts_workspace_bytes(gamma, G, M) == 0) return DSPARK_ERR_INVALID;
     if (!is_device_ptr(score) || !is_device_ptr(acc_len) || !is_device_ptr(grid) || !is_device_ptr(T_out) ||
         !is_device_ptr(idx_out) || !is_device_ptr(ece_out) || !is_device_ptr(ws))
