@@ -647,8 +647,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     }
     if (kTgt && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.ws.tgt_token = p.tgt_token;
     if (warp == kMmaWarp) { ptx::tmem_alloc(base + L.misc, 512u); ptx::tmem_relinquish(); }
-    // the target stream launched behind this draft runs on the SMs beside it
-    if (kSide && tid == 0) grid_launch_dependents();
+    // the target stream launched behind this draft runs on the SMs beside it;
+    // the launch behind the residual draw (compaction) is scheduled early and
+    // waits for it
+    if ((kSide || kResid) && tid == 0) grid_launch_dependents();
     // the residual draw is launched as a programmatic dependent of the accept
     // walk: its set-up above overlaps the walk's tail, and it waits here before
     // reading the rejected rows and log-normalisers the walk writes

@@ -64,6 +64,9 @@ __global__ void __maxnreg__(72) verify_stream_side_kernel(const VerifyParams p) 
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
+    // the launch behind this one (the accept walk) is scheduled now and
+    // waits for this grid, so its launch latency hides under the draft
+    if (threadIdx.x == 0) grid_launch_dependents();
     vstream_run<TT, kStreamLse, kSideCons, kSideStages>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1,
                                                         blockIdx.x == 0, gridDim.x);
     if (threadIdx.x == 0 && blockIdx.x == 0) *p.ws.tgt_token = p.tgt_token;
@@ -80,6 +83,9 @@ constexpr int kAcceptStaged = 2048;   // partials staged in shared memory (32 KB
 template <typename TT>
 __global__ void __launch_bounds__(32)
 verify_accept_kernel(const VerifyParams p) {
+    // the residual launch behind this one starts its set-up (TMEM, barriers,
+    // the W2 prefetch) during the walk; it waits for the walk before reading
+    if (threadIdx.x == 0) grid_launch_dependents();
     grid_dependency_wait();
     const int b = blockIdx.x, lane = threadIdx.x;
     const int gamma = p.gamma, V = p.V, nseg = p.ws.nseg;
