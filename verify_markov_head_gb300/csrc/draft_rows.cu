@@ -655,11 +655,13 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     // walk: its set-up above overlaps the walk's tail, and it waits here before
     // reading the rejected rows and log-normalisers the walk writes
     if constexpr (kResid) {
-        // W2 does not depend on the walk: the CTA's first two super-tiles of it
-        // go to L2 before the wait
+        // W2 does not depend on the walk: the CTA's first super-tile of it goes
+        // to L2 before the wait (two measured slower at b64, 297.0 against
+        // 292.7 us a step: the launch starts during the walk, whose loads they
+        // delay)
         if (tid == kProducerWarp * 32) {
             const int ntl = (V + kTN * RF - 1) / (kTN * RF);
-            for (int t = blockIdx.x, n = 0; t < ntl && n < 2; t += GX, ++n)
+            for (int t = blockIdx.x, n = 0; t < ntl && n < 1; t += GX, ++n)
                 for (int i = 0; i < RF; ++i)
                     for (int j = 0; j < KCH; ++j) {
                         ptx::tma_prefetch_2d(&a.w2map, t * kTN * RF + i * kTN, j * KC);
