@@ -144,6 +144,27 @@ def test_temperature_request_base_and_stored_logits():
     _check_against_oracle(inp, w, buf, seed=4, step=3, req_base=500, tau=0.7)
 
 
+@pytest.mark.parametrize("tdt", [torch.float32, torch.bfloat16])
+def test_stream_beside_the_draft_short_chain_temperature_request_base(tdt):
+    """gamma = 2 (the shortest chain the stream beside the draft takes), a
+    temperature, a request base and a vocabulary whose last segment is short;
+    the residual launch also draws the bonus tokens (full-prefix dspark_verify)."""
+    w = workload.custom("tiny", B=24, V=33800, r=128, gamma=2, w_dtype=torch.bfloat16, w_std=0.1, seed=31,
+                        target_dtype=tdt)
+    inp = workload.inputs(w, device=DEV)
+    assert vm.target_stream_beside(inp)
+    buf = vm.StepBuffers(w.B, w.gamma, w.V, w.r)
+    _fused_draft(inp, w, buf, seed=7, step=5, req_base=100, tau=0.8)
+    _full_verify(inp, buf, seed=7, step=5, req_base=100, tau=0.8)
+    st, bits = vm.dspark_sync_status(buf.ws.buf)
+    assert st == 0, bits
+    ci = _cpu(inp)
+    d = oracle.draft_markov(ci["U"], ci["W1"], ci["W2"], ci["anchor"], seed=7, step=5, tau=0.8,
+                            req=np.arange(100, 100 + w.B))
+    compare_draft(buf.draft_tok.cpu().numpy(), d["tok"], d["gap"])
+    _check_against_oracle(inp, w, buf, seed=7, step=5, req_base=100, tau=0.8)
+
+
 def test_single_position_target_stream():
     """gamma = 1 runs the target-stream draft as one single-position launch
     (the epilogue form, the launch every position uses where cooperative
