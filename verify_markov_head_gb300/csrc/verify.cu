@@ -48,18 +48,19 @@ verify_stream_kernel(const VerifyParams p) {
     vstream_run<TT, kMode>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1, blockIdx.x == 0, gridDim.x);
 }
 
-// The lean instance that runs beside the draft: 4 consumer warps and a
-// 2-stage ring (about 65 KB of shared memory, 160 threads of at most 72
-// registers), which fits next to one draft CTA on an SM.  It reduces rows
+// The lean instance that runs beside the draft: 4 consumer warps (2 for one
+// chunk of several requests, 1 < B <= 64, whose stream is short: at half the
+// rate it disturbs the draft less) and a 2-stage ring (about 65 KB of shared memory,
+// at most 160 threads of at most 72 registers), which fits next to one draft
+// CTA on an SM.  It reduces rows
 // 0..gamma of every request (vs_full): the walked rows and the bonus row,
 // whose draw then runs in the residual kernel (a random number per entry
 // beside the draft would compete with the draft's own).  It needs nothing
 // the draft writes, so it starts without waiting on it; it waits at its end,
 // so that the launches behind it see the draft's outputs too.
-constexpr int kSideCons = 4, kSideStages = 2;
-constexpr int kSideThreads = (kSideCons + 1) * 32;
+constexpr int kSideStages = 2;
 
-template <typename TT>
+template <typename TT, int kCons>
 __global__ void __maxnreg__(72) verify_stream_side_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -67,8 +68,8 @@ __global__ void __maxnreg__(72) verify_stream_side_kernel(const VerifyParams p) 
     // the launch behind this one (the accept walk) is scheduled now and
     // waits for this grid, so its launch latency hides under the draft
     if (threadIdx.x == 0) grid_launch_dependents();
-    vstream_run<TT, kStreamLse, kSideCons, kSideStages>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1,
-                                                        blockIdx.x == 0, gridDim.x);
+    vstream_run<TT, kStreamLse, kCons, kSideStages>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1,
+                                                    blockIdx.x == 0, gridDim.x);
     if (threadIdx.x == 0 && blockIdx.x == 0) *p.ws.tgt_token = p.tgt_token;
     grid_dependency_wait();
 }
@@ -485,20 +486,24 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
 
 }  // namespace
 
-template <typename TT>
+template <typename TT, int kCons>
 static cudaError_t launch_side_t(const VerifyParams& v, cudaStream_t s) {
     const size_t smem = 128 + vstream_smem_bytes<kSideStages>(v.B);
-    cudaError_t e = cudaFuncSetAttribute(verify_stream_side_kernel<TT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = verify_stream_side_kernel<TT, kCons>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(verify_stream_side_kernel<TT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    return launch_dependent(verify_stream_side_kernel<TT>, dim3(num_sms()), dim3(kSideThreads), smem, s, v);
+    return launch_dependent(kern, dim3(num_sms()), dim3((kCons + 1) * 32), smem, s, v);
 }
 
+// Measured (graph-replay steps, same outputs): two consumer warps at b64
+// (296.6 -> 294.7 us), four at b256 (653.5 with two against 627.6 us) and at
+// b1, whose draft leaves no room beside it, so the stream runs after it
+// (142.8 against 145.5 us with two).
 cudaError_t launch_target_stream_side(const VerifyParams& v, cudaStream_t s) {
-    return v.target_bf16 ? launch_side_t<uint16_t>(v, s) : launch_side_t<float>(v, s);
+    if (v.B > 1 && v.B <= 64) return v.target_bf16 ? launch_side_t<uint16_t, 2>(v, s) : launch_side_t<float, 2>(v, s);
+    return v.target_bf16 ? launch_side_t<uint16_t, 4>(v, s) : launch_side_t<float, 4>(v, s);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
