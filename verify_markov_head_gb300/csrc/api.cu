@@ -54,6 +54,8 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.conf = o;        o = align256(o + sizeof(uint32_t) * (size_t)B + sizeof(float) * (size_t)B * gamma);
     L.rnn_gh = o;      o = align256(o + sizeof(float) * (size_t)B * 3 * kMaxRnnRank);
     L.bonus_tickets = o; o = align256(o + sizeof(uint32_t) * (size_t)B);
+    L.row_lse = o;     o = align256(o + sizeof(float) * (size_t)B * (gamma + 1));
+    L.row_tickets = o; o = align256(o + sizeof(uint32_t) * (size_t)B * (gamma + 1));
     L.total = o;
     return L;
 }
@@ -82,6 +84,8 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     P.conf_score = reinterpret_cast<float*>(base + L.conf + sizeof(uint32_t) * (size_t)B);
     P.rnn_gh = reinterpret_cast<float*>(base + L.rnn_gh);
     P.bonus_tickets = reinterpret_cast<uint32_t*>(base + L.bonus_tickets);
+    P.row_lse = reinterpret_cast<float*>(base + L.row_lse);
+    P.row_tickets = reinterpret_cast<uint32_t*>(base + L.row_tickets);
     P.nseg = L.nseg;
     P.parts = L.parts;
     return P;

@@ -53,7 +53,7 @@ constexpr WsDraftPrefix ws_draft_prefix(int B, int gamma, int parts) {
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
     size_t status, tickets, gbar, win, vq, draft_part, verify_part, tgt_part, tgt_token, rej, acc, fin, lse_rej,
-        resid_part, conf, rnn_gh, bonus_tickets, total;
+        resid_part, conf, rnn_gh, bonus_tickets, row_lse, row_tickets, total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -81,6 +81,10 @@ struct WsPtrs {
     float* conf_score;       // [B][gamma]
     float* rnn_gh;           // [B][3 kMaxRnnRank] RNN head scratch
     uint32_t* bonus_tickets; // [B] bonus-draw arrival counters, zero between launches
+    // the stream beside the draft: each row's log-sum-exp, merged by the warp
+    // that writes the row's last partial (arrival counters zero between launches)
+    float* row_lse;          // [B][gamma+1]
+    uint32_t* row_tickets;   // [B][gamma+1]
     int nseg;
     int parts;
 };
@@ -204,6 +208,10 @@ cudaError_t launch_resid_rows(const VerifyParams& v, cudaStream_t s);
 // kernel that runs on the SMs beside the draft launched just before it (one
 // instance per SM).
 cudaError_t launch_target_stream_side(const VerifyParams& v, cudaStream_t s);
+
+// Whether the stream beside the draft also merges each row's partials into
+// ws.row_lse (one chunk of requests), which the accept walk then reads.
+__host__ __device__ inline bool vs_row_merge(const VerifyParams& v) { return v.vs_full && v.B <= 64; }
 
 // The draft-side view of a verify call (same U, W1, W2, tokens and workspace).
 inline DraftParams draft_view(const VerifyParams& v) {

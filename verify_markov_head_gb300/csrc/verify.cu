@@ -118,7 +118,10 @@ verify_accept_kernel(const VerifyParams p) {
     // full prefix beside the draft: row K_b too (the bonus draw's law)
     const int nrows = Kb + (p.vs_full ? 1 : 0);
     const int nparts = nrows * ns;                 // rows 0..nrows-1, staged row after row
-    if (nrows > 0 && nparts <= kAcceptStaged) {
+    if (vs_row_merge(p)) {
+        // the stream beside the draft merged every row already
+        if (lane < nrows) lse_mine = __ldcg(&p.ws.row_lse[(size_t)b * (gamma + 1) + lane]);
+    } else if (nrows > 0 && nparts <= kAcceptStaged) {
         // the partials of the walked rows, every load in flight, through shared
         // memory (row i from index i * ns); then lanes fold their row
         __shared__ float4 s_part[kAcceptStaged];

@@ -82,6 +82,7 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
     // rows with log-sum-exp items: the walked rows, and in full-prefix mode
     // beside the draft also row K_b = gamma (its draw runs with the residual)
     const int lextra = p.vs_full ? 1 : 0;
+    const bool row_merge = vs_row_merge(p);
     const int lrows = gamma + lextra;
     const int items = nbonus + (kHasLse ? p.B * lrows * nseg : 0);
     const int warp = tid / 32, lane = tid % 32;
@@ -185,6 +186,34 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
                 row_part[seg * kVerifySub + warp] = st;
 #pragma unroll
                 for (int h = 1; h < kVirt; ++h) row_part[seg * kVerifySub + warp + h * kCons] = lsedraw_empty();
+            }
+            if (kHasLse && !bonus && row_merge) {
+                // beside the draft of one chunk of requests the stream has time to
+                // spare: the warp that writes a row's last partial (an arrival
+                // ticket per row) merges them into the row's log-sum-exp, so the
+                // accept walk reads one value per row (above 64 requests the
+                // longer stream has no such slack: b256 measured 630 -> 652 us)
+                const int nsub = nseg * kVerifySub;
+                uint32_t* tk = &p.ws.row_tickets[(size_t)b * (gamma + 1) + i];
+                unsigned last = 0u;
+                if (lane == 0) {
+                    __threadfence();
+                    last = atomicAdd(tk, (unsigned)kVirt) == (unsigned)(nsub - kVirt) ? 1u : 0u;
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence();
+                    LseDraw a = lsedraw_empty();
+                    for (int sg = lane; sg < nsub; sg += 32) {
+                        const float4 c = __ldcg(reinterpret_cast<const float4*>(row_part) + sg);
+                        a = lsedraw_merge(a, LseDraw{c.x, c.y, c.z, __float_as_int(c.w)});
+                    }
+#pragma unroll
+                    for (int m = 1; m < 32; m <<= 1) a = lsedraw_merge(a, shfl_xor(a, m));
+                    if (lane == 0) {
+                        p.ws.row_lse[(size_t)b * (gamma + 1) + i] = a.m + logf(a.s);
+                        *tk = 0u;                        // zero again for the next launch
+                    }
+                }
             }
             if (kHasBonus && bonus) {
                 // the warp that completes request b's partials merges them into its token
