@@ -56,6 +56,7 @@ WsLayout ws_layout(int B, int gamma, int V) {
     L.bonus_tickets = o; o = align256(o + sizeof(uint32_t) * (size_t)B);
     L.row_lse = o;     o = align256(o + sizeof(float) * (size_t)B * (gamma + 1));
     L.row_tickets = o; o = align256(o + sizeof(uint32_t) * (size_t)B * (gamma + 1));
+    L.rtok = o;        o = align256(o + sizeof(int32_t) * (size_t)B);
     L.total = o;
     return L;
 }
@@ -86,6 +87,7 @@ WsPtrs ws_ptrs(void* ws, int B, int gamma, int V) {
     P.bonus_tickets = reinterpret_cast<uint32_t*>(base + L.bonus_tickets);
     P.row_lse = reinterpret_cast<float*>(base + L.row_lse);
     P.row_tickets = reinterpret_cast<uint32_t*>(base + L.row_tickets);
+    P.rtok = reinterpret_cast<int32_t*>(base + L.rtok);
     P.nseg = L.nseg;
     P.parts = L.parts;
     return P;

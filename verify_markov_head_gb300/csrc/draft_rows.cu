@@ -675,8 +675,10 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         if (n < nb) {
             const int b = b_base + n;
             if constexpr (kResid) {
+                // both written by the accept walk: no load waits on another
                 prow = __ldcg(&p.ws.rej[b]);
-                if (prow >= 0) x = (prow == 0) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (prow - 1)];
+                x = __ldcg(&p.ws.rtok[b]);
+                if (prow < 0) x = -1;
             } else {
                 x = (k_first == 1) ? p.anchor[b] : p.draft_tok[(size_t)b * gamma + (k_first - 2)];
             }

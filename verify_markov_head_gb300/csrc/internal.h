@@ -53,7 +53,7 @@ constexpr WsDraftPrefix ws_draft_prefix(int B, int gamma, int parts) {
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
     size_t status, tickets, gbar, win, vq, draft_part, verify_part, tgt_part, tgt_token, rej, acc, fin, lse_rej,
-        resid_part, conf, rnn_gh, bonus_tickets, row_lse, row_tickets, total;
+        resid_part, conf, rnn_gh, bonus_tickets, row_lse, row_tickets, rtok, total;
     int nseg;    // verify-stream segments per row
     int parts;   // partial-state slots per request (>= CTAs along V of any launch)
 };
@@ -85,6 +85,9 @@ struct WsPtrs {
     // that writes the row's last partial (arrival counters zero between launches)
     float* row_lse;          // [B][gamma+1]
     uint32_t* row_tickets;   // [B][gamma+1]
+    // [B] the token before the rejected draft (the anchor when the first is
+    // rejected; -1 when none is): its W1 row is the residual draw's A row
+    int32_t* rtok;
     int nseg;
     int parts;
 };

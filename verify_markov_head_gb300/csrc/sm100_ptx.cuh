@@ -174,6 +174,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// Start the 128-byte lines that hold [p, p + bytes) towards L2: a hint that
+// nothing waits for, with no alignment rule.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    const uint64_t a = reinterpret_cast<uint64_t>(p);
+    for (uint64_t l = a & ~(uint64_t)127; l < a + bytes; l += 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(l));
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

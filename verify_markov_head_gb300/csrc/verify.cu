@@ -98,16 +98,25 @@ verify_accept_kernel(const VerifyParams p) {
     const TT* target = static_cast<const TT*>(p.target);
     const uint32_t row0 = (uint32_t)(p.req_base + b) * (uint32_t)(gamma + 1);
     // per-lane draft data for position k = lane + 1 (issued before the merges)
-    int x = 0;
+    int x = 0, x_raw = -1;
     float t = 0.f, lq = 0.f, u = 1.f;
     const bool walk = lane < Kb;
+    // the token before draft k+1, whose W1 row the residual draw gathers if
+    // draft k+1 is rejected: lane k holds draft k, lane 31 the anchor
+    if (lane == 31 && Kb > 0) x_raw = p.anchor[b];
     if (walk) {
         const size_t o = (size_t)b * gamma + lane;
-        x = p.draft_tok[o];
+        x = x_raw = p.draft_tok[o];
         if (x < 0 || x >= V) { raise_status(p.ws.status, kBadToken); x = 0; }
         t = load_scalar(target, ((size_t)b * (gamma + 1) + lane) * V + x) * p.inv_tau;
         lq = p.z_tok[o] - p.lse_q[o];
         u = uniform_of(Stream(p.seed, p.step, 1u, row0 + (uint32_t)lane).word(0));
+    }
+    // every row the residual may gather, on its way to L2 during the walk
+    // (the stored-logits residual and the RNN head read no W1 row)
+    if (!p.zlog && !p.state && (lane == 31 || lane + 1 < Kb) && x_raw >= 0 && x_raw < V) {
+        const size_t rb = (size_t)p.r * (p.W_bf16 ? 2 : 4);
+        ptx::prefetch_l2(static_cast<const char*>(p.W1) + (size_t)x_raw * rb, (uint32_t)rb);
     }
     float lse_mine = 0.f;        // lse_p of row `lane` (walked rows 0..K_b-1)
     const int nsub = nseg * kVerifySub;            // verify-stream partials per row
@@ -179,10 +188,12 @@ verify_accept_kernel(const VerifyParams p) {
     if (p.near_ties && near && (rej < 0 || lane <= rej)) atomicAdd(&p.near_ties[0], 1u);   // decisions taken
     const float lse_rej = __shfl_sync(0xffffffffu, lse_mine, rej < 0 ? 0 : rej);
     const float lse_bonus = __shfl_sync(0xffffffffu, lse_mine, Kb & 31);   // row K_b (full prefix beside the draft)
+    const int x_prev = __shfl_sync(0xffffffffu, x_raw, rej <= 0 ? 31 : rej - 1);
     if (lane == 0) {
         const int A = rej < 0 ? Kb : rej;
         p.ws.acc[b] = A;
         p.ws.rej[b] = rej;      // the final token: the residual draw (rej >= 0) or the bonus pass
+        p.ws.rtok[b] = rej < 0 ? -1 : x_prev;
         if (rej >= 0) p.ws.lse_rej[b] = make_float2(lse_rej, p.lse_q[(size_t)b * gamma + rej]);
         // the bonus draw in the residual kernel: the law p of row K_b (q taken as 0)
         else if (p.vs_full) p.ws.lse_rej[b] = make_float2(lse_bonus, INFINITY);
