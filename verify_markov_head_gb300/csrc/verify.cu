@@ -68,7 +68,7 @@ __global__ void __maxnreg__(72) verify_stream_side_kernel(const VerifyParams p) 
     // the launch behind this one (the accept walk) is scheduled now and
     // waits for this grid, so its launch latency hides under the draft
     if (threadIdx.x == 0) grid_launch_dependents();
-    vstream_run<TT, kStreamLse, kCons, kSideStages>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1,
+    vstream_run<TT, kStreamLse, kCons, kSideStages, kSidePiece>(p, smem_raw + (base - raw), base, (int)threadIdx.x, 1,
                                                     blockIdx.x == 0, gridDim.x);
     if (threadIdx.x == 0 && blockIdx.x == 0) *p.ws.tgt_token = p.tgt_token;
     grid_dependency_wait();

@@ -18,6 +18,12 @@ constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;  // + one producer w
 constexpr int kStreamStages = 3;
 constexpr int kStreamChunk = 8192;                           // entries per bulk copy
 constexpr int kStreamStageBytes = kStreamChunk * 4;          // fp32 chunk (bf16 uses half)
+// Beside the draft, whose W2 and U tiles go through the same SM's bulk-copy
+// engine, a chunk is copied in pieces of this many bytes: one 32 KB copy held
+// the draft's copies back longer than four of 8 KB (b64 step 293.2 -> 290.2
+// us, b256 635.7 -> 622.9 us; 4 KB pieces were slower again).  The standalone
+// stream keeps one copy a chunk (b512 with pieces: 1322.9 -> 1330.6 us).
+constexpr uint32_t kSidePiece = 8192;
 constexpr int kPerThread = kStreamChunk / (32 * kStreamConsumers);   // 32 entries per consumer per chunk
 constexpr long long kStreamDrainCycles = 200000000LL;        // ~0.1 s: bulk copies already issued landing
 constexpr float kLog2e = 1.4426950408889634f;
@@ -58,7 +64,8 @@ __host__ __device__ constexpr size_t vstream_smem_bytes(int B) {
 // entries of two of the 8 consumer slots of a chunk, keeps one running state
 // for both, writes the empty state to the second slot's partial and counts
 // for both slots in a bonus row's arrival ticket.
-template <typename TT, int kMode, int kCons = kStreamConsumers, int kStages = kStreamStages>
+template <typename TT, int kMode, int kCons = kStreamConsumers, int kStages = kStreamStages,
+          uint32_t kPiece = (uint32_t)kStreamStageBytes>
 __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbase, uint32_t base, int tid, int bar_id,
                                          bool first_instance, unsigned ninst) {
     constexpr bool kHasBonus = kMode != kStreamLse, kHasLse = kMode != kStreamBonus;
@@ -138,7 +145,10 @@ __device__ __forceinline__ void vstream_run(const VerifyParams& p, uint8_t* gbas
                     s_meta[stage] = make_int2(u, v0);
                     const uint32_t bytes = (uint32_t)(min(kStreamChunk, v_end - v0) * (int)sizeof(TT));
                     ptx::mbar_arrive_expect_tx(full(stage), bytes);
-                    ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes, row + v0, bytes, full(stage), pol);
+                    for (uint32_t o = 0; o < bytes; o += kPiece)
+                        ptx::bulk_load(base + (uint32_t)stage * kStreamStageBytes + o,
+                                       reinterpret_cast<const char*>(row + v0) + o, min(kPiece, bytes - o),
+                                       full(stage), pol);
                     ++nf;
                     if (++stage == kStages) { stage = 0; ph ^= 1u; }
                 }
