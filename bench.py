@@ -659,14 +659,15 @@ def run_kernel(args):
     stream, accept walk, residual draw, compaction); fused: the draft with the
     target stream beside it (dspark_draft_markov_target); fused-verify: one
     such draft, then dspark_verify in full-prefix mode (accept walk, residual
-    and bonus draws, compaction)."""
+    and bonus draws, compaction); confidence: one draft, then
+    dspark_confidence_sts (this mode also holds the embedding table)."""
     import verify_markov_head_gb300 as vm
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     w = workload.WORKLOADS[args.workload]
     B, gamma, V, r = w.B, w.gamma, w.V, w.r
-    inp = workload.draft_weights(w, device=dev)
+    inp = (workload.weights if args.kernel == "confidence" else workload.draft_weights)(w, device=dev)
     st = workload.step_inputs(w, device=dev)
     inp.update(U=st["U"], target=st["target"], anchor=st["anchor"])
     ws = vm.Workspace(B, gamma, V, r, dev)
@@ -690,8 +691,14 @@ def run_kernel(args):
         vm.dspark_draft_markov_target(inp["U"], inp["W1"], inp["W2"], inp["target"], inp["anchor"], tok, lse, zt,
                                       ws, seed=w.seed)
 
-    calls = {"draft": draft, "verify": verify, "fused": fused, "fused-verify": lambda: verify(None)}
-    if args.kernel == "verify":
+    def confidence():
+        vm.dspark_confidence_sts(st["h"], inp["emb"], inp["anchor"], tok, inp["w_c"], inp["b_c"], inp["T"], conf,
+                                 surv, ws)
+
+    conf, surv = torch.empty((B, gamma), device=dev), torch.empty((B, gamma), device=dev)
+    calls = {"draft": draft, "verify": verify, "fused": fused, "fused-verify": lambda: verify(None),
+             "confidence": confidence}
+    if args.kernel in ("verify", "confidence"):
         draft()
     if args.kernel == "fused-verify":
         fused()
@@ -938,7 +945,7 @@ def main():
                          "in full-prefix mode; auto takes it where the stream beside the draft pays (B <= 256)")
     ap.add_argument("--sts", action="store_true",
                     help="time the STS temperature fit (2^20 validation blocks, 256 temperatures)")
-    ap.add_argument("--kernel", default=None, choices=["draft", "verify", "fused", "fused-verify"],
+    ap.add_argument("--kernel", default=None, choices=["draft", "verify", "fused", "fused-verify", "confidence"],
                     help="run one ABI call --calls times on the workload's shapes (for profiler captures); "
                          "prints no metric")
     ap.add_argument("--calls", type=int, default=3)
