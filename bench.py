@@ -714,7 +714,7 @@ def run_kernel(args):
 # Sources the draft kernel is compiled from: DRAM traffic taken from an ncu
 # capture is reported only while they are unchanged since the capture.
 _DRAFT_SOURCES = ("draft_rows.cu", "verify.cu", "common.cuh", "sm100_ptx.cuh", "internal.h", "vstream.cuh",
-                  "pdl.cuh")
+                  "pdl.cuh", "resid_tail.cuh")
 
 
 def _draft_source_hash():

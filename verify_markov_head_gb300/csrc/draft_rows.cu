@@ -63,6 +63,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "pdl.cuh"
+#include "resid_tail.cuh"
 #include "sm100_ptx.cuh"
 #include "vstream.cuh"
 
@@ -243,50 +244,6 @@ __device__ __forceinline__ void lse2_merge(float& m, float& s, const float2 e) {
     else s += e.y * fast_exp2(e.x - m);
 }
 
-// The residual draw's fallback law p for request bb, whose residual
-// max(0, p - q) had no mass at all (only rounding produces that): the draw
-// from p on the rejected row urow with the residual's noise E (domain 2; for a
-// bonus draw, row gamma with the bonus noise, domain 3), by the whole CTA over
-// the row, lowest index on ties.  Kept out of line so its
-// registers do not weigh on the kernel's tile loop.
-template <typename TT>
-__device__ __noinline__ void resid_fallback_draw(const DraftParams& p, const void* target, int bb, int urow,
-                                                 uint32_t domain) {
-    __shared__ float s_fkey[32];
-    __shared__ int s_fidx[32];
-    const int tid = (int)threadIdx.x, lane = tid % 32, warp = tid / 32, nwarps = (int)blockDim.x / 32;
-    const int gamma = p.gamma, V = p.V;
-    const float scale2 = p.inv_tau * 1.4426950408889634f;
-    const StreamRK rng(p.seed, p.step, domain, (uint32_t)(p.req_base + bb) * (uint32_t)(gamma + 1) + (uint32_t)urow);
-    const TT* trow = static_cast<const TT*>(target) + ((size_t)bb * (gamma + 1) + urow) * V;
-    const float lse_p2 = p.ws.lse_rej[bb].x * 1.4426950408889634f;
-    float key = INFINITY;
-    int idx = 0x7fffffff;
-    for (int qd = tid; qd < V / 4; qd += (int)blockDim.x) {
-        const uint4 w = rng.quad((uint32_t)qd);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float pv = fast_exp2(fmaf(to_f32(trow[4 * qd + e]), scale2, -lse_p2));
-            const float E = exp2_variate_of(ws[e]) * kLn2;
-            if (pv > 0.f && E < key * pv) { key = E / pv; idx = 4 * qd + e; }
-        }
-    }
-#pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, key, sh);
-        const int oi = __shfl_xor_sync(0xffffffffu, idx, sh);
-        if (ok < key || (ok == key && oi < idx)) { key = ok; idx = oi; }
-    }
-    if (lane == 0) { s_fkey[warp] = key; s_fidx[warp] = idx; }
-    __syncthreads();
-    if (tid == 0) {
-        for (int w2 = 1; w2 < nwarps; ++w2)
-            if (s_fkey[w2] < key || (s_fkey[w2] == key && s_fidx[w2] < idx)) { key = s_fkey[w2]; idx = s_fidx[w2]; }
-        p.ws.fin[bb] = idx;
-    }
-    __syncthreads();
-}
 
 // Bounded grid-wide barrier on a counter in global memory: every CTA adds 1,
 // then waits until all `target` CTAs have.  The kernel is launched
@@ -386,9 +343,6 @@ __device__ __forceinline__ unsigned long long win_key(const DrawLse& d) {
     const uint32_t bits = __float_as_uint(d.best == 0.f ? 0.f : d.best);
     const uint32_t ord = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
     return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)d.idx);
-}
-__device__ __forceinline__ int win_token(unsigned long long key) {
-    return (int)(0xFFFFFFFFu - (uint32_t)key);
 }
 
 // One warp stages a 32-entry segment [v0, v0 + 32) of 32 rows (one per lane,
@@ -1457,10 +1411,13 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
         return;
     }
 
+    // residual draw: every CTA has folded its draws into the winner keys; the
+    // compaction launch behind this one decodes them (and draws the fallback
+    // law where a request found no residual mass)
+    if constexpr (kResid) return;
     // single position: the last-arriving CTA of this request chunk merges the partial states
-    uint32_t* ticket = kResid ? &p.ws.tickets_resid[chunk] : &p.ws.tickets_draft[chunk];
+    uint32_t* ticket = &p.ws.tickets_draft[chunk];
     __shared__ int s_last;
-    __shared__ int s_fb[128];                        // residual mode: request needs the fallback draw
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -1479,24 +1436,7 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
     constexpr int kBatch = 5;
     if (tid < 32 * kEpiWarps) {
         const int bb = b_base + n;
-        if constexpr (kResid) {
-            // the winner keys hold the draws: decode them and clear the lines for
-            // the next draft; a request without any residual winner draws from p
-            if (sub == 0 && n < nb) {
-                s_fb[n] = 0;
-                if (s_row[n] >= 0 || p.resid_bonus) {
-                    unsigned long long* wk = &p.ws.win[(size_t)bb * kWinStride];
-                    const unsigned long long key = __ldcg(wk);
-                    *wk = 0ull;
-                    if (key != 0ull) {
-                        p.ws.fin[bb] = win_token(key);
-                    } else {
-                        s_fb[n] = 1;                     // no residual mass: draw from p below
-                        if (a.near_ties) atomicAdd(&a.near_ties[1], 1u);
-                    }
-                }
-            }
-        } else {
+        {
             DrawLse m = drawlse_empty();
             if (n < nb) {
                 const float4* part = reinterpret_cast<const float4*>(
@@ -1520,16 +1460,6 @@ rows_kernel(const __grid_constant__ RowsArgs a, const int k_first, const int k_l
                 p.z_tok[o] = m.zb;
             }
         }
-    }
-    if constexpr (kResid) {
-        // The fallback law p for the requests whose residual r = max(0, p - q)
-        // had no mass at all: the draw from p with the same E (domain 2, the
-        // rejected row), by the whole CTA over the row; lowest index on ties.
-        __syncthreads();
-        for (int nf = 0; nf < nb; ++nf)
-            if (s_fb[nf])     // uniform branch; a bonus request draws on row gamma with the bonus noise
-                resid_fallback_draw<TT>(p, a.target, b_base + nf, s_row[nf] >= 0 ? s_row[nf] : gamma,
-                                        s_row[nf] >= 0 ? 2u : 3u);
     }
     if (tid == 0) *ticket = 0u;
 }

@@ -181,6 +181,9 @@ struct VerifyParams {
     // full-prefix mode after a draft whose verify stream ran beside it: the
     // walked rows' partials and the bonus tokens are already in the workspace
     int vs_full = 0;
+    // the tensor-core residual launch left its draws as winner keys: the
+    // compaction decodes them (set by the verify launcher)
+    int resid_keys = 0;
 };
 
 struct StsFitParams {

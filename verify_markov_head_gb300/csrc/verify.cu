@@ -30,6 +30,7 @@
 #include "sm100_ptx.cuh"
 #include "vstream.cuh"
 #include "pdl.cuh"
+#include "resid_tail.cuh"
 
 namespace dspark {
 namespace {
@@ -358,15 +359,52 @@ verify_residual_simt_kernel(const VerifyParams p) {
 // ----------------------------------------------------------------- compaction
 constexpr int kCompactThreads = 1024;
 
+// After the tensor-core residual launch (p.resid_keys) the final tokens of
+// the requests it drew (every rejected one, and with the stream beside the
+// draft the bonus draws too) are still winner keys: they are decoded here
+// first, the keys cleared for the next draft, and a request whose residual
+// had no mass at all draws from p itself (the fallback law).
+template <typename TT>
 __global__ void __launch_bounds__(kCompactThreads)
 verify_compact_kernel(const VerifyParams p) {
     __shared__ int s_warp[kCompactThreads / 32];
     __shared__ int s_carry;
+    __shared__ int s_nfb;
+    __shared__ int s_fb[kCompactThreads];
     grid_dependency_wait();
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int gamma = p.gamma;
     if (tid == 0) s_carry = 0;
     __syncthreads();
+    if (p.resid_keys) {
+        for (int base = 0; base < p.B; base += kCompactThreads) {
+            const int b = base + tid;
+            if (tid == 0) s_nfb = 0;
+            __syncthreads();
+            if (b < p.B) {
+                const int rej = __ldcg(&p.ws.rej[b]);
+                if (rej >= 0 || p.vs_full) {
+                    unsigned long long* wk = &p.ws.win[(size_t)b * kWinStride];
+                    const unsigned long long key = __ldcg(wk);
+                    *wk = 0ull;
+                    if (key != 0ull) {
+                        p.ws.fin[b] = win_token(key);
+                    } else {
+                        s_fb[atomicAdd(&s_nfb, 1)] = b;   // no residual mass: draw from p below
+                        if (p.near_ties) atomicAdd(&p.near_ties[1], 1u);
+                    }
+                }
+            }
+            __syncthreads();
+            for (int f = 0; f < s_nfb; ++f) {       // uniform loop; a bonus request draws on row gamma
+                const int bb = s_fb[f];
+                const int rej = __ldcg(&p.ws.rej[bb]);
+                resid_fallback_draw<TT>(p.seed, p.step, p.req_base, gamma, p.V, p.inv_tau, p.ws.lse_rej[bb].x,
+                                        p.target, bb, rej >= 0 ? rej : gamma, rej >= 0 ? 2u : 3u, &p.ws.fin[bb]);
+            }
+            __syncthreads();
+        }
+    }
     for (int base = 0; base < p.B; base += kCompactThreads) {
         const int b = base + tid;
         const int A = (b < p.B) ? p.ws.acc[b] : 0;
@@ -460,7 +498,7 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
                                  dim3(kStreamThreads), smem1, s, p);
             if (e != cudaSuccess) return e;
         }
-        const cudaError_t e = launch_dependent(verify_compact_kernel, dim3(1), dim3(kCompactThreads), 0, s, p);
+        const cudaError_t e = launch_dependent(verify_compact_kernel<TT>, dim3(1), dim3(kCompactThreads), 0, s, p);
         return e != cudaSuccess ? e : cudaGetLastError();
     };
     const int nchunks = (p.B + kBC - 1) / kBC;
@@ -481,7 +519,18 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     if (p.state || resid_rows_supported(p)) {
         const cudaError_t e = launch_resid_rows(p, s);
         if (e != cudaSuccess) return e;
-        return finish();
+        VerifyParams pk = p;
+        pk.resid_keys = 1;                       // the residual's draws are winner keys
+        if (deferred) {
+            cudaError_t e2 = cudaFuncSetAttribute(verify_stream_kernel<TT, kStreamBonus>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+            if (e2 != cudaSuccess) return e2;
+            e2 = launch_dependent(verify_stream_kernel<TT, kStreamBonus>, dim3(stream_grid(bonus_items)),
+                                  dim3(kStreamThreads), smem1, s, p);
+            if (e2 != cudaSuccess) return e2;
+        }
+        const cudaError_t e3 = launch_dependent(verify_compact_kernel<TT>, dim3(1), dim3(kCompactThreads), 0, s, pk);
+        return e3 != cudaSuccess ? e3 : cudaGetLastError();
     }
 #define DSPARK_RES_LAUNCH(WT, UT)                                                                    \
     do {                                                                                             \
