@@ -375,40 +375,49 @@ verify_compact_kernel(const VerifyParams p) {
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int gamma = p.gamma;
     if (tid == 0) s_carry = 0;
-    __syncthreads();
-    if (p.resid_keys) {
-        for (int base = 0; base < p.B; base += kCompactThreads) {
-            const int b = base + tid;
-            if (tid == 0) s_nfb = 0;
-            __syncthreads();
-            if (b < p.B) {
-                const int rej = __ldcg(&p.ws.rej[b]);
-                if (rej >= 0 || p.vs_full) {
-                    unsigned long long* wk = &p.ws.win[(size_t)b * kWinStride];
-                    const unsigned long long key = __ldcg(wk);
-                    *wk = 0ull;
-                    if (key != 0ull) {
-                        p.ws.fin[b] = win_token(key);
-                    } else {
-                        s_fb[atomicAdd(&s_nfb, 1)] = b;   // no residual mass: draw from p below
-                        if (p.near_ties) atomicAdd(&p.near_ties[1], 1u);
-                    }
-                }
-            }
-            __syncthreads();
-            for (int f = 0; f < s_nfb; ++f) {       // uniform loop; a bonus request draws on row gamma
-                const int bb = s_fb[f];
-                const int rej = __ldcg(&p.ws.rej[bb]);
-                resid_fallback_draw<TT>(p.seed, p.step, p.req_base, gamma, p.V, p.inv_tau, p.ws.lse_rej[bb].x,
-                                        p.target, bb, rej >= 0 ? rej : gamma, rej >= 0 ? 2u : 3u, &p.ws.fin[bb]);
-            }
-            __syncthreads();
-        }
-    }
     for (int base = 0; base < p.B; base += kCompactThreads) {
         const int b = base + tid;
-        const int A = (b < p.B) ? p.ws.acc[b] : 0;
-        const int len = (b < p.B) ? A + 1 : 0;
+        const bool in = b < p.B;
+        if (tid == 0) s_nfb = 0;
+        // every load of request b at once: its accepted count, its final token
+        // or winner key, and its drafts
+        int A = 0, rej = -1, fin = 0;
+        unsigned long long key = 0ull;
+        int tk[DSPARK_MAX_GAMMA];
+        if (in) {
+            A = __ldcg(&p.ws.acc[b]);
+            fin = __ldcg(&p.ws.fin[b]);
+            if (p.resid_keys) {
+                rej = __ldcg(&p.ws.rej[b]);
+                key = __ldcg(&p.ws.win[(size_t)b * kWinStride]);
+            }
+#pragma unroll
+            for (int i = 0; i < DSPARK_MAX_GAMMA; ++i)
+                if (i < gamma) tk[i] = __ldcg(&p.draft_tok[(size_t)b * gamma + i]);
+        }
+        __syncthreads();
+        bool fb = false;
+        if (in && p.resid_keys && (rej >= 0 || p.vs_full)) {
+            p.ws.win[(size_t)b * kWinStride] = 0ull;   // cleared for the next draft
+            if (key != 0ull) {
+                fin = win_token(key);
+                p.ws.fin[b] = fin;
+            } else {
+                fb = true;                              // no residual mass: draw from p below
+                s_fb[atomicAdd(&s_nfb, 1)] = b;
+                if (p.near_ties) atomicAdd(&p.near_ties[1], 1u);
+            }
+        }
+        __syncthreads();
+        for (int f = 0; f < s_nfb; ++f) {           // uniform loop; a bonus request draws on row gamma
+            const int bb = s_fb[f];
+            const int rb = __ldcg(&p.ws.rej[bb]);
+            resid_fallback_draw<TT>(p.seed, p.step, p.req_base, gamma, p.V, p.inv_tau, p.ws.lse_rej[bb].x,
+                                    p.target, bb, rb >= 0 ? rb : gamma, rb >= 0 ? 2u : 3u, &p.ws.fin[bb]);
+        }
+        if (fb) fin = __ldcg(&p.ws.fin[b]);          // written by this CTA before the draw's barrier
+        // offsets: an exclusive prefix sum of A + 1 over the requests
+        const int len = in ? A + 1 : 0;
         int incl = len;
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
@@ -428,13 +437,14 @@ verify_compact_kernel(const VerifyParams p) {
         }
         __syncthreads();
         const int off = s_carry + (warp ? s_warp[warp - 1] : 0) + incl - len;
-        if (b < p.B) {
-            const int fin = p.ws.fin[b];
-            for (int i = 0; i < A; ++i) {
-                p.out_tok[off + i] = p.draft_tok[(size_t)b * gamma + i];
-                p.out_req[off + i] = b;
-                p.out_pos[off + i] = i;
-            }
+        if (in) {
+#pragma unroll
+            for (int i = 0; i < DSPARK_MAX_GAMMA; ++i)
+                if (i < A) {
+                    p.out_tok[off + i] = tk[i];
+                    p.out_req[off + i] = b;
+                    p.out_pos[off + i] = i;
+                }
             p.out_tok[off + A] = fin;
             p.out_req[off + A] = b;
             p.out_pos[off + A] = A;
