@@ -223,7 +223,8 @@ def target_stream_preferred(inp: dict) -> bool:
     """Whether the step with the scheduler off should draft with the target
     stream beside the draft rather than stream the target after it.  Measured
     on one GB300 (graph replay, same outputs): b64 327 -> 301 us, b256 660 ->
-    627 us, b512 1319 -> 1325 us (its draft already moves 2 TB/s of U), so up
+    627 us, b512 1319 -> 1325 us (its draft already moves 2 TB/s of U); again
+    on the current kernels b256 651 -> 631 us and b512 1316 -> 1331 us, so up
     to 256 requests."""
     return target_stream_beside(inp) and inp["U"].shape[0] <= 256
 
