@@ -43,10 +43,12 @@
 // ("DSpark：半自回归生成与置信度调度的投机解码" section 形式化定义): for every
 // request whose walk rejected draft j, h = W1[x~_{j-1}] and the epilogue forms
 // q = softmax(z_j) and p = softmax(t_j / tau) from the passed log-normalisers,
-// then draws argmax_v log(max(0, p - q)) + G (domain 2), with the draw from p
-// kept for the case p <= q everywhere.  Each thread reads its own row of U and
-// of the target logits (the rejected rows differ per request, so no common
-// TMA box exists): D is h.W2 alone and no U slice ring is used.
+// then draws argmax_v log(max(0, p - q)) + G (domain 2); the CTAs fold their
+// draws into one 64-bit winner key per request and end, and the compaction
+// launch behind them decodes the keys (drawing from p where p <= q
+// everywhere left no key).  Each thread reads its own row of U and of the
+// target logits (the rejected rows differ per request, so no common TMA box
+// exists): D is h.W2 alone and no U slice ring is used.
 //
 // The first pass of a full-prefix verification (every draft checked against
 // the target, section 形式化定义), the log-sum-exps of target rows
