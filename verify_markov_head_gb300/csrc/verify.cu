@@ -225,8 +225,14 @@ verify_residual_simt_kernel(const VerifyParams p) {
     const int nb = min(kBC, p.B - b0);
     if (tid == 0) s_any = 0;
     __syncthreads();
+    // the stored-logits draw after the stream beside the draft (vs_full) also
+    // takes the bonus token of every request that rejected nothing: row gamma
+    // of the target, q taken as 0 (its log-normaliser is +inf), the bonus
+    // noise (domain 3); such a request is marked with row gamma here
+    const bool bonus_here = kStored && p.vs_full;
     if (tid < kBC) {
-        const int row = (tid < nb) ? __ldcg(&p.ws.rej[b0 + tid]) : -1;
+        int row = (tid < nb) ? __ldcg(&p.ws.rej[b0 + tid]) : -1;
+        if (bonus_here && tid < nb && row < 0) row = gamma;
         s_row[tid] = row;
         if (row >= 0) atomicOr(&s_any, 1);
     }
@@ -256,7 +262,7 @@ verify_residual_simt_kernel(const VerifyParams p) {
         const int ntiles = (V + kTV - 1) / kTV;
         const int my_row = (bl_e < nb) ? s_row[bl_e] : -1;
         const float2 lse = (my_row >= 0) ? p.ws.lse_rej[b0 + bl_e] : make_float2(0.f, 0.f);
-        const Stream rng(p.seed, p.step, 2u,
+        const Stream rng(p.seed, p.step, (kStored && my_row == gamma) ? 3u : 2u,
                          (uint32_t)(p.req_base + b0 + bl_e) * (uint32_t)(gamma + 1) + (uint32_t)(my_row < 0 ? 0 : my_row));
         const TT* trow = target + ((size_t)(b0 + bl_e) * (gamma + 1) + (my_row < 0 ? 0 : my_row)) * V;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -280,7 +286,7 @@ verify_residual_simt_kernel(const VerifyParams p) {
                 float z = 0.f;
                 if (row >= 0 && v < V) {
                     if constexpr (kStored)
-                        z = p.zlog[((size_t)(b0 + bl) * gamma + row) * V + v];
+                        z = row < gamma ? p.zlog[((size_t)(b0 + bl) * gamma + row) * V + v] : 0.f;
                     else
                         z = (to_f32(U[((size_t)(b0 + bl) * gamma + row) * V + v]) + acc[j]) * p.inv_tau;
                 }
@@ -472,9 +478,10 @@ cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     // the bytes and leaves the draws exposed, full-prefix mode has no stream
     // before the accept walk, and the stored-logits path serves small steps:
     // there the draws run after the walk, for the requests that emit them.
-    // Beside the draft (vs_full) the tensor-core residual kernel draws them;
-    // the stored-logits residual does not, so the pass stays there.
-    const bool deferred = p.zlog != nullptr || (!p.vs_full && (p.target_bf16 || p.tgt_slots > 0));
+    // Beside the draft (vs_full) the residual kernel draws them, the
+    // tensor-core one or the stored-logits one (b1 step 143.9 -> 139.2 us
+    // without the pass).
+    const bool deferred = !p.vs_full && (p.zlog != nullptr || p.target_bf16 || p.tgt_slots > 0);
     const long long lse_items = (long long)p.B * p.gamma * p.ws.nseg;
     const long long bonus_items = (long long)p.B * p.ws.nseg;
     cudaError_t e0 = cudaSuccess;
