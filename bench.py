@@ -717,19 +717,26 @@ _DRAFT_SOURCES = ("draft_rows.cu", "verify.cu", "common.cuh", "sm100_ptx.cuh", "
                   "pdl.cuh", "resid_tail.cuh")
 
 
-def _draft_source_hash():
-    """SHA-256 (first 16 hex digits) of the draft kernel's sources with
-    comments and blank space removed: edits to comments keep the hash."""
+def _normalised_source_hash(texts):
+    """SHA-256 (first 16 hex digits) of source texts with comments and blank
+    space removed: edits to comments keep the hash, edits to code change it."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for f in _DRAFT_SOURCES:
-        with open(os.path.join(ROOT, "verify_markov_head_gb300", "csrc", f)) as fh:
-            text = fh.read()
+    for text in texts:
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         h.update("".join(text.split()).encode())
     return h.hexdigest()[:16]
+
+
+def _draft_source_hash():
+    """The normalised hash of the draft kernel's sources."""
+    texts = []
+    for f in _DRAFT_SOURCES:
+        with open(os.path.join(ROOT, "verify_markov_head_gb300", "csrc", f)) as fh:
+            texts.append(fh.read())
+    return _normalised_source_hash(texts)
 
 
 def _draft_traffic(workload_name, fused=False):
